@@ -1,0 +1,528 @@
+"""Benchmark of the GB300 quantized matvec library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one call of the hot path on the Q4_K 4096x4096 workload (rows =
+k = 4096, seed 1): qmv_q4k reads the packed weight straight from HBM, decodes
+it in registers and writes y. Consecutive steps cycle through enough distinct
+copies of the weight (more than 3x the L2 size in total) that every call reads
+its weight HBM-cold. The K timed steps are one CUDA-graph replay bracketed by
+CUDA events on the launching stream, with a barrier and a device synchronize
+on both sides; the line reports the max over ranks.
+
+The printed JSON line also carries the other four workloads of the suite
+(``per_config``), the roofline of the timed kernel against the measured HBM
+copy bandwidth, the end-to-end number through the public API with host
+buffers, the CPU oracle as a baseline and the SM clocks seen while timing.
+
+``--impl reference`` times the CPU oracle (plain C, f64) on the same workload
+on the host cores: the only other implementation of the method available here
+(the pages' Vulkan kernels cannot run on this machine).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("packed-weight GB/s and % of GB300 HBM peak per quant matvec (µs/call, HBM-cold)")
+HEADLINE = "q4k_4096x4096"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+
+# ncu DRAM traffic of one qmv_q4k launch on the headline workload, valid only
+# for the kernel sources whose hash is recorded with it (see profiles/).
+NCU_TRAFFIC = {}
+
+KERNEL_SOURCES = ["qmv_device.cuh", "qmv_formats.cuh", "qmv_kernel.cuh", "qmv_launch.cuh", "qmv_q4k.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "ggml_format_dequant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def weight_bytes(name: str) -> int:
+    c = synth.CONFIGS[name]
+    if c["kind"] == "q4k":
+        return synth.row_bytes("q4k", c["k"]) * c["rows"]
+    if c["kind"] == "q6k":
+        return synth.row_bytes("q6k", c["k"]) * c["rows"]
+    if c["kind"] == "q8_0_dp4a":
+        return synth.row_bytes("q8_0", c["k"]) * c["rows"]
+    if c["kind"] == "moe_q4k":
+        return synth.row_bytes("q4k", c["k"]) * c["rows"] * c["slots"]   # routed rows only
+    raise ValueError(name)
+
+
+def algorithmic_bytes(name: str) -> int:
+    """Bytes a call must move at minimum: packed weight rows read, activation
+    read, output written."""
+    c = synth.CONFIGS[name]
+    wb = weight_bytes(name)
+    if c["kind"] == "moe_q4k":
+        return wb + 4 * c["slots"] * c["k"] + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
+    if c["kind"] == "q8_0_dp4a":
+        return wb + c["k"] + 4 * (c["k"] // 32) + 4 * c["rows"]
+    return wb + 4 * c["k"] + 4 * c["rows"]
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,power.draw")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+
+        def reader():
+            for ln in self.proc.stdout:
+                self.lines.append((time.time(), ln.strip()))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, ln in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                power.append(float(parts[7]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------ GPU side
+
+class Workload:
+    """Device buffers of one named workload, rotated over `copies` weights."""
+
+    def __init__(self, q, torch, name: str, l2_bytes: int, device):
+        self.name = name
+        c = synth.make_config(name)
+        self.c = c
+        self.kind = c["kind"]
+        self.rows, self.k = c["rows"], c["k"]
+        dev = device
+        wb = c["w"].nbytes
+        self.copies = max(4, math.ceil(3 * l2_bytes / wb) + 1)
+        # one pinned host copy, `copies` device copies (content identical; the
+        # addresses differ, which is what makes each call read from HBM)
+        w0 = torch.from_numpy(c["w"].reshape(-1))
+        self.w = [w0.to(dev) for _ in range(self.copies)]
+        self.x = torch.from_numpy(np.ascontiguousarray(c["x"])).to(dev)
+        if self.kind == "moe_q4k":
+            self.y = torch.empty(c["slots"], self.rows, dtype=torch.float32, device=dev)
+            # a cycle of seeded id sets so no (bank, expert) slice repeats within 3x L2
+            st = synth.Stream(1003)
+            self.ids = [torch.from_numpy(c["ids"]).to(dev)]
+            for _ in range(15):
+                self.ids.append(torch.from_numpy(synth.gen_moe_ids(st, c["slots"], c["n_experts"])).to(dev))
+        else:
+            self.y = torch.empty(self.rows, dtype=torch.float32, device=dev)
+        if self.kind == "q8_0_dp4a":
+            self.xq = torch.empty(self.k, dtype=torch.int8, device=dev)
+            self.xs = torch.empty(self.k // 32, dtype=torch.float32, device=dev)
+            q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k)
+        self.q = q
+
+    def call(self, i: int, stream: int, with_quant: bool = False) -> int:
+        """Enqueue call i; returns the number of kernels it launched."""
+        q, w = self.q, self.w[i % self.copies]
+        if self.kind == "q4k":
+            q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream)
+        elif self.kind == "q6k":
+            q.qmv_q6k(w, self.x, self.y, self.rows, self.k, stream=stream)
+        elif self.kind == "q8_0_dp4a":
+            n = 1
+            if with_quant:
+                q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k, stream=stream)
+                n = 2
+            q.qmv_q8_dp4a(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream)
+            return n
+        elif self.kind == "moe_q4k":
+            c = self.c
+            q.moe_qmv_q4k(w, self.x, self.y, self.rows, self.k, self.ids[i % len(self.ids)], c["slots"],
+                          c["n_experts"], stream=stream)
+        return 1
+
+
+def time_graph(torch, wl: Workload, n_calls: int, with_quant=False, replays=1, barrier=None):
+    """Capture n_calls rotated calls into one CUDA graph; return (ms per call,
+    kernels per call, graph). Times `replays` replays with CUDA events."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        # eager warm-up outside capture (sets kernel attributes, loads modules)
+        for i in range(min(4, n_calls)):
+            wl.call(i, s.cuda_stream, with_quant)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    launches = 0
+    with torch.cuda.graph(g, stream=s):
+        for i in range(n_calls):
+            launches += wl.call(i, s.cuda_stream, with_quant)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(replays):
+            g.replay()
+        e1.record(s)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    ms = e0.elapsed_time(e1) / (replays * n_calls)
+    return ms, launches / n_calls, g, s
+
+
+def run_ours(args):
+    import torch
+
+    import __graft_entry__
+    import ggml_format_dequant_gb300 as q
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    __graft_entry__.build()
+    q.load()
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+    peak, peak_kind = measured_peak()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+
+    # ------------------------------------------------ the headline workload
+    wl = Workload(q, torch, HEADLINE, l2, device)
+    K, W = args.steps, args.warmup
+    # warm-up steps (untimed)
+    _, _, gw, sw = time_graph(torch, wl, max(W, 1))
+    # pre-roll: keep the GPU busy with the same work so clock samples exist
+    # even when the K-step region is short
+    _, _, gk, sk = time_graph(torch, wl, K)
+    pre_t0 = time.time()
+    while time.time() - pre_t0 < 0.5:
+        with torch.cuda.stream(sk):
+            gk.replay()
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(sk):
+        e0.record(sk)
+        gk.replay()
+        e1.record(sk)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    post_t0 = time.time()
+    while time.time() - post_t0 < 0.5:
+        with torch.cuda.stream(sk):
+            gk.replay()
+        torch.cuda.synchronize()
+    clock_window = (pre_t0, time.time())
+
+    ms_t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    wbytes = weight_bytes(HEADLINE)
+    value = world * K * wbytes / (ms_max * 1e-3) / 1e9
+    ms_step = ms_max / K
+    alg = algorithmic_bytes(HEADLINE)
+    achieved = alg / (ms_step * 1e-3) / 1e9
+
+    # ------------------------------------------------ end to end (host buffers)
+    e2e = end_to_end(torch, q, wl, device, K)
+
+    # ------------------------------------------------ the other workloads
+    per_config = {HEADLINE: config_row(HEADLINE, ms_step, peak, peak_kind, wl.copies)}
+    del wl, gk, gw
+    torch.cuda.empty_cache()
+    if not args.headline_only:
+        for name in synth.CONFIGS:
+            if name == HEADLINE:
+                continue
+            w2 = Workload(q, torch, name, l2, device)
+            n = max(64, w2.copies)
+            ms, _, g2, _ = time_graph(torch, w2, n, replays=4)
+            per_config[name] = config_row(name, ms, peak, peak_kind, w2.copies)
+            if w2.kind == "q8_0_dp4a":
+                msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
+                per_config[name]["with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
+                del g3
+            del w2, g2
+            torch.cuda.empty_cache()
+    sampler.stop()
+    clocks = sampler.summary(*clock_window)
+    clocks["window"] = "nvidia-smi every 50 ms over a 0.5 s pre-roll, the timed region and a 0.5 s post-roll of the same graph"
+
+    traffic = NCU_TRAFFIC.get(kernel_hash())
+    cpu = cpu_baseline(args) if rank == 0 else None
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": round(ms_step, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "i8dp4a+f32",
+            "data": "synthetic (seeded splitmix64 Q4_K blocks and N(0,1) activations; no model weights)",
+            "config": {
+                "workload": "q4k_4096x4096: Q4_K matvec rows=4096 k=4096 (attention-projection shape), seed 1",
+                "rows": 4096, "k": 4096, "format": "Q4_K", "packed_weight_bytes": wbytes,
+                "l2": f"inputs larger than L2: {per_config[HEADLINE]['rotation_copies']} rotated weight copies "
+                      f"({per_config[HEADLINE]['rotation_copies'] * wbytes / 2**20:.0f} MiB) vs L2 {l2 / 2**20:.0f} MiB",
+                "timing": "K calls captured in one CUDA graph, CUDA events on the launching stream",
+                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            },
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "algorithmic_bytes_per_launch": alg},
+            "e2e": e2e,
+            "gpu_launches": K,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "per_config": per_config,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def config_row(name, ms, peak, peak_kind, copies):
+    wb = weight_bytes(name)
+    gbs = wb / (ms * 1e-3) / 1e9
+    return {"us_per_call": round(ms * 1e3, 3), "packed_weight_bytes": wb,
+            "packed_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+            "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+            "algorithmic_gbs": round(algorithmic_bytes(name) / (ms * 1e-3) / 1e9, 1),
+            "rotation_copies": copies}
+
+
+def end_to_end(torch, q, wl, device, K):
+    """Public API with host buffers: per step, copy the weight and x from
+    pinned host memory, run qmv_q4k, copy y back; K steps in one graph."""
+    c = wl.c
+    hw = torch.from_numpy(c["w"].reshape(-1)).pin_memory()
+    hx = torch.from_numpy(c["x"]).pin_memory()
+    hy = torch.empty(wl.rows, dtype=torch.float32).pin_memory()
+    dw = torch.empty_like(hw, device=device)
+    dx = torch.empty_like(hx, device=device)
+    dy = torch.empty(wl.rows, dtype=torch.float32, device=device)
+    s = torch.cuda.Stream()
+    steps = max(1, min(K, 200))
+
+    def step():
+        dw.copy_(hw, non_blocking=True)
+        dx.copy_(hx, non_blocking=True)
+        q.qmv_q4k(dw, dx, dy, wl.rows, wl.k, stream=s.cuda_stream)
+        hy.copy_(dy, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):
+            step()
+        e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ok = bool(np.isfinite(hy.numpy()).all())
+    return {"value": round(weight_bytes(HEADLINE) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": hw.numel() + 4 * hx.numel(), "d2h_bytes_per_step": 4 * hy.numel(),
+            "ms_per_step": round(ms, 4), "steps": steps, "finite": ok}
+
+
+# ------------------------------------------------------------- CPU side
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(args, seconds: float = 10.0) -> dict:
+    """The oracle as it stands, rows split over the host cores, repeated on the
+    full headline workload for about `seconds` of wall time."""
+    import oracle
+
+    c = synth.make_config(HEADLINE)
+    n = cpu_cores()
+    oracle.qmv_threaded("q4k", c["w"], c["x"], 4096, 4096, n)   # load + warm
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.qmv_threaded("q4k", c["w"], c["x"], 4096, 4096, n)
+        calls += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(calls * weight_bytes(HEADLINE) / dt / 1e9, 4), "unit": "GB/s", "cores": n,
+            "kind": "oracle",
+            "sample": f"{calls} full 4096x4096 Q4_K matvecs (f64 dequantize-then-dot), rows split over {n} threads, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+
+    c = synth.make_config(HEADLINE)
+    n = cpu_cores()
+    for _ in range(args.warmup):
+        oracle.qmv_threaded("q4k", c["w"], c["x"], 4096, 4096, n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.qmv_threaded("q4k", c["w"], c["x"], 4096, 4096, n)
+    dt = time.perf_counter() - t0
+    value = args.steps * weight_bytes(HEADLINE) / dt / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded splitmix64 Q4_K blocks and N(0,1) activations; no model weights)",
+        "config": {"workload": "q4k_4096x4096: Q4_K matvec rows=4096 k=4096 (attention-projection shape), seed 1",
+                   "rows": 4096, "k": 4096, "format": "Q4_K"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+                         "sample": f"each step one full 4096x4096 Q4_K matvec, rows split over {n} threads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the reference is the CPU oracle: the pages' own kernels are Vulkan/SPIR-V and cannot run here",
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true", help="skip the per-config table")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+"""Python binding of libqmv.so, the GB300 GGML-block quantized matvec library.
+
+Argument marshalling only: every function forwards to the C entry point of the
+same name (see ``include/qmv.h``), which enqueues the CUDA kernels on the
+given stream. Arguments may be ``torch.Tensor`` objects on the GPU (their
+``data_ptr()`` is passed) or raw device addresses as ``int``. The stream
+defaults to torch's current stream on the current device.
+
+There is no CPU fallback: if the compiled library is missing, loading raises
+``QmvLibraryMissing``; build it with ``__graft_entry__.build()`` (or
+``python -m ggml_format_dequant_gb300._build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+QMV_OK = 0
+QMV_EINVAL = -1
+QMV_EALIGN = -2
+QMV_ECUDA = -3
+QMV_ETOOBIG = -4
+QMV_STATUS_BAD_EXPERT_ID = 1
+QMV_STATUS_WAIT_TIMEOUT = 2
+
+FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K = 0, 1, 2, 3, 4
+
+
+class QmvLibraryMissing(RuntimeError):
+    pass
+
+
+class QmvError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        msg = f"{fn} failed: {code} ({strerror(code)})"
+        if code == QMV_ECUDA:
+            msg += f": {load().qmv_last_cuda_error().decode()}"
+        super().__init__(msg)
+
+
+class qmv_cfg(ctypes.Structure):
+    _fields_ = [("ctas", ctypes.c_int), ("stage_rows", ctypes.c_int), ("stages", ctypes.c_int)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIG = {
+    "qmv_q4k": [_P, _P, _P, _I, _I, _P],
+    "qmv_q6k": [_P, _P, _P, _I, _I, _P],
+    "qmv_q8_0": [_P, _P, _P, _I, _I, _P],
+    "quantize_act_q8": [_P, _P, _P, _P, _I, _I, _P],
+    "qmv_q8_dp4a": [_P, _P, _P, _P, _I, _I, _P],
+    "moe_qmv_q4k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
+    "qmv_q4k_cfg": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q6k_cfg": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q8_0_cfg": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q8_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _P],
+    "moe_qmv_q4k_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "qmv_dequant_q4k": [_P, _P, _I, _I, _P],
+    "qmv_dequant_q6k": [_P, _P, _I, _I, _P],
+    "qmv_dequant_q8_0": [_P, _P, _I, _I, _P],
+    "qmv_q8_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
+    "qmv_device_status": [_P, _I],
+    "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
+}
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load(path: str | None = None):
+    """Load libqmv.so (once). Raises QmvLibraryMissing if it was not built."""
+    global _LIB
+    if _LIB is None:
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise QmvLibraryMissing(f"libqmv.so not built at {p}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        for name, args in _SIG.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        lib.qmv_strerror.argtypes = [ctypes.c_int]
+        lib.qmv_strerror.restype = ctypes.c_char_p
+        lib.qmv_last_cuda_error.argtypes = []
+        lib.qmv_last_cuda_error.restype = ctypes.c_char_p
+        _LIB = lib
+    return _LIB
+
+
+def strerror(code: int) -> str:
+    return load().qmv_strerror(int(code)).decode()
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _cfg(cfg):
+    if cfg is None:
+        return None
+    if isinstance(cfg, qmv_cfg):
+        return ctypes.byref(cfg)
+    c = qmv_cfg(int(cfg.get("ctas", 0)), int(cfg.get("stage_rows", 0)), int(cfg.get("stages", 0)))
+    return ctypes.byref(c)
+
+
+def _call(name, *args, check=True):
+    rc = getattr(load(), name)(*args)
+    if check and rc != QMV_OK:
+        raise QmvError(name, rc)
+    return rc
+
+
+def qmv_q4k(w, x, y, rows, k, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("qmv_q4k", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q4k_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+
+
+def qmv_q6k(w, x, y, rows, k, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("qmv_q6k", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q6k_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+
+
+def qmv_q8_0(w, x, y, rows, k, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("qmv_q8_0", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q8_0_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+
+
+def quantize_act_q8(x, xq, xs, xsum, m, k, stream=None, check=True):
+    return _call("quantize_act_q8", _ptr(x), _ptr(xq), _ptr(xs), _ptr(xsum), m, k, _stream(stream), check=check)
+
+
+def qmv_q8_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("qmv_q8_dp4a", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q8_dp4a_cfg", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _cfg(cfg), _stream(stream),
+                 check=check)
+
+
+def moe_qmv_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("moe_qmv_q4k", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                     _stream(stream), check=check)
+    return _call("moe_qmv_q4k_cfg", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                 _cfg(cfg), _stream(stream), check=check)
+
+
+def qmv_dequant_q4k(w, out, rows, k, stream=None, check=True):
+    return _call("qmv_dequant_q4k", _ptr(w), _ptr(out), rows, k, _stream(stream), check=check)
+
+
+def qmv_dequant_q6k(w, out, rows, k, stream=None, check=True):
+    return _call("qmv_dequant_q6k", _ptr(w), _ptr(out), rows, k, _stream(stream), check=check)
+
+
+def qmv_dequant_q8_0(w, out, rows, k, stream=None, check=True):
+    return _call("qmv_dequant_q8_0", _ptr(w), _ptr(out), rows, k, _stream(stream), check=check)
+
+
+def qmv_q8_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):
+    return _call("qmv_q8_dp4a_blockdots", _ptr(w), _ptr(xq), _ptr(dots), rows, k, _stream(stream), check=check)
+
+
+def qmv_device_status(clear=True) -> int:
+    v = ctypes.c_uint(0)
+    _call("qmv_device_status", ctypes.cast(ctypes.byref(v), ctypes.c_void_p), 1 if clear else 0)
+    return v.value
+
+
+def qmv_plan_info(fmt, rows, k, slots=1, cfg=None) -> dict:
+    out = [ctypes.c_int(0) for _ in range(5)]
+    _call("qmv_plan_info", fmt, rows, k, slots, _cfg(cfg), *[ctypes.cast(ctypes.byref(o), ctypes.c_void_p)
+                                                           for o in out])
+    return dict(zip(["threads", "ctas", "stage_rows", "stages", "smem_bytes"], [o.value for o in out]))

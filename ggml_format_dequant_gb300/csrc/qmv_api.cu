@@ -1,0 +1,167 @@
+// qmv_api.cu -- the extern "C" entry points of libqmv.so: argument validation
+// on the host (nothing is enqueued for a bad call), then the launch in the
+// format's translation unit.
+#include <climits>
+#include <cstdint>
+
+#include "qmv_internal.h"
+#include "qmv_launch.cuh"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Common checks of a dense matvec: non-null pointers, rows > 0, k a positive
+// multiple of the block size, weight 16-byte and f32 buffers 4-byte aligned,
+// and a total weight size that fits the address arithmetic.
+int check_dense(const void* w, const void* x, const void* y, int rows, int k, int qk, int block_bytes) {
+    if (!w || !x || !y) return QMV_EINVAL;
+    if (rows <= 0 || k <= 0 || k % qk) return QMV_EINVAL;
+    if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return QMV_EALIGN;
+    const long long rb = static_cast<long long>(k / qk) * block_bytes;
+    if (rb > INT_MAX || static_cast<long long>(rows) > LLONG_MAX / rb) return QMV_EINVAL;
+    return QMV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmv_q4k_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+                cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 144);
+    return rc ? rc : qmvi::q4k(w, x, y, rows, k, cfg, stream);
+}
+
+int qmv_q4k(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
+    return qmv_q4k_cfg(w, x, y, rows, k, nullptr, stream);
+}
+
+int qmv_q6k_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+                cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 210);
+    return rc ? rc : qmvi::q6k(w, x, y, rows, k, cfg, stream);
+}
+
+int qmv_q6k(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
+    return qmv_q6k_cfg(w, x, y, rows, k, nullptr, stream);
+}
+
+int qmv_q8_0_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+                 cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 32, 34);
+    return rc ? rc : qmvi::q8_0(w, x, y, rows, k, cfg, stream);
+}
+
+int qmv_q8_0(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
+    return qmv_q8_0_cfg(w, x, y, rows, k, nullptr, stream);
+}
+
+int quantize_act_q8(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t stream) {
+    if (!x || !xq || !xs) return QMV_EINVAL;
+    if (m <= 0 || k <= 0 || k % 32) return QMV_EINVAL;
+    if (!aligned(x, 4) || !aligned(xs, 4) || (xsum && !aligned(xsum, 4))) return QMV_EALIGN;
+    if (static_cast<long long>(m) * k > (LLONG_MAX >> 8)) return QMV_EINVAL;
+    return qmvi::quantize_act(x, xq, xs, xsum, m, k, stream);
+}
+
+int qmv_q8_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                    const qmv_cfg* cfg, cudaStream_t stream) {
+    if (!xs) return QMV_EINVAL;
+    int rc = check_dense(w, xq, y, rows, k, 32, 34);
+    if (rc) return rc;
+    if (!aligned(xq, 16) || !aligned(xs, 4)) return QMV_EALIGN;
+    return qmvi::q8_dp4a(w, xq, xs, y, rows, k, cfg, stream);
+}
+
+int qmv_q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                cudaStream_t stream) {
+    return qmv_q8_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
+}
+
+int moe_qmv_q4k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids,
+                    int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+    int rc = check_dense(w_bank, x, y, rows, k, 256, 144);
+    if (rc) return rc;
+    if (!ids) return QMV_EINVAL;
+    if (slots <= 0 || slots > 65535 || n_experts <= 0) return QMV_EINVAL;
+    if (!aligned(ids, 4)) return QMV_EALIGN;
+    const long long rb = static_cast<long long>(k / 256) * 144;
+    if (static_cast<long long>(n_experts) > LLONG_MAX / rb / rows) return QMV_EINVAL;
+    return qmvi::moe_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
+}
+
+int moe_qmv_q4k(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                int n_experts, cudaStream_t stream) {
+    return moe_qmv_q4k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+}
+
+int qmv_dequant_q4k(const void* w, float* out, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, out, out, rows, k, 256, 144);
+    return rc ? rc : qmvi::dequant_q4k(w, out, rows, k, stream);
+}
+
+int qmv_dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, out, out, rows, k, 256, 210);
+    return rc ? rc : qmvi::dequant_q6k(w, out, rows, k, stream);
+}
+
+int qmv_dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, out, out, rows, k, 32, 34);
+    return rc ? rc : qmvi::dequant_q8_0(w, out, rows, k, stream);
+}
+
+int qmv_q8_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, xq, dots, rows, k, 32, 34);
+    if (rc) return rc;
+    if (!aligned(xq, 16)) return QMV_EALIGN;
+    return qmvi::q8_blockdots(w, xq, dots, rows, k, stream);
+}
+
+const char* qmv_strerror(int code) {
+    switch (code) {
+    case QMV_OK: return "ok";
+    case QMV_EINVAL: return "invalid argument (null pointer or shape not a positive block multiple)";
+    case QMV_EALIGN: return "misaligned pointer (weights and int8 activations need 16 bytes, f32 buffers 4)";
+    case QMV_ECUDA: return "CUDA runtime error or kernel launch failure";
+    case QMV_ETOOBIG: return "shape too large for the shared-memory plan of this build";
+    default: return "unknown qmv error code";
+    }
+}
+
+const char* qmv_last_cuda_error(void) {
+    return cudaGetErrorString(qmv::last_cuda_error());
+}
+
+int qmv_device_status(unsigned int* status, int clear) {
+    if (!status) return QMV_EINVAL;
+    unsigned int a = 0, b = 0, c = 0;
+    int rc = qmvi::status_q4k(&a, clear);
+    if (!rc) rc = qmvi::status_q6k(&b, clear);
+    if (!rc) rc = qmvi::status_q8(&c, clear);
+    if (rc) return rc;
+    *status = a | b | c;
+    return QMV_OK;
+}
+
+int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* threads, int* ctas,
+                  int* stage_rows, int* stages, int* smem_bytes) {
+    static const int qk[5] = {256, 256, 32, 32, 256};
+    static const int bb[5] = {144, 210, 34, 34, 144};
+    static const int upb[5] = {4, 4, 1, 1, 4};
+    if (fmt < 0 || fmt > 4 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
+    if (fmt == 4 && slots <= 0) return QMV_EINVAL;
+    qmv::KParams kp{};
+    qmv::Plan pl;
+    const long long rb = static_cast<long long>(k / qk[fmt]) * bb[fmt];
+    int rc = qmv::make_plan(upb[fmt] * (k / qk[fmt]), rb, rows, k, fmt != 3, fmt == 4 ? slots : 1, cfg, &kp, &pl);
+    if (rc) return rc;
+    if (threads) *threads = pl.T;
+    if (ctas) *ctas = pl.parts * (fmt == 4 ? slots : 1);
+    if (stage_rows) *stage_rows = pl.G;
+    if (stages) *stages = pl.S;
+    if (smem_bytes) *smem_bytes = static_cast<int>(pl.smem);
+    return QMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,33 @@
+// qmv_internal.h -- host functions each kernel translation unit exports to the
+// C ABI layer (qmv_api.cu). Arguments are already validated by the caller.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "../../include/qmv.h"
+
+namespace qmvi {
+
+// qmv_q4k.cu
+int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s);
+int moe_q4k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+            int n_experts, const qmv_cfg* cfg, cudaStream_t s);
+int dequant_q4k(const void* w, float* out, int rows, int k, cudaStream_t s);
+int status_q4k(unsigned int* out, int clear);
+
+// qmv_q6k.cu
+int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s);
+int dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t s);
+int status_q6k(unsigned int* out, int clear);
+
+// qmv_q8.cu
+int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s);
+int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+            cudaStream_t s);
+int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s);
+int quantize_act(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t s);
+int dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t s);
+int status_q8(unsigned int* out, int clear);
+
+}  // namespace qmvi

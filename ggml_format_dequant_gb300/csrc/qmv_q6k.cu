@@ -1,0 +1,66 @@
+// qmv_q6k.cu -- Q6_K dense matvec launch and the Q6_K dequantizer used by the
+// tests.
+#include "qmv_internal.h"
+#include "qmv_launch.cuh"
+
+namespace {
+
+using namespace qmv;
+
+// One thread per (row, block, 16-weight scale group gi): weight i = 16*gi + t
+// sits in half H = i/128, quarter qd = (i%128)/32, position l = i%32, and
+// d*scale*(q - 32) is exact in f32 (d*scale has at most 18 significant bits).
+__global__ void dequant_q6k_kernel(const uint8_t* __restrict__ w, float* __restrict__ out, long long ngroups) {
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < ngroups;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int gi = static_cast<int>(idx & 15);
+        const long long blk = idx >> 4;
+        const uint8_t* p = w + blk * 210;
+        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(p[208] | (p[209] << 8))));
+        const float ds = d * static_cast<float>(static_cast<int8_t>(p[192 + gi]));
+        float* o = out + blk * 256;
+        for (int t = 0; t < 16; t++) {
+            const int i = 16 * gi + t;
+            const int H = i >> 7, qd = (i & 127) >> 5, l = i & 31;
+            const int qlb = p[64 * H + 32 * (qd & 1) + l];
+            const int lo4 = (qd < 2) ? (qlb & 15) : (qlb >> 4);
+            const int hi2 = (p[128 + 32 * H + l] >> (2 * qd)) & 3;
+            o[i] = __fmul_rn(ds, static_cast<float>((lo4 | (hi2 << 4)) - 32));
+        }
+    }
+}
+
+}  // namespace
+
+namespace qmvi {
+
+using namespace qmv;
+
+int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s) {
+    KParams kp{};
+    kp.w = static_cast<const uint8_t*>(w);
+    kp.x = x;
+    kp.y = y;
+    kp.rows = rows;
+    kp.k = k;
+    kp.nb = k / 256;
+    kp.rowbytes = static_cast<long long>(kp.nb) * 210;
+    kp.wbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    Plan pl;
+    int rc = make_plan(4 * kp.nb, kp.rowbytes, rows, k, true, 1, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q6K, false, MODE_MATVEC>(kp, pl, 1, s);
+}
+
+int dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t s) {
+    const long long ng = static_cast<long long>(rows) * (k / 256) * 16;
+    const int threads = 256;
+    const long long want = (ng + threads - 1) / threads;
+    const int blocks = static_cast<int>(want < 65536 ? want : 65536);
+    dequant_q6k_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint8_t*>(w), out, ng);
+    return cuda_rc(cudaGetLastError());
+}
+
+int status_q6k(unsigned int* out, int clear) { return status_rw(out, clear); }
+
+}  // namespace qmvi

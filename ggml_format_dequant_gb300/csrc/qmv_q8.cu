@@ -1,0 +1,116 @@
+// qmv_q8.cu -- Q8_0 matvecs (f32 activation and dp4a), the dp4a block dots,
+// the activation quantizer and the Q8_0 dequantizer.
+#include "qmv_internal.h"
+#include "qmv_launch.cuh"
+
+namespace {
+
+using namespace qmv;
+
+// One warp per 32-element block of x: amax by a warp max over |x| bit
+// patterns (ordered like the magnitudes for finite values), then the IEEE f32
+// divide / multiply / round-half-even steps of the quantizer.
+__global__ void quantize_act_q8_kernel(const float* __restrict__ x, int8_t* __restrict__ xq,
+                                       float* __restrict__ xs, float* __restrict__ xsum, long long nblocks) {
+    const int lane = threadIdx.x & 31;
+    const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+    const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    for (long long b = wid; b < nblocks; b += nw) {
+        const float v = x[b * 32 + lane];
+        const float amax = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(v) & 0x7fffffffu));
+        int q = 0;
+        float d = 0.0f;
+        if (amax != 0.0f) {
+            const float inv = __fdiv_rn(127.0f, amax);
+            q = __float2int_rn(__fmul_rn(v, inv));
+            q = q > 127 ? 127 : (q < -127 ? -127 : q);
+            d = __fdiv_rn(amax, 127.0f);
+        }
+        xq[b * 32 + lane] = static_cast<int8_t>(q);
+        const int sum = __reduce_add_sync(FULL, q);
+        if (lane == 0) {
+            xs[b] = d;
+            if (xsum) xsum[b] = __fmul_rn(d, __int2float_rn(sum));
+        }
+    }
+}
+
+// One thread per (row, block): d*q is exact in f32.
+__global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ w, float* __restrict__ out, long long nblk) {
+    for (long long blk = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; blk < nblk;
+         blk += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const uint8_t* p = w + blk * 34;
+        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(p[0] | (p[1] << 8))));
+        for (int i = 0; i < 32; i++) out[blk * 32 + i] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(p[2 + i])));
+    }
+}
+
+KParams q8_params(const void* w, int rows, int k) {
+    KParams kp{};
+    kp.w = static_cast<const uint8_t*>(w);
+    kp.rows = rows;
+    kp.k = k;
+    kp.nb = k / 32;
+    kp.rowbytes = static_cast<long long>(kp.nb) * 34;
+    kp.wbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    return kp;
+}
+
+int grid_for(long long items, int threads) {
+    const long long want = (items + threads - 1) / threads;
+    return static_cast<int>(want < 65536 ? (want > 0 ? want : 1) : 65536);
+}
+
+}  // namespace
+
+namespace qmvi {
+
+using namespace qmv;
+
+int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s) {
+    KParams kp = q8_params(w, rows, k);
+    kp.x = x;
+    kp.y = y;
+    Plan pl;
+    int rc = make_plan(kp.nb, kp.rowbytes, rows, k, true, 1, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q8F, false, MODE_MATVEC>(kp, pl, 1, s);
+}
+
+int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+            cudaStream_t s) {
+    KParams kp = q8_params(w, rows, k);
+    kp.xq = xq;
+    kp.xqs = xs;
+    kp.y = y;
+    Plan pl;
+    int rc = make_plan(kp.nb, kp.rowbytes, rows, k, false, 1, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q8D, false, MODE_MATVEC>(kp, pl, 1, s);
+}
+
+int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s) {
+    KParams kp = q8_params(w, rows, k);
+    kp.xq = xq;
+    kp.dots = dots;
+    Plan pl;
+    int rc = make_plan(kp.nb, kp.rowbytes, rows, k, false, 1, nullptr, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q8D, false, MODE_BLOCKDOTS>(kp, pl, 1, s);
+}
+
+int quantize_act(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t s) {
+    const long long nblocks = static_cast<long long>(m) * (k / 32);
+    quantize_act_q8_kernel<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(x, xq, xs, xsum, nblocks);
+    return cuda_rc(cudaGetLastError());
+}
+
+int dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t s) {
+    const long long nblk = static_cast<long long>(rows) * (k / 32);
+    dequant_q8_0_kernel<<<grid_for(nblk, 256), 256, 0, s>>>(static_cast<const uint8_t*>(w), out, nblk);
+    return cuda_rc(cudaGetLastError());
+}
+
+int status_q8(unsigned int* out, int clear) { return status_rw(out, clear); }
+
+}  // namespace qmvi

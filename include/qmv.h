@@ -1,0 +1,167 @@
+/*
+ * qmv.h -- C ABI of the GB300 (sm_103a) GGML-block quantized matrix-vector
+ * product library (libqmv.so).
+ *
+ * Operation (hanzo-ml src/vulkan_backend.rs, matvec_q4k_gpu / matvec_q6k_gpu /
+ * matvec_q8_0_gpu and moe_matvec_gpu): y = W x for a weight matrix W[rows, k]
+ * whose rows are stored verbatim in GGML block formats and decoded inside the
+ * kernel, never materialized:
+ *   Q4_K: 144-byte super-blocks of 256 weights (d, dmin f16; 12 bytes of packed
+ *         6-bit scales and mins; 128 bytes of 4-bit codes),
+ *         w = d*sc_j*q - dmin*m_j for sub-block j = i/32 (quantize_q4k);
+ *   Q6_K: 210-byte blocks of 256 weights (ql[128], qh[64], int8 scales[16],
+ *         d f16), w = d*scale*(q - 32) (quantize_q6k);
+ *   Q8_0: 34-byte blocks of 32 weights (d f16 then 32 int8), w = d*q
+ *         (quantize_q8_blocks).
+ *
+ * Conventions shared by every entry point:
+ *  - All data pointers are DEVICE pointers owned by the caller. The library
+ *    allocates no memory, keeps no per-call state and never synchronizes.
+ *  - Work is enqueued on `stream` (0 = the legacy default stream) and runs
+ *    asynchronously; outputs are valid once the stream reaches that point.
+ *  - Packed weights are rows of whole blocks, row-major and contiguous (row r
+ *    starts at byte r * (k / block_weights) * block_bytes). The weight pointer
+ *    must be 16-byte aligned. Only the bytes of the rows read are accessed.
+ *  - Outputs are overwritten, never accumulated into.
+ *  - Return value: QMV_OK (0) or a negative QMV_E* code; qmv_strerror() names
+ *    it. Argument errors are detected on the host before anything is enqueued.
+ *  - Numerics: decoded weights are exact (each is the round-to-nearest f32 of
+ *    its exact value). The f32-activation entry points carry x into integer
+ *    dp4a dot products as three signed-byte limbs per element, with one
+ *    power-of-two scale per 32 activations (21 bits kept below the block's
+ *    largest |x|), and sum scaled group results in f32; results agree with an
+ *    f64 dequantize-then-dot reference to a scale-relative error
+ *    max|a-b|/max|a| far below 1e-4. Non-finite inputs give unspecified
+ *    (possibly non-finite) outputs.
+ *  - Threading: every entry point is reentrant; calls on different streams may
+ *    run concurrently.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMV_OK 0
+#define QMV_EINVAL (-1)  /* bad shape or null pointer (k not a block multiple, rows/m/slots/n_experts <= 0) */
+#define QMV_EALIGN (-2)  /* a pointer that must be 16-byte (or 4-byte) aligned is not */
+#define QMV_ECUDA (-3)   /* a CUDA runtime call or the kernel launch failed */
+#define QMV_ETOOBIG (-4) /* valid shape too large for this build's shared-memory plan */
+
+/* Q4_K matvec: y[r] = sum_j W[r, j] * x[j].
+ * w: rows * (k/256) * 144 bytes, 16-byte aligned; x: f32 [k]; y: f32 [rows].
+ * k must be a positive multiple of 256, rows > 0.
+ * Cites hanzo-ml src/vulkan_backend.rs, matvec_q4k_gpu_off and quantize_q4k. */
+int qmv_q4k(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
+
+/* Q6_K matvec: y = W x. w: rows * (k/256) * 210 bytes (the 210-byte blocks are
+ * read unpadded), 16-byte aligned; x: f32 [k]; y: f32 [rows]; k % 256 == 0.
+ * Cites hanzo-ml src/vulkan_backend.rs, matvec_q6k_gpu and quantize_q6k. */
+int qmv_q6k(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
+
+/* Q8_0 matvec with an f32 activation: y = W x. w: rows * (k/32) * 34 bytes,
+ * 16-byte aligned; x: f32 [k]; y: f32 [rows]; k % 32 == 0.
+ * Cites hanzo-ml src/vulkan_backend.rs, matvec_q8_0_gpu (raw 34-byte blocks). */
+int qmv_q8_0(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
+
+/* Activation quantization for the dp4a path, per 32-element block of x[m, k]:
+ * amax = max|x|; inv = 127/amax and d = amax/127 (IEEE f32 divides);
+ * q = clamp(round_half_even(x * inv), -127, 127) (one f32 multiply); amax == 0
+ * gives d = 0 and q = 0. Outputs: xq int8 [m, k]; xs f32 [m, k/32] = d;
+ * xsum (may be NULL) f32 [m, k/32] = d * (integer sum of the block's q).
+ * m > 0, k % 32 == 0; x, xs, xsum 4-byte aligned.
+ * Cites hanzo-ml src/vulkan_backend.rs, quantize_act_q8 and quantize_q8. */
+int quantize_act_q8(const float *x, int8_t *xq, float *xs, float *xsum, int m, int k,
+                    cudaStream_t stream);
+
+/* dp4a matvec of Q8_0 weights with a quantized activation:
+ * y[r] = sum_b (d_w[r, b] * d_x[b]) * dot[r, b] in f32, where dot[r, b] is the
+ * exact int32 sum of the block's 32 int8*int8 products.
+ * w: Q8_0 rows as for qmv_q8_0; xq: int8 [k], 16-byte aligned; xs: f32 [k/32];
+ * y: f32 [rows]. Cites hanzo-kernel src/main.rs, check_dp4a (matvec_q8_dp4a_*). */
+int qmv_q8_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                cudaStream_t stream);
+
+/* MoE indexed Q4_K matvec: y[s, r] = sum_j W[ids[s], r, j] * x[s, j].
+ * w_bank: one resident bank [n_experts, rows, k] of Q4_K rows (expert e's
+ * matrix starts at byte e * rows * (k/256) * 144), 16-byte aligned;
+ * x: f32 [slots, k] (one activation row per slot); y: f32 [slots, rows];
+ * ids: DEVICE int32 [slots], read on the GPU (duplicates allowed). Only the
+ * rows of the routed experts are read. A slot whose id lies outside
+ * [0, n_experts) gets NaN in all its outputs and raises QMV_STATUS_BAD_EXPERT_ID
+ * in the device status word (see qmv_device_status); nothing traps.
+ * Cites hanzo-ml src/vulkan_backend.rs, moe_matvec_gpu. */
+int moe_qmv_q4k(const void *w_bank, const float *x, float *y, int rows, int k,
+                const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+
+/* Name of a QMV_* return code. Never NULL. */
+const char *qmv_strerror(int code);
+
+/* Text of the last CUDA error behind a QMV_ECUDA return on the calling thread
+ * ("no error" if there was none). Never NULL. */
+const char *qmv_last_cuda_error(void);
+
+/* ----------------------------------------------------------------------
+ * Device status word: bits raised by kernels on conditions that cannot be
+ * seen on the host without a synchronization.
+ */
+#define QMV_STATUS_BAD_EXPERT_ID 1u /* an MoE id was outside [0, n_experts) */
+#define QMV_STATUS_WAIT_TIMEOUT 2u  /* a staged weight copy did not land in time */
+
+/* OR of the status bits raised on the current device since the last clear;
+ * clears them when `clear` is non-zero. Synchronizes with the device (it reads
+ * device memory through the legacy stream). */
+int qmv_device_status(unsigned int *status, int clear);
+
+/* ----------------------------------------------------------------------
+ * Test and benchmark exports (not needed for inference).
+ */
+
+/* Forced launch configuration: any field <= 0 keeps the automatic choice.
+ * ctas: CTAs per weight matrix; stage_rows: rows per pipeline stage;
+ * stages: pipeline depth. Used to exercise multi-stage pipelines and ragged
+ * tails on small inputs. */
+typedef struct qmv_cfg {
+    int ctas;
+    int stage_rows;
+    int stages;
+} qmv_cfg;
+
+int qmv_q4k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
+                cudaStream_t stream);
+int qmv_q6k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
+                cudaStream_t stream);
+int qmv_q8_0_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
+                 cudaStream_t stream);
+int qmv_q8_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                    const qmv_cfg *cfg, cudaStream_t stream);
+int moe_qmv_q4k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
+                    const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
+                    cudaStream_t stream);
+
+/* Exact decoded weights: out f32 [rows, k] (each the round-to-nearest f32 of
+ * the weight's exact value). Same argument rules as the matvecs. */
+int qmv_dequant_q4k(const void *w, float *out, int rows, int k, cudaStream_t stream);
+int qmv_dequant_q6k(const void *w, float *out, int rows, int k, cudaStream_t stream);
+int qmv_dequant_q8_0(const void *w, float *out, int rows, int k, cudaStream_t stream);
+
+/* Per-block int32 dots of the dp4a path, dots[r, b] (int32 [rows, k/32]),
+ * computed by the same code path qmv_q8_dp4a uses. */
+int qmv_q8_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int rows, int k,
+                          cudaStream_t stream);
+
+/* Launch plan the library would use (for benchmark reports): threads per CTA,
+ * CTAs per matrix, rows per stage, pipeline depth and dynamic shared bytes.
+ * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K. */
+int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
+                  int *stage_rows, int *stages, int *smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

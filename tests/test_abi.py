@@ -1,0 +1,81 @@
+"""The C ABI library without a GPU: it builds, loads, exports every function
+include/qmv.h declares, and rejects bad arguments on the host before touching
+CUDA (so these calls are safe on a machine with no device)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import ggml_format_dequant_gb300 as q
+    return q
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["qmv_q4k", "qmv_q6k", "qmv_q8_0", "quantize_act_q8", "qmv_q8_dp4a", "moe_qmv_q4k",
+              "qmv_strerror"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    L = lib.load()
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert os.path.abspath(lib.library_path()).startswith(ROOT)
+
+
+def test_strerror(lib):
+    for code in [0, -1, -2, -3, -4, 12345]:
+        assert isinstance(lib.strerror(code), str) and lib.strerror(code)
+    assert lib.strerror(-2).startswith("misaligned")
+
+
+def test_host_side_validation_without_gpu(lib):
+    A = 0x10000   # a 16-byte aligned fake address; never dereferenced
+    S = 0
+    assert lib.qmv_q4k(A, A, A, 4, 300, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_q4k(A, A, A, 0, 256, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_q4k(A, A, A, -3, 256, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_q4k(None, A, A, 4, 256, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_q4k(A + 8, A, A, 4, 256, stream=S, check=False) == lib.QMV_EALIGN
+    assert lib.qmv_q4k(A, A + 2, A, 4, 256, stream=S, check=False) == lib.QMV_EALIGN
+    assert lib.qmv_q6k(A, A, A, 4, 32, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_q8_0(A, A, A, 4, 33, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.quantize_act_q8(A, A, A, None, 0, 32, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.quantize_act_q8(A, A, None, None, 1, 32, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_q8_dp4a(A, A + 4, A, A, 4, 32, stream=S, check=False) == lib.QMV_EALIGN
+    assert lib.qmv_q8_dp4a(A, A, None, A, 4, 32, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.moe_qmv_q4k(A, A, A, 4, 256, None, 2, 8, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.moe_qmv_q4k(A, A, A, 4, 256, A, 70000, 8, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.moe_qmv_q4k(A, A, A, 4, 256, A + 2, 2, 8, stream=S, check=False) == lib.QMV_EALIGN
+    assert lib.qmv_dequant_q4k(A, A, 4, 100, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_q8_dp4a_blockdots(A, A + 1, A, 4, 32, stream=S, check=False) == lib.QMV_EALIGN
+    with pytest.raises(lib.QmvError):
+        lib.qmv_q4k(A, A, A, 4, 300, stream=S)
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import ggml_format_dequant_gb300 as q
+    saved = q._LIB
+    try:
+        q._LIB = None
+        with pytest.raises(q.QmvLibraryMissing):
+            q.load(str(tmp_path / "missing.so"))
+    finally:
+        q._LIB = saved

@@ -1,0 +1,329 @@
+"""GPU parity of every entry point against the CPU oracle, through the C ABI.
+
+Bars (stated here, derived in the design doc): decoded weights, quantized
+activations, int32 block dots and MoE row gathers are bit-exact; f32 matvec
+outputs are within scale-relative error max|a-b|/max|a| <= 1e-4 of the f64
+oracle.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+SCALE_REL_TOL = 1e-4
+GEN = {"q4k": synth.gen_q4k_rows, "q6k": synth.gen_q6k_rows, "q8_0": synth.gen_q8_0_rows}
+QK = {"q4k": 256, "q6k": 256, "q8_0": 32}
+
+
+@pytest.fixture(scope="module")
+def q():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    import ggml_format_dequant_gb300 as lib
+    lib.qmv_device_status(clear=True)
+    return lib
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def scale_rel(ref, got):
+    ref = np.asarray(ref, dtype=np.float64)
+    got = np.asarray(got, dtype=np.float64)
+    return float(np.max(np.abs(ref - got)) / max(float(np.max(np.abs(ref))), 1e-30))
+
+
+def run_matvec(q, fmt, w, x, rows, k, cfg=None):
+    y = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+    fn = {"q4k": q.qmv_q4k, "q6k": q.qmv_q6k, "q8_0": q.qmv_q8_0}[fmt]
+    fn(dev(w), dev(x), y, rows, k, cfg=cfg)
+    return host(y)
+
+
+# ------------------------------------------------------------------ decode
+
+@pytest.mark.parametrize("fmt,rows,k", [("q4k", 37, 512), ("q4k", 3, 2304), ("q6k", 37, 512),
+                                        ("q6k", 5, 256), ("q8_0", 37, 96), ("q8_0", 3, 4096)])
+def test_dequant_bit_exact(q, fmt, rows, k):
+    st = synth.Stream(1000 + rows + k)
+    w = GEN[fmt](st, rows, k) if fmt != "q8_0" else synth.gen_q8_0_rows(st, rows, k, q_range=(-128, 127))
+    out = torch.empty(rows, k, dtype=torch.float32, device="cuda")
+    getattr(q, f"qmv_dequant_{fmt}")(dev(w), out, rows, k)
+    ref = oracle.dequant(fmt, w, rows, k).astype(np.float32)   # RNE of the exact value
+    assert np.array_equal(host(out), ref)
+
+
+def test_dequant_subnormal_scales(q):
+    st = synth.Stream(5)
+    w = synth.gen_q4k_rows(st, 4, 256, d_range=(0.0, 6e-8), dmin_range=(0.0, 6e-8))
+    out = torch.empty(4, 256, dtype=torch.float32, device="cuda")
+    q.qmv_dequant_q4k(dev(w), out, 4, 256)
+    assert np.array_equal(host(out), oracle.dequant("q4k", w, 4, 256).astype(np.float32))
+
+
+# ------------------------------------------------------------------ matvec
+
+SHAPES = [("q4k", 256, 1024), ("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 4352), ("q4k", 20, 16384),
+          ("q6k", 300, 512), ("q6k", 3, 256), ("q6k", 41, 14336), ("q6k", 130, 2816),
+          ("q8_0", 300, 96), ("q8_0", 7, 4096), ("q8_0", 13, 32), ("q8_0", 64, 11008)]
+
+
+@pytest.mark.parametrize("fmt,rows,k", SHAPES)
+def test_matvec_matches_oracle(q, fmt, rows, k):
+    st = synth.Stream(rows * 7 + k)
+    w = GEN[fmt](st, rows, k)
+    x = synth.gen_normal(st, k)
+    y = run_matvec(q, fmt, w, x, rows, k)
+    assert scale_rel(oracle.qmv(fmt, w, x, rows, k), y) <= SCALE_REL_TOL
+
+
+@pytest.mark.parametrize("cfg", [dict(ctas=1, stage_rows=1, stages=2), dict(ctas=3, stage_rows=5, stages=2),
+                                 dict(ctas=2, stage_rows=3, stages=1), dict(ctas=7, stages=3)])
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0"])
+def test_matvec_forced_pipelines(q, fmt, cfg):
+    """Small CTA counts and stages force many trips around the stage ring and a
+    ragged last stage; every output must still match."""
+    rows, k = 61, 512
+    st = synth.Stream(17)
+    w = GEN[fmt](st, rows, k)
+    x = synth.gen_normal(st, k)
+    y = run_matvec(q, fmt, w, x, rows, k, cfg=cfg)
+    assert not np.any(np.isnan(y))
+    assert scale_rel(oracle.qmv(fmt, w, x, rows, k), y) <= SCALE_REL_TOL
+
+
+@pytest.mark.parametrize("fmt,rows,k", [("q4k", 64, 1024), ("q6k", 24, 768), ("q8_0", 40, 256),
+                                        ("q4k", 9, 16384)])
+def test_unit_vector_is_exact(q, fmt, rows, k):
+    """x = e_j leaves one nonzero product: y[r] must equal the decoded weight
+    W[r, j] bit for bit, through the real matvec kernel."""
+    st = synth.Stream(23)
+    w = GEN[fmt](st, rows, k)
+    W = oracle.dequant(fmt, w, rows, k).astype(np.float32)
+    for j in sorted({0, 1, 15, 16, 31, 32, 63, 64, 100, 127, 128, 200, 255, k // 2 + 3, k - 1}):
+        e = np.zeros(k, dtype=np.float32)
+        e[j] = 1.0
+        y = run_matvec(q, fmt, w, e, rows, k)
+        assert np.array_equal(y, W[:, j]), f"column {j}"
+
+
+def test_matvec_scaled_unit_vectors(q):
+    """Powers of two other than 1 must stay exact as well (limb scaling)."""
+    rows, k = 16, 512
+    w = synth.gen_q4k_rows(synth.Stream(3), rows, k)
+    W = oracle.dequant("q4k", w, rows, k)
+    for j, v in [(5, 0.125), (300, 1024.0), (511, -2.0 ** -20)]:
+        e = np.zeros(k, dtype=np.float32)
+        e[j] = v
+        y = run_matvec(q, "q4k", w, e, rows, k)
+        assert np.array_equal(y, (W[:, j] * v).astype(np.float32))
+
+
+def test_matvec_deterministic_and_stream(q):
+    rows, k = 512, 4096
+    st = synth.Stream(8)
+    w = dev(synth.gen_q4k_rows(st, rows, k))
+    x = dev(synth.gen_normal(st, k))
+    s = torch.cuda.Stream()
+    y1 = torch.empty(rows, device="cuda")
+    y2 = torch.empty(rows, device="cuda")
+    with torch.cuda.stream(s):
+        q.qmv_q4k(w, x, y1, rows, k)
+        q.qmv_q4k(w, x, y2, rows, k, stream=s)
+    s.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_matvec_extreme_activations(q):
+    """Groups of tiny, huge and zero activations next to ordinary ones."""
+    rows, k = 33, 1024
+    st = synth.Stream(41)
+    w = synth.gen_q4k_rows(st, rows, k)
+    x = synth.gen_normal(st, k)
+    x[0:32] = 0.0
+    x[32:64] *= np.float32(1e-30)
+    x[64:96] *= np.float32(1e30)
+    x[96:128] = np.float32(1e-40)   # subnormal
+    x[200] = np.float32(1e36)    # sum(q*x) of its sub-block must stay finite in f32
+    ref = oracle.qmv("q4k", w, x, rows, k)
+    y = run_matvec(q, "q4k", w, x, rows, k)
+    assert scale_rel(ref, y) <= SCALE_REL_TOL
+
+
+# ------------------------------------------------- activation quant + dp4a
+
+def test_quantize_act_bit_exact(q):
+    m, k = 3, 4096
+    x = synth.gen_normal(synth.Stream(12), m * k).astype(np.float32) * np.float32(2.5)
+    x[0:32] = 0.0                                     # amax == 0 block
+    x[32:64] = 0.0
+    x[32:38] = [127.0, 2.5, 3.5, -2.5, 0.5, -0.5]     # exact ties
+    x[64:96] *= np.float32(1e-38)
+    xq = torch.empty(m * k, dtype=torch.int8, device="cuda")
+    xs = torch.empty(m * k // 32, dtype=torch.float32, device="cuda")
+    xsum = torch.empty(m * k // 32, dtype=torch.float32, device="cuda")
+    q.quantize_act_q8(dev(x), xq, xs, xsum, m, k)
+    oq, os_, osum = oracle.quantize_act_q8(x, m, k)
+    assert np.array_equal(host(xq), oq.reshape(-1))
+    assert np.array_equal(host(xs), os_.reshape(-1))
+    assert np.array_equal(host(xsum), osum.reshape(-1))
+    # without the optional sum
+    q.quantize_act_q8(dev(x), xq, xs, None, m, k)
+    assert np.array_equal(host(xq), oq.reshape(-1))
+
+
+@pytest.mark.parametrize("rows,k", [(300, 4096), (7, 96), (1, 32)])
+def test_blockdots_bit_exact(q, rows, k):
+    st = synth.Stream(rows + k)
+    w = synth.gen_q8_0_rows(st, rows, k, q_range=(-128, 127))
+    xq, xs, _ = oracle.quantize_act_q8(synth.gen_normal(st, k), 1, k)
+    dots = torch.empty(rows, k // 32, dtype=torch.int32, device="cuda")
+    q.qmv_q8_dp4a_blockdots(dev(w), dev(xq.reshape(-1)), dots, rows, k)
+    assert np.array_equal(host(dots), oracle.q8_blockdots(w, xq.reshape(-1), rows, k))
+
+
+@pytest.mark.parametrize("rows,k,cfg", [(300, 4096, None), (61, 256, dict(ctas=2, stage_rows=3, stages=2)),
+                                        (5, 32, None)])
+def test_dp4a_matvec(q, rows, k, cfg):
+    st = synth.Stream(99 + rows)
+    w = synth.gen_q8_0_rows(st, rows, k)
+    x = synth.gen_normal(st, k)
+    xq = torch.empty(k, dtype=torch.int8, device="cuda")
+    xs = torch.empty(k // 32, dtype=torch.float32, device="cuda")
+    q.quantize_act_q8(dev(x), xq, xs, None, 1, k)
+    y = torch.empty(rows, dtype=torch.float32, device="cuda")
+    q.qmv_q8_dp4a(dev(w), xq, xs, y, rows, k, cfg=cfg)
+    oq, os_, _ = oracle.quantize_act_q8(x, 1, k)
+    ref = oracle.qmv_q8_dp4a(w, oq.reshape(-1), os_.reshape(-1), rows, k)
+    assert scale_rel(ref, host(y)) <= SCALE_REL_TOL
+
+
+# --------------------------------------------------------------------- MoE
+
+def moe_run(q, bank, x, ids, rows, k, n_experts, cfg=None):
+    slots = len(ids)
+    y = torch.full((slots, rows), 7.0, dtype=torch.float32, device="cuda")
+    q.moe_qmv_q4k(dev(bank), dev(x), y, rows, k, dev(np.asarray(ids, dtype=np.int32)), slots, n_experts, cfg=cfg)
+    return host(y)
+
+
+@pytest.mark.parametrize("e,n,k,ids", [(16, 96, 512, [3, 15, 0, 3]), (4, 768, 512, [1, 2]),
+                                       (8, 7, 256, [7, 6, 5, 4, 3, 2, 1, 0, 7])])
+def test_moe_matches_oracle(q, e, n, k, ids):
+    st = synth.Stream(e * n + k)
+    bank = synth.gen_q4k_rows(st, e * n, k)
+    x = synth.gen_normal(st, len(ids) * k).reshape(len(ids), k)
+    y = moe_run(q, bank, x, ids, n, k, e)
+    ref = oracle.moe_qmv("q4k", bank, x, np.array(ids, dtype=np.int32), n, k, e)
+    for s in range(len(ids)):
+        assert scale_rel(ref[s], y[s]) <= SCALE_REL_TOL
+
+
+def test_moe_gather_exact(q):
+    """x[s] = e_j in every slot: y[s] must be column j of expert ids[s] exactly,
+    so any wrong expert or row shows up bit-wise."""
+    e, n, k = 12, 40, 512
+    bank = synth.gen_q4k_rows(synth.Stream(4), e * n, k)
+    W = oracle.dequant("q4k", bank, e * n, k).reshape(e, n, k).astype(np.float32)
+    ids = [11, 0, 5, 5, 3]
+    for j in [0, 77, 511]:
+        x = np.zeros((len(ids), k), dtype=np.float32)
+        x[:, j] = 1.0
+        y = moe_run(q, bank, x, ids, n, k, e, cfg=dict(ctas=2, stage_rows=3, stages=2))
+        for s, eid in enumerate(ids):
+            assert np.array_equal(y[s], W[eid, :, j])
+
+
+def test_moe_bad_ids_give_nan_and_status(q):
+    e, n, k = 4, 16, 256
+    st = synth.Stream(6)
+    bank = synth.gen_q4k_rows(st, e * n, k)
+    x = synth.gen_normal(st, 4 * k).reshape(4, k)
+    q.qmv_device_status(clear=True)
+    y = moe_run(q, bank, x, [1, 4, -1, 2], n, k, e)
+    assert np.all(np.isnan(y[1])) and np.all(np.isnan(y[2]))
+    ref = oracle.moe_qmv("q4k", bank, x, np.array([1, 0, 0, 2], dtype=np.int32), n, k, e)
+    assert scale_rel(ref[0], y[0]) <= SCALE_REL_TOL and scale_rel(ref[3], y[3]) <= SCALE_REL_TOL
+    assert q.qmv_device_status(clear=True) & q.QMV_STATUS_BAD_EXPERT_ID
+    assert q.qmv_device_status(clear=True) == 0
+
+
+# ----------------------------------------------------------- argument errors
+
+def test_argument_errors(q):
+    w = torch.zeros(144 * 4 + 16, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(512, dtype=torch.float32, device="cuda")
+    y = torch.zeros(8, dtype=torch.float32, device="cuda")
+    assert q.qmv_q4k(w, x, y, 2, 300, check=False) == q.QMV_EINVAL
+    assert q.qmv_q4k(w, x, y, 0, 256, check=False) == q.QMV_EINVAL
+    assert q.qmv_q4k(None, x, y, 2, 256, check=False) == q.QMV_EINVAL
+    assert q.qmv_q4k(w.data_ptr() + 2, x, y, 2, 256, check=False) == q.QMV_EALIGN
+    assert q.qmv_q8_0(w, x, y, 2, 48, check=False) == q.QMV_EINVAL
+    ids = torch.zeros(2, dtype=torch.int32, device="cuda")
+    assert q.moe_qmv_q4k(w, x, y, 2, 256, ids, 0, 2, check=False) == q.QMV_EINVAL
+    assert q.moe_qmv_q4k(w, x, y, 2, 256, ids, 2, 0, check=False) == q.QMV_EINVAL
+    assert q.quantize_act_q8(x, w, y, None, 1, 40, check=False) == q.QMV_EINVAL
+    assert q.qmv_q8_dp4a(w, w.data_ptr() + 4, y, y, 2, 32, check=False) == q.QMV_EALIGN
+
+
+# ------------------------------------------------- full-size workloads
+
+def _full(q, name):
+    c = synth.make_config(name)
+    return c
+
+
+def test_full_q4k_4096(q):
+    c = synth.make_config("q4k_4096x4096")
+    y = run_matvec(q, "q4k", c["w"], c["x"], 4096, 4096)
+    assert scale_rel(oracle.qmv("q4k", c["w"], c["x"], 4096, 4096), y) <= SCALE_REL_TOL
+
+
+def test_full_q4k_256(q):
+    c = synth.make_config("q4k_256x1024")
+    y = run_matvec(q, "q4k", c["w"], c["x"], 256, 1024)
+    assert scale_rel(oracle.qmv("q4k", c["w"], c["x"], 256, 1024), y) <= SCALE_REL_TOL
+
+
+def test_full_q6k_4096x14336(q):
+    c = synth.make_config("q6k_4096x14336")
+    y = run_matvec(q, "q6k", c["w"], c["x"], 4096, 14336)
+    assert scale_rel(oracle.qmv("q6k", c["w"], c["x"], 4096, 14336), y) <= SCALE_REL_TOL
+
+
+def test_full_q8_dp4a_14336x4096(q):
+    c = synth.make_config("q8_0_dp4a_14336x4096")
+    rows, k = 14336, 4096
+    xq = torch.empty(k, dtype=torch.int8, device="cuda")
+    xs = torch.empty(k // 32, dtype=torch.float32, device="cuda")
+    wd = dev(c["w"])
+    q.quantize_act_q8(dev(c["x"]), xq, xs, None, 1, k)
+    y = torch.empty(rows, dtype=torch.float32, device="cuda")
+    q.qmv_q8_dp4a(wd, xq, xs, y, rows, k)
+    dots = torch.empty(rows, k // 32, dtype=torch.int32, device="cuda")
+    q.qmv_q8_dp4a_blockdots(wd, xq, dots, rows, k)
+    oq, os_, _ = oracle.quantize_act_q8(c["x"], 1, k)
+    assert np.array_equal(host(xq), oq.reshape(-1)) and np.array_equal(host(xs), os_.reshape(-1))
+    assert np.array_equal(host(dots), oracle.q8_blockdots(c["w"], oq.reshape(-1), rows, k))
+    ref = oracle.qmv_q8_dp4a(c["w"], oq.reshape(-1), os_.reshape(-1), rows, k)
+    assert scale_rel(ref, host(y)) <= SCALE_REL_TOL
+
+
+def test_full_moe(q):
+    c = synth.make_config("moe_q4k_e128_n768_k2048_s8")
+    y = moe_run(q, c["w"], c["x"], c["ids"], 768, 2048, 128)
+    ref = oracle.moe_qmv("q4k", c["w"], c["x"], c["ids"], 768, 2048, 128)
+    assert scale_rel(ref, y) <= SCALE_REL_TOL
