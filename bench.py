@@ -166,7 +166,7 @@ class ClockSampler:
 class Workload:
     """Device buffers of one named workload, rotated over `copies` weights."""
 
-    def __init__(self, q, torch, name: str, l2_bytes: int, device):
+    def __init__(self, q, torch, name: str, l2_bytes: int, device, copies: int = 0):
         self.name = name
         c = synth.make_config(name)
         self.c = c
@@ -174,7 +174,7 @@ class Workload:
         self.rows, self.k = c["rows"], c["k"]
         dev = device
         wb = c["w"].nbytes
-        self.copies = max(4, math.ceil(3 * l2_bytes / wb) + 1)
+        self.copies = copies if copies > 0 else max(4, math.ceil(3 * l2_bytes / wb) + 1)
         # one pinned host copy, `copies` device copies (content identical; the
         # addresses differ, which is what makes each call read from HBM)
         w0 = torch.from_numpy(c["w"].reshape(-1))
@@ -194,25 +194,26 @@ class Workload:
             self.xs = torch.empty(self.k // 32, dtype=torch.float32, device=dev)
             q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k)
         self.q = q
+        self.cfg = None   # optional forced launch configuration (dict), for tuning sweeps
 
     def call(self, i: int, stream: int, with_quant: bool = False) -> int:
         """Enqueue call i; returns the number of kernels it launched."""
-        q, w = self.q, self.w[i % self.copies]
+        q, w, cfg = self.q, self.w[i % self.copies], self.cfg
         if self.kind == "q4k":
-            q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream)
+            q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
         elif self.kind == "q6k":
-            q.qmv_q6k(w, self.x, self.y, self.rows, self.k, stream=stream)
+            q.qmv_q6k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
         elif self.kind == "q8_0_dp4a":
             n = 1
             if with_quant:
                 q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k, stream=stream)
                 n = 2
-            q.qmv_q8_dp4a(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream)
+            q.qmv_q8_dp4a(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg)
             return n
         elif self.kind == "moe_q4k":
             c = self.c
             q.moe_qmv_q4k(w, self.x, self.y, self.rows, self.k, self.ids[i % len(self.ids)], c["slots"],
-                          c["n_experts"], stream=stream)
+                          c["n_experts"], stream=stream, cfg=cfg)
         return 1
 
 
@@ -282,6 +283,9 @@ def run_ours(args):
     sampler.start()
 
     # ------------------------------------------------ the headline workload
+    # Decode-chain mode: each call streams its (constant) weights while the
+    # previous call finishes (programmatic dependent launch); see qmv.h.
+    q.qmv_set_weight_prefetch(not args.isolated)
     wl = Workload(q, torch, HEADLINE, l2, device)
     K, W = args.steps, args.warmup
     # warm-up steps (untimed)
@@ -329,23 +333,32 @@ def run_ours(args):
     e2e = end_to_end(torch, q, wl, device, K)
 
     # ------------------------------------------------ the other workloads
-    per_config = {HEADLINE: config_row(HEADLINE, ms_step, peak, peak_kind, wl.copies)}
+    # every workload, chained (overlap on) and isolated (overlap off)
+    per_config = {}
     del wl, gk, gw
     torch.cuda.empty_cache()
-    if not args.headline_only:
-        for name in synth.CONFIGS:
-            if name == HEADLINE:
-                continue
-            w2 = Workload(q, torch, name, l2, device)
-            n = max(64, w2.copies)
+    names = [HEADLINE] if args.headline_only else list(synth.CONFIGS)
+    for name in names:
+        w2 = Workload(q, torch, name, l2, device)
+        n = max(64, w2.copies)
+        row = None
+        for chained in (True, False):
+            q.qmv_set_weight_prefetch(chained)
             ms, _, g2, _ = time_graph(torch, w2, n, replays=4)
-            per_config[name] = config_row(name, ms, peak, peak_kind, w2.copies)
+            del g2
+            if chained:
+                row = config_row(name, ms, peak, peak_kind, w2.copies)
+            else:
+                row["isolated_us_per_call"] = round(ms * 1e3, 3)
+                row["isolated_packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
             if w2.kind == "q8_0_dp4a":
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
-                per_config[name]["with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
+                row[("" if chained else "isolated_") + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
                 del g3
-            del w2, g2
-            torch.cuda.empty_cache()
+        per_config[name] = row
+        del w2
+        torch.cuda.empty_cache()
+    q.qmv_set_weight_prefetch(False)
     sampler.stop()
     clocks = sampler.summary(*clock_window)
     clocks["window"] = "nvidia-smi every 50 ms over a 0.5 s pre-roll, the timed region and a 0.5 s post-roll of the same graph"
@@ -372,6 +385,9 @@ def run_ours(args):
                 "l2": f"inputs larger than L2: {per_config[HEADLINE]['rotation_copies']} rotated weight copies "
                       f"({per_config[HEADLINE]['rotation_copies'] * wbytes / 2**20:.0f} MiB) vs L2 {l2 / 2**20:.0f} MiB",
                 "timing": "K calls captured in one CUDA graph, CUDA events on the launching stream",
+                "launch": ("isolated calls" if args.isolated else
+                           "decode chain: programmatic dependent launch, each call streams its weights while "
+                           "the previous call finishes (qmv_set_weight_prefetch)"),
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             },
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -509,6 +525,27 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_profile(args):
+    """A few eager calls of one workload and nothing else: the command ncu
+    captures (ncu flushes the caches between its replay passes, so one weight
+    copy suffices)."""
+    import torch
+
+    import __graft_entry__
+    import ggml_format_dequant_gb300 as q
+
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    wl = Workload(q, torch, args.profile_workload, 0, device, copies=1)
+    s = torch.cuda.current_stream().cuda_stream
+    for i in range(args.warmup + args.steps):
+        wl.call(i, s, with_quant=True)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_workload": args.profile_workload, "calls": args.warmup + args.steps,
+                      "y_finite": bool(torch.isfinite(wl.y).all().item())}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,7 +553,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="skip the per-config table")
+    ap.add_argument("--isolated", action="store_true",
+                    help="time the headline without decode-chain overlap (programmatic dependent launch off)")
+    ap.add_argument("--profile-workload", choices=list(synth.CONFIGS),
+                    help="only run warmup+steps eager calls of this workload (the command ncu captures)")
     args = ap.parse_args()
+    if args.profile_workload:
+        run_profile(args)
+        return
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)

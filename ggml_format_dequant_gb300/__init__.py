@@ -43,7 +43,8 @@ class QmvError(RuntimeError):
 
 
 class qmv_cfg(ctypes.Structure):
-    _fields_ = [("ctas", ctypes.c_int), ("stage_rows", ctypes.c_int), ("stages", ctypes.c_int)]
+    _fields_ = [("ctas", ctypes.c_int), ("stage_rows", ctypes.c_int), ("stages", ctypes.c_int),
+                ("copy", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -66,6 +67,7 @@ _SIG = {
     "qmv_q8_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_device_status": [_P, _I],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
+    "qmv_set_weight_prefetch": [_I],
 }
 
 _LIB = None
@@ -121,7 +123,8 @@ def _cfg(cfg):
         return None
     if isinstance(cfg, qmv_cfg):
         return ctypes.byref(cfg)
-    c = qmv_cfg(int(cfg.get("ctas", 0)), int(cfg.get("stage_rows", 0)), int(cfg.get("stages", 0)))
+    c = qmv_cfg(int(cfg.get("ctas", 0)), int(cfg.get("stage_rows", 0)), int(cfg.get("stages", 0)),
+                int(cfg.get("copy", 0)))
     return ctypes.byref(c)
 
 
@@ -189,6 +192,11 @@ def qmv_device_status(clear=True) -> int:
     v = ctypes.c_uint(0)
     _call("qmv_device_status", ctypes.cast(ctypes.byref(v), ctypes.c_void_p), 1 if clear else 0)
     return v.value
+
+
+def qmv_set_weight_prefetch(enable: bool) -> bool:
+    """Enable decode-chain overlap (see qmv.h); returns the previous setting."""
+    return bool(load().qmv_set_weight_prefetch(1 if enable else 0))
 
 
 def qmv_plan_info(fmt, rows, k, slots=1, cfg=None) -> dict:

@@ -12,12 +12,12 @@ namespace {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Common checks of a dense matvec: non-null pointers, rows > 0, k a positive
-// multiple of the block size, weight 16-byte and f32 buffers 4-byte aligned,
-// and a total weight size that fits the address arithmetic.
+// multiple of the block size, weight and activation 16-byte and the output
+// 4-byte aligned, and a total weight size that fits the address arithmetic.
 int check_dense(const void* w, const void* x, const void* y, int rows, int k, int qk, int block_bytes) {
     if (!w || !x || !y) return QMV_EINVAL;
     if (rows <= 0 || k <= 0 || k % qk) return QMV_EINVAL;
-    if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return QMV_EALIGN;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4)) return QMV_EALIGN;
     const long long rb = static_cast<long long>(k / qk) * block_bytes;
     if (rb > INT_MAX || static_cast<long long>(rows) > LLONG_MAX / rb) return QMV_EINVAL;
     return QMV_OK;
@@ -97,17 +97,17 @@ int moe_qmv_q4k(const void* w_bank, const float* x, float* y, int rows, int k, c
 }
 
 int qmv_dequant_q4k(const void* w, float* out, int rows, int k, cudaStream_t stream) {
-    int rc = check_dense(w, out, out, rows, k, 256, 144);
+    int rc = check_dense(w, w, out, rows, k, 256, 144);
     return rc ? rc : qmvi::dequant_q4k(w, out, rows, k, stream);
 }
 
 int qmv_dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t stream) {
-    int rc = check_dense(w, out, out, rows, k, 256, 210);
+    int rc = check_dense(w, w, out, rows, k, 256, 210);
     return rc ? rc : qmvi::dequant_q6k(w, out, rows, k, stream);
 }
 
 int qmv_dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t stream) {
-    int rc = check_dense(w, out, out, rows, k, 32, 34);
+    int rc = check_dense(w, w, out, rows, k, 32, 34);
     return rc ? rc : qmvi::dequant_q8_0(w, out, rows, k, stream);
 }
 
@@ -129,6 +129,12 @@ const char* qmv_strerror(int code) {
     }
 }
 
+int qmv_set_weight_prefetch(int enable) {
+    const int old = __atomic_load_n(&qmv::weight_prefetch_flag(), __ATOMIC_RELAXED);
+    __atomic_store_n(&qmv::weight_prefetch_flag(), enable ? 1 : 0, __ATOMIC_RELAXED);
+    return old;
+}
+
 const char* qmv_last_cuda_error(void) {
     return cudaGetErrorString(qmv::last_cuda_error());
 }
@@ -147,19 +153,23 @@ int qmv_device_status(unsigned int* status, int clear) {
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* threads, int* ctas,
                   int* stage_rows, int* stages, int* smem_bytes) {
     static const int qk[5] = {256, 256, 32, 32, 256};
-    static const int bb[5] = {144, 210, 34, 34, 144};
-    static const int upb[5] = {4, 4, 1, 1, 4};
     if (fmt < 0 || fmt > 4 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
     if (fmt == 4 && slots <= 0) return QMV_EINVAL;
     qmv::KParams kp{};
     qmv::Plan pl;
-    const long long rb = static_cast<long long>(k / qk[fmt]) * bb[fmt];
-    int rc = qmv::make_plan(upb[fmt] * (k / qk[fmt]), rb, rows, k, fmt != 3, fmt == 4 ? slots : 1, cfg, &kp, &pl);
+    int rc;
+    switch (fmt) {
+    case 0: rc = qmv::make_plan<qmv::Q4K>(rows, k, 1, cfg, &kp, &pl); break;
+    case 1: rc = qmv::make_plan<qmv::Q6K>(rows, k, 1, cfg, &kp, &pl); break;
+    case 2: rc = qmv::make_plan<qmv::Q8F>(rows, k, 1, cfg, &kp, &pl); break;
+    case 3: rc = qmv::make_plan<qmv::Q8D>(rows, k, 1, cfg, &kp, &pl); break;
+    default: rc = qmv::make_plan<qmv::Q4K>(rows, k, slots, cfg, &kp, &pl); break;
+    }
     if (rc) return rc;
     if (threads) *threads = pl.T;
     if (ctas) *ctas = pl.parts * (fmt == 4 ? slots : 1);
-    if (stage_rows) *stage_rows = pl.G;
-    if (stages) *stages = pl.S;
+    if (stage_rows) *stage_rows = kp.KS == 1 ? kp.R * (32 / kp.GS) : 1;
+    if (stages) *stages = kp.S;
     if (smem_bytes) *smem_bytes = static_cast<int>(pl.smem);
     return QMV_OK;
 }

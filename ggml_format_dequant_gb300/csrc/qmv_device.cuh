@@ -52,14 +52,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One potentially blocking test of phase `parity`: the hardware suspends the
+// thread until the phase completes or the hint (in ns) runs out, so waiting
+// warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
@@ -75,23 +78,40 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
-// L2 policy for the weight stream: each packed byte is read once per call, so
-// it is marked first-to-evict; the activation and other small data keep L2.
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
+// Programmatic dependent launch. launch_dependents lets the next kernel on the
+// stream be scheduled before this one ends; dependency_wait blocks until every
+// kernel this one depends on has finished and its memory is visible. Both are
+// no-ops for a kernel launched without the programmatic-serialization
+// attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // One bulk (non-tensor) TMA copy global -> shared, completing on `bar`.
 // dst, src and bytes must all be multiples of 16.
-__device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                             uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
+__device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through L2 only (LDGSTS); both
+// addresses 16-byte aligned. Completion is tracked with commit/wait groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most n of this thread's most recent groups are still pending.
+__device__ __forceinline__ void cp_async_wait(int n) {
+    switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
 }
 
 // d = c + sum of the four (unsigned byte of a) * (signed byte of b) products.
@@ -171,33 +191,62 @@ struct XPrepSmem {
     float* xsum16;     // [k/16] (sum of X over 16 elements) * 2^-s
 };
 
-// Fill the limb tables for x[0, k) (k a multiple of 32) with every warp of the
-// block; lanes map to elements so global loads are coalesced.
-__device__ __forceinline__ void prep_limbs(const float* __restrict__ x, int k, const XPrepSmem& P,
-                                           int warp, int nwarps, int lane) {
-    const int ngroups = k >> 5;
-    for (int g = warp; g < ngroups; g += nwarps) {
-        const float v = __ldg(x + (g << 5) + lane);
-        const uint32_t mag = __float_as_uint(v) & 0x7fffffffu;
-        const uint32_t mx = __reduce_max_sync(FULL, mag);
-        const int E = static_cast<int>(mx >> 23);          // biased exponent of the maximum
-        int s = LIMB_BITS - (E - 126);                      // max < 2^(E-126) for normal max
-        s = s > 126 ? 126 : s;                              // zero / tiny groups
-        const float p2s = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
-        const float p2ms = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-        const float t = __fmaf_rn(v, p2s, LIMB_MAGIC);
-        const uint32_t M = __float_as_uint(t) & 0x7fffffu;
-        const int i = (g << 5) + lane;
-        P.lc[i] = static_cast<uint8_t>((M & 0xffu) ^ 0x80u);
-        P.lb[i] = static_cast<uint8_t>(((M >> 8) & 0xffu) ^ 0x80u);
-        P.la[i] = static_cast<uint8_t>(static_cast<int>((M >> 16) & 0xffu) - 32);
-        int X = static_cast<int>(M) - 0x208080;
-        X += __shfl_xor_sync(FULL, X, 8);
-        X += __shfl_xor_sync(FULL, X, 4);
-        X += __shfl_xor_sync(FULL, X, 2);
-        X += __shfl_xor_sync(FULL, X, 1);
-        if ((lane & 15) == 0) P.xsum16[(g << 1) + (lane >> 4)] = __int2float_rn(X) * p2ms;
-        if (lane == 0) P.xs[g] = p2ms;
+// Fill the limb tables for x[0, k) (k a multiple of 32) with all T threads of
+// the block. Each thread owns float4 slots i = tid, tid + T, ...; a 32-element
+// group is 8 consecutive float4 slots, i.e. 8 consecutive lanes of one warp
+// (T is a multiple of 32). Loads are issued BATCH at a time before any use so
+// the prologue costs one or two memory round trips, not one per group.
+template <int BATCH>
+__device__ __forceinline__ void prep_limbs(const float* __restrict__ x, int k, const XPrepSmem& P, int tid,
+                                           int T) {
+    const int nvec = k >> 2;
+    const float4* __restrict__ x4 = reinterpret_cast<const float4*>(x);
+    for (int base = 0; base < nvec; base += BATCH * T) {
+        float4 v[BATCH];
+#pragma unroll
+        for (int b = 0; b < BATCH; b++) {
+            const int i = base + b * T + tid;
+            v[b] = (i < nvec) ? __ldg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; b++) {
+            if (base + b * T >= nvec) break;   // uniform: nvec is a multiple of 8 and T of 32
+            const int i = base + b * T + tid;
+            const uint32_t m4 = max(max(__float_as_uint(v[b].x) & 0x7fffffffu, __float_as_uint(v[b].y) & 0x7fffffffu),
+                                    max(__float_as_uint(v[b].z) & 0x7fffffffu, __float_as_uint(v[b].w) & 0x7fffffffu));
+            uint32_t mx = max(m4, __shfl_xor_sync(FULL, m4, 4));
+            mx = max(mx, __shfl_xor_sync(FULL, mx, 2));
+            mx = max(mx, __shfl_xor_sync(FULL, mx, 1));
+            const int E = static_cast<int>(mx >> 23);   // biased exponent of the group maximum
+            int s = LIMB_BITS - (E - 126);               // max < 2^(E-126) for a normal maximum
+            s = s > 126 ? 126 : s;                       // zero / tiny groups
+            const float p2s = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+            const float p2ms = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+            const uint32_t M0 = __float_as_uint(__fmaf_rn(v[b].x, p2s, LIMB_MAGIC)) & 0x7fffffu;
+            const uint32_t M1 = __float_as_uint(__fmaf_rn(v[b].y, p2s, LIMB_MAGIC)) & 0x7fffffu;
+            const uint32_t M2 = __float_as_uint(__fmaf_rn(v[b].z, p2s, LIMB_MAGIC)) & 0x7fffffu;
+            const uint32_t M3 = __float_as_uint(__fmaf_rn(v[b].w, p2s, LIMB_MAGIC)) & 0x7fffffu;
+            // byte 0 of M is c + 128, byte 1 is b + 128, byte 2 is a + 32
+            const uint32_t cw = __byte_perm(__byte_perm(M0, M1, 0x0040), __byte_perm(M2, M3, 0x0040), 0x5410) ^ 0x80808080u;
+            const uint32_t bw = __byte_perm(__byte_perm(M0, M1, 0x0051), __byte_perm(M2, M3, 0x0051), 0x5410) ^ 0x80808080u;
+            const uint32_t a0 = static_cast<uint32_t>(static_cast<int>(M0 >> 16) - 32);
+            const uint32_t a1 = static_cast<uint32_t>(static_cast<int>(M1 >> 16) - 32);
+            const uint32_t a2 = static_cast<uint32_t>(static_cast<int>(M2 >> 16) - 32);
+            const uint32_t a3 = static_cast<uint32_t>(static_cast<int>(M3 >> 16) - 32);
+            const uint32_t aw = __byte_perm(__byte_perm(a0, a1, 0x0040), __byte_perm(a2, a3, 0x0040), 0x5410);
+            int X = static_cast<int>(M0 + M1 + M2 + M3) - 4 * 0x208080;
+            X += __shfl_xor_sync(FULL, X, 2);
+            X += __shfl_xor_sync(FULL, X, 1);
+            // A whole 8-lane group is either inside [0, nvec) or past it
+            // (nvec is a multiple of 8), so the shuffles above stay in step.
+            if (i < nvec) {
+                reinterpret_cast<uint32_t*>(P.la)[i] = aw;
+                reinterpret_cast<uint32_t*>(P.lb)[i] = bw;
+                reinterpret_cast<uint32_t*>(P.lc)[i] = cw;
+                if ((tid & 3) == 0) P.xsum16[i >> 2] = __int2float_rn(X) * p2ms;
+                if ((tid & 7) == 0) P.xs[i >> 3] = p2ms;
+            }
+        }
     }
 }
 

@@ -29,11 +29,16 @@ namespace qmv {
 // d*sc_j*q_i - dmin*m_j, so the chunk contributes
 //     d*sc_2c * sum(q*x) - dmin*m_2c * sum(x)  +  (same for 2c+1).
 struct Q4K {
+    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 256;
     static constexpr int BLOCK_BYTES = 144;
-    static constexpr int UNITS_PER_BLOCK = 4;
-    static constexpr int UNIT_WEIGHTS = 64;
+    static constexpr int SLICE_BLOCKS = 8;    // 32 units = one warp's k-slice (1152 bytes)
     static constexpr bool LIMBS = true;
+
+    __host__ __device__ static int units(int nb) { return 4 * nb; }
+    // Unit u of a slice: byte offset of its block, index of its first weight.
+    __device__ __forceinline__ static int unit_byte(int u) { return (u >> 2) * BLOCK_BYTES; }
+    __device__ __forceinline__ static int unit_elem(int u) { return (u >> 2) * QK + 64 * (u & 3); }
 
     struct X {
         uint32_t a[16], b[16], c[16];   // limbs of the chunk's 64 activations
@@ -47,7 +52,8 @@ struct Q4K {
         bool hic;
     };
 
-    __device__ __forceinline__ static L lane_consts(int c) {
+    __device__ __forceinline__ static L lane_consts(int u, int /*nb*/, int /*ug*/) {
+        const int c = u & 3;
         L l;
         l.c = c;
         l.hic = c >= 2;
@@ -123,11 +129,17 @@ struct Q4K {
 // qh[32H + l], and all 16 share scale 8H + 2qd + hh. w = d*scale*(q - 32), so
 // each quarter contributes d*scale*(sum(q*x) - 32*sum(x)).
 struct Q6K {
+    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 256;
     static constexpr int BLOCK_BYTES = 210;
-    static constexpr int UNITS_PER_BLOCK = 4;
-    static constexpr int UNIT_WEIGHTS = 64;
+    static constexpr int SLICE_BLOCKS = 8;    // 32 units = one warp's k-slice (1680 bytes)
     static constexpr bool LIMBS = true;
+
+    __host__ __device__ static int units(int nb) { return 4 * nb; }
+    __device__ __forceinline__ static int unit_byte(int u) { return (u >> 2) * BLOCK_BYTES; }
+    __device__ __forceinline__ static int unit_elem(int u) {
+        return (u >> 2) * QK + 128 * ((u & 3) >> 1) + 16 * (u & 1);
+    }
 
     struct X {
         uint32_t a[16], b[16], c[16];   // [4*qd + i]: limbs of weights 128H+32qd+16hh+4i..
@@ -137,10 +149,10 @@ struct Q6K {
         int H, hh;
     };
 
-    __device__ __forceinline__ static L lane_consts(int v) {
+    __device__ __forceinline__ static L lane_consts(int u, int /*nb*/, int /*ug*/) {
         L l;
-        l.H = v >> 1;
-        l.hh = v & 1;
+        l.H = (u & 3) >> 1;
+        l.hh = u & 1;
         return l;
     }
 
@@ -206,11 +218,15 @@ struct Q6K {
 
 // ============================================================ Q8_0, f32 x
 struct Q8F {
+    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 32;
     static constexpr int BLOCK_BYTES = 34;
-    static constexpr int UNITS_PER_BLOCK = 1;
-    static constexpr int UNIT_WEIGHTS = 32;
+    static constexpr int SLICE_BLOCKS = 32;   // 32 one-block units (1088 bytes)
     static constexpr bool LIMBS = true;
+
+    __host__ __device__ static int units(int nb) { return nb; }
+    __device__ __forceinline__ static int unit_byte(int u) { return u * BLOCK_BYTES; }
+    __device__ __forceinline__ static int unit_elem(int u) { return u * QK; }
 
     struct X {
         uint32_t a[8], b[8], c[8];
@@ -219,7 +235,7 @@ struct Q8F {
     struct L {
         int unused;
     };
-    __device__ __forceinline__ static L lane_consts(int) { return L{0}; }
+    __device__ __forceinline__ static L lane_consts(int, int, int) { return L{0}; }
 
     __device__ __forceinline__ static void load_x(X& x, const XPrepSmem& P, int e0) {
 #pragma unroll
@@ -257,52 +273,79 @@ struct Q8F {
 // ======================================================= Q8_0, q8 activation
 //
 // The dp4a path: the activation is already int8 codes with one f32 scale per
-// 32-block (quantize_act_q8). Per block, dot = sum of 32 int8*int8 products
-// (exact int32), and the row sums d_w * d_x * dot in f32.
+// 32-block (quantize_act_q8). A unit is 4 consecutive blocks (128 weights), so
+// one warp's 32 units cover 4096 weights. Per block, dot = sum of 32
+// int8*int8 products (exact int32), and the row sums d_w * d_x * dot in f32.
 struct Q8D {
+    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 32;
     static constexpr int BLOCK_BYTES = 34;
-    static constexpr int UNITS_PER_BLOCK = 1;
-    static constexpr int UNIT_WEIGHTS = 32;
+    static constexpr int SLICE_BLOCKS = 128;  // 32 four-block units (4352 bytes)
     static constexpr bool LIMBS = false;
 
+    __host__ __device__ static int units(int nb) { return (nb + 3) / 4; }
+    __device__ __forceinline__ static int unit_byte(int u) { return u * 4 * BLOCK_BYTES; }
+    __device__ __forceinline__ static int unit_elem(int u) { return u * 4 * QK; }
+
     struct X {
-        uint32_t q[8];
-        float xs;
+        uint32_t q[4][8];
+        float xs[4];
     };
     struct L {
-        int unused;
+        int nblk;   // blocks in this unit (4 except at a row's ragged end)
     };
-    __device__ __forceinline__ static L lane_consts(int) { return L{0}; }
-
-    __device__ __forceinline__ static void load_xq(X& x, const int8_t* __restrict__ xq,
-                                                   const float* __restrict__ xs, int e0) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(xq + e0));
-        const uint4 b = __ldg(reinterpret_cast<const uint4*>(xq + e0 + 16));
-        x.q[0] = a.x; x.q[1] = a.y; x.q[2] = a.z; x.q[3] = a.w;
-        x.q[4] = b.x; x.q[5] = b.y; x.q[6] = b.z; x.q[7] = b.w;
-        x.xs = __ldg(xs + (e0 >> 5));
+    // ug: the unit's index within the row; nb: blocks per row.
+    __device__ __forceinline__ static L lane_consts(int, int nb, int ug) {
+        const int left = nb - 4 * ug;
+        return L{left < 4 ? left : 4};
     }
 
-    __device__ __forceinline__ static int block_dot(const uint8_t* blk, const X& x) {
+    __device__ __forceinline__ static void load_xq(X& x, const L& l, const int8_t* __restrict__ xq,
+                                                   const float* __restrict__ xs, int e0) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (j < l.nblk) {
+                const uint4 a = __ldg(reinterpret_cast<const uint4*>(xq + e0 + 32 * j));
+                const uint4 b = __ldg(reinterpret_cast<const uint4*>(xq + e0 + 32 * j + 16));
+                x.q[j][0] = a.x; x.q[j][1] = a.y; x.q[j][2] = a.z; x.q[j][3] = a.w;
+                x.q[j][4] = b.x; x.q[j][5] = b.y; x.q[j][6] = b.z; x.q[j][7] = b.w;
+                x.xs[j] = __ldg(xs + (e0 >> 5) + j);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i++) x.q[j][i] = 0;
+                x.xs[j] = 0.0f;
+            }
+        }
+    }
+
+    // blk: one 34-byte block in shared memory (2-byte aligned).
+    __device__ __forceinline__ static int block_dot(const uint8_t* blk, const uint32_t* xq) {
         const uint4 q0 = lds16_a2(blk + 2);
         const uint4 q1 = lds16_a2(blk + 18);
         int s = 0;
-        s = dp4a_ss(q0.x, x.q[0], s);
-        s = dp4a_ss(q0.y, x.q[1], s);
-        s = dp4a_ss(q0.z, x.q[2], s);
-        s = dp4a_ss(q0.w, x.q[3], s);
-        s = dp4a_ss(q1.x, x.q[4], s);
-        s = dp4a_ss(q1.y, x.q[5], s);
-        s = dp4a_ss(q1.z, x.q[6], s);
-        s = dp4a_ss(q1.w, x.q[7], s);
+        s = dp4a_ss(q0.x, xq[0], s);
+        s = dp4a_ss(q0.y, xq[1], s);
+        s = dp4a_ss(q0.z, xq[2], s);
+        s = dp4a_ss(q0.w, xq[3], s);
+        s = dp4a_ss(q1.x, xq[4], s);
+        s = dp4a_ss(q1.y, xq[5], s);
+        s = dp4a_ss(q1.z, xq[6], s);
+        s = dp4a_ss(q1.w, xq[7], s);
         return s;
     }
 
-    __device__ __forceinline__ static float dot(const uint8_t* blk, const L&, const X& x, float r) {
-        const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16_a2(blk))));
-        const int s = block_dot(blk, x);
-        return __fmaf_rn(dw * x.xs, __int2float_rn(s), r);
+    // ub: the unit's first block in shared memory.
+    __device__ __forceinline__ static float dot(const uint8_t* ub, const L& l, const X& x, float r) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (j < l.nblk) {
+                const uint8_t* blk = ub + j * BLOCK_BYTES;
+                const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16_a2(blk))));
+                const int s = block_dot(blk, x.q[j]);
+                r = __fmaf_rn(dw * x.xs[j], __int2float_rn(s), r);
+            }
+        }
+        return r;
     }
 };
 

@@ -12,9 +12,8 @@
 
 namespace qmv {
 
-constexpr int THREADS_MAX = 256;
-constexpr long long STAGE_MAX_BYTES = 40 * 1024;   // rows per stage are capped by this
-constexpr int STAGES_MAX = 6;
+constexpr long long STAGE_MAX_BYTES = 32 * 1024;   // rows per stage are capped by this
+constexpr int STAGES_MAX = 8;
 constexpr int MAX_DEVICES = 64;
 
 // The last CUDA error seen by a launch on this thread (for qmv_last_cuda_error).
@@ -27,6 +26,13 @@ inline int cuda_rc(cudaError_t e) {
     if (e == cudaSuccess) return QMV_OK;
     last_cuda_error() = e;
     return QMV_ECUDA;
+}
+
+// Process-wide opt-in: launch with programmatic stream serialization so a call
+// streams its packed weights while the previous kernel on the stream finishes.
+inline int& weight_prefetch_flag() {
+    static int f = 0;
+    return f;
 }
 
 struct DevInfo {
@@ -56,9 +62,10 @@ inline int dev_info(DevInfo* out, int* dev_out) {
 }
 
 struct Plan {
-    int T = 0, GS = 0, NG = 0, UPL = 1, RG = 1, G = 1, S = 1;
+    int T = 0;            // threads per CTA
     int parts = 1;        // CTAs per matrix (grid.x)
-    bool resident = true;
+    int R = 1;            // row steps per slot (kernel template parameter)
+    bool bulk = false;    // copy engine: bulk TMA (true) or warp-wide cp.async (false)
     size_t smem = 0;
 };
 
@@ -70,94 +77,130 @@ inline int pow2ceil(int v) {
 
 inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a; }
 
-// U: units per row; limbs: the format keeps integer activation limbs in shared
-// memory; slots: MoE slot count (1 for dense).
-inline int make_plan(int U, long long rowbytes, int rows, int k, bool limbs, int slots,
-                     const qmv_cfg* cfg, KParams* kp, Plan* pl) {
+// Target bytes in flight per SM: measured on GB300, bulk copies reach the
+// HBM copy rate once roughly 64-128 KB per SM are outstanding; much more only
+// adds queueing delay before a CTA's first slot lands.
+constexpr long long IN_FLIGHT_BYTES = 96 * 1024;
+constexpr long long DEFER_MAX_BYTES = 48 * 1024;
+
+// Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense).
+template <class F>
+inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
     DevInfo di;
     int rc = dev_info(&di, nullptr);
     if (rc) return rc;
-    Plan P;
-    if (U <= 32) {
-        P.GS = pow2ceil(U);
-        P.NG = THREADS_MAX / P.GS;
-        P.T = THREADS_MAX;
-    } else if (U <= THREADS_MAX) {
-        P.GS = static_cast<int>(round_up(U, 32));
-        P.NG = THREADS_MAX / P.GS;
-        P.T = P.NG * P.GS;
-    } else {
-        P.GS = THREADS_MAX;
-        P.NG = 1;
-        P.T = THREADS_MAX;
-        P.UPL = (U + THREADS_MAX - 1) / THREADS_MAX;
-        P.resident = false;
-    }
+    const int nb = k / F::QK;
+    const int U = F::units(nb);
+    const int KS = (U + 31) / 32;
+    const int GS = KS == 1 ? pow2ceil(U) : 32;
+    const int rpw = 32 / GS;
+    const int nw_max = F::MAX_THREADS / 32;
+    if (KS > nw_max) return QMV_ETOOBIG;
+    const long long rowbytes = static_cast<long long>(nb) * F::BLOCK_BYTES;
 
-    // CTAs per matrix: enough to cover every SM once (MoE: shared by the
-    // slots), never fewer rows per CTA than the groups can take in one pass
-    // unless the matrix is that small.
-    const int by_groups = (rows + P.NG - 1) / P.NG;
+    Plan P;
+    // CTAs per matrix: one per SM (MoE: the SMs are shared by the slots), but
+    // not more than there are rows.
     if (cfg && cfg->ctas > 0)
         P.parts = std::min(cfg->ctas, rows);
     else if (slots > 1)
-        P.parts = std::min((di.nsm + slots - 1) / slots, by_groups);
+        P.parts = std::min((di.nsm + slots - 1) / slots, rows);
     else
-        P.parts = std::min(di.nsm, by_groups);
+        P.parts = std::min(di.nsm, rows);
     P.parts = std::max(P.parts, 1);
     const int rpc = (rows + P.parts - 1) / P.parts;
 
-    // Rows per stage: up to 4 per group, as many as the CTA has, capped by the
-    // stage byte budget.
-    long long G = std::min<long long>(4LL * P.NG, rpc);
-    if (cfg && cfg->stage_rows > 0) G = std::min<long long>(G, cfg->stage_rows);
-    G = std::min<long long>(G, (STAGE_MAX_BYTES - 32) / rowbytes);
-    if (G < 1) return QMV_ETOOBIG;
-    P.G = static_cast<int>(G);
-    P.RG = pow2ceil((P.G + P.NG - 1) / P.NG);
+    // Row groups: as many as the thread budget holds, no more than the CTA's
+    // rows can feed.
+    int NG = std::max(1, nw_max / KS);
+    NG = std::min(NG, (rpc + rpw - 1) / rpw);
+    NG = std::max(NG, 1);
+    const int nwarps = NG * KS;
+    P.T = 32 * nwarps;
+    const int rows_per_group = (rpc + NG - 1) / NG;
 
-    const long long stage_stride = round_up(P.G * rowbytes + 32, 128);
-    const int nst_max = (rpc + P.G - 1) / P.G;
+    // Slot = R row steps (KS == 1) or one row's slice (KS > 1).
+    int R = 1;
+    if (KS == 1 && cfg && cfg->stage_rows > 0) {
+        const int want = std::max(1, cfg->stage_rows / rpw);
+        R = want >= 4 ? 4 : (want >= 2 ? 2 : 1);
+    }
+    P.R = R;
+    // Copy engine. At the start of a microsecond-scale kernel a single lane
+    // issuing bulk copies generates requests more slowly than 32 lanes issuing
+    // 16-byte cp.async, so cp.async is the default; bulk TMA stays selectable.
+    P.bulk = cfg && cfg->copy == 1;
+    const long long slot_bytes = KS == 1 ? static_cast<long long>(R) * rpw * rowbytes
+                                         : static_cast<long long>(F::SLICE_BLOCKS) * F::BLOCK_BYTES;
+    if (slot_bytes + 32 > 0x7fffffffLL) return QMV_ETOOBIG;
+    const long long slot_stride = round_up(slot_bytes + 32, 128);
+    const int steps = KS == 1 ? (rows_per_group + R * rpw - 1) / (R * rpw) : rows_per_group;
 
-    // Shared-memory layout: limb tables, reduction buffer, stages, barriers.
+    // Shared-memory layout: limb tables, slice partials, slots, barriers.
     long long off = 0;
     kp->off_la = kp->off_lb = kp->off_lc = kp->off_xs = kp->off_xsum = 0;
-    if (limbs) {
+    if (F::LIMBS) {
         kp->off_la = static_cast<uint32_t>(off); off = round_up(off + k, 128);
         kp->off_lb = static_cast<uint32_t>(off); off = round_up(off + k, 128);
         kp->off_lc = static_cast<uint32_t>(off); off = round_up(off + k, 128);
         kp->off_xs = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 32), 128);
         kp->off_xsum = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 16), 128);
     }
+    // Row partials: park every lane's partial ([rows][KS * GS] floats) and
+    // reduce once at the end when that fits comfortably; otherwise reduce each
+    // slot with shuffles and keep only per-slice partials ([rows][KS]).
+    const int W = KS * GS;
+    const bool defer = 4LL * rpc * W <= DEFER_MAX_BYTES;
     kp->off_red = static_cast<uint32_t>(off);
-    if (P.GS > 32) off = round_up(off + 2LL * P.G * (P.GS / 32) * 4, 128);
-    const long long fixed = off + 8 * STAGES_MAX + 1024;   // + barriers + static shared memory
-    const long long avail = di.smem_optin - fixed;
-    int S = (cfg && cfg->stages > 0) ? std::min(cfg->stages, STAGES_MAX) : STAGES_MAX;
-    S = std::min<long long>(S, nst_max);
-    S = static_cast<int>(std::min<long long>(S, avail / stage_stride));
+    if (defer)
+        off = round_up(off + 4LL * rpc * W, 128);
+    else if (KS > 1)
+        off = round_up(off + 4LL * rpc * KS, 128);
+    const long long avail = di.smem_optin - 1024 - off;   // 1 KB for static shared memory
+    const long long per_slot = nwarps * (slot_stride + (P.bulk ? 8 : 0));
+    int S;
+    if (cfg && cfg->stages > 0)
+        S = cfg->stages;
+    else
+        S = static_cast<int>(std::min<long long>(8, std::max<long long>(2, IN_FLIGHT_BYTES / (nwarps * slot_bytes))));
+    S = std::min(S, std::max(steps, 1));
+    S = static_cast<int>(std::min<long long>(S, avail / per_slot));
     if (S < 1) return QMV_ETOOBIG;
-    P.S = S;
-    kp->off_stage = static_cast<uint32_t>(off);
-    kp->stage_stride = static_cast<uint32_t>(stage_stride);
-    off += stage_stride * S;
-    kp->off_bar = static_cast<uint32_t>(off);
-    off += 8 * S;
+    kp->off_slots = static_cast<uint32_t>(off);
+    kp->slot_stride = static_cast<uint32_t>(slot_stride);
+    off += static_cast<long long>(nwarps) * S * slot_stride;
+    kp->off_bars = static_cast<uint32_t>(off);
+    off += 8LL * nwarps * S;
     P.smem = static_cast<size_t>(off);
 
+    kp->nb = nb;
+    kp->rowbytes = rowbytes;
     kp->U = U;
-    kp->GS = P.GS;
-    kp->NG = P.NG;
-    kp->G = P.G;
-    kp->S = P.S;
-    kp->UPL = P.UPL;
+    kp->KS = KS;
+    kp->GS = GS;
+    int lg = 0;
+    while ((1 << lg) < GS) lg++;
+    kp->lgGS = lg;
+    kp->NG = NG;
+    kp->R = R;
+    kp->S = S;
+    kp->defer = defer ? 1 : 0;
+    kp->W = W;
+    // Balanced splits, precomputed so the kernel only multiplies.
+    kp->rq = rows / P.parts;
+    kp->rrem = rows % P.parts;
+    for (int b = 0; b < 2; b++) {
+        const int n = kp->rq + b;
+        kp->gq[b] = n / NG;
+        kp->grem[b] = n % NG;
+    }
     *pl = P;
     return QMV_OK;
 }
 
-template <class F, int RG, bool RES, bool MOE, int MODE>
+template <class F, int R, bool MOE, int MODE, bool BULK>
 inline int launch_one(const KParams& kp, const Plan& pl, int slots, cudaStream_t stream) {
-    auto kern = qmv_stream_kernel<F, RG, RES, MOE, MODE>;
+    auto kern = qmv_stream_kernel<F, R, MOE, MODE, BULK>;
     // Dynamic shared memory above 48 KB must be opted into per kernel; the
     // attribute only ever grows, once per size class and device.
     static int configured[MAX_DEVICES] = {};
@@ -170,24 +213,32 @@ inline int launch_one(const KParams& kp, const Plan& pl, int slots, cudaStream_t
         if (rc) return rc;
         configured[dev] = static_cast<int>(pl.smem);
     }
-    kern<<<dim3(pl.parts, MOE ? slots : 1, 1), pl.T, pl.smem, stream>>>(kp);
-    return cuda_rc(cudaGetLastError());
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(pl.parts, MOE ? slots : 1, 1);
+    lc.blockDim = dim3(pl.T, 1, 1);
+    lc.dynamicSmemBytes = pl.smem;
+    lc.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED) ? 1 : 0;
+    return cuda_rc(cudaLaunchKernelEx(&lc, kern, kp));
+}
+
+template <class F, bool MOE, int MODE, bool BULK>
+inline int launch_r(const KParams& kp, const Plan& pl, int slots, cudaStream_t stream) {
+    switch (pl.R) {
+    case 1: return launch_one<F, 1, MOE, MODE, BULK>(kp, pl, slots, stream);
+    case 2: return launch_one<F, 2, MOE, MODE, BULK>(kp, pl, slots, stream);
+    default: return launch_one<F, 4, MOE, MODE, BULK>(kp, pl, slots, stream);
+    }
 }
 
 template <class F, bool MOE, int MODE>
 inline int launch(const KParams& kp, const Plan& pl, int slots, cudaStream_t stream) {
-    if (pl.resident) {
-        switch (pl.RG) {
-        case 1: return launch_one<F, 1, true, MOE, MODE>(kp, pl, slots, stream);
-        case 2: return launch_one<F, 2, true, MOE, MODE>(kp, pl, slots, stream);
-        default: return launch_one<F, 4, true, MOE, MODE>(kp, pl, slots, stream);
-        }
-    }
-    switch (pl.RG) {
-    case 1: return launch_one<F, 1, false, MOE, MODE>(kp, pl, slots, stream);
-    case 2: return launch_one<F, 2, false, MOE, MODE>(kp, pl, slots, stream);
-    default: return launch_one<F, 4, false, MOE, MODE>(kp, pl, slots, stream);
-    }
+    return pl.bulk ? launch_r<F, MOE, MODE, true>(kp, pl, slots, stream)
+                   : launch_r<F, MOE, MODE, false>(kp, pl, slots, stream);
 }
 
 // Read (and optionally clear) this translation unit's device status word.

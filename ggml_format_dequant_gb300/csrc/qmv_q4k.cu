@@ -57,7 +57,7 @@ int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
     kp.rowbytes = static_cast<long long>(kp.nb) * 144;
     kp.wbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
     Plan pl;
-    int rc = make_plan(4 * kp.nb, kp.rowbytes, rows, k, true, 1, cfg, &kp, &pl);
+    int rc = make_plan<Q4K>(rows, k, 1, cfg, &kp, &pl);
     if (rc) return rc;
     return launch<Q4K, false, MODE_MATVEC>(kp, pl, 1, s);
 }
@@ -76,7 +76,7 @@ int moe_q4k(const void* bank, const float* x, float* y, int rows, int k, const i
     kp.rowbytes = static_cast<long long>(kp.nb) * 144;
     kp.wbytes = static_cast<unsigned long long>(n_experts) * rows * kp.rowbytes;
     Plan pl;
-    int rc = make_plan(4 * kp.nb, kp.rowbytes, rows, k, true, slots, cfg, &kp, &pl);
+    int rc = make_plan<Q4K>(rows, k, slots, cfg, &kp, &pl);
     if (rc) return rc;
     return launch<Q4K, true, MODE_MATVEC>(kp, pl, slots, s);
 }

@@ -47,7 +47,7 @@ int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
     kp.rowbytes = static_cast<long long>(kp.nb) * 210;
     kp.wbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
     Plan pl;
-    int rc = make_plan(4 * kp.nb, kp.rowbytes, rows, k, true, 1, cfg, &kp, &pl);
+    int rc = make_plan<Q6K>(rows, k, 1, cfg, &kp, &pl);
     if (rc) return rc;
     return launch<Q6K, false, MODE_MATVEC>(kp, pl, 1, s);
 }

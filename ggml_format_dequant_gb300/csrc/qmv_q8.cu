@@ -72,7 +72,7 @@ int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg
     kp.x = x;
     kp.y = y;
     Plan pl;
-    int rc = make_plan(kp.nb, kp.rowbytes, rows, k, true, 1, cfg, &kp, &pl);
+    int rc = make_plan<Q8F>(rows, k, 1, cfg, &kp, &pl);
     if (rc) return rc;
     return launch<Q8F, false, MODE_MATVEC>(kp, pl, 1, s);
 }
@@ -84,7 +84,7 @@ int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows
     kp.xqs = xs;
     kp.y = y;
     Plan pl;
-    int rc = make_plan(kp.nb, kp.rowbytes, rows, k, false, 1, cfg, &kp, &pl);
+    int rc = make_plan<Q8D>(rows, k, 1, cfg, &kp, &pl);
     if (rc) return rc;
     return launch<Q8D, false, MODE_MATVEC>(kp, pl, 1, s);
 }
@@ -94,7 +94,7 @@ int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k
     kp.xq = xq;
     kp.dots = dots;
     Plan pl;
-    int rc = make_plan(kp.nb, kp.rowbytes, rows, k, false, 1, nullptr, &kp, &pl);
+    int rc = make_plan<Q8D>(rows, k, 1, nullptr, &kp, &pl);
     if (rc) return rc;
     return launch<Q8D, false, MODE_BLOCKDOTS>(kp, pl, 1, s);
 }

@@ -21,7 +21,9 @@
  *    asynchronously; outputs are valid once the stream reaches that point.
  *  - Packed weights are rows of whole blocks, row-major and contiguous (row r
  *    starts at byte r * (k / block_weights) * block_bytes). The weight pointer
- *    must be 16-byte aligned. Only the bytes of the rows read are accessed.
+ *    and the activation pointer (f32 x, or int8 xq) must be 16-byte aligned;
+ *    f32 outputs and scales 4-byte aligned. Only the bytes of the rows read
+ *    are accessed.
  *  - Outputs are overwritten, never accumulated into.
  *  - Return value: QMV_OK (0) or a negative QMV_E* code; qmv_strerror() names
  *    it. Argument errors are detected on the host before anything is enqueued.
@@ -53,18 +55,18 @@ extern "C" {
 #define QMV_ETOOBIG (-4) /* valid shape too large for this build's shared-memory plan */
 
 /* Q4_K matvec: y[r] = sum_j W[r, j] * x[j].
- * w: rows * (k/256) * 144 bytes, 16-byte aligned; x: f32 [k]; y: f32 [rows].
+ * w: rows * (k/256) * 144 bytes; x: f32 [k]; y: f32 [rows].
  * k must be a positive multiple of 256, rows > 0.
  * Cites hanzo-ml src/vulkan_backend.rs, matvec_q4k_gpu_off and quantize_q4k. */
 int qmv_q4k(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
 
 /* Q6_K matvec: y = W x. w: rows * (k/256) * 210 bytes (the 210-byte blocks are
- * read unpadded), 16-byte aligned; x: f32 [k]; y: f32 [rows]; k % 256 == 0.
+ * read unpadded); x: f32 [k]; y: f32 [rows]; k % 256 == 0.
  * Cites hanzo-ml src/vulkan_backend.rs, matvec_q6k_gpu and quantize_q6k. */
 int qmv_q6k(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
 
 /* Q8_0 matvec with an f32 activation: y = W x. w: rows * (k/32) * 34 bytes,
- * 16-byte aligned; x: f32 [k]; y: f32 [rows]; k % 32 == 0.
+ * x: f32 [k]; y: f32 [rows]; k % 32 == 0.
  * Cites hanzo-ml src/vulkan_backend.rs, matvec_q8_0_gpu (raw 34-byte blocks). */
 int qmv_q8_0(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
 
@@ -88,7 +90,7 @@ int qmv_q8_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int 
 
 /* MoE indexed Q4_K matvec: y[s, r] = sum_j W[ids[s], r, j] * x[s, j].
  * w_bank: one resident bank [n_experts, rows, k] of Q4_K rows (expert e's
- * matrix starts at byte e * rows * (k/256) * 144), 16-byte aligned;
+ * matrix starts at byte e * rows * (k/256) * 144);
  * x: f32 [slots, k] (one activation row per slot); y: f32 [slots, rows];
  * ids: DEVICE int32 [slots], read on the GPU (duplicates allowed). Only the
  * rows of the routed experts are read. A slot whose id lies outside
@@ -97,6 +99,16 @@ int qmv_q8_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int 
  * Cites hanzo-ml src/vulkan_backend.rs, moe_matvec_gpu. */
 int moe_qmv_q4k(const void *w_bank, const float *x, float *y, int rows, int k,
                 const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+
+/* Decode-chain overlap (off by default; process-wide). When enabled, every
+ * matvec launch allows programmatic dependent launch: a call may be scheduled
+ * while the previous kernel on the same stream is still running and starts
+ * streaming its packed weights at once, but it waits for that kernel to finish
+ * before it reads x (or, for MoE, ids) and before it writes y. Only enable it
+ * if the packed weights of a call are never written by the kernel launched just
+ * before it on the stream (true for inference, where weights are constant).
+ * Returns the previous setting. */
+int qmv_set_weight_prefetch(int enable);
 
 /* Name of a QMV_* return code. Never NULL. */
 const char *qmv_strerror(int code);
@@ -123,12 +135,14 @@ int qmv_device_status(unsigned int *status, int clear);
 
 /* Forced launch configuration: any field <= 0 keeps the automatic choice.
  * ctas: CTAs per weight matrix; stage_rows: rows per pipeline stage;
- * stages: pipeline depth. Used to exercise multi-stage pipelines and ragged
- * tails on small inputs. */
+ * stages: pipeline depth (slots per warp); copy: 1 = bulk TMA copies,
+ * 2 = 16-byte cp.async copies. Used to exercise multi-stage pipelines,
+ * ragged tails and both copy engines on small inputs. */
 typedef struct qmv_cfg {
     int ctas;
     int stage_rows;
     int stages;
+    int copy;
 } qmv_cfg;
 
 int qmv_q4k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,

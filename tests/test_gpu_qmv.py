@@ -91,7 +91,9 @@ def test_matvec_matches_oracle(q, fmt, rows, k):
 
 
 @pytest.mark.parametrize("cfg", [dict(ctas=1, stage_rows=1, stages=2), dict(ctas=3, stage_rows=5, stages=2),
-                                 dict(ctas=2, stage_rows=3, stages=1), dict(ctas=7, stages=3)])
+                                 dict(ctas=2, stage_rows=3, stages=1), dict(ctas=7, stages=3),
+                                 dict(ctas=1, stages=2, copy=1), dict(ctas=3, stage_rows=4, stages=3, copy=1),
+                                 dict(ctas=2, stages=1, copy=1), dict(ctas=5, stage_rows=2, stages=4, copy=2)])
 @pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0"])
 def test_matvec_forced_pipelines(q, fmt, cfg):
     """Small CTA counts and stages force many trips around the stage ring and a
@@ -327,3 +329,46 @@ def test_full_moe(q):
     y = moe_run(q, c["w"], c["x"], c["ids"], 768, 2048, 128)
     ref = oracle.moe_qmv("q4k", c["w"], c["x"], c["ids"], 768, 2048, 128)
     assert scale_rel(ref, y) <= SCALE_REL_TOL
+
+
+# ------------------------------------------------- decode-chain overlap mode
+
+def test_weight_prefetch_chain_matches(q):
+    """With programmatic dependent launch enabled, each call streams weights
+    while the previous kernel finishes but must still see that kernel's output
+    as its input. Run a chain y1 = W1 x, y2 = W2 y1, ... (square matrices,
+    every call reading the previous call's output, plus an MoE call reading
+    ids written by a torch kernel just before) with and without the overlap:
+    the results must be bitwise identical."""
+    n = 2048
+    st = synth.Stream(77)
+    ws = [dev(synth.gen_q4k_rows(st, n, n)) for _ in range(6)]
+    w6 = dev(synth.gen_q6k_rows(st, n, n))
+    bank = dev(synth.gen_q4k_rows(st, 8 * n, n))
+    x0 = dev(synth.gen_normal(st, n) / np.float32(16))
+
+    def chain():
+        bufs = [torch.empty(n, device="cuda") for _ in range(8)]
+        cur = x0
+        for i, w in enumerate(ws):
+            q.qmv_q4k(w, cur, bufs[i], n, n)
+            cur = bufs[i]
+        q.qmv_q6k(w6, cur, bufs[6], n, n)
+        ids = (torch.arange(2, device="cuda", dtype=torch.int32) * 3 + 1)   # written by a torch kernel
+        ym = torch.empty(2, n, device="cuda")
+        xm = torch.stack([bufs[6], bufs[5]])
+        q.moe_qmv_q4k(bank, xm, ym, n, n, ids, 2, 8)
+        torch.cuda.synchronize()
+        return [b.clone() for b in bufs[:7]] + [ym.clone()]
+
+    old = q.qmv_set_weight_prefetch(False)
+    try:
+        ref = chain()
+        q.qmv_set_weight_prefetch(True)
+        for _ in range(3):
+            got = chain()
+            for a, b in zip(ref, got):
+                assert torch.equal(a, b)
+    finally:
+        q.qmv_set_weight_prefetch(old)
+    assert torch.isfinite(ref[-1]).all()
