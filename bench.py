@@ -45,9 +45,10 @@ HEADLINE = "q4k_4096x4096"
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 
-# ncu DRAM traffic of one qmv_q4k launch on the headline workload, valid only
-# for the kernel sources whose hash is recorded with it (see profiles/).
-NCU_TRAFFIC = {}
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
+# qmv_q4k launch on the headline workload, valid only for the kernel sources
+# whose hash it is recorded under (profiles/qmv_stream_kernel_full_captures.md).
+NCU_TRAFFIC = {"a7695ea372a27ed3": 9476608}
 
 KERNEL_SOURCES = ["qmv_device.cuh", "qmv_formats.cuh", "qmv_kernel.cuh", "qmv_launch.cuh", "qmv_q4k.cu"]
 

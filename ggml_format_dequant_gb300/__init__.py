@@ -44,7 +44,7 @@ class QmvError(RuntimeError):
 
 class qmv_cfg(ctypes.Structure):
     _fields_ = [("ctas", ctypes.c_int), ("stage_rows", ctypes.c_int), ("stages", ctypes.c_int),
-                ("copy", ctypes.c_int)]
+                ("copy", ctypes.c_int), ("warps", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -124,7 +124,7 @@ def _cfg(cfg):
     if isinstance(cfg, qmv_cfg):
         return ctypes.byref(cfg)
     c = qmv_cfg(int(cfg.get("ctas", 0)), int(cfg.get("stage_rows", 0)), int(cfg.get("stages", 0)),
-                int(cfg.get("copy", 0)))
+                int(cfg.get("copy", 0)), int(cfg.get("warps", 0)))
     return ctypes.byref(c)
 
 

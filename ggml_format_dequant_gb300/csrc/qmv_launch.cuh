@@ -77,10 +77,11 @@ inline int pow2ceil(int v) {
 
 inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a; }
 
-// Target bytes in flight per SM: measured on GB300, bulk copies reach the
-// HBM copy rate once roughly 64-128 KB per SM are outstanding; much more only
-// adds queueing delay before a CTA's first slot lands.
-constexpr long long IN_FLIGHT_BYTES = 96 * 1024;
+// Target bytes in flight per SM. Measured on GB300 (tuning sweeps over the
+// five workloads): two slots per warp, about 40-60 KB per SM, is as fast as or
+// faster than deeper rings; more outstanding copies only delay the moment a
+// CTA's first slot lands.
+constexpr long long IN_FLIGHT_BYTES = 48 * 1024;
 constexpr long long DEFER_MAX_BYTES = 48 * 1024;
 
 // Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense).
@@ -94,7 +95,8 @@ inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp
     const int KS = (U + 31) / 32;
     const int GS = KS == 1 ? pow2ceil(U) : 32;
     const int rpw = 32 / GS;
-    const int nw_max = F::MAX_THREADS / 32;
+    int nw_max = F::MAX_THREADS / 32;
+    if (cfg && cfg->warps > 0) nw_max = std::min(nw_max, cfg->warps);
     if (KS > nw_max) return QMV_ETOOBIG;
     const long long rowbytes = static_cast<long long>(nb) * F::BLOCK_BYTES;
 
@@ -126,10 +128,9 @@ inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp
         R = want >= 4 ? 4 : (want >= 2 ? 2 : 1);
     }
     P.R = R;
-    // Copy engine. At the start of a microsecond-scale kernel a single lane
-    // issuing bulk copies generates requests more slowly than 32 lanes issuing
-    // 16-byte cp.async, so cp.async is the default; bulk TMA stays selectable.
-    P.bulk = cfg && cfg->copy == 1;
+    // Copy engine: bulk TMA from one lane per warp by default; 16-byte
+    // cp.async from all 32 lanes stays selectable (measured equal or slower).
+    P.bulk = !(cfg && cfg->copy == 2);
     const long long slot_bytes = KS == 1 ? static_cast<long long>(R) * rpw * rowbytes
                                          : static_cast<long long>(F::SLICE_BLOCKS) * F::BLOCK_BYTES;
     if (slot_bytes + 32 > 0x7fffffffLL) return QMV_ETOOBIG;
@@ -157,7 +158,7 @@ inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp
     else if (KS > 1)
         off = round_up(off + 4LL * rpc * KS, 128);
     const long long avail = di.smem_optin - 1024 - off;   // 1 KB for static shared memory
-    const long long per_slot = nwarps * (slot_stride + (P.bulk ? 8 : 0));
+    const long long per_slot = nwarps * (slot_stride + 8);
     int S;
     if (cfg && cfg->stages > 0)
         S = cfg->stages;

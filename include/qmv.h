@@ -135,14 +135,16 @@ int qmv_device_status(unsigned int *status, int clear);
 
 /* Forced launch configuration: any field <= 0 keeps the automatic choice.
  * ctas: CTAs per weight matrix; stage_rows: rows per pipeline stage;
- * stages: pipeline depth (slots per warp); copy: 1 = bulk TMA copies,
- * 2 = 16-byte cp.async copies. Used to exercise multi-stage pipelines,
- * ragged tails and both copy engines on small inputs. */
+ * stages: pipeline depth (slots per warp); copy: 1 = bulk TMA copies (the
+ * default), 2 = 16-byte cp.async copies; warps: at most this many warps per CTA. Used to
+ * exercise multi-stage pipelines, ragged tails and both copy engines on small
+ * inputs, and for tuning sweeps. */
 typedef struct qmv_cfg {
     int ctas;
     int stage_rows;
     int stages;
     int copy;
+    int warps;
 } qmv_cfg;
 
 int qmv_q4k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
