@@ -43,8 +43,8 @@ class QmvError(RuntimeError):
 
 
 class qmv_cfg(ctypes.Structure):
-    _fields_ = [("ctas", ctypes.c_int), ("stage_rows", ctypes.c_int), ("stages", ctypes.c_int),
-                ("copy", ctypes.c_int), ("warps", ctypes.c_int)]
+    _fields_ = [("ctas", ctypes.c_int), ("chunk_rows", ctypes.c_int), ("chunks", ctypes.c_int),
+                ("unroll", ctypes.c_int), ("warps", ctypes.c_int), ("cluster", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -67,6 +67,7 @@ _SIG = {
     "qmv_q8_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_device_status": [_P, _I],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
+    "qmv_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
     "qmv_set_weight_prefetch": [_I],
 }
 
@@ -123,8 +124,8 @@ def _cfg(cfg):
         return None
     if isinstance(cfg, qmv_cfg):
         return ctypes.byref(cfg)
-    c = qmv_cfg(int(cfg.get("ctas", 0)), int(cfg.get("stage_rows", 0)), int(cfg.get("stages", 0)),
-                int(cfg.get("copy", 0)), int(cfg.get("warps", 0)))
+    c = qmv_cfg(int(cfg.get("ctas", 0)), int(cfg.get("chunk_rows", 0)), int(cfg.get("chunks", 0)),
+                int(cfg.get("unroll", 0)), int(cfg.get("warps", 0)), int(cfg.get("cluster", 0)))
     return ctypes.byref(c)
 
 
@@ -203,4 +204,23 @@ def qmv_plan_info(fmt, rows, k, slots=1, cfg=None) -> dict:
     out = [ctypes.c_int(0) for _ in range(5)]
     _call("qmv_plan_info", fmt, rows, k, slots, _cfg(cfg), *[ctypes.cast(ctypes.byref(o), ctypes.c_void_p)
                                                            for o in out])
-    return dict(zip(["threads", "ctas", "stage_rows", "stages", "smem_bytes"], [o.value for o in out]))
+    return dict(zip(["threads", "ctas", "chunk_rows", "chunks", "smem_bytes"], [o.value for o in out]))
+
+
+PLAN_DETAIL_FIELDS = ("threads", "ctas", "unroll", "smem", "U", "KS", "GS", "NG", "CR", "S", "rowbytes", "W",
+                      "slot_stride", "aligned8", "rq", "rrem", "gq0", "grem0", "gq1", "grem1", "off_la", "off_lb",
+                      "off_lc", "off_xs", "off_xsum16", "off_red", "off_ring", "off_bars", "off_cnt", "CL")
+
+# A GB300's numbers: 152 SMs, 227 KB opt-in shared memory per CTA, 228 KB per
+# SM, 1 KB reserved per CTA.
+GB300_DEVICE = (152, 232448, 233472, 1024)
+
+
+def qmv_plan_detail(fmt, rows, k, slots=1, cfg=None, device=GB300_DEVICE) -> dict:
+    """The planner's full choice for a described device, computed on the host
+    (no GPU needed). Raises QmvError for shapes the planner rejects."""
+    dev = (ctypes.c_int * 4)(*device)
+    out = (ctypes.c_int * len(PLAN_DETAIL_FIELDS))()
+    _call("qmv_plan_detail", fmt, rows, k, slots, _cfg(cfg), ctypes.cast(dev, ctypes.c_void_p),
+          ctypes.cast(out, ctypes.c_void_p))
+    return dict(zip(PLAN_DETAIL_FIELDS, list(out)))

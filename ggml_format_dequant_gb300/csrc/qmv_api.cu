@@ -150,27 +150,63 @@ int qmv_device_status(unsigned int* status, int clear) {
     return QMV_OK;
 }
 
-int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* threads, int* ctas,
-                  int* stage_rows, int* stages, int* smem_bytes) {
+namespace {
+
+// Plan of format fmt on device `di`.
+int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_cfg* cfg, qmv::KParams* kp,
+            qmv::Plan* pl) {
     static const int qk[5] = {256, 256, 32, 32, 256};
     if (fmt < 0 || fmt > 4 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
     if (fmt == 4 && slots <= 0) return QMV_EINVAL;
+    if (fmt != 4) slots = 1;
+    switch (fmt) {
+    case 0: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, 1, cfg, kp, pl);
+    case 1: return qmv::make_plan_for<qmv::Q6K>(di, rows, k, 1, cfg, kp, pl);
+    case 2: return qmv::make_plan_for<qmv::Q8F>(di, rows, k, 1, cfg, kp, pl);
+    case 3: return qmv::make_plan_for<qmv::Q8D>(di, rows, k, 1, cfg, kp, pl);
+    default: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, slots, cfg, kp, pl);
+    }
+}
+
+}  // namespace
+
+int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* threads, int* ctas,
+                  int* chunk_rows, int* chunks, int* smem_bytes) {
+    qmv::DevInfo di;
+    int rc = qmv::dev_info(&di, nullptr);
+    if (rc) return rc;
     qmv::KParams kp{};
     qmv::Plan pl;
-    int rc;
-    switch (fmt) {
-    case 0: rc = qmv::make_plan<qmv::Q4K>(rows, k, 1, cfg, &kp, &pl); break;
-    case 1: rc = qmv::make_plan<qmv::Q6K>(rows, k, 1, cfg, &kp, &pl); break;
-    case 2: rc = qmv::make_plan<qmv::Q8F>(rows, k, 1, cfg, &kp, &pl); break;
-    case 3: rc = qmv::make_plan<qmv::Q8D>(rows, k, 1, cfg, &kp, &pl); break;
-    default: rc = qmv::make_plan<qmv::Q4K>(rows, k, slots, cfg, &kp, &pl); break;
-    }
+    rc = plan_of(di, fmt, rows, k, slots, cfg, &kp, &pl);
     if (rc) return rc;
     if (threads) *threads = pl.T;
     if (ctas) *ctas = pl.parts * (fmt == 4 ? slots : 1);
-    if (stage_rows) *stage_rows = kp.KS == 1 ? kp.R * (32 / kp.GS) : 1;
-    if (stages) *stages = kp.S;
+    if (chunk_rows) *chunk_rows = kp.CR;
+    if (chunks) *chunks = kp.S;
     if (smem_bytes) *smem_bytes = static_cast<int>(pl.smem);
+    return QMV_OK;
+}
+
+int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, const int* device, int* out) {
+    if (!device || !out) return QMV_EINVAL;
+    qmv::DevInfo di;
+    di.nsm = device[0];
+    di.smem_optin = device[1];
+    di.smem_sm = device[2];
+    di.smem_reserved = device[3];
+    if (di.nsm <= 0 || di.smem_optin <= 0 || di.smem_sm <= 0 || di.smem_reserved < 0) return QMV_EINVAL;
+    qmv::KParams kp{};
+    qmv::Plan pl;
+    const int rc = plan_of(di, fmt, rows, k, slots, cfg, &kp, &pl);
+    if (rc) return rc;
+    const int v[QMV_PLAN_DETAIL_FIELDS] = {
+        pl.T, pl.parts, pl.R, static_cast<int>(pl.smem), kp.U, kp.KS, kp.GS, kp.NG, kp.CR, kp.S,
+        static_cast<int>(kp.rowbytes), kp.W, static_cast<int>(kp.slot_stride), kp.aligned8, kp.rq, kp.rrem,
+        kp.gq[0], kp.grem[0], kp.gq[1], kp.grem[1], static_cast<int>(kp.lt.la), static_cast<int>(kp.lt.lb),
+        static_cast<int>(kp.lt.lc), static_cast<int>(kp.lt.xs), static_cast<int>(kp.lt.xsum16),
+        static_cast<int>(kp.off_red), static_cast<int>(kp.off_ring), static_cast<int>(kp.off_bars),
+        static_cast<int>(kp.off_cnt), pl.CL};
+    for (int i = 0; i < QMV_PLAN_DETAIL_FIELDS; i++) out[i] = v[i];
     return QMV_OK;
 }
 

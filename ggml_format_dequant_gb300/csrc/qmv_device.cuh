@@ -1,6 +1,6 @@
 // qmv_device.cuh -- device-side building blocks shared by the quantized matvec
-// kernels: bulk-copy (TMA) staging with bounded mbarrier waits, the integer
-// "limb" form of the f32 activation, and deterministic group reductions.
+// kernels: bulk-copy (TMA) staging with bounded mbarrier waits, shared-memory
+// loads by 32-bit address, and the integer "limb" form of the f32 activation.
 //
 // Target: sm_103a only (GB300). Nothing here is used by the CPU oracle.
 #pragma once
@@ -40,6 +40,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
 // Make freshly initialized barriers visible to the bulk-copy (async) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Order earlier generic-proxy shared-memory accesses (as seen by this thread)
+// before its later bulk copies into the same memory.
+__device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
@@ -94,25 +100,89 @@ __device__ __forceinline__ void tma_bulk_g2s(uint32_t dst, const void* src, uint
                  : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared through L2 only (LDGSTS); both
-// addresses 16-byte aligned. Completion is tracked with commit/wait groups.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// ------------------------------------------------------- thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most n of this thread's most recent groups are still pending.
-__device__ __forceinline__ void cp_async_wait(int n) {
-    switch (n) {
-    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
-    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
-    }
+
+// The address, in the cluster's shared window, of shared address `a` of CTA
+// `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
 }
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t a, const uint4& v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t a, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+// Every thread of every CTA of the cluster: writes before it (to any CTA's
+// shared memory) are visible to all after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// ------------------------------------------- shared loads by 32-bit address
+//
+// The staged weights are read with explicit ld.shared on 32-bit addresses (the
+// immediate offsets fold into the instruction). They are volatile so that they
+// stay after the mbarrier wait that publishes the data.
+
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+    return v;
+}
+
+template <int OFF>
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));
+    return v;
+}
+
+template <int OFF>
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a), "n"(OFF));
+    return v;
+}
+
+// 16 bytes of a run that starts `sh` bits (0 or 16) past the 4-byte-aligned
+// address wa + OFF: five aligned loads and four funnel shifts. Reads up to 4
+// bytes past the run.
+template <int OFF>
+__device__ __forceinline__ uint4 lds16_sh(uint32_t wa, uint32_t sh) {
+    const uint32_t w0 = lds32<OFF>(wa), w1 = lds32<OFF + 4>(wa), w2 = lds32<OFF + 8>(wa),
+                   w3 = lds32<OFF + 12>(wa), w4 = lds32<OFF + 16>(wa);
+    uint4 r;
+    r.x = __funnelshift_r(w0, w1, sh);
+    r.y = __funnelshift_r(w1, w2, sh);
+    r.z = __funnelshift_r(w2, w3, sh);
+    r.w = __funnelshift_r(w3, w4, sh);
+    return r;
+}
+
+// 8 bytes, same convention (reads up to 4 bytes past the run).
+template <int OFF>
+__device__ __forceinline__ uint2 lds8_sh(uint32_t wa, uint32_t sh) {
+    const uint32_t w0 = lds32<OFF>(wa), w1 = lds32<OFF + 4>(wa), w2 = lds32<OFF + 8>(wa);
+    return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
+}
+
+// ---------------------------------------------------------------- integers
 
 // d = c + sum of the four (unsigned byte of a) * (signed byte of b) products.
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -135,35 +205,13 @@ __device__ __forceinline__ float f16_hi(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 
-// 16 bytes starting at a shared-memory address that is only 2-byte aligned:
-// five aligned 32-bit loads and a funnel shift by 0 or 16 bits. The caller
-// guarantees 4 readable bytes past the run.
-__device__ __forceinline__ uint4 lds16_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
-    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
-    uint4 r;
-    r.x = __funnelshift_r(w0, w1, sh);
-    r.y = __funnelshift_r(w1, w2, sh);
-    r.z = __funnelshift_r(w2, w3, sh);
-    r.w = __funnelshift_r(w3, w4, sh);
-    return r;
-}
-
-// 8 bytes at a 2-byte aligned shared address (three aligned loads).
-__device__ __forceinline__ uint2 lds8_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
-    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
-    return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
-}
-
-// The 16-bit little-endian value at a 2-byte aligned shared address.
-__device__ __forceinline__ uint32_t lds_u16_a2(const uint8_t* p) {
-    return *reinterpret_cast<const unsigned short*>(p);
-}
+// Small integers reach f32 through the exponent field: for 0 <= v < 2^22 the
+// bit pattern 0x4B000000 + v is the float 2^23 + v, so s*v = fma(s, that,
+// -s*2^23) is the correctly rounded product in one instruction once -s*2^23 is
+// known. The pattern 0x4B400000 (the float 1.5*2^23) plus a sign-extended v in
+// [-2^22, 2^22) is 1.5*2^23 + v, used the same way with -s*1.5*2^23.
+constexpr float TWO23 = 8388608.0f;
+constexpr float THREE22 = 12582912.0f;   // 1.5 * 2^23
 
 // --------------------------------------------------------- activation limbs
 //
@@ -181,79 +229,120 @@ __device__ __forceinline__ uint32_t lds_u16_a2(const uint8_t* p) {
 // rounding of x*2^s, and the low 23 bits of t are M = X + 0x208080 whose three
 // bytes are c + 128, b + 128 and a + 32.
 constexpr int LIMB_BITS = 21;
-constexpr float LIMB_MAGIC = 10518656.0f;   // 2^23 + 0x208080
+constexpr float LIMB_MAGIC = 10518656.0f;          // 2^23 + 0x208080
+constexpr uint32_t LIMB_MAGIC_BITS = 0x4B208080u;  // its bit pattern
 
-struct XPrepSmem {
-    uint8_t* la;       // [k] limb a (signed byte)
-    uint8_t* lb;       // [k] limb b
-    uint8_t* lc;       // [k] limb c
-    float* xs;         // [k/32] 2^-s of each 32-group
-    float* xsum16;     // [k/16] (sum of X over 16 elements) * 2^-s
+// Shared-memory limb tables of x[0, k), as byte offsets into dynamic shared
+// memory: limb bytes la, lb, lc [k rounded up to 128]; the 2^-s of every
+// 32-group (xs, [k/32] floats); and (sum of X over every 16 elements) * 2^-s
+// (xsum16, [k/16]).
+struct LimbTables {
+    uint32_t la, lb, lc, xs, xsum16;
 };
 
+// The limb bytes of elements 16c .. 16c+15 (16-byte chunk c) are stored in
+// chunk limb_chunk(c): bits 3..5 of c are XORed into bits 0..2, which permutes
+// chunks within each aligned group of 8. Lanes that read chunks 4u + v or
+// 2u + v (one unit of 64 or 32 activations each) then hit distinct banks.
+__host__ __device__ __forceinline__ uint32_t limb_chunk(uint32_t c) { return c ^ ((c >> 3) & 7u); }
+
+// Limb words of four consecutive elements from their fma bit patterns (see
+// above): the words of limbs a, b and c, one signed byte per element.
+__device__ __forceinline__ void limb_words(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, uint32_t& aw,
+                                           uint32_t& bw, uint32_t& cw) {
+    // byte transpose: (c0 c1 b0 b1), (c2 c3 b2 b3), (a0 a1 . .), (a2 a3 . .)
+    const uint32_t s01 = __byte_perm(t0, t1, 0x5140);
+    const uint32_t s23 = __byte_perm(t2, t3, 0x5140);
+    const uint32_t a01 = __byte_perm(t0, t1, 0x0062);
+    const uint32_t a23 = __byte_perm(t2, t3, 0x0062);
+    cw = __byte_perm(s01, s23, 0x5410) ^ 0x80808080u;
+    bw = __byte_perm(s01, s23, 0x7632) ^ 0x80808080u;
+    // bytes a + 32 lie in [0, 64], so (byte + 96) ^ 0x80 is a as a signed byte
+    // and the word add never carries between bytes
+    aw = (__byte_perm(a01, a23, 0x5410) + 0x60606060u) ^ 0x80808080u;
+}
+
 // Fill the limb tables for x[0, k) (k a multiple of 32) with all T threads of
-// the block. Each thread owns float4 slots i = tid, tid + T, ...; a 32-element
-// group is 8 consecutive float4 slots, i.e. 8 consecutive lanes of one warp
-// (T is a multiple of 32). Loads are issued BATCH at a time before any use so
-// the prologue costs one or two memory round trips, not one per group.
+// the block (T even), shared among the CL CTAs of a cluster: CTA `rank`
+// converts halves [rank * nh / CL, (rank + 1) * nh / CL) of the nh = k/16
+// 16-element halves and writes them into the tables of every CTA of the
+// cluster (CL == 1: its own tables only). The caller makes them visible with a
+// cluster (or block) barrier. A 32-element group is converted by two
+// neighbouring threads, 16 elements (one 16-byte chunk of each limb table)
+// each: thread slot h covers elements 16h .. 16h+15 and its partner (lane ^ 1)
+// the other half of the group. All of a thread's loads are issued before any
+// use, BATCH halves at a time. nh / CL must be even.
 template <int BATCH>
-__device__ __forceinline__ void prep_limbs(const float* __restrict__ x, int k, const XPrepSmem& P, int tid,
-                                           int T) {
-    const int nvec = k >> 2;
-    const float4* __restrict__ x4 = reinterpret_cast<const float4*>(x);
-    for (int base = 0; base < nvec; base += BATCH * T) {
-        float4 v[BATCH];
+__device__ __forceinline__ void prep_limbs(const float* __restrict__ x, int k, uint8_t* smem, const LimbTables& L,
+                                           int tid, int T, int CL, uint32_t rank) {
+    const int nhc = (k >> 4) / CL;            // halves converted by this CTA
+    const int h0 = static_cast<int>(rank) * nhc;
+    const uint32_t sbase = smem_u32(smem);
+    const float4* __restrict__ x4 = reinterpret_cast<const float4*>(x) + 4 * h0;
+    for (int base = 0; base < nhc; base += BATCH * T) {
+        float4 v[BATCH][4];
 #pragma unroll
         for (int b = 0; b < BATCH; b++) {
-            const int i = base + b * T + tid;
-            v[b] = (i < nvec) ? __ldg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int hl = base + b * T + tid;
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+                v[b][m] = (hl < nhc) ? __ldg(x4 + 4 * hl + m) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int b = 0; b < BATCH; b++) {
-            if (base + b * T >= nvec) break;   // uniform: nvec is a multiple of 8 and T of 32
-            const int i = base + b * T + tid;
-            const uint32_t m4 = max(max(__float_as_uint(v[b].x) & 0x7fffffffu, __float_as_uint(v[b].y) & 0x7fffffffu),
-                                    max(__float_as_uint(v[b].z) & 0x7fffffffu, __float_as_uint(v[b].w) & 0x7fffffffu));
-            uint32_t mx = max(m4, __shfl_xor_sync(FULL, m4, 4));
-            mx = max(mx, __shfl_xor_sync(FULL, mx, 2));
-            mx = max(mx, __shfl_xor_sync(FULL, mx, 1));
-            const int E = static_cast<int>(mx >> 23);   // biased exponent of the group maximum
-            int s = LIMB_BITS - (E - 126);               // max < 2^(E-126) for a normal maximum
-            s = s > 126 ? 126 : s;                       // zero / tiny groups
+            if (base + b * T >= nhc) break;   // uniform: nhc and T are even, so partners stay together
+            const int hl = base + b * T + tid;
+            uint32_t mx = 0;
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+                mx = max(mx, max(max(__float_as_uint(v[b][m].x) & 0x7fffffffu, __float_as_uint(v[b][m].y) & 0x7fffffffu),
+                                 max(__float_as_uint(v[b][m].z) & 0x7fffffffu, __float_as_uint(v[b][m].w) & 0x7fffffffu)));
+            mx = max(mx, __shfl_xor_sync(FULL, mx, 1));   // the group's other half
+            const int E = static_cast<int>(mx >> 23);     // biased exponent of the group maximum
+            int s = LIMB_BITS - (E - 126);                 // max < 2^(E-126) for a normal maximum
+            s = s > 126 ? 126 : s;                         // zero / tiny groups
             const float p2s = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
             const float p2ms = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-            const uint32_t M0 = __float_as_uint(__fmaf_rn(v[b].x, p2s, LIMB_MAGIC)) & 0x7fffffu;
-            const uint32_t M1 = __float_as_uint(__fmaf_rn(v[b].y, p2s, LIMB_MAGIC)) & 0x7fffffu;
-            const uint32_t M2 = __float_as_uint(__fmaf_rn(v[b].z, p2s, LIMB_MAGIC)) & 0x7fffffu;
-            const uint32_t M3 = __float_as_uint(__fmaf_rn(v[b].w, p2s, LIMB_MAGIC)) & 0x7fffffu;
-            // byte 0 of M is c + 128, byte 1 is b + 128, byte 2 is a + 32
-            const uint32_t cw = __byte_perm(__byte_perm(M0, M1, 0x0040), __byte_perm(M2, M3, 0x0040), 0x5410) ^ 0x80808080u;
-            const uint32_t bw = __byte_perm(__byte_perm(M0, M1, 0x0051), __byte_perm(M2, M3, 0x0051), 0x5410) ^ 0x80808080u;
-            const uint32_t a0 = static_cast<uint32_t>(static_cast<int>(M0 >> 16) - 32);
-            const uint32_t a1 = static_cast<uint32_t>(static_cast<int>(M1 >> 16) - 32);
-            const uint32_t a2 = static_cast<uint32_t>(static_cast<int>(M2 >> 16) - 32);
-            const uint32_t a3 = static_cast<uint32_t>(static_cast<int>(M3 >> 16) - 32);
-            const uint32_t aw = __byte_perm(__byte_perm(a0, a1, 0x0040), __byte_perm(a2, a3, 0x0040), 0x5410);
-            int X = static_cast<int>(M0 + M1 + M2 + M3) - 4 * 0x208080;
-            X += __shfl_xor_sync(FULL, X, 2);
-            X += __shfl_xor_sync(FULL, X, 1);
-            // A whole 8-lane group is either inside [0, nvec) or past it
-            // (nvec is a multiple of 8), so the shuffles above stay in step.
-            if (i < nvec) {
-                reinterpret_cast<uint32_t*>(P.la)[i] = aw;
-                reinterpret_cast<uint32_t*>(P.lb)[i] = bw;
-                reinterpret_cast<uint32_t*>(P.lc)[i] = cw;
-                if ((tid & 3) == 0) P.xsum16[i >> 2] = __int2float_rn(X) * p2ms;
-                if ((tid & 7) == 0) P.xs[i >> 3] = p2ms;
+            uint4 A, B, C;
+            uint32_t tsum = 0;
+            uint32_t* Ap = &A.x;
+            uint32_t* Bp = &B.x;
+            uint32_t* Cp = &C.x;
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                // bit patterns 0x4B000000 | M; M's bytes are c + 128, b + 128, a + 32
+                const uint32_t t0 = __float_as_uint(__fmaf_rn(v[b][m].x, p2s, LIMB_MAGIC));
+                const uint32_t t1 = __float_as_uint(__fmaf_rn(v[b][m].y, p2s, LIMB_MAGIC));
+                const uint32_t t2 = __float_as_uint(__fmaf_rn(v[b][m].z, p2s, LIMB_MAGIC));
+                const uint32_t t3 = __float_as_uint(__fmaf_rn(v[b][m].w, p2s, LIMB_MAGIC));
+                limb_words(t0, t1, t2, t3, Ap[m], Bp[m], Cp[m]);
+                tsum += t0 + t1 + t2 + t3;
+            }
+            // sum of the 16 X: sum of the patterns minus 16 magic patterns (mod 2^32)
+            const int X = static_cast<int>(tsum - 16u * LIMB_MAGIC_BITS);
+            const float xsum = __int2float_rn(X) * p2ms;
+            if (hl < nhc) {   // always true here; keeps the stores visibly in bounds
+                const uint32_t h = static_cast<uint32_t>(h0 + hl);
+                const uint32_t o = limb_chunk(h) << 4;
+                if (CL == 1) {
+                    *reinterpret_cast<uint4*>(smem + L.la + o) = A;
+                    *reinterpret_cast<uint4*>(smem + L.lb + o) = B;
+                    *reinterpret_cast<uint4*>(smem + L.lc + o) = C;
+                    reinterpret_cast<float*>(smem + L.xsum16)[h] = xsum;
+                    if ((h & 1u) == 0) reinterpret_cast<float*>(smem + L.xs)[h >> 1] = p2ms;
+                } else {
+                    for (int r = 0; r < CL; r++) {
+                        const uint32_t rr = static_cast<uint32_t>(r);
+                        st_cluster_v4(cluster_addr(sbase + L.la + o, rr), A);
+                        st_cluster_v4(cluster_addr(sbase + L.lb + o, rr), B);
+                        st_cluster_v4(cluster_addr(sbase + L.lc + o, rr), C);
+                        st_cluster_f32(cluster_addr(sbase + L.xsum16 + 4u * h, rr), xsum);
+                        if ((h & 1u) == 0) st_cluster_f32(cluster_addr(sbase + L.xs + 4u * (h >> 1), rr), p2ms);
+                    }
+                }
             }
         }
     }
-}
-
-// Combine the three limb partial sums into the exact integer sum q*X. The
-// callers bound |sum q*X| below 2^31, so the wrapped 32-bit arithmetic is exact.
-__device__ __forceinline__ int limb_combine(int sa, int sb, int sc) {
-    return sa * 65536 + sb * 256 + sc;
 }
 
 }  // namespace qmv

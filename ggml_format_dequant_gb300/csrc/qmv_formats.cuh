@@ -1,25 +1,36 @@
 // qmv_formats.cuh -- in-register decode of one "unit" of a packed GGML block
 // against the activation, for Q4_K, Q6_K and Q8_0.
 //
-// A unit is the slice of a block one lane owns for every row it processes:
+// A unit is the part of a row one lane owns for every row it processes:
 //   Q4_K: one 64-weight chunk of a 256-weight super-block (4 per block)
-//   Q6_K: one (half, 16-position) slice, 64 weights (4 per block)
-//   Q8_0: one 32-weight block
+//   Q6_K: one (half, 16-position) slice of a block, 64 weights (4 per block)
+//   Q8_0, f32 x: one 32-weight block;  Q8_0, q8 x (dp4a): four blocks
 // The lane keeps the activation for its unit in registers (as integer limbs or
-// int8 codes) and, per row, reads the unit's packed bytes from the shared-memory
-// stage, unpacks the codes into byte lanes and forms integer dot products with
-// dp4a, then applies the block's scales once per scale group.
+// int8 codes) and, per row, reads the unit's packed bytes from the staged
+// rows in shared memory (by 32-bit address), unpacks the codes into byte lanes
+// and forms integer dot products with dp4a, then applies the block's scales
+// once per scale group.
 //
 // Block layouts (hanzo-ml src/vulkan_backend.rs): Q4_K = d, dmin (f16), 12 bytes
 // of packed 6-bit scales/mins, 128 bytes of 4-bit codes (quantize_q4k,
 // quantize_q4k_split); Q6_K = ql[128], qh[64], int8 scales[16], d (f16)
 // (quantize_q6k); Q8_0 = d (f16) + 32 int8 (quantize_q8_blocks). The bit
 // mapping inside the blocks is GGML's k-quant layout.
+//
+// Every format states SLICE_BLOCKS (blocks of a row covered by one warp's 32
+// units) and SLACK (bytes its loads may read past the end of a row).
 #pragma once
 
 #include "qmv_device.cuh"
 
 namespace qmv {
+
+// Signed byte `sel` (selector with sign replication) of w, as an int.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
 
 // ====================================================================== Q4_K
 //
@@ -29,15 +40,16 @@ namespace qmv {
 // d*sc_j*q_i - dmin*m_j, so the chunk contributes
 //     d*sc_2c * sum(q*x) - dmin*m_2c * sum(x)  +  (same for 2c+1).
 struct Q4K {
-    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 256;
     static constexpr int BLOCK_BYTES = 144;
-    static constexpr int SLICE_BLOCKS = 8;    // 32 units = one warp's k-slice (1152 bytes)
+    static constexpr int SLICE_BLOCKS = 8;    // 32 units (1152 bytes)
+    static constexpr int SLACK = 0;
     static constexpr bool LIMBS = true;
+    static constexpr int DEFAULT_UNROLL = 2;
 
     __host__ __device__ static int units(int nb) { return 4 * nb; }
-    // Unit u of a slice: byte offset of its block, index of its first weight.
-    __device__ __forceinline__ static int unit_byte(int u) { return (u >> 2) * BLOCK_BYTES; }
+    // Unit u of a slice: byte offset of its block in the slice, first weight.
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u >> 2) * BLOCK_BYTES; }
     __device__ __forceinline__ static int unit_elem(int u) { return (u >> 2) * QK + 64 * (u & 3); }
 
     struct X {
@@ -45,54 +57,53 @@ struct Q4K {
         float xs0, xs1;                 // 2^-s of the two 32-groups
         float xsum0, xsum1;             // activation sums of the two sub-blocks
     };
-    // Lane-constant selectors for the scale/min bit fields of chunk c.
     struct L {
-        int c, sh, shm;
-        uint32_t mlo, mhi;
-        bool hic;
+        uint32_t qoff;   // byte offset of the chunk's codes in the block: 16 + 32c
+        uint32_t sel;    // prmt selector giving 0x4B0000vv for scale byte 2(c & 1)
+        bool hic;        // c >= 2: scales and mins of sub-blocks 4..7
     };
 
     __device__ __forceinline__ static L lane_consts(int u, int /*nb*/, int /*ug*/) {
         const int c = u & 3;
         L l;
-        l.c = c;
+        l.qoff = 16u + 32u * static_cast<uint32_t>(c);
+        l.sel = 0x7440u | static_cast<uint32_t>(2 * (c & 1));
         l.hic = c >= 2;
-        l.sh = 16 * (c & 1);
-        l.shm = l.hic ? l.sh + 4 : l.sh;
-        l.mlo = l.hic ? 15u : 63u;
-        l.mhi = l.hic ? 0x30u : 0u;
         return l;
     }
 
     // e0 = index of the chunk's first weight in the row.
-    __device__ __forceinline__ static void load_x(X& x, const XPrepSmem& P, int e0) {
-        const uint4* A = reinterpret_cast<const uint4*>(P.la + e0);
-        const uint4* B = reinterpret_cast<const uint4*>(P.lb + e0);
-        const uint4* C = reinterpret_cast<const uint4*>(P.lc + e0);
+    __device__ __forceinline__ static void load_x(X& x, const uint8_t* smem, const LimbTables& T, int e0) {
 #pragma unroll
         for (int v = 0; v < 4; v++) {
-            const uint4 a = A[v], b = B[v], c = C[v];
+            const uint32_t o = limb_chunk(static_cast<uint32_t>(e0 >> 4) + v) << 4;
+            const uint4 a = *reinterpret_cast<const uint4*>(smem + T.la + o);
+            const uint4 b = *reinterpret_cast<const uint4*>(smem + T.lb + o);
+            const uint4 c = *reinterpret_cast<const uint4*>(smem + T.lc + o);
             x.a[4 * v] = a.x; x.a[4 * v + 1] = a.y; x.a[4 * v + 2] = a.z; x.a[4 * v + 3] = a.w;
             x.b[4 * v] = b.x; x.b[4 * v + 1] = b.y; x.b[4 * v + 2] = b.z; x.b[4 * v + 3] = b.w;
             x.c[4 * v] = c.x; x.c[4 * v + 1] = c.y; x.c[4 * v + 2] = c.z; x.c[4 * v + 3] = c.w;
         }
-        x.xs0 = P.xs[e0 >> 5];
-        x.xs1 = P.xs[(e0 >> 5) + 1];
-        x.xsum0 = P.xsum16[e0 >> 4] + P.xsum16[(e0 >> 4) + 1];
-        x.xsum1 = P.xsum16[(e0 >> 4) + 2] + P.xsum16[(e0 >> 4) + 3];
+        const float* xs = reinterpret_cast<const float*>(smem + T.xs);
+        const float* xsum16 = reinterpret_cast<const float*>(smem + T.xsum16);
+        x.xs0 = xs[e0 >> 5];
+        x.xs1 = xs[(e0 >> 5) + 1];
+        x.xsum0 = xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1];
+        x.xsum1 = xsum16[(e0 >> 4) + 2] + xsum16[(e0 >> 4) + 3];
     }
 
-    // blk: the super-block in shared memory (16-byte aligned).
-    __device__ __forceinline__ static float dot(const uint8_t* blk, const L& l, const X& x, float r) {
-        const uint4 h = *reinterpret_cast<const uint4*>(blk);
-        const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * l.c);
-        const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * l.c);
+    // a: shared address of the super-block (16-byte aligned).
+    __device__ __forceinline__ static float dot(uint32_t a, const L& l, const X& x, float r) {
+        const uint4 h = lds128<0>(a);
+        const uint32_t aq = a + l.qoff;
+        const uint4 qa = lds128<0>(aq);
+        const uint4 qb = lds128<16>(aq);
         const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
         int a0 = 0, b0 = 0, c0 = 0, a1 = 0, b1 = 0, c1 = 0;
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             const uint32_t lo = q[i] & 0x0f0f0f0fu;
-            const uint32_t hi = (q[i] >> 4) & 0x0f0f0f0fu;
+            const uint32_t hi = q[i] & 0xf0f0f0f0u;   // 16 * the high nibbles
             a0 = dp4a_us(lo, x.a[i], a0);
             b0 = dp4a_us(lo, x.b[i], b0);
             c0 = dp4a_us(lo, x.c[i], c0);
@@ -100,22 +111,30 @@ struct Q4K {
             b1 = dp4a_us(hi, x.b[8 + i], b1);
             c1 = dp4a_us(hi, x.c[8 + i], c1);
         }
-        // |sum q*X| <= 32 * 15 * 2^21 < 2^31 per sub-block.
-        const int s0 = limb_combine(a0, b0, c0);
-        const int s1 = limb_combine(a1, b1, c1);
-        const uint32_t srcS = l.hic ? h.w : h.y;
-        const uint32_t srcM = l.hic ? h.w : h.z;
-        const int sc0 = static_cast<int>(((srcS >> l.sh) & l.mlo) | ((h.y >> (l.sh + 2)) & l.mhi));
-        const int m0 = static_cast<int>(((srcM >> l.shm) & l.mlo) | ((h.z >> (l.sh + 2)) & l.mhi));
-        const int sc1 = static_cast<int>(((srcS >> (l.sh + 8)) & l.mlo) | ((h.y >> (l.sh + 10)) & l.mhi));
-        const int m1 = static_cast<int>(((srcM >> (l.shm + 8)) & l.mlo) | ((h.z >> (l.sh + 10)) & l.mhi));
+        // Exact sums q*X, |.| <= 32 * 15 * 2^21 < 2^31 per sub-block. The high
+        // nibbles' limb sums carry a factor 16 (a multiple of 16 each, so the
+        // shift of c1 is exact).
+        const int s0 = a0 * 65536 + b0 * 256 + c0;
+        const int s1 = a1 * 4096 + b1 * 16 + (c1 >> 4);
+        // The 6-bit scales and mins of sub-blocks 0..3 and 4..7 as byte lanes.
+        const uint32_t sc_lo = h.y & 0x3f3f3f3fu;
+        const uint32_t m_lo = h.z & 0x3f3f3f3fu;
+        const uint32_t sc_hi = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
+        const uint32_t m_hi = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+        const uint32_t SC = l.hic ? sc_hi : sc_lo;
+        const uint32_t M = l.hic ? m_hi : m_lo;
         const float d = f16_lo(h.x), dmin = f16_hi(h.x);
+        const float nd = -d * TWO23, ndm = -dmin * TWO23;
+        const float dsc0 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel)), nd);
+        const float dsc1 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel + 1)), nd);
+        const float dm0 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel)), ndm);
+        const float dm1 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel + 1)), ndm);
         const float t0 = __int2float_rn(s0) * x.xs0;
         const float t1 = __int2float_rn(s1) * x.xs1;
-        r = __fmaf_rn(d * __int2float_rn(sc0), t0, r);
-        r = __fmaf_rn(-(dmin * __int2float_rn(m0)), x.xsum0, r);
-        r = __fmaf_rn(d * __int2float_rn(sc1), t1, r);
-        r = __fmaf_rn(-(dmin * __int2float_rn(m1)), x.xsum1, r);
+        r = __fmaf_rn(dsc0, t0, r);
+        r = __fmaf_rn(-dm0, x.xsum0, r);
+        r = __fmaf_rn(dsc1, t1, r);
+        r = __fmaf_rn(-dm1, x.xsum1, r);
         return r;
     }
 };
@@ -129,14 +148,15 @@ struct Q4K {
 // qh[32H + l], and all 16 share scale 8H + 2qd + hh. w = d*scale*(q - 32), so
 // each quarter contributes d*scale*(sum(q*x) - 32*sum(x)).
 struct Q6K {
-    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 256;
     static constexpr int BLOCK_BYTES = 210;
-    static constexpr int SLICE_BLOCKS = 8;    // 32 units = one warp's k-slice (1680 bytes)
+    static constexpr int SLICE_BLOCKS = 8;    // 32 units (1680 bytes)
+    static constexpr int SLACK = 16;
     static constexpr bool LIMBS = true;
+    static constexpr int DEFAULT_UNROLL = 2;
 
     __host__ __device__ static int units(int nb) { return 4 * nb; }
-    __device__ __forceinline__ static int unit_byte(int u) { return (u >> 2) * BLOCK_BYTES; }
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u >> 2) * BLOCK_BYTES; }
     __device__ __forceinline__ static int unit_elem(int u) {
         return (u >> 2) * QK + 128 * ((u & 3) >> 1) + 16 * (u & 1);
     }
@@ -146,39 +166,51 @@ struct Q6K {
         float xs[4], xsum[4];
     };
     struct L {
-        int H, hh;
+        uint32_t ql_off, qh_off, sc_off;   // byte offsets in the block
+        uint32_t sel0, sel1;               // sign-extending selectors of scale bytes hh, 2 + hh
     };
 
     __device__ __forceinline__ static L lane_consts(int u, int /*nb*/, int /*ug*/) {
+        const uint32_t H = static_cast<uint32_t>((u & 3) >> 1), hh = static_cast<uint32_t>(u & 1);
         L l;
-        l.H = (u & 3) >> 1;
-        l.hh = u & 1;
+        l.ql_off = 64u * H + 16u * hh;
+        l.qh_off = 128u + 32u * H + 16u * hh;
+        l.sc_off = 192u + 8u * H;
+        const uint32_t b0 = hh, b1 = 2u + hh;
+        l.sel0 = b0 | ((8u | b0) * 0x1110u);
+        l.sel1 = b1 | ((8u | b1) * 0x1110u);
         return l;
     }
 
     // e0 = index (in the row) of weight 128H + 16hh of the unit's block.
-    __device__ __forceinline__ static void load_x(X& x, const XPrepSmem& P, int e0) {
+    __device__ __forceinline__ static void load_x(X& x, const uint8_t* smem, const LimbTables& T, int e0) {
+        const float* xs = reinterpret_cast<const float*>(smem + T.xs);
+        const float* xsum16 = reinterpret_cast<const float*>(smem + T.xsum16);
 #pragma unroll
         for (int qd = 0; qd < 4; qd++) {
             const int e = e0 + 32 * qd;
-            const uint4 a = *reinterpret_cast<const uint4*>(P.la + e);
-            const uint4 b = *reinterpret_cast<const uint4*>(P.lb + e);
-            const uint4 c = *reinterpret_cast<const uint4*>(P.lc + e);
+            const uint32_t o = limb_chunk(static_cast<uint32_t>(e >> 4)) << 4;
+            const uint4 a = *reinterpret_cast<const uint4*>(smem + T.la + o);
+            const uint4 b = *reinterpret_cast<const uint4*>(smem + T.lb + o);
+            const uint4 c = *reinterpret_cast<const uint4*>(smem + T.lc + o);
             x.a[4 * qd] = a.x; x.a[4 * qd + 1] = a.y; x.a[4 * qd + 2] = a.z; x.a[4 * qd + 3] = a.w;
             x.b[4 * qd] = b.x; x.b[4 * qd + 1] = b.y; x.b[4 * qd + 2] = b.z; x.b[4 * qd + 3] = b.w;
             x.c[4 * qd] = c.x; x.c[4 * qd + 1] = c.y; x.c[4 * qd + 2] = c.z; x.c[4 * qd + 3] = c.w;
-            x.xs[qd] = P.xs[e >> 5];
-            x.xsum[qd] = P.xsum16[e >> 4];
+            x.xs[qd] = xs[e >> 5];
+            x.xsum[qd] = xsum16[e >> 4];
         }
     }
 
-    // blk: the block in shared memory (2-byte aligned).
-    __device__ __forceinline__ static float dot(const uint8_t* blk, const L& l, const X& x, float r) {
-        const uint4 qla = lds16_a2(blk + 64 * l.H + 16 * l.hh);
-        const uint4 qlb = lds16_a2(blk + 64 * l.H + 32 + 16 * l.hh);
-        const uint4 qhv = lds16_a2(blk + 128 + 32 * l.H + 16 * l.hh);
-        const uint2 scw = lds8_a2(blk + 192 + 8 * l.H);
-        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16_a2(blk + 208))));
+    // a: shared address of the block (2-byte aligned).
+    __device__ __forceinline__ static float dot(uint32_t a, const L& l, const X& x, float r) {
+        const uint32_t wa = a & ~3u;
+        const uint32_t sh = (a & 3u) * 8u;   // every field offset is a multiple of 4
+        const uint32_t w1 = wa + l.ql_off;
+        const uint4 qla = lds16_sh<0>(w1, sh);
+        const uint4 qlb = lds16_sh<32>(w1, sh);
+        const uint4 qhv = lds16_sh<0>(wa + l.qh_off, sh);
+        const uint2 scw = lds8_sh<0>(wa + l.sc_off, sh);
+        const float d = f16_lo(lds32<208>(wa) >> sh);
         const uint32_t A[4] = {qla.x, qla.y, qla.z, qla.w};
         const uint32_t B[4] = {qlb.x, qlb.y, qlb.z, qlb.w};
         const uint32_t Hq[4] = {qhv.x, qhv.y, qhv.z, qhv.w};
@@ -186,15 +218,15 @@ struct Q6K {
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const uint32_t w0 = (A[i] & 0x0f0f0f0fu) | ((Hq[i] << 4) & 0x30303030u);
-            const uint32_t w1 = (B[i] & 0x0f0f0f0fu) | ((Hq[i] << 2) & 0x30303030u);
+            const uint32_t w1q = (B[i] & 0x0f0f0f0fu) | ((Hq[i] << 2) & 0x30303030u);
             const uint32_t w2 = ((A[i] >> 4) & 0x0f0f0f0fu) | (Hq[i] & 0x30303030u);
             const uint32_t w3 = ((B[i] >> 4) & 0x0f0f0f0fu) | ((Hq[i] >> 2) & 0x30303030u);
             sa[0] = dp4a_us(w0, x.a[i], sa[0]);
             sb[0] = dp4a_us(w0, x.b[i], sb[0]);
             sc[0] = dp4a_us(w0, x.c[i], sc[0]);
-            sa[1] = dp4a_us(w1, x.a[4 + i], sa[1]);
-            sb[1] = dp4a_us(w1, x.b[4 + i], sb[1]);
-            sc[1] = dp4a_us(w1, x.c[4 + i], sc[1]);
+            sa[1] = dp4a_us(w1q, x.a[4 + i], sa[1]);
+            sb[1] = dp4a_us(w1q, x.b[4 + i], sb[1]);
+            sc[1] = dp4a_us(w1q, x.c[4 + i], sc[1]);
             sa[2] = dp4a_us(w2, x.a[8 + i], sa[2]);
             sb[2] = dp4a_us(w2, x.b[8 + i], sb[2]);
             sc[2] = dp4a_us(w2, x.c[8 + i], sc[2]);
@@ -202,15 +234,17 @@ struct Q6K {
             sb[3] = dp4a_us(w3, x.b[12 + i], sb[3]);
             sc[3] = dp4a_us(w3, x.c[12 + i], sc[3]);
         }
+        const float nd = -d * THREE22;
 #pragma unroll
         for (int qd = 0; qd < 4; qd++) {
             // |sum q*X| <= 16 * 63 * 2^21 < 2^31 per quarter.
-            const int s = limb_combine(sa[qd], sb[qd], sc[qd]);
+            const int s = sa[qd] * 65536 + sb[qd] * 256 + sc[qd];
             const uint32_t sw = (qd < 2) ? scw.x : scw.y;
-            const int scale = static_cast<int>(static_cast<int8_t>((sw >> (8 * (l.hh + 2 * (qd & 1)))) & 0xffu));
+            const uint32_t sx = prmt(sw, 0u, (qd & 1) ? l.sel1 : l.sel0);   // the int8 scale, sign-extended
+            const float ds = __fmaf_rn(d, __uint_as_float(sx + 0x4B400000u), nd);
             const float t = __int2float_rn(s) * x.xs[qd];
             const float u = __fmaf_rn(-32.0f, x.xsum[qd], t);
-            r = __fmaf_rn(d * __int2float_rn(scale), u, r);
+            r = __fmaf_rn(ds, u, r);
         }
         return r;
     }
@@ -218,14 +252,15 @@ struct Q6K {
 
 // ============================================================ Q8_0, f32 x
 struct Q8F {
-    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 32;
     static constexpr int BLOCK_BYTES = 34;
     static constexpr int SLICE_BLOCKS = 32;   // 32 one-block units (1088 bytes)
+    static constexpr int SLACK = 16;
     static constexpr bool LIMBS = true;
+    static constexpr int DEFAULT_UNROLL = 2;
 
     __host__ __device__ static int units(int nb) { return nb; }
-    __device__ __forceinline__ static int unit_byte(int u) { return u * BLOCK_BYTES; }
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u) * BLOCK_BYTES; }
     __device__ __forceinline__ static int unit_elem(int u) { return u * QK; }
 
     struct X {
@@ -237,24 +272,30 @@ struct Q8F {
     };
     __device__ __forceinline__ static L lane_consts(int, int, int) { return L{0}; }
 
-    __device__ __forceinline__ static void load_x(X& x, const XPrepSmem& P, int e0) {
+    __device__ __forceinline__ static void load_x(X& x, const uint8_t* smem, const LimbTables& T, int e0) {
 #pragma unroll
         for (int v = 0; v < 2; v++) {
-            const uint4 a = *reinterpret_cast<const uint4*>(P.la + e0 + 16 * v);
-            const uint4 b = *reinterpret_cast<const uint4*>(P.lb + e0 + 16 * v);
-            const uint4 c = *reinterpret_cast<const uint4*>(P.lc + e0 + 16 * v);
+            const uint32_t o = limb_chunk(static_cast<uint32_t>(e0 >> 4) + v) << 4;
+            const uint4 a = *reinterpret_cast<const uint4*>(smem + T.la + o);
+            const uint4 b = *reinterpret_cast<const uint4*>(smem + T.lb + o);
+            const uint4 c = *reinterpret_cast<const uint4*>(smem + T.lc + o);
             x.a[4 * v] = a.x; x.a[4 * v + 1] = a.y; x.a[4 * v + 2] = a.z; x.a[4 * v + 3] = a.w;
             x.b[4 * v] = b.x; x.b[4 * v + 1] = b.y; x.b[4 * v + 2] = b.z; x.b[4 * v + 3] = b.w;
             x.c[4 * v] = c.x; x.c[4 * v + 1] = c.y; x.c[4 * v + 2] = c.z; x.c[4 * v + 3] = c.w;
         }
-        x.xs = P.xs[e0 >> 5];
+        x.xs = reinterpret_cast<const float*>(smem + T.xs)[e0 >> 5];
     }
 
-    // blk: the 34-byte block in shared memory (2-byte aligned).
-    __device__ __forceinline__ static float dot(const uint8_t* blk, const L&, const X& x, float r) {
-        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16_a2(blk))));
-        const uint4 q0 = lds16_a2(blk + 2);
-        const uint4 q1 = lds16_a2(blk + 18);
+    // a: shared address of the 34-byte block (2-byte aligned).
+    __device__ __forceinline__ static float dot(uint32_t a, const L&, const X& x, float r) {
+        const uint32_t wa = a & ~3u;
+        const uint32_t sh = (a & 3u) * 8u;
+        const float d = f16_lo(lds32<0>(wa) >> sh);
+        // the codes start at a + 2: word-aligned when sh == 16
+        const uint32_t wq = wa + (sh >> 2);
+        const uint32_t qsh = 16u - sh;
+        const uint4 q0 = lds16_sh<0>(wq, qsh);
+        const uint4 q1 = lds16_sh<16>(wq, qsh);
         const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         int sa = 0, sb = 0, sc = 0;
 #pragma unroll
@@ -277,14 +318,15 @@ struct Q8F {
 // one warp's 32 units cover 4096 weights. Per block, dot = sum of 32
 // int8*int8 products (exact int32), and the row sums d_w * d_x * dot in f32.
 struct Q8D {
-    static constexpr int MAX_THREADS = 512;   // launch bound (registers: 65536 / MAX_THREADS)
     static constexpr int QK = 32;
     static constexpr int BLOCK_BYTES = 34;
     static constexpr int SLICE_BLOCKS = 128;  // 32 four-block units (4352 bytes)
+    static constexpr int SLACK = 144;         // a ragged last unit still loads 136 bytes
     static constexpr bool LIMBS = false;
+    static constexpr int DEFAULT_UNROLL = 2;
 
     __host__ __device__ static int units(int nb) { return (nb + 3) / 4; }
-    __device__ __forceinline__ static int unit_byte(int u) { return u * 4 * BLOCK_BYTES; }
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u) * 4u * BLOCK_BYTES; }
     __device__ __forceinline__ static int unit_elem(int u) { return u * 4 * QK; }
 
     struct X {
@@ -318,34 +360,80 @@ struct Q8D {
         }
     }
 
-    // blk: one 34-byte block in shared memory (2-byte aligned).
-    __device__ __forceinline__ static int block_dot(const uint8_t* blk, const uint32_t* xq) {
-        const uint4 q0 = lds16_a2(blk + 2);
-        const uint4 q1 = lds16_a2(blk + 18);
+    __device__ __forceinline__ static int block_dot8(const uint32_t* q, const uint32_t* xq) {
         int s = 0;
-        s = dp4a_ss(q0.x, xq[0], s);
-        s = dp4a_ss(q0.y, xq[1], s);
-        s = dp4a_ss(q0.z, xq[2], s);
-        s = dp4a_ss(q0.w, xq[3], s);
-        s = dp4a_ss(q1.x, xq[4], s);
-        s = dp4a_ss(q1.y, xq[5], s);
-        s = dp4a_ss(q1.z, xq[6], s);
-        s = dp4a_ss(q1.w, xq[7], s);
+#pragma unroll
+        for (int i = 0; i < 8; i++) s = dp4a_ss(q[i], xq[i], s);
         return s;
     }
 
-    // ub: the unit's first block in shared memory.
-    __device__ __forceinline__ static float dot(const uint8_t* ub, const L& l, const X& x, float r) {
+    // The four blocks of a unit that starts 8-byte aligned: 17 64-bit loads;
+    // the codes of blocks 0 and 2 sit 2 bytes off a word boundary.
+    // Outputs: d bit patterns (in the low 16 bits) and the code words.
+    __device__ __forceinline__ static void load_unit8(uint32_t a, uint32_t (&dh)[4], uint32_t (&q)[4][8]) {
+        uint32_t W[34];
+#define QMV_LD(m) { const uint2 v = lds64<8 * (m)>(a); W[2 * (m)] = v.x; W[2 * (m) + 1] = v.y; }
+        QMV_LD(0) QMV_LD(1) QMV_LD(2) QMV_LD(3) QMV_LD(4) QMV_LD(5) QMV_LD(6) QMV_LD(7) QMV_LD(8)
+        QMV_LD(9) QMV_LD(10) QMV_LD(11) QMV_LD(12) QMV_LD(13) QMV_LD(14) QMV_LD(15) QMV_LD(16)
+#undef QMV_LD
+        dh[0] = W[0];
+        dh[1] = W[8] >> 16;
+        dh[2] = W[17];
+        dh[3] = W[25] >> 16;
+#pragma unroll
+        for (int m = 0; m < 8; m++) {
+            q[0][m] = __funnelshift_r(W[m], W[m + 1], 16);
+            q[1][m] = W[9 + m];
+            q[2][m] = __funnelshift_r(W[17 + m], W[18 + m], 16);
+            q[3][m] = W[26 + m];
+        }
+    }
+
+    // The same from any 2-byte aligned address, block by block.
+    __device__ __forceinline__ static void load_block_a2(uint32_t a, uint32_t& dh, uint32_t (&q)[8]) {
+        const uint32_t wa = a & ~3u;
+        const uint32_t sh = (a & 3u) * 8u;
+        dh = lds32<0>(wa) >> sh;
+        const uint32_t wq = wa + (sh >> 2);
+        const uint32_t qsh = 16u - sh;
+        const uint4 q0 = lds16_sh<0>(wq, qsh);
+        const uint4 q1 = lds16_sh<16>(wq, qsh);
+        q[0] = q0.x; q[1] = q0.y; q[2] = q0.z; q[3] = q0.w;
+        q[4] = q1.x; q[5] = q1.y; q[6] = q1.z; q[7] = q1.w;
+    }
+
+    __device__ __forceinline__ static void load_unit(uint32_t a, bool aligned8, uint32_t (&dh)[4],
+                                                     uint32_t (&q)[4][8]) {
+        if (aligned8) {
+            load_unit8(a, dh, q);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; j++) load_block_a2(a + 34u * j, dh[j], q[j]);
+        }
+    }
+
+    // a: shared address of the unit's first block.
+    __device__ __forceinline__ static float dot(uint32_t a, const L& l, const X& x, float r, bool aligned8) {
+        uint32_t dh[4], q[4][8];
+        load_unit(a, aligned8, dh, q);
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             if (j < l.nblk) {
-                const uint8_t* blk = ub + j * BLOCK_BYTES;
-                const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16_a2(blk))));
-                const int s = block_dot(blk, x.q[j]);
-                r = __fmaf_rn(dw * x.xs[j], __int2float_rn(s), r);
+                const int s = block_dot8(q[j], x.q[j]);
+                r = __fmaf_rn(f16_lo(dh[j]) * x.xs[j], __int2float_rn(s), r);
             }
         }
         return r;
+    }
+
+    // The exact int32 dots of the unit's blocks (MODE_BLOCKDOTS).
+    __device__ __forceinline__ static void block_dots(uint32_t a, const L& l, const X& x, bool aligned8,
+                                                      int32_t* out) {
+        uint32_t dh[4], q[4][8];
+        load_unit(a, aligned8, dh, q);
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if (j < l.nblk) out[j] = block_dot8(q[j], x.q[j]);
     }
 };
 

@@ -3,25 +3,31 @@
 //
 // Shape of the computation (y[r] = sum_j W[r, j] x[j], W in packed GGML blocks):
 //  * A row is cut into k-slices of 32 "units" (one unit per lane, see
-//    qmv_formats.cuh). For every format a slice is a whole number of blocks
-//    whose byte length is a multiple of 16 (Q4_K 8 blocks = 1152 B, Q6_K 8
-//    blocks = 1680 B, Q8_0 32 blocks = 1088 B, Q8_0 dp4a 128 blocks = 4352 B),
-//    so one bulk TMA copy (cp.async.bulk ... mbarrier::complete_tx) brings one
-//    slice of one row into shared memory.
-//  * Each CTA owns a contiguous range of rows; its warps form NG row groups x
-//    KS k-slices. Every warp runs its own pipeline: lane 0 requests the warp's
-//    next S slots, the warp waits on the slot's mbarrier, decodes its 32 units
-//    in registers against the activation it keeps in registers, and lane 0
-//    re-fills the slot after a __syncwarp. No producer warp, no cross-warp
-//    barrier in the stream; copy issue is spread over all warps.
+//    qmv_formats.cuh); KS warps, one per slice, cover a row. A CTA owns a
+//    contiguous run of rows, split evenly over NG row groups of KS warps.
+//  * Every row group streams its rows through its own ring of S shared-memory
+//    slots. A slot holds a piece of CR whole rows, which are contiguous in
+//    memory, so one bulk TMA copy (cp.async.bulk ... mbarrier::complete_tx)
+//    fills it. The first S pieces are requested before anything else, before
+//    the kernel even waits for the previous one on the stream (the packed
+//    weights are constant). The group's warps wait on the slot's mbarrier,
+//    decode their slice of every row of the piece against the activation they
+//    keep in registers, and count themselves done; the last of them re-fills
+//    the slot with the group's next piece. No producer warp, no CTA barrier in
+//    the stream.
 //  * Rows narrower than a warp (fewer than 32 units) put 32/GS rows side by
-//    side in one warp. A warp reduces its lanes' partial sums with a fixed
-//    shuffle tree; when a row spans several k-slices the per-slice partials
-//    wait in shared memory and are summed in a fixed order once the CTA is
-//    done, so results are deterministic and no scratch memory or atomics are
-//    needed.
+//    side in one warp.
+//  * A warp reduces its lanes' partial sums of every row with a fixed shuffle
+//    tree right after decoding it, while other warps keep the memory busy. A
+//    row of one slice is written to y at once; a row of several slices parks
+//    its slice sums in shared memory and they are added in slice order once
+//    the CTA is done (deterministic, no atomics on the data, no memory beyond
+//    the inputs and the output).
 //  * MoE: grid.y is the slot; the CTA reads ids[slot] once and streams rows of
-//    expert ids[slot]'s slice of the bank, so only routed rows are read.
+//    expert ids[slot]'s matrix, so only routed rows are read.
+//  * Every wait is bounded (WAIT_LIMIT_NS): a copy that never lands raises
+//    STATUS_WAIT_TIMEOUT, and the CTA still waits (bounded) for the copies it
+//    issued before it exits.
 #pragma once
 
 #include <cstdint>
@@ -46,83 +52,99 @@ struct KParams {
     const int32_t* ids;         // [slots] expert ids (MoE)
     int n_experts;
     int rows, k, nb;            // rows per matrix, k, blocks per row
-    long long rowbytes;
-    unsigned long long wbytes;  // readable bytes starting at w (tail clipping)
+    uint32_t rowbytes;
+    unsigned long long matbytes;   // bytes of one matrix (MoE expert stride)
+    unsigned long long wbytes;     // readable bytes starting at w (tail clipping)
     int U;                      // units per row
-    int KS;                     // k-slices per row
+    int KS;                     // k-slices (warps) per row
     int GS;                     // lanes per row inside a warp: 32, or a smaller power of two when KS == 1
-    int NG;                     // row groups per CTA (working warps = NG * KS)
-    int R;                      // row steps per slot (KS == 1); 1 otherwise
-    int S;                      // slots per warp
     int lgGS;                   // log2(GS)
+    int NG;                     // row groups per CTA (working warps = NG * KS)
+    int CR;                     // rows per piece (one ring slot)
+    int S;                      // ring slots per row group
     int rq, rrem;               // rows per CTA: rq or rq + 1 (the first rrem CTAs)
     int gq[2], grem[2];         // rows per row group for a CTA of rq ([0]) or rq + 1 ([1]) rows
-    int defer;                  // 1: lanes park partial sums in shared memory, reduced once at the end
-    int W;                      // units per row rounded up (KS * GS): the width of a parked row
-    uint32_t off_la, off_lb, off_lc, off_xs, off_xsum;   // activation limb tables
-    uint32_t off_red;           // parked lane partials [rows][W] (defer), else slice partials [rows][KS]
-    uint32_t off_slots, slot_stride, off_bars;
+    int W;                      // parked partials per row (KS when KS > 1)
+    int aligned8;               // every unit starts 8-byte aligned in shared memory (Q8_0 dp4a)
+    int CL;                     // CTAs per cluster sharing the activation prep (1: no cluster)
+    uint32_t slot_stride;
+    LimbTables lt;              // activation limb tables (f32-activation formats)
+    uint32_t off_red;           // parked slice sums [rows of the CTA][W]
+    uint32_t off_ring;          // NG * S slots
+    uint32_t off_bars;          // NG * S mbarriers
+    uint32_t off_cnt;           // NG * S done-counters, NG issued-piece counts, 1 timeout flag
 };
 
-// Copy bytes [gs, gs + bytes) of global memory into the slot at `dst`
-// (16-byte aligned), starting the data at dst + (gs & 15). The bulk engine
-// takes the 16-byte-aligned cover of the range; if that cover would run past
-// the caller's buffer, the ragged last bytes are copied one by one before the
-// barrier is armed (so the arrive releases them to the waiting lanes).
-__device__ __forceinline__ void issue_copy(const KParams& p, uint8_t* dst, uint32_t bar, uintptr_t gs,
-                                           uintptr_t bytes) {
+// Copy bytes [gs, gs + bytes) of global memory into the slot at shared
+// address dst (128-byte aligned), the data starting at dst + (gs & 15). The
+// bulk engine takes the 16-byte-aligned cover of the range; if that cover would
+// run past the caller's buffer, the ragged last bytes are copied one by one
+// before the barrier is armed (so the arrive releases them to the waiters).
+__device__ __forceinline__ void issue_copy(const KParams& p, uint8_t* dst_ptr, uint32_t dst, uint32_t bar,
+                                           uintptr_t gs, uintptr_t bytes) {
     const uintptr_t ge = gs + bytes;
     const uintptr_t a0 = gs & ~uintptr_t(15);
     uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
     const uintptr_t lim = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(p.wbytes);
     if (a1 > lim) {
         a1 = ge & ~uintptr_t(15);
-        for (uintptr_t b = (a1 > a0 ? a1 : a0); b < ge; b++) dst[b - a0] = *reinterpret_cast<const uint8_t*>(b);
+        for (uintptr_t b = (a1 > a0 ? a1 : a0); b < ge; b++) dst_ptr[b - a0] = *reinterpret_cast<const uint8_t*>(b);
     }
     if (a1 > a0) {
         const uint32_t n = static_cast<uint32_t>(a1 - a0);
         mbar_arrive_expect_tx(bar, n);
-        tma_bulk_g2s(smem_u32(dst), reinterpret_cast<const void*>(a0), n, bar);
+        tma_bulk_g2s(dst, reinterpret_cast<const void*>(a0), n, bar);
     } else {
         mbar_arrive(bar);
     }
 }
 
-// The same copy as issue_copy done by the 32 lanes of a warp with 16-byte
-// cp.async (LDGSTS) requests, committed as one group per call.
-__device__ __forceinline__ void issue_copy_async(const KParams& p, uint8_t* dst, uintptr_t gs, uintptr_t bytes,
-                                                 int lane) {
-    const uintptr_t ge = gs + bytes;
-    const uintptr_t a0 = gs & ~uintptr_t(15);
-    uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
-    const uintptr_t lim = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(p.wbytes);
-    if (a1 > lim) {
-        a1 = ge & ~uintptr_t(15);
-        if (lane == 0)
-            for (uintptr_t b = (a1 > a0 ? a1 : a0); b < ge; b++) dst[b - a0] = *reinterpret_cast<const uint8_t*>(b);
-    }
-    const int n16 = a1 > a0 ? static_cast<int>((a1 - a0) >> 4) : 0;
-    const uint32_t d0 = smem_u32(dst);
-    for (int i = lane; i < n16; i += 32) cp_async16(d0 + 16u * i, reinterpret_cast<const void*>(a0 + 16u * i));
-    cp_async_commit();
+// The lane's dot for the unit at shared address a.
+template <class F>
+__device__ __forceinline__ float dot_of(uint32_t a, const typename F::L& lc, const typename F::X& xr, bool aligned8) {
+    if constexpr (F::LIMBS)
+        return F::dot(a, lc, xr, 0.0f);
+    else
+        return F::dot(a, lc, xr, 0.0f, aligned8);
 }
 
-template <class F, int R, bool MOE, int MODE, bool BULK>
-__global__ void __launch_bounds__(F::MAX_THREADS, 1) qmv_stream_kernel(const KParams p) {
+// Sum of v over each aligned group of GS lanes (a fixed xor tree); every lane
+// of the group ends with the group's sum.
+template <bool WIDE>
+__device__ __forceinline__ float group_sum(float v, int GS) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (WIDE || off < GS) v += __shfl_xor_sync(FULL, v, off);
+    }
+    return v;
+}
+
+// Sums over all 32 lanes of two values at once: lanes 0..15 end with the sum
+// of a, lanes 16..31 with the sum of b (one exchange splits the pair, then a
+// 16-lane tree), 12 instructions instead of 20.
+__device__ __forceinline__ float pair_sum(float a, float b, int lane) {
+    const bool hi = (lane & 16) != 0;
+    float keep = hi ? b : a;
+    const float send = hi ? a : b;
+    keep += __shfl_xor_sync(FULL, send, 16);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) keep += __shfl_xor_sync(FULL, keep, off);
+    return keep;
+}
+
+template <class F, int R, bool MOE, int MODE, bool WIDE>
+__global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
-    // ---- rows of this CTA
+    // ---- rows of this CTA (balanced split precomputed on the host)
     const int slot = MOE ? static_cast<int>(blockIdx.y) : 0;
-    // Balanced split precomputed on the host: no integer division here (a
-    // 64-bit division is a long serial routine right where latency matters).
     const int part = blockIdx.x;
     const int big = part < p.rrem ? 1 : 0;
     const int nrows = p.rq + big;
     const int R0 = part * p.rq + min(part, p.rrem);
-    const int R1 = R0 + nrows;
     const long long yoff = MOE ? static_cast<long long>(slot) * p.rows : 0;
 
     // The next call on the stream may be scheduled now; it still waits for
@@ -138,211 +160,204 @@ __global__ void __launch_bounds__(F::MAX_THREADS, 1) qmv_stream_kernel(const KPa
         if (e < 0 || e >= p.n_experts) {
             // Unroutable slot: NaN marks every output of it, and the status
             // word records the fact. No byte of the bank is touched.
-            for (int r = R0 + tid; r < R1; r += blockDim.x) p.y[yoff + r] = __int_as_float(0x7fc00000);
+            for (int r = R0 + tid; r < R0 + nrows; r += blockDim.x) p.y[yoff + r] = __int_as_float(0x7fc00000);
             if (tid == 0) atomicOr(&g_status, STATUS_BAD_EXPERT_ID);
             return;
         }
-        wbase = p.w + static_cast<long long>(e) * p.rows * p.rowbytes;
+        wbase = p.w + static_cast<unsigned long long>(e) * p.matbytes;
         xrow = p.x + static_cast<long long>(slot) * p.k;
     }
+    // (The planner never gives a CTA zero rows, and the MoE check above is the
+    // same for every CTA of a cluster, which all serve one slot: no CTA leaves
+    // before the cluster barrier below unless all of its cluster do.)
     if (nrows <= 0) return;
 
-    // ---- this warp's tile: row group rg (a contiguous run of the CTA's rows) x k-slice ks
-    const bool working = warp < p.NG * p.KS;
+    // ---- this warp: row group rg, k-slice ks
+    const int nwork = p.NG * p.KS;
+    const bool working = warp < nwork;
     const int rg = warp / p.KS;
     const int ks = warp - rg * p.KS;
     const int gq = p.gq[big], grem = p.grem[big];
-    const int row_lo = R0 + rg * gq + min(rg, grem);
-    const int row_hi = row_lo + gq + (rg < grem ? 1 : 0);
-    const int lg_rpw = 5 - p.lgGS;                       // log2 of the rows side by side in a warp
-    const int rpw = 1 << lg_rpw;
-    constexpr int LG_R = R == 4 ? 2 : (R == 2 ? 1 : 0);
-    const int lg_rps = (p.KS == 1) ? LG_R + lg_rpw : 0;  // log2 of the rows per slot
-    const int rows_per_slot = 1 << lg_rps;
-    const int nslot = working ? (row_hi - row_lo + rows_per_slot - 1) >> lg_rps : 0;
-    // bytes of the slice inside a row
-    const int blk0 = ks * F::SLICE_BLOCKS;
-    const int nblk = min(F::SLICE_BLOCKS, p.nb - blk0);
-    const uintptr_t slice_off = static_cast<uintptr_t>(blk0) * F::BLOCK_BYTES;
-    const uintptr_t slice_len = static_cast<uintptr_t>(nblk) * F::BLOCK_BYTES;
+    const int glo = rg * gq + min(rg, grem);          // first row of the group, CTA-local
+    const int gn = working ? gq + (rg < grem ? 1 : 0) : 0;
+    const int npc = (gn + p.CR - 1) / p.CR;          // pieces of the group
 
-    uint8_t* myslots = smem + p.off_slots + static_cast<uint32_t>(warp) * p.S * p.slot_stride;
-    const uint32_t mybars = smem_u32(smem + p.off_bars) + 8u * static_cast<uint32_t>(warp * p.S);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t ring = sbase + p.off_ring + static_cast<uint32_t>(rg * p.S) * p.slot_stride;
+    uint8_t* ring_ptr = smem + p.off_ring + static_cast<uint32_t>(rg * p.S) * p.slot_stride;
+    const uint32_t bars = sbase + p.off_bars + 8u * static_cast<uint32_t>(rg * p.S);
+    int* cnt = reinterpret_cast<int*>(smem + p.off_cnt);
+    int* done = cnt + rg * p.S;                       // this group's per-slot done-counters
+    int* issued = cnt + p.NG * p.S + rg;              // pieces requested so far by this group
+    int* timeout = cnt + p.NG * p.S + p.NG;           // CTA-wide flag
 
-    // Request slot t: bulk TMA from lane 0, or cp.async from every lane.
-    auto issue = [&](int t, int sl) {
-        const int r = row_lo + (t << lg_rps);
-        const int nr = min(rows_per_slot, row_hi - r);
-        const uintptr_t gs = reinterpret_cast<uintptr_t>(wbase) + static_cast<uintptr_t>(r) * p.rowbytes + slice_off;
-        const uintptr_t bytes = (p.KS == 1) ? static_cast<uintptr_t>(nr) * p.rowbytes : slice_len;
-        if constexpr (BULK) {
-            if (lane == 0) issue_copy(p, myslots + sl * p.slot_stride, mybars + 8u * sl, gs, bytes);
-        } else {
-            issue_copy_async(p, myslots + sl * p.slot_stride, gs, bytes, lane);
-        }
+    // Request piece pc of the group into slot s (one thread).
+    auto issue = [&](int pc, int s) {
+        const int r0 = R0 + glo + pc * p.CR;
+        const int nr = min(p.CR, gn - pc * p.CR);
+        const uintptr_t gs = reinterpret_cast<uintptr_t>(wbase) + static_cast<uintptr_t>(r0) * p.rowbytes;
+        issue_copy(p, ring_ptr + static_cast<uint32_t>(s) * p.slot_stride, ring + static_cast<uint32_t>(s) * p.slot_stride,
+                   bars + 8u * s, gs, static_cast<uintptr_t>(nr) * p.rowbytes);
     };
 
     // ---- first requests, before anything else
-    if (working) {
-        if (BULK && lane == 0) {
-            for (int s = 0; s < p.S; s++) mbar_init(mybars + 8u * s, 1);
-            fence_mbar_init();
+    if (working && ks == 0 && lane == 0) {
+        for (int s = 0; s < p.S; s++) {
+            mbar_init(bars + 8u * s, 1);
+            done[s] = 0;
         }
-        const int first = nslot < p.S ? nslot : p.S;
-        for (int t = 0; t < first; t++) issue(t, t);
+        fence_mbar_init();
+        const int first = npc < p.S ? npc : p.S;
+        for (int pc = 0; pc < first; pc++) issue(pc, pc);
+        *issued = first;
     }
-    int issued = nslot < p.S ? nslot : p.S;
+    if (tid == 0) *timeout = 0;
 
     // The packed weights are constant, so they were requested above without
     // waiting for the previous kernel; x (and y, written below) may be shared
     // with it.
     if (!MOE) pdl_dependency_wait();
 
-    // ---- activation limbs into shared memory (f32 formats), all threads
-    XPrepSmem P;
-    P.la = smem + p.off_la;
-    P.lb = smem + p.off_lb;
-    P.lc = smem + p.off_lc;
-    P.xs = reinterpret_cast<float*>(smem + p.off_xs);
-    P.xsum16 = reinterpret_cast<float*>(smem + p.off_xsum);
-    if constexpr (F::LIMBS) prep_limbs<4>(xrow, p.k, P, tid, static_cast<int>(blockDim.x));
-    __syncthreads();   // limb tables written; every warp's barriers initialized
+    if constexpr (F::LIMBS) {
+        // The activation limb tables, shared among the CTAs of a cluster (all
+        // of them work on the same x: the same matrix, or the same MoE slot).
+        prep_limbs<2>(xrow, p.k, smem, p.lt, tid, static_cast<int>(blockDim.x), p.CL, p.CL > 1 ? cluster_rank() : 0u);
+    }
+    if (p.CL > 1)
+        cluster_sync();   // every CTA's limb tables complete; barriers and counters initialized
+    else
+        __syncthreads();
 
     float* red = reinterpret_cast<float*>(smem + p.off_red);
 
     if (working) {
         // ---- this lane's unit: unit u of slice ks (KS > 1), or of the row
         const int u = (p.KS == 1) ? (lane & (p.GS - 1)) : lane;
+        const int sub = (p.KS == 1) ? (lane >> p.lgGS) : 0;   // which of the side-by-side rows
         const int ug = ks * 32 + u;                 // unit index within the row
         const bool has_unit = ug < p.U;
-        const int sub = (p.KS == 1) ? (lane >> p.lgGS) : 0;   // which of the side-by-side rows
-        const int wcol = ks * p.GS + u;             // this lane's column in a parked row
+        const int rpw = 32 >> p.lgGS;               // rows side by side in a warp step
         typename F::X xr;
-        typename F::L lc = F::lane_consts(u, p.nb, ug);
+        const typename F::L lc = F::lane_consts(u, p.nb, ug);
         if (has_unit) {
-            const int e0 = blk0 * F::QK + F::unit_elem(u);
+            const int e0 = ks * F::SLICE_BLOCKS * F::QK + F::unit_elem(u);
             if constexpr (F::LIMBS)
-                F::load_x(xr, P, e0);
+                F::load_x(xr, smem, p.lt, e0);
             else
                 F::load_xq(xr, lc, p.xq, p.xqs, e0);
         }
-        const int ubyte = F::unit_byte(u);
+        // Byte offset of the lane's unit inside a row, and 16-byte phase of the
+        // group's rows in memory (pieces may start off a 16-byte boundary).
+        const uint32_t ubyte = static_cast<uint32_t>(ks) * (F::SLICE_BLOCKS * F::BLOCK_BYTES) + F::unit_byte(u);
+        const uint32_t gphase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(wbase)) +
+                                static_cast<uint32_t>(R0 + glo) * p.rowbytes;
+        const uint32_t piece_bytes = static_cast<uint32_t>(p.CR) * p.rowbytes;
+        const uint32_t rstep = static_cast<uint32_t>(rpw) * p.rowbytes;   // bytes between warp steps
+        const bool aligned8 = p.aligned8 != 0;
+        // A finished row sum: to y (rows of one slice) or parked by slice.
+        auto store_row = [&](int rl, float v) {
+            if (p.KS == 1)
+                p.y[yoff + R0 + rl] = v;
+            else
+                red[rl * p.KS + ks] = v;
+        };
 
-        int sl = 0;          // slot of step t
-        uint32_t ph = 0;     // its barrier phase
-        for (int t = 0; t < nslot; t++) {
-            bool landed = true;
-            if constexpr (BULK) {
-                landed = __all_sync(FULL, mbar_wait_bounded(mybars + 8u * sl, ph));
-                if (!landed && lane == 0) atomicOr(&g_status, STATUS_WAIT_TIMEOUT);
-            } else {
-                // slots t+1 .. min(t+S-1, nslot-1) may still be in flight
-                cp_async_wait(min(p.S - 1, nslot - 1 - t));
-                __syncwarp();
-            }
-            const int r = row_lo + (t << lg_rps);
-            const int nr = min(rows_per_slot, row_hi - r);
-            const uintptr_t gs = reinterpret_cast<uintptr_t>(wbase) + static_cast<uintptr_t>(r) * p.rowbytes + slice_off;
-            const uint8_t* data = myslots + sl * p.slot_stride + static_cast<uint32_t>(gs & 15u);
-
-            if constexpr (MODE == MODE_BLOCKDOTS) {
-                if constexpr (!F::LIMBS) {
-                    for (int i = 0; i < R; i++) {
-                        const int j = (i << lg_rpw) + sub;
-                        if (has_unit && j < nr) {
-                            const uint8_t* ub = data + static_cast<long long>(j) * p.rowbytes + ubyte;
-                            for (int b = 0; b < lc.nblk; b++)
-                                p.dots[static_cast<long long>(r + j) * p.nb + blk0 + 4 * u + b] =
-                                    F::block_dot(ub + b * F::BLOCK_BYTES, xr.q[b]);
-                        }
-                    }
-                }
-            } else {
-                float acc[R];
-#pragma unroll
-                for (int i = 0; i < R; i++) {
-                    // Row j of the slot; steps past the slot's rows recompute
-                    // the lane's row of step 0 (valid data) and are dropped, so
-                    // the unrolled dots carry no control dependence.
-                    int j = (i << lg_rpw) + sub;
-                    j = j < nr ? j : sub;
-                    acc[i] = has_unit ? F::dot(data + static_cast<long long>(j) * p.rowbytes + ubyte, lc, xr, 0.0f)
-                                      : 0.0f;
-                }
-                if (p.defer) {
-                    // Park the lane partials; the rows are reduced once, at the end.
-#pragma unroll
-                    for (int i = 0; i < R; i++) {
-                        const int j = (i << lg_rpw) + sub;
-                        if (j < nr) red[static_cast<long long>(r + j - R0) * p.W + wcol] = acc[i];
-                    }
-                } else {
-                    for (int off = p.GS >> 1; off > 0; off >>= 1) {
-#pragma unroll
-                        for (int i = 0; i < R; i++) acc[i] += __shfl_xor_sync(FULL, acc[i], off);
-                    }
-                    if (u == 0) {
-#pragma unroll
-                        for (int i = 0; i < R; i++) {
-                            const int j = (i << lg_rpw) + sub;
-                            if (j < nr) {
-                                if (p.KS == 1)
-                                    p.y[yoff + r + j] = acc[i];
-                                else
-                                    red[static_cast<long long>(r + j - R0) * p.KS + ks] = acc[i];
-                            }
-                        }
-                    }
-                }
-            }
-            __syncwarp();   // the whole warp is done with slot sl
-            if (landed && t + p.S < nslot) {
-                issue(t + p.S, sl);
-                issued = t + p.S + 1;
-            }
+        int s = 0;
+        uint32_t par = 0;
+        for (int pc = 0; pc < npc; pc++) {
+            const bool landed = __all_sync(FULL, mbar_wait_bounded(bars + 8u * s, par));
             if (!landed) {
-                // A copy did not land in time: stop, but give the copies this
-                // warp still has in flight a bounded chance to land before the
-                // shared memory is released.
                 if (lane == 0) {
-                    int s2 = sl;
-                    uint32_t ph2 = ph;
-                    for (int tt = t + 1; tt < issued; tt++) {
-                        if (++s2 == p.S) {
-                            s2 = 0;
-                            ph2 ^= 1u;
-                        }
-                        if (!mbar_wait_bounded(mybars + 8u * s2, ph2)) break;
-                    }
+                    atomicOr(&g_status, STATUS_WAIT_TIMEOUT);
+                    atomicExch(timeout, 1);
                 }
                 break;
             }
-            if (++sl == p.S) {
-                sl = 0;
-                ph ^= 1u;
+            const int nr = min(p.CR, gn - pc * p.CR);
+            const int rl0 = glo + pc * p.CR;                     // CTA-local row of the piece's first row
+            const uint32_t d0 = (gphase + static_cast<uint32_t>(pc) * piece_bytes) & 15u;
+            const uint32_t prow0 = ring + static_cast<uint32_t>(s) * p.slot_stride + d0 + ubyte;   // unit, row 0
+            uint32_t a = prow0 + static_cast<uint32_t>(sub) * p.rowbytes;                     // unit, step 0
+            int jb = 0;
+            if constexpr (MODE == MODE_MATVEC) {
+                // Whole steps of R * rpw rows: R independent dots, then the
+                // row sums (every row of such a step lies inside the piece).
+                for (; jb + R * rpw <= nr; jb += R * rpw, a += R * rstep) {
+                    float acc[R];
+#pragma unroll
+                    for (int q = 0; q < R; q++) acc[q] = has_unit ? dot_of<F>(a + q * rstep, lc, xr, aligned8) : 0.0f;
+                    if constexpr (WIDE && R == 2) {
+                        const float v = pair_sum(acc[0], acc[1], lane);
+                        if ((lane & 15) == 0) store_row(rl0 + jb + (lane >> 4), v);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < R; q++) {
+                            const float v = group_sum<WIDE>(acc[q], p.GS);
+                            if (u == 0) store_row(rl0 + jb + q * rpw + sub, v);
+                        }
+                    }
+                }
+                // The piece's remaining rows, one step at a time; lanes whose
+                // row lies past the piece decode row 0 and drop the result.
+                for (; jb < nr; jb += rpw, a += rstep) {
+                    const bool valid = jb + sub < nr;
+                    float v = has_unit ? dot_of<F>(valid ? a : prow0, lc, xr, aligned8) : 0.0f;
+                    v = group_sum<WIDE>(v, p.GS);
+                    if (u == 0 && valid) store_row(rl0 + jb + sub, v);
+                }
+            } else {
+                // MODE_BLOCKDOTS: the exact int32 dots of every block.
+                if constexpr (!F::LIMBS) {
+                    for (; jb < nr; jb += rpw, a += rstep) {
+                        if (has_unit && jb + sub < nr)
+                            F::block_dots(a, lc, xr, aligned8,
+                                          p.dots + static_cast<long long>(R0 + rl0 + jb + sub) * p.nb + 4 * ug);
+                    }
+                }
+            }
+            __syncwarp();   // the whole warp is done with slot s
+            if (pc + p.S < npc) {
+                // The group's piece pc + S goes into this slot once every warp of
+                // the group is done with it; the last one to finish requests it.
+                if (lane == 0) {
+                    bool last = true;
+                    if (p.KS > 1) {
+                        __threadfence_block();
+                        last = atomicAdd(&done[s], 1) == p.KS - 1;
+                        if (last) done[s] = 0;
+                    }
+                    if (last) {
+                        fence_proxy_async();
+                        issue(pc + p.S, s);
+                        atomicMax(issued, pc + p.S + 1);
+                    }
+                }
+            }
+            if (++s == p.S) {
+                s = 0;
+                par ^= 1u;
             }
         }
     }
 
-    if (MODE == MODE_MATVEC && p.defer) {
-        // One warp per row: strided lane sums over the parked partials, then a
-        // fixed shuffle tree.
-        __syncthreads();
-        const int nwarps = blockDim.x >> 5;
-        for (int r = warp; r < nrows; r += nwarps) {
-            float s = 0.0f;
-            for (int c = lane; c < p.W; c += 32) s += red[static_cast<long long>(r) * p.W + c];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
-            if (lane == 0) p.y[yoff + R0 + r] = s;
+    __syncthreads();
+    if (*timeout) {
+        // A copy did not land in time: give every copy this group still has in
+        // flight a bounded chance to land before the shared memory is released.
+        if (working && ks == 0 && lane == 0) {
+            const int n = *issued;
+            for (int pc = n - p.S > 0 ? n - p.S : 0; pc < n; pc++)
+                if (!mbar_wait_bounded(bars + 8u * (pc % p.S), static_cast<uint32_t>((pc / p.S) & 1))) break;
         }
-    } else if (MODE == MODE_MATVEC && p.KS > 1) {
-        // Rows spanning several k-slices: sum the slice partials in a fixed order.
-        __syncthreads();
+        return;
+    }
+
+    if (MODE == MODE_MATVEC && p.KS > 1) {
+        // Rows spanning several k-slices: add the slice sums in slice order.
         for (int r = tid; r < nrows; r += blockDim.x) {
-            float s = 0.0f;
-            for (int q = 0; q < p.KS; q++) s += red[static_cast<long long>(r) * p.KS + q];
-            p.y[yoff + R0 + r] = s;
+            float v = 0.0f;
+            for (int q = 0; q < p.KS; q++) v += red[r * p.KS + q];
+            p.y[yoff + R0 + r] = v;
         }
     }
 }

@@ -1,6 +1,6 @@
 // qmv_launch.cuh -- host-side launch plan for qmv_stream_kernel: lane groups,
-// grid size, rows per pipeline stage, pipeline depth and the shared-memory
-// layout, chosen per shape (or forced through qmv_cfg for tests).
+// row groups, grid size, rows per ring slot, ring depth and the shared-memory
+// layout, chosen per shape (or forced through qmv_cfg for tests and sweeps).
 #pragma once
 
 #include <algorithm>
@@ -12,9 +12,12 @@
 
 namespace qmv {
 
-constexpr long long STAGE_MAX_BYTES = 32 * 1024;   // rows per stage are capped by this
-constexpr int STAGES_MAX = 8;
 constexpr int MAX_DEVICES = 64;
+constexpr int MAX_WARPS = 16;               // kernel launch bound: 512 threads, <= 128 registers each
+constexpr int WARPS_TWO_PER_SM = 8;         // default CTA size: two CTAs fit on one SM
+constexpr long long PIECE_TARGET_BYTES = 16 * 1024;   // rows per ring slot: about this many bytes
+constexpr long long RED_MAX_BYTES = 64 * 1024;        // parked slice sums per CTA, at most
+constexpr long long MIN_CTA_BYTES = 4 * 1024;         // packed weights per CTA, at least (small matrices)
 
 // The last CUDA error seen by a launch on this thread (for qmv_last_cuda_error).
 inline cudaError_t& last_cuda_error() {
@@ -37,7 +40,9 @@ inline int& weight_prefetch_flag() {
 
 struct DevInfo {
     int nsm = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;   // per CTA
+    int smem_sm = 0;      // per SM
+    int smem_reserved = 0;
 };
 
 inline int dev_info(DevInfo* out, int* dev_out) {
@@ -52,7 +57,9 @@ inline int dev_info(DevInfo* out, int* dev_out) {
     if (cache[dev].nsm == 0) {
         DevInfo d;
         if (cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
             return QMV_ECUDA;
         cache[dev] = d;
     }
@@ -64,10 +71,16 @@ inline int dev_info(DevInfo* out, int* dev_out) {
 struct Plan {
     int T = 0;            // threads per CTA
     int parts = 1;        // CTAs per matrix (grid.x)
-    int R = 1;            // row steps per slot (kernel template parameter)
-    bool bulk = false;    // copy engine: bulk TMA (true) or warp-wide cp.async (false)
+    int R = 1;            // rows per warp step (kernel template parameter)
+    int CL = 1;           // cluster size along grid.x
     size_t smem = 0;
 };
+
+// CTAs sharing one activation prep, by default none: on GB300 a GPC holds 19
+// SMs, so clusters of 2 or more leave SMs idle in every wave; measured slower
+// (clusters of 4: +23 % on Q4_K 4096 x 4096, +80 % on Q6_K 4096 x 14336).
+constexpr int CLUSTER_DEFAULT = 1;
+constexpr int CLUSTER_MAX = 8;       // portable cluster size limit
 
 inline int pow2ceil(int v) {
     int p = 1;
@@ -77,105 +90,160 @@ inline int pow2ceil(int v) {
 
 inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a; }
 
-// Target bytes in flight per SM. Measured on GB300 (tuning sweeps over the
-// five workloads): two slots per warp, about 40-60 KB per SM, is as fast as or
-// faster than deeper rings; more outstanding copies only delay the moment a
-// CTA's first slot lands.
-constexpr long long IN_FLIGHT_BYTES = 48 * 1024;
-constexpr long long DEFER_MAX_BYTES = 48 * 1024;
-
-// Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense).
+// Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense)
+// on a device described by `di`.
 template <class F>
-inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
-    DevInfo di;
-    int rc = dev_info(&di, nullptr);
-    if (rc) return rc;
+inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
     const int nb = k / F::QK;
     const int U = F::units(nb);
     const int KS = (U + 31) / 32;
     const int GS = KS == 1 ? pow2ceil(U) : 32;
     const int rpw = 32 / GS;
-    int nw_max = F::MAX_THREADS / 32;
-    if (cfg && cfg->warps > 0) nw_max = std::min(nw_max, cfg->warps);
-    if (KS > nw_max) return QMV_ETOOBIG;
     const long long rowbytes = static_cast<long long>(nb) * F::BLOCK_BYTES;
+    if (KS > MAX_WARPS) return QMV_ETOOBIG;
+
+    // Warps per CTA: by default 8, so that the next call's CTAs can fit beside
+    // this call's on every SM; rows of more than 4 slices take up to 16 (a
+    // single row group of 5..8 warps would leave too few warps to hide
+    // latency).
+    int nw_max = (cfg && cfg->warps > 0) ? std::min(cfg->warps, MAX_WARPS)
+                                         : (KS > 4 ? MAX_WARPS : WARPS_TWO_PER_SM);
+    if (KS > nw_max) return QMV_ETOOBIG;
 
     Plan P;
     // CTAs per matrix: one per SM (MoE: the SMs are shared by the slots), but
-    // not more than there are rows.
-    if (cfg && cfg->ctas > 0)
-        P.parts = std::min(cfg->ctas, rows);
-    else if (slots > 1)
-        P.parts = std::min((di.nsm + slots - 1) / slots, rows);
-    else
-        P.parts = std::min(di.nsm, rows);
-    P.parts = std::max(P.parts, 1);
+    // not more than there are rows, and enough that the parked partials fit.
+    const int W = KS > 1 ? KS : 0;   // parked slice sums per row
+    if (cfg && cfg->ctas > 0) {
+        P.parts = cfg->ctas;
+    } else {
+        P.parts = slots > 1 ? (di.nsm + slots - 1) / slots : di.nsm;
+        // small matrices: at least MIN_CTA_BYTES of weights per CTA (a CTA
+        // pays a fixed start-up cost, the activation prep among it)
+        const long long by_bytes = std::max<long long>(1, static_cast<long long>(rows) * rowbytes / MIN_CTA_BYTES);
+        if (by_bytes < P.parts) P.parts = static_cast<int>(by_bytes);
+        const long long max_rows = std::max<long long>(1, RED_MAX_BYTES / (4LL * std::max(W, 1)));
+        const long long need = (rows + max_rows - 1) / max_rows;
+        if (need > P.parts) P.parts = static_cast<int>(std::min<long long>(need, 1 << 30));
+    }
+    P.parts = std::max(1, std::min(P.parts, rows));
+    // Clusters share the activation prep: CL CTAs of one matrix each convert
+    // 1/CL of x. CL divides the CTA count and half the 16-element groups.
+    {
+        int want = (cfg && cfg->cluster > 0) ? std::min(cfg->cluster, CLUSTER_MAX) : CLUSTER_DEFAULT;
+        if (!F::LIMBS) want = 1;
+        int cl = 1;
+        for (int c = want; c > 1; c--) {
+            if ((c & (c - 1)) == 0 && P.parts % c == 0 && (k / 16) % (2 * c) == 0) {
+                cl = c;
+                break;
+            }
+        }
+        if (cfg && cfg->cluster > 0 && cl != std::min(cfg->cluster, CLUSTER_MAX) && F::LIMBS) {
+            // a forced size the shape cannot take: round the CTA count down to it
+            const int c = std::min(cfg->cluster, CLUSTER_MAX);
+            if ((c & (c - 1)) == 0 && (k / 16) % (2 * c) == 0 && P.parts >= c) {
+                P.parts = P.parts / c * c;
+                cl = c;
+            }
+        }
+        P.CL = cl;
+    }
     const int rpc = (rows + P.parts - 1) / P.parts;
 
-    // Row groups: as many as the thread budget holds, no more than the CTA's
+    // Row groups: as many as the warp budget holds, no more than the CTA's
     // rows can feed.
     int NG = std::max(1, nw_max / KS);
     NG = std::min(NG, (rpc + rpw - 1) / rpw);
     NG = std::max(NG, 1);
     const int nwarps = NG * KS;
     P.T = 32 * nwarps;
-    const int rows_per_group = (rpc + NG - 1) / NG;
+    const int gmax = (rpc + NG - 1) / NG;   // rows of the largest row group
 
-    // Slot = R row steps (KS == 1) or one row's slice (KS > 1).
-    int R = 1;
-    if (KS == 1 && cfg && cfg->stage_rows > 0) {
-        const int want = std::max(1, cfg->stage_rows / rpw);
-        R = want >= 4 ? 4 : (want >= 2 ? 2 : 1);
-    }
+    // Rows per warp step: 2 by default for the lighter decoders.
+    int R = (cfg && cfg->unroll > 0) ? (cfg->unroll >= 2 ? 2 : 1) : F::DEFAULT_UNROLL;
     P.R = R;
-    // Copy engine: bulk TMA from one lane per warp by default; 16-byte
-    // cp.async from all 32 lanes stays selectable (measured equal or slower).
-    P.bulk = !(cfg && cfg->copy == 2);
-    const long long slot_bytes = KS == 1 ? static_cast<long long>(R) * rpw * rowbytes
-                                         : static_cast<long long>(F::SLICE_BLOCKS) * F::BLOCK_BYTES;
-    if (slot_bytes + 32 > 0x7fffffffLL) return QMV_ETOOBIG;
-    const long long slot_stride = round_up(slot_bytes + 32, 128);
-    const int steps = KS == 1 ? (rows_per_group + R * rpw - 1) / (R * rpw) : rows_per_group;
 
-    // Shared-memory layout: limb tables, slice partials, slots, barriers.
+    // Shared-memory layout: limb tables, parked partials, ring, barriers, counters.
     long long off = 0;
-    kp->off_la = kp->off_lb = kp->off_lc = kp->off_xs = kp->off_xsum = 0;
+    kp->lt = LimbTables{0, 0, 0, 0, 0};
     if (F::LIMBS) {
-        kp->off_la = static_cast<uint32_t>(off); off = round_up(off + k, 128);
-        kp->off_lb = static_cast<uint32_t>(off); off = round_up(off + k, 128);
-        kp->off_lc = static_cast<uint32_t>(off); off = round_up(off + k, 128);
-        kp->off_xs = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 32), 128);
-        kp->off_xsum = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 16), 128);
+        kp->lt.la = static_cast<uint32_t>(off); off = round_up(off + k, 128);
+        kp->lt.lb = static_cast<uint32_t>(off); off = round_up(off + k, 128);
+        kp->lt.lc = static_cast<uint32_t>(off); off = round_up(off + k, 128);
+        kp->lt.xs = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 32), 128);
+        kp->lt.xsum16 = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 16), 128);
     }
-    // Row partials: park every lane's partial ([rows][KS * GS] floats) and
-    // reduce once at the end when that fits comfortably; otherwise reduce each
-    // slot with shuffles and keep only per-slice partials ([rows][KS]).
-    const int W = KS * GS;
-    const bool defer = 4LL * rpc * W <= DEFER_MAX_BYTES;
     kp->off_red = static_cast<uint32_t>(off);
-    if (defer)
-        off = round_up(off + 4LL * rpc * W, 128);
-    else if (KS > 1)
-        off = round_up(off + 4LL * rpc * KS, 128);
-    const long long avail = di.smem_optin - 1024 - off;   // 1 KB for static shared memory
-    const long long per_slot = nwarps * (slot_stride + 8);
-    int S;
-    if (cfg && cfg->stages > 0)
-        S = cfg->stages;
-    else
-        S = static_cast<int>(std::min<long long>(8, std::max<long long>(2, IN_FLIGHT_BYTES / (nwarps * slot_bytes))));
-    S = std::min(S, std::max(steps, 1));
-    S = static_cast<int>(std::min<long long>(S, avail / per_slot));
-    if (S < 1) return QMV_ETOOBIG;
-    kp->off_slots = static_cast<uint32_t>(off);
-    kp->slot_stride = static_cast<uint32_t>(slot_stride);
-    off += static_cast<long long>(nwarps) * S * slot_stride;
+    off = round_up(off + 4LL * rpc * W, 128);   // W == 0: nothing parked
+    const long long fixed = off;
+
+    // Budget: half an SM's shared memory when two CTAs are meant to share it,
+    // else all a CTA may take.
+    const long long per_sm = di.smem_sm - 2LL * di.smem_reserved;
+    const long long half = per_sm / 2;
+    const long long full = di.smem_optin;
+
+    auto slot_stride_of = [&](int cr) { return round_up(static_cast<long long>(cr) * rowbytes + 32 + F::SLACK, 128); };
+    auto tail = [&](int s) { return 8LL * NG * s + 4LL * (NG * s + NG + 1); };
+    auto fits = [&](int cr, int s, long long budget) { return fixed + NG * s * slot_stride_of(cr) + tail(s) <= budget; };
+    const int step = R * rpw;   // rows of one unrolled warp step
+    int CR = 0, S = 0;
+    bool done = false;
+    if (cfg && (cfg->chunk_rows > 0 || cfg->chunks > 0)) {
+        // Forced pieces and/or depth: as asked, within the CTA's limit.
+        CR = cfg->chunk_rows > 0 ? cfg->chunk_rows
+                                 : static_cast<int>(std::max<long long>(step, PIECE_TARGET_BYTES / rowbytes));
+        CR = std::max(1, std::min(CR, gmax));
+        const int pieces = (gmax + CR - 1) / CR;
+        S = cfg->chunks > 0 ? std::min(cfg->chunks, pieces) : pieces;
+        while (S > 0 && !fits(CR, S, full)) S--;
+        done = S >= 1;
+    } else {
+        // 1. The CTA's whole share at once, one piece per row group, next to a
+        //    second CTA on the SM (small CTAs) or alone.
+        const long long whole_budget = nwarps <= WARPS_TWO_PER_SM ? half : full;
+        if (fits(gmax, 1, whole_budget)) {
+            CR = gmax;
+            S = 1;
+            done = true;
+        } else {
+            // 2. A ring per row group: pieces of about PIECE_TARGET_BYTES (whole
+            //    warp steps where possible), as deep as the SM's shared memory
+            //    allows, at least two slots when a group has two pieces.
+            CR = static_cast<int>(std::max<long long>(step, PIECE_TARGET_BYTES / rowbytes));
+            CR = std::max(1, std::min(CR / step * step > 0 ? CR / step * step : CR, gmax));
+            while (true) {
+                const int pieces = (gmax + CR - 1) / CR;
+                S = pieces;
+                while (S > 0 && !fits(CR, S, full)) S--;
+                if (S >= 2 || (S >= 1 && pieces == 1)) {
+                    done = true;
+                    break;
+                }
+                if (CR == 1) {
+                    done = S >= 1;
+                    break;
+                }
+                CR = (CR / 2 >= step) ? (CR / 2) / step * step : std::max(1, CR / 2);
+            }
+        }
+    }
+    if (!done) return QMV_ETOOBIG;
+    const long long stride = slot_stride_of(CR);
+    if (stride > 0x7fffffffLL) return QMV_ETOOBIG;
+
+    kp->off_ring = static_cast<uint32_t>(off);
+    off += static_cast<long long>(NG) * S * stride;
     kp->off_bars = static_cast<uint32_t>(off);
-    off += 8LL * nwarps * S;
-    P.smem = static_cast<size_t>(off);
+    off += 8LL * NG * S;
+    kp->off_cnt = static_cast<uint32_t>(off);
+    off += 4LL * (NG * S + NG + 1);
+    P.smem = static_cast<size_t>(round_up(off, 16));
+    if (static_cast<long long>(P.smem) > full) return QMV_ETOOBIG;
 
     kp->nb = nb;
-    kp->rowbytes = rowbytes;
+    kp->rowbytes = static_cast<uint32_t>(rowbytes);
     kp->U = U;
     kp->KS = KS;
     kp->GS = GS;
@@ -183,10 +251,12 @@ inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp
     while ((1 << lg) < GS) lg++;
     kp->lgGS = lg;
     kp->NG = NG;
-    kp->R = R;
+    kp->CR = CR;
     kp->S = S;
-    kp->defer = defer ? 1 : 0;
     kp->W = W;
+    kp->slot_stride = static_cast<uint32_t>(stride);
+    kp->aligned8 = (rowbytes % 8 == 0) ? 1 : 0;
+    kp->CL = P.CL;
     // Balanced splits, precomputed so the kernel only multiplies.
     kp->rq = rows / P.parts;
     kp->rrem = rows % P.parts;
@@ -199,9 +269,17 @@ inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp
     return QMV_OK;
 }
 
-template <class F, int R, bool MOE, int MODE, bool BULK>
+// The same on the current device.
+template <class F>
+inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
+    DevInfo di;
+    const int rc = dev_info(&di, nullptr);
+    return rc ? rc : make_plan_for<F>(di, rows, k, slots, cfg, kp, pl);
+}
+
+template <class F, int R, bool MOE, int MODE, bool WIDE>
 inline int launch_one(const KParams& kp, const Plan& pl, int slots, cudaStream_t stream) {
-    auto kern = qmv_stream_kernel<F, R, MOE, MODE, BULK>;
+    auto kern = qmv_stream_kernel<F, R, MOE, MODE, WIDE>;
     // Dynamic shared memory above 48 KB must be opted into per kernel; the
     // attribute only ever grows, once per size class and device.
     static int configured[MAX_DEVICES] = {};
@@ -219,27 +297,33 @@ inline int launch_one(const KParams& kp, const Plan& pl, int slots, cudaStream_t
     lc.blockDim = dim3(pl.T, 1, 1);
     lc.dynamicSmemBytes = pl.smem;
     lc.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = at;
-    lc.numAttrs = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED) ? 1 : 0;
-    return cuda_rc(cudaLaunchKernelEx(&lc, kern, kp));
-}
-
-template <class F, bool MOE, int MODE, bool BULK>
-inline int launch_r(const KParams& kp, const Plan& pl, int slots, cudaStream_t stream) {
-    switch (pl.R) {
-    case 1: return launch_one<F, 1, MOE, MODE, BULK>(kp, pl, slots, stream);
-    case 2: return launch_one<F, 2, MOE, MODE, BULK>(kp, pl, slots, stream);
-    default: return launch_one<F, 4, MOE, MODE, BULK>(kp, pl, slots, stream);
+    cudaLaunchAttribute at[2];
+    int na = 0;
+    if (pl.CL > 1) {
+        at[na].id = cudaLaunchAttributeClusterDimension;
+        at[na].val.clusterDim.x = static_cast<unsigned>(pl.CL);
+        at[na].val.clusterDim.y = 1;
+        at[na].val.clusterDim.z = 1;
+        na++;
     }
+    if (__atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED)) {
+        at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[na].val.programmaticStreamSerializationAllowed = 1;
+        na++;
+    }
+    lc.attrs = at;
+    lc.numAttrs = na;
+    return cuda_rc(cudaLaunchKernelEx(&lc, kern, kp));
 }
 
 template <class F, bool MOE, int MODE>
 inline int launch(const KParams& kp, const Plan& pl, int slots, cudaStream_t stream) {
-    return pl.bulk ? launch_r<F, MOE, MODE, true>(kp, pl, slots, stream)
-                   : launch_r<F, MOE, MODE, false>(kp, pl, slots, stream);
+    // WIDE: a row's units fill whole warps (32 lanes per row).
+    if (kp.GS == 32)
+        return pl.R >= 2 ? launch_one<F, 2, MOE, MODE, true>(kp, pl, slots, stream)
+                         : launch_one<F, 1, MOE, MODE, true>(kp, pl, slots, stream);
+    return pl.R >= 2 ? launch_one<F, 2, MOE, MODE, false>(kp, pl, slots, stream)
+                     : launch_one<F, 1, MOE, MODE, false>(kp, pl, slots, stream);
 }
 
 // Read (and optionally clear) this translation unit's device status word.

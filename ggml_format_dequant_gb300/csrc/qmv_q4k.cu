@@ -54,8 +54,9 @@ int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
     kp.rows = rows;
     kp.k = k;
     kp.nb = k / 256;
-    kp.rowbytes = static_cast<long long>(kp.nb) * 144;
-    kp.wbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 144u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = kp.matbytes;
     Plan pl;
     int rc = make_plan<Q4K>(rows, k, 1, cfg, &kp, &pl);
     if (rc) return rc;
@@ -73,8 +74,9 @@ int moe_q4k(const void* bank, const float* x, float* y, int rows, int k, const i
     kp.rows = rows;
     kp.k = k;
     kp.nb = k / 256;
-    kp.rowbytes = static_cast<long long>(kp.nb) * 144;
-    kp.wbytes = static_cast<unsigned long long>(n_experts) * rows * kp.rowbytes;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 144u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = static_cast<unsigned long long>(n_experts) * kp.matbytes;
     Plan pl;
     int rc = make_plan<Q4K>(rows, k, slots, cfg, &kp, &pl);
     if (rc) return rc;

@@ -44,8 +44,9 @@ int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
     kp.rows = rows;
     kp.k = k;
     kp.nb = k / 256;
-    kp.rowbytes = static_cast<long long>(kp.nb) * 210;
-    kp.wbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 210u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = kp.matbytes;
     Plan pl;
     int rc = make_plan<Q6K>(rows, k, 1, cfg, &kp, &pl);
     if (rc) return rc;

@@ -51,8 +51,9 @@ KParams q8_params(const void* w, int rows, int k) {
     kp.rows = rows;
     kp.k = k;
     kp.nb = k / 32;
-    kp.rowbytes = static_cast<long long>(kp.nb) * 34;
-    kp.wbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 34u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = kp.matbytes;
     return kp;
 }
 

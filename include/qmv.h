@@ -134,17 +134,20 @@ int qmv_device_status(unsigned int *status, int clear);
  */
 
 /* Forced launch configuration: any field <= 0 keeps the automatic choice.
- * ctas: CTAs per weight matrix; stage_rows: rows per pipeline stage;
- * stages: pipeline depth (slots per warp); copy: 1 = bulk TMA copies (the
- * default), 2 = 16-byte cp.async copies; warps: at most this many warps per CTA. Used to
- * exercise multi-stage pipelines, ragged tails and both copy engines on small
- * inputs, and for tuning sweeps. */
+ * ctas: CTAs per weight matrix (per MoE slot); chunk_rows: rows per ring slot
+ * (one bulk copy); chunks: ring slots per row group; unroll: rows each warp
+ * decodes per step (1 or 2); warps: at most this many warps per CTA (at least
+ * the k-slices of one row); cluster: CTAs (a power of two up to 8) that share
+ * the conversion of the f32 activation (the CTA count is rounded down to a
+ * multiple of it). Used to exercise ring reuse, ragged pieces and
+ * small CTAs on small inputs, and for tuning sweeps. */
 typedef struct qmv_cfg {
     int ctas;
-    int stage_rows;
-    int stages;
-    int copy;
+    int chunk_rows;
+    int chunks;
+    int unroll;
     int warps;
+    int cluster;
 } qmv_cfg;
 
 int qmv_q4k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
@@ -171,10 +174,25 @@ int qmv_q8_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int ro
                           cudaStream_t stream);
 
 /* Launch plan the library would use (for benchmark reports): threads per CTA,
- * CTAs per matrix, rows per stage, pipeline depth and dynamic shared bytes.
+ * CTAs (all slots), rows per ring slot, ring slots per row group and dynamic
+ * shared bytes per CTA.
  * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K. */
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
-                  int *stage_rows, int *stages, int *smem_bytes);
+                  int *chunk_rows, int *chunks, int *smem_bytes);
+
+/* The complete launch plan for a described device, computed on the host
+ * without touching a GPU (for tests of the planner). device = {SM count,
+ * opt-in shared bytes per CTA, shared bytes per SM, reserved shared bytes per
+ * CTA}. out receives QMV_PLAN_DETAIL_FIELDS ints in this order: threads, ctas
+ * (per matrix), rows per warp step, dynamic shared bytes, units per row,
+ * k-slices per row, lanes per row, row groups, rows per ring slot, ring slots
+ * per group, bytes per row, parked row width, slot stride, 8-byte unit
+ * alignment flag, rows per CTA (q, rem), rows per group for the smaller CTAs
+ * (q, rem) and the larger ones (q, rem), shared offsets of the limb tables
+ * (a, b, c, scales, sums), of the parked partials, the ring, the barriers and
+ * the counters, and the cluster size. */
+#define QMV_PLAN_DETAIL_FIELDS 30
+int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, const int *device, int *out);
 
 #ifdef __cplusplus
 }

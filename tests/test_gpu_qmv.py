@@ -90,14 +90,15 @@ def test_matvec_matches_oracle(q, fmt, rows, k):
     assert scale_rel(oracle.qmv(fmt, w, x, rows, k), y) <= SCALE_REL_TOL
 
 
-@pytest.mark.parametrize("cfg", [dict(ctas=1, stage_rows=1, stages=2), dict(ctas=3, stage_rows=5, stages=2),
-                                 dict(ctas=2, stage_rows=3, stages=1), dict(ctas=7, stages=3),
-                                 dict(ctas=1, stages=2, copy=1), dict(ctas=3, stage_rows=4, stages=3, copy=1),
-                                 dict(ctas=2, stages=1, copy=1), dict(ctas=5, stage_rows=2, stages=4, copy=2)])
+@pytest.mark.parametrize("cfg", [dict(ctas=1, chunk_rows=1, chunks=2), dict(ctas=3, chunk_rows=5, chunks=2),
+                                 dict(ctas=2, chunk_rows=3, chunks=1), dict(ctas=7, chunks=3),
+                                 dict(ctas=1, chunks=2, unroll=1), dict(ctas=3, chunk_rows=4, chunks=3, unroll=2),
+                                 dict(ctas=2, chunks=1, warps=2), dict(ctas=5, chunk_rows=2, chunks=4, warps=4),
+                                 dict(ctas=1, chunk_rows=7, chunks=2, warps=16, unroll=1)])
 @pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0"])
 def test_matvec_forced_pipelines(q, fmt, cfg):
-    """Small CTA counts and stages force many trips around the stage ring and a
-    ragged last stage; every output must still match."""
+    """Small CTA counts and rings force many trips around each row group's
+    ring, shared pieces and ragged last pieces; every output must still match."""
     rows, k = 61, 512
     st = synth.Stream(17)
     w = GEN[fmt](st, rows, k)
@@ -105,6 +106,38 @@ def test_matvec_forced_pipelines(q, fmt, cfg):
     y = run_matvec(q, fmt, w, x, rows, k, cfg=cfg)
     assert not np.any(np.isnan(y))
     assert scale_rel(oracle.qmv(fmt, w, x, rows, k), y) <= SCALE_REL_TOL
+
+
+@pytest.mark.parametrize("cfg", [dict(ctas=1, chunk_rows=3, chunks=2), dict(ctas=2, chunk_rows=1, chunks=1),
+                                 dict(ctas=3, chunk_rows=2, chunks=3, unroll=1), dict(ctas=1, chunks=2, warps=16)])
+@pytest.mark.parametrize("fmt,k", [("q4k", 4352), ("q6k", 2816), ("q8_0", 4096), ("q4k", 16384)])
+def test_matvec_forced_pipelines_wide(q, fmt, k, cfg):
+    """Rows of several k-slices: the warps of a row group share every piece and
+    the last one to finish re-fills the slot; ragged slices and pieces."""
+    rows = 29
+    st = synth.Stream(k + 5)
+    w = GEN[fmt](st, rows, k)
+    x = synth.gen_normal(st, k)
+    y = run_matvec(q, fmt, w, x, rows, k, cfg=cfg)
+    assert not np.any(np.isnan(y))
+    assert scale_rel(oracle.qmv(fmt, w, x, rows, k), y) <= SCALE_REL_TOL
+
+
+@pytest.mark.parametrize("cluster", [2, 4, 8])
+@pytest.mark.parametrize("fmt,rows,k", [("q4k", 97, 4352), ("q6k", 41, 2048), ("q8_0", 64, 1024)])
+def test_matvec_cluster_shared_prep(q, fmt, rows, k, cluster):
+    """CTAs of a cluster each convert part of x and write it into every
+    member's shared memory: results must match, and equal the unclustered
+    ones bit for bit (the same limbs, the same order of sums)."""
+    st = synth.Stream(k + cluster)
+    w = GEN[fmt](st, rows, k)
+    x = synth.gen_normal(st, k)
+    cfg = dict(ctas=8, cluster=cluster)
+    assert q.qmv_plan_info({"q4k": 0, "q6k": 1, "q8_0": 2}[fmt], rows, k, cfg=cfg)["ctas"] % cluster == 0
+    y = run_matvec(q, fmt, w, x, rows, k, cfg=cfg)
+    y1 = run_matvec(q, fmt, w, x, rows, k, cfg=dict(ctas=8))
+    assert scale_rel(oracle.qmv(fmt, w, x, rows, k), y) <= SCALE_REL_TOL
+    assert np.array_equal(y, y1)
 
 
 @pytest.mark.parametrize("fmt,rows,k", [("q4k", 64, 1024), ("q6k", 24, 768), ("q8_0", 40, 256),
@@ -197,7 +230,7 @@ def test_blockdots_bit_exact(q, rows, k):
     assert np.array_equal(host(dots), oracle.q8_blockdots(w, xq.reshape(-1), rows, k))
 
 
-@pytest.mark.parametrize("rows,k,cfg", [(300, 4096, None), (61, 256, dict(ctas=2, stage_rows=3, stages=2)),
+@pytest.mark.parametrize("rows,k,cfg", [(300, 4096, None), (61, 256, dict(ctas=2, chunk_rows=3, chunks=2)),
                                         (5, 32, None)])
 def test_dp4a_matvec(q, rows, k, cfg):
     st = synth.Stream(99 + rows)
@@ -244,7 +277,7 @@ def test_moe_gather_exact(q):
     for j in [0, 77, 511]:
         x = np.zeros((len(ids), k), dtype=np.float32)
         x[:, j] = 1.0
-        y = moe_run(q, bank, x, ids, n, k, e, cfg=dict(ctas=2, stage_rows=3, stages=2))
+        y = moe_run(q, bank, x, ids, n, k, e, cfg=dict(ctas=2, chunk_rows=3, chunks=2))
         for s, eid in enumerate(ids):
             assert np.array_equal(y[s], W[eid, :, j])
 

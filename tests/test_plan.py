@@ -1,0 +1,216 @@
+"""The launch planner without a GPU: for each shape (the five workloads, the
+GPU test shapes and forced configurations) the plan is taken from the library
+for a described GB300 and the kernel's work assignment is replayed here, so
+that every index the kernel forms is checked before it runs:
+
+* every (row, unit) pair of every matrix is decoded exactly once;
+* every shared-memory read of a unit (including the bytes a format's loads
+  read past its block) stays inside its ring slot, and every slot holds the
+  16-byte-aligned cover its bulk copy writes;
+* unit addresses have the alignment their loads need (16 bytes for Q4_K, 8 for
+  the aligned Q8_0 dp4a path, 2 otherwise);
+* parked partials stay inside the CTA's table, and the shared-memory regions
+  are disjoint and fit the device.
+
+The replay restates the kernel's arithmetic (qmv_kernel.cuh) in numpy; it is a
+check of index bounds, not of numerics."""
+
+import numpy as np
+import pytest
+
+DEVICE = (152, 232448, 233472, 1024)
+FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4}
+
+
+# Per format: weights per block, bytes per block, blocks per warp slice,
+# units per row, a unit's block offset in its slice, and the byte range a
+# unit's loads touch relative to its address a (lo may depend on a & 3).
+def fmt_info(fmt):
+    if fmt in ("q4k", "moe"):
+        return dict(qk=256, bb=144, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 144,
+                    extent=lambda a: (a, a + 144), align=16)
+    if fmt == "q6k":
+        return dict(qk=256, bb=210, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 210,
+                    extent=lambda a: (a - (a & 3), a - (a & 3) + 212), align=2)
+    if fmt == "q8_0":
+        return dict(qk=32, bb=34, sb=32, units=lambda nb: nb, ubyte=lambda u: u * 34,
+                    extent=lambda a: (a - (a & 3), a - (a & 3) + 40), align=2)
+    if fmt == "q8d":
+        # aligned path: [a, a + 136); block-by-block path: up to a + 142
+        return dict(qk=32, bb=34, sb=128, units=lambda nb: (nb + 3) // 4, ubyte=lambda u: u * 136,
+                    extent=lambda a: (a - (a & 3), a - (a & 3) + 144), align=2)
+    raise ValueError(fmt)
+
+
+@pytest.fixture(scope="module")
+def q():
+    import __graft_entry__
+    __graft_entry__.build()
+    import ggml_format_dequant_gb300 as lib
+    return lib
+
+
+def replay(q, fmt, rows, k, slots=1, cfg=None):
+    P = q.qmv_plan_detail(FMT_ID[fmt], rows, k, slots, cfg, DEVICE)
+    f = fmt_info(fmt)
+    nb = k // f["qk"]
+    U = f["units"](nb)
+    KS, GS, NG, CR, S, R, W = P["KS"], P["GS"], P["NG"], P["CR"], P["S"], P["unroll"], P["W"]
+    rowbytes, stride, parts = P["rowbytes"], P["slot_stride"], P["ctas"]
+    assert rowbytes == nb * f["bb"] and U == P["U"]
+    assert KS == (U + 31) // 32 and W == (KS if KS > 1 else 0) and GS & (GS - 1) == 0 and U <= KS * GS
+    assert 32 * NG * KS == P["threads"] <= 512
+    assert P["rq"] * parts + P["rrem"] == rows and 0 <= P["rrem"] < parts
+    # clusters share the activation prep: the CTAs of a matrix fill whole
+    # clusters, every CTA converts an even number of 16-element halves, and the
+    # integer-activation path has no prep to share
+    CL = P["CL"]
+    assert CL in (1, 2, 4, 8) and parts % CL == 0 and (k // 16) % (2 * CL) == 0
+    assert P["rq"] >= 1
+    if fmt == "q8d":
+        assert CL == 1
+    lg = GS.bit_length() - 1
+    rpw = 32 >> lg
+    aligned8 = P["aligned8"] == 1
+    if fmt == "q8d":
+        assert aligned8 == (rowbytes % 8 == 0)
+
+    # shared-memory layout: disjoint, ordered regions inside the device limit
+    regions = []
+    if fmt not in ("q8d",):
+        regions += [(P["off_la"], k), (P["off_lb"], k), (P["off_lc"], k), (P["off_xs"], 4 * (k // 32)),
+                    (P["off_xsum16"], 4 * (k // 16))]
+        for o, _ in regions:
+            assert o % 16 == 0
+    rpc = P["rq"] + (1 if P["rrem"] else 0)
+    regions += [(P["off_red"], 4 * rpc * W), (P["off_ring"], NG * S * stride), (P["off_bars"], 8 * NG * S),
+                (P["off_cnt"], 4 * (NG * S + NG + 1))]
+    regions.sort()
+    for (o1, n1), (o2, _) in zip(regions, regions[1:]):
+        assert o1 + n1 <= o2
+    assert regions[-1][0] + regions[-1][1] <= P["smem"] <= DEVICE[1]
+    assert P["off_ring"] % 128 == 0 and stride % 128 == 0 and P["off_bars"] % 8 == 0
+
+    lanes = np.arange(32)
+    covered = np.zeros((rows, U), dtype=np.int32)
+    for part in range(parts):
+        big = part < P["rrem"]
+        nrows = P["rq"] + (1 if big else 0)
+        R0 = part * P["rq"] + min(part, P["rrem"])
+        gq, grem = (P["gq1"], P["grem1"]) if big else (P["gq0"], P["grem0"])
+        assert gq * NG + grem == nrows
+        for rg in range(NG):
+            glo = rg * gq + min(rg, grem)
+            gn = gq + (1 if rg < grem else 0)
+            npc = -(-gn // CR)
+            for pc in range(npc):
+                nr = min(CR, gn - pc * CR)
+                rl0 = glo + pc * CR
+                gs = (R0 + rl0) * rowbytes          # the weight base is 16-byte aligned
+                d0 = gs & 15
+                a0, a1 = gs & ~15, (gs + nr * rowbytes + 15) & ~15
+                assert a1 - a0 <= stride               # the bulk copy's cover fits its slot
+                for ks in range(KS):
+                    u = (lanes & (GS - 1)) if KS == 1 else lanes
+                    sub = (lanes >> lg) if KS == 1 else np.zeros(32, dtype=int)
+                    ug = ks * 32 + u
+                    has = ug < U
+                    ubyte = ks * f["sb"] * f["bb"] + np.array([f["ubyte"](int(v)) for v in u])
+                    # R-row steps, then single steps for the remainder
+                    steps, jb = [], 0
+                    while jb + R * rpw <= nr:
+                        steps.append((jb, R))
+                        jb += R * rpw
+                    while jb < nr:
+                        steps.append((jb, 1))
+                        jb += rpw
+                    for jb, nq in steps:
+                        for qq in range(nq):
+                            j = jb + qq * rpw + sub
+                            valid = j < nr
+                            jj = np.where(valid, j, 0)
+                            a = d0 + jj * rowbytes + ubyte
+                            for ai in a[has]:
+                                lo, hi = f["extent"](int(ai))
+                                assert 0 <= lo and hi <= stride, (ai, lo, hi, stride)
+                                assert ai % f["align"] == 0
+                                if fmt == "q8d" and aligned8:
+                                    assert ai % 8 == 0
+                            sel = valid & has
+                            np.add.at(covered, (R0 + rl0 + j[sel], ug[sel]), 1)
+                            # parked slice sum of every valid row (rows of several slices)
+                            if KS > 1:
+                                idx = (rl0 + j[valid]) * W + ks
+                                assert idx.size == 0 or (idx.min() >= 0 and idx.max() < nrows * W)
+    assert np.all(covered == 1), np.argwhere(covered != 1)[:5]
+    return P
+
+
+WORKLOADS = [("q4k", 4096, 4096, 1), ("q4k", 256, 1024, 1), ("q8d", 14336, 4096, 1), ("q6k", 4096, 14336, 1),
+             ("moe", 768, 2048, 8)]
+
+
+@pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
+def test_workload_plans(q, fmt, rows, k, slots):
+    P = replay(q, fmt, rows, k, slots)
+    assert P["S"] >= 1
+    if (fmt, rows) in (("q4k", 4096), ("moe", 768)):
+        # the whole share in flight at once, in small CTAs that leave room for
+        # the next call's CTA on every SM
+        assert P["S"] == 1 and P["CR"] * P["NG"] >= P["rq"]
+        assert P["threads"] <= 256 and P["smem"] <= (DEVICE[2] - 2 * DEVICE[3]) // 2
+    if (fmt, rows) in (("q8d", 14336), ("q6k", 4096)):
+        # streamed through a ring at least two slots deep
+        assert P["S"] >= 2
+
+
+SHAPES = [("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 4352), ("q4k", 20, 16384), ("q6k", 300, 512),
+          ("q6k", 3, 256), ("q6k", 41, 14336), ("q6k", 130, 2816), ("q8_0", 300, 96), ("q8_0", 7, 4096),
+          ("q8_0", 13, 32), ("q8_0", 64, 11008), ("q8d", 300, 4096), ("q8d", 7, 96), ("q8d", 1, 32),
+          ("q8d", 61, 256), ("q8d", 5, 4160), ("moe", 96, 512, ), ("moe", 7, 256)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_shape_plans(q, shape):
+    fmt, rows, k = shape
+    replay(q, fmt, rows, k, 4 if fmt == "moe" else 1)
+
+
+CFGS = [dict(ctas=1, chunk_rows=1, chunks=2), dict(ctas=3, chunk_rows=5, chunks=2), dict(ctas=2, chunk_rows=3, chunks=1),
+        dict(ctas=7, chunks=3), dict(ctas=1, chunks=2, unroll=1), dict(ctas=3, chunk_rows=4, chunks=3, unroll=2),
+        dict(ctas=2, chunks=1, warps=2), dict(ctas=5, chunk_rows=2, chunks=4, warps=4),
+        dict(ctas=1, chunk_rows=7, chunks=2, warps=16, unroll=1)]
+
+
+@pytest.mark.parametrize("cfg", CFGS)
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q8d"])
+def test_forced_plans(q, fmt, cfg):
+    replay(q, fmt, 61, 512 if fmt != "q8d" else 256, 1, cfg)
+
+
+WIDE_CFGS = [dict(ctas=1, chunk_rows=3, chunks=2), dict(ctas=2, chunk_rows=1, chunks=1),
+             dict(ctas=3, chunk_rows=2, chunks=3, unroll=1), dict(ctas=1, chunks=2, warps=16)]
+
+
+@pytest.mark.parametrize("cfg", WIDE_CFGS)
+@pytest.mark.parametrize("fmt,k", [("q4k", 4352), ("q6k", 2816), ("q8_0", 4096), ("q4k", 16384)])
+def test_forced_wide_plans(q, fmt, k, cfg):
+    replay(q, fmt, 29, k, 1, cfg)
+
+
+def test_moe_forced_plan(q):
+    replay(q, "moe", 40, 512, 5, dict(ctas=2, chunk_rows=3, chunks=2))
+
+
+def test_chain_shapes(q):
+    for fmt in ("q4k", "q6k"):
+        replay(q, fmt, 2048, 2048)
+    replay(q, "moe", 2048, 2048, 2)
+
+
+def test_planner_rejects(q):
+    assert q.qmv_plan_detail.__name__
+    with pytest.raises(q.QmvError):
+        q.qmv_plan_detail(FMT_ID["q4k"], 10, 256 * 1024, 1, None, DEVICE)   # 64 k-slices per row
+    with pytest.raises(q.QmvError):
+        q.qmv_plan_detail(FMT_ID["q4k"], 10, 8192, 1, dict(warps=2), DEVICE)   # 4 slices, 2 warps
