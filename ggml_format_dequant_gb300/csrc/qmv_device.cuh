@@ -73,9 +73,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of the barrier to complete, giving up after
-// WAIT_LIMIT_NS. Returns false on timeout.
+// WAIT_LIMIT_NS. Returns false on timeout. A phase that is already complete
+// (the usual case when the data was requested long before) costs one test.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_test_wait(bar, parity)) return true;
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
@@ -277,13 +292,18 @@ __device__ __forceinline__ void prep_limbs(const float* __restrict__ x, int k, u
                                            int tid, int T, int CL, uint32_t rank) {
     const int nhc = (k >> 4) / CL;            // halves converted by this CTA
     const int h0 = static_cast<int>(rank) * nhc;
+    // Every CTA reads the same x: start each one at a different (even) offset
+    // so that their requests spread over the lines instead of all asking for
+    // the same line at once.
+    const int rot = static_cast<int>((blockIdx.x * 64u) % static_cast<unsigned>(nhc));
     const uint32_t sbase = smem_u32(smem);
     const float4* __restrict__ x4 = reinterpret_cast<const float4*>(x) + 4 * h0;
     for (int base = 0; base < nhc; base += BATCH * T) {
         float4 v[BATCH][4];
 #pragma unroll
         for (int b = 0; b < BATCH; b++) {
-            const int hl = base + b * T + tid;
+            int hl = base + b * T + tid;
+            hl = (hl < nhc) ? (hl + rot < nhc ? hl + rot : hl + rot - nhc) : nhc;
 #pragma unroll
             for (int m = 0; m < 4; m++)
                 v[b][m] = (hl < nhc) ? __ldg(x4 + 4 * hl + m) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -291,7 +311,8 @@ __device__ __forceinline__ void prep_limbs(const float* __restrict__ x, int k, u
 #pragma unroll
         for (int b = 0; b < BATCH; b++) {
             if (base + b * T >= nhc) break;   // uniform: nhc and T are even, so partners stay together
-            const int hl = base + b * T + tid;
+            int hl = base + b * T + tid;      // rotated like the loads (rot even: partners stay partners)
+            hl = (hl < nhc) ? (hl + rot < nhc ? hl + rot : hl + rot - nhc) : nhc;
             uint32_t mx = 0;
 #pragma unroll
             for (int m = 0; m < 4; m++)

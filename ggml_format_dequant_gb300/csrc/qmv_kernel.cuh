@@ -236,11 +236,16 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         const int sub = (p.KS == 1) ? (lane >> p.lgGS) : 0;   // which of the side-by-side rows
         const int ug = ks * 32 + u;                 // unit index within the row
         const bool has_unit = ug < p.U;
+        // Lanes past the row's last unit decode that unit too (valid data and
+        // activation) and drop the result, so every dot is unconditional and
+        // the unrolled dots of a step can be interleaved.
+        const int ugc = has_unit ? ug : p.U - 1;
+        const int uc = ugc - ks * 32;
         const int rpw = 32 >> p.lgGS;               // rows side by side in a warp step
         typename F::X xr;
-        const typename F::L lc = F::lane_consts(u, p.nb, ug);
-        if (has_unit) {
-            const int e0 = ks * F::SLICE_BLOCKS * F::QK + F::unit_elem(u);
+        const typename F::L lc = F::lane_consts(uc, p.nb, ugc);
+        {
+            const int e0 = ks * F::SLICE_BLOCKS * F::QK + F::unit_elem(uc);
             if constexpr (F::LIMBS)
                 F::load_x(xr, smem, p.lt, e0);
             else
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         }
         // Byte offset of the lane's unit inside a row, and 16-byte phase of the
         // group's rows in memory (pieces may start off a 16-byte boundary).
-        const uint32_t ubyte = static_cast<uint32_t>(ks) * (F::SLICE_BLOCKS * F::BLOCK_BYTES) + F::unit_byte(u);
+        const uint32_t ubyte = static_cast<uint32_t>(ks) * (F::SLICE_BLOCKS * F::BLOCK_BYTES) + F::unit_byte(uc);
         const uint32_t gphase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(wbase)) +
                                 static_cast<uint32_t>(R0 + glo) * p.rowbytes;
         const uint32_t piece_bytes = static_cast<uint32_t>(p.CR) * p.rowbytes;
@@ -285,7 +290,10 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
                 for (; jb + R * rpw <= nr; jb += R * rpw, a += R * rstep) {
                     float acc[R];
 #pragma unroll
-                    for (int q = 0; q < R; q++) acc[q] = has_unit ? dot_of<F>(a + q * rstep, lc, xr, aligned8) : 0.0f;
+                    for (int q = 0; q < R; q++) {
+                        acc[q] = dot_of<F>(a + q * rstep, lc, xr, aligned8);
+                        acc[q] = has_unit ? acc[q] : 0.0f;
+                    }
                     if constexpr (WIDE && R == 2) {
                         const float v = pair_sum(acc[0], acc[1], lane);
                         if ((lane & 15) == 0) store_row(rl0 + jb + (lane >> 4), v);
@@ -301,7 +309,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
                 // row lies past the piece decode row 0 and drop the result.
                 for (; jb < nr; jb += rpw, a += rstep) {
                     const bool valid = jb + sub < nr;
-                    float v = has_unit ? dot_of<F>(valid ? a : prow0, lc, xr, aligned8) : 0.0f;
+                    float v = dot_of<F>(valid ? a : prow0, lc, xr, aligned8);
+                    v = has_unit ? v : 0.0f;
                     v = group_sum<WIDE>(v, p.GS);
                     if (u == 0 && valid) store_row(rl0 + jb + sub, v);
                 }

@@ -115,7 +115,10 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
                     sub = (lanes >> lg) if KS == 1 else np.zeros(32, dtype=int)
                     ug = ks * 32 + u
                     has = ug < U
-                    ubyte = ks * f["sb"] * f["bb"] + np.array([f["ubyte"](int(v)) for v in u])
+                    # lanes past the last unit decode the last unit (result dropped)
+                    uc = np.where(has, u, U - 1 - ks * 32)
+                    assert np.all(uc >= 0)
+                    ubyte = ks * f["sb"] * f["bb"] + np.array([f["ubyte"](int(v)) for v in uc])
                     # R-row steps, then single steps for the remainder
                     steps, jb = [], 0
                     while jb + R * rpw <= nr:
@@ -130,7 +133,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
                             valid = j < nr
                             jj = np.where(valid, j, 0)
                             a = d0 + jj * rowbytes + ubyte
-                            for ai in a[has]:
+                            for ai in a:
                                 lo, hi = f["extent"](int(ai))
                                 assert 0 <= lo and hi <= stride, (ai, lo, hi, stride)
                                 assert ai % f["align"] == 0
