@@ -6,9 +6,14 @@ One step is one call of the hot path on the Q4_K 4096x4096 workload (rows =
 k = 4096, seed 1): qmv_q4k reads the packed weight straight from HBM, decodes
 it in registers and writes y. Consecutive steps cycle through enough distinct
 copies of the weight (more than 3x the L2 size in total) that every call reads
-its weight HBM-cold. The K timed steps are one CUDA-graph replay bracketed by
-CUDA events on the launching stream, with a barrier and a device synchronize
-on both sides; the line reports the max over ranks.
+its weight HBM-cold. The steps are independent (each reads the same x), and
+are launched as such (qmv_set_weight_prefetch mode 2: a call overlaps the
+previous one and waits for it only before writing y); ``--chain`` times a
+dependent decode chain instead (mode 1) and ``--isolated`` plain launches, and
+``per_config`` reports all three for every workload. The K timed steps are one
+CUDA-graph replay bracketed by CUDA events on the launching stream, with a
+barrier and a device synchronize on both sides; the line reports the max over
+ranks.
 
 The printed JSON line also carries the other four workloads of the suite
 (``per_config``), the roofline of the timed kernel against the measured HBM
@@ -48,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
 # qmv_q4k launch on the headline workload, valid only for the kernel sources
 # whose hash it is recorded under (profiles/qmv_stream_kernel_full_captures.md).
-NCU_TRAFFIC = {"d362b4a0dc730074": 9487104}
+NCU_TRAFFIC = {"15b0ed5706124965": 9488384}
 
 KERNEL_SOURCES = ["qmv_device.cuh", "qmv_formats.cuh", "qmv_kernel.cuh", "qmv_launch.cuh", "qmv_q4k.cu"]
 
@@ -284,9 +289,15 @@ def run_ours(args):
     sampler.start()
 
     # ------------------------------------------------ the headline workload
-    # Decode-chain mode: each call streams its (constant) weights while the
-    # previous call finishes (programmatic dependent launch); see qmv.h.
-    q.qmv_set_weight_prefetch(not args.isolated)
+    # The timed calls are independent of one another (every call reads the
+    # same x, like the Q / K / V projections of one activation), so they run
+    # in mode 2 of qmv_set_weight_prefetch: each call is scheduled while the
+    # previous one runs, streams its weights and decodes at once, and waits for
+    # the previous call only before it writes y. --chain times the
+    # conservative decode chain (mode 1: x is read only after the previous call
+    # is done), --isolated plain launches (mode 0); per_config reports all three.
+    head_mode = 0 if args.isolated else (1 if args.chain else 2)
+    q.qmv_set_weight_prefetch(head_mode)
     wl = Workload(q, torch, HEADLINE, l2, device)
     K, W = args.steps, args.warmup
     # warm-up steps (untimed)
@@ -334,7 +345,10 @@ def run_ours(args):
     e2e = end_to_end(torch, q, wl, device, K)
 
     # ------------------------------------------------ the other workloads
-    # every workload, chained (overlap on) and isolated (overlap off)
+    # every workload: a decode chain (mode 1, the headline's), isolated calls
+    # (mode 0), and a stream of independent calls (mode 2: the calls share no
+    # inputs with the call before, like the Q / K / V projections of one
+    # activation)
     per_config = {}
     del wl, gk, gw
     torch.cuda.empty_cache()
@@ -343,23 +357,25 @@ def run_ours(args):
         w2 = Workload(q, torch, name, l2, device)
         n = max(64, w2.copies)
         row = None
-        for chained in (True, False):
-            q.qmv_set_weight_prefetch(chained)
+        for mode in (1, 0, 2):
+            q.qmv_set_weight_prefetch(mode)
             ms, _, g2, _ = time_graph(torch, w2, n, replays=4)
             del g2
-            if chained:
+            tag = {1: "", 0: "isolated_", 2: "independent_"}[mode]
+            if mode == 1:
                 row = config_row(name, ms, peak, peak_kind, w2.copies)
             else:
-                row["isolated_us_per_call"] = round(ms * 1e3, 3)
-                row["isolated_packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
-            if w2.kind == "q8_0_dp4a":
+                row[tag + "us_per_call"] = round(ms * 1e3, 3)
+                row[tag + "packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
+                row[tag + "frac_of_measured_hbm"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9 / peak, 4)
+            if w2.kind == "q8_0_dp4a" and mode != 2:
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
-                row[("" if chained else "isolated_") + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
+                row[tag + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
                 del g3
         per_config[name] = row
         del w2
         torch.cuda.empty_cache()
-    q.qmv_set_weight_prefetch(False)
+    q.qmv_set_weight_prefetch(0)
     sampler.stop()
     clocks = sampler.summary(*clock_window)
     clocks["window"] = "nvidia-smi every 50 ms over a 0.5 s pre-roll, the timed region and a 0.5 s post-roll of the same graph"
@@ -386,9 +402,14 @@ def run_ours(args):
                 "l2": f"inputs larger than L2: {per_config[HEADLINE]['rotation_copies']} rotated weight copies "
                       f"({per_config[HEADLINE]['rotation_copies'] * wbytes / 2**20:.0f} MiB) vs L2 {l2 / 2**20:.0f} MiB",
                 "timing": "K calls captured in one CUDA graph, CUDA events on the launching stream",
-                "launch": ("isolated calls" if args.isolated else
-                           "decode chain: programmatic dependent launch, each call streams its weights while "
-                           "the previous call finishes (qmv_set_weight_prefetch)"),
+                "launch": {0: "isolated calls (qmv_set_weight_prefetch mode 0)",
+                           1: "dependent decode chain (mode 1): programmatic dependent launch, each call streams "
+                              "its weights while the previous call finishes, reads x after it",
+                           2: "independent calls (mode 2): programmatic dependent launch, each call streams its "
+                              "weights and decodes while the previous call finishes, writes y after it"}[head_mode],
+                "dependent_chain_us_per_call": per_config[HEADLINE]["us_per_call"],
+                "isolated_us_per_call": per_config[HEADLINE].get("isolated_us_per_call"),
+                "independent_us_per_call": per_config[HEADLINE].get("independent_us_per_call"),
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             },
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -554,6 +575,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="skip the per-config table")
+    ap.add_argument("--chain", action="store_true",
+                    help="time the headline as a dependent decode chain (mode 1)")
     ap.add_argument("--isolated", action="store_true",
                     help="time the headline without decode-chain overlap (programmatic dependent launch off)")
     ap.add_argument("--profile-workload", choices=list(synth.CONFIGS),

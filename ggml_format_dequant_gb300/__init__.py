@@ -195,9 +195,10 @@ def qmv_device_status(clear=True) -> int:
     return v.value
 
 
-def qmv_set_weight_prefetch(enable: bool) -> bool:
-    """Enable decode-chain overlap (see qmv.h); returns the previous setting."""
-    return bool(load().qmv_set_weight_prefetch(1 if enable else 0))
+def qmv_set_weight_prefetch(mode) -> int:
+    """Decode-chain overlap mode (see qmv.h): 0 off, 1 (or True) weights
+    requested early, 2 inputs read early too. Returns the previous mode."""
+    return int(load().qmv_set_weight_prefetch(int(mode)))
 
 
 def qmv_plan_info(fmt, rows, k, slots=1, cfg=None) -> dict:

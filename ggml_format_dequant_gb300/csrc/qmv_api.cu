@@ -129,9 +129,9 @@ const char* qmv_strerror(int code) {
     }
 }
 
-int qmv_set_weight_prefetch(int enable) {
+int qmv_set_weight_prefetch(int mode) {
     const int old = __atomic_load_n(&qmv::weight_prefetch_flag(), __ATOMIC_RELAXED);
-    __atomic_store_n(&qmv::weight_prefetch_flag(), enable ? 1 : 0, __ATOMIC_RELAXED);
+    __atomic_store_n(&qmv::weight_prefetch_flag(), mode <= 0 ? 0 : (mode >= 2 ? 2 : 1), __ATOMIC_RELAXED);
     return old;
 }
 

@@ -64,9 +64,10 @@ struct KParams {
     int S;                      // ring slots per row group
     int rq, rrem;               // rows per CTA: rq or rq + 1 (the first rrem CTAs)
     int gq[2], grem[2];         // rows per row group for a CTA of rq ([0]) or rq + 1 ([1]) rows
-    int W;                      // parked partials per row (KS when KS > 1)
+    int W;                      // parked sums per row: KS, or 1 (early inputs), or 0 (rows written at once)
     int aligned8;               // every unit starts 8-byte aligned in shared memory (Q8_0 dp4a)
     int CL;                     // CTAs per cluster sharing the activation prep (1: no cluster)
+    int early_inputs;           // x / ids may be read before waiting for the previous kernel (only y waits)
     uint32_t slot_stride;
     LimbTables lt;              // activation limb tables (f32-activation formats)
     uint32_t off_red;           // parked slice sums [rows of the CTA][W]
@@ -154,12 +155,14 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
     const uint8_t* wbase = p.w;
     const float* xrow = p.x;
     if (MOE) {
-        // ids may come from the kernel just before (the router).
-        pdl_dependency_wait();
+        // ids may come from the kernel just before (the router), unless the
+        // caller declared this call's inputs independent of it.
+        if (!p.early_inputs) pdl_dependency_wait();
         const int e = __ldg(p.ids + slot);
         if (e < 0 || e >= p.n_experts) {
             // Unroutable slot: NaN marks every output of it, and the status
             // word records the fact. No byte of the bank is touched.
+            pdl_dependency_wait();
             for (int r = R0 + tid; r < R0 + nrows; r += blockDim.x) p.y[yoff + r] = __int_as_float(0x7fc00000);
             if (tid == 0) atomicOr(&g_status, STATUS_BAD_EXPERT_ID);
             return;
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
 
     // The packed weights are constant, so they were requested above without
     // waiting for the previous kernel; x (and y, written below) may be shared
-    // with it.
-    if (!MOE) pdl_dependency_wait();
+    // with it. With early inputs only the writes of y wait (at the end).
+    if (!MOE && (!p.early_inputs || MODE == MODE_BLOCKDOTS)) pdl_dependency_wait();
 
     if constexpr (F::LIMBS) {
         // The activation limb tables, shared among the CTAs of a cluster (all
@@ -259,12 +262,13 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         const uint32_t piece_bytes = static_cast<uint32_t>(p.CR) * p.rowbytes;
         const uint32_t rstep = static_cast<uint32_t>(rpw) * p.rowbytes;   // bytes between warp steps
         const bool aligned8 = p.aligned8 != 0;
-        // A finished row sum: to y (rows of one slice) or parked by slice.
+        // A finished row sum: to y (rows of one slice, no early inputs) or
+        // parked by slice until the CTA is done.
         auto store_row = [&](int rl, float v) {
-            if (p.KS == 1)
+            if (p.W == 0)
                 p.y[yoff + R0 + rl] = v;
             else
-                red[rl * p.KS + ks] = v;
+                red[rl * p.W + ks] = v;
         };
 
         int s = 0;
@@ -361,11 +365,13 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         return;
     }
 
-    if (MODE == MODE_MATVEC && p.KS > 1) {
-        // Rows spanning several k-slices: add the slice sums in slice order.
+    if (MODE == MODE_MATVEC && p.W > 0) {
+        // Parked rows (several k-slices, or early inputs): add the slice sums
+        // in slice order, once the previous kernel is done with y.
+        if (p.early_inputs) pdl_dependency_wait();
         for (int r = tid; r < nrows; r += blockDim.x) {
             float v = 0.0f;
-            for (int q = 0; q < p.KS; q++) v += red[r * p.KS + q];
+            for (int q = 0; q < p.W; q++) v += red[r * p.W + q];
             p.y[yoff + R0 + r] = v;
         }
     }

@@ -31,8 +31,10 @@ inline int cuda_rc(cudaError_t e) {
     return QMV_ECUDA;
 }
 
-// Process-wide opt-in: launch with programmatic stream serialization so a call
-// streams its packed weights while the previous kernel on the stream finishes.
+// Process-wide decode-chain mode (qmv_set_weight_prefetch): 0 plain launches;
+// 1 programmatic dependent launch, packed weights requested before waiting for
+// the previous kernel; 2 also x / ids read early (the caller guarantees that
+// the previous kernel writes none of this call's inputs; y still waits).
 inline int& weight_prefetch_flag() {
     static int f = 0;
     return f;
@@ -113,7 +115,9 @@ inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qm
     Plan P;
     // CTAs per matrix: one per SM (MoE: the SMs are shared by the slots), but
     // not more than there are rows, and enough that the parked partials fit.
-    const int W = KS > 1 ? KS : 0;   // parked slice sums per row
+    const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
+    const int early = mode >= 2 ? 1 : 0;
+    const int W = KS > 1 ? KS : early;   // parked slice sums per row
     if (cfg && cfg->ctas > 0) {
         P.parts = cfg->ctas;
     } else {
@@ -257,6 +261,7 @@ inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qm
     kp->slot_stride = static_cast<uint32_t>(stride);
     kp->aligned8 = (rowbytes % 8 == 0) ? 1 : 0;
     kp->CL = P.CL;
+    kp->early_inputs = early;
     // Balanced splits, precomputed so the kernel only multiplies.
     kp->rq = rows / P.parts;
     kp->rrem = rows % P.parts;

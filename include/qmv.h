@@ -100,15 +100,21 @@ int qmv_q8_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int 
 int moe_qmv_q4k(const void *w_bank, const float *x, float *y, int rows, int k,
                 const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
 
-/* Decode-chain overlap (off by default; process-wide). When enabled, every
- * matvec launch allows programmatic dependent launch: a call may be scheduled
- * while the previous kernel on the same stream is still running and starts
- * streaming its packed weights at once, but it waits for that kernel to finish
- * before it reads x (or, for MoE, ids) and before it writes y. Only enable it
- * if the packed weights of a call are never written by the kernel launched just
- * before it on the stream (true for inference, where weights are constant).
- * Returns the previous setting. */
-int qmv_set_weight_prefetch(int enable);
+/* Decode-chain overlap (process-wide; 0 by default).
+ * mode 1: every matvec launch allows programmatic dependent launch: a call may
+ *   be scheduled while the previous kernel on the same stream is still running
+ *   and starts streaming its packed weights at once, but it waits for that
+ *   kernel to finish before it reads x (or, for MoE, ids) and before it writes
+ *   y. Only use it if the packed weights of a call are never written by the
+ *   kernel launched just before it on the stream (true for inference, where
+ *   weights are constant).
+ * mode 2: as mode 1, and x and ids are read (and the whole product computed)
+ *   before that wait; only the writes of y wait for the previous kernel. Only
+ *   use it when the kernel launched just before writes none of this call's
+ *   inputs, e.g. consecutive projections of one activation (Q, K and V; gate
+ *   and up).
+ * mode 0: plain launches. Returns the previous mode. */
+int qmv_set_weight_prefetch(int mode);
 
 /* Name of a QMV_* return code. Never NULL. */
 const char *qmv_strerror(int code);

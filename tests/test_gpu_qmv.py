@@ -405,3 +405,43 @@ def test_weight_prefetch_chain_matches(q):
     finally:
         q.qmv_set_weight_prefetch(old)
     assert torch.isfinite(ref[-1]).all()
+
+
+def test_independent_inputs_mode_matches(q):
+    """Mode 2 (inputs read before the dependency wait): a stream of calls that
+    share one activation (like Q, K, V projections), with every output buffer
+    reused by the next-but-one call, must give bitwise the results of plain
+    launches; the MoE call reads ids written long before."""
+    n = 2048
+    st = synth.Stream(78)
+    ws = [dev(synth.gen_q4k_rows(st, n, n)) for _ in range(5)]
+    w6 = dev(synth.gen_q6k_rows(st, n, n))
+    bank = dev(synth.gen_q4k_rows(st, 8 * n, n))
+    x = dev(synth.gen_normal(st, n))
+    xm = dev(synth.gen_normal(st, 2 * n).reshape(2, n))
+    ids = dev(np.array([3, 6], dtype=np.int32))
+    torch.cuda.synchronize()
+
+    def stream_of_calls():
+        bufs = [torch.full((n,), float("nan"), device="cuda") for _ in range(2)]
+        outs = []
+        for i, w in enumerate(ws):
+            q.qmv_q4k(w, x, bufs[i % 2], n, n)
+            outs.append(bufs[i % 2].clone())   # a torch kernel between calls
+        q.qmv_q6k(w6, x, bufs[0], n, n)
+        ym = torch.empty(2, n, device="cuda")
+        q.moe_qmv_q4k(bank, xm, ym, n, n, ids, 2, 8)
+        torch.cuda.synchronize()
+        return outs + [bufs[0].clone(), ym.clone()]
+
+    old = q.qmv_set_weight_prefetch(0)
+    try:
+        ref = stream_of_calls()
+        for mode in (2, 1, 2):
+            q.qmv_set_weight_prefetch(mode)
+            got = stream_of_calls()
+            for a, b in zip(ref, got):
+                assert torch.equal(a, b)
+    finally:
+        q.qmv_set_weight_prefetch(old)
+    assert all(torch.isfinite(t).all() for t in ref)
