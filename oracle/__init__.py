@@ -75,6 +75,8 @@ def _lib():
             L.orc_quantize_act_q8.argtypes = [P, lg, lg, P, P, P]
             L.orc_q8_blockdots.argtypes = [P, P, lg, lg, P]
             L.orc_qmv_q8_dp4a.argtypes = [P, P, P, lg, lg, P]
+            L.orc_q4k_dp4a_blockdots.argtypes = [P, P, lg, lg, P]
+            L.orc_qmv_q4k_dp4a.argtypes = [P, P, P, lg, lg, P]
             _LIB = L
     return _LIB
 
@@ -175,6 +177,28 @@ def qmv_q8_dp4a(w, xq, xs, rows: int, k: int) -> np.ndarray:
     xs = _f32(xs)
     y = np.empty(rows, dtype=np.float64)
     rc = _lib().orc_qmv_q8_dp4a(_p(w), _p(xq), _p(xs), rows, k, _p(y))
+    assert rc == 0
+    return y
+
+
+def q4k_dp4a_blockdots(w, xq, rows: int, k: int) -> np.ndarray:
+    """Exact int32 dots [rows, k/32] of every 32-weight Q4_K sub-block's 4-bit
+    codes with the int8 activation codes of the same positions."""
+    w = _u8(w)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    dots = np.empty((rows, k // 32), dtype=np.int32)
+    rc = _lib().orc_q4k_dp4a_blockdots(_p(w), _p(xq), rows, k, _p(dots))
+    assert rc == 0
+    return dots
+
+
+def qmv_q4k_dp4a(w, xq, xs, rows: int, k: int) -> np.ndarray:
+    """Q4_K dp4a-path matvec in f64: y[r] = sum_t xs_t (d sc dot_t - dmin m sumq_t)."""
+    w = _u8(w)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xs = _f32(xs)
+    y = np.empty(rows, dtype=np.float64)
+    rc = _lib().orc_qmv_q4k_dp4a(_p(w), _p(xq), _p(xs), rows, k, _p(y))
     assert rc == 0
     return y
 

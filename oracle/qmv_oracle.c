@@ -315,3 +315,65 @@ int orc_qmv_q8_dp4a(const uint8_t *w, const int8_t *xq, const float *xs, long ro
     }
     return 0;
 }
+
+/* ------------------------------------------- Q4_K x q8 activation (dp4a) -- */
+
+/* The dense dp4a Q4_K matvec of hanzo-ml src/vulkan_backend.rs (the
+ * `matvec_q4k_dp4a_blk` dispatch in the decode path): the activation is
+ * quantized to int8 codes with one f32 scale per 32 values (quantize_act_q8),
+ * and every 32-weight Q4_K sub-block is dotted, as integers, with the 32 codes
+ * of the same positions. One sub-block's exact integer dot of its 4-bit codes
+ * with the activation codes: */
+static long q4k_subblock_dot(const uint8_t *b, int j, const int8_t *xq32) {
+    const uint8_t *qs = b + 16 + 32 * (j / 2);
+    long dot = 0;
+    for (int l = 0; l < 32; l++) {
+        int q = (j % 2 == 0) ? (qs[l] & 15) : (qs[l] >> 4);
+        dot += (long)q * (long)xq32[l];
+    }
+    return dot;
+}
+
+/* dots[r, t] = integer dot of the 32-weight sub-block t of row r (t = 8 *
+ * block + j) with xq[32t .. 32t + 31]. */
+int orc_q4k_dp4a_blockdots(const uint8_t *w, const int8_t *xq, long rows, long k, int32_t *dots) {
+    if (k % ORC_QK_K) return -1;
+    long nb = k / ORC_QK_K;
+    for (long r = 0; r < rows; r++)
+        for (long bi = 0; bi < nb; bi++) {
+            const uint8_t *b = w + (r * nb + bi) * ORC_Q4K_BYTES;
+            for (int j = 0; j < 8; j++) {
+                long t = bi * 8 + j;
+                dots[r * (k / 32) + t] = (int32_t)q4k_subblock_dot(b, j, xq + 32 * t);
+            }
+        }
+    return 0;
+}
+
+/* y[r] = sum over sub-blocks t of  xs[t] * (d*sc_j*dot_t - dmin*m_j*sumq_t),
+ * with sumq_t the integer sum of the activation codes of sub-block t: the
+ * weights w = d*sc*q - dmin*m against the dequantized activation xs*xq, in f64
+ * with exact integer dots. */
+int orc_qmv_q4k_dp4a(const uint8_t *w, const int8_t *xq, const float *xs, long rows, long k, double *y) {
+    if (k % ORC_QK_K) return -1;
+    long nb = k / ORC_QK_K;
+    for (long r = 0; r < rows; r++) {
+        double acc = 0.0;
+        for (long bi = 0; bi < nb; bi++) {
+            const uint8_t *b = w + (r * nb + bi) * ORC_Q4K_BYTES;
+            double d = orc_f16_to_f64(rd_le16(b));
+            double dmin = orc_f16_to_f64(rd_le16(b + 2));
+            for (int j = 0; j < 8; j++) {
+                long t = bi * 8 + j;
+                int sc, m;
+                q4k_scale_min(j, b + 4, &sc, &m);
+                long dot = q4k_subblock_dot(b, j, xq + 32 * t);
+                long sumq = 0;
+                for (int l = 0; l < 32; l++) sumq += xq[32 * t + l];
+                acc += (double)xs[t] * (d * sc * (double)dot - dmin * m * (double)sumq);
+            }
+        }
+        y[r] = acc;
+    }
+    return 0;
+}

@@ -348,6 +348,51 @@ def test_dp4a_matvec_closed_form():
     assert np.max(np.abs(y - yf)) <= 0.05 * np.max(np.abs(yf)) + 1e-6
 
 
+def test_q4k_dp4a_blockdots_of_known_codes():
+    """Blocks built by the inverse of the layout with d = 1, dmin = 0 and all
+    scales 1 decode (by the pinned decoder) to their codes, so every
+    sub-block dot must be that decoded matrix times the activation codes."""
+    rng = np.random.default_rng(11)
+    rows, k = 3, 512
+    blocks = []
+    for _ in range(rows * (k // 256)):
+        q = rng.integers(0, 16, size=256)
+        blocks.append(pack_q4k(f16_bits(1.0), 0, [1] * 8, [0] * 8, q))
+    w = np.concatenate(blocks)
+    W = oracle.dequant("q4k", w, rows, k)
+    assert np.all(W == np.round(W)) and W.min() >= 0 and W.max() <= 15
+    xq = rng.integers(-127, 128, size=k).astype(np.int8)
+    dots = oracle.q4k_dp4a_blockdots(w, xq, rows, k)
+    ref = (W.astype(np.int64) * xq.astype(np.int64)).reshape(rows, k // 32, 32).sum(2)
+    assert np.array_equal(dots, ref)
+    # a single code 127 at position j isolates column j of the codes
+    for j in [0, 31, 32, 63, 64, 200, 511]:
+        e = np.zeros(k, dtype=np.int8)
+        e[j] = 127
+        d1 = oracle.q4k_dp4a_blockdots(w, e, rows, k)
+        assert np.array_equal(d1[:, j // 32], 127 * W[:, j].astype(np.int64))
+        assert np.count_nonzero(np.delete(d1, j // 32, axis=1)) == 0
+
+
+def test_q4k_dp4a_matvec_is_the_matvec_of_the_dequantized_activation():
+    """With scales and mins, the dp4a-path matvec equals (to f64 rounding) the
+    pinned f64 matvec of the decoded weights against xs * xq; a swapped scale
+    and min, a dropped min term or a wrong sub-block would not."""
+    rows, k = 5, 768
+    st = synth.Stream(21)
+    w = synth.gen_q4k_rows(st, rows, k)
+    x = synth.gen_normal(st, k)
+    xq, xs, _ = oracle.quantize_act_q8(x, 1, k)
+    xq, xs = xq.reshape(-1), xs.reshape(-1)
+    xhat = xs.astype(np.float64).repeat(32) * xq.astype(np.float64)
+    ref = oracle.dequant("q4k", w, rows, k) @ xhat
+    y = oracle.qmv_q4k_dp4a(w, xq, xs, rows, k)
+    assert np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref))
+    # and it approximates the f32-activation matvec to within the q8 error
+    yf = oracle.qmv("q4k", w, x, rows, k)
+    assert np.max(np.abs(y - yf)) <= 0.05 * np.max(np.abs(yf))
+
+
 # ------------------------------------------------------------------------ MoE
 
 def test_moe_matches_dense_per_expert_and_flags_bad_ids():
