@@ -78,7 +78,7 @@ def measured_peak():
 
 def weight_bytes(name: str) -> int:
     c = synth.CONFIGS[name]
-    if c["kind"] == "q4k":
+    if c["kind"] in ("q4k", "q4k_dp4a"):
         return synth.row_bytes("q4k", c["k"]) * c["rows"]
     if c["kind"] == "q6k":
         return synth.row_bytes("q6k", c["k"]) * c["rows"]
@@ -96,7 +96,7 @@ def algorithmic_bytes(name: str) -> int:
     wb = weight_bytes(name)
     if c["kind"] == "moe_q4k":
         return wb + 4 * c["slots"] * c["k"] + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
-    if c["kind"] == "q8_0_dp4a":
+    if c["kind"] in ("q8_0_dp4a", "q4k_dp4a"):
         return wb + c["k"] + 4 * (c["k"] // 32) + 4 * c["rows"]
     return wb + 4 * c["k"] + 4 * c["rows"]
 
@@ -195,7 +195,7 @@ class Workload:
                 self.ids.append(torch.from_numpy(synth.gen_moe_ids(st, c["slots"], c["n_experts"])).to(dev))
         else:
             self.y = torch.empty(self.rows, dtype=torch.float32, device=dev)
-        if self.kind == "q8_0_dp4a":
+        if self.kind in ("q8_0_dp4a", "q4k_dp4a"):
             self.xq = torch.empty(self.k, dtype=torch.int8, device=dev)
             self.xs = torch.empty(self.k // 32, dtype=torch.float32, device=dev)
             q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k)
@@ -209,12 +209,13 @@ class Workload:
             q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
         elif self.kind == "q6k":
             q.qmv_q6k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
-        elif self.kind == "q8_0_dp4a":
+        elif self.kind in ("q8_0_dp4a", "q4k_dp4a"):
             n = 1
             if with_quant:
                 q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k, stream=stream)
                 n = 2
-            q.qmv_q8_dp4a(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg)
+            fn = q.qmv_q8_dp4a if self.kind == "q8_0_dp4a" else q.qmv_q4k_dp4a
+            fn(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg)
             return n
         elif self.kind == "moe_q4k":
             c = self.c
@@ -368,7 +369,7 @@ def run_ours(args):
                 row[tag + "us_per_call"] = round(ms * 1e3, 3)
                 row[tag + "packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
                 row[tag + "frac_of_measured_hbm"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9 / peak, 4)
-            if w2.kind == "q8_0_dp4a" and mode != 2:
+            if w2.kind in ("q8_0_dp4a", "q4k_dp4a") and mode != 2:
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
                 row[tag + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
                 del g3

@@ -79,6 +79,20 @@ int qmv_q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int 
     return qmv_q8_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
 }
 
+int qmv_q4k_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                     const qmv_cfg* cfg, cudaStream_t stream) {
+    if (!xs) return QMV_EINVAL;
+    int rc = check_dense(w, xq, y, rows, k, 256, 144);
+    if (rc) return rc;
+    if (!aligned(xq, 16) || !aligned(xs, 4)) return QMV_EALIGN;
+    return qmvi::q4k_dp4a(w, xq, xs, y, rows, k, cfg, stream);
+}
+
+int qmv_q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                 cudaStream_t stream) {
+    return qmv_q4k_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
+}
+
 int moe_qmv_q4k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids,
                     int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
     int rc = check_dense(w_bank, x, y, rows, k, 256, 144);
@@ -118,6 +132,13 @@ int qmv_q8_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int ro
     return qmvi::q8_blockdots(w, xq, dots, rows, k, stream);
 }
 
+int qmv_q4k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, xq, dots, rows, k, 256, 144);
+    if (rc) return rc;
+    if (!aligned(xq, 16)) return QMV_EALIGN;
+    return qmvi::q4k_dp4a_blockdots(w, xq, dots, rows, k, stream);
+}
+
 const char* qmv_strerror(int code) {
     switch (code) {
     case QMV_OK: return "ok";
@@ -155,8 +176,8 @@ namespace {
 // Plan of format fmt on device `di`.
 int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_cfg* cfg, qmv::KParams* kp,
             qmv::Plan* pl) {
-    static const int qk[5] = {256, 256, 32, 32, 256};
-    if (fmt < 0 || fmt > 4 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
+    static const int qk[6] = {256, 256, 32, 32, 256, 256};
+    if (fmt < 0 || fmt > 5 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
     if (fmt == 4 && slots <= 0) return QMV_EINVAL;
     if (fmt != 4) slots = 1;
     switch (fmt) {
@@ -164,6 +185,7 @@ int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const q
     case 1: return qmv::make_plan_for<qmv::Q6K>(di, rows, k, 1, cfg, kp, pl);
     case 2: return qmv::make_plan_for<qmv::Q8F>(di, rows, k, 1, cfg, kp, pl);
     case 3: return qmv::make_plan_for<qmv::Q8D>(di, rows, k, 1, cfg, kp, pl);
+    case 5: return qmv::make_plan_for<qmv::Q4D>(di, rows, k, 1, cfg, kp, pl);
     default: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, slots, cfg, kp, pl);
     }
 }

@@ -139,6 +139,107 @@ struct Q4K {
     }
 };
 
+// ============================================================ Q4_K, q8 activation
+//
+// The dp4a path of Q4_K (hanzo-ml src/vulkan_backend.rs, the dense
+// `matvec_q4k_dp4a_blk` decode): the activation is int8 codes with one f32
+// scale xs per 32 values (quantize_act_q8). A unit is one 64-weight chunk as in
+// Q4K; its two sub-blocks' integer dots with the codes give
+//     xs_j * (d*sc_j * dot_j - dmin*m_j * sumq_j)
+// with sumq_j the sum of the sub-block's activation codes, which the lane forms
+// once from its codes (no separate sum input is needed).
+struct Q4D {
+    static constexpr int QK = 256;
+    static constexpr int BLOCK_BYTES = 144;
+    static constexpr int SLICE_BLOCKS = 8;    // 32 units (1152 bytes)
+    static constexpr int SLACK = 0;
+    static constexpr bool LIMBS = false;
+    static constexpr int DEFAULT_UNROLL = 2;
+    static constexpr int DOTS_PER_UNIT = 2;   // 32-weight sub-blocks per unit
+
+    __host__ __device__ static int units(int nb) { return 4 * nb; }
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u >> 2) * BLOCK_BYTES; }
+    __device__ __forceinline__ static int unit_elem(int u) { return (u >> 2) * QK + 64 * (u & 3); }
+
+    struct X {
+        uint32_t q[16];        // codes of the chunk's 64 activations (sub-block 2c, then 2c+1)
+        float xs0, xs1;        // their scales
+        float xm0, xm1;        // xs_j * (sum of the sub-block's codes)
+    };
+    using L = Q4K::L;
+    __device__ __forceinline__ static L lane_consts(int u, int nb, int ug) { return Q4K::lane_consts(u, nb, ug); }
+
+    // e0 = index of the chunk's first activation in the row.
+    __device__ __forceinline__ static void load_xq(X& x, const L&, const int8_t* __restrict__ xq,
+                                                   const float* __restrict__ xs, int e0) {
+        const uint4* v = reinterpret_cast<const uint4*>(xq + e0);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint4 t = __ldg(v + i);
+            x.q[4 * i] = t.x; x.q[4 * i + 1] = t.y; x.q[4 * i + 2] = t.z; x.q[4 * i + 3] = t.w;
+        }
+        x.xs0 = __ldg(xs + (e0 >> 5));
+        x.xs1 = __ldg(xs + (e0 >> 5) + 1);
+        int s0 = 0, s1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            s0 = dp4a_ss(0x01010101u, x.q[i], s0);
+            s1 = dp4a_ss(0x01010101u, x.q[8 + i], s1);
+        }
+        x.xm0 = x.xs0 * __int2float_rn(s0);
+        x.xm1 = x.xs1 * __int2float_rn(s1);
+    }
+
+    // The two sub-blocks' exact dots (the high nibbles enter as 16 q, so the
+    // second sum is divided by 16, exactly).
+    __device__ __forceinline__ static void subblock_dots(uint32_t a, const L& l, const X& x, int& dot0, int& dot1) {
+        const uint32_t aq = a + l.qoff;
+        const uint4 qa = lds128<0>(aq);
+        const uint4 qb = lds128<16>(aq);
+        const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        int s0 = 0, s1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            s0 = dp4a_us(q[i] & 0x0f0f0f0fu, x.q[i], s0);
+            s1 = dp4a_us(q[i] & 0xf0f0f0f0u, x.q[8 + i], s1);
+        }
+        dot0 = s0;
+        dot1 = s1 >> 4;
+    }
+
+    // a: shared address of the super-block (16-byte aligned).
+    __device__ __forceinline__ static float dot(uint32_t a, const L& l, const X& x, float r, bool) {
+        const uint4 h = lds128<0>(a);
+        int dot0, dot1;
+        subblock_dots(a, l, x, dot0, dot1);
+        const uint32_t sc_lo = h.y & 0x3f3f3f3fu;
+        const uint32_t m_lo = h.z & 0x3f3f3f3fu;
+        const uint32_t sc_hi = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
+        const uint32_t m_hi = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+        const uint32_t SC = l.hic ? sc_hi : sc_lo;
+        const uint32_t M = l.hic ? m_hi : m_lo;
+        const float d = f16_lo(h.x), dmin = f16_hi(h.x);
+        const float nd = -d * TWO23, ndm = -dmin * TWO23;
+        const float dsc0 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel)), nd);
+        const float dsc1 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel + 1)), nd);
+        const float dm0 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel)), ndm);
+        const float dm1 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel + 1)), ndm);
+        r = __fmaf_rn(dsc0, __int2float_rn(dot0) * x.xs0, r);
+        r = __fmaf_rn(-dm0, x.xm0, r);
+        r = __fmaf_rn(dsc1, __int2float_rn(dot1) * x.xs1, r);
+        r = __fmaf_rn(-dm1, x.xm1, r);
+        return r;
+    }
+
+    // The exact int32 dots of the unit's two sub-blocks (MODE_BLOCKDOTS).
+    __device__ __forceinline__ static void block_dots(uint32_t a, const L& l, const X& x, bool, int32_t* out) {
+        int dot0, dot1;
+        subblock_dots(a, l, x, dot0, dot1);
+        out[0] = dot0;
+        out[1] = dot1;
+    }
+};
+
 // ====================================================================== Q6_K
 //
 // Unit v = 2*H + hh of a block covers, in half H (weights 128H..128H+127), the
@@ -324,6 +425,7 @@ struct Q8D {
     static constexpr int SLACK = 144;         // a ragged last unit still loads 136 bytes
     static constexpr bool LIMBS = false;
     static constexpr int DEFAULT_UNROLL = 2;
+    static constexpr int DOTS_PER_UNIT = 4;   // 32-weight blocks per unit
 
     __host__ __device__ static int units(int nb) { return (nb + 3) / 4; }
     __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u) * 4u * BLOCK_BYTES; }

@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
                     for (; jb < nr; jb += rpw, a += rstep) {
                         if (has_unit && jb + sub < nr)
                             F::block_dots(a, lc, xr, aligned8,
-                                          p.dots + static_cast<long long>(R0 + rl0 + jb + sub) * p.nb + 4 * ug);
+                                          p.dots + static_cast<long long>(R0 + rl0 + jb + sub) * (p.k >> 5) +
+                                              F::DOTS_PER_UNIT * ug);
                     }
                 }
             }

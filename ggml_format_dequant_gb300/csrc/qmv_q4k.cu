@@ -83,6 +83,42 @@ int moe_q4k(const void* bank, const float* x, float* y, int rows, int k, const i
     return launch<Q4K, true, MODE_MATVEC>(kp, pl, slots, s);
 }
 
+int q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+             cudaStream_t s) {
+    KParams kp{};
+    kp.w = static_cast<const uint8_t*>(w);
+    kp.xq = xq;
+    kp.xqs = xs;
+    kp.y = y;
+    kp.rows = rows;
+    kp.k = k;
+    kp.nb = k / 256;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 144u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = kp.matbytes;
+    Plan pl;
+    int rc = make_plan<Q4D>(rows, k, 1, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q4D, false, MODE_MATVEC>(kp, pl, 1, s);
+}
+
+int q4k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s) {
+    KParams kp{};
+    kp.w = static_cast<const uint8_t*>(w);
+    kp.xq = xq;
+    kp.dots = dots;
+    kp.rows = rows;
+    kp.k = k;
+    kp.nb = k / 256;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 144u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = kp.matbytes;
+    Plan pl;
+    int rc = make_plan<Q4D>(rows, k, 1, nullptr, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q4D, false, MODE_BLOCKDOTS>(kp, pl, 1, s);
+}
+
 int dequant_q4k(const void* w, float* out, int rows, int k, cudaStream_t s) {
     const long long nsub = static_cast<long long>(rows) * (k / 256) * 8;
     const int threads = 256;

@@ -88,6 +88,18 @@ int quantize_act_q8(const float *x, int8_t *xq, float *xs, float *xsum, int m, i
 int qmv_q8_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
                 cudaStream_t stream);
 
+/* dp4a matvec of Q4_K weights with a quantized activation (the pages' dense
+ * dp4a Q4_K decode): y[r] = sum_t xs[t] * (d*sc_t * dot[r, t] - dmin*m_t *
+ * sumq[t]) in f32, over the 32-weight sub-blocks t of row r, where dot[r, t]
+ * is the exact int32 dot of the sub-block's 4-bit codes with the 32 int8 codes
+ * xq of the same positions and sumq[t] the sum of those codes (formed in the
+ * kernel from xq; no separate sum input). w: Q4_K rows as for qmv_q4k;
+ * xq: int8 [k], 16-byte aligned; xs: f32 [k/32]; y: f32 [rows]; k % 256 == 0.
+ * Cites hanzo-ml src/vulkan_backend.rs, the `matvec_q4k_dp4a_blk` dispatch of
+ * the decode matvec (quantize the activation once, dp4a the Q4_K codes). */
+int qmv_q4k_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                 cudaStream_t stream);
+
 /* MoE indexed Q4_K matvec: y[s, r] = sum_j W[ids[s], r, j] * x[s, j].
  * w_bank: one resident bank [n_experts, rows, k] of Q4_K rows (expert e's
  * matrix starts at byte e * rows * (k/256) * 144);
@@ -164,6 +176,8 @@ int qmv_q8_0_cfg(const void *w, const float *x, float *y, int rows, int k, const
                  cudaStream_t stream);
 int qmv_q8_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
                     const qmv_cfg *cfg, cudaStream_t stream);
+int qmv_q4k_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                     const qmv_cfg *cfg, cudaStream_t stream);
 int moe_qmv_q4k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
                     cudaStream_t stream);
@@ -178,11 +192,16 @@ int qmv_dequant_q8_0(const void *w, float *out, int rows, int k, cudaStream_t st
  * computed by the same code path qmv_q8_dp4a uses. */
 int qmv_q8_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int rows, int k,
                           cudaStream_t stream);
+/* The same for Q4_K rows: dots[r, t] (int32 [rows, k/32]) of every 32-weight
+ * sub-block t, computed by the code path qmv_q4k_dp4a uses. */
+int qmv_q4k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int rows, int k,
+                           cudaStream_t stream);
 
 /* Launch plan the library would use (for benchmark reports): threads per CTA,
  * CTAs (all slots), rows per ring slot, ring slots per row group and dynamic
  * shared bytes per CTA.
- * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K. */
+ * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K,
+ * 5 = Q4_K dp4a. */
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
                   int *chunk_rows, int *chunks, int *smem_bytes);
 

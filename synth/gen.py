@@ -150,7 +150,8 @@ def gen_moe_ids(st: Stream, slots: int, n_experts: int) -> np.ndarray:
     return perm[:slots].astype(np.int32)
 
 
-# The five synthetic workloads: name -> (kind, parameters, seed).
+# The synthetic workloads: name -> (kind, parameters, seed). The first five are
+# the suite's; the last is the second one on the dp4a path.
 CONFIGS = {
     "q4k_256x1024": dict(kind="q4k", rows=256, k=1024, seed=0),
     "q4k_4096x4096": dict(kind="q4k", rows=4096, k=4096, seed=1),
@@ -158,6 +159,9 @@ CONFIGS = {
     "moe_q4k_e128_n768_k2048_s8": dict(kind="moe_q4k", rows=768, k=2048, seed=3,
                                        n_experts=128, slots=8),
     "q6k_4096x14336": dict(kind="q6k", rows=4096, k=14336, seed=4),
+    # The Q4_K 4096 x 4096 workload (same seed, so the same bytes) on the dp4a
+    # path: x is quantized on the device and the codes are dp4a-dotted.
+    "q4k_dp4a_4096x4096": dict(kind="q4k_dp4a", rows=4096, k=4096, seed=1),
 }
 
 
@@ -167,7 +171,7 @@ def make_config(name: str) -> dict:
     c = dict(CONFIGS[name])
     st = Stream(c["seed"])
     kind, rows, k = c["kind"], c["rows"], c["k"]
-    if kind == "q4k":
+    if kind in ("q4k", "q4k_dp4a"):
         c["w"] = gen_q4k_rows(st, rows, k)
         c["x"] = gen_normal(st, k)
     elif kind == "q6k":

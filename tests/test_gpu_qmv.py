@@ -246,6 +246,51 @@ def test_dp4a_matvec(q, rows, k, cfg):
     assert scale_rel(ref, host(y)) <= SCALE_REL_TOL
 
 
+# ------------------------------------------------- Q4_K x q8 activation (dp4a)
+
+def _q4k_dp4a_inputs(q, rows, k, seed):
+    st = synth.Stream(seed)
+    w = synth.gen_q4k_rows(st, rows, k)
+    x = synth.gen_normal(st, k)
+    xq = torch.empty(k, dtype=torch.int8, device="cuda")
+    xs = torch.empty(k // 32, dtype=torch.float32, device="cuda")
+    q.quantize_act_q8(dev(x), xq, xs, None, 1, k)
+    oq, os_, _ = oracle.quantize_act_q8(x, 1, k)
+    assert np.array_equal(host(xq), oq.reshape(-1)) and np.array_equal(host(xs), os_.reshape(-1))
+    return w, xq, xs, oq.reshape(-1), os_.reshape(-1)
+
+
+@pytest.mark.parametrize("rows,k,cfg", [(300, 4096, None), (61, 512, None), (1, 256, None), (97, 4352, None),
+                                        (29, 16384, None), (61, 512, dict(ctas=2, chunk_rows=3, chunks=2)),
+                                        (29, 4352, dict(ctas=1, chunk_rows=1, chunks=1)),
+                                        (300, 768, dict(ctas=3, unroll=1, warps=4))])
+def test_q4k_dp4a_matvec(q, rows, k, cfg):
+    w, xq, xs, oq, os_ = _q4k_dp4a_inputs(q, rows, k, 5000 + rows + k)
+    y = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+    q.qmv_q4k_dp4a(dev(w), xq, xs, y, rows, k, cfg=cfg)
+    assert scale_rel(oracle.qmv_q4k_dp4a(w, oq, os_, rows, k), host(y)) <= SCALE_REL_TOL
+
+
+@pytest.mark.parametrize("rows,k", [(300, 4096), (7, 256), (33, 4352)])
+def test_q4k_dp4a_blockdots_bit_exact(q, rows, k):
+    w, xq, xs, oq, _ = _q4k_dp4a_inputs(q, rows, k, 6000 + rows)
+    dots = torch.empty(rows, k // 32, dtype=torch.int32, device="cuda")
+    q.qmv_q4k_dp4a_blockdots(dev(w), xq, dots, rows, k)
+    assert np.array_equal(host(dots), oracle.q4k_dp4a_blockdots(w, oq, rows, k))
+
+
+def test_full_q4k_dp4a_4096(q):
+    c = synth.make_config("q4k_dp4a_4096x4096")
+    rows, k = 4096, 4096
+    xq = torch.empty(k, dtype=torch.int8, device="cuda")
+    xs = torch.empty(k // 32, dtype=torch.float32, device="cuda")
+    q.quantize_act_q8(dev(c["x"]), xq, xs, None, 1, k)
+    y = torch.empty(rows, dtype=torch.float32, device="cuda")
+    q.qmv_q4k_dp4a(dev(c["w"]), xq, xs, y, rows, k)
+    oq, os_, _ = oracle.quantize_act_q8(c["x"], 1, k)
+    assert scale_rel(oracle.qmv_q4k_dp4a(c["w"], oq.reshape(-1), os_.reshape(-1), rows, k), host(y)) <= SCALE_REL_TOL
+
+
 # --------------------------------------------------------------------- MoE
 
 def moe_run(q, bank, x, ids, rows, k, n_experts, cfg=None):
