@@ -77,6 +77,7 @@ def _lib():
             L.orc_qmv_q8_dp4a.argtypes = [P, P, P, lg, lg, P]
             L.orc_q4k_dp4a_blockdots.argtypes = [P, P, lg, lg, P]
             L.orc_qmv_q4k_dp4a.argtypes = [P, P, P, lg, lg, P]
+            L.orc_moe_qmv_q4k_dp4a.argtypes = [P, P, P, P, lg, lg, lg, lg, P]
             _LIB = L
     return _LIB
 
@@ -199,6 +200,21 @@ def qmv_q4k_dp4a(w, xq, xs, rows: int, k: int) -> np.ndarray:
     xs = _f32(xs)
     y = np.empty(rows, dtype=np.float64)
     rc = _lib().orc_qmv_q4k_dp4a(_p(w), _p(xq), _p(xs), rows, k, _p(y))
+    assert rc == 0
+    return y
+
+
+def moe_qmv_q4k_dp4a(bank, xq, xs, ids, rows: int, k: int, n_experts: int) -> np.ndarray:
+    """MoE on the Q4_K dp4a path, y[slots, rows]: slot s uses expert ids[s]
+    and its own codes xq[s] / scales xs[s] (NaN rows for out-of-range ids)."""
+    bank = _u8(bank)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xs = _f32(xs)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    slots = ids.size
+    assert xq.size == slots * k and xs.size == slots * (k // 32)
+    y = np.empty((slots, rows), dtype=np.float64)
+    rc = _lib().orc_moe_qmv_q4k_dp4a(_p(bank), _p(xq), _p(xs), _p(ids), slots, rows, k, n_experts, _p(y))
     assert rc == 0
     return y
 

@@ -377,3 +377,23 @@ int orc_qmv_q4k_dp4a(const uint8_t *w, const int8_t *xq, const float *xs, long r
     }
     return 0;
 }
+
+/* MoE on the Q4_K dp4a path (hanzo-ml src/vulkan_backend.rs,
+ * `moe_matvec_q4k_dp4a_blk_*`: the routed token's activation quantized once,
+ * the experts' Q4_K codes dotted with it): slot s multiplies expert ids[s] of
+ * the [E, rows, k] bank with its own codes xq[s, :] and scales xs[s, :]. A slot
+ * whose id is outside [0, n_experts) gets NaN in every output. */
+int orc_moe_qmv_q4k_dp4a(const uint8_t *bank, const int8_t *xq, const float *xs, const int32_t *ids,
+                         long slots, long rows, long k, long n_experts, double *y) {
+    if (k % ORC_QK_K) return -1;
+    long rb = (k / ORC_QK_K) * ORC_Q4K_BYTES;
+    for (long s = 0; s < slots; s++) {
+        long e = ids[s];
+        if (e < 0 || e >= n_experts) {
+            for (long r = 0; r < rows; r++) y[s * rows + r] = NAN;
+            continue;
+        }
+        orc_qmv_q4k_dp4a(bank + e * rows * rb, xq + s * k, xs + s * (k / 32), rows, k, y + s * rows);
+    }
+    return 0;
+}

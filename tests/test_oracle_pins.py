@@ -410,6 +410,37 @@ def test_moe_matches_dense_per_expert_and_flags_bad_ids():
     assert not np.any(np.isnan(y_bad[0])) and not np.any(np.isnan(y_bad[3]))
 
 
+def test_moe_q6k_matches_dense_per_expert():
+    """The MoE oracle on a Q6_K bank (the pages' down-projection layout) is the
+    pinned dense matvec of each slot's expert."""
+    e, n, k, slots = 4, 3, 512, 3
+    st = synth.Stream(14)
+    bank = synth.gen_q6k_rows(st, e * n, k)
+    x = synth.gen_normal(st, slots * k).reshape(slots, k)
+    ids = np.array([3, 3, 0], dtype=np.int32)
+    y = oracle.moe_qmv("q6k", bank, x, ids, n, k, e)
+    W = oracle.dequant("q6k", bank, e * n, k).reshape(e, n, k)
+    for s in range(slots):
+        assert np.allclose(y[s], W[ids[s]] @ x[s].astype(np.float64), rtol=1e-12, atol=1e-12)
+
+
+def test_moe_q4k_dp4a_matches_dense_per_expert_and_flags_bad_ids():
+    e, n, k, slots = 5, 4, 512, 4
+    st = synth.Stream(15)
+    bank = synth.gen_q4k_rows(st, e * n, k)
+    x = synth.gen_normal(st, slots * k).reshape(slots, k)
+    xq, xs, _ = oracle.quantize_act_q8(x, slots, k)
+    ids = np.array([4, 0, 4, 2], dtype=np.int32)
+    y = oracle.moe_qmv_q4k_dp4a(bank, xq, xs, ids, n, k, e)
+    rb = (k // 256) * 144
+    for s in range(slots):
+        part = bank[ids[s] * n * rb:(ids[s] + 1) * n * rb]
+        assert np.array_equal(y[s], oracle.qmv_q4k_dp4a(part, xq[s], xs[s], n, k))
+    y_bad = oracle.moe_qmv_q4k_dp4a(bank, xq, xs, np.array([1, 5, -1, 0], dtype=np.int32), n, k, e)
+    assert np.all(np.isnan(y_bad[1])) and np.all(np.isnan(y_bad[2]))
+    assert not np.any(np.isnan(y_bad[0])) and not np.any(np.isnan(y_bad[3]))
+
+
 # ------------------------------------------------------------ a planted bug
 
 def test_pins_catch_a_planted_q4k_mistake(monkeypatch):
