@@ -433,8 +433,9 @@ def test_moe_q4k_dp4a_matches_dense_per_expert_and_flags_bad_ids():
     ids = np.array([4, 0, 4, 2], dtype=np.int32)
     y = oracle.moe_qmv_q4k_dp4a(bank, xq, xs, ids, n, k, e)
     rb = (k // 256) * 144
+    flat = bank.reshape(-1)
     for s in range(slots):
-        part = bank[ids[s] * n * rb:(ids[s] + 1) * n * rb]
+        part = flat[ids[s] * n * rb:(ids[s] + 1) * n * rb]
         assert np.array_equal(y[s], oracle.qmv_q4k_dp4a(part, xq[s], xs[s], n, k))
     y_bad = oracle.moe_qmv_q4k_dp4a(bank, xq, xs, np.array([1, 5, -1, 0], dtype=np.int32), n, k, e)
     assert np.all(np.isnan(y_bad[1])) and np.all(np.isnan(y_bad[2]))
