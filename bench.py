@@ -84,8 +84,10 @@ def weight_bytes(name: str) -> int:
         return synth.row_bytes("q6k", c["k"]) * c["rows"]
     if c["kind"] == "q8_0_dp4a":
         return synth.row_bytes("q8_0", c["k"]) * c["rows"]
-    if c["kind"] == "moe_q4k":
+    if c["kind"] in ("moe_q4k", "moe_q4k_dp4a"):
         return synth.row_bytes("q4k", c["k"]) * c["rows"] * c["slots"]   # routed rows only
+    if c["kind"] == "moe_q6k":
+        return synth.row_bytes("q6k", c["k"]) * c["rows"] * c["slots"]
     raise ValueError(name)
 
 
@@ -94,8 +96,10 @@ def algorithmic_bytes(name: str) -> int:
     read, output written."""
     c = synth.CONFIGS[name]
     wb = weight_bytes(name)
-    if c["kind"] == "moe_q4k":
+    if c["kind"] in ("moe_q4k", "moe_q6k"):
         return wb + 4 * c["slots"] * c["k"] + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
+    if c["kind"] == "moe_q4k_dp4a":
+        return wb + c["slots"] * (c["k"] + 4 * (c["k"] // 32)) + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
     if c["kind"] in ("q8_0_dp4a", "q4k_dp4a"):
         return wb + c["k"] + 4 * (c["k"] // 32) + 4 * c["rows"]
     return wb + 4 * c["k"] + 4 * c["rows"]
@@ -186,7 +190,7 @@ class Workload:
         w0 = torch.from_numpy(c["w"].reshape(-1))
         self.w = [w0.to(dev) for _ in range(self.copies)]
         self.x = torch.from_numpy(np.ascontiguousarray(c["x"])).to(dev)
-        if self.kind == "moe_q4k":
+        if self.kind.startswith("moe_"):
             self.y = torch.empty(c["slots"], self.rows, dtype=torch.float32, device=dev)
             # a cycle of seeded id sets so no (bank, expert) slice repeats within 3x L2
             st = synth.Stream(1003)
@@ -195,10 +199,12 @@ class Workload:
                 self.ids.append(torch.from_numpy(synth.gen_moe_ids(st, c["slots"], c["n_experts"])).to(dev))
         else:
             self.y = torch.empty(self.rows, dtype=torch.float32, device=dev)
-        if self.kind in ("q8_0_dp4a", "q4k_dp4a"):
-            self.xq = torch.empty(self.k, dtype=torch.int8, device=dev)
-            self.xs = torch.empty(self.k // 32, dtype=torch.float32, device=dev)
-            q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k)
+        if self.kind in ("q8_0_dp4a", "q4k_dp4a", "moe_q4k_dp4a"):
+            m = c.get("slots", 1) if self.kind.startswith("moe_") else 1
+            self.m = m
+            self.xq = torch.empty(m * self.k, dtype=torch.int8, device=dev)
+            self.xs = torch.empty(m * (self.k // 32), dtype=torch.float32, device=dev)
+            q.quantize_act_q8(self.x, self.xq, self.xs, None, m, self.k)
         self.q = q
         self.cfg = None   # optional forced launch configuration (dict), for tuning sweeps
 
@@ -217,10 +223,20 @@ class Workload:
             fn = q.qmv_q8_dp4a if self.kind == "q8_0_dp4a" else q.qmv_q4k_dp4a
             fn(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg)
             return n
-        elif self.kind == "moe_q4k":
+        elif self.kind in ("moe_q4k", "moe_q6k"):
             c = self.c
-            q.moe_qmv_q4k(w, self.x, self.y, self.rows, self.k, self.ids[i % len(self.ids)], c["slots"],
-                          c["n_experts"], stream=stream, cfg=cfg)
+            fn = q.moe_qmv_q4k if self.kind == "moe_q4k" else q.moe_qmv_q6k
+            fn(w, self.x, self.y, self.rows, self.k, self.ids[i % len(self.ids)], c["slots"],
+               c["n_experts"], stream=stream, cfg=cfg)
+        elif self.kind == "moe_q4k_dp4a":
+            c = self.c
+            n = 1
+            if with_quant:
+                q.quantize_act_q8(self.x, self.xq, self.xs, None, self.m, self.k, stream=stream)
+                n = 2
+            q.moe_qmv_q4k_dp4a(w, self.xq, self.xs, self.y, self.rows, self.k, self.ids[i % len(self.ids)],
+                               c["slots"], c["n_experts"], stream=stream, cfg=cfg)
+            return n
         return 1
 
 
@@ -369,7 +385,7 @@ def run_ours(args):
                 row[tag + "us_per_call"] = round(ms * 1e3, 3)
                 row[tag + "packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
                 row[tag + "frac_of_measured_hbm"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9 / peak, 4)
-            if w2.kind in ("q8_0_dp4a", "q4k_dp4a") and mode != 2:
+            if w2.kind in ("q8_0_dp4a", "q4k_dp4a", "moe_q4k_dp4a") and mode != 2:
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
                 row[tag + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
                 del g3

@@ -26,7 +26,7 @@ QMV_ETOOBIG = -4
 QMV_STATUS_BAD_EXPERT_ID = 1
 QMV_STATUS_WAIT_TIMEOUT = 2
 
-FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A = 0, 1, 2, 3, 4, 5
+FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A = range(8)
 
 
 class QmvLibraryMissing(RuntimeError):
@@ -57,6 +57,10 @@ _SIG = {
     "qmv_q8_dp4a": [_P, _P, _P, _P, _I, _I, _P],
     "moe_qmv_q4k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
     "qmv_q4k_dp4a": [_P, _P, _P, _P, _I, _I, _P],
+    "moe_qmv_q6k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
+    "moe_qmv_q6k_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q4k_dp4a": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P],
+    "moe_qmv_q4k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "qmv_q4k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _P],
     "qmv_q4k_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_q4k_cfg": [_P, _P, _P, _I, _I, _P, _P],
@@ -185,6 +189,22 @@ def moe_qmv_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=N
                      _stream(stream), check=check)
     return _call("moe_qmv_q4k_cfg", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
                  _cfg(cfg), _stream(stream), check=check)
+
+
+def moe_qmv_q6k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("moe_qmv_q6k", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                     _stream(stream), check=check)
+    return _call("moe_qmv_q6k_cfg", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                 _cfg(cfg), _stream(stream), check=check)
+
+
+def moe_qmv_q4k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("moe_qmv_q4k_dp4a", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
+                     n_experts, _stream(stream), check=check)
+    return _call("moe_qmv_q4k_dp4a_cfg", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
+                 n_experts, _cfg(cfg), _stream(stream), check=check)
 
 
 def qmv_dequant_q4k(w, out, rows, k, stream=None, check=True):

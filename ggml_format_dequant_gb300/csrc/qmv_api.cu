@@ -23,6 +23,17 @@ int check_dense(const void* w, const void* x, const void* y, int rows, int k, in
     return QMV_OK;
 }
 
+// Checks shared by the MoE entry points beyond the dense ones: ids, slot and
+// expert counts, and a bank size that fits the address arithmetic.
+int check_moe(const int32_t* ids, int slots, int n_experts, int rows, int k, int qk, int block_bytes) {
+    if (!ids) return QMV_EINVAL;
+    if (slots <= 0 || slots > 65535 || n_experts <= 0) return QMV_EINVAL;
+    if (!aligned(ids, 4)) return QMV_EALIGN;
+    const long long rb = static_cast<long long>(k / qk) * block_bytes;
+    if (static_cast<long long>(n_experts) > LLONG_MAX / rb / rows) return QMV_EINVAL;
+    return QMV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -96,18 +107,40 @@ int qmv_q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int
 int moe_qmv_q4k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids,
                     int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
     int rc = check_dense(w_bank, x, y, rows, k, 256, 144);
-    if (rc) return rc;
-    if (!ids) return QMV_EINVAL;
-    if (slots <= 0 || slots > 65535 || n_experts <= 0) return QMV_EINVAL;
-    if (!aligned(ids, 4)) return QMV_EALIGN;
-    const long long rb = static_cast<long long>(k / 256) * 144;
-    if (static_cast<long long>(n_experts) > LLONG_MAX / rb / rows) return QMV_EINVAL;
-    return qmvi::moe_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
+    if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 144);
+    return rc ? rc : qmvi::moe_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
 }
 
 int moe_qmv_q4k(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
                 int n_experts, cudaStream_t stream) {
     return moe_qmv_q4k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+}
+
+int moe_qmv_q6k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                    int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+    int rc = check_dense(w_bank, x, y, rows, k, 256, 210);
+    if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 210);
+    return rc ? rc : qmvi::moe_q6k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
+}
+
+int moe_qmv_q6k(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                int n_experts, cudaStream_t stream) {
+    return moe_qmv_q6k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+}
+
+int moe_qmv_q4k_dp4a_cfg(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                         const int32_t* ids, int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+    if (!xs) return QMV_EINVAL;
+    int rc = check_dense(w_bank, xq, y, rows, k, 256, 144);
+    if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 144);
+    if (rc) return rc;
+    if (!aligned(xq, 16) || !aligned(xs, 4)) return QMV_EALIGN;
+    return qmvi::moe_q4k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, cfg, stream);
+}
+
+int moe_qmv_q4k_dp4a(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                     const int32_t* ids, int slots, int n_experts, cudaStream_t stream) {
+    return moe_qmv_q4k_dp4a_cfg(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
 int qmv_dequant_q4k(const void* w, float* out, int rows, int k, cudaStream_t stream) {
@@ -176,16 +209,19 @@ namespace {
 // Plan of format fmt on device `di`.
 int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_cfg* cfg, qmv::KParams* kp,
             qmv::Plan* pl) {
-    static const int qk[6] = {256, 256, 32, 32, 256, 256};
-    if (fmt < 0 || fmt > 5 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
-    if (fmt == 4 && slots <= 0) return QMV_EINVAL;
-    if (fmt != 4) slots = 1;
+    static const int qk[8] = {256, 256, 32, 32, 256, 256, 256, 256};
+    if (fmt < 0 || fmt > 7 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
+    const bool moe = fmt == 4 || fmt == 6 || fmt == 7;
+    if (moe && slots <= 0) return QMV_EINVAL;
+    if (!moe) slots = 1;
     switch (fmt) {
     case 0: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, 1, cfg, kp, pl);
     case 1: return qmv::make_plan_for<qmv::Q6K>(di, rows, k, 1, cfg, kp, pl);
     case 2: return qmv::make_plan_for<qmv::Q8F>(di, rows, k, 1, cfg, kp, pl);
     case 3: return qmv::make_plan_for<qmv::Q8D>(di, rows, k, 1, cfg, kp, pl);
     case 5: return qmv::make_plan_for<qmv::Q4D>(di, rows, k, 1, cfg, kp, pl);
+    case 6: return qmv::make_plan_for<qmv::Q6K>(di, rows, k, slots, cfg, kp, pl);
+    case 7: return qmv::make_plan_for<qmv::Q4D>(di, rows, k, slots, cfg, kp, pl);
     default: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, slots, cfg, kp, pl);
     }
 }
@@ -202,7 +238,7 @@ int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* 
     rc = plan_of(di, fmt, rows, k, slots, cfg, &kp, &pl);
     if (rc) return rc;
     if (threads) *threads = pl.T;
-    if (ctas) *ctas = pl.parts * (fmt == 4 ? slots : 1);
+    if (ctas) *ctas = pl.parts * ((fmt == 4 || fmt == 6 || fmt == 7) ? slots : 1);
     if (chunk_rows) *chunk_rows = kp.CR;
     if (chunks) *chunks = kp.S;
     if (smem_bytes) *smem_bytes = static_cast<int>(pl.smem);

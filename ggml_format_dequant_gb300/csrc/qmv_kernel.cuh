@@ -45,8 +45,8 @@ enum Mode : int { MODE_MATVEC = 0, MODE_BLOCKDOTS = 1 };
 struct KParams {
     const uint8_t* w;           // packed rows (dense) or the [E, rows] bank (MoE)
     const float* x;             // f32 activation: [k] dense, [slots, k] MoE
-    const int8_t* xq;           // dp4a activation codes [k]
-    const float* xqs;           // dp4a activation scales [k/32]
+    const int8_t* xq;           // dp4a activation codes: [k] dense, [slots, k] MoE
+    const float* xqs;           // dp4a activation scales: [k/32] dense, [slots, k/32] MoE
     float* y;                   // [rows] dense, [slots, rows] MoE
     int32_t* dots;              // [rows, k/32] block dots (MODE_BLOCKDOTS)
     const int32_t* ids;         // [slots] expert ids (MoE)
@@ -154,6 +154,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
 
     const uint8_t* wbase = p.w;
     const float* xrow = p.x;
+    const int8_t* xqrow = p.xq;      // integer-activation formats: this slot's codes and scales
+    const float* xqsrow = p.xqs;
     if (MOE) {
         // ids may come from the kernel just before (the router), unless the
         // caller declared this call's inputs independent of it.
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         }
         wbase = p.w + static_cast<unsigned long long>(e) * p.matbytes;
         xrow = p.x + static_cast<long long>(slot) * p.k;
+        xqrow = p.xq + static_cast<long long>(slot) * p.k;
+        xqsrow = p.xqs + static_cast<long long>(slot) * (p.k >> 5);
     }
     // (The planner never gives a CTA zero rows, and the MoE check above is the
     // same for every CTA of a cluster, which all serve one slot: no CTA leaves
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
             if constexpr (F::LIMBS)
                 F::load_x(xr, smem, p.lt, e0);
             else
-                F::load_xq(xr, lc, p.xq, p.xqs, e0);
+                F::load_xq(xr, lc, xqrow, xqsrow, e0);
         }
         // Byte offset of the lane's unit inside a row, and 16-byte phase of the
         // group's rows in memory (pieces may start off a 16-byte boundary).

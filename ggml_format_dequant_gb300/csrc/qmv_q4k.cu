@@ -119,6 +119,27 @@ int q4k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows,
     return launch<Q4D, false, MODE_BLOCKDOTS>(kp, pl, 1, s);
 }
 
+int moe_q4k_dp4a(const void* bank, const int8_t* xq, const float* xs, float* y, int rows, int k, const int32_t* ids,
+                 int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+    KParams kp{};
+    kp.w = static_cast<const uint8_t*>(bank);
+    kp.xq = xq;
+    kp.xqs = xs;
+    kp.y = y;
+    kp.ids = ids;
+    kp.n_experts = n_experts;
+    kp.rows = rows;
+    kp.k = k;
+    kp.nb = k / 256;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 144u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = static_cast<unsigned long long>(n_experts) * kp.matbytes;
+    Plan pl;
+    int rc = make_plan<Q4D>(rows, k, slots, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q4D, true, MODE_MATVEC>(kp, pl, slots, s);
+}
+
 int dequant_q4k(const void* w, float* out, int rows, int k, cudaStream_t s) {
     const long long nsub = static_cast<long long>(rows) * (k / 256) * 8;
     const int threads = 256;

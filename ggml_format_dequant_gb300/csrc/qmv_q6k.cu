@@ -53,6 +53,26 @@ int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
     return launch<Q6K, false, MODE_MATVEC>(kp, pl, 1, s);
 }
 
+int moe_q6k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+            int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+    KParams kp{};
+    kp.w = static_cast<const uint8_t*>(bank);
+    kp.x = x;
+    kp.y = y;
+    kp.ids = ids;
+    kp.n_experts = n_experts;
+    kp.rows = rows;
+    kp.k = k;
+    kp.nb = k / 256;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 210u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = static_cast<unsigned long long>(n_experts) * kp.matbytes;
+    Plan pl;
+    int rc = make_plan<Q6K>(rows, k, slots, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q6K, true, MODE_MATVEC>(kp, pl, slots, s);
+}
+
 int dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t s) {
     const long long ng = static_cast<long long>(rows) * (k / 256) * 16;
     const int threads = 256;

@@ -112,6 +112,23 @@ int qmv_q4k_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int
 int moe_qmv_q4k(const void *w_bank, const float *x, float *y, int rows, int k,
                 const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
 
+/* MoE indexed Q6_K matvec (the pages' Q6_K down-projection experts):
+ * y[s, r] = sum_j W[ids[s], r, j] * x[s, j] over one resident bank
+ * [n_experts, rows, k] of Q6_K rows (expert e's matrix starts at byte
+ * e * rows * (k/256) * 210); x f32 [slots, k]; y f32 [slots, rows]; ids as for
+ * moe_qmv_q4k (out-of-range ids: NaN rows and QMV_STATUS_BAD_EXPERT_ID).
+ * Cites hanzo-ml src/vulkan_backend.rs, the `moe_matvec_q6k*` kernels. */
+int moe_qmv_q6k(const void *w_bank, const float *x, float *y, int rows, int k,
+                const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+
+/* MoE indexed Q4_K matvec on the dp4a path: slot s multiplies expert ids[s]
+ * with its own quantized activation, xq int8 [slots, k] (16-byte aligned) and
+ * xs f32 [slots, k/32] (quantize_act_q8 with m = slots), as qmv_q4k_dp4a does.
+ * Bank, ids, y and errors as for moe_qmv_q4k.
+ * Cites hanzo-ml src/vulkan_backend.rs, `moe_matvec_q4k_dp4a_blk_*`. */
+int moe_qmv_q4k_dp4a(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                     const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+
 /* Decode-chain overlap (process-wide; 0 by default).
  * mode 1: every matvec launch allows programmatic dependent launch: a call may
  *   be scheduled while the previous kernel on the same stream is still running
@@ -178,6 +195,12 @@ int qmv_q8_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, 
                     const qmv_cfg *cfg, cudaStream_t stream);
 int qmv_q4k_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
                      const qmv_cfg *cfg, cudaStream_t stream);
+int moe_qmv_q6k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
+                    const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
+                    cudaStream_t stream);
+int moe_qmv_q4k_dp4a_cfg(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows,
+                         int k, const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
+                         cudaStream_t stream);
 int moe_qmv_q4k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
                     cudaStream_t stream);
@@ -201,7 +224,7 @@ int qmv_q4k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int r
  * CTAs (all slots), rows per ring slot, ring slots per row group and dynamic
  * shared bytes per CTA.
  * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K,
- * 5 = Q4_K dp4a. */
+ * 5 = Q4_K dp4a, 6 = MoE Q6_K, 7 = MoE Q4_K dp4a. */
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
                   int *chunk_rows, int *chunks, int *smem_bytes);
 

@@ -151,7 +151,8 @@ def gen_moe_ids(st: Stream, slots: int, n_experts: int) -> np.ndarray:
 
 
 # The synthetic workloads: name -> (kind, parameters, seed). The first five are
-# the suite's; the last is the second one on the dp4a path.
+# the suite's; the others are the second and fourth on the dp4a path and a
+# Q6_K MoE bank.
 CONFIGS = {
     "q4k_256x1024": dict(kind="q4k", rows=256, k=1024, seed=0),
     "q4k_4096x4096": dict(kind="q4k", rows=4096, k=4096, seed=1),
@@ -162,6 +163,12 @@ CONFIGS = {
     # The Q4_K 4096 x 4096 workload (same seed, so the same bytes) on the dp4a
     # path: x is quantized on the device and the codes are dp4a-dotted.
     "q4k_dp4a_4096x4096": dict(kind="q4k_dp4a", rows=4096, k=4096, seed=1),
+    # The MoE workload on the dp4a path (same seed: the same bank, ids and x),
+    # and the pages' second MoE workload, Q6_K down-projection experts
+    # [128, 2048, 768] with 8 routed slots.
+    "moe_q4k_dp4a_e128_n768_k2048_s8": dict(kind="moe_q4k_dp4a", rows=768, k=2048, seed=3,
+                                            n_experts=128, slots=8),
+    "moe_q6k_e128_n2048_k768_s8": dict(kind="moe_q6k", rows=2048, k=768, seed=5, n_experts=128, slots=8),
 }
 
 
@@ -180,9 +187,10 @@ def make_config(name: str) -> dict:
     elif kind == "q8_0_dp4a":
         c["w"] = gen_q8_0_rows(st, rows, k)
         c["x"] = gen_normal(st, k)
-    elif kind == "moe_q4k":
+    elif kind in ("moe_q4k", "moe_q4k_dp4a", "moe_q6k"):
         e, s = c["n_experts"], c["slots"]
-        c["w"] = gen_q4k_rows(st, e * rows, k).reshape(e, rows, -1)
+        gen = gen_q6k_rows if kind == "moe_q6k" else gen_q4k_rows
+        c["w"] = gen(st, e * rows, k).reshape(e, rows, -1)
         c["ids"] = gen_moe_ids(st, s, e)
         c["x"] = gen_normal(st, s * k).reshape(s, k)
     else:

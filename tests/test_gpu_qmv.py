@@ -341,6 +341,97 @@ def test_moe_bad_ids_give_nan_and_status(q):
     assert q.qmv_device_status(clear=True) == 0
 
 
+# ------------------------------------------- MoE: Q6_K bank, Q4_K dp4a path
+
+def moe6_run(q, bank, x, ids, rows, k, n_experts, cfg=None):
+    slots = len(ids)
+    y = torch.full((slots, rows), 7.0, dtype=torch.float32, device="cuda")
+    q.moe_qmv_q6k(dev(bank), dev(x), y, rows, k, dev(np.asarray(ids, dtype=np.int32)), slots, n_experts, cfg=cfg)
+    return host(y)
+
+
+@pytest.mark.parametrize("e,n,k,ids,cfg", [(16, 96, 512, [3, 15, 0, 3], None), (8, 257, 768, [1, 2], None),
+                                           (8, 7, 256, [7, 6, 5, 4, 3, 2, 1, 0, 7], None),
+                                           (6, 40, 768, [5, 1, 1], dict(ctas=2, chunk_rows=3, chunks=2))])
+def test_moe_q6k_matches_oracle(q, e, n, k, ids, cfg):
+    st = synth.Stream(e * n + k + 1)
+    bank = synth.gen_q6k_rows(st, e * n, k)
+    x = synth.gen_normal(st, len(ids) * k).reshape(len(ids), k)
+    y = moe6_run(q, bank, x, ids, n, k, e, cfg=cfg)
+    ref = oracle.moe_qmv("q6k", bank, x, np.array(ids, dtype=np.int32), n, k, e)
+    for s in range(len(ids)):
+        assert scale_rel(ref[s], y[s]) <= SCALE_REL_TOL
+
+
+def test_moe_q6k_gather_exact(q):
+    e, n, k = 10, 24, 768
+    bank = synth.gen_q6k_rows(synth.Stream(44), e * n, k)
+    W = oracle.dequant("q6k", bank, e * n, k).reshape(e, n, k).astype(np.float32)
+    ids = [9, 0, 4, 4]
+    for j in [0, 100, 767]:
+        x = np.zeros((len(ids), k), dtype=np.float32)
+        x[:, j] = 1.0
+        y = moe6_run(q, bank, x, ids, n, k, e)
+        for s, eid in enumerate(ids):
+            assert np.array_equal(y[s], W[eid, :, j])
+
+
+def _moe_dp4a_run(q, bank, x, ids, rows, k, n_experts, cfg=None):
+    slots = len(ids)
+    xq = torch.empty(slots * k, dtype=torch.int8, device="cuda")
+    xs = torch.empty(slots * (k // 32), dtype=torch.float32, device="cuda")
+    q.quantize_act_q8(dev(x), xq, xs, None, slots, k)
+    y = torch.full((slots, rows), 7.0, dtype=torch.float32, device="cuda")
+    q.moe_qmv_q4k_dp4a(dev(bank), xq, xs, y, rows, k, dev(np.asarray(ids, dtype=np.int32)), slots, n_experts, cfg=cfg)
+    oq, os_, _ = oracle.quantize_act_q8(x, slots, k)
+    assert np.array_equal(host(xq), oq.reshape(-1))
+    return host(y), oq, os_
+
+
+@pytest.mark.parametrize("e,n,k,ids,cfg", [(16, 96, 512, [3, 15, 0, 3], None), (4, 768, 2048, [1, 2], None),
+                                           (8, 7, 256, [7, 6, 5, 4, 3, 2, 1, 0, 7], None),
+                                           (12, 40, 512, [11, 0, 5], dict(ctas=2, chunk_rows=3, chunks=2))])
+def test_moe_q4k_dp4a_matches_oracle(q, e, n, k, ids, cfg):
+    st = synth.Stream(e * n + k + 2)
+    bank = synth.gen_q4k_rows(st, e * n, k)
+    x = synth.gen_normal(st, len(ids) * k).reshape(len(ids), k)
+    y, oq, os_ = _moe_dp4a_run(q, bank, x, ids, n, k, e, cfg=cfg)
+    ref = oracle.moe_qmv_q4k_dp4a(bank, oq, os_, np.array(ids, dtype=np.int32), n, k, e)
+    for s in range(len(ids)):
+        assert scale_rel(ref[s], y[s]) <= SCALE_REL_TOL
+
+
+def test_moe_variants_bad_ids_give_nan_and_status(q):
+    e, n, k = 4, 16, 256
+    st = synth.Stream(61)
+    bank4 = synth.gen_q4k_rows(st, e * n, k)
+    bank6 = synth.gen_q6k_rows(st, e * n, k)
+    x = synth.gen_normal(st, 4 * k).reshape(4, k)
+    ids = [1, 4, -1, 2]
+    q.qmv_device_status(clear=True)
+    y6 = moe6_run(q, bank6, x, ids, n, k, e)
+    assert np.all(np.isnan(y6[1])) and np.all(np.isnan(y6[2])) and not np.any(np.isnan(y6[0]))
+    assert q.qmv_device_status(clear=True) & q.QMV_STATUS_BAD_EXPERT_ID
+    y4, _, _ = _moe_dp4a_run(q, bank4, x, ids, n, k, e)
+    assert np.all(np.isnan(y4[1])) and np.all(np.isnan(y4[2])) and not np.any(np.isnan(y4[3]))
+    assert q.qmv_device_status(clear=True) & q.QMV_STATUS_BAD_EXPERT_ID
+    assert q.qmv_device_status(clear=True) == 0
+
+
+def test_full_moe_q6k(q):
+    c = synth.make_config("moe_q6k_e128_n2048_k768_s8")
+    y = moe6_run(q, c["w"], c["x"], c["ids"], 2048, 768, 128)
+    ref = oracle.moe_qmv("q6k", c["w"], c["x"], c["ids"], 2048, 768, 128)
+    assert scale_rel(ref, y) <= SCALE_REL_TOL
+
+
+def test_full_moe_q4k_dp4a(q):
+    c = synth.make_config("moe_q4k_dp4a_e128_n768_k2048_s8")
+    y, oq, os_ = _moe_dp4a_run(q, c["w"], c["x"], c["ids"], 768, 2048, 128)
+    ref = oracle.moe_qmv_q4k_dp4a(c["w"], oq, os_, c["ids"], 768, 2048, 128)
+    assert scale_rel(ref, y) <= SCALE_REL_TOL
+
+
 # ----------------------------------------------------------- argument errors
 
 def test_argument_errors(q):

@@ -19,17 +19,17 @@ import numpy as np
 import pytest
 
 DEVICE = (152, 232448, 233472, 1024)
-FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5}
+FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5, "moe6": 6, "moe4d": 7}
 
 
 # Per format: weights per block, bytes per block, blocks per warp slice,
 # units per row, a unit's block offset in its slice, and the byte range a
 # unit's loads touch relative to its address a (lo may depend on a & 3).
 def fmt_info(fmt):
-    if fmt in ("q4k", "moe", "q4d"):
+    if fmt in ("q4k", "moe", "q4d", "moe4d"):
         return dict(qk=256, bb=144, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 144,
                     extent=lambda a: (a, a + 144), align=16)
-    if fmt == "q6k":
+    if fmt in ("q6k", "moe6"):
         return dict(qk=256, bb=210, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 210,
                     extent=lambda a: (a - (a & 3), a - (a & 3) + 212), align=2)
     if fmt == "q8_0":
@@ -67,7 +67,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
     CL = P["CL"]
     assert CL in (1, 2, 4, 8) and parts % CL == 0 and (k // 16) % (2 * CL) == 0
     assert P["rq"] >= 1
-    if fmt in ("q8d", "q4d"):
+    if fmt in ("q8d", "q4d", "moe4d"):
         assert CL == 1
     lg = GS.bit_length() - 1
     rpw = 32 >> lg
@@ -77,7 +77,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
 
     # shared-memory layout: disjoint, ordered regions inside the device limit
     regions = []
-    if fmt not in ("q8d", "q4d"):
+    if fmt not in ("q8d", "q4d", "moe4d"):
         regions += [(P["off_la"], k), (P["off_lb"], k), (P["off_lc"], k), (P["off_xs"], 4 * (k // 32)),
                     (P["off_xsum16"], 4 * (k // 16))]
         for o, _ in regions:
@@ -150,7 +150,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
 
 
 WORKLOADS = [("q4k", 4096, 4096, 1), ("q4k", 256, 1024, 1), ("q8d", 14336, 4096, 1), ("q6k", 4096, 14336, 1),
-             ("moe", 768, 2048, 8), ("q4d", 4096, 4096, 1)]
+             ("moe", 768, 2048, 8), ("q4d", 4096, 4096, 1), ("moe6", 2048, 768, 8), ("moe4d", 768, 2048, 8)]
 
 
 @pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
@@ -171,13 +171,13 @@ SHAPES = [("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 4352), ("q4k", 20, 163
           ("q6k", 3, 256), ("q6k", 41, 14336), ("q6k", 130, 2816), ("q8_0", 300, 96), ("q8_0", 7, 4096),
           ("q8_0", 13, 32), ("q8_0", 64, 11008), ("q8d", 300, 4096), ("q8d", 7, 96), ("q8d", 1, 32),
           ("q8d", 61, 256), ("q8d", 5, 4160), ("moe", 96, 512, ), ("moe", 7, 256), ("q4d", 300, 768), ("q4d", 1, 256),
-          ("q4d", 97, 4352), ("q4d", 20, 16384)]
+          ("q4d", 97, 4352), ("q4d", 20, 16384), ("moe6", 96, 512), ("moe6", 7, 256), ("moe4d", 40, 512)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
 def test_shape_plans(q, shape):
     fmt, rows, k = shape
-    replay(q, fmt, rows, k, 4 if fmt == "moe" else 1)
+    replay(q, fmt, rows, k, 4 if fmt.startswith("moe") else 1)
 
 
 CFGS = [dict(ctas=1, chunk_rows=1, chunks=2), dict(ctas=3, chunk_rows=5, chunks=2), dict(ctas=2, chunk_rows=3, chunks=1),
