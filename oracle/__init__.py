@@ -31,9 +31,9 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB = None
 _LOCK = threading.Lock()
 
-FMT = {"q4k": 0, "q6k": 1, "q8_0": 2}
-QK = {"q4k": 256, "q6k": 256, "q8_0": 32}
-BLOCK_BYTES = {"q4k": 144, "q6k": 210, "q8_0": 34}
+FMT = {"q4k": 0, "q6k": 1, "q8_0": 2, "q4_0": 3, "q5k": 4}
+QK = {"q4k": 256, "q6k": 256, "q8_0": 32, "q4_0": 32, "q5k": 256}
+BLOCK_BYTES = {"q4k": 144, "q6k": 210, "q8_0": 34, "q4_0": 18, "q5k": 176}
 
 
 def lib_path() -> str:
@@ -63,10 +63,10 @@ def _lib():
             lg = ctypes.c_long
             L.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
             L.orc_f16_to_f64.restype = ctypes.c_double
-            for f in ("orc_q4k_block_decode", "orc_q6k_block_decode", "orc_q8_0_block_decode"):
-                getattr(L, f).argtypes = [P, P]
-                getattr(L, f).restype = None
-            for f in ("orc_q4k_elem", "orc_q6k_elem", "orc_q8_0_elem"):
+            for fmt in FMT:
+                getattr(L, f"orc_{fmt}_block_decode").argtypes = [P, P]
+                getattr(L, f"orc_{fmt}_block_decode").restype = None
+            for f in (f"orc_{fmt}_elem" for fmt in FMT):
                 getattr(L, f).argtypes = [P, ctypes.c_int]
                 getattr(L, f).restype = ctypes.c_double
             L.orc_dequant.argtypes = [ctypes.c_int, P, lg, lg, P]

@@ -24,6 +24,15 @@
  *    +-127) and `quantize_act_q8` (per-32 block int8 codes, f32 scale and a
  *    per-block sum): the activation quantizer of the dp4a path, with the
  *    rounding taken as round-to-nearest-even on an IEEE f32 product.
+ *  - same file, `matvec_q4_0_gpu`: the native 18-byte Q4_0 block, decode
+ *    byte-exact with the CPU `BlockQ4_0::to_float` (the reading taken here: d
+ *    (f16) then 16 bytes; weight i < 16 is the low nibble of qs[i], weight
+ *    i >= 16 the high nibble of qs[i-16]; w = d*(q - 8)).
+ *  - same file, `quantize_q5k` / `matvec_q5k`: the 176-byte GGUF Q5_K block is
+ *    d, dmin, 12 scale bytes, 32 qh bytes, 128 qs bytes, decode matching the
+ *    CPU `BlockQ5K::to_float` (the reading taken here: scales and mins packed
+ *    as in Q4_K, the 4 low bits of each code laid out as Q4_K's, the fifth bit
+ *    of weight i being bit (i/32) of qh[i%32]; w = d*sc_j*q - dmin*m_j).
  *  - vulkan_backend.rs `moe_matvec_gpu`: y[s, r] = sum_k W[ids[s], r, k] x[s, k]
  *    over one resident [E, n, k] bank, output in slot order.
  *
@@ -42,6 +51,8 @@
 #define ORC_Q4K_BYTES 144
 #define ORC_Q6K_BYTES 210
 #define ORC_Q8_0_BYTES 34
+#define ORC_Q4_0_BYTES 18
+#define ORC_Q5K_BYTES 176
 
 /* IEEE 754 binary16 -> binary64, exact for every encoding: normal numbers are
  * (1024 + mantissa) * 2^(exponent - 25), subnormals mantissa * 2^-24. */
@@ -174,22 +185,92 @@ double orc_q8_0_elem(const uint8_t *b, int i) {
     return orc_f16_to_f64(rd_le16(b)) * (double)(int8_t)b[2 + i];
 }
 
+/* ---------------------------------------------------------------- Q4_0 -- */
+
+/* Loop-structured decode: byte l of qs carries weight l in its low nibble and
+ * weight l+16 in its high nibble. */
+void orc_q4_0_block_decode(const uint8_t *b, double *out) {
+    double d = orc_f16_to_f64(rd_le16(b));
+    for (int l = 0; l < 16; l++) {
+        out[l] = d * ((b[2 + l] & 15) - 8);
+        out[l + 16] = d * ((b[2 + l] >> 4) - 8);
+    }
+}
+
+/* Per-element closed form: code = bits 4*(i/16)..4*(i/16)+3 of byte i%16. */
+double orc_q4_0_elem(const uint8_t *b, int i) {
+    int q = (b[2 + i % 16] >> (4 * (i / 16))) & 0x0F;
+    return orc_f16_to_f64(rd_le16(b)) * (q - 8);
+}
+
+/* ---------------------------------------------------------------- Q5_K -- */
+
+/* Loop-structured decode: four 64-weight chunks as in Q4_K; in chunk c the 32
+ * qh bytes give the fifth bit of the low-nibble weights in bit 2c and of the
+ * high-nibble weights in bit 2c+1. Scales and mins use Q4_K's packing. */
+void orc_q5k_block_decode(const uint8_t *b, double *out) {
+    double d = orc_f16_to_f64(rd_le16(b));
+    double dmin = orc_f16_to_f64(rd_le16(b + 2));
+    const uint8_t *s = b + 4;
+    const uint8_t *qh = b + 16;
+    const uint8_t *qs = b + 48;
+    for (int c = 0; c < 4; c++) {
+        int sc0, m0, sc1, m1;
+        q4k_scale_min(2 * c, s, &sc0, &m0);
+        q4k_scale_min(2 * c + 1, s, &sc1, &m1);
+        for (int l = 0; l < 32; l++) {
+            int lo = (qs[32 * c + l] & 15) + (((qh[l] >> (2 * c)) & 1) ? 16 : 0);
+            int hi = (qs[32 * c + l] >> 4) + (((qh[l] >> (2 * c + 1)) & 1) ? 16 : 0);
+            out[64 * c + l] = d * sc0 * lo - dmin * m0;
+            out[64 * c + 32 + l] = d * sc1 * hi - dmin * m1;
+        }
+    }
+}
+
+/* Per-element closed form, written apart from the loop above: sub-block
+ * j = i/32; low 4 bits as Q4_K's element i (qs at byte 48 instead of 16); the
+ * fifth bit is bit j of qh[i%32]; scale and min read with bits_of(). */
+double orc_q5k_elem(const uint8_t *b, int i) {
+    int j = i / 32;
+    int byte = 48 + 32 * (i / 64) + (i % 32);
+    int q = ((j % 2 == 0) ? (b[byte] & 0x0F) : (b[byte] >> 4)) + 16 * ((b[16 + i % 32] >> j) & 1);
+    const uint8_t *s = b + 4;
+    int sc, m;
+    if (j < 4) {
+        sc = bits_of(s, j, 0, 6);
+        m = bits_of(s, j + 4, 0, 6);
+    } else {
+        sc = bits_of(s, j + 4, 0, 4) + 16 * bits_of(s, j - 4, 6, 2);
+        m = bits_of(s, j + 4, 4, 4) + 16 * bits_of(s, j, 6, 2);
+    }
+    double d = orc_f16_to_f64(rd_le16(b));
+    double dmin = orc_f16_to_f64(rd_le16(b + 2));
+    return d * sc * q - dmin * m;
+}
+
 /* ----------------------------------------------------- row dequant + matvec */
 
-/* fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0. Returns the block geometry. */
+/* fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0, 3 = Q4_0, 4 = Q5_K. Returns the block
+ * geometry. */
 static int fmt_geom(int fmt, int *qk, int *bb) {
     switch (fmt) {
     case 0: *qk = ORC_QK_K; *bb = ORC_Q4K_BYTES; return 0;
     case 1: *qk = ORC_QK_K; *bb = ORC_Q6K_BYTES; return 0;
     case 2: *qk = ORC_QK8_0; *bb = ORC_Q8_0_BYTES; return 0;
+    case 3: *qk = ORC_QK8_0; *bb = ORC_Q4_0_BYTES; return 0;
+    case 4: *qk = ORC_QK_K; *bb = ORC_Q5K_BYTES; return 0;
     default: return -1;
     }
 }
 
 static void decode_block(int fmt, const uint8_t *b, double *out) {
-    if (fmt == 0) orc_q4k_block_decode(b, out);
-    else if (fmt == 1) orc_q6k_block_decode(b, out);
-    else orc_q8_0_block_decode(b, out);
+    switch (fmt) {
+    case 0: orc_q4k_block_decode(b, out); break;
+    case 1: orc_q6k_block_decode(b, out); break;
+    case 2: orc_q8_0_block_decode(b, out); break;
+    case 3: orc_q4_0_block_decode(b, out); break;
+    default: orc_q5k_block_decode(b, out); break;
+    }
 }
 
 /* Exact decoded weights of `rows` packed rows into out[rows*k] (f64). */

@@ -19,9 +19,14 @@ from .gen import (  # noqa: F401
     Q4K_BLOCK_BYTES,
     Q6K_BLOCK_BYTES,
     Q8_0_BLOCK_BYTES,
+    Q4_0_BLOCK_BYTES,
+    Q5K_BLOCK_BYTES,
+    GEN_ROWS,
     gen_q4k_rows,
     gen_q6k_rows,
     gen_q8_0_rows,
+    gen_q4_0_rows,
+    gen_q5k_rows,
     gen_normal,
     gen_moe_ids,
     make_config,

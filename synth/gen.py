@@ -1,10 +1,12 @@
-"""Seeded generators for raw Q4_K / Q6_K / Q8_0 weight rows, f32 activations and
-MoE expert ids.
+"""Seeded generators for raw Q4_K / Q6_K / Q8_0 / Q4_0 / Q5_K weight rows, f32
+activations and MoE expert ids.
 
 The block byte layouts follow the GGML/GGUF block structs the pages upload
 verbatim (hanzo-ml ``vulkan_backend.rs``: ``quantize_q4k`` for the 144-byte
 ``block_q4_K``, ``quantize_q6k`` for the 210-byte ``block_q6_K`` and
-``quantize_q8_blocks`` for the 34-byte ``block_q8_0``). Only the field sizes and
+``quantize_q8_blocks`` for the 34-byte ``block_q8_0``, ``matvec_q4_0_gpu`` for
+the native 18-byte ``block_q4_0`` and ``quantize_q5k`` for the 176-byte
+``block_q5_K``). Only the field sizes and
 their order matter here; how the fields decode is the oracle's business.
 
 Draw order (this repository's choice): blocks in row-major order, and inside a
@@ -16,6 +18,10 @@ after all weight draws. Per block:
 * Q6_K (41 draws): 16 draws -> ``ql[128]``, 8 draws -> ``qh[64]``, 16 draws ->
   one int8 scale each, 1 draw -> d.
 * Q8_0 (33 draws): 1 draw -> d, 32 draws -> one int8 weight each.
+* Q4_0 (3 draws): 1 draw -> d (either sign), 2 draws -> the 16 ``qs`` bytes.
+* Q5_K (24 draws): d, dmin (one draw each), 2 draws -> 16 bytes of which the
+  first 12 are the packed scales/mins, 4 draws -> the 32 ``qh`` bytes, 16 draws
+  -> the 128 ``qs`` bytes.
 
 A value U[a, b] is ``a + (b - a) * u53`` in f64 with ``u53 = (z >> 11) * 2**-53``,
 then rounded to f32 and to f16 (numpy's round-to-nearest-even conversions).
@@ -33,6 +39,8 @@ _M2 = np.uint64(0x94D049BB133111EB)
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
 Q8_0_BLOCK_BYTES = 34
+Q4_0_BLOCK_BYTES = 18
+Q5K_BLOCK_BYTES = 176
 QK_K = 256
 QK8_0 = 32
 
@@ -45,6 +53,10 @@ def row_bytes(fmt: str, k: int) -> int:
         return (k // QK_K) * Q6K_BLOCK_BYTES
     if fmt == "q8_0":
         return (k // QK8_0) * Q8_0_BLOCK_BYTES
+    if fmt == "q4_0":
+        return (k // QK8_0) * Q4_0_BLOCK_BYTES
+    if fmt == "q5k":
+        return (k // QK_K) * Q5K_BLOCK_BYTES
     raise ValueError(fmt)
 
 
@@ -123,6 +135,35 @@ def gen_q8_0_rows(st: Stream, rows: int, k: int, d_range=(1e-3, 1e-2),
     blk[:, 0:2] = _uniform_f16_bits(z[:, 0], *d_range).view(np.uint8).reshape(-1, 2)
     blk[:, 2:34] = _uniform_int(z[:, 1:33], *q_range).astype(np.int8).view(np.uint8)
     return blk.reshape(rows, nb * Q8_0_BLOCK_BYTES)
+
+
+def gen_q4_0_rows(st: Stream, rows: int, k: int, d_range=(-1e-2, 1e-2)) -> np.ndarray:
+    """Raw Q4_0 rows, uint8 [rows, k/32*18]; d uniform in ``d_range`` (GGML's
+    quantizer gives d either sign, so both occur)."""
+    nb = k // QK8_0
+    z = st.draw(rows * nb * 3).reshape(rows * nb, 3)
+    blk = np.empty((rows * nb, Q4_0_BLOCK_BYTES), dtype=np.uint8)
+    blk[:, 0:2] = _uniform_f16_bits(z[:, 0], *d_range).view(np.uint8).reshape(-1, 2)
+    blk[:, 2:18] = _bytes_of(z[:, 1:3], 16)
+    return blk.reshape(rows, nb * Q4_0_BLOCK_BYTES)
+
+
+def gen_q5k_rows(st: Stream, rows: int, k: int,
+                 d_range=(5e-4, 2e-3), dmin_range=(0.0, 2e-3)) -> np.ndarray:
+    """Raw Q5_K rows, uint8 [rows, k/256*176]."""
+    nb = k // QK_K
+    z = st.draw(rows * nb * 24).reshape(rows * nb, 24)
+    blk = np.empty((rows * nb, Q5K_BLOCK_BYTES), dtype=np.uint8)
+    blk[:, 0:2] = _uniform_f16_bits(z[:, 0], *d_range).view(np.uint8).reshape(-1, 2)
+    blk[:, 2:4] = _uniform_f16_bits(z[:, 1], *dmin_range).view(np.uint8).reshape(-1, 2)
+    blk[:, 4:16] = _bytes_of(z[:, 2:4], 12)
+    blk[:, 16:48] = _bytes_of(z[:, 4:8], 32)
+    blk[:, 48:176] = _bytes_of(z[:, 8:24], 128)
+    return blk.reshape(rows, nb * Q5K_BLOCK_BYTES)
+
+
+GEN_ROWS = {"q4k": gen_q4k_rows, "q6k": gen_q6k_rows, "q8_0": gen_q8_0_rows,
+            "q4_0": gen_q4_0_rows, "q5k": gen_q5k_rows}
 
 
 def gen_normal(st: Stream, n: int) -> np.ndarray:

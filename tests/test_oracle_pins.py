@@ -75,13 +75,34 @@ def pack_q8_0(d_bits, q):
     return b
 
 
+def pack_q4_0(d_bits, q):
+    """Build a Q4_0 block: code i (0..15) of element i < 16 in the low nibble of
+    qs byte i, of element i >= 16 in the high nibble of qs byte i-16."""
+    b = np.zeros(18, dtype=np.uint8)
+    b[0], b[1] = d_bits & 0xFF, d_bits >> 8
+    for i in range(32):
+        b[2 + i % 16] |= (q[i] & 15) << (4 * (i // 16))
+    return b
+
+
+def pack_q5k(d_bits, dmin_bits, sc, m, q):
+    """Build a Q5_K block: the low 4 bits of each code placed as in
+    ``pack_q4k`` (qs at byte 48), bit 4 of element i's code as bit i//32 of
+    qh byte i%32 (qh at byte 16)."""
+    b4 = pack_q4k(d_bits, dmin_bits, sc, m, [v & 15 for v in q])
+    b = np.zeros(176, dtype=np.uint8)
+    b[0:16] = b4[0:16]
+    b[48:176] = b4[16:144]
+    for i in range(256):
+        b[16 + i % 32] |= ((q[i] >> 4) & 1) << (i // 32)
+    return b
+
+
 def rand_blocks(fmt, n, seed):
     st = synth.Stream(seed)
-    if fmt == "q4k":
-        return synth.gen_q4k_rows(st, n, 256)
-    if fmt == "q6k":
-        return synth.gen_q6k_rows(st, n, 256)
-    return synth.gen_q8_0_rows(st, n, 32, q_range=(-128, 127))
+    if fmt == "q8_0":
+        return synth.gen_q8_0_rows(st, n, 32, q_range=(-128, 127))
+    return synth.GEN_ROWS[fmt](st, n, oracle.QK[fmt])
 
 
 # --------------------------------------------------------------- f16 decode
@@ -204,9 +225,86 @@ def test_q8_0_closed_form():
     assert np.array_equal(oracle.decode_block("q8_0", b2), -3.0 * np.array(q2, dtype=np.float64))
 
 
+# --------------------------------------------------------------- Q4_0 pins
+
+def test_q4_0_closed_form_and_positions():
+    q = [(i * 7 + i // 16) % 16 for i in range(32)]
+    b = pack_q4_0(f16_bits(0.5), q)
+    assert np.array_equal(oracle.decode_block("q4_0", b), 0.5 * (np.array(q, dtype=np.float64) - 8))
+    b2 = pack_q4_0(f16_bits(-3.0), list(range(16)) + list(range(15, -1, -1)))
+    got = oracle.decode_block("q4_0", b2)
+    assert got[0] == 24.0 and got[15] == -21.0 and got[16] == -21.0 and got[31] == 24.0
+
+
+def test_q4_0_each_element_is_its_own_nibble():
+    """One non-zero code at a time: exactly one output moves, at its index."""
+    for i in range(32):
+        q = [8] * 32
+        q[i] = 9
+        got = oracle.decode_block("q4_0", pack_q4_0(f16_bits(1.0), q))
+        want = np.zeros(32)
+        want[i] = 1.0
+        assert np.array_equal(got, want)
+
+
+def test_q4_0_subnormal_d():
+    b = pack_q4_0(0x0001, [0] * 32)
+    assert np.all(oracle.decode_block("q4_0", b) == -8 * 2.0 ** -24)
+
+
+# --------------------------------------------------------------- Q5_K pins
+
+def test_q5k_closed_form_scales_and_codes():
+    q = [(i * 3 + i // 32) % 32 for i in range(256)]
+    b = pack_q5k(f16_bits(1.0), f16_bits(0.5), SC, MN, q)
+    want = np.array([SC[i // 32] * q[i] - 0.5 * MN[i // 32] for i in range(256)])
+    assert np.array_equal(oracle.decode_block("q5k", b), want)
+
+
+def test_q5k_fifth_bit_positions():
+    """Code 16 (only the fifth bit set) at one element at a time."""
+    for i in range(256):
+        q = [0] * 256
+        q[i] = 16
+        got = oracle.decode_block("q5k", pack_q5k(f16_bits(1.0), 0, [1] * 8, [0] * 8, q))
+        want = np.zeros(256)
+        want[i] = 16.0
+        assert np.array_equal(got, want), i
+
+
+def test_q5k_without_fifth_bits_is_q4k():
+    """With every qh byte zero a Q5_K block decodes as the Q4_K block holding
+    the same d, dmin, scales and qs bytes (the pinned Q4_K decoder)."""
+    blocks = rand_blocks("q5k", 300, 77)
+    for b in blocks:
+        b = b.copy()
+        b[16:48] = 0
+        b4 = np.concatenate([b[0:16], b[48:176]])
+        assert np.array_equal(oracle.decode_block("q5k", b), oracle.decode_block("q4k", b4))
+
+
+def test_q5k_fifth_bit_adds_sixteen_scaled_steps():
+    """Setting bit j of qh[l] adds exactly 16*d*sc_j to element 32*j + l."""
+    blocks = rand_blocks("q5k", 40, 78)
+    for n, b in enumerate(blocks):
+        b = b.copy()
+        j, l = n % 8, (n * 11) % 32
+        b[16 + l] &= ~np.uint8(1 << j)
+        base = oracle.decode_block("q5k", b)
+        b[16 + l] |= np.uint8(1 << j)
+        up = oracle.decode_block("q5k", b)
+        d = oracle.f16_to_f64(int(b[0]) | (int(b[1]) << 8))
+        s = b[4:16]
+        sc = (s[j] & 63) if j < 4 else ((s[j + 4] & 15) | ((s[j - 4] >> 6) << 4))
+        diff = up - base
+        assert diff[32 * j + l] == 16 * d * int(sc)
+        diff[32 * j + l] = 0
+        assert not np.any(diff)
+
+
 # -------------------------------------------- two independent decoders agree
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q4_0", "q5k"])
 def test_two_decoders_agree(fmt):
     n = 10000 if fmt != "q4k" else 10000
     blocks = rand_blocks(fmt, n, 100 + oracle.FMT[fmt])
@@ -224,11 +322,12 @@ def test_two_decoders_agree(fmt):
 # -------------------------------------------------- matvec: brute force etc.
 
 @pytest.mark.parametrize("fmt,rows,k", [("q4k", 3, 256), ("q4k", 4, 512), ("q6k", 2, 512),
-                                        ("q6k", 4, 256), ("q8_0", 4, 96), ("q8_0", 1, 512)])
+                                        ("q6k", 4, 256), ("q8_0", 4, 96), ("q8_0", 1, 512),
+                                        ("q4_0", 4, 96), ("q4_0", 2, 512), ("q5k", 3, 256),
+                                        ("q5k", 2, 768)])
 def test_matvec_brute_force(fmt, rows, k):
     st = synth.Stream(7 + rows + k)
-    gen = {"q4k": synth.gen_q4k_rows, "q6k": synth.gen_q6k_rows, "q8_0": synth.gen_q8_0_rows}[fmt]
-    w = gen(st, rows, k)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
     x = synth.gen_normal(st, k)
     W = oracle.dequant(fmt, w, rows, k)
     # brute force: the materialized f64 matrix times x by numpy, element by element
@@ -238,12 +337,11 @@ def test_matvec_brute_force(fmt, rows, k):
     assert np.allclose(W @ x.astype(np.float64), got, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q4_0", "q5k"])
 def test_matvec_unit_vector_and_row_sums(fmt):
     rows, k = 5, 512
     st = synth.Stream(31)
-    gen = {"q4k": synth.gen_q4k_rows, "q6k": synth.gen_q6k_rows, "q8_0": synth.gen_q8_0_rows}[fmt]
-    w = gen(st, rows, k)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
     W = oracle.dequant(fmt, w, rows, k)
     for j in [0, 1, 31, 32, 100, 255, 256, 511]:
         e = np.zeros(k, dtype=np.float32)
@@ -422,6 +520,24 @@ def test_moe_q6k_matches_dense_per_expert():
     W = oracle.dequant("q6k", bank, e * n, k).reshape(e, n, k)
     for s in range(slots):
         assert np.allclose(y[s], W[ids[s]] @ x[s].astype(np.float64), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+def test_moe_q8_0_and_q4_0_banks_match_dense_per_expert(fmt):
+    """The MoE oracle over a Q8_0 or Q4_0 bank equals the pinned dense matvec
+    of each slot's expert, and flags ids outside the bank with NaN."""
+    e, n, k, slots = 4, 3, 96, 4
+    st = synth.Stream(16 + oracle.FMT[fmt])
+    bank = synth.GEN_ROWS[fmt](st, e * n, k)
+    x = synth.gen_normal(st, slots * k).reshape(slots, k)
+    ids = np.array([2, 0, 3, 2], dtype=np.int32)
+    y = oracle.moe_qmv(fmt, bank, x, ids, n, k, e)
+    W = oracle.dequant(fmt, bank, e * n, k).reshape(e, n, k)
+    for s in range(slots):
+        assert np.allclose(y[s], W[ids[s]] @ x[s].astype(np.float64), rtol=1e-12, atol=1e-12)
+    y_bad = oracle.moe_qmv(fmt, bank, x, np.array([0, 4, -1, 1], dtype=np.int32), n, k, e)
+    assert np.all(np.isnan(y_bad[1])) and np.all(np.isnan(y_bad[2]))
+    assert not np.any(np.isnan(y_bad[0])) and not np.any(np.isnan(y_bad[3]))
 
 
 def test_moe_q4k_dp4a_matches_dense_per_expert_and_flags_bad_ids():
