@@ -76,19 +76,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Block format of each workload kind's weights.
+KIND_FMT = {"q4k": "q4k", "q4k_dp4a": "q4k", "q6k": "q6k", "q8_0_dp4a": "q8_0", "q5k": "q5k", "q4_0": "q4_0",
+            "moe_q4k": "q4k", "moe_q4k_dp4a": "q4k", "moe_q6k": "q6k", "moe_q8_0": "q8_0", "moe_q4_0": "q4_0",
+            "moe_q5k": "q5k"}
+# MoE kinds with an f32 activation (one entry point each, same arguments).
+MOE_F32 = ("moe_q4k", "moe_q6k", "moe_q8_0", "moe_q4_0", "moe_q5k")
+
+
 def weight_bytes(name: str) -> int:
     c = synth.CONFIGS[name]
-    if c["kind"] in ("q4k", "q4k_dp4a"):
-        return synth.row_bytes("q4k", c["k"]) * c["rows"]
-    if c["kind"] == "q6k":
-        return synth.row_bytes("q6k", c["k"]) * c["rows"]
-    if c["kind"] == "q8_0_dp4a":
-        return synth.row_bytes("q8_0", c["k"]) * c["rows"]
-    if c["kind"] in ("moe_q4k", "moe_q4k_dp4a"):
-        return synth.row_bytes("q4k", c["k"]) * c["rows"] * c["slots"]   # routed rows only
-    if c["kind"] == "moe_q6k":
-        return synth.row_bytes("q6k", c["k"]) * c["rows"] * c["slots"]
-    raise ValueError(name)
+    rb = synth.row_bytes(KIND_FMT[c["kind"]], c["k"]) * c["rows"]
+    if c["kind"].startswith("moe_"):
+        return rb * c["slots"]   # routed rows only
+    return rb
 
 
 def algorithmic_bytes(name: str) -> int:
@@ -96,7 +97,7 @@ def algorithmic_bytes(name: str) -> int:
     read, output written."""
     c = synth.CONFIGS[name]
     wb = weight_bytes(name)
-    if c["kind"] in ("moe_q4k", "moe_q6k"):
+    if c["kind"] in MOE_F32:
         return wb + 4 * c["slots"] * c["k"] + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
     if c["kind"] == "moe_q4k_dp4a":
         return wb + c["slots"] * (c["k"] + 4 * (c["k"] // 32)) + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
@@ -213,8 +214,8 @@ class Workload:
         q, w, cfg = self.q, self.w[i % self.copies], self.cfg
         if self.kind == "q4k":
             q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
-        elif self.kind == "q6k":
-            q.qmv_q6k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
+        elif self.kind in ("q6k", "q5k", "q4_0"):
+            getattr(q, f"qmv_{self.kind}")(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
         elif self.kind in ("q8_0_dp4a", "q4k_dp4a"):
             n = 1
             if with_quant:
@@ -223,9 +224,9 @@ class Workload:
             fn = q.qmv_q8_dp4a if self.kind == "q8_0_dp4a" else q.qmv_q4k_dp4a
             fn(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg)
             return n
-        elif self.kind in ("moe_q4k", "moe_q6k"):
+        elif self.kind in MOE_F32:
             c = self.c
-            fn = q.moe_qmv_q4k if self.kind == "moe_q4k" else q.moe_qmv_q6k
+            fn = getattr(q, f"moe_qmv_{self.kind[4:]}")
             fn(w, self.x, self.y, self.rows, self.k, self.ids[i % len(self.ids)], c["slots"],
                c["n_experts"], stream=stream, cfg=cfg)
         elif self.kind == "moe_q4k_dp4a":

@@ -26,7 +26,8 @@ QMV_ETOOBIG = -4
 QMV_STATUS_BAD_EXPERT_ID = 1
 QMV_STATUS_WAIT_TIMEOUT = 2
 
-FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A = range(8)
+(FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A,
+ FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K) = range(13)
 
 
 class QmvLibraryMissing(RuntimeError):
@@ -71,6 +72,18 @@ _SIG = {
     "qmv_dequant_q4k": [_P, _P, _I, _I, _P],
     "qmv_dequant_q6k": [_P, _P, _I, _I, _P],
     "qmv_dequant_q8_0": [_P, _P, _I, _I, _P],
+    "qmv_dequant_q5k": [_P, _P, _I, _I, _P],
+    "qmv_dequant_q4_0": [_P, _P, _I, _I, _P],
+    "qmv_q5k": [_P, _P, _P, _I, _I, _P],
+    "qmv_q5k_cfg": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q4_0": [_P, _P, _P, _I, _I, _P],
+    "qmv_q4_0_cfg": [_P, _P, _P, _I, _I, _P, _P],
+    "moe_qmv_q8_0": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
+    "moe_qmv_q8_0_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q4_0": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
+    "moe_qmv_q4_0_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q5k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
+    "moe_qmv_q5k_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "qmv_q8_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_device_status": [_P, _I],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
@@ -161,6 +174,18 @@ def qmv_q8_0(w, x, y, rows, k, stream=None, cfg=None, check=True):
     return _call("qmv_q8_0_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
 
 
+def qmv_q5k(w, x, y, rows, k, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("qmv_q5k", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q5k_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+
+
+def qmv_q4_0(w, x, y, rows, k, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("qmv_q4_0", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q4_0_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+
+
 def quantize_act_q8(x, xq, xs, xsum, m, k, stream=None, check=True):
     return _call("quantize_act_q8", _ptr(x), _ptr(xq), _ptr(xs), _ptr(xsum), m, k, _stream(stream), check=check)
 
@@ -199,6 +224,26 @@ def moe_qmv_q6k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=N
                  _cfg(cfg), _stream(stream), check=check)
 
 
+def _moe_f32(name, w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check):
+    if cfg is None:
+        return _call(name, _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                     _stream(stream), check=check)
+    return _call(name + "_cfg", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                 _cfg(cfg), _stream(stream), check=check)
+
+
+def moe_qmv_q8_0(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
+    return _moe_f32("moe_qmv_q8_0", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check)
+
+
+def moe_qmv_q4_0(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
+    return _moe_f32("moe_qmv_q4_0", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check)
+
+
+def moe_qmv_q5k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
+    return _moe_f32("moe_qmv_q5k", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check)
+
+
 def moe_qmv_q4k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
     if cfg is None:
         return _call("moe_qmv_q4k_dp4a", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
@@ -217,6 +262,14 @@ def qmv_dequant_q6k(w, out, rows, k, stream=None, check=True):
 
 def qmv_dequant_q8_0(w, out, rows, k, stream=None, check=True):
     return _call("qmv_dequant_q8_0", _ptr(w), _ptr(out), rows, k, _stream(stream), check=check)
+
+
+def qmv_dequant_q5k(w, out, rows, k, stream=None, check=True):
+    return _call("qmv_dequant_q5k", _ptr(w), _ptr(out), rows, k, _stream(stream), check=check)
+
+
+def qmv_dequant_q4_0(w, out, rows, k, stream=None, check=True):
+    return _call("qmv_dequant_q4_0", _ptr(w), _ptr(out), rows, k, _stream(stream), check=check)
 
 
 def qmv_q8_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):

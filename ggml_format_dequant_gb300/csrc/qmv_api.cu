@@ -68,6 +68,26 @@ int qmv_q8_0(const void* w, const float* x, float* y, int rows, int k, cudaStrea
     return qmv_q8_0_cfg(w, x, y, rows, k, nullptr, stream);
 }
 
+int qmv_q5k_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+                cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 176);
+    return rc ? rc : qmvi::q5k(w, x, y, rows, k, cfg, stream);
+}
+
+int qmv_q5k(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
+    return qmv_q5k_cfg(w, x, y, rows, k, nullptr, stream);
+}
+
+int qmv_q4_0_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+                 cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 32, 18);
+    return rc ? rc : qmvi::q4_0(w, x, y, rows, k, cfg, stream);
+}
+
+int qmv_q4_0(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
+    return qmv_q4_0_cfg(w, x, y, rows, k, nullptr, stream);
+}
+
 int quantize_act_q8(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t stream) {
     if (!x || !xq || !xs) return QMV_EINVAL;
     if (m <= 0 || k <= 0 || k % 32) return QMV_EINVAL;
@@ -128,6 +148,42 @@ int moe_qmv_q6k(const void* w_bank, const float* x, float* y, int rows, int k, c
     return moe_qmv_q6k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
+int moe_qmv_q8_0_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                     int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+    int rc = check_dense(w_bank, x, y, rows, k, 32, 34);
+    if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 32, 34);
+    return rc ? rc : qmvi::moe_q8_0(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
+}
+
+int moe_qmv_q8_0(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                 int n_experts, cudaStream_t stream) {
+    return moe_qmv_q8_0_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+}
+
+int moe_qmv_q4_0_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                     int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+    int rc = check_dense(w_bank, x, y, rows, k, 32, 18);
+    if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 32, 18);
+    return rc ? rc : qmvi::moe_q4_0(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
+}
+
+int moe_qmv_q4_0(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                 int n_experts, cudaStream_t stream) {
+    return moe_qmv_q4_0_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+}
+
+int moe_qmv_q5k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                    int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+    int rc = check_dense(w_bank, x, y, rows, k, 256, 176);
+    if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 176);
+    return rc ? rc : qmvi::moe_q5k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
+}
+
+int moe_qmv_q5k(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                int n_experts, cudaStream_t stream) {
+    return moe_qmv_q5k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+}
+
 int moe_qmv_q4k_dp4a_cfg(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
                          const int32_t* ids, int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
     if (!xs) return QMV_EINVAL;
@@ -156,6 +212,16 @@ int qmv_dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t str
 int qmv_dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t stream) {
     int rc = check_dense(w, w, out, rows, k, 32, 34);
     return rc ? rc : qmvi::dequant_q8_0(w, out, rows, k, stream);
+}
+
+int qmv_dequant_q5k(const void* w, float* out, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, w, out, rows, k, 256, 176);
+    return rc ? rc : qmvi::dequant_q5k(w, out, rows, k, stream);
+}
+
+int qmv_dequant_q4_0(const void* w, float* out, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, w, out, rows, k, 32, 18);
+    return rc ? rc : qmvi::dequant_q4_0(w, out, rows, k, stream);
 }
 
 int qmv_q8_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t stream) {
@@ -195,23 +261,28 @@ const char* qmv_last_cuda_error(void) {
 
 int qmv_device_status(unsigned int* status, int clear) {
     if (!status) return QMV_EINVAL;
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0, e = 0;
     int rc = qmvi::status_q4k(&a, clear);
     if (!rc) rc = qmvi::status_q6k(&b, clear);
     if (!rc) rc = qmvi::status_q8(&c, clear);
+    if (!rc) rc = qmvi::status_q5k(&d, clear);
+    if (!rc) rc = qmvi::status_q4_0(&e, clear);
     if (rc) return rc;
-    *status = a | b | c;
+    *status = a | b | c | d | e;
     return QMV_OK;
 }
 
 namespace {
 
+// Plan ids that describe an MoE launch (grid.y = slots).
+bool plan_is_moe(int fmt) { return fmt == 4 || fmt == 6 || fmt == 7 || fmt >= 10; }
+
 // Plan of format fmt on device `di`.
 int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_cfg* cfg, qmv::KParams* kp,
             qmv::Plan* pl) {
-    static const int qk[8] = {256, 256, 32, 32, 256, 256, 256, 256};
-    if (fmt < 0 || fmt > 7 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
-    const bool moe = fmt == 4 || fmt == 6 || fmt == 7;
+    static const int qk[13] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256};
+    if (fmt < 0 || fmt > 12 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
+    const bool moe = plan_is_moe(fmt);
     if (moe && slots <= 0) return QMV_EINVAL;
     if (!moe) slots = 1;
     switch (fmt) {
@@ -222,6 +293,11 @@ int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const q
     case 5: return qmv::make_plan_for<qmv::Q4D>(di, rows, k, 1, cfg, kp, pl);
     case 6: return qmv::make_plan_for<qmv::Q6K>(di, rows, k, slots, cfg, kp, pl);
     case 7: return qmv::make_plan_for<qmv::Q4D>(di, rows, k, slots, cfg, kp, pl);
+    case 8: return qmv::make_plan_for<qmv::Q5K>(di, rows, k, 1, cfg, kp, pl);
+    case 9: return qmv::make_plan_for<qmv::Q40>(di, rows, k, 1, cfg, kp, pl);
+    case 10: return qmv::make_plan_for<qmv::Q8F>(di, rows, k, slots, cfg, kp, pl);
+    case 11: return qmv::make_plan_for<qmv::Q40>(di, rows, k, slots, cfg, kp, pl);
+    case 12: return qmv::make_plan_for<qmv::Q5K>(di, rows, k, slots, cfg, kp, pl);
     default: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, slots, cfg, kp, pl);
     }
 }
@@ -238,7 +314,7 @@ int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* 
     rc = plan_of(di, fmt, rows, k, slots, cfg, &kp, &pl);
     if (rc) return rc;
     if (threads) *threads = pl.T;
-    if (ctas) *ctas = pl.parts * ((fmt == 4 || fmt == 6 || fmt == 7) ? slots : 1);
+    if (ctas) *ctas = pl.parts * (plan_is_moe(fmt) ? slots : 1);
     if (chunk_rows) *chunk_rows = kp.CR;
     if (chunks) *chunks = kp.S;
     if (smem_bytes) *smem_bytes = static_cast<int>(pl.smem);

@@ -1,10 +1,11 @@
 // qmv_formats.cuh -- in-register decode of one "unit" of a packed GGML block
-// against the activation, for Q4_K, Q6_K and Q8_0.
+// against the activation, for Q4_K, Q5_K, Q6_K, Q8_0 and Q4_0.
 //
 // A unit is the part of a row one lane owns for every row it processes:
-//   Q4_K: one 64-weight chunk of a 256-weight super-block (4 per block)
+//   Q4_K, Q5_K: one 64-weight chunk of a 256-weight super-block (4 per block)
 //   Q6_K: one (half, 16-position) slice of a block, 64 weights (4 per block)
 //   Q8_0, f32 x: one 32-weight block;  Q8_0, q8 x (dp4a): four blocks
+//   Q4_0: one 32-weight block
 // The lane keeps the activation for its unit in registers (as integer limbs or
 // int8 codes) and, per row, reads the unit's packed bytes from the staged
 // rows in shared memory (by 32-bit address), unpacks the codes into byte lanes
@@ -14,8 +15,10 @@
 // Block layouts (hanzo-ml src/vulkan_backend.rs): Q4_K = d, dmin (f16), 12 bytes
 // of packed 6-bit scales/mins, 128 bytes of 4-bit codes (quantize_q4k,
 // quantize_q4k_split); Q6_K = ql[128], qh[64], int8 scales[16], d (f16)
-// (quantize_q6k); Q8_0 = d (f16) + 32 int8 (quantize_q8_blocks). The bit
-// mapping inside the blocks is GGML's k-quant layout.
+// (quantize_q6k); Q8_0 = d (f16) + 32 int8 (quantize_q8_blocks); Q5_K = d,
+// dmin (f16), 12 scale bytes, qh[32], qs[128] (quantize_q5k); Q4_0 = d (f16)
+// + 16 bytes of 4-bit codes (matvec_q4_0_gpu). The bit mapping inside the
+// blocks is GGML's layout.
 //
 // Every format states SLICE_BLOCKS (blocks of a row covered by one warp's 32
 // units) and SLACK (bytes its loads may read past the end of a row).
@@ -240,6 +243,96 @@ struct Q4D {
     }
 };
 
+// ====================================================================== Q5_K
+//
+// Laid out as Q4_K with 32 bytes qh between the scales and the codes: chunk c
+// covers weights 64c .. 64c+63, the low 4 bits of its codes are the nibbles of
+// qs bytes 32c .. 32c+31 (low: sub-block 2c, high: 2c+1), and the fifth bit of
+// the code at position l of sub-block j is bit j of qh[l]. So qs word i and
+// qh word i (bytes 4i .. 4i+3) carry the same four positions, and rotating the
+// qh word left by 4 - 2c brings, in every byte, bit 2c to bit 4 and bit 2c+1
+// to bit 5. w = d*sc_j*q - dmin*m_j with q in [0, 31].
+struct Q5K {
+    static constexpr int QK = 256;
+    static constexpr int BLOCK_BYTES = 176;
+    static constexpr int SLICE_BLOCKS = 8;    // 32 units (1408 bytes)
+    static constexpr int SLACK = 0;
+    static constexpr bool LIMBS = true;
+    static constexpr int DEFAULT_UNROLL = 2;
+
+    __host__ __device__ static int units(int nb) { return 4 * nb; }
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u >> 2) * BLOCK_BYTES; }
+    __device__ __forceinline__ static int unit_elem(int u) { return (u >> 2) * QK + 64 * (u & 3); }
+
+    using X = Q4K::X;
+    struct L {
+        uint32_t qoff;   // byte offset of the chunk's codes in the block: 48 + 32c
+        uint32_t sel;    // prmt selector of scale byte 2(c & 1), as in Q4K
+        uint32_t rot;    // left rotation of the qh words: (4 - 2c) mod 32
+        bool hic;        // c >= 2
+    };
+
+    __device__ __forceinline__ static L lane_consts(int u, int /*nb*/, int /*ug*/) {
+        const int c = u & 3;
+        L l;
+        l.qoff = 48u + 32u * static_cast<uint32_t>(c);
+        l.sel = 0x7440u | static_cast<uint32_t>(2 * (c & 1));
+        l.rot = static_cast<uint32_t>(4 - 2 * c) & 31u;
+        l.hic = c >= 2;
+        return l;
+    }
+
+    __device__ __forceinline__ static void load_x(X& x, const uint8_t* smem, const LimbTables& T, int e0) {
+        Q4K::load_x(x, smem, T, e0);
+    }
+
+    // a: shared address of the super-block (16-byte aligned).
+    __device__ __forceinline__ static float dot(uint32_t a, const L& l, const X& x, float r) {
+        const uint4 h = lds128<0>(a);
+        const uint4 ha = lds128<16>(a);
+        const uint4 hb = lds128<32>(a);
+        const uint32_t aq = a + l.qoff;
+        const uint4 qa = lds128<0>(aq);
+        const uint4 qb = lds128<16>(aq);
+        const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const uint32_t qh[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+        int a0 = 0, b0 = 0, c0 = 0, a1 = 0, b1 = 0, c1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t t = __funnelshift_l(qh[i], qh[i], l.rot);
+            const uint32_t lo = (q[i] & 0x0f0f0f0fu) | (t & 0x10101010u);         // codes of sub-block 2c
+            const uint32_t hi = ((q[i] >> 3) & 0x1e1e1e1eu) | (t & 0x20202020u);  // 2 * codes of 2c+1
+            a0 = dp4a_us(lo, x.a[i], a0);
+            b0 = dp4a_us(lo, x.b[i], b0);
+            c0 = dp4a_us(lo, x.c[i], c0);
+            a1 = dp4a_us(hi, x.a[8 + i], a1);
+            b1 = dp4a_us(hi, x.b[8 + i], b1);
+            c1 = dp4a_us(hi, x.c[8 + i], c1);
+        }
+        // Exact sums q*X, |.| <= 32 * 31 * 2^21 < 2^31 per sub-block; the
+        // second carries a factor 2 (even limb sums, so the shift is exact).
+        const int s0 = a0 * 65536 + b0 * 256 + c0;
+        const int s1 = a1 * 32768 + b1 * 128 + (c1 >> 1);
+        const uint32_t sc_lo = h.y & 0x3f3f3f3fu;
+        const uint32_t m_lo = h.z & 0x3f3f3f3fu;
+        const uint32_t sc_hi = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
+        const uint32_t m_hi = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+        const uint32_t SC = l.hic ? sc_hi : sc_lo;
+        const uint32_t M = l.hic ? m_hi : m_lo;
+        const float d = f16_lo(h.x), dmin = f16_hi(h.x);
+        const float nd = -d * TWO23, ndm = -dmin * TWO23;
+        const float dsc0 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel)), nd);
+        const float dsc1 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel + 1)), nd);
+        const float dm0 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel)), ndm);
+        const float dm1 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel + 1)), ndm);
+        r = __fmaf_rn(dsc0, __int2float_rn(s0) * x.xs0, r);
+        r = __fmaf_rn(-dm0, x.xsum0, r);
+        r = __fmaf_rn(dsc1, __int2float_rn(s1) * x.xs1, r);
+        r = __fmaf_rn(-dm1, x.xsum1, r);
+        return r;
+    }
+};
+
 // ====================================================================== Q6_K
 //
 // Unit v = 2*H + hh of a block covers, in half H (weights 128H..128H+127), the
@@ -409,6 +502,80 @@ struct Q8F {
         // in f32 (the full integer could exceed 2^31 here).
         const float t = __fmaf_rn(__int2float_rn(sa), 65536.0f, __int2float_rn(sb * 256 + sc)) * x.xs;
         return __fmaf_rn(d, t, r);
+    }
+};
+
+// ============================================================ Q4_0, f32 x
+//
+// The native 18-byte block: d (f16), then 16 bytes whose low nibbles are the
+// codes of weights 0..15 and high nibbles those of weights 16..31;
+// w = d*(q - 8), so the block contributes d*(sum(q*x) - 8*sum(x)). Blocks sit
+// at 2-byte alignment; five 32-bit loads from the word below the block hold
+// all of it.
+struct Q40 {
+    static constexpr int QK = 32;
+    static constexpr int BLOCK_BYTES = 18;
+    static constexpr int SLICE_BLOCKS = 32;   // 32 one-block units (576 bytes)
+    static constexpr int SLACK = 16;
+    static constexpr bool LIMBS = true;
+    static constexpr int DEFAULT_UNROLL = 2;
+
+    __host__ __device__ static int units(int nb) { return nb; }
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u) * BLOCK_BYTES; }
+    __device__ __forceinline__ static int unit_elem(int u) { return u * QK; }
+
+    struct X {
+        uint32_t a[8], b[8], c[8];   // limbs of the block's 32 activations
+        float xs;                    // 2^-s of the 32-group
+        float xsum;                  // its activation sum
+    };
+    struct L {
+        int unused;
+    };
+    __device__ __forceinline__ static L lane_consts(int, int, int) { return L{0}; }
+
+    __device__ __forceinline__ static void load_x(X& x, const uint8_t* smem, const LimbTables& T, int e0) {
+#pragma unroll
+        for (int v = 0; v < 2; v++) {
+            const uint32_t o = limb_chunk(static_cast<uint32_t>(e0 >> 4) + v) << 4;
+            const uint4 a = *reinterpret_cast<const uint4*>(smem + T.la + o);
+            const uint4 b = *reinterpret_cast<const uint4*>(smem + T.lb + o);
+            const uint4 c = *reinterpret_cast<const uint4*>(smem + T.lc + o);
+            x.a[4 * v] = a.x; x.a[4 * v + 1] = a.y; x.a[4 * v + 2] = a.z; x.a[4 * v + 3] = a.w;
+            x.b[4 * v] = b.x; x.b[4 * v + 1] = b.y; x.b[4 * v + 2] = b.z; x.b[4 * v + 3] = b.w;
+            x.c[4 * v] = c.x; x.c[4 * v + 1] = c.y; x.c[4 * v + 2] = c.z; x.c[4 * v + 3] = c.w;
+        }
+        const float* xsum16 = reinterpret_cast<const float*>(smem + T.xsum16);
+        x.xs = reinterpret_cast<const float*>(smem + T.xs)[e0 >> 5];
+        x.xsum = xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1];
+    }
+
+    // a: shared address of the 18-byte block (2-byte aligned).
+    __device__ __forceinline__ static float dot(uint32_t a, const L&, const X& x, float r) {
+        const uint32_t wa = a & ~3u;
+        const uint32_t sh = (a & 3u) * 8u;   // 0 or 16
+        const uint32_t w[5] = {lds32<0>(wa), lds32<4>(wa), lds32<8>(wa), lds32<12>(wa), lds32<16>(wa)};
+        const float d = f16_lo(__funnelshift_r(w[0], w[1], sh));
+        int a0 = 0, b0 = 0, c0 = 0, a1 = 0, b1 = 0, c1 = 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            // code bytes 4j .. 4j+3 start 2 + 4j bytes past the block; the
+            // clamped shift (16 or 32) takes them from words j, j+1
+            const uint32_t q = __funnelshift_rc(w[j], w[j + 1], 16u + sh);
+            const uint32_t lo = q & 0x0f0f0f0fu;   // weights 4j .. 4j+3
+            const uint32_t hi = q & 0xf0f0f0f0u;   // 16 * weights 16+4j ..
+            a0 = dp4a_us(lo, x.a[j], a0);
+            b0 = dp4a_us(lo, x.b[j], b0);
+            c0 = dp4a_us(lo, x.c[j], c0);
+            a1 = dp4a_us(hi, x.a[4 + j], a1);
+            b1 = dp4a_us(hi, x.b[4 + j], b1);
+            c1 = dp4a_us(hi, x.c[4 + j], c1);
+        }
+        // |sum q*X| <= 16 * 15 * 2^21 per half; the high half carries a factor
+        // 16 (multiples of 16, so the shift of c1 is exact).
+        const int s = (a0 * 65536 + b0 * 256 + c0) + (a1 * 4096 + b1 * 16 + (c1 >> 4));
+        const float t = __int2float_rn(s) * x.xs;
+        return __fmaf_rn(d, __fmaf_rn(-8.0f, x.xsum, t), r);
     }
 };
 

@@ -28,8 +28,24 @@ int moe_q6k(const void* bank, const float* x, float* y, int rows, int k, const i
 int dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t s);
 int status_q6k(unsigned int* out, int clear);
 
+// qmv_q5k.cu
+int q5k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s);
+int moe_q5k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+            int n_experts, const qmv_cfg* cfg, cudaStream_t s);
+int dequant_q5k(const void* w, float* out, int rows, int k, cudaStream_t s);
+int status_q5k(unsigned int* out, int clear);
+
+// qmv_q4_0.cu
+int q4_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s);
+int moe_q4_0(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+             int n_experts, const qmv_cfg* cfg, cudaStream_t s);
+int dequant_q4_0(const void* w, float* out, int rows, int k, cudaStream_t s);
+int status_q4_0(unsigned int* out, int clear);
+
 // qmv_q8.cu
 int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s);
+int moe_q8_0(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+             int n_experts, const qmv_cfg* cfg, cudaStream_t s);
 int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
             cudaStream_t s);
 int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s);

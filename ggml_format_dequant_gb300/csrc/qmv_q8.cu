@@ -1,4 +1,4 @@
-// qmv_q8.cu -- Q8_0 matvecs (f32 activation and dp4a), the dp4a block dots,
+// qmv_q8.cu -- Q8_0 matvecs (f32 activation, dense and MoE, and dp4a), the dp4a block dots,
 // the activation quantizer and the Q8_0 dequantizer.
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
@@ -76,6 +76,20 @@ int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg
     int rc = make_plan<Q8F>(rows, k, 1, cfg, &kp, &pl);
     if (rc) return rc;
     return launch<Q8F, false, MODE_MATVEC>(kp, pl, 1, s);
+}
+
+int moe_q8_0(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+             int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+    KParams kp = q8_params(bank, rows, k);
+    kp.x = x;
+    kp.y = y;
+    kp.ids = ids;
+    kp.n_experts = n_experts;
+    kp.wbytes = static_cast<unsigned long long>(n_experts) * kp.matbytes;
+    Plan pl;
+    int rc = make_plan<Q8F>(rows, k, slots, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q8F, true, MODE_MATVEC>(kp, pl, slots, s);
 }
 
 int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,

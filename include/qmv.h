@@ -12,7 +12,13 @@
  *   Q6_K: 210-byte blocks of 256 weights (ql[128], qh[64], int8 scales[16],
  *         d f16), w = d*scale*(q - 32) (quantize_q6k);
  *   Q8_0: 34-byte blocks of 32 weights (d f16 then 32 int8), w = d*q
- *         (quantize_q8_blocks).
+ *         (quantize_q8_blocks);
+ *   Q5_K: 176-byte super-blocks of 256 weights (d, dmin f16; 12 scale bytes
+ *         packed as Q4_K's; qh[32]; qs[128]), 5-bit codes whose fifth bit for
+ *         weight i is bit i/32 of qh[i%32], w = d*sc_j*q - dmin*m_j
+ *         (quantize_q5k, matvec_q5k_gpu);
+ *   Q4_0: 18-byte blocks of 32 weights (d f16, then 16 bytes: low nibbles are
+ *         weights 0..15, high nibbles 16..31), w = d*(q - 8) (matvec_q4_0_gpu).
  *
  * Conventions shared by every entry point:
  *  - All data pointers are DEVICE pointers owned by the caller. The library
@@ -70,6 +76,16 @@ int qmv_q6k(const void *w, const float *x, float *y, int rows, int k, cudaStream
  * Cites hanzo-ml src/vulkan_backend.rs, matvec_q8_0_gpu (raw 34-byte blocks). */
 int qmv_q8_0(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
 
+/* Q5_K matvec: y = W x. w: rows * (k/256) * 176 bytes (verbatim GGUF
+ * super-blocks); x: f32 [k]; y: f32 [rows]; k % 256 == 0.
+ * Cites hanzo-ml src/vulkan_backend.rs, matvec_q5k_gpu and quantize_q5k. */
+int qmv_q5k(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
+
+/* Q4_0 matvec: y = W x. w: rows * (k/32) * 18 bytes (native 18-byte blocks,
+ * read unpadded); x: f32 [k]; y: f32 [rows]; k % 32 == 0.
+ * Cites hanzo-ml src/vulkan_backend.rs, matvec_q4_0_gpu. */
+int qmv_q4_0(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
+
 /* Activation quantization for the dp4a path, per 32-element block of x[m, k]:
  * amax = max|x|; inv = 127/amax and d = amax/127 (IEEE f32 divides);
  * q = clamp(round_half_even(x * inv), -127, 127) (one f32 multiply); amax == 0
@@ -119,6 +135,24 @@ int moe_qmv_q4k(const void *w_bank, const float *x, float *y, int rows, int k,
  * moe_qmv_q4k (out-of-range ids: NaN rows and QMV_STATUS_BAD_EXPERT_ID).
  * Cites hanzo-ml src/vulkan_backend.rs, the `moe_matvec_q6k*` kernels. */
 int moe_qmv_q6k(const void *w_bank, const float *x, float *y, int rows, int k,
+                const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+
+/* MoE indexed matvecs over banks of the other formats, f32 activation; bank
+ * layout [n_experts, rows, k] of verbatim rows (expert e's matrix starts at
+ * byte e * rows * (k / block_weights) * block_bytes), x, y, ids and errors as
+ * for moe_qmv_q4k.
+ *   moe_qmv_q8_0: 34-byte Q8_0 blocks, k % 32 == 0 (the pages' moe_matvec_q8_0
+ *                 reads a repacked bank; here the blocks are read as stored);
+ *   moe_qmv_q4_0: 18-byte Q4_0 blocks, k % 32 == 0 (moe_matvec_q4_0);
+ *   moe_qmv_q5k:  176-byte Q5_K blocks, k % 256 == 0 (one expert's slice of a
+ *                 bank, as matvec_q5k_gpu_off selects it, for every slot).
+ * Cites hanzo-ml src/vulkan_backend.rs, moe_matvec_gpu and the
+ * `moe_matvec_q8_0` / `moe_matvec_q4_0` kernels. */
+int moe_qmv_q8_0(const void *w_bank, const float *x, float *y, int rows, int k,
+                 const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+int moe_qmv_q4_0(const void *w_bank, const float *x, float *y, int rows, int k,
+                 const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+int moe_qmv_q5k(const void *w_bank, const float *x, float *y, int rows, int k,
                 const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
 
 /* MoE indexed Q4_K matvec on the dp4a path: slot s multiplies expert ids[s]
@@ -204,12 +238,27 @@ int moe_qmv_q4k_dp4a_cfg(const void *w_bank, const int8_t *xq, const float *xs, 
 int moe_qmv_q4k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
                     cudaStream_t stream);
+int qmv_q5k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
+                cudaStream_t stream);
+int qmv_q4_0_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
+                 cudaStream_t stream);
+int moe_qmv_q8_0_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
+                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
+                     cudaStream_t stream);
+int moe_qmv_q4_0_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
+                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
+                     cudaStream_t stream);
+int moe_qmv_q5k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
+                    const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
+                    cudaStream_t stream);
 
 /* Exact decoded weights: out f32 [rows, k] (each the round-to-nearest f32 of
  * the weight's exact value). Same argument rules as the matvecs. */
 int qmv_dequant_q4k(const void *w, float *out, int rows, int k, cudaStream_t stream);
 int qmv_dequant_q6k(const void *w, float *out, int rows, int k, cudaStream_t stream);
 int qmv_dequant_q8_0(const void *w, float *out, int rows, int k, cudaStream_t stream);
+int qmv_dequant_q5k(const void *w, float *out, int rows, int k, cudaStream_t stream);
+int qmv_dequant_q4_0(const void *w, float *out, int rows, int k, cudaStream_t stream);
 
 /* Per-block int32 dots of the dp4a path, dots[r, b] (int32 [rows, k/32]),
  * computed by the same code path qmv_q8_dp4a uses. */
@@ -224,7 +273,8 @@ int qmv_q4k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int r
  * CTAs (all slots), rows per ring slot, ring slots per row group and dynamic
  * shared bytes per CTA.
  * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K,
- * 5 = Q4_K dp4a, 6 = MoE Q6_K, 7 = MoE Q4_K dp4a. */
+ * 5 = Q4_K dp4a, 6 = MoE Q6_K, 7 = MoE Q4_K dp4a, 8 = Q5_K, 9 = Q4_0,
+ * 10 = MoE Q8_0, 11 = MoE Q4_0, 12 = MoE Q5_K. */
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
                   int *chunk_rows, int *chunks, int *smem_bytes);
 

@@ -210,6 +210,13 @@ CONFIGS = {
     "moe_q4k_dp4a_e128_n768_k2048_s8": dict(kind="moe_q4k_dp4a", rows=768, k=2048, seed=3,
                                             n_experts=128, slots=8),
     "moe_q6k_e128_n2048_k768_s8": dict(kind="moe_q6k", rows=2048, k=768, seed=5, n_experts=128, slots=8),
+    # The other formats of the same kernel skeleton: dense Q5_K and Q4_0 at the
+    # headline shape, and MoE over Q8_0, Q4_0 and Q5_K banks at the MoE shape.
+    "q5k_4096x4096": dict(kind="q5k", rows=4096, k=4096, seed=6),
+    "q4_0_4096x4096": dict(kind="q4_0", rows=4096, k=4096, seed=7),
+    "moe_q8_0_e128_n768_k2048_s8": dict(kind="moe_q8_0", rows=768, k=2048, seed=8, n_experts=128, slots=8),
+    "moe_q4_0_e128_n768_k2048_s8": dict(kind="moe_q4_0", rows=768, k=2048, seed=9, n_experts=128, slots=8),
+    "moe_q5k_e128_n768_k2048_s8": dict(kind="moe_q5k", rows=768, k=2048, seed=10, n_experts=128, slots=8),
 }
 
 
@@ -228,10 +235,13 @@ def make_config(name: str) -> dict:
     elif kind == "q8_0_dp4a":
         c["w"] = gen_q8_0_rows(st, rows, k)
         c["x"] = gen_normal(st, k)
-    elif kind in ("moe_q4k", "moe_q4k_dp4a", "moe_q6k"):
+    elif kind in ("q5k", "q4_0"):
+        c["w"] = GEN_ROWS[kind](st, rows, k)
+        c["x"] = gen_normal(st, k)
+    elif kind in ("moe_q4k", "moe_q4k_dp4a", "moe_q6k", "moe_q8_0", "moe_q4_0", "moe_q5k"):
         e, s = c["n_experts"], c["slots"]
-        gen = gen_q6k_rows if kind == "moe_q6k" else gen_q4k_rows
-        c["w"] = gen(st, e * rows, k).reshape(e, rows, -1)
+        fmt = "q4k" if kind == "moe_q4k_dp4a" else kind[4:]
+        c["w"] = GEN_ROWS[fmt](st, e * rows, k).reshape(e, rows, -1)
         c["ids"] = gen_moe_ids(st, s, e)
         c["x"] = gen_normal(st, s * k).reshape(s, k)
     else:

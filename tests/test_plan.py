@@ -7,7 +7,7 @@ that every index the kernel forms is checked before it runs:
 * every shared-memory read of a unit (including the bytes a format's loads
   read past its block) stays inside its ring slot, and every slot holds the
   16-byte-aligned cover its bulk copy writes;
-* unit addresses have the alignment their loads need (16 bytes for Q4_K, 8 for
+* unit addresses have the alignment their loads need (16 bytes for Q4_K and Q5_K, 8 for
   the aligned Q8_0 dp4a path, 2 otherwise);
 * parked partials stay inside the CTA's table, and the shared-memory regions
   are disjoint and fit the device.
@@ -19,7 +19,8 @@ import numpy as np
 import pytest
 
 DEVICE = (152, 232448, 233472, 1024)
-FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5, "moe6": 6, "moe4d": 7}
+FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5, "moe6": 6, "moe4d": 7, "q5k": 8,
+          "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12}
 
 
 # Per format: weights per block, bytes per block, blocks per warp slice,
@@ -29,10 +30,17 @@ def fmt_info(fmt):
     if fmt in ("q4k", "moe", "q4d", "moe4d"):
         return dict(qk=256, bb=144, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 144,
                     extent=lambda a: (a, a + 144), align=16)
+    if fmt in ("q5k", "moe5"):
+        return dict(qk=256, bb=176, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 176,
+                    extent=lambda a: (a, a + 176), align=16)
+    if fmt in ("q4_0", "moe40"):
+        # five 32-bit loads from the word below the 2-byte aligned block
+        return dict(qk=32, bb=18, sb=32, units=lambda nb: nb, ubyte=lambda u: u * 18,
+                    extent=lambda a: (a - (a & 3), a - (a & 3) + 20), align=2)
     if fmt in ("q6k", "moe6"):
         return dict(qk=256, bb=210, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 210,
                     extent=lambda a: (a - (a & 3), a - (a & 3) + 212), align=2)
-    if fmt == "q8_0":
+    if fmt in ("q8_0", "moe8"):
         return dict(qk=32, bb=34, sb=32, units=lambda nb: nb, ubyte=lambda u: u * 34,
                     extent=lambda a: (a - (a & 3), a - (a & 3) + 40), align=2)
     if fmt == "q8d":
@@ -150,7 +158,9 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
 
 
 WORKLOADS = [("q4k", 4096, 4096, 1), ("q4k", 256, 1024, 1), ("q8d", 14336, 4096, 1), ("q6k", 4096, 14336, 1),
-             ("moe", 768, 2048, 8), ("q4d", 4096, 4096, 1), ("moe6", 2048, 768, 8), ("moe4d", 768, 2048, 8)]
+             ("moe", 768, 2048, 8), ("q4d", 4096, 4096, 1), ("moe6", 2048, 768, 8), ("moe4d", 768, 2048, 8),
+             ("q5k", 4096, 4096, 1), ("q4_0", 4096, 4096, 1), ("moe8", 768, 2048, 8), ("moe40", 768, 2048, 8),
+             ("moe5", 768, 2048, 8)]
 
 
 @pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
@@ -171,7 +181,10 @@ SHAPES = [("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 4352), ("q4k", 20, 163
           ("q6k", 3, 256), ("q6k", 41, 14336), ("q6k", 130, 2816), ("q8_0", 300, 96), ("q8_0", 7, 4096),
           ("q8_0", 13, 32), ("q8_0", 64, 11008), ("q8d", 300, 4096), ("q8d", 7, 96), ("q8d", 1, 32),
           ("q8d", 61, 256), ("q8d", 5, 4160), ("moe", 96, 512, ), ("moe", 7, 256), ("q4d", 300, 768), ("q4d", 1, 256),
-          ("q4d", 97, 4352), ("q4d", 20, 16384), ("moe6", 96, 512), ("moe6", 7, 256), ("moe4d", 40, 512)]
+          ("q4d", 97, 4352), ("q4d", 20, 16384), ("moe6", 96, 512), ("moe6", 7, 256), ("moe4d", 40, 512),
+          ("q5k", 300, 768), ("q5k", 1, 256), ("q5k", 97, 4352), ("q5k", 20, 16384), ("q4_0", 300, 96),
+          ("q4_0", 7, 4096), ("q4_0", 13, 32), ("q4_0", 64, 11008), ("q4_0", 33, 1056), ("moe8", 96, 512),
+          ("moe8", 7, 96), ("moe40", 96, 512), ("moe40", 7, 96), ("moe5", 40, 512), ("moe5", 7, 256)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -187,7 +200,7 @@ CFGS = [dict(ctas=1, chunk_rows=1, chunks=2), dict(ctas=3, chunk_rows=5, chunks=
 
 
 @pytest.mark.parametrize("cfg", CFGS)
-@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q8d", "q4d"])
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q8d", "q4d", "q5k", "q4_0"])
 def test_forced_plans(q, fmt, cfg):
     replay(q, fmt, 61, 512 if fmt != "q8d" else 256, 1, cfg)
 
@@ -197,13 +210,16 @@ WIDE_CFGS = [dict(ctas=1, chunk_rows=3, chunks=2), dict(ctas=2, chunk_rows=1, ch
 
 
 @pytest.mark.parametrize("cfg", WIDE_CFGS)
-@pytest.mark.parametrize("fmt,k", [("q4k", 4352), ("q6k", 2816), ("q8_0", 4096), ("q4k", 16384)])
+@pytest.mark.parametrize("fmt,k", [("q4k", 4352), ("q6k", 2816), ("q8_0", 4096), ("q4k", 16384), ("q5k", 4352),
+                                   ("q4_0", 4096), ("q4_0", 1056)])
 def test_forced_wide_plans(q, fmt, k, cfg):
     replay(q, fmt, 29, k, 1, cfg)
 
 
 def test_moe_forced_plan(q):
     replay(q, "moe", 40, 512, 5, dict(ctas=2, chunk_rows=3, chunks=2))
+    for fmt in ("moe8", "moe40", "moe5"):
+        replay(q, fmt, 40, 512, 5, dict(ctas=2, chunk_rows=3, chunks=2))
 
 
 def test_chain_shapes(q):
