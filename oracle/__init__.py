@@ -72,6 +72,7 @@ def _lib():
             L.orc_dequant.argtypes = [ctypes.c_int, P, lg, lg, P]
             L.orc_qmv.argtypes = [ctypes.c_int, P, P, lg, lg, P]
             L.orc_moe_qmv.argtypes = [ctypes.c_int, P, P, P, lg, lg, lg, lg, P]
+            L.orc_qmm.argtypes = [ctypes.c_int, P, P, lg, lg, lg, P]
             L.orc_quantize_act_q8.argtypes = [P, lg, lg, P, P, P]
             L.orc_q8_blockdots.argtypes = [P, P, lg, lg, P]
             L.orc_qmv_q8_dp4a.argtypes = [P, P, P, lg, lg, P]
@@ -132,6 +133,17 @@ def qmv(fmt: str, w, x, rows: int, k: int) -> np.ndarray:
     assert w.size == rows * (k // QK[fmt]) * BLOCK_BYTES[fmt] and x.size == k
     y = np.empty(rows, dtype=np.float64)
     rc = _lib().orc_qmv(FMT[fmt], _p(w), _p(x), rows, k, _p(y))
+    assert rc == 0
+    return y
+
+
+def qmm(fmt: str, w, x, m: int, rows: int, k: int) -> np.ndarray:
+    """Small-M batch: y[m, rows] (f64) for the m rows of x[m, k]."""
+    w = _u8(w)
+    x = _f32(x)
+    assert w.size == rows * (k // QK[fmt]) * BLOCK_BYTES[fmt] and x.size == m * k
+    y = np.empty((m, rows), dtype=np.float64)
+    rc = _lib().orc_qmm(FMT[fmt], _p(w), _p(x), m, rows, k, _p(y))
     assert rc == 0
     return y
 

@@ -302,6 +302,30 @@ int orc_qmv(int fmt, const uint8_t *w, const float *x, long rows, long k, double
     return 0;
 }
 
+/* Small-M batch (hanzo-ml src/vulkan_backend.rs, the `matmul_q*_gpu`
+ * prefill products): y[i, r] = sum_j W[r, j] * x[i, j] for the m rows of
+ * x[m, k] (row-major), output y[m, rows] row-major. Each block is decoded to
+ * its exact value once and used for every row of x; each dot accumulates in
+ * f64 in index order. */
+int orc_qmm(int fmt, const uint8_t *w, const float *x, long m, long rows, long k, double *y) {
+    int qk, bb;
+    double blk[ORC_QK_K];
+    if (fmt_geom(fmt, &qk, &bb) || k % qk || m < 1) return -1;
+    long nb = k / qk;
+    for (long i = 0; i < m * rows; i++) y[i] = 0.0;
+    for (long r = 0; r < rows; r++) {
+        for (long b = 0; b < nb; b++) {
+            decode_block(fmt, w + (r * nb + b) * bb, blk);
+            for (long i = 0; i < m; i++) {
+                double acc = y[i * rows + r];
+                for (int t = 0; t < qk; t++) acc += blk[t] * (double)x[i * k + b * qk + t];
+                y[i * rows + r] = acc;
+            }
+        }
+    }
+    return 0;
+}
+
 /* MoE: y[s, r] = dense matvec of expert ids[s] (rows r of bank slice
  * [ids[s]*rows, (ids[s]+1)*rows)) with x[s, :]. A slot whose id is outside
  * [0, n_experts) gets NaN in every output (the CUDA path's contract). */

@@ -491,6 +491,55 @@ def test_q4k_dp4a_matvec_is_the_matvec_of_the_dequantized_activation():
     assert np.max(np.abs(y - yf)) <= 0.05 * np.max(np.abs(yf))
 
 
+# ------------------------------------------------------------- small-M batch
+
+@pytest.mark.parametrize("fmt,m,rows,k", [("q4k", 3, 4, 512), ("q6k", 2, 3, 256), ("q8_0", 8, 5, 96),
+                                          ("q5k", 5, 2, 256), ("q4_0", 4, 3, 64)])
+def test_batch_brute_force(fmt, m, rows, k):
+    """y[i, r] equals an element loop over the materialized f64 matrix and the
+    m rows of x, for every (i, r)."""
+    st = synth.Stream(300 + m + rows + k)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    W = oracle.dequant(fmt, w, rows, k)
+    ref = np.array([[sum(W[r, j] * float(x[i, j]) for j in range(k)) for r in range(rows)] for i in range(m)])
+    got = oracle.qmm(fmt, w, x, m, rows, k)
+    assert got.shape == (m, rows)
+    assert np.allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_batch_unit_rows_and_order():
+    """Row i of x = e_{j_i} picks column j_i of W into row i of y exactly (the
+    output is [m, rows], x rows in order); a row of zeros gives zeros."""
+    rows, k = 6, 512
+    w = synth.gen_q4k_rows(synth.Stream(51), rows, k)
+    W = oracle.dequant("q4k", w, rows, k)
+    cols = [0, 511, 37, 256]
+    x = np.zeros((5, k), dtype=np.float32)
+    for i, j in enumerate(cols):
+        x[i, j] = 1.0
+    y = oracle.qmm("q4k", w, x, 5, rows, k)
+    for i, j in enumerate(cols):
+        assert np.array_equal(y[i], W[:, j])
+    assert np.all(y[4] == 0.0)
+
+
+def test_batch_rows_are_independent():
+    """Changing one row of x changes only that row of y, and each row equals
+    the pinned matvec of that row alone."""
+    m, rows, k = 4, 5, 768
+    st = synth.Stream(52)
+    w = synth.gen_q6k_rows(st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    y = oracle.qmm("q6k", w, x, m, rows, k)
+    x2 = x.copy()
+    x2[2] = synth.gen_normal(st, k)
+    y2 = oracle.qmm("q6k", w, x2, m, rows, k)
+    assert np.array_equal(np.delete(y, 2, axis=0), np.delete(y2, 2, axis=0))
+    for i in range(m):
+        assert np.array_equal(y2[i], oracle.qmv("q6k", w, x2[i], rows, k))
+
+
 # ------------------------------------------------------------------------ MoE
 
 def test_moe_matches_dense_per_expert_and_flags_bad_ids():
