@@ -79,7 +79,7 @@ def measured_peak():
 # Block format of each workload kind's weights.
 KIND_FMT = {"q4k": "q4k", "q4k_dp4a": "q4k", "q6k": "q6k", "q8_0_dp4a": "q8_0", "q5k": "q5k", "q4_0": "q4_0",
             "moe_q4k": "q4k", "moe_q4k_dp4a": "q4k", "moe_q6k": "q6k", "moe_q8_0": "q8_0", "moe_q4_0": "q4_0",
-            "moe_q5k": "q5k"}
+            "moe_q5k": "q5k", "qmm_q4k": "q4k", "qmm_q6k": "q6k", "qmm_q8_0": "q8_0"}
 # MoE kinds with an f32 activation (one entry point each, same arguments).
 MOE_F32 = ("moe_q4k", "moe_q6k", "moe_q8_0", "moe_q4_0", "moe_q5k")
 
@@ -99,6 +99,8 @@ def algorithmic_bytes(name: str) -> int:
     wb = weight_bytes(name)
     if c["kind"] in MOE_F32:
         return wb + 4 * c["slots"] * c["k"] + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
+    if c["kind"].startswith("qmm_"):
+        return wb + 4 * c["m"] * c["k"] + 4 * c["m"] * c["rows"]   # W read once for all m rows
     if c["kind"] == "moe_q4k_dp4a":
         return wb + c["slots"] * (c["k"] + 4 * (c["k"] // 32)) + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
     if c["kind"] in ("q8_0_dp4a", "q4k_dp4a"):
@@ -198,6 +200,8 @@ class Workload:
             self.ids = [torch.from_numpy(c["ids"]).to(dev)]
             for _ in range(15):
                 self.ids.append(torch.from_numpy(synth.gen_moe_ids(st, c["slots"], c["n_experts"])).to(dev))
+        elif self.kind.startswith("qmm_"):
+            self.y = torch.empty(c["m"], self.rows, dtype=torch.float32, device=dev)
         else:
             self.y = torch.empty(self.rows, dtype=torch.float32, device=dev)
         if self.kind in ("q8_0_dp4a", "q4k_dp4a", "moe_q4k_dp4a"):
@@ -216,6 +220,10 @@ class Workload:
             q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
         elif self.kind in ("q6k", "q5k", "q4_0"):
             getattr(q, f"qmv_{self.kind}")(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
+        elif self.kind.startswith("qmm_"):
+            m = self.c["m"]
+            getattr(q, self.kind)(w, self.x, self.y, self.rows, self.k, m, stream=stream, cfg=cfg)
+            return q.qmm_launches(self.kind[4:], self.k, m)
         elif self.kind in ("q8_0_dp4a", "q4k_dp4a"):
             n = 1
             if with_quant:
@@ -449,11 +457,17 @@ def run_ours(args):
 def config_row(name, ms, peak, peak_kind, copies):
     wb = weight_bytes(name)
     gbs = wb / (ms * 1e-3) / 1e9
-    return {"us_per_call": round(ms * 1e3, 3), "packed_weight_bytes": wb,
-            "packed_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
-            "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
-            "algorithmic_gbs": round(algorithmic_bytes(name) / (ms * 1e-3) / 1e9, 1),
-            "rotation_copies": copies}
+    row = {"us_per_call": round(ms * 1e3, 3), "packed_weight_bytes": wb,
+           "packed_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+           "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+           "algorithmic_gbs": round(algorithmic_bytes(name) / (ms * 1e-3) / 1e9, 1),
+           "rotation_copies": copies}
+    m = synth.CONFIGS[name].get("m")
+    if m:
+        # a batch of m rows of x: time per row of x, against one matvec each
+        row["m"] = m
+        row["us_per_x_row"] = round(ms * 1e3 / m, 3)
+    return row
 
 
 def end_to_end(torch, q, wl, device, K):

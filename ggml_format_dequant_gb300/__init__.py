@@ -27,7 +27,7 @@ QMV_STATUS_BAD_EXPERT_ID = 1
 QMV_STATUS_WAIT_TIMEOUT = 2
 
 (FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A,
- FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K) = range(13)
+ FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K, FMT_QMM_Q4K, FMT_QMM_Q6K, FMT_QMM_Q8_0) = range(16)
 
 
 class QmvLibraryMissing(RuntimeError):
@@ -74,6 +74,12 @@ _SIG = {
     "qmv_dequant_q8_0": [_P, _P, _I, _I, _P],
     "qmv_dequant_q5k": [_P, _P, _I, _I, _P],
     "qmv_dequant_q4_0": [_P, _P, _I, _I, _P],
+    "qmm_q4k": [_P, _P, _P, _I, _I, _I, _P],
+    "qmm_q4k_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q6k": [_P, _P, _P, _I, _I, _I, _P],
+    "qmm_q6k_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q8_0": [_P, _P, _P, _I, _I, _I, _P],
+    "qmm_q8_0_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmv_q5k": [_P, _P, _P, _I, _I, _P],
     "qmv_q5k_cfg": [_P, _P, _P, _I, _I, _P, _P],
     "qmv_q4_0": [_P, _P, _P, _I, _I, _P],
@@ -172,6 +178,36 @@ def qmv_q8_0(w, x, y, rows, k, stream=None, cfg=None, check=True):
     if cfg is None:
         return _call("qmv_q8_0", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
     return _call("qmv_q8_0_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+
+
+def _qmm(name, w, x, y, rows, k, m, stream, cfg, check):
+    if cfg is None:
+        return _call(name, _ptr(w), _ptr(x), _ptr(y), rows, k, m, _stream(stream), check=check)
+    return _call(name + "_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _cfg(cfg), _stream(stream), check=check)
+
+
+def qmm_q4k(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
+    return _qmm("qmm_q4k", w, x, y, rows, k, m, stream, cfg, check)
+
+
+def qmm_q6k(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
+    return _qmm("qmm_q6k", w, x, y, rows, k, m, stream, cfg, check)
+
+
+def qmm_q8_0(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
+    return _qmm("qmm_q8_0", w, x, y, rows, k, m, stream, cfg, check)
+
+
+def qmm_launches(fmt, k, m) -> int:
+    """Kernel launches one qmm_<fmt> call makes: ceil(m / tile) with the
+    widest tile (8, 4, 2 or 1 rows of x) whose units per row fit a CTA."""
+    qk, uw_units = (32, {8: 4, 4: 2, 2: 1}) if fmt == "q8_0" else (256, {8: 32, 4: 16, 2: 8})
+    tile = 1
+    for t in (8, 4, 2):
+        if (k // qk) * uw_units[t] <= 512:
+            tile = t
+            break
+    return 1 if m == 1 else -(-m // tile)
 
 
 def qmv_q5k(w, x, y, rows, k, stream=None, cfg=None, check=True):

@@ -4,6 +4,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "qmm_formats.cuh"
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
 
@@ -86,6 +87,46 @@ int qmv_q4_0_cfg(const void* w, const float* x, float* y, int rows, int k, const
 
 int qmv_q4_0(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
     return qmv_q4_0_cfg(w, x, y, rows, k, nullptr, stream);
+}
+
+// Small-M batch: m == 1 is the matvec itself; m >= 2 the batched kernels.
+int qmm_q4k_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+                cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 144);
+    if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
+        rc = QMV_EINVAL;
+    if (rc) return rc;
+    return m == 1 ? qmvi::q4k(w, x, y, rows, k, cfg, stream) : qmvi::qmm_q4k(w, x, y, rows, k, m, cfg, stream);
+}
+
+int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
+    return qmm_q4k_cfg(w, x, y, rows, k, m, nullptr, stream);
+}
+
+int qmm_q6k_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+                cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 210);
+    if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
+        rc = QMV_EINVAL;
+    if (rc) return rc;
+    return m == 1 ? qmvi::q6k(w, x, y, rows, k, cfg, stream) : qmvi::qmm_q6k(w, x, y, rows, k, m, cfg, stream);
+}
+
+int qmm_q6k(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
+    return qmm_q6k_cfg(w, x, y, rows, k, m, nullptr, stream);
+}
+
+int qmm_q8_0_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+                 cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 32, 34);
+    if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
+        rc = QMV_EINVAL;
+    if (rc) return rc;
+    return m == 1 ? qmvi::q8_0(w, x, y, rows, k, cfg, stream) : qmvi::qmm_q8_0(w, x, y, rows, k, m, cfg, stream);
+}
+
+int qmm_q8_0(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
+    return qmm_q8_0_cfg(w, x, y, rows, k, m, nullptr, stream);
 }
 
 int quantize_act_q8(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t stream) {
@@ -261,29 +302,46 @@ const char* qmv_last_cuda_error(void) {
 
 int qmv_device_status(unsigned int* status, int clear) {
     if (!status) return QMV_EINVAL;
-    unsigned int a = 0, b = 0, c = 0, d = 0, e = 0;
-    int rc = qmvi::status_q4k(&a, clear);
-    if (!rc) rc = qmvi::status_q6k(&b, clear);
-    if (!rc) rc = qmvi::status_q8(&c, clear);
-    if (!rc) rc = qmvi::status_q5k(&d, clear);
-    if (!rc) rc = qmvi::status_q4_0(&e, clear);
-    if (rc) return rc;
-    *status = a | b | c | d | e;
+    int (*const readers[])(unsigned int*, int) = {qmvi::status_q4k,     qmvi::status_q6k,     qmvi::status_q8,
+                                                  qmvi::status_q5k,     qmvi::status_q4_0,    qmvi::status_qmm_q4k,
+                                                  qmvi::status_qmm_q6k, qmvi::status_qmm_q8_0};
+    unsigned int all = 0;
+    for (auto rd : readers) {
+        unsigned int v = 0;
+        const int rc = rd(&v, clear);
+        if (rc) return rc;
+        all |= v;
+    }
+    *status = all;
     return QMV_OK;
 }
 
 namespace {
 
 // Plan ids that describe an MoE launch (grid.y = slots).
-bool plan_is_moe(int fmt) { return fmt == 4 || fmt == 6 || fmt == 7 || fmt >= 10; }
+bool plan_is_moe(int fmt) { return fmt == 4 || fmt == 6 || fmt == 7 || (fmt >= 10 && fmt <= 12); }
 
 // Plan of format fmt on device `di`.
 int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_cfg* cfg, qmv::KParams* kp,
             qmv::Plan* pl) {
-    static const int qk[13] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256};
-    if (fmt < 0 || fmt > 12 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
+    static const int qk[16] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256, 256, 256, 32};
+    if (fmt < 0 || fmt > 15 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
     const bool moe = plan_is_moe(fmt);
     if (moe && slots <= 0) return QMV_EINVAL;
+    if (fmt >= 13) {
+        // batched: `slots` is the tile's row count of x, 2..8
+        switch (slots) {
+#define QMM_PLAN(MM)                                                                                    \
+    case MM:                                                                                            \
+        return fmt == 13 ? qmv::make_plan_for<qmv::Q4KB<MM>>(di, rows, k, 1, cfg, kp, pl)              \
+             : fmt == 14 ? qmv::make_plan_for<qmv::Q6KB<MM>>(di, rows, k, 1, cfg, kp, pl)              \
+                         : qmv::make_plan_for<qmv::Q8B<MM>>(di, rows, k, 1, cfg, kp, pl);
+            QMM_PLAN(2) QMM_PLAN(3) QMM_PLAN(4) QMM_PLAN(5) QMM_PLAN(6) QMM_PLAN(7) QMM_PLAN(8)
+#undef QMM_PLAN
+        default:
+            return QMV_EINVAL;
+        }
+    }
     if (!moe) slots = 1;
     switch (fmt) {
     case 0: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, 1, cfg, kp, pl);

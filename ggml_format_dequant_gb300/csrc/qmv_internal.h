@@ -53,4 +53,12 @@ int quantize_act(const float* x, int8_t* xq, float* xs, float* xsum, int m, int 
 int dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t s);
 int status_q8(unsigned int* out, int clear);
 
+// qmm_q4k.cu, qmm_q6k.cu, qmm_q8_0.cu: the small-M batched product (m >= 2)
+int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s);
+int qmm_q6k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s);
+int qmm_q8_0(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s);
+int status_qmm_q4k(unsigned int* out, int clear);
+int status_qmm_q6k(unsigned int* out, int clear);
+int status_qmm_q8_0(unsigned int* out, int clear);
+
 }  // namespace qmvi

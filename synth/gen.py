@@ -217,6 +217,14 @@ CONFIGS = {
     "moe_q8_0_e128_n768_k2048_s8": dict(kind="moe_q8_0", rows=768, k=2048, seed=8, n_experts=128, slots=8),
     "moe_q4_0_e128_n768_k2048_s8": dict(kind="moe_q4_0", rows=768, k=2048, seed=9, n_experts=128, slots=8),
     "moe_q5k_e128_n768_k2048_s8": dict(kind="moe_q5k", rows=768, k=2048, seed=10, n_experts=128, slots=8),
+    # Small-M batches (m rows of x sharing one weight read) on the headline and
+    # the two large suite matrices (same seeds: the same weight bytes; the
+    # first row of x is the single-row workload's x).
+    "qmm_q4k_4096x4096_m2": dict(kind="qmm_q4k", rows=4096, k=4096, seed=1, m=2),
+    "qmm_q4k_4096x4096_m4": dict(kind="qmm_q4k", rows=4096, k=4096, seed=1, m=4),
+    "qmm_q4k_4096x4096_m8": dict(kind="qmm_q4k", rows=4096, k=4096, seed=1, m=8),
+    "qmm_q6k_4096x14336_m4": dict(kind="qmm_q6k", rows=4096, k=14336, seed=4, m=4),
+    "qmm_q8_0_14336x4096_m8": dict(kind="qmm_q8_0", rows=14336, k=4096, seed=2, m=8),
 }
 
 
@@ -238,6 +246,9 @@ def make_config(name: str) -> dict:
     elif kind in ("q5k", "q4_0"):
         c["w"] = GEN_ROWS[kind](st, rows, k)
         c["x"] = gen_normal(st, k)
+    elif kind.startswith("qmm_"):
+        c["w"] = GEN_ROWS[kind[4:]](st, rows, k)
+        c["x"] = gen_normal(st, c["m"] * k).reshape(c["m"], k)
     elif kind in ("moe_q4k", "moe_q4k_dp4a", "moe_q6k", "moe_q8_0", "moe_q4_0", "moe_q5k"):
         e, s = c["n_experts"], c["slots"]
         fmt = "q4k" if kind == "moe_q4k_dp4a" else kind[4:]
