@@ -379,6 +379,8 @@ def run_ours(args):
     del wl, gk, gw
     torch.cuda.empty_cache()
     names = [HEADLINE] if args.headline_only else list(synth.CONFIGS)
+    if args.only:
+        names = [n for n in synth.CONFIGS if n == HEADLINE or any(n.startswith(o) for o in args.only.split(","))]
     for name in names:
         w2 = Workload(q, torch, name, l2, device)
         n = max(64, w2.copies)
@@ -607,6 +609,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="skip the per-config table")
+    ap.add_argument("--only", default="", help="per-config table for the workloads whose names start with one of "
+                                               "these comma-separated prefixes")
     ap.add_argument("--chain", action="store_true",
                     help="time the headline as a dependent decode chain (mode 1)")
     ap.add_argument("--isolated", action="store_true",

@@ -95,6 +95,7 @@ _SIG = {
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "qmv_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
     "qmv_set_weight_prefetch": [_I],
+    "qmm_tc_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
 }
 
 _LIB = None
@@ -348,3 +349,16 @@ def qmv_plan_detail(fmt, rows, k, slots=1, cfg=None, device=GB300_DEVICE) -> dic
     _call("qmv_plan_detail", fmt, rows, k, slots, _cfg(cfg), ctypes.cast(dev, ctypes.c_void_p),
           ctypes.cast(out, ctypes.c_void_p))
     return dict(zip(PLAN_DETAIL_FIELDS, list(out)))
+
+
+QMM_TC_PLAN_FIELDS = ("threads", "ctas", "smem", "KS", "CR", "S", "rowbytes", "stride", "slot_stride", "rq", "rrem",
+                      "ngroups", "off_st", "off_red", "off_ring", "off_bars", "off_cnt")
+
+
+def qmm_tc_plan_detail(fmt, rows, k, m, cfg=None, device=GB300_DEVICE) -> dict:
+    """The tensor-core batch planner's choice (fmt 0 = Q4_K, 1 = Q6_K, 2 = Q8_0)
+    for a described device, computed on the host without a GPU."""
+    out = (ctypes.c_int * len(QMM_TC_PLAN_FIELDS))()
+    dev = (ctypes.c_int * 4)(*device)
+    _call("qmm_tc_plan_detail", fmt, rows, k, m, _cfg(cfg), dev, out)
+    return dict(zip(QMM_TC_PLAN_FIELDS, list(out)))

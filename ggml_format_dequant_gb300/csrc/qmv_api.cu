@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include "qmm_formats.cuh"
+#include "qmm_tc.cuh"
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
 
@@ -399,6 +400,45 @@ int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, con
         static_cast<int>(kp.off_red), static_cast<int>(kp.off_ring), static_cast<int>(kp.off_bars),
         static_cast<int>(kp.off_cnt), pl.CL};
     for (int i = 0; i < QMV_PLAN_DETAIL_FIELDS; i++) out[i] = v[i];
+    return QMV_OK;
+}
+
+int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_cfg* cfg, const int* device, int* out) {
+    if (!device || !out) return QMV_EINVAL;
+    qmv::DevInfo di;
+    di.nsm = device[0];
+    di.smem_optin = device[1];
+    di.smem_sm = device[2];
+    di.smem_reserved = device[3];
+    if (di.nsm <= 0 || di.smem_optin <= 0 || di.smem_sm <= 0 || di.smem_reserved < 0) return QMV_EINVAL;
+    qmv::TParams tp{};
+    qmv::Plan pl;
+    int rc;
+    switch (fmt) {
+    case 0: rc = qmv::make_tc_plan_for<qmv::Q4KT>(di, rows, k, m, cfg, &tp, &pl); break;
+    case 1: rc = qmv::make_tc_plan_for<qmv::Q6KT>(di, rows, k, m, cfg, &tp, &pl); break;
+    case 2: rc = qmv::make_tc_plan_for<qmv::Q8T>(di, rows, k, m, cfg, &tp, &pl); break;
+    default: rc = QMV_EINVAL;
+    }
+    if (rc) return rc;
+    const int v[QMM_TC_PLAN_FIELDS] = {pl.T,
+                                      pl.parts,
+                                      static_cast<int>(pl.smem),
+                                      tp.KS,
+                                      tp.CR,
+                                      tp.S,
+                                      static_cast<int>(tp.rowbytes),
+                                      static_cast<int>(tp.stride),
+                                      static_cast<int>(tp.slot_stride),
+                                      tp.rq,
+                                      tp.rrem,
+                                      tp.ngroups,
+                                      static_cast<int>(tp.off_st),
+                                      static_cast<int>(tp.off_red),
+                                      static_cast<int>(tp.off_ring),
+                                      static_cast<int>(tp.off_bars),
+                                      static_cast<int>(tp.off_cnt)};
+    for (int i = 0; i < QMM_TC_PLAN_FIELDS; i++) out[i] = v[i];
     return QMV_OK;
 }
 
