@@ -200,15 +200,16 @@ def qmm_q8_0(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
 
 
 def qmm_launches(fmt, k, m) -> int:
-    """Kernel launches one qmm_<fmt> call makes: ceil(m / tile) with the
-    widest tile (8, 4, 2 or 1 rows of x) whose units per row fit a CTA."""
-    qk, uw_units = (32, {8: 4, 4: 2, 2: 1}) if fmt == "q8_0" else (256, {8: 32, 4: 16, 2: 8})
-    tile = 1
-    for t in (8, 4, 2):
-        if (k // qk) * uw_units[t] <= 512:
-            tile = t
-            break
-    return 1 if m == 1 else -(-m // tile)
+    """Kernel launches one qmm_<fmt> call makes: the matvec for m = 1; for
+    m = 2 the register kernel, ceil(m / tile) launches with the widest tile
+    (2 or 1 rows of x) whose units per row fit a CTA; from m = 3 on the
+    tensor-core kernel, ceil(m / 8) tiles times ceil(k / 4096) k-chunks."""
+    if m == 1:
+        return 1
+    if m >= 3:
+        return -(-m // 8) * -(-k // 4096)
+    qk, units = (32, 1) if fmt == "q8_0" else (256, 8)
+    return 1 if (k // qk) * units <= 512 else 2
 
 
 def qmv_q5k(w, x, y, rows, k, stream=None, cfg=None, check=True):

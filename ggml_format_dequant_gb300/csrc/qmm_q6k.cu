@@ -1,7 +1,7 @@
 // qmm_q6k.cu -- small-M batched product y[m, rows] = x[m, k] W^T over packed
 // Q6_K rows (m >= 2; tiles of up to 8 rows of x per launch, fewer when k
-// is large; tiles of one row run the matvec). From three rows of x on, rows
-// of up to 4096 weights go to the tensor-core kernel of qmm_tc.cuh.
+// is large; tiles of one row run the matvec). From three rows of x on, the
+// tensor-core kernel of qmm_tc.cuh takes over.
 #include "qmv_internal.h"
 #include "qmm_kernel.cuh"
 #include "qmm_tc.cuh"
@@ -11,10 +11,10 @@ namespace qmvi {
 using namespace qmv;
 
 int qmm_q6k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s) {
-    // Three or more rows of x and rows of up to 4096 weights: the tensor-core
-    // kernel (its cost hardly depends on m, measured faster from m = 3 on);
-    // otherwise the register-activation kernel, in narrower tiles for long rows.
-    if (m >= 3 && k / 32 <= TC_GROUPS_PER_SLICE * MAX_WARPS) return qmm_tc_run<Q6KT>(w, x, y, rows, k, m, cfg, s);
+    // Three or more rows of x: the tensor-core kernel (its cost hardly
+    // depends on m; measured faster from m = 3 on); two: the register-activation
+    // kernel.
+    if (m >= 3) return qmm_tc_run<Q6KT>(w, x, y, rows, k, m, cfg, s);
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(w);
     kp.rows = rows;

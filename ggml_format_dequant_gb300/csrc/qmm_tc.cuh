@@ -1,6 +1,6 @@
 // qmm_tc.cuh -- the small-M batched product y[m, rows] = x[m, k] W^T on the
-// tensor cores (warp-level mma.sync m16n8k16, f16 operands, f32 accumulate),
-// for rows of up to 4096 weights.
+// tensor cores (warp-level mma.sync m16n8k16, f16 operands, f32 accumulate);
+// one launch covers rows of up to 4096 weights, longer rows go in k-chunks.
 //
 // The product is a skinny dense contraction (m <= 8 columns), so a warp-level
 // MMA with register accumulators fits it: the weights' per-32 (Q4_K, Q8_0) or
@@ -37,13 +37,17 @@
 namespace qmv {
 
 struct TParams {
-    const uint8_t* w;             // packed rows [rows, k / QK blocks]
-    const float* x;               // [m, k]
+    const uint8_t* w;             // packed rows [rows, K / QK blocks], K the full row length
+    const float* x;               // x[i, 0] of this launch's k-chunk (row stride xstride)
     float* y;                     // [m, rows]
     unsigned long long wbytes;    // readable bytes from w (tail clipping)
-    int rows, k, m;               // m: rows of x, 1..8
+    int rows, k, m;               // k: the chunk's weights per row; m: rows of x, 1..8
+    int xstride;                  // floats between rows of x (the full row length)
+    uint32_t wpitch;              // bytes between rows of W
+    uint32_t woff;                // byte offset of the chunk inside a row
+    int accumulate;               // add to y (a later k-chunk) instead of writing it
     int ngroups;                  // k / 32
-    uint32_t rowbytes;
+    uint32_t rowbytes;            // bytes of one row's chunk
     uint32_t stride;              // shared-memory row stride (16 mod 128)
     int KS;                       // warps, one per slice of 8 groups
     int CR;                       // rows per piece
@@ -301,7 +305,7 @@ __device__ __forceinline__ void tc_issue_warp(const TParams& p, uint8_t* dst_ptr
     const uintptr_t lim = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(p.wbytes);
     uint32_t total = 0;
     for (int i = lane; i < nr; i += 32) {
-        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.rowbytes;
+        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.wpitch + p.woff;
         const uintptr_t ge = gs + p.rowbytes;
         const uintptr_t a0 = gs & ~uintptr_t(15);
         uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
@@ -317,7 +321,7 @@ __device__ __forceinline__ void tc_issue_warp(const TParams& p, uint8_t* dst_ptr
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
     for (int i = lane; i < nr; i += 32) {
-        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.rowbytes;
+        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.wpitch + p.woff;
         const uintptr_t ge = gs + p.rowbytes;
         const uintptr_t a0 = gs & ~uintptr_t(15);
         uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
         float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         const bool live = j < ng && g < p.m;
         if (live) {
-            const float* src = p.x + static_cast<long long>(g) * p.k + 32 * (G0 + j) + 4 * t;
+            const float* src = p.x + static_cast<long long>(g) * p.xstride + 32 * (G0 + j) + 4 * t;
             const float4 u0 = __ldg(reinterpret_cast<const float4*>(src));
             const float4 u1 = __ldg(reinterpret_cast<const float4*>(src + 16));
             v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
@@ -445,8 +449,10 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
         for (int r = 0; r < nr; r += TC_TILE_ROWS) {
             const int ia = r + g, ib = r + g + 8;
             // rows past the piece read the slot's spare rows (results dropped)
-            const uint32_t pa = static_cast<uint32_t>((wbase + static_cast<uintptr_t>(R0 + rl0 + ia) * p.rowbytes) & 15u);
-            const uint32_t pb = static_cast<uint32_t>((wbase + static_cast<uintptr_t>(R0 + rl0 + ib) * p.rowbytes) & 15u);
+            const uint32_t pa =
+                static_cast<uint32_t>((wbase + static_cast<uintptr_t>(R0 + rl0 + ia) * p.wpitch + p.woff) & 15u);
+            const uint32_t pb =
+                static_cast<uint32_t>((wbase + static_cast<uintptr_t>(R0 + rl0 + ib) * p.wpitch + p.woff) & 15u);
             const uint32_t ra = slot + static_cast<uint32_t>(ia) * p.stride + pa;
             const uint32_t rb = slot + static_cast<uint32_t>(ib) * p.stride + pb;
             float y4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -497,7 +503,8 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
         const int r = e / p.m, i = e - (e / p.m) * p.m;
         float v = 0.0f;
         for (int q = 0; q < p.KS; q++) v += red[(r * p.KS + q) * TC_COLS + i];
-        p.y[static_cast<long long>(i) * p.rows + R0 + r] = v;
+        float* dst = p.y + static_cast<long long>(i) * p.rows + R0 + r;
+        *dst = p.accumulate ? *dst + v : v;
     }
 }
 
@@ -558,6 +565,10 @@ inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv
             tp->rows = rows;
             tp->k = k;
             tp->m = m;
+            tp->xstride = k;
+            tp->wpitch = static_cast<uint32_t>(rowbytes);
+            tp->woff = 0;
+            tp->accumulate = 0;
             tp->ngroups = ngroups;
             tp->rowbytes = static_cast<uint32_t>(rowbytes);
             tp->stride = stride;
@@ -606,27 +617,40 @@ inline int launch_tc(const TParams& tp, const Plan& pl, cudaStream_t stream) {
     return cuda_rc(cudaLaunchKernelEx(&lc, kern, tp));
 }
 
+// Weights per row one launch takes: 16 warps x 256.
+constexpr int TC_MAX_K = TC_GROUPS_PER_SLICE * 32 * MAX_WARPS;
+
 // y[m, rows] = x[m, k] W^T on the tensor cores, m >= 1: ceil(m / 8) balanced
-// tiles of rows of x, one launch each.
+// tiles of rows of x; rows longer than TC_MAX_K weights in k-chunks of
+// TC_MAX_K, one launch each, the later chunks adding to y in chunk order
+// (each launch reads its chunk of W once).
 template <class F>
 inline int qmm_tc_run(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
                       cudaStream_t s) {
     const int tiles = (m + TC_COLS - 1) / TC_COLS;
+    const long long pitch = static_cast<long long>(k / F::QK) * F::BLOCK_BYTES;
+    DevInfo di;
+    int rc = dev_info(&di, nullptr);
+    if (rc) return rc;
     for (int t0 = 0, m0 = 0; t0 < tiles; t0++) {
         const int mt = m / tiles + (t0 < m % tiles ? 1 : 0);
-        DevInfo di;
-        int rc = dev_info(&di, nullptr);
-        if (rc) return rc;
-        TParams tp{};
-        Plan pl;
-        rc = make_tc_plan_for<F>(di, rows, k, mt, cfg, &tp, &pl);
-        if (rc) return rc;
-        tp.w = static_cast<const uint8_t*>(w);
-        tp.x = x + static_cast<long long>(m0) * k;
-        tp.y = y + static_cast<long long>(m0) * rows;
-        tp.wbytes = static_cast<unsigned long long>(rows) * tp.rowbytes;
-        rc = launch_tc<F>(tp, pl, s);
-        if (rc) return rc;
+        for (int k0 = 0; k0 < k; k0 += TC_MAX_K) {
+            const int kc = std::min(TC_MAX_K, k - k0);
+            TParams tp{};
+            Plan pl;
+            rc = make_tc_plan_for<F>(di, rows, kc, mt, cfg, &tp, &pl);
+            if (rc) return rc;
+            tp.w = static_cast<const uint8_t*>(w);
+            tp.x = x + static_cast<long long>(m0) * k + k0;
+            tp.y = y + static_cast<long long>(m0) * rows;
+            tp.xstride = k;
+            tp.wpitch = static_cast<uint32_t>(pitch);
+            tp.woff = static_cast<uint32_t>(static_cast<long long>(k0 / F::QK) * F::BLOCK_BYTES);
+            tp.accumulate = k0 > 0 ? 1 : 0;
+            tp.wbytes = static_cast<unsigned long long>(rows) * static_cast<unsigned long long>(pitch);
+            rc = launch_tc<F>(tp, pl, s);
+            if (rc) return rc;
+        }
         m0 += mt;
     }
     return QMV_OK;
