@@ -79,6 +79,9 @@ def _lib():
             L.orc_q4k_dp4a_blockdots.argtypes = [P, P, lg, lg, P]
             L.orc_qmv_q4k_dp4a.argtypes = [P, P, P, lg, lg, P]
             L.orc_moe_qmv_q4k_dp4a.argtypes = [P, P, P, P, lg, lg, lg, lg, P]
+            L.orc_q6k_dp4a_groupdots.argtypes = [P, P, lg, lg, P]
+            L.orc_qmv_q6k_dp4a.argtypes = [P, P, P, lg, lg, P]
+            L.orc_moe_qmv_q6k_dp4a.argtypes = [P, P, P, P, lg, lg, lg, lg, P]
             _LIB = L
     return _LIB
 
@@ -227,6 +230,41 @@ def moe_qmv_q4k_dp4a(bank, xq, xs, ids, rows: int, k: int, n_experts: int) -> np
     assert xq.size == slots * k and xs.size == slots * (k // 32)
     y = np.empty((slots, rows), dtype=np.float64)
     rc = _lib().orc_moe_qmv_q4k_dp4a(_p(bank), _p(xq), _p(xs), _p(ids), slots, rows, k, n_experts, _p(y))
+    assert rc == 0
+    return y
+
+
+def q6k_dp4a_groupdots(w, xq, rows: int, k: int) -> np.ndarray:
+    """int32 [rows, k/16]: (q - 32) . xq over every 16-weight scale group."""
+    w = _u8(w)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    assert xq.size == k
+    out = np.empty((rows, k // 16), dtype=np.int32)
+    assert _lib().orc_q6k_dp4a_groupdots(_p(w), _p(xq), rows, k, _p(out)) == 0
+    return out
+
+
+def qmv_q6k_dp4a(w, xq, xs, rows: int, k: int) -> np.ndarray:
+    """Q6_K x int8 activation matvec (f64)."""
+    w = _u8(w)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xs = _f32(xs)
+    assert xq.size == k and xs.size == k // 32
+    y = np.empty(rows, dtype=np.float64)
+    assert _lib().orc_qmv_q6k_dp4a(_p(w), _p(xq), _p(xs), rows, k, _p(y)) == 0
+    return y
+
+
+def moe_qmv_q6k_dp4a(bank, xq, xs, ids, rows: int, k: int, n_experts: int) -> np.ndarray:
+    """MoE on the Q6_K dp4a path, y[slots, rows] (NaN rows for bad ids)."""
+    bank = _u8(bank)
+    xq = np.ascontiguousarray(xq, dtype=np.int8)
+    xs = _f32(xs)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    slots = ids.size
+    assert xq.size == slots * k and xs.size == slots * (k // 32)
+    y = np.empty((slots, rows), dtype=np.float64)
+    rc = _lib().orc_moe_qmv_q6k_dp4a(_p(bank), _p(xq), _p(xs), _p(ids), slots, rows, k, n_experts, _p(y))
     assert rc == 0
     return y
 

@@ -302,6 +302,80 @@ int orc_qmv(int fmt, const uint8_t *w, const float *x, long rows, long k, double
     return 0;
 }
 
+/* ----------------------------------------------- Q6_K x int8 activation */
+
+/* Code minus 32 of element i of a Q6_K block (the layout of
+ * orc_q6k_block_decode: half H = i/128, quarter qd = (i%128)/32, l = i%32). */
+static int q6k_code(const uint8_t *b, int i) {
+    int H = i / 128, qd = (i % 128) / 32, l = i % 32;
+    int qlb = b[64 * H + 32 * (qd % 2) + l];
+    int lo4 = (qd < 2) ? (qlb & 15) : (qlb >> 4);
+    int hi2 = (b[128 + 32 * H + l] >> (2 * qd)) & 3;
+    return lo4 + 16 * hi2 - 32;
+}
+
+/* dots[r, g] = sum over the 16 weights of scale group g of row r (elements
+ * 16g .. 16g+15; the group of element i of a block is i/16, the index of its
+ * scale) of (q - 32) * xq: the integer dots of the Q6_K dp4a decode
+ * (hanzo-ml src/vulkan_backend.rs, `moe_matvec_q6k_dp4a_blk_dn`, which folds
+ * the -32 against sums of the activation codes). */
+int orc_q6k_dp4a_groupdots(const uint8_t *w, const int8_t *xq, long rows, long k, int32_t *dots) {
+    if (k % ORC_QK_K) return -1;
+    long nb = k / ORC_QK_K;
+    for (long r = 0; r < rows; r++)
+        for (long bi = 0; bi < nb; bi++) {
+            const uint8_t *b = w + (r * nb + bi) * ORC_Q6K_BYTES;
+            for (int g = 0; g < 16; g++) {
+                long dot = 0;
+                for (int t = 0; t < 16; t++)
+                    dot += (long)q6k_code(b, 16 * g + t) * (long)xq[bi * 256 + 16 * g + t];
+                dots[r * (k / 16) + bi * 16 + g] = (int32_t)dot;
+            }
+        }
+    return 0;
+}
+
+/* y[r] = sum over 16-groups g of d * scale_g * xs[g/2] * dot_g in f64: the
+ * Q6_K weights against the dequantized activation xs * xq. */
+int orc_qmv_q6k_dp4a(const uint8_t *w, const int8_t *xq, const float *xs, long rows, long k, double *y) {
+    if (k % ORC_QK_K) return -1;
+    long nb = k / ORC_QK_K;
+    for (long r = 0; r < rows; r++) {
+        double acc = 0.0;
+        for (long bi = 0; bi < nb; bi++) {
+            const uint8_t *b = w + (r * nb + bi) * ORC_Q6K_BYTES;
+            double d = orc_f16_to_f64(rd_le16(b + 208));
+            for (int g = 0; g < 16; g++) {
+                long dot = 0;
+                for (int t = 0; t < 16; t++)
+                    dot += (long)q6k_code(b, 16 * g + t) * (long)xq[bi * 256 + 16 * g + t];
+                double scale = (double)(int8_t)b[192 + g];
+                acc += d * scale * (double)xs[(bi * 256 + 16 * g) / 32] * (double)dot;
+            }
+        }
+        y[r] = acc;
+    }
+    return 0;
+}
+
+/* MoE on the Q6_K dp4a path: slot s multiplies expert ids[s] of the
+ * [E, rows, k] bank with its own codes xq[s, :] and scales xs[s, :]; NaN for
+ * ids outside [0, n_experts). */
+int orc_moe_qmv_q6k_dp4a(const uint8_t *bank, const int8_t *xq, const float *xs, const int32_t *ids,
+                         long slots, long rows, long k, long n_experts, double *y) {
+    if (k % ORC_QK_K) return -1;
+    long rb = (k / ORC_QK_K) * ORC_Q6K_BYTES;
+    for (long s = 0; s < slots; s++) {
+        long e = ids[s];
+        if (e < 0 || e >= n_experts) {
+            for (long r = 0; r < rows; r++) y[s * rows + r] = NAN;
+            continue;
+        }
+        orc_qmv_q6k_dp4a(bank + e * rows * rb, xq + s * k, xs + s * (k / 32), rows, k, y + s * rows);
+    }
+    return 0;
+}
+
 /* Small-M batch (hanzo-ml src/vulkan_backend.rs, the `matmul_q*_gpu`
  * prefill products): y[i, r] = sum_j W[r, j] * x[i, j] for the m rows of
  * x[m, k] (row-major), output y[m, rows] row-major. Each block is decoded to

@@ -491,6 +491,67 @@ def test_q4k_dp4a_matvec_is_the_matvec_of_the_dequantized_activation():
     assert np.max(np.abs(y - yf)) <= 0.05 * np.max(np.abs(yf))
 
 
+# ------------------------------------------------- Q6_K x int8 (dp4a path)
+
+def test_q6k_dp4a_groupdots_of_known_codes():
+    """xq = 127 e_j picks 127 * (q_j - 32) into the 16-group of j, zeros elsewhere."""
+    q = [(i * 5 + 3 * (i // 32)) % 64 for i in range(256)]
+    b = pack_q6k(f16_bits(1.0), [1] * 16, q)
+    for j in [0, 15, 16, 31, 100, 128, 200, 255]:
+        xq = np.zeros(256, dtype=np.int8)
+        xq[j] = 127
+        dots = oracle.q6k_dp4a_groupdots(b, xq, 1, 256)[0]
+        want = np.zeros(16, dtype=np.int64)
+        want[j // 16] = 127 * (q[j] - 32)
+        assert np.array_equal(dots, want)
+
+
+def test_q6k_dp4a_groupdots_brute_force():
+    """With d = 1 and every scale 1 the pinned decoder returns q - 32 itself:
+    the group dots are its integer dots with xq, in groups of 16."""
+    rows, k = 3, 512
+    st = synth.Stream(93)
+    w = synth.gen_q6k_rows(st, rows, k)
+    w = w.reshape(rows, k // 256, 210).copy()
+    w[:, :, 192:208] = 1
+    w[:, :, 208], w[:, :, 209] = 0x00, 0x3C
+    w = w.reshape(rows, -1)
+    codes = oracle.dequant("q6k", w, rows, k).astype(np.int64)
+    xq = oracle.quantize_act_q8(synth.gen_normal(st, k), 1, k)[0].reshape(-1)
+    want = (codes * xq.astype(np.int64)).reshape(rows, k // 16, 16).sum(axis=2)
+    assert np.array_equal(oracle.q6k_dp4a_groupdots(w, xq, rows, k), want)
+
+
+def test_q6k_dp4a_matvec_is_the_matvec_of_the_dequantized_activation():
+    rows, k = 5, 768
+    st = synth.Stream(94)
+    w = synth.gen_q6k_rows(st, rows, k)
+    x = synth.gen_normal(st, k)
+    xq, xs, _ = oracle.quantize_act_q8(x, 1, k)
+    xdq = (xs.reshape(-1, 1).astype(np.float64) * xq.reshape(-1, 32)).reshape(-1)
+    W = oracle.dequant("q6k", w, rows, k)
+    assert np.allclose(oracle.qmv_q6k_dp4a(w, xq.reshape(-1), xs.reshape(-1), rows, k), W @ xdq,
+                       rtol=1e-12, atol=1e-12)
+
+
+def test_moe_q6k_dp4a_matches_dense_per_expert_and_flags_bad_ids():
+    e, n, k, slots = 4, 3, 512, 4
+    st = synth.Stream(95)
+    bank = synth.gen_q6k_rows(st, e * n, k)
+    x = synth.gen_normal(st, slots * k).reshape(slots, k)
+    xq, xs, _ = oracle.quantize_act_q8(x, slots, k)
+    ids = np.array([3, 0, 3, 1], dtype=np.int32)
+    y = oracle.moe_qmv_q6k_dp4a(bank, xq, xs, ids, n, k, e)
+    rb = (k // 256) * 210
+    flat = bank.reshape(-1)
+    for s_ in range(slots):
+        part = flat[ids[s_] * n * rb:(ids[s_] + 1) * n * rb]
+        assert np.array_equal(y[s_], oracle.qmv_q6k_dp4a(part, xq[s_], xs[s_], n, k))
+    y_bad = oracle.moe_qmv_q6k_dp4a(bank, xq, xs, np.array([1, 4, -1, 0], dtype=np.int32), n, k, e)
+    assert np.all(np.isnan(y_bad[1])) and np.all(np.isnan(y_bad[2]))
+    assert not np.any(np.isnan(y_bad[0])) and not np.any(np.isnan(y_bad[3]))
+
+
 # ------------------------------------------------------------- small-M batch
 
 @pytest.mark.parametrize("fmt,m,rows,k", [("q4k", 3, 4, 512), ("q6k", 2, 3, 256), ("q8_0", 8, 5, 96),
