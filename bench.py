@@ -77,7 +77,8 @@ def measured_peak():
 
 
 # Block format of each workload kind's weights.
-KIND_FMT = {"q4k": "q4k", "q4k_dp4a": "q4k", "q6k": "q6k", "q8_0_dp4a": "q8_0", "q5k": "q5k", "q4_0": "q4_0",
+KIND_FMT = {"q4k": "q4k", "q4k_dp4a": "q4k", "q6k": "q6k", "q6k_dp4a": "q6k", "moe_q6k_dp4a": "q6k",
+            "q8_0_dp4a": "q8_0", "q5k": "q5k", "q4_0": "q4_0",
             "moe_q4k": "q4k", "moe_q4k_dp4a": "q4k", "moe_q6k": "q6k", "moe_q8_0": "q8_0", "moe_q4_0": "q4_0",
             "moe_q5k": "q5k", "qmm_q4k": "q4k", "qmm_q6k": "q6k", "qmm_q8_0": "q8_0"}
 # MoE kinds with an f32 activation (one entry point each, same arguments).
@@ -101,9 +102,9 @@ def algorithmic_bytes(name: str) -> int:
         return wb + 4 * c["slots"] * c["k"] + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
     if c["kind"].startswith("qmm_"):
         return wb + 4 * c["m"] * c["k"] + 4 * c["m"] * c["rows"]   # W read once for all m rows
-    if c["kind"] == "moe_q4k_dp4a":
+    if c["kind"] in ("moe_q4k_dp4a", "moe_q6k_dp4a"):
         return wb + c["slots"] * (c["k"] + 4 * (c["k"] // 32)) + 4 * c["slots"] * c["rows"] + 4 * c["slots"]
-    if c["kind"] in ("q8_0_dp4a", "q4k_dp4a"):
+    if c["kind"] in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a"):
         return wb + c["k"] + 4 * (c["k"] // 32) + 4 * c["rows"]
     return wb + 4 * c["k"] + 4 * c["rows"]
 
@@ -204,7 +205,7 @@ class Workload:
             self.y = torch.empty(c["m"], self.rows, dtype=torch.float32, device=dev)
         else:
             self.y = torch.empty(self.rows, dtype=torch.float32, device=dev)
-        if self.kind in ("q8_0_dp4a", "q4k_dp4a", "moe_q4k_dp4a"):
+        if self.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a", "moe_q4k_dp4a", "moe_q6k_dp4a"):
             m = c.get("slots", 1) if self.kind.startswith("moe_") else 1
             self.m = m
             self.xq = torch.empty(m * self.k, dtype=torch.int8, device=dev)
@@ -224,12 +225,12 @@ class Workload:
             m = self.c["m"]
             getattr(q, self.kind)(w, self.x, self.y, self.rows, self.k, m, stream=stream, cfg=cfg)
             return q.qmm_launches(self.kind[4:], self.k, m)
-        elif self.kind in ("q8_0_dp4a", "q4k_dp4a"):
+        elif self.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a"):
             n = 1
             if with_quant:
                 q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k, stream=stream)
                 n = 2
-            fn = q.qmv_q8_dp4a if self.kind == "q8_0_dp4a" else q.qmv_q4k_dp4a
+            fn = {"q8_0_dp4a": q.qmv_q8_dp4a, "q4k_dp4a": q.qmv_q4k_dp4a, "q6k_dp4a": q.qmv_q6k_dp4a}[self.kind]
             fn(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg)
             return n
         elif self.kind in MOE_F32:
@@ -237,14 +238,15 @@ class Workload:
             fn = getattr(q, f"moe_qmv_{self.kind[4:]}")
             fn(w, self.x, self.y, self.rows, self.k, self.ids[i % len(self.ids)], c["slots"],
                c["n_experts"], stream=stream, cfg=cfg)
-        elif self.kind == "moe_q4k_dp4a":
+        elif self.kind in ("moe_q4k_dp4a", "moe_q6k_dp4a"):
             c = self.c
             n = 1
             if with_quant:
                 q.quantize_act_q8(self.x, self.xq, self.xs, None, self.m, self.k, stream=stream)
                 n = 2
-            q.moe_qmv_q4k_dp4a(w, self.xq, self.xs, self.y, self.rows, self.k, self.ids[i % len(self.ids)],
-                               c["slots"], c["n_experts"], stream=stream, cfg=cfg)
+            fn = q.moe_qmv_q4k_dp4a if self.kind == "moe_q4k_dp4a" else q.moe_qmv_q6k_dp4a
+            fn(w, self.xq, self.xs, self.y, self.rows, self.k, self.ids[i % len(self.ids)],
+               c["slots"], c["n_experts"], stream=stream, cfg=cfg)
             return n
         return 1
 
@@ -396,7 +398,7 @@ def run_ours(args):
                 row[tag + "us_per_call"] = round(ms * 1e3, 3)
                 row[tag + "packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
                 row[tag + "frac_of_measured_hbm"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9 / peak, 4)
-            if w2.kind in ("q8_0_dp4a", "q4k_dp4a", "moe_q4k_dp4a") and mode != 2:
+            if w2.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a", "moe_q4k_dp4a", "moe_q6k_dp4a") and mode != 2:
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
                 row[tag + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
                 del g3

@@ -27,7 +27,8 @@ QMV_STATUS_BAD_EXPERT_ID = 1
 QMV_STATUS_WAIT_TIMEOUT = 2
 
 (FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A,
- FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K, FMT_QMM_Q4K, FMT_QMM_Q6K, FMT_QMM_Q8_0) = range(16)
+ FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K, FMT_QMM_Q4K, FMT_QMM_Q6K, FMT_QMM_Q8_0,
+ FMT_Q6K_DP4A, FMT_MOE_Q6K_DP4A) = range(18)
 
 
 class QmvLibraryMissing(RuntimeError):
@@ -64,6 +65,11 @@ _SIG = {
     "moe_qmv_q4k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "qmv_q4k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _P],
     "qmv_q4k_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
+    "qmv_q6k_dp4a": [_P, _P, _P, _P, _I, _I, _P],
+    "qmv_q6k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _P],
+    "qmv_q6k_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
+    "moe_qmv_q6k_dp4a": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P],
+    "moe_qmv_q6k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "qmv_q4k_cfg": [_P, _P, _P, _I, _I, _P, _P],
     "qmv_q6k_cfg": [_P, _P, _P, _I, _I, _P, _P],
     "qmv_q8_0_cfg": [_P, _P, _P, _I, _I, _P, _P],
@@ -240,6 +246,25 @@ def qmv_q4k_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, check=True):
         return _call("qmv_q4k_dp4a", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _stream(stream), check=check)
     return _call("qmv_q4k_dp4a_cfg", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _cfg(cfg), _stream(stream),
                  check=check)
+
+
+def qmv_q6k_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("qmv_q6k_dp4a", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q6k_dp4a_cfg", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _cfg(cfg), _stream(stream),
+                 check=check)
+
+
+def qmv_q6k_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):
+    return _call("qmv_q6k_dp4a_blockdots", _ptr(w), _ptr(xq), _ptr(dots), rows, k, _stream(stream), check=check)
+
+
+def moe_qmv_q6k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
+    if cfg is None:
+        return _call("moe_qmv_q6k_dp4a", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
+                     n_experts, _stream(stream), check=check)
+    return _call("moe_qmv_q6k_dp4a_cfg", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
+                 n_experts, _cfg(cfg), _stream(stream), check=check)
 
 
 def qmv_q4k_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):

@@ -166,6 +166,42 @@ int qmv_q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int
     return qmv_q4k_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
 }
 
+int qmv_q6k_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                     const qmv_cfg* cfg, cudaStream_t stream) {
+    if (!xs) return QMV_EINVAL;
+    int rc = check_dense(w, xq, y, rows, k, 256, 210);
+    if (rc) return rc;
+    if (!aligned(xq, 16) || !aligned(xs, 4)) return QMV_EALIGN;
+    return qmvi::q6k_dp4a(w, xq, xs, y, rows, k, cfg, stream);
+}
+
+int qmv_q6k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                 cudaStream_t stream) {
+    return qmv_q6k_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
+}
+
+int moe_qmv_q6k_dp4a_cfg(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                         const int32_t* ids, int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+    if (!xs) return QMV_EINVAL;
+    int rc = check_dense(w_bank, xq, y, rows, k, 256, 210);
+    if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 210);
+    if (rc) return rc;
+    if (!aligned(xq, 16) || !aligned(xs, 4)) return QMV_EALIGN;
+    return qmvi::moe_q6k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, cfg, stream);
+}
+
+int moe_qmv_q6k_dp4a(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                     const int32_t* ids, int slots, int n_experts, cudaStream_t stream) {
+    return moe_qmv_q6k_dp4a_cfg(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, nullptr, stream);
+}
+
+int qmv_q6k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t stream) {
+    int rc = check_dense(w, xq, dots, rows, k, 256, 210);
+    if (rc) return rc;
+    if (!aligned(xq, 16)) return QMV_EALIGN;
+    return qmvi::q6k_dp4a_blockdots(w, xq, dots, rows, k, stream);
+}
+
 int moe_qmv_q4k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids,
                     int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
     int rc = check_dense(w_bank, x, y, rows, k, 256, 144);
@@ -320,15 +356,17 @@ int qmv_device_status(unsigned int* status, int clear) {
 namespace {
 
 // Plan ids that describe an MoE launch (grid.y = slots).
-bool plan_is_moe(int fmt) { return fmt == 4 || fmt == 6 || fmt == 7 || (fmt >= 10 && fmt <= 12); }
+bool plan_is_moe(int fmt) { return fmt == 4 || fmt == 6 || fmt == 7 || (fmt >= 10 && fmt <= 12) || fmt == 17; }
 
 // Plan of format fmt on device `di`.
 int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_cfg* cfg, qmv::KParams* kp,
             qmv::Plan* pl) {
-    static const int qk[16] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256, 256, 256, 32};
-    if (fmt < 0 || fmt > 15 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
+    static const int qk[18] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256, 256, 256, 32, 256, 256};
+    if (fmt < 0 || fmt > 17 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
     const bool moe = plan_is_moe(fmt);
     if (moe && slots <= 0) return QMV_EINVAL;
+    if (fmt == 16) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, 1, cfg, kp, pl);
+    if (fmt == 17) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, slots, cfg, kp, pl);
     if (fmt >= 13) {
         // batched: `slots` is the tile's row count of x, 2..8
         switch (slots) {

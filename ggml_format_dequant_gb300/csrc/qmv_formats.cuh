@@ -159,6 +159,8 @@ struct Q4D {
     static constexpr bool LIMBS = false;
     static constexpr int DEFAULT_UNROLL = 2;
     static constexpr int DOTS_PER_UNIT = 2;   // 32-weight sub-blocks per unit
+    static constexpr int DOT_WEIGHTS = 32;    // weights per exported dot
+    __device__ __forceinline__ static int dot_base(int ug) { return DOTS_PER_UNIT * ug; }
 
     __host__ __device__ static int units(int nb) { return 4 * nb; }
     __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u >> 2) * BLOCK_BYTES; }
@@ -444,6 +446,110 @@ struct Q6K {
     }
 };
 
+// ============================================================ Q6_K, q8 activation
+//
+// The dp4a path of Q6_K (hanzo-ml src/vulkan_backend.rs, the
+// `moe_matvec_q6k_dp4a_blk_dn` decode): units as in Q6K, the activation as
+// int8 codes with one f32 scale per 32. The 6-bit codes q (unsigned bytes) are
+// dotted with the codes exactly, and the -32 is folded against the sum of the
+// 16 activation codes of each quarter, formed once at load:
+//     d * scale * xs * (sum(q * xq) - 32 * sum(xq))   per 16-weight group.
+struct Q6D {
+    static constexpr int QK = 256;
+    static constexpr int BLOCK_BYTES = 210;
+    static constexpr int SLICE_BLOCKS = 8;    // 32 units (1680 bytes)
+    static constexpr int SLACK = 16;
+    static constexpr bool LIMBS = false;
+    static constexpr int DEFAULT_UNROLL = 2;
+    static constexpr int DOTS_PER_UNIT = 4;   // 16-weight scale groups per unit
+    static constexpr int DOT_WEIGHTS = 16;    // weights per exported dot
+    // The unit's groups are 8H + 2qd + hh of its block: the first at
+    // 16 * block + 8H + hh, the others every 2.
+    __device__ __forceinline__ static int dot_base(int ug) { return 16 * (ug >> 2) + 8 * ((ug & 3) >> 1) + (ug & 1); }
+
+    __host__ __device__ static int units(int nb) { return 4 * nb; }
+    __device__ __forceinline__ static uint32_t unit_byte(int u) { return Q6K::unit_byte(u); }
+    __device__ __forceinline__ static int unit_elem(int u) { return Q6K::unit_elem(u); }
+
+    struct X {
+        uint32_t q[16];   // [4*qd + i]: codes of weights 128H + 32qd + 16hh + 4i ..
+        float xs[4];      // scale of quarter qd's 32-group
+        int xsum[4];      // sum of quarter qd's 16 codes
+    };
+    using L = Q6K::L;
+    __device__ __forceinline__ static L lane_consts(int u, int nb, int ug) { return Q6K::lane_consts(u, nb, ug); }
+
+    // e0 = index of weight 128H + 16hh of the unit's block, in the row.
+    __device__ __forceinline__ static void load_xq(X& x, const L&, const int8_t* __restrict__ xq,
+                                                   const float* __restrict__ xs, int e0) {
+#pragma unroll
+        for (int qd = 0; qd < 4; qd++) {
+            const int e = e0 + 32 * qd;
+            const uint4 t = __ldg(reinterpret_cast<const uint4*>(xq + e));
+            x.q[4 * qd] = t.x; x.q[4 * qd + 1] = t.y; x.q[4 * qd + 2] = t.z; x.q[4 * qd + 3] = t.w;
+            x.xs[qd] = __ldg(xs + (e >> 5));
+            int sm = 0;
+#pragma unroll
+            for (int i = 0; i < 4; i++) sm = dp4a_ss(0x01010101u, x.q[4 * qd + i], sm);
+            x.xsum[qd] = sm;
+        }
+    }
+
+    // The four groups' exact dots sum((q - 32) * xq) (|.| <= 16 * 32 * 127).
+    __device__ __forceinline__ static void group_dots(uint32_t a, const L& l, const X& x, int (&dot)[4], uint2& scw,
+                                                      float& d) {
+        const uint32_t wa = a & ~3u;
+        const uint32_t sh = (a & 3u) * 8u;
+        const uint32_t w1 = wa + l.ql_off;
+        const uint4 qla = lds16_sh<0>(w1, sh);
+        const uint4 qlb = lds16_sh<32>(w1, sh);
+        const uint4 qhv = lds16_sh<0>(wa + l.qh_off, sh);
+        scw = lds8_sh<0>(wa + l.sc_off, sh);
+        d = f16_lo(lds32<208>(wa) >> sh);
+        const uint32_t A[4] = {qla.x, qla.y, qla.z, qla.w};
+        const uint32_t B[4] = {qlb.x, qlb.y, qlb.z, qlb.w};
+        const uint32_t Hq[4] = {qhv.x, qhv.y, qhv.z, qhv.w};
+        int s[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            s[0] = dp4a_us((A[i] & 0x0f0f0f0fu) | ((Hq[i] << 4) & 0x30303030u), x.q[i], s[0]);
+            s[1] = dp4a_us((B[i] & 0x0f0f0f0fu) | ((Hq[i] << 2) & 0x30303030u), x.q[4 + i], s[1]);
+            s[2] = dp4a_us(((A[i] >> 4) & 0x0f0f0f0fu) | (Hq[i] & 0x30303030u), x.q[8 + i], s[2]);
+            s[3] = dp4a_us(((B[i] >> 4) & 0x0f0f0f0fu) | ((Hq[i] >> 2) & 0x30303030u), x.q[12 + i], s[3]);
+        }
+#pragma unroll
+        for (int qd = 0; qd < 4; qd++) dot[qd] = s[qd] - 32 * x.xsum[qd];
+    }
+
+    // a: shared address of the block (2-byte aligned).
+    __device__ __forceinline__ static float dot(uint32_t a, const L& l, const X& x, float r, bool) {
+        int dt[4];
+        uint2 scw;
+        float d;
+        group_dots(a, l, x, dt, scw, d);
+        const float nd = -d * THREE22;
+#pragma unroll
+        for (int qd = 0; qd < 4; qd++) {
+            const uint32_t sw = (qd < 2) ? scw.x : scw.y;
+            const uint32_t sx = prmt(sw, 0u, (qd & 1) ? l.sel1 : l.sel0);   // the int8 scale, sign-extended
+            const float ds = __fmaf_rn(d, __uint_as_float(sx + 0x4B400000u), nd);
+            r = __fmaf_rn(ds * x.xs[qd], __int2float_rn(dt[qd]), r);
+        }
+        return r;
+    }
+
+    // The exact int32 dots of the unit's four groups (MODE_BLOCKDOTS), at
+    // out[0], out[2], out[4], out[6].
+    __device__ __forceinline__ static void block_dots(uint32_t a, const L& l, const X& x, bool, int32_t* out) {
+        int dt[4];
+        uint2 scw;
+        float d;
+        group_dots(a, l, x, dt, scw, d);
+#pragma unroll
+        for (int qd = 0; qd < 4; qd++) out[2 * qd] = dt[qd];
+    }
+};
+
 // ============================================================ Q8_0, f32 x
 struct Q8F {
     static constexpr int QK = 32;
@@ -593,6 +699,8 @@ struct Q8D {
     static constexpr bool LIMBS = false;
     static constexpr int DEFAULT_UNROLL = 2;
     static constexpr int DOTS_PER_UNIT = 4;   // 32-weight blocks per unit
+    static constexpr int DOT_WEIGHTS = 32;    // weights per exported dot
+    __device__ __forceinline__ static int dot_base(int ug) { return DOTS_PER_UNIT * ug; }
 
     __host__ __device__ static int units(int nb) { return (nb + 3) / 4; }
     __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u) * 4u * BLOCK_BYTES; }

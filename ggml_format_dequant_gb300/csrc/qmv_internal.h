@@ -25,6 +25,11 @@ int status_q4k(unsigned int* out, int clear);
 int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s);
 int moe_q6k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
             int n_experts, const qmv_cfg* cfg, cudaStream_t s);
+int q6k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+             cudaStream_t s);
+int q6k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s);
+int moe_q6k_dp4a(const void* bank, const int8_t* xq, const float* xs, float* y, int rows, int k, const int32_t* ids,
+                 int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t s);
 int dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t s);
 int status_q6k(unsigned int* out, int clear);
 

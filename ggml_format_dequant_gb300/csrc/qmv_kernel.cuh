@@ -48,7 +48,7 @@ struct KParams {
     const int8_t* xq;           // dp4a activation codes: [k] dense, [slots, k] MoE
     const float* xqs;           // dp4a activation scales: [k/32] dense, [slots, k/32] MoE
     float* y;                   // [rows] dense, [slots, rows] MoE
-    int32_t* dots;              // [rows, k/32] block dots (MODE_BLOCKDOTS)
+    int32_t* dots;              // [rows, k / F::DOT_WEIGHTS] integer dots (MODE_BLOCKDOTS)
     const int32_t* ids;         // [slots] expert ids (MoE)
     int n_experts;
     int rows, k, nb;            // rows per matrix, k, blocks per row
@@ -328,8 +328,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
                     for (; jb < nr; jb += rpw, a += rstep) {
                         if (has_unit && jb + sub < nr)
                             F::block_dots(a, lc, xr, aligned8,
-                                          p.dots + static_cast<long long>(R0 + rl0 + jb + sub) * (p.k >> 5) +
-                                              F::DOTS_PER_UNIT * ug);
+                                          p.dots + static_cast<long long>(R0 + rl0 + jb + sub) * (p.k / F::DOT_WEIGHTS) +
+                                              F::dot_base(ug));
                     }
                 }
             }

@@ -1,5 +1,6 @@
-// qmv_q6k.cu -- Q6_K dense matvec launch and the Q6_K dequantizer used by the
-// tests.
+// qmv_q6k.cu -- Q6_K dense and MoE matvec launches (f32 activation and the
+// int8-activation dp4a path), the dp4a group dots and the Q6_K dequantizer
+// used by the tests.
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
 
@@ -71,6 +72,59 @@ int moe_q6k(const void* bank, const float* x, float* y, int rows, int k, const i
     int rc = make_plan<Q6K>(rows, k, slots, cfg, &kp, &pl);
     if (rc) return rc;
     return launch<Q6K, true, MODE_MATVEC>(kp, pl, slots, s);
+}
+
+namespace {
+
+KParams q6k_params(const void* w, int rows, int k) {
+    KParams kp{};
+    kp.w = static_cast<const uint8_t*>(w);
+    kp.rows = rows;
+    kp.k = k;
+    kp.nb = k / 256;
+    kp.rowbytes = static_cast<uint32_t>(kp.nb) * 210u;
+    kp.matbytes = static_cast<unsigned long long>(rows) * kp.rowbytes;
+    kp.wbytes = kp.matbytes;
+    return kp;
+}
+
+}  // namespace
+
+int q6k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+             cudaStream_t s) {
+    KParams kp = q6k_params(w, rows, k);
+    kp.xq = xq;
+    kp.xqs = xs;
+    kp.y = y;
+    Plan pl;
+    int rc = make_plan<Q6D>(rows, k, 1, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q6D, false, MODE_MATVEC>(kp, pl, 1, s);
+}
+
+int q6k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s) {
+    KParams kp = q6k_params(w, rows, k);
+    kp.xq = xq;
+    kp.dots = dots;
+    Plan pl;
+    int rc = make_plan<Q6D>(rows, k, 1, nullptr, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q6D, false, MODE_BLOCKDOTS>(kp, pl, 1, s);
+}
+
+int moe_q6k_dp4a(const void* bank, const int8_t* xq, const float* xs, float* y, int rows, int k, const int32_t* ids,
+                 int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+    KParams kp = q6k_params(bank, rows, k);
+    kp.xq = xq;
+    kp.xqs = xs;
+    kp.y = y;
+    kp.ids = ids;
+    kp.n_experts = n_experts;
+    kp.wbytes = static_cast<unsigned long long>(n_experts) * kp.matbytes;
+    Plan pl;
+    int rc = make_plan<Q6D>(rows, k, slots, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q6D, true, MODE_MATVEC>(kp, pl, slots, s);
 }
 
 int dequant_q6k(const void* w, float* out, int rows, int k, cudaStream_t s) {

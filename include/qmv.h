@@ -131,6 +131,16 @@ int qmv_q8_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int 
 int qmv_q4k_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
                  cudaStream_t stream);
 
+/* dp4a matvec of Q6_K weights with a quantized activation (the pages' Q6_K
+ * dp4a decode): y[r] = sum_g d*scale_g * xs[g/2] * dot[r, g] in f32 over the
+ * 16-weight scale groups g of row r, where dot[r, g] is the exact int32
+ * sum of (q - 32) * xq over the group (formed as sum(q * xq) - 32 * sum(xq)).
+ * w: Q6_K rows as for qmv_q6k; xq: int8 [k], 16-byte aligned; xs: f32 [k/32];
+ * y: f32 [rows]; k % 256 == 0. Cites hanzo-ml src/vulkan_backend.rs,
+ * `moe_matvec_q6k_dp4a_blk_dn` (the -32 folded against activation sums). */
+int qmv_q6k_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                 cudaStream_t stream);
+
 /* MoE indexed Q4_K matvec: y[s, r] = sum_j W[ids[s], r, j] * x[s, j].
  * w_bank: one resident bank [n_experts, rows, k] of Q4_K rows (expert e's
  * matrix starts at byte e * rows * (k/256) * 144);
@@ -176,6 +186,14 @@ int moe_qmv_q5k(const void *w_bank, const float *x, float *y, int rows, int k,
  * Bank, ids, y and errors as for moe_qmv_q4k.
  * Cites hanzo-ml src/vulkan_backend.rs, `moe_matvec_q4k_dp4a_blk_*`. */
 int moe_qmv_q4k_dp4a(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                     const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
+
+/* MoE indexed Q6_K matvec on the dp4a path: slot s multiplies expert ids[s]
+ * with its own quantized activation, xq int8 [slots, k] (16-byte aligned) and
+ * xs f32 [slots, k/32], as qmv_q6k_dp4a does. Bank, ids, y and errors as for
+ * moe_qmv_q6k. Cites hanzo-ml src/vulkan_backend.rs,
+ * `moe_matvec_q6k_dp4a_blk_dn`. */
+int moe_qmv_q6k_dp4a(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows, int k,
                      const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
 
 /* Decode-chain overlap (process-wide; 0 by default).
@@ -253,6 +271,11 @@ int moe_qmv_q4k_dp4a_cfg(const void *w_bank, const int8_t *xq, const float *xs, 
 int moe_qmv_q4k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
                     cudaStream_t stream);
+int qmv_q6k_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                     const qmv_cfg *cfg, cudaStream_t stream);
+int moe_qmv_q6k_dp4a_cfg(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows,
+                         int k, const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
+                         cudaStream_t stream);
 int qmm_q4k_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
                 cudaStream_t stream);
 int qmm_q6k_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
@@ -289,6 +312,11 @@ int qmv_q8_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int ro
  * sub-block t, computed by the code path qmv_q4k_dp4a uses. */
 int qmv_q4k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int rows, int k,
                            cudaStream_t stream);
+/* The same for Q6_K rows: dots[r, g] (int32 [rows, k/16]) of every 16-weight
+ * scale group g, sum((q - 32) * xq), computed by the code path qmv_q6k_dp4a
+ * uses. */
+int qmv_q6k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int rows, int k,
+                           cudaStream_t stream);
 
 /* Launch plan the library would use (for benchmark reports): threads per CTA,
  * CTAs (all slots), rows per ring slot, ring slots per row group and dynamic
@@ -296,7 +324,8 @@ int qmv_q4k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int r
  * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K,
  * 5 = Q4_K dp4a, 6 = MoE Q6_K, 7 = MoE Q4_K dp4a, 8 = Q5_K, 9 = Q4_0,
  * 10 = MoE Q8_0, 11 = MoE Q4_0, 12 = MoE Q5_K, 13 / 14 / 15 = the batched
- * Q4_K / Q6_K / Q8_0 product for one tile of `slots` (2..8) rows of x. */
+ * Q4_K / Q6_K / Q8_0 register kernel for one tile of `slots` (2..8) rows of x,
+ * 16 = Q6_K dp4a, 17 = MoE Q6_K dp4a. */
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
                   int *chunk_rows, int *chunks, int *smem_bytes);
 

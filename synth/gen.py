@@ -217,6 +217,10 @@ CONFIGS = {
     "moe_q8_0_e128_n768_k2048_s8": dict(kind="moe_q8_0", rows=768, k=2048, seed=8, n_experts=128, slots=8),
     "moe_q4_0_e128_n768_k2048_s8": dict(kind="moe_q4_0", rows=768, k=2048, seed=9, n_experts=128, slots=8),
     "moe_q5k_e128_n768_k2048_s8": dict(kind="moe_q5k", rows=768, k=2048, seed=10, n_experts=128, slots=8),
+    # The Q6_K suite matrix and the Q6_K MoE bank on the dp4a path (same seeds:
+    # the same bytes, ids and x).
+    "q6k_dp4a_4096x14336": dict(kind="q6k_dp4a", rows=4096, k=14336, seed=4),
+    "moe_q6k_dp4a_e128_n2048_k768_s8": dict(kind="moe_q6k_dp4a", rows=2048, k=768, seed=5, n_experts=128, slots=8),
     # Small-M batches (m rows of x sharing one weight read) on the headline and
     # the two large suite matrices (same seeds: the same weight bytes; the
     # first row of x is the single-row workload's x).
@@ -237,7 +241,7 @@ def make_config(name: str) -> dict:
     if kind in ("q4k", "q4k_dp4a"):
         c["w"] = gen_q4k_rows(st, rows, k)
         c["x"] = gen_normal(st, k)
-    elif kind == "q6k":
+    elif kind in ("q6k", "q6k_dp4a"):
         c["w"] = gen_q6k_rows(st, rows, k)
         c["x"] = gen_normal(st, k)
     elif kind == "q8_0_dp4a":
@@ -249,9 +253,9 @@ def make_config(name: str) -> dict:
     elif kind.startswith("qmm_"):
         c["w"] = GEN_ROWS[kind[4:]](st, rows, k)
         c["x"] = gen_normal(st, c["m"] * k).reshape(c["m"], k)
-    elif kind in ("moe_q4k", "moe_q4k_dp4a", "moe_q6k", "moe_q8_0", "moe_q4_0", "moe_q5k"):
+    elif kind in ("moe_q4k", "moe_q4k_dp4a", "moe_q6k", "moe_q6k_dp4a", "moe_q8_0", "moe_q4_0", "moe_q5k"):
         e, s = c["n_experts"], c["slots"]
-        fmt = "q4k" if kind == "moe_q4k_dp4a" else kind[4:]
+        fmt = kind[4:].replace("_dp4a", "")
         c["w"] = GEN_ROWS[fmt](st, e * rows, k).reshape(e, rows, -1)
         c["ids"] = gen_moe_ids(st, s, e)
         c["x"] = gen_normal(st, s * k).reshape(s, k)

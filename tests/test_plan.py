@@ -20,7 +20,8 @@ import pytest
 
 DEVICE = (152, 232448, 233472, 1024)
 FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5, "moe6": 6, "moe4d": 7, "q5k": 8,
-          "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12, "qmm4": 13, "qmm6": 14, "qmm8": 15}
+          "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12, "qmm4": 13, "qmm6": 14, "qmm8": 15,
+          "q6d": 16, "moe6d": 17}
 
 
 def batch_uw(m):
@@ -55,7 +56,7 @@ def fmt_info(fmt, m=1):
         # five 32-bit loads from the word below the 2-byte aligned block
         return dict(qk=32, bb=18, sb=32, units=lambda nb: nb, ubyte=lambda u: u * 18,
                     extent=lambda a: (a - (a & 3), a - (a & 3) + 20), align=2)
-    if fmt in ("q6k", "moe6"):
+    if fmt in ("q6k", "moe6", "q6d", "moe6d"):
         return dict(qk=256, bb=210, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 210,
                     extent=lambda a: (a - (a & 3), a - (a & 3) + 212), align=2)
     if fmt in ("q8_0", "moe8"):
@@ -94,7 +95,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
     CL = P["CL"]
     assert CL in (1, 2, 4, 8) and parts % CL == 0 and (k // 16) % (2 * CL) == 0
     assert P["rq"] >= 1
-    if fmt in ("q8d", "q4d", "moe4d", "qmm4", "qmm6", "qmm8"):
+    if fmt in ("q8d", "q4d", "moe4d", "qmm4", "qmm6", "qmm8", "q6d", "moe6d"):
         assert CL == 1
     lg = GS.bit_length() - 1
     rpw = 32 >> lg
@@ -104,7 +105,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
 
     # shared-memory layout: disjoint, ordered regions inside the device limit
     regions = []
-    if fmt not in ("q8d", "q4d", "moe4d", "qmm4", "qmm6", "qmm8"):
+    if fmt not in ("q8d", "q4d", "moe4d", "qmm4", "qmm6", "qmm8", "q6d", "moe6d"):
         regions += [(P["off_la"], k), (P["off_lb"], k), (P["off_lc"], k), (P["off_xs"], 4 * (k // 32)),
                     (P["off_xsum16"], 4 * (k // 16))]
         for o, _ in regions:
@@ -179,7 +180,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
 WORKLOADS = [("q4k", 4096, 4096, 1), ("q4k", 256, 1024, 1), ("q8d", 14336, 4096, 1), ("q6k", 4096, 14336, 1),
              ("moe", 768, 2048, 8), ("q4d", 4096, 4096, 1), ("moe6", 2048, 768, 8), ("moe4d", 768, 2048, 8),
              ("q5k", 4096, 4096, 1), ("q4_0", 4096, 4096, 1), ("moe8", 768, 2048, 8), ("moe40", 768, 2048, 8),
-             ("moe5", 768, 2048, 8)]
+             ("moe5", 768, 2048, 8), ("q6d", 4096, 14336, 1), ("moe6d", 2048, 768, 8)]
 
 
 @pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
@@ -203,7 +204,9 @@ SHAPES = [("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 4352), ("q4k", 20, 163
           ("q4d", 97, 4352), ("q4d", 20, 16384), ("moe6", 96, 512), ("moe6", 7, 256), ("moe4d", 40, 512),
           ("q5k", 300, 768), ("q5k", 1, 256), ("q5k", 97, 4352), ("q5k", 20, 16384), ("q4_0", 300, 96),
           ("q4_0", 7, 4096), ("q4_0", 13, 32), ("q4_0", 64, 11008), ("q4_0", 33, 1056), ("moe8", 96, 512),
-          ("moe8", 7, 96), ("moe40", 96, 512), ("moe40", 7, 96), ("moe5", 40, 512), ("moe5", 7, 256)]
+          ("moe8", 7, 96), ("moe40", 96, 512), ("moe40", 7, 96), ("moe5", 40, 512), ("moe5", 7, 256),
+          ("q6d", 300, 512), ("q6d", 3, 256), ("q6d", 41, 14336), ("q6d", 130, 2816), ("moe6d", 96, 512),
+          ("moe6d", 7, 256)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -219,7 +222,7 @@ CFGS = [dict(ctas=1, chunk_rows=1, chunks=2), dict(ctas=3, chunk_rows=5, chunks=
 
 
 @pytest.mark.parametrize("cfg", CFGS)
-@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q8d", "q4d", "q5k", "q4_0"])
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q8d", "q4d", "q5k", "q4_0", "q6d"])
 def test_forced_plans(q, fmt, cfg):
     replay(q, fmt, 61, 512 if fmt != "q8d" else 256, 1, cfg)
 
@@ -237,7 +240,7 @@ def test_forced_wide_plans(q, fmt, k, cfg):
 
 def test_moe_forced_plan(q):
     replay(q, "moe", 40, 512, 5, dict(ctas=2, chunk_rows=3, chunks=2))
-    for fmt in ("moe8", "moe40", "moe5"):
+    for fmt in ("moe8", "moe40", "moe5", "moe6d"):
         replay(q, fmt, 40, 512, 5, dict(ctas=2, chunk_rows=3, chunks=2))
 
 
