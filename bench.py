@@ -194,17 +194,20 @@ class Workload:
         w0 = torch.from_numpy(c["w"].reshape(-1))
         self.w = [w0.to(dev) for _ in range(self.copies)]
         self.x = torch.from_numpy(np.ascontiguousarray(c["x"])).to(dev)
+        # one output buffer per weight copy: consecutive calls write different
+        # outputs, as the Q, K and V projections of one activation do
         if self.kind.startswith("moe_"):
-            self.y = torch.empty(c["slots"], self.rows, dtype=torch.float32, device=dev)
+            self.ys = [torch.empty(c["slots"], self.rows, dtype=torch.float32, device=dev) for _ in range(self.copies)]
             # a cycle of seeded id sets so no (bank, expert) slice repeats within 3x L2
             st = synth.Stream(1003)
             self.ids = [torch.from_numpy(c["ids"]).to(dev)]
             for _ in range(15):
                 self.ids.append(torch.from_numpy(synth.gen_moe_ids(st, c["slots"], c["n_experts"])).to(dev))
         elif self.kind.startswith("qmm_"):
-            self.y = torch.empty(c["m"], self.rows, dtype=torch.float32, device=dev)
+            self.ys = [torch.empty(c["m"], self.rows, dtype=torch.float32, device=dev) for _ in range(self.copies)]
         else:
-            self.y = torch.empty(self.rows, dtype=torch.float32, device=dev)
+            self.ys = [torch.empty(self.rows, dtype=torch.float32, device=dev) for _ in range(self.copies)]
+        self.y = self.ys[0]
         if self.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a", "moe_q4k_dp4a", "moe_q6k_dp4a"):
             m = c.get("slots", 1) if self.kind.startswith("moe_") else 1
             self.m = m
@@ -217,6 +220,7 @@ class Workload:
     def call(self, i: int, stream: int, with_quant: bool = False) -> int:
         """Enqueue call i; returns the number of kernels it launched."""
         q, w, cfg = self.q, self.w[i % self.copies], self.cfg
+        self.y = self.ys[i % self.copies]
         if self.kind == "q4k":
             q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
         elif self.kind in ("q6k", "q5k", "q4_0"):
@@ -324,7 +328,7 @@ def run_ours(args):
     # the previous call only before it writes y. --chain times the
     # conservative decode chain (mode 1: x is read only after the previous call
     # is done), --isolated plain launches (mode 0); per_config reports all three.
-    head_mode = 0 if args.isolated else (1 if args.chain else 2)
+    head_mode = args.headline_mode if args.headline_mode is not None else (0 if args.isolated else (1 if args.chain else 2))
     q.qmv_set_weight_prefetch(head_mode)
     wl = Workload(q, torch, HEADLINE, l2, device)
     K, W = args.steps, args.warmup
@@ -398,7 +402,7 @@ def run_ours(args):
                 row[tag + "us_per_call"] = round(ms * 1e3, 3)
                 row[tag + "packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
                 row[tag + "frac_of_measured_hbm"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9 / peak, 4)
-            if w2.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a", "moe_q4k_dp4a", "moe_q6k_dp4a") and mode != 2:
+            if w2.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a", "moe_q4k_dp4a", "moe_q6k_dp4a") and mode in (0, 1):
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
                 row[tag + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
                 del g3
@@ -486,6 +490,9 @@ def end_to_end(torch, q, wl, device, K):
     dy = torch.empty(wl.rows, dtype=torch.float32, device=device)
     s = torch.cuda.Stream()
     steps = max(1, min(K, 200))
+    # plain launches: each call follows host-to-device copies of its own
+    # weights and x, which no overlap mode may run ahead of
+    old_mode = q.qmv_set_weight_prefetch(0)
 
     def step():
         dw.copy_(hw, non_blocking=True)
@@ -506,6 +513,7 @@ def end_to_end(torch, q, wl, device, K):
         e1.record(s)
     e1.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    q.qmv_set_weight_prefetch(old_mode)
     ok = bool(np.isfinite(hy.numpy()).all())
     return {"value": round(weight_bytes(HEADLINE) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": hw.numel() + 4 * hx.numel(), "d2h_bytes_per_step": 4 * hy.numel(),
@@ -622,6 +630,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="skip the per-config table")
+    ap.add_argument("--headline-mode", type=int, choices=[0, 1, 2], default=None,
+                    help="launch mode of the headline calls (qmv_set_weight_prefetch); default 2")
     ap.add_argument("--only", default="", help="per-config table for the workloads whose names start with one of "
                                                "these comma-separated prefixes")
     ap.add_argument("--chain", action="store_true",
