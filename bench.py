@@ -255,6 +255,21 @@ class Workload:
         return 1
 
 
+def max_over_ranks(torch, ms: float, dist, device) -> float:
+    """The slowest rank's timed region (every rank calls it; one process, or
+    no process group: its own)."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, steps: int, bytes_per_step: int, ms_max: float) -> float:
+    """Packed-weight GB/s of the whole job: every rank ran `steps` steps of
+    `bytes_per_step` (replicas, weak scaling) within the slowest rank's time."""
+    return world * steps * bytes_per_step / (ms_max * 1e-3) / 1e9
+
+
 def time_graph(torch, wl: Workload, n_calls: int, with_quant=False, replays=1, barrier=None):
     """Capture n_calls rotated calls into one CUDA graph; return (ms per call,
     kernels per call, graph). Times `replays` replays with CUDA events."""
@@ -363,12 +378,9 @@ def run_ours(args):
         torch.cuda.synchronize()
     clock_window = (pre_t0, time.time())
 
-    ms_t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(torch, ms_total, dist, device)
     wbytes = weight_bytes(HEADLINE)
-    value = world * K * wbytes / (ms_max * 1e-3) / 1e9
+    value = whole_job_gbs(world, K, wbytes, ms_max)
     ms_step = ms_max / K
     alg = algorithmic_bytes(HEADLINE)
     achieved = alg / (ms_step * 1e-3) / 1e9
