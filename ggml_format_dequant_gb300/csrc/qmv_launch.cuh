@@ -106,9 +106,9 @@ template <class F>
 constexpr int outs_of() { return OutsOf<F>::value; }
 
 // Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense)
-// on a device described by `di`.
+// on a device described by `di`, for a given (or the default) CTA count.
 template <class F>
-inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
+inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
     const int nb = k / F::QK;
     const int U = F::units(nb);
     const int KS = (U + 31) / 32;
@@ -286,6 +286,40 @@ inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qm
     }
     *pl = P;
     return QMV_OK;
+}
+
+// Launch plan of format F. Independent calls (mode 2 of
+// qmv_set_weight_prefetch) overlap best when one call takes about two thirds
+// of the SMs, with CTAs that still hold their whole share in half an SM: more
+// calls are then in flight at once (measured on GB300: MoE Q4_K E128 n768
+// k2048 with 8 slots 2.32 -> 1.76 us a call, Q4_K 4096 x 4096 2.43 -> 2.26 us,
+// Q4_K dp4a 4096 x 4096 2.25 -> 1.82 us). Chained and plain calls, and shapes
+// whose share does not fit, use every SM.
+template <class F>
+inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
+    const int rc = make_plan_core<F>(di, rows, k, slots, cfg, kp, pl);
+    const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
+    if (rc || mode != 2 || (cfg && cfg->ctas > 0)) return rc;
+    const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;
+    const int per = slots > 1 ? slots : 1;
+    const int start = (2 * di.nsm + 3 * per - 1) / (3 * per);   // ceil(2 nsm / 3 / slots)
+    if (start >= pl->parts) return rc;                           // small shapes: already fewer CTAs
+    qmv_cfg c = cfg ? *cfg : qmv_cfg{0, 0, 0, 0, 0, 0};
+    const int step = per == 1 ? 4 : 1;
+    for (int parts = start; parts < pl->parts; parts += step) {
+        c.ctas = parts;
+        KParams k2 = *kp;
+        Plan p2;
+        if (make_plan_core<F>(di, rows, k, slots, &c, &k2, &p2)) continue;
+        const int rpc = k2.rq + (k2.rrem ? 1 : 0);
+        if (k2.S == 1 && k2.CR * k2.NG >= rpc && static_cast<long long>(p2.smem) <= half &&
+            p2.T <= 32 * WARPS_TWO_PER_SM) {
+            *kp = k2;
+            *pl = p2;
+            return QMV_OK;
+        }
+    }
+    return rc;
 }
 
 // The same on the current device.

@@ -77,8 +77,14 @@ def q():
     return lib
 
 
-def replay(q, fmt, rows, k, slots=1, cfg=None):
-    P = q.qmv_plan_detail(FMT_ID[fmt], rows, k, slots, cfg, DEVICE)
+def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
+    """Replay the plan computed under launch mode `mode` (0: plain, 2:
+    independent calls)."""
+    old = q.qmv_set_weight_prefetch(mode)
+    try:
+        P = q.qmv_plan_detail(FMT_ID[fmt], rows, k, slots, cfg, DEVICE)
+    finally:
+        q.qmv_set_weight_prefetch(old)
     f = fmt_info(fmt, slots)
     outs = f.get("outs", 1)
     nb = k // f["qk"]
@@ -86,7 +92,8 @@ def replay(q, fmt, rows, k, slots=1, cfg=None):
     KS, GS, NG, CR, S, R, W = P["KS"], P["GS"], P["NG"], P["CR"], P["S"], P["unroll"], P["W"]
     rowbytes, stride, parts = P["rowbytes"], P["slot_stride"], P["ctas"]
     assert rowbytes == nb * f["bb"] and U == P["U"]
-    assert KS == (U + 31) // 32 and W == (KS if KS > 1 else 0) and GS & (GS - 1) == 0 and U <= KS * GS
+    early = 1 if mode == 2 else 0
+    assert KS == (U + 31) // 32 and W == (KS if KS > 1 else early) and GS & (GS - 1) == 0 and U <= KS * GS
     assert 32 * NG * KS == P["threads"] <= 512
     assert P["rq"] * parts + P["rrem"] == rows and 0 <= P["rrem"] < parts
     # clusters share the activation prep: the CTAs of a matrix fill whole
@@ -267,6 +274,20 @@ def test_batch_plans(q, shape, m):
 @pytest.mark.parametrize("fmt,m", [("qmm4", 2), ("qmm4", 8), ("qmm6", 3), ("qmm8", 5)])
 def test_batch_forced_plans(q, fmt, m, cfg):
     replay(q, fmt, 61, 512, m, cfg)
+
+
+@pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
+def test_independent_call_plans(q, fmt, rows, k, slots):
+    """Mode 2 (independent calls): the whole-share workloads take about two
+    thirds of the SMs with CTAs that still fit in half an SM; every index is
+    replayed as for the default plans."""
+    P = replay(q, fmt, rows, k, slots, mode=2)
+    per = max(slots, 1)
+    if (fmt, rows) in (("q4k", 4096), ("moe", 768), ("q4d", 4096), ("moe4d", 768)):
+        assert -(-2 * DEVICE[0] // (3 * per)) <= P["ctas"] < -(-DEVICE[0] // per)
+        assert P["S"] == 1 and P["smem"] <= (DEVICE[2] - 2 * DEVICE[3]) // 2 and P["threads"] <= 256
+    if (fmt, rows) in (("q8d", 14336), ("q6k", 4096)):
+        assert P["ctas"] == DEVICE[0]
 
 
 def test_chain_shapes(q):
