@@ -1,6 +1,6 @@
 """GPU parity of every entry point against the CPU oracle, through the C ABI.
 
-Bars (stated here, derived in the design doc): decoded weights, quantized
+Bars: decoded weights, quantized
 activations, int32 block dots and MoE row gathers are bit-exact; f32 matvec
 outputs are within scale-relative error max|a-b|/max|a| <= 1e-4 of the f64
 oracle.
