@@ -7,8 +7,8 @@
 // per-16 (Q6_K) scales are applied to each group's partial product in
 // registers right after its MMAs, which keeps every operand exact:
 //  * A (16 weight rows x 16 k): the integer codes, exact in f16: Q4_K's q as
-//    the subnormal q * 2^-24 (a shift and a mask per pair; the 2^24 goes into
-//    the row scale), Q6_K's q - 32 and Q8_0's q made from the code bytes with
+//    the subnormal q * 2^-24 or 16 q * 2^-24 (one mask, or a shift and a
+//    mask, per pair; the power of two goes into the row scale), Q6_K's q - 32 and Q8_0's q made from the code bytes with
 //    one byte permute into the f16 pattern of 1024 + v and one f16x2
 //    subtraction.
 //  * B (16 k x 8 rows of x): x in two f16 parts, hi + lo, after a power-of-two
@@ -168,7 +168,7 @@ struct Q4KT {
         const uint32_t sb_lo = hb.y & 0x3f3f3f3fu, mb_lo = hb.z & 0x3f3f3f3fu;
         const uint32_t sb_hi = (hb.w & 0x0f0f0f0fu) | ((hb.y >> 2) & 0x30303030u);
         const uint32_t mb_hi = ((hb.w >> 4) & 0x0f0f0f0fu) | ((hb.z >> 2) & 0x30303030u);
-        const float da = f16_lo(ha.x), dma = f16_hi(ha.x), db = f16_lo(hb.x), dmb = f16_hi(hb.x);
+        const float dma = f16_hi(ha.x), dmb = f16_hi(hb.x);
 #pragma unroll
         for (int c = 0; c < 4; c++) {
             const uint32_t off = 16u + 32u * c + 4u * static_cast<uint32_t>(t);
@@ -177,22 +177,26 @@ struct Q4KT {
 #pragma unroll
             for (int h = 0; h < 2; h++) {
                 const int j = 2 * c + h;
-                // The 4-bit codes as f16 subnormals q * 2^-24, exact: nibble
-                // 4h of bytes 0 and 2 (even columns) or 1 and 3 (odd) moved
-                // into the low bits of each half by one shift and one mask.
-                const int se = 4 * h, so = 8 + 4 * h;
+                // The 4-bit codes as f16 subnormals, exact: the low nibbles
+                // (h = 0) as q * 2^-24, the high nibbles (h = 1) left in place
+                // as 16 q * 2^-24; bytes 0 and 2 (even columns) by one mask,
+                // bytes 1 and 3 (odd) by a shift and a mask.
+                const uint32_t me = h ? 0x00f000f0u : 0x000f000fu;
                 float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_half_a(D, (wa0 >> se) & 0x000f000fu, (wb0 >> se) & 0x000f000fu, (wa0 >> so) & 0x000f000fu,
-                           (wb0 >> so) & 0x000f000fu, xh[j][0], xh[j][1], xl[j][0], xl[j][1]);
-                mma_half_a(D, (wa1 >> se) & 0x000f000fu, (wb1 >> se) & 0x000f000fu, (wa1 >> so) & 0x000f000fu,
-                           (wb1 >> so) & 0x000f000fu, xh[j][2], xh[j][3], xl[j][2], xl[j][3]);
+                mma_half_a(D, wa0 & me, wb0 & me, (wa0 >> 8) & me, (wb0 >> 8) & me, xh[j][0], xh[j][1], xl[j][0],
+                           xl[j][1]);
+                mma_half_a(D, wa1 & me, wb1 & me, (wa1 >> 8) & me, (wb1 >> 8) & me, xh[j][2], xh[j][3], xl[j][2],
+                           xl[j][3]);
+                // d * sc_j scaled by 2^24 (2^20 for the high nibbles), exactly
+                const float da = f16_lo(ha.x) * (h ? TWO24 / 16.0f : TWO24);
+                const float db = f16_lo(hb.x) * (h ? TWO24 / 16.0f : TWO24);
                 const uint32_t sel = 0x7440u | static_cast<uint32_t>(j & 3);
                 const float dsa = __fmaf_rn(da, __uint_as_float(prmt(j < 4 ? sa_lo : sa_hi, 0x4B000000u, sel)), -da * TWO23);
                 const float dna = __fmaf_rn(dma, __uint_as_float(prmt(j < 4 ? ma_lo : ma_hi, 0x4B000000u, sel)), -dma * TWO23);
                 const float dsb = __fmaf_rn(db, __uint_as_float(prmt(j < 4 ? sb_lo : sb_hi, 0x4B000000u, sel)), -db * TWO23);
                 const float dnb = __fmaf_rn(dmb, __uint_as_float(prmt(j < 4 ? mb_lo : mb_hi, 0x4B000000u, sel)), -dmb * TWO23);
                 const float4 s = lds_f4(st + 64u * j);
-                fold(y4, D, dsa * TWO24, dsb * TWO24, s.x, s.z);   // D is in units of 2^-24
+                fold(y4, D, dsa, dsb, s.x, s.z);
                 y4[0] = __fmaf_rn(-dna, s.y, y4[0]);
                 y4[1] = __fmaf_rn(-dna, s.w, y4[1]);
                 y4[2] = __fmaf_rn(-dnb, s.y, y4[2]);
