@@ -229,16 +229,11 @@ __global__ void __launch_bounds__(512, 1) qmm_stream_kernel(const KParams p) {
 template <class F, int M, bool WIDE>
 inline int launch_qmm_one(const KParams& kp, const Plan& pl, cudaStream_t stream) {
     auto kern = qmm_stream_kernel<F, M, WIDE>;
-    static int configured[MAX_DEVICES] = {};
+    static SmemOptIn opted;
     int dev = 0;
     DevInfo di;
     if (dev_info(&di, &dev)) return QMV_ECUDA;
-    if (static_cast<int>(pl.smem) > configured[dev]) {
-        int rc = cuda_rc(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              static_cast<int>(pl.smem)));
-        if (rc) return rc;
-        configured[dev] = static_cast<int>(pl.smem);
-    }
+    if (const int rc = ensure_smem(kern, opted, dev, static_cast<int>(pl.smem))) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(pl.parts, 1, 1);
     lc.blockDim = dim3(pl.T, 1, 1);

@@ -594,16 +594,11 @@ inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv
 template <class F>
 inline int launch_tc(const TParams& tp, const Plan& pl, cudaStream_t stream) {
     auto kern = qmm_tc_kernel<F>;
-    static int configured[MAX_DEVICES] = {};
+    static SmemOptIn opted;
     int dev = 0;
     DevInfo di;
     if (dev_info(&di, &dev)) return QMV_ECUDA;
-    if (static_cast<int>(pl.smem) > configured[dev]) {
-        int rc = cuda_rc(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              static_cast<int>(pl.smem)));
-        if (rc) return rc;
-        configured[dev] = static_cast<int>(pl.smem);
-    }
+    if (const int rc = ensure_smem(kern, opted, dev, static_cast<int>(pl.smem))) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(pl.parts, 1, 1);
     lc.blockDim = dim3(pl.T, 1, 1);

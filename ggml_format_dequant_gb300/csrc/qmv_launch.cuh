@@ -4,7 +4,9 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "../../include/qmv.h"
@@ -47,8 +49,12 @@ struct DevInfo {
     int smem_reserved = 0;
 };
 
+// The current device's properties, queried once per device (under a lock, so
+// that host threads calling concurrently see a complete record).
 inline int dev_info(DevInfo* out, int* dev_out) {
     static DevInfo cache[MAX_DEVICES];
+    static std::atomic<int> ready[MAX_DEVICES];
+    static std::mutex mu;
     int dev = 0;
     const cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -56,17 +62,41 @@ inline int dev_info(DevInfo* out, int* dev_out) {
         return QMV_ECUDA;
     }
     if (dev < 0 || dev >= MAX_DEVICES) return QMV_ECUDA;
-    if (cache[dev].nsm == 0) {
-        DevInfo d;
-        if (cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-            return QMV_ECUDA;
-        cache[dev] = d;
+    if (!ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> g(mu);
+        if (!ready[dev].load(std::memory_order_relaxed)) {
+            DevInfo d;
+            if (cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+                return QMV_ECUDA;
+            cache[dev] = d;
+            ready[dev].store(1, std::memory_order_release);
+        }
     }
     *out = cache[dev];
     if (dev_out) *dev_out = dev;
+    return QMV_OK;
+}
+
+// Dynamic shared memory above 48 KB must be opted into per kernel and device.
+// The opted-in size only grows; it is raised under a lock so that concurrent
+// first launches from several host threads cannot leave it below a size that
+// one of them launches with.
+struct SmemOptIn {
+    std::atomic<int> bytes[MAX_DEVICES];
+    std::mutex mu;
+};
+
+template <class K>
+inline int ensure_smem(K kern, SmemOptIn& st, int dev, int smem) {
+    if (smem <= st.bytes[dev].load(std::memory_order_acquire)) return QMV_OK;
+    std::lock_guard<std::mutex> g(st.mu);
+    if (smem <= st.bytes[dev].load(std::memory_order_relaxed)) return QMV_OK;
+    const int rc = cuda_rc(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    if (rc) return rc;
+    st.bytes[dev].store(smem, std::memory_order_release);
     return QMV_OK;
 }
 
@@ -334,18 +364,11 @@ inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp
 template <class F, int R, bool MOE, int MODE, bool WIDE>
 inline int launch_one(const KParams& kp, const Plan& pl, int slots, cudaStream_t stream) {
     auto kern = qmv_stream_kernel<F, R, MOE, MODE, WIDE>;
-    // Dynamic shared memory above 48 KB must be opted into per kernel; the
-    // attribute only ever grows, once per size class and device.
-    static int configured[MAX_DEVICES] = {};
+    static SmemOptIn opted;
     int dev = 0;
     DevInfo di;
     if (dev_info(&di, &dev)) return QMV_ECUDA;
-    if (static_cast<int>(pl.smem) > configured[dev]) {
-        int rc = cuda_rc(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              static_cast<int>(pl.smem)));
-        if (rc) return rc;
-        configured[dev] = static_cast<int>(pl.smem);
-    }
+    if (const int rc = ensure_smem(kern, opted, dev, static_cast<int>(pl.smem))) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(pl.parts, MOE ? slots : 1, 1);
     lc.blockDim = dim3(pl.T, 1, 1);
