@@ -1,0 +1,77 @@
+"""Seeded random shapes and launch configurations for every matvec family,
+against the oracle: rows, k and the forced plan (CTAs, rows per slot, ring
+depth, unroll, warps) drawn from a fixed stream, so the same cases run every
+time."""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+SCALE_REL_TOL = 1e-4
+FAMILIES = ["q4k", "q6k", "q8_0", "q5k", "q4_0", "q8d", "q4d", "q6d"]
+QK = {"q4k": 256, "q6k": 256, "q8_0": 32, "q5k": 256, "q4_0": 32, "q8d": 32, "q4d": 256, "q6d": 256}
+FMT = {"q8d": "q8_0", "q4d": "q4k", "q6d": "q6k"}
+
+
+def cases(n=6):
+    out = []
+    z = synth.Stream(4242).draw(len(FAMILIES) * n * 8).reshape(len(FAMILIES), n, 8)
+    for fi, fam in enumerate(FAMILIES):
+        for ci in range(n):
+            d = [int(v >> np.uint64(33)) for v in z[fi, ci]]
+            nb_max = 8192 // QK[fam]
+            nb = 1 + d[0] % nb_max
+            rows = 1 + d[1] % 200
+            cfg = None
+            if d[2] % 2:
+                cfg = dict(ctas=1 + d[3] % 9, chunk_rows=d[4] % 6, chunks=d[5] % 4, unroll=d[6] % 3,
+                           warps=[0, 4, 8, 16][d[7] % 4])
+            out.append((fam, rows, nb * QK[fam], cfg))
+    return out
+
+
+@pytest.fixture(scope="module")
+def q():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    import ggml_format_dequant_gb300 as lib
+    return lib
+
+
+@pytest.mark.parametrize("fam,rows,k,cfg", cases())
+def test_random_shape(q, fam, rows, k, cfg):
+    fmt = FMT.get(fam, fam)
+    st = synth.Stream(rows * 131 + k)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, k)
+    wd = torch.from_numpy(w).cuda()
+    y = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+    if fam in FMT:
+        xq = torch.empty(k, dtype=torch.int8, device="cuda")
+        xs = torch.empty(k // 32, dtype=torch.float32, device="cuda")
+        q.quantize_act_q8(torch.from_numpy(x).cuda(), xq, xs, None, 1, k)
+        oq, os_, _ = oracle.quantize_act_q8(x, 1, k)
+        entry = {"q8d": q.qmv_q8_dp4a, "q4d": q.qmv_q4k_dp4a, "q6d": q.qmv_q6k_dp4a}[fam]
+        rc = entry(wd, xq, xs, y, rows, k, cfg=cfg, check=False)
+        ref = {"q8d": oracle.qmv_q8_dp4a, "q4d": oracle.qmv_q4k_dp4a, "q6d": oracle.qmv_q6k_dp4a}[fam](
+            w, oq.reshape(-1), os_.reshape(-1), rows, k)
+    else:
+        rc = getattr(q, f"qmv_{fam}")(wd, torch.from_numpy(x).cuda(), y, rows, k, cfg=cfg, check=False)
+        ref = oracle.qmv(fam, w, x, rows, k)
+    if rc == q.QMV_ETOOBIG:
+        # a forced plan that cannot hold the rows it was given: refused on the
+        # host, nothing launched
+        assert cfg is not None
+        return
+    assert rc == q.QMV_OK, q.strerror(rc)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    assert not np.any(np.isnan(got))
+    assert float(np.max(np.abs(ref - got)) / max(np.max(np.abs(ref)), 1e-30)) <= SCALE_REL_TOL

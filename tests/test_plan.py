@@ -386,3 +386,18 @@ def test_tc_forced_plans(q, fmt, cfg):
 def test_tc_planner_rejects_long_rows(q):
     with pytest.raises(q.QmvError):
         q.qmm_tc_plan_detail(0, 64, 4352, 4, None, DEVICE)
+
+
+def _random_cases():
+    from test_gpu_random_shapes import cases
+    return cases()
+
+
+@pytest.mark.parametrize("fam,rows,k,cfg", _random_cases())
+def test_random_shape_plans(q, fam, rows, k, cfg):
+    """The seeded random shapes and forced plans of the GPU test, replayed on
+    the host before they run (a plan the host refuses is never launched)."""
+    try:
+        replay(q, fam, rows, k, 1, cfg)
+    except q.QmvError as e:
+        assert cfg is not None and e.code == q.QMV_ETOOBIG
