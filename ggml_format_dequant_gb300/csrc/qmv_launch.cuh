@@ -319,13 +319,12 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
 }
 
 // Launch plan of format F. Independent calls (mode 2 of
-// qmv_set_weight_prefetch) overlap best when one call takes about two thirds
-// of the SMs (at most a third of the two CTA slots of every SM, where the
-// share allows), with CTAs that still hold their whole share in half an SM:
-// more calls are then in flight at once (measured on GB300: MoE Q4_K E128 n768
-// k2048 with 8 slots 2.32 -> 1.76 us a call, Q4_K 4096 x 4096 2.43 -> 2.26 us,
-// Q4_K dp4a 4096 x 4096 2.25 -> 1.82 us). Chained and plain calls, and shapes
-// whose share does not fit, use every SM.
+// qmv_set_weight_prefetch) overlap best when one call takes as few CTAs as
+// still hold their whole share in half an SM (but at least half the SMs'
+// worth): more calls are then in flight at once (measured on GB300: MoE Q4_K
+// E128 n768 k2048 with 8 slots 2.32 -> 1.59 us a call, Q4_K 4096 x 4096
+// 2.43 -> 2.18 us, Q4_K dp4a 4096 x 4096 2.25 -> ~1.76 us). Chained and plain
+// calls, and shapes whose share does not fit, use every SM.
 template <class F>
 inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
     const int rc = make_plan_core<F>(di, rows, k, slots, cfg, kp, pl);
@@ -333,8 +332,9 @@ inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qm
     if (rc || mode != 2 || (cfg && cfg->ctas > 0)) return rc;
     const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;
     const int per = slots > 1 ? slots : 1;
-    // floor(2 nsm / 3 / slots): with two CTAs an SM, three calls in flight
-    const int start = std::max(1, (2 * di.nsm) / (3 * per));
+    // From half the SMs up (with two CTAs an SM, four calls in flight), the
+    // fewest CTAs whose whole share fits in half an SM.
+    const int start = std::max(1, di.nsm / (2 * per));
     if (start >= pl->parts) return rc;   // small shapes: already fewer CTAs
     qmv_cfg c = cfg ? *cfg : qmv_cfg{0, 0, 0, 0, 0, 0};
     for (int parts = start; parts < pl->parts; parts++) {
