@@ -98,6 +98,7 @@ _SIG = {
     "moe_qmv_q5k_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "qmv_q8_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_device_status": [_P, _I],
+    "qmv_selftest_wait_timeout": [ctypes.c_ulonglong, _P],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "qmv_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
     "qmv_set_weight_prefetch": [_I],
@@ -337,6 +338,10 @@ def qmv_dequant_q4_0(w, out, rows, k, stream=None, check=True):
 
 def qmv_q8_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):
     return _call("qmv_q8_dp4a_blockdots", _ptr(w), _ptr(xq), _ptr(dots), rows, k, _stream(stream), check=check)
+
+
+def qmv_selftest_wait_timeout(limit_ns, stream=None, check=True):
+    return _call("qmv_selftest_wait_timeout", int(limit_ns), _stream(stream), check=check)
 
 
 def qmv_device_status(clear=True) -> int:

@@ -333,6 +333,11 @@ int qmv_set_weight_prefetch(int mode) {
     return old;
 }
 
+int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {
+    if (limit_ns == 0 || limit_ns > 100000000ull) return QMV_EINVAL;
+    return qmvi::selftest_wait_timeout(limit_ns, stream);
+}
+
 const char* qmv_last_cuda_error(void) {
     return cudaGetErrorString(qmv::last_cuda_error());
 }

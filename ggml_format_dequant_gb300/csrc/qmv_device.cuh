@@ -87,16 +87,21 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of the barrier to complete, giving up after
-// WAIT_LIMIT_NS. Returns false on timeout. A phase that is already complete
-// (the usual case when the data was requested long before) costs one test.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// limit_ns. Returns false on timeout. A phase that is already complete (the
+// usual case when the data was requested long before) costs one test.
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_test_wait(bar, parity)) return true;
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The same with the kernels' limit, WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    return mbar_wait_bounded_ns(bar, parity, WAIT_LIMIT_NS);
 }
 
 // Programmatic dependent launch. launch_dependents lets the next kernel on the

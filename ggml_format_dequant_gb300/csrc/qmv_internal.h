@@ -56,6 +56,7 @@ int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows
 int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s);
 int quantize_act(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t s);
 int dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t s);
+int selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t s);
 int status_q8(unsigned int* out, int clear);
 
 // qmm_q4k.cu, qmm_q6k.cu, qmm_q8_0.cu: the small-M batched product (m >= 2)

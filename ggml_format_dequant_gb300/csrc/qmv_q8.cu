@@ -45,6 +45,18 @@ __global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ w, float* __rest
     }
 }
 
+// Failure-path self-test: one thread waits, with the kernels' bounded wait,
+// on a shared-memory barrier that nothing ever arrives on; when the limit runs
+// out it raises STATUS_WAIT_TIMEOUT, exactly as a matvec whose staged copy
+// never landed would, and the kernel returns.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar_storage;
+    const uint32_t bar = smem_u32(&bar_storage);
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded_ns(bar, 0u, limit_ns)) atomicOr(&g_status, STATUS_WAIT_TIMEOUT);
+}
+
 KParams q8_params(const void* w, int rows, int k) {
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(w);
@@ -123,6 +135,11 @@ int quantize_act(const float* x, int8_t* xq, float* xs, float* xsum, int m, int 
 int dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t s) {
     const long long nblk = static_cast<long long>(rows) * (k / 32);
     dequant_q8_0_kernel<<<grid_for(nblk, 256), 256, 0, s>>>(static_cast<const uint8_t*>(w), out, nblk);
+    return cuda_rc(cudaGetLastError());
+}
+
+int selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 1, 0, s>>>(limit_ns);
     return cuda_rc(cudaGetLastError());
 }
 

@@ -226,6 +226,13 @@ const char *qmv_last_cuda_error(void);
 #define QMV_STATUS_BAD_EXPERT_ID 1u /* an MoE id was outside [0, n_experts) */
 #define QMV_STATUS_WAIT_TIMEOUT 2u  /* a staged weight copy did not land in time */
 
+/* Failure-path self-test: launches one thread that waits, through the same
+ * bounded wait every staged copy goes through, on a barrier nothing arrives
+ * on, for limit_ns (1 ns .. 100 ms); when the limit runs out it raises
+ * QMV_STATUS_WAIT_TIMEOUT and returns, as a matvec whose copy never landed
+ * would. Nothing hangs or traps; the context stays usable. */
+int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
+
 /* OR of the status bits raised on the current device since the last clear;
  * clears them when `clear` is non-zero. Synchronizes with the device (it reads
  * device memory through the legacy stream). */

@@ -66,6 +66,8 @@ def test_host_side_validation_without_gpu(lib):
     assert lib.moe_qmv_q4k(A, A, A, 4, 256, A + 2, 2, 8, stream=S, check=False) == lib.QMV_EALIGN
     assert lib.qmv_dequant_q4k(A, A, 4, 100, stream=S, check=False) == lib.QMV_EINVAL
     assert lib.qmv_q8_dp4a_blockdots(A, A + 1, A, 4, 32, stream=S, check=False) == lib.QMV_EALIGN
+    assert lib.qmv_selftest_wait_timeout(0, stream=S, check=False) == lib.QMV_EINVAL
+    assert lib.qmv_selftest_wait_timeout(200_000_000, stream=S, check=False) == lib.QMV_EINVAL
     with pytest.raises(lib.QmvError):
         lib.qmv_q4k(A, A, A, 4, 300, stream=S)
 
