@@ -210,11 +210,12 @@ def qmm_launches(fmt, k, m) -> int:
     """Kernel launches one qmm_<fmt> call makes: the matvec for m = 1; for
     m = 2 the register kernel, ceil(m / tile) launches with the widest tile
     (2 or 1 rows of x) whose units per row fit a CTA; from m = 3 on the
-    tensor-core kernel, ceil(m / 8) tiles times ceil(k / 4096) k-chunks."""
+    tensor-core kernel, one launch per tile of up to 8 rows of x (ceil(m / 8)),
+    whatever k."""
     if m == 1:
         return 1
     if m >= 3:
-        return -(-m // 8) * -(-k // 4096)
+        return -(-m // 8)
     qk, units = (32, 1) if fmt == "q8_0" else (256, 8)
     return 1 if (k // qk) * units <= 512 else 2
 
@@ -382,8 +383,8 @@ def qmv_plan_detail(fmt, rows, k, slots=1, cfg=None, device=GB300_DEVICE) -> dic
     return dict(zip(PLAN_DETAIL_FIELDS, list(out)))
 
 
-QMM_TC_PLAN_FIELDS = ("threads", "ctas", "smem", "KS", "CR", "S", "rowbytes", "stride", "slot_stride", "rq", "rrem",
-                      "ngroups", "off_st", "off_red", "off_ring", "off_bars", "off_cnt")
+QMM_TC_PLAN_FIELDS = ("threads", "ctas", "smem", "KS", "CR", "S", "chunk_bytes", "stride", "slot_stride", "rq",
+                      "rrem", "ngroups", "nchunks", "off_red", "off_sums", "off_ring", "off_bars", "off_cnt")
 
 
 def qmm_tc_plan_detail(fmt, rows, k, m, cfg=None, device=GB300_DEVICE) -> dict:

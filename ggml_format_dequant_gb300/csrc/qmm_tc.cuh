@@ -1,6 +1,7 @@
 // qmm_tc.cuh -- the small-M batched product y[m, rows] = x[m, k] W^T on the
-// tensor cores (warp-level mma.sync m16n8k16, f16 operands, f32 accumulate);
-// one launch covers rows of up to 4096 weights, longer rows go in k-chunks.
+// tensor cores (warp-level mma.sync, f16 operands, f32 accumulate), one launch
+// per tile of up to 8 rows of x; rows of any length, in k-chunks inside the
+// launch.
 //
 // The product is a skinny dense contraction (m <= 8 columns), so a warp-level
 // MMA with register accumulators fits it: the weights' per-32 (Q4_K, Q8_0) or
@@ -8,27 +9,34 @@
 // registers right after its MMAs, which keeps every operand exact:
 //  * A (16 weight rows x 16 k): the integer codes, exact in f16: Q4_K's q as
 //    the subnormal q * 2^-24 or 16 q * 2^-24 (one mask, or a shift and a
-//    mask, per pair; the power of two goes into the row scale), Q6_K's q - 32 and Q8_0's q made from the code bytes with
-//    one byte permute into the f16 pattern of 1024 + v and one f16x2
-//    subtraction.
+//    mask, per pair; the power of two goes into the row scale), Q6_K's q - 32
+//    and Q8_0's q made from the code bytes with one byte permute into the f16
+//    pattern of 1024 + v and one f16x2 subtraction.
 //  * B (16 k x 8 rows of x): x in two f16 parts, hi + lo, after a power-of-two
-//    scale per 32-group and row of x that puts the group maximum in
-//    [2^14, 2^15); hi + lo carries x to about 22 bits, so the MMA pair
-//    A*hi + A*lo is the group's integer-code dot at f32 accuracy.
+//    scale per row of x and warp slice (256 weights) that puts the slice's
+//    maximum in [2^14, 2^15); hi + lo carries x to about 22 bits, so the MMA
+//    pair A*hi + A*lo is the group's integer-code dot at f32 accuracy, and
+//    the scale comes off once per tile when the slice's sums are parked.
 //  * Per group the accumulator D (16 x 8, four values a lane) is folded into
-//    the row sums: y += (d*sc * 2^-s) * D  (- dmin*m * sum(x) for Q4_K).
+//    the row sums: y += d*sc * D. Q4_K's min term, dmin * sum_j m_j S_j with
+//    S_j the sum of x over group j, is one more product per tile: A' = the
+//    six-bit m_j of the 16 rows, B' = a lane's partial sums of the groups
+//    (hi + lo), over a k made of (group, lane) pairs, so that no lane needs
+//    another lane's sums.
 // The k order inside each 16-column half of a group is permuted identically
 // for A and B so that a lane's code bytes are aligned 4-byte runs: MMA
 // columns (2t, 2t+1, 2t+8, 2t+9) of lane group t hold positions (4t, 4t+2,
 // 4t+1, 4t+3) of the half.
 //
-// Staging: a CTA owns a run of rows; every row of a piece is copied by its own
-// bulk TMA copy into a slot whose row stride is 16 bytes past a multiple of
-// 128, so that the 32 lanes of a warp, reading 8 rows x 4 runs, hit 32
-// different banks. Warps split k into slices of 8 groups (256 weights); each
-// keeps its slice's x fragments (hi and lo, 64 registers) for the whole call.
-// Rows are processed in tiles of 16; slice partials are parked per (row,
-// slice, column) and summed in slice order at the end. Waits are bounded as in
+// Staging: a CTA owns a run of rows; the pieces it streams are (k-chunk, rows)
+// pairs, k-chunk major; every row of a piece is copied by its own bulk TMA
+// copy into a slot whose row stride is 16 bytes past a multiple of 128, so
+// that the 32 lanes of a warp, reading 8 rows x 4 runs, hit 32 different
+// banks. A k-chunk is one slice of 8 groups (256 weights) per warp; a warp
+// converts its slice of x when it enters a chunk and keeps the fragments (hi
+// and lo, 64 registers) for the chunk's pieces. Rows are processed in tiles of
+// 16; slice partials are parked per (row, slice, column), added over the
+// chunks, and summed in slice order at the end. Waits are bounded as in
 // qmv_kernel.cuh.
 #pragma once
 
@@ -37,25 +45,23 @@
 namespace qmv {
 
 struct TParams {
-    const uint8_t* w;             // packed rows [rows, K / QK blocks], K the full row length
-    const float* x;               // x[i, 0] of this launch's k-chunk (row stride xstride)
+    const uint8_t* w;             // packed rows [rows, k / QK blocks]
+    const float* x;               // [m, k], row-major
     float* y;                     // [m, rows]
     unsigned long long wbytes;    // readable bytes from w (tail clipping)
-    int rows, k, m;               // k: the chunk's weights per row; m: rows of x, 1..8
-    int xstride;                  // floats between rows of x (the full row length)
+    int rows, k, m;               // m: rows of x, 1..8
     uint32_t wpitch;              // bytes between rows of W
-    uint32_t woff;                // byte offset of the chunk inside a row
-    int accumulate;               // add to y (a later k-chunk) instead of writing it
     int ngroups;                  // k / 32
-    uint32_t rowbytes;            // bytes of one row's chunk
+    int KS;                       // warps; a k-chunk is KS slices of 8 groups
+    int nchunks;                  // k-chunks (the last one may hold fewer slices)
+    uint32_t chunk_bytes;         // bytes of one row's full k-chunk
     uint32_t stride;              // shared-memory row stride (16 mod 128)
-    int KS;                       // warps, one per slice of 8 groups
     int CR;                       // rows per piece
     int S;                        // ring slots
     int rq, rrem;                 // rows per CTA: rq or rq + 1 (the first rrem CTAs)
     int early_inputs;
     uint32_t slot_stride;         // bytes per slot (rows rounded up to 16)
-    uint32_t off_st, off_red, off_ring, off_bars, off_cnt;
+    uint32_t off_red, off_sums, off_ring, off_bars, off_cnt;
 };
 
 constexpr int TC_GROUPS_PER_SLICE = 8;   // 32-weight groups per warp slice
@@ -79,6 +85,7 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     return d;
 }
 
+
 // Bytes 0 and 2 (even) or 1 and 3 (odd) of w, each v <= 1023, as the f16
 // pair (v - off), bias being the f16x2 pattern of 1024 + off.
 __device__ __forceinline__ uint32_t f16_even(uint32_t w, uint32_t bias) {
@@ -97,55 +104,150 @@ __device__ __forceinline__ float2 unpack_h2(uint32_t v) {
     return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // 4 bytes at the 2-byte aligned shared address a.
 __device__ __forceinline__ uint32_t lds32_a2(uint32_t a) {
     const uint32_t wa = a & ~3u;
     return __funnelshift_r(lds32<0>(wa), lds32<4>(wa), (a & 3u) * 8u);
 }
 
-// Four floats at the 16-byte aligned shared address a.
-__device__ __forceinline__ float4 lds_f4(uint32_t a) {
-    const uint4 v = lds128<0>(a);
-    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+// MMA of one 16-column half with A given directly (rows g, g+8; even, odd
+// columns) against hi and lo; packed (P): the lane's one fragment already
+// holds hi (columns 0-3) or lo (columns 4-7), one MMA.
+template <bool P>
+__device__ __forceinline__ void mma_half_a(float (&D)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+    mma16816(D, a0, a1, a2, a3, bh0, bh1);
+    if (!P) mma16816(D, a0, a1, a2, a3, bl0, bl1);
 }
 
-// MMA of one 16-column half (A from the code words of rows g and g+8, already
-// shifted/masked to one byte per weight, with the f16 bias) against hi and lo.
+// The same with A from the code words of rows g and g+8, already shifted /
+// masked to one byte per weight, with the f16 bias.
+template <bool P>
 __device__ __forceinline__ void mma_half(float (&D)[4], uint32_t ka, uint32_t kb, uint32_t bias, uint32_t bh0,
                                          uint32_t bh1, uint32_t bl0, uint32_t bl1) {
     const uint32_t a0 = f16_even(ka, bias), a1 = f16_even(kb, bias);
     const uint32_t a2 = f16_odd(ka, bias), a3 = f16_odd(kb, bias);
-    mma16816(D, a0, a1, a2, a3, bh0, bh1);
-    mma16816(D, a0, a1, a2, a3, bl0, bl1);
-}
-
-// MMA of one 16-column half with A given directly (rows g, g+8; even, odd
-// columns) against hi and lo.
-__device__ __forceinline__ void mma_half_a(float (&D)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                           uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
-    mma16816(D, a0, a1, a2, a3, bh0, bh1);
-    mma16816(D, a0, a1, a2, a3, bl0, bl1);
+    mma_half_a<P>(D, a0, a1, a2, a3, bh0, bh1, bl0, bl1);
 }
 
 constexpr float TWO24 = 16777216.0f;
 
-// y4 += scale_row * inv_col * D (columns 2t, 2t+1 for rows g, g+8).
-__device__ __forceinline__ void fold(float (&y4)[4], const float (&D)[4], float sa, float sb, float inv0, float inv1) {
-    y4[0] = __fmaf_rn(sa * inv0, D[0], y4[0]);
-    y4[1] = __fmaf_rn(sa * inv1, D[1], y4[1]);
-    y4[2] = __fmaf_rn(sb * inv0, D[2], y4[2]);
-    y4[3] = __fmaf_rn(sb * inv1, D[3], y4[3]);
+// y4 += scale_row * D (columns 2t, 2t+1 for rows g, g+8).
+__device__ __forceinline__ void fold(float (&y4)[4], const float (&D)[4], float sa, float sb) {
+    y4[0] = __fmaf_rn(sa, D[0], y4[0]);
+    y4[1] = __fmaf_rn(sa, D[1], y4[1]);
+    y4[2] = __fmaf_rn(sb, D[2], y4[2]);
+    y4[3] = __fmaf_rn(sb, D[3], y4[3]);
+}
+
+// A lane's B fragments for its warp's slice (column g of the MMA, scaled): h /
+// l = hi / lo parts, [group][4] = MMA0 b0, b1, MMA1 b0, b1. Packed (m <= 4
+// rows of x): MMA column g < 4 is hi of row g of x and column g >= 4 lo of row
+// g - 4, all in h; l is unused. sh (Q4_K, packed): the lane's partial sums of
+// groups (0, 1), (2, 3), (4, 5), (6, 7) over its eight positions each, times
+// 1/8, as f16 pairs (hi or lo as h); unpacked, the same pairs (hi, then lo)
+// go to the lane's 32 bytes of shared memory instead, to spare registers.
+struct XFrag {
+    uint32_t h[8][4], l[8][4];
+    uint32_t sh[4];
+};
+
+// The lane's fragments of one slice: its row of x (zeros when !live), groups
+// 0 .. ng - 1 starting at src = &x[row, 32 G + 4t]; inv receives 2^-s, s the
+// power of two that puts the slice's maximum (over the four lanes of the row)
+// in [2^14, 2^15). sums: the lane's 32 bytes of shared memory (Q4_K unpacked).
+template <bool SUMS, bool P>
+__device__ __forceinline__ void tc_load_x(const float* src, bool live, int ng, bool lo_lane, uint32_t sums, XFrag& xf,
+                                          float& inv) {
+    // all 64 values first (one round of loads), then the slice maximum
+    float4 u[2 * TC_GROUPS_PER_SLICE];
+#pragma unroll
+    for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
+        u[2 * j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        u[2 * j + 1] = u[2 * j];
+        if (live && j < ng) {
+            u[2 * j] = __ldg(reinterpret_cast<const float4*>(src + 32 * j));
+            u[2 * j + 1] = __ldg(reinterpret_cast<const float4*>(src + 32 * j + 16));
+        }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 2 * TC_GROUPS_PER_SLICE; i++)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(u[i].x), fabsf(u[i].y)), fmaxf(fabsf(u[i].z), fabsf(u[i].w))));
+    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+    int s = 0;
+    if (amax > 0.0f) {
+        s = 141 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
+        s = s > 126 ? 126 : s;
+    }
+    const float p2 = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
+    inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+    const float neg = lo_lane ? -1.0f : 0.0f;
+    if (SUMS) {
+        // group sums of the lane's eight values (scaled: the power of two
+        // commutes with the rounding), before the conversion frees u
+        float ps[TC_GROUPS_PER_SLICE];
+#pragma unroll
+        for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
+            const float4 a = u[2 * j], b = u[2 * j + 1];
+            ps[j] = (((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w))) * p2;
+        }
+        uint32_t sl[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float a = ps[2 * i] * 0.125f, b = ps[2 * i + 1] * 0.125f;
+            const uint32_t hs = pack_h2(a, b);
+            const float2 f = unpack_h2(hs);
+            if (P) {
+                xf.sh[i] = pack_h2(__fmaf_rn(f.x, neg, a), __fmaf_rn(f.y, neg, b));
+            } else {
+                xf.sh[i] = hs;
+                sl[i] = pack_h2(a - f.x, b - f.y);
+            }
+        }
+        if (!P) {
+            sts128(sums, make_uint4(xf.sh[0], xf.sh[1], xf.sh[2], xf.sh[3]));
+            sts128(sums + 16u, make_uint4(sl[0], sl[1], sl[2], sl[3]));
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
+        const float v[8] = {u[2 * j].x * p2,     u[2 * j].y * p2,     u[2 * j].z * p2,     u[2 * j].w * p2,
+                            u[2 * j + 1].x * p2, u[2 * j + 1].y * p2, u[2 * j + 1].z * p2, u[2 * j + 1].w * p2};
+        // MMA-k order of a half: (4t, 4t+2) then (4t+1, 4t+3)
+        const uint32_t h0 = pack_h2(v[0], v[2]), h1 = pack_h2(v[1], v[3]);
+        const uint32_t h2 = pack_h2(v[4], v[6]), h3 = pack_h2(v[5], v[7]);
+        const float2 f0 = unpack_h2(h0), f1 = unpack_h2(h1), f2 = unpack_h2(h2), f3 = unpack_h2(h3);
+        if (P) {
+            // hi lanes keep v (its pack is hi again), lo lanes v - hi
+            xf.h[j][0] = pack_h2(__fmaf_rn(f0.x, neg, v[0]), __fmaf_rn(f0.y, neg, v[2]));
+            xf.h[j][1] = pack_h2(__fmaf_rn(f1.x, neg, v[1]), __fmaf_rn(f1.y, neg, v[3]));
+            xf.h[j][2] = pack_h2(__fmaf_rn(f2.x, neg, v[4]), __fmaf_rn(f2.y, neg, v[6]));
+            xf.h[j][3] = pack_h2(__fmaf_rn(f3.x, neg, v[5]), __fmaf_rn(f3.y, neg, v[7]));
+        } else {
+            xf.h[j][0] = h0; xf.h[j][1] = h1; xf.h[j][2] = h2; xf.h[j][3] = h3;
+            xf.l[j][0] = pack_h2(v[0] - f0.x, v[2] - f0.y);
+            xf.l[j][1] = pack_h2(v[1] - f1.x, v[3] - f1.y);
+            xf.l[j][2] = pack_h2(v[4] - f2.x, v[6] - f2.y);
+            xf.l[j][3] = pack_h2(v[5] - f3.x, v[7] - f3.y);
+        }
+    }
 }
 
 // ------------------------------------------------------- format bodies
 //
 // slice(): one 16-row tile against the warp's slice of groups. ra / rb:
-// shared addresses of rows g and g + 8 of the tile (their first byte);
-// xh / xl: the lane's B fragments (hi, lo) of the slice's groups, [group][4]
-// = MMA0 b0, b1, MMA1 b0, b1; st: shared address of the statistics
-// (2^-s, sum x) of columns 2t, 2t + 1 of the slice's group 0 (64 bytes per
-// group further); y4: the row sums of (g, 2t), (g, 2t + 1), (g + 8, 2t),
-// (g + 8, 2t + 1).
+// shared addresses of rows g and g + 8 of the tile (the first byte of their
+// k-chunk); ks: the slice within the chunk; ng: its groups (Q8_0's last slice
+// may hold fewer than 8); xf: the lane's fragments; sums (Q4_K unpacked): the
+// shared address of the lane's min-term fragments; y4: the row sums of (g,
+// 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1) in the slice's scaled units.
 
 // Q4_K: a slice is one 144-byte block; group j = sub-block j. The code bytes
 // of a lane's positions in chunk c (sub-blocks 2c, 2c+1) are qs[32c + 4t ..]
@@ -154,21 +256,52 @@ struct Q4KT {
     static constexpr int QK = 256;
     static constexpr int BLOCK_BYTES = 144;
     static constexpr int SLACK = 0;
+    static constexpr bool SUMS = true;
 
-    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int, int t,
-                                                 const uint32_t (&xh)[8][4], const uint32_t (&xl)[8][4],
-                                                 uint32_t st, float (&y4)[4]) {
+    template <bool P>
+    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int, int t, const XFrag& xf,
+                                                 uint32_t sums, float (&y4)[4]) {
         const uint32_t ba = ra + static_cast<uint32_t>(ks) * BLOCK_BYTES;
         const uint32_t bb = rb + static_cast<uint32_t>(ks) * BLOCK_BYTES;
         const uint4 ha = lds128<0>(ba);
         const uint4 hb = lds128<0>(bb);
+        // six-bit scales (sc) and mins (m) of sub-blocks 0-3 (lo) and 4-7 (hi)
         const uint32_t sa_lo = ha.y & 0x3f3f3f3fu, ma_lo = ha.z & 0x3f3f3f3fu;
         const uint32_t sa_hi = (ha.w & 0x0f0f0f0fu) | ((ha.y >> 2) & 0x30303030u);
         const uint32_t ma_hi = ((ha.w >> 4) & 0x0f0f0f0fu) | ((ha.z >> 2) & 0x30303030u);
         const uint32_t sb_lo = hb.y & 0x3f3f3f3fu, mb_lo = hb.z & 0x3f3f3f3fu;
         const uint32_t sb_hi = (hb.w & 0x0f0f0f0fu) | ((hb.y >> 2) & 0x30303030u);
         const uint32_t mb_hi = ((hb.w >> 4) & 0x0f0f0f0fu) | ((hb.z >> 2) & 0x30303030u);
-        const float dma = f16_hi(ha.x), dmb = f16_hi(hb.x);
+        // The min term first (its operands then die) as one more product, A' =
+        // the m_j as f16 pairs (groups 0,1 | 2,3 | 4,5 | 6,7).
+        {
+            const uint32_t one = 0x64006400u;
+            const uint32_t m01a = hsub2(prmt(ma_lo, 0x64646464u, 0x4140u), one);
+            const uint32_t m23a = hsub2(prmt(ma_lo, 0x64646464u, 0x4342u), one);
+            const uint32_t m45a = hsub2(prmt(ma_hi, 0x64646464u, 0x4140u), one);
+            const uint32_t m67a = hsub2(prmt(ma_hi, 0x64646464u, 0x4342u), one);
+            const uint32_t m01b = hsub2(prmt(mb_lo, 0x64646464u, 0x4140u), one);
+            const uint32_t m23b = hsub2(prmt(mb_lo, 0x64646464u, 0x4342u), one);
+            const uint32_t m45b = hsub2(prmt(mb_hi, 0x64646464u, 0x4140u), one);
+            const uint32_t m67b = hsub2(prmt(mb_hi, 0x64646464u, 0x4342u), one);
+            float Dm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (P) {
+                mma16816(Dm, m01a, m01b, m23a, m23b, xf.sh[0], xf.sh[1]);
+                mma16816(Dm, m45a, m45b, m67a, m67b, xf.sh[2], xf.sh[3]);
+            } else {
+                const uint4 sh = lds128<0>(sums), sl = lds128<16>(sums);
+                mma16816(Dm, m01a, m01b, m23a, m23b, sh.x, sh.y);
+                mma16816(Dm, m01a, m01b, m23a, m23b, sl.x, sl.y);
+                mma16816(Dm, m45a, m45b, m67a, m67b, sh.z, sh.w);
+                mma16816(Dm, m45a, m45b, m67a, m67b, sl.z, sl.w);
+            }
+            // the partial sums carry a factor 1/8
+            fold(y4, Dm, -8.0f * f16_hi(ha.x), -8.0f * f16_hi(hb.x));
+        }
+        // d * 2^24 for the low nibbles (q * 2^-24), d * 2^20 for the high ones
+        // (16 q * 2^-24), exactly
+        const float da0 = f16_lo(ha.x) * TWO24, da1 = f16_lo(ha.x) * (TWO24 / 16.0f);
+        const float db0 = f16_lo(hb.x) * TWO24, db1 = f16_lo(hb.x) * (TWO24 / 16.0f);
 #pragma unroll
         for (int c = 0; c < 4; c++) {
             const uint32_t off = 16u + 32u * c + 4u * static_cast<uint32_t>(t);
@@ -183,24 +316,16 @@ struct Q4KT {
                 // bytes 1 and 3 (odd) by a shift and a mask.
                 const uint32_t me = h ? 0x00f000f0u : 0x000f000fu;
                 float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_half_a(D, wa0 & me, wb0 & me, (wa0 >> 8) & me, (wb0 >> 8) & me, xh[j][0], xh[j][1], xl[j][0],
-                           xl[j][1]);
-                mma_half_a(D, wa1 & me, wb1 & me, (wa1 >> 8) & me, (wb1 >> 8) & me, xh[j][2], xh[j][3], xl[j][2],
-                           xl[j][3]);
-                // d * sc_j scaled by 2^24 (2^20 for the high nibbles), exactly
-                const float da = f16_lo(ha.x) * (h ? TWO24 / 16.0f : TWO24);
-                const float db = f16_lo(hb.x) * (h ? TWO24 / 16.0f : TWO24);
+                mma_half_a<P>(D, wa0 & me, wb0 & me, (wa0 >> 8) & me, (wb0 >> 8) & me, xf.h[j][0], xf.h[j][1],
+                              xf.l[j][0], xf.l[j][1]);
+                mma_half_a<P>(D, wa1 & me, wb1 & me, (wa1 >> 8) & me, (wb1 >> 8) & me, xf.h[j][2], xf.h[j][3],
+                              xf.l[j][2], xf.l[j][3]);
+                // (d scaled) * sc_j, exactly: sc_j as the float 2^23 + sc_j
+                const float da = h ? da1 : da0, db = h ? db1 : db0;
                 const uint32_t sel = 0x7440u | static_cast<uint32_t>(j & 3);
                 const float dsa = __fmaf_rn(da, __uint_as_float(prmt(j < 4 ? sa_lo : sa_hi, 0x4B000000u, sel)), -da * TWO23);
-                const float dna = __fmaf_rn(dma, __uint_as_float(prmt(j < 4 ? ma_lo : ma_hi, 0x4B000000u, sel)), -dma * TWO23);
                 const float dsb = __fmaf_rn(db, __uint_as_float(prmt(j < 4 ? sb_lo : sb_hi, 0x4B000000u, sel)), -db * TWO23);
-                const float dnb = __fmaf_rn(dmb, __uint_as_float(prmt(j < 4 ? mb_lo : mb_hi, 0x4B000000u, sel)), -dmb * TWO23);
-                const float4 s = lds_f4(st + 64u * j);
-                fold(y4, D, dsa, dsb, s.x, s.z);
-                y4[0] = __fmaf_rn(-dna, s.y, y4[0]);
-                y4[1] = __fmaf_rn(-dna, s.w, y4[1]);
-                y4[2] = __fmaf_rn(-dnb, s.y, y4[2]);
-                y4[3] = __fmaf_rn(-dnb, s.w, y4[3]);
+                fold(y4, D, dsa, dsb);
             }
         }
     }
@@ -215,14 +340,16 @@ struct Q6KT {
     static constexpr int QK = 256;
     static constexpr int BLOCK_BYTES = 210;
     static constexpr int SLACK = 16;
+    static constexpr bool SUMS = false;
 
-    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int, int t,
-                                                 const uint32_t (&xh)[8][4], const uint32_t (&xl)[8][4],
-                                                 uint32_t st, float (&y4)[4]) {
+    template <bool P>
+    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int, int t, const XFrag& xf,
+                                                 uint32_t, float (&y4)[4]) {
         const uint32_t ba = ra + static_cast<uint32_t>(ks) * BLOCK_BYTES;
         const uint32_t bb = rb + static_cast<uint32_t>(ks) * BLOCK_BYTES;
         const uint32_t bias = 0x64206420u;   // 1024 + 32: the codes become q - 32
         const float da = f16_lo(lds32_a2(ba + 208u)), db = f16_lo(lds32_a2(bb + 208u));
+        const float nda = -da * THREE22, ndb = -db * THREE22;
         const uint32_t lt = 4u * static_cast<uint32_t>(t);
 #pragma unroll
         for (int H = 0; H < 2; H++) {
@@ -246,20 +373,19 @@ struct Q6KT {
                     const uint32_t kb0 = ((hi ? qlb0 >> 4 : qlb0) & 0x0f0f0f0fu) | (((qhb0 >> sh) & 0x03030303u) << 4);
                     const uint32_t kb1 = ((hi ? qlb1 >> 4 : qlb1) & 0x0f0f0f0fu) | (((qhb1 >> sh) & 0x03030303u) << 4);
                     float D0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    mma_half(D0, ka0, kb0, bias, xh[q][0], xh[q][1], xl[q][0], xl[q][1]);
-                    mma_half(D1, ka1, kb1, bias, xh[q][2], xh[q][3], xl[q][2], xl[q][3]);
-                    // scale bytes 2qd and 2qd + 1 of this half's 8 (sign-extended)
+                    mma_half<P>(D0, ka0, kb0, bias, xf.h[q][0], xf.h[q][1], xf.l[q][0], xf.l[q][1]);
+                    mma_half<P>(D1, ka1, kb1, bias, xf.h[q][2], xf.h[q][3], xf.l[q][2], xf.l[q][3]);
+                    // scale bytes 2qd and 2qd + 1 of this half's 8 (sign-extended),
+                    // times d exactly: the int8 as the float 1.5 * 2^23 + sc
                     const uint32_t wa = qd < 2 ? sca0 : sca1, wb = qd < 2 ? scb0 : scb1;
                     const uint32_t b0 = static_cast<uint32_t>((2 * qd) & 3), b1 = b0 + 1u;
                     const uint32_t s0 = b0 | ((8u | b0) * 0x1110u), s1 = b1 | ((8u | b1) * 0x1110u);
-                    const float nda = -da * THREE22, ndb = -db * THREE22;
                     const float ds0a = __fmaf_rn(da, __uint_as_float(prmt(wa, 0u, s0) + 0x4B400000u), nda);
                     const float ds1a = __fmaf_rn(da, __uint_as_float(prmt(wa, 0u, s1) + 0x4B400000u), nda);
                     const float ds0b = __fmaf_rn(db, __uint_as_float(prmt(wb, 0u, s0) + 0x4B400000u), ndb);
                     const float ds1b = __fmaf_rn(db, __uint_as_float(prmt(wb, 0u, s1) + 0x4B400000u), ndb);
-                    const float4 s = lds_f4(st + 64u * q);
-                    fold(y4, D0, ds0a, ds0b, s.x, s.z);
-                    fold(y4, D1, ds1a, ds1b, s.x, s.z);
+                    fold(y4, D0, ds0a, ds0b);
+                    fold(y4, D1, ds1a, ds1b);
                 }
             }
         }
@@ -273,10 +399,11 @@ struct Q8T {
     static constexpr int QK = 32;
     static constexpr int BLOCK_BYTES = 34;
     static constexpr int SLACK = 16;
+    static constexpr bool SUMS = false;
 
-    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int ng, int t,
-                                                 const uint32_t (&xh)[8][4], const uint32_t (&xl)[8][4],
-                                                 uint32_t st, float (&y4)[4]) {
+    template <bool P>
+    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int ng, int t, const XFrag& xf,
+                                                 uint32_t, float (&y4)[4]) {
         const uint32_t bias = 0x64806480u;
         const uint32_t lt = 4u * static_cast<uint32_t>(t);
 #pragma unroll
@@ -288,10 +415,9 @@ struct Q8T {
                 const uint32_t ka0 = lds32_a2(ba + 2u + lt) ^ 0x80808080u, ka1 = lds32_a2(ba + 18u + lt) ^ 0x80808080u;
                 const uint32_t kb0 = lds32_a2(bb + 2u + lt) ^ 0x80808080u, kb1 = lds32_a2(bb + 18u + lt) ^ 0x80808080u;
                 float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_half(D, ka0, kb0, bias, xh[j][0], xh[j][1], xl[j][0], xl[j][1]);
-                mma_half(D, ka1, kb1, bias, xh[j][2], xh[j][3], xl[j][2], xl[j][3]);
-                const float4 s = lds_f4(st + 64u * j);
-                fold(y4, D, da, db, s.x, s.z);
+                mma_half<P>(D, ka0, kb0, bias, xf.h[j][0], xf.h[j][1], xf.l[j][0], xf.l[j][1]);
+                mma_half<P>(D, ka1, kb1, bias, xf.h[j][2], xf.h[j][3], xf.l[j][2], xf.l[j][3]);
+                fold(y4, D, da, db);
             }
         }
     }
@@ -299,18 +425,18 @@ struct Q8T {
 
 // ------------------------------------------------------------------ kernel
 
-// Copy rows [r0, r0 + nr) of W into the slot at shared address dst (row i at
-// dst + i * stride + (its address & 15)), one bulk copy per row, the rows
-// spread over the lanes of the calling warp (all 32 lanes call it). The ragged
-// bytes of a row whose 16-byte cover would run past the buffer are copied by
-// hand before the barrier is armed.
+// Copy rows [r0, r0 + nr) of W, bytes [woff, woff + rowbytes) of each, into
+// the slot at shared address dst (row i at dst + i * stride + (its address &
+// 15)), one bulk copy per row, the rows spread over the lanes of the calling
+// warp (all 32 lanes call it). The ragged bytes of a row whose 16-byte cover
+// would run past the buffer are copied by hand before the barrier is armed.
 __device__ __forceinline__ void tc_issue_warp(const TParams& p, uint8_t* dst_ptr, uint32_t dst, uint32_t bar, int r0,
-                                              int nr, int lane) {
+                                              int nr, uint32_t woff, uint32_t rowbytes, int lane) {
     const uintptr_t lim = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(p.wbytes);
     uint32_t total = 0;
     for (int i = lane; i < nr; i += 32) {
-        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.wpitch + p.woff;
-        const uintptr_t ge = gs + p.rowbytes;
+        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.wpitch + woff;
+        const uintptr_t ge = gs + rowbytes;
         const uintptr_t a0 = gs & ~uintptr_t(15);
         uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
         if (a1 > lim) {
@@ -325,8 +451,8 @@ __device__ __forceinline__ void tc_issue_warp(const TParams& p, uint8_t* dst_ptr
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
     for (int i = lane; i < nr; i += 32) {
-        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.wpitch + p.woff;
-        const uintptr_t ge = gs + p.rowbytes;
+        const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.wpitch + woff;
+        const uintptr_t ge = gs + rowbytes;
         const uintptr_t a0 = gs & ~uintptr_t(15);
         uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
         if (a1 > lim) a1 = ge & ~uintptr_t(15);
@@ -336,12 +462,12 @@ __device__ __forceinline__ void tc_issue_warp(const TParams& p, uint8_t* dst_ptr
     }
 }
 
-template <class F>
+template <class F, bool P>
 __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    const int ks = tid >> 5;   // this warp's slice
+    const int ks = tid >> 5;   // this warp's slice of every k-chunk
     const int g = lane >> 2, t = lane & 3;
 
     const int part = blockIdx.x;
@@ -351,7 +477,9 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
     pdl_launch_dependents();
     if (nrows <= 0) return;
 
-    const int npc = (nrows + p.CR - 1) / p.CR;
+    const int npc = (nrows + p.CR - 1) / p.CR;   // row pieces per k-chunk
+    const int np = npc * p.nchunks;              // pieces, k-chunk major
+    const int cgroups = p.KS * TC_GROUPS_PER_SLICE;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t ring = sbase + p.off_ring;
     const uint32_t bars = sbase + p.off_bars;
@@ -360,11 +488,14 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
     int* issued = cnt + p.S;
     int* timeout = cnt + p.S + 1;
 
-    // Request piece pc into slot s (a whole warp).
-    auto issue = [&](int pc, int s) {
+    // Request piece pi into slot s (a whole warp).
+    auto issue = [&](int pi, int s) {
+        const int c = pi / npc, pc = pi - (pi / npc) * npc;
+        const int gc = min(cgroups, p.ngroups - c * cgroups);
+        const uint32_t cb = static_cast<uint32_t>(gc * 32 / F::QK) * F::BLOCK_BYTES;
         tc_issue_warp(p, smem + p.off_ring + static_cast<uint32_t>(s) * p.slot_stride,
                       ring + static_cast<uint32_t>(s) * p.slot_stride, bars + 8u * s, R0 + pc * p.CR,
-                      min(p.CR, nrows - pc * p.CR), lane);
+                      min(p.CR, nrows - pc * p.CR), static_cast<uint32_t>(c) * p.chunk_bytes, cb, lane);
     };
 
     if (ks == 0) {
@@ -377,68 +508,40 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
             *timeout = 0;
         }
         __syncwarp();
-        const int first = npc < p.S ? npc : p.S;
-        for (int pc = 0; pc < first; pc++) issue(pc, pc);
+        const int first = np < p.S ? np : p.S;
+        for (int pi = 0; pi < first; pi++) issue(pi, pi);
         if (lane == 0) *issued = first;
     }
     if (!p.early_inputs) pdl_dependency_wait();
 
-    // ---- this lane's x fragments: column m = g of the slice's groups
-    const int G0 = ks * TC_GROUPS_PER_SLICE;
-    const int ng = min(TC_GROUPS_PER_SLICE, p.ngroups - G0);
-    uint32_t xh[8][4], xl[8][4];
-    float2* stt = reinterpret_cast<float2*>(smem + p.off_st);
-#pragma unroll
-    for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
-        float v[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-        const bool live = j < ng && g < p.m;
-        if (live) {
-            const float* src = p.x + static_cast<long long>(g) * p.xstride + 32 * (G0 + j) + 4 * t;
-            const float4 u0 = __ldg(reinterpret_cast<const float4*>(src));
-            const float4 u1 = __ldg(reinterpret_cast<const float4*>(src + 16));
-            v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
-            v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
-        }
-        float amax = 0.0f, sum = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            amax = fmaxf(amax, fabsf(v[i]));
-            sum += v[i];
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
-        sum += __shfl_xor_sync(FULL, sum, 1);
-        sum += __shfl_xor_sync(FULL, sum, 2);
-        // power-of-two scale putting the group maximum in [2^14, 2^15)
-        int s = 0;
-        if (amax > 0.0f) {
-            s = 141 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
-            s = s > 126 ? 126 : (s < -126 ? -126 : s);
-        }
-        const float p2 = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
-        const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-#pragma unroll
-        for (int i = 0; i < 8; i++) v[i] *= p2;
-        // MMA-k order of a half: (4t, 4t+2) then (4t+1, 4t+3)
-        const uint32_t h0 = pack_h2(v[0], v[2]), h1 = pack_h2(v[1], v[3]);
-        const uint32_t h2 = pack_h2(v[4], v[6]), h3 = pack_h2(v[5], v[7]);
-        const float2 f0 = unpack_h2(h0), f1 = unpack_h2(h1), f2 = unpack_h2(h2), f3 = unpack_h2(h3);
-        xh[j][0] = h0; xh[j][1] = h1; xh[j][2] = h2; xh[j][3] = h3;
-        xl[j][0] = pack_h2(v[0] - f0.x, v[2] - f0.y);
-        xl[j][1] = pack_h2(v[1] - f1.x, v[3] - f1.y);
-        xl[j][2] = pack_h2(v[4] - f2.x, v[6] - f2.y);
-        xl[j][3] = pack_h2(v[5] - f3.x, v[7] - f3.y);
-        if (t == 0 && j < ng) stt[(G0 + j) * TC_COLS + g] = live ? make_float2(inv, sum) : make_float2(0.0f, 0.0f);
-    }
-    __syncthreads();   // statistics complete; barriers initialized
+    // this lane's x fragments for k-chunk c: MMA column g of the warp's slice
+    // (row xr of x; packed, hi for g < 4 and lo for g >= 4)
+    const int xr = P ? (g & 3) : g;
+    const uint32_t sums_l = sbase + p.off_sums + static_cast<uint32_t>(tid) * 32u;
+    XFrag xf;
+    int ng = 0;
+    float inv0 = 1.0f, inv1 = 1.0f;   // scale of columns 2t, 2t + 1
+    auto load_chunk = [&](int c) {
+        const int G = c * cgroups + ks * TC_GROUPS_PER_SLICE;
+        ng = max(0, min(TC_GROUPS_PER_SLICE, p.ngroups - G));
+        const bool live = xr < p.m && ng > 0;
+        float inv;
+        tc_load_x<F::SUMS, P>(p.x + static_cast<long long>(xr) * p.k + 32 * G + 4 * t, live, ng, P && g >= 4, sums_l,
+                              xf, inv);
+        inv0 = __shfl_sync(FULL, inv, 8 * t);
+        inv1 = __shfl_sync(FULL, inv, 8 * t + 4);
+    };
+    load_chunk(0);
+    __syncthreads();   // barriers initialized
 
     float* red = reinterpret_cast<float*>(smem + p.off_red);
-    const uint32_t st = sbase + p.off_st + static_cast<uint32_t>((G0 * TC_COLS + 2 * t) * 8);
-    const uintptr_t wbase = reinterpret_cast<uintptr_t>(p.w);
+    const uint32_t wbase32 = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.w));
 
     int s = 0;
     uint32_t par = 0;
-    for (int pc = 0; pc < npc; pc++) {
+    for (int pi = 0; pi < np; pi++) {
+        const int c = pi / npc, pc = pi - (pi / npc) * npc;
+        if (pc == 0 && c > 0) load_chunk(c);
         const bool landed = __all_sync(FULL, mbar_wait_bounded(bars + 8u * s, par));
         if (!landed) {
             if (lane == 0) {
@@ -450,30 +553,45 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
         const int nr = min(p.CR, nrows - pc * p.CR);
         const int rl0 = pc * p.CR;   // CTA-local row of the piece's first row
         const uint32_t slot = ring + static_cast<uint32_t>(s) * p.slot_stride;
-        for (int r = 0; r < nr; r += TC_TILE_ROWS) {
-            const int ia = r + g, ib = r + g + 8;
-            // rows past the piece read the slot's spare rows (results dropped)
-            const uint32_t pa =
-                static_cast<uint32_t>((wbase + static_cast<uintptr_t>(R0 + rl0 + ia) * p.wpitch + p.woff) & 15u);
-            const uint32_t pb =
-                static_cast<uint32_t>((wbase + static_cast<uintptr_t>(R0 + rl0 + ib) * p.wpitch + p.woff) & 15u);
-            const uint32_t ra = slot + static_cast<uint32_t>(ia) * p.stride + pa;
-            const uint32_t rb = slot + static_cast<uint32_t>(ib) * p.stride + pb;
-            float y4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            F::slice(ra, rb, ks, ng, t, xh, xl, st, y4);
-            // park this slice's sums of columns 2t, 2t + 1
-            if (ia < nr) {
-                red[((rl0 + ia) * p.KS + ks) * TC_COLS + 2 * t] = y4[0];
-                red[((rl0 + ia) * p.KS + ks) * TC_COLS + 2 * t + 1] = y4[1];
-            }
-            if (ib < nr) {
-                red[((rl0 + ib) * p.KS + ks) * TC_COLS + 2 * t] = y4[2];
-                red[((rl0 + ib) * p.KS + ks) * TC_COLS + 2 * t + 1] = y4[3];
+        // low bits of the global address of the piece's first row chunk
+        const uint32_t pbase = wbase32 + static_cast<uint32_t>(c) * p.chunk_bytes +
+                               static_cast<uint32_t>(R0 + rl0) * p.wpitch;
+        if (ng > 0) {
+            for (int r = 0; r < nr; r += TC_TILE_ROWS) {
+                const int ia = r + g, ib = r + g + 8;
+                // rows past the piece read the slot's spare rows (results dropped)
+                const uint32_t pa = (pbase + static_cast<uint32_t>(ia) * p.wpitch) & 15u;
+                const uint32_t pb = (pbase + static_cast<uint32_t>(ib) * p.wpitch) & 15u;
+                const uint32_t ra = slot + static_cast<uint32_t>(ia) * p.stride + pa;
+                const uint32_t rb = slot + static_cast<uint32_t>(ib) * p.stride + pb;
+                float y4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                F::template slice<P>(ra, rb, ks, ng, t, xf, sums_l, y4);
+                // park this slice's sums of columns 2t, 2t + 1, unscaled
+                float2 va = make_float2(y4[0] * inv0, y4[1] * inv1);
+                float2 vb = make_float2(y4[2] * inv0, y4[3] * inv1);
+                float2* qa = reinterpret_cast<float2*>(red + ((rl0 + ia) * p.KS + ks) * TC_COLS + 2 * t);
+                float2* qb = reinterpret_cast<float2*>(red + ((rl0 + ib) * p.KS + ks) * TC_COLS + 2 * t);
+                if (ia < nr) {
+                    if (c > 0) {
+                        const float2 o = *qa;
+                        va.x += o.x;
+                        va.y += o.y;
+                    }
+                    *qa = va;
+                }
+                if (ib < nr) {
+                    if (c > 0) {
+                        const float2 o = *qb;
+                        vb.x += o.x;
+                        vb.y += o.y;
+                    }
+                    *qb = vb;
+                }
             }
         }
         __syncwarp();
-        if (pc + p.S < npc) {
-            // the last warp done with slot s re-fills it with piece pc + S
+        if (pi + p.S < np) {
+            // the last warp done with slot s re-fills it with piece pi + S
             int last = 1;
             if (lane == 0 && p.KS > 1) {
                 __threadfence_block();
@@ -483,8 +601,8 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
             last = __shfl_sync(FULL, last, 0);
             if (last) {
                 fence_proxy_async();
-                issue(pc + p.S, s);
-                if (lane == 0) atomicMax(issued, pc + p.S + 1);
+                issue(pi + p.S, s);
+                if (lane == 0) atomicMax(issued, pi + p.S + 1);
             }
         }
         if (++s == p.S) {
@@ -497,8 +615,8 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
     if (*timeout) {
         if (tid == 0) {
             const int n = *issued;
-            for (int pc = n - p.S > 0 ? n - p.S : 0; pc < n; pc++)
-                if (!mbar_wait_bounded(bars + 8u * (pc % p.S), static_cast<uint32_t>((pc / p.S) & 1))) break;
+            for (int pi = n - p.S > 0 ? n - p.S : 0; pi < n; pi++)
+                if (!mbar_wait_bounded(bars + 8u * (pi % p.S), static_cast<uint32_t>((pi / p.S) & 1))) break;
         }
         return;
     }
@@ -506,9 +624,11 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
     for (int e = tid; e < nrows * p.m; e += blockDim.x) {
         const int r = e / p.m, i = e - (e / p.m) * p.m;
         float v = 0.0f;
-        for (int q = 0; q < p.KS; q++) v += red[(r * p.KS + q) * TC_COLS + i];
-        float* dst = p.y + static_cast<long long>(i) * p.rows + R0 + r;
-        *dst = p.accumulate ? *dst + v : v;
+        for (int q = 0; q < p.KS; q++) {
+            v += red[(r * p.KS + q) * TC_COLS + i];
+            if (P) v += red[(r * p.KS + q) * TC_COLS + i + 4];
+        }
+        p.y[static_cast<long long>(i) * p.rows + R0 + r] = v;
     }
 }
 
@@ -521,15 +641,22 @@ inline uint32_t tc_row_stride(uint32_t rowbytes, int slack) {
     return s + ((16u + 128u - (s & 127u)) & 127u);
 }
 
-// Launch plan for m (1..8) rows of x on a device described by di.
+// Launch plan for m (1..8) rows of x on a device described by di. The k-slices
+// of a row (8 groups each) are dealt into the fewest k-chunks of at most
+// MAX_WARPS slices (cfg->warps, when given, lowers that bound), balanced; a
+// chunk's slices are the CTA's warps.
 template <class F>
 inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv_cfg* cfg, TParams* tp, Plan* pl) {
     if (m < 1 || m > TC_COLS || rows <= 0 || k <= 0 || k % F::QK) return QMV_EINVAL;
     const int ngroups = k / 32;
-    const int KS = (ngroups + TC_GROUPS_PER_SLICE - 1) / TC_GROUPS_PER_SLICE;
-    if (KS > MAX_WARPS) return QMV_ETOOBIG;
+    const int NS = (ngroups + TC_GROUPS_PER_SLICE - 1) / TC_GROUPS_PER_SLICE;
+    const int kmax = (cfg && cfg->warps > 0) ? std::min(cfg->warps, MAX_WARPS) : MAX_WARPS;
+    const int nchunks = (NS + kmax - 1) / kmax;
+    const int KS = (NS + nchunks - 1) / nchunks;
     const long long rowbytes = static_cast<long long>(k / F::QK) * F::BLOCK_BYTES;
-    const uint32_t stride = tc_row_stride(static_cast<uint32_t>(rowbytes), F::SLACK);
+    const long long chunk_bytes = static_cast<long long>(KS * TC_GROUPS_PER_SLICE * 32 / F::QK) * F::BLOCK_BYTES;
+    if (rowbytes > 0x7fffffffLL) return QMV_ETOOBIG;
+    const uint32_t stride = tc_row_stride(static_cast<uint32_t>(std::min(chunk_bytes, rowbytes)), F::SLACK);
     const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
     const long long full = di.smem_optin;
 
@@ -545,16 +672,17 @@ inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv
         CR = std::max(1, std::min(CR, rpc));
         const long long cap = round_up(CR, TC_TILE_ROWS);   // rows a slot holds (tiles of 16)
         const long long slot = round_up(cap * stride, 128);
-        const int pieces = (rpc + CR - 1) / CR;
-        const long long fixed = round_up(8LL * ngroups * TC_COLS, 128) + round_up(4LL * rpc * KS * TC_COLS, 128);
-        int S = (cfg && cfg->chunks > 0) ? std::min(cfg->chunks, pieces) : pieces;
+        const long long pieces = static_cast<long long>((rpc + CR - 1) / CR) * nchunks;
+        const long long sums = F::SUMS ? 32LL * 32 * KS : 0;   // 32 bytes a thread
+        const long long fixed = round_up(4LL * rpc * KS * TC_COLS, 128) + sums;
+        long long S = (cfg && cfg->chunks > 0) ? std::min<long long>(cfg->chunks, pieces) : pieces;
         while (S > 0 && fixed + S * slot + 8LL * S + 4LL * (S + 2) > full) S--;
         if (S >= 1 && slot <= 0x7fffffffLL) {
             long long off = 0;
-            tp->off_st = 0;
-            off = round_up(8LL * ngroups * TC_COLS, 128);
-            tp->off_red = static_cast<uint32_t>(off);
-            off = round_up(off + 4LL * rpc * KS * TC_COLS, 128);
+            tp->off_red = 0;
+            off = round_up(4LL * rpc * KS * TC_COLS, 128);
+            tp->off_sums = static_cast<uint32_t>(off);
+            off += sums;
             tp->off_ring = static_cast<uint32_t>(off);
             off += S * slot;
             tp->off_bars = static_cast<uint32_t>(off);
@@ -569,16 +697,14 @@ inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv
             tp->rows = rows;
             tp->k = k;
             tp->m = m;
-            tp->xstride = k;
             tp->wpitch = static_cast<uint32_t>(rowbytes);
-            tp->woff = 0;
-            tp->accumulate = 0;
             tp->ngroups = ngroups;
-            tp->rowbytes = static_cast<uint32_t>(rowbytes);
-            tp->stride = stride;
             tp->KS = KS;
+            tp->nchunks = nchunks;
+            tp->chunk_bytes = static_cast<uint32_t>(std::min(chunk_bytes, rowbytes));
+            tp->stride = stride;
             tp->CR = CR;
-            tp->S = S;
+            tp->S = static_cast<int>(S);
             tp->rq = rows / parts;
             tp->rrem = rows % parts;
             tp->early_inputs = mode >= 2 ? 1 : 0;
@@ -591,9 +717,9 @@ inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv
     }
 }
 
-template <class F>
-inline int launch_tc(const TParams& tp, const Plan& pl, cudaStream_t stream) {
-    auto kern = qmm_tc_kernel<F>;
+template <class F, bool P>
+inline int launch_tc_kernel(const TParams& tp, const Plan& pl, cudaStream_t stream) {
+    auto kern = qmm_tc_kernel<F, P>;
     static SmemOptIn opted;
     int dev = 0;
     DevInfo di;
@@ -616,40 +742,34 @@ inline int launch_tc(const TParams& tp, const Plan& pl, cudaStream_t stream) {
     return cuda_rc(cudaLaunchKernelEx(&lc, kern, tp));
 }
 
-// Weights per row one launch takes: 16 warps x 256.
-constexpr int TC_MAX_K = TC_GROUPS_PER_SLICE * 32 * MAX_WARPS;
+// Up to 4 rows of x take the packed kernel (hi and lo in the two halves of
+// the MMA's 8 columns: half the MMAs).
+template <class F>
+inline int launch_tc(const TParams& tp, const Plan& pl, cudaStream_t stream) {
+    return tp.m <= TC_COLS / 2 ? launch_tc_kernel<F, true>(tp, pl, stream) : launch_tc_kernel<F, false>(tp, pl, stream);
+}
 
 // y[m, rows] = x[m, k] W^T on the tensor cores, m >= 1: ceil(m / 8) balanced
-// tiles of rows of x; rows longer than TC_MAX_K weights in k-chunks of
-// TC_MAX_K, one launch each, the later chunks adding to y in chunk order
-// (each launch reads its chunk of W once).
+// tiles of rows of x, one launch each (each launch reads W once).
 template <class F>
 inline int qmm_tc_run(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
                       cudaStream_t s) {
     const int tiles = (m + TC_COLS - 1) / TC_COLS;
-    const long long pitch = static_cast<long long>(k / F::QK) * F::BLOCK_BYTES;
     DevInfo di;
     int rc = dev_info(&di, nullptr);
     if (rc) return rc;
     for (int t0 = 0, m0 = 0; t0 < tiles; t0++) {
         const int mt = m / tiles + (t0 < m % tiles ? 1 : 0);
-        for (int k0 = 0; k0 < k; k0 += TC_MAX_K) {
-            const int kc = std::min(TC_MAX_K, k - k0);
-            TParams tp{};
-            Plan pl;
-            rc = make_tc_plan_for<F>(di, rows, kc, mt, cfg, &tp, &pl);
-            if (rc) return rc;
-            tp.w = static_cast<const uint8_t*>(w);
-            tp.x = x + static_cast<long long>(m0) * k + k0;
-            tp.y = y + static_cast<long long>(m0) * rows;
-            tp.xstride = k;
-            tp.wpitch = static_cast<uint32_t>(pitch);
-            tp.woff = static_cast<uint32_t>(static_cast<long long>(k0 / F::QK) * F::BLOCK_BYTES);
-            tp.accumulate = k0 > 0 ? 1 : 0;
-            tp.wbytes = static_cast<unsigned long long>(rows) * static_cast<unsigned long long>(pitch);
-            rc = launch_tc<F>(tp, pl, s);
-            if (rc) return rc;
-        }
+        TParams tp{};
+        Plan pl;
+        rc = make_tc_plan_for<F>(di, rows, k, mt, cfg, &tp, &pl);
+        if (rc) return rc;
+        tp.w = static_cast<const uint8_t*>(w);
+        tp.x = x + static_cast<long long>(m0) * k;
+        tp.y = y + static_cast<long long>(m0) * rows;
+        tp.wbytes = static_cast<unsigned long long>(rows) * tp.wpitch;
+        rc = launch_tc<F>(tp, pl, s);
+        if (rc) return rc;
         m0 += mt;
     }
     return QMV_OK;

@@ -470,14 +470,15 @@ int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_cfg* cfg, cons
                                       tp.KS,
                                       tp.CR,
                                       tp.S,
-                                      static_cast<int>(tp.rowbytes),
+                                      static_cast<int>(tp.chunk_bytes),
                                       static_cast<int>(tp.stride),
                                       static_cast<int>(tp.slot_stride),
                                       tp.rq,
                                       tp.rrem,
                                       tp.ngroups,
-                                      static_cast<int>(tp.off_st),
+                                      tp.nchunks,
                                       static_cast<int>(tp.off_red),
+                                      static_cast<int>(tp.off_sums),
                                       static_cast<int>(tp.off_ring),
                                       static_cast<int>(tp.off_bars),
                                       static_cast<int>(tp.off_cnt)};

@@ -350,15 +350,16 @@ int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *
 #define QMV_PLAN_DETAIL_FIELDS 30
 int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, const int *device, int *out);
 
-/* The tensor-core plan of the batched product (rows of up to 4096 weights)
- * for one tile of m (1..8) rows of x on a described device (as for
- * qmv_plan_detail). fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0. out receives
- * QMM_TC_PLAN_FIELDS ints: threads, ctas, dynamic shared bytes, warps
- * (k-slices of 256 weights), rows per ring slot, ring slots, bytes per row,
- * shared row stride, slot stride, rows per CTA (q, rem), 32-weight groups per
- * row, shared offsets of the x statistics, the parked partials, the ring, the
- * barriers and the counters. */
-#define QMM_TC_PLAN_FIELDS 17
+/* The tensor-core plan of the batched product for one tile of m (1..8) rows
+ * of x on a described device (as for qmv_plan_detail). fmt: 0 = Q4_K,
+ * 1 = Q6_K, 2 = Q8_0. out receives QMM_TC_PLAN_FIELDS ints: threads, ctas,
+ * dynamic shared bytes, warps (k-slices of 256 weights per k-chunk), rows per
+ * ring slot, ring slots, bytes of one row's k-chunk, shared row stride, slot
+ * stride, rows per CTA (q, rem), 32-weight groups per row, k-chunks, shared
+ * offsets of the parked partials, the min-term fragments (Q4_K, 32 bytes a
+ * thread; none for the other formats), the ring, the barriers and the
+ * counters. */
+#define QMM_TC_PLAN_FIELDS 18
 int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_cfg *cfg, const int *device, int *out);
 
 #ifdef __cplusplus

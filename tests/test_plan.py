@@ -309,63 +309,84 @@ def test_planner_rejects(q):
 TC_FMT = {"q4k": (0, 256, 144), "q6k": (1, 256, 210), "q8_0": (2, 32, 34)}
 
 
-def tc_max_read(fmt, KS, ngroups):
-    """Last byte (exclusive) a lane may read past a staged row's first byte."""
+def tc_max_read(fmt, slices, groups):
+    """Last byte (exclusive) a lane may read past the first byte of a staged
+    row's k-chunk of `slices` slices and `groups` groups."""
     if fmt == "q4k":
-        return KS * 144
+        return slices * 144
     if fmt == "q6k":
-        return (KS - 1) * 210 + 216   # funnel loads of d at 208: 8 bytes from the word below
-    return (ngroups - 1) * 34 + 38    # codes at 18 + 4t: 8 bytes from the word below
+        return (slices - 1) * 210 + 216   # funnel loads of d at 208: 8 bytes from the word below
+    return (groups - 1) * 34 + 38          # codes at 18 + 4t: 8 bytes from the word below
 
 
 def tc_replay(q, fmt, rows, k, m, cfg=None):
     fid, qk, bb = TC_FMT[fmt]
     P = q.qmm_tc_plan_detail(fid, rows, k, m, cfg, DEVICE)
     ng = k // 32
-    KS = -(-ng // 8)
-    assert P["KS"] == KS and P["threads"] == 32 * KS <= 512 and P["ngroups"] == ng
-    rowbytes, stride, CR, S, parts = P["rowbytes"], P["stride"], P["CR"], P["S"], P["ctas"]
-    assert rowbytes == (k // qk) * bb
-    assert stride % 128 == 16 and stride >= rowbytes + 16
+    NS = -(-ng // 8)
+    kmax = min(cfg["warps"], 16) if cfg and cfg.get("warps") else 16
+    nch = -(-NS // kmax)
+    KS = -(-NS // nch)
+    assert P["KS"] == KS and P["nchunks"] == nch and P["threads"] == 32 * KS <= 512 and P["ngroups"] == ng
+    rowbytes = (k // qk) * bb
+    cgroups = 8 * KS
+    chunk = min(cgroups * 32 // qk * bb, rowbytes)
+    stride, CR, S, parts = P["stride"], P["CR"], P["S"], P["ctas"]
+    assert P["chunk_bytes"] == chunk
+    assert stride % 128 == 16 and stride >= chunk + 16
     cap = -(-CR // 16) * 16
     assert P["slot_stride"] >= cap * stride and P["slot_stride"] % 128 == 0
     assert P["rq"] * parts + P["rrem"] == rows and P["rq"] >= 1
     rpc = P["rq"] + (1 if P["rrem"] else 0)
-    regions = [(P["off_st"], 8 * ng * 8), (P["off_red"], 4 * rpc * KS * 8), (P["off_ring"], S * P["slot_stride"]),
+    sums = 32 * 32 * KS if fmt == "q4k" else 0   # 32 bytes a thread (Q4_K min-term fragments)
+    regions = [(P["off_red"], 4 * rpc * KS * 8), (P["off_sums"], sums), (P["off_ring"], S * P["slot_stride"]),
                (P["off_bars"], 8 * S), (P["off_cnt"], 4 * (S + 2))]
     regions.sort()
     for (o1, n1), (o2, _) in zip(regions, regions[1:]):
         assert o1 + n1 <= o2
     assert regions[-1][0] + regions[-1][1] <= P["smem"] <= DEVICE[1]
-    assert P["off_ring"] % 128 == 0 and P["off_bars"] % 8 == 0 and P["off_st"] % 16 == 0
-    last = tc_max_read(fmt, KS, ng)
+    assert P["off_ring"] % 128 == 0 and P["off_bars"] % 8 == 0 and P["off_red"] % 16 == 0 and P["off_sums"] % 16 == 0
+    # the chunks tile each row: chunk c holds groups [c * cgroups, ...), every
+    # chunk non-empty, the last one ending at the row's end
+    ends = []
+    for c in range(nch):
+        gc = min(cgroups, ng - c * cgroups)
+        assert gc > 0
+        cb = gc * 32 // qk * bb
+        woff = c * chunk
+        assert woff == c * cgroups * 32 // qk * bb and woff + cb <= rowbytes
+        ends.append((woff, cb, -(-gc // 8), gc))
+    assert ends[-1][0] + ends[-1][1] == rowbytes
     wbytes = rows * rowbytes
-    covered = np.zeros(rows, dtype=np.int32)
-    for part in range(parts):
-        nrows = P["rq"] + (1 if part < P["rrem"] else 0)
-        R0 = part * P["rq"] + min(part, P["rrem"])
-        for pc in range(-(-nrows // CR)):
-            nr = min(CR, nrows - pc * CR)
-            for i in range(nr):
-                gs = (R0 + pc * CR + i) * rowbytes      # the weight base is 16-byte aligned
-                a0, a1 = gs & ~15, (gs + rowbytes + 15) & ~15
-                if a1 > wbytes:
-                    a1 = (gs + rowbytes) & ~15
-                assert a1 - a0 <= stride
-                covered[R0 + pc * CR + i] += 1
-            # every row a tile touches (spare rows included) stays in the slot
-            for r in range(0, nr, 16):
-                for ia in range(r, r + 16):
-                    assert ia < cap
-                    ph = ((R0 + pc * CR + ia) * rowbytes) & 15
-                    assert ia * stride + ph + last <= P["slot_stride"]
-    assert np.all(covered == 1)
+    covered = np.zeros(rows, dtype=np.int64)
+    for woff, cb, slices, gc in ends:
+        last = tc_max_read(fmt, slices, gc)
+        for part in range(parts):
+            nrows = P["rq"] + (1 if part < P["rrem"] else 0)
+            R0 = part * P["rq"] + min(part, P["rrem"])
+            for pc in range(-(-nrows // CR)):
+                nr = min(CR, nrows - pc * CR)
+                for i in range(nr):
+                    gs = (R0 + pc * CR + i) * rowbytes + woff   # the weight base is 16-byte aligned
+                    a0, a1 = gs & ~15, (gs + cb + 15) & ~15
+                    if a1 > wbytes:
+                        a1 = (gs + cb) & ~15
+                    assert a1 - a0 <= stride
+                    covered[R0 + pc * CR + i] += cb
+                # every row a tile touches (spare rows included) stays in the slot
+                for r in range(0, nr, 16):
+                    for ia in range(r, r + 16):
+                        assert ia < cap
+                        ph = ((R0 + pc * CR + ia) * rowbytes + woff) & 15
+                        assert ia * stride + ph + last <= P["slot_stride"]
+    assert np.all(covered == rowbytes)
     return P
 
 
 TC_SHAPES = [("q4k", 4096, 4096), ("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 2304), ("q6k", 4096, 4096),
              ("q6k", 300, 512), ("q6k", 3, 256), ("q6k", 41, 3840), ("q8_0", 14336, 4096), ("q8_0", 300, 96),
-             ("q8_0", 13, 32), ("q8_0", 7, 4064), ("q8_0", 64, 1056)]
+             ("q8_0", 13, 32), ("q8_0", 7, 4064), ("q8_0", 64, 1056), ("q4k", 20, 16384), ("q4k", 97, 4352),
+             ("q6k", 4096, 14336), ("q6k", 41, 14336), ("q8_0", 64, 11008), ("q8_0", 5, 4160), ("q8_0", 3, 12320)]
 
 
 @pytest.mark.parametrize("m", [1, 2, 5, 8])
@@ -377,15 +398,24 @@ def test_tc_plans(q, shape, m):
 
 @pytest.mark.parametrize("cfg", [dict(ctas=1, chunk_rows=1, chunks=2), dict(ctas=3, chunk_rows=5, chunks=2),
                                  dict(ctas=2, chunk_rows=20, chunks=1), dict(ctas=7, chunks=3),
-                                 dict(ctas=1, chunk_rows=16, chunks=2)])
+                                 dict(ctas=1, chunk_rows=16, chunks=2), dict(ctas=2, chunks=2, warps=1),
+                                 dict(ctas=3, chunk_rows=7, chunks=3, warps=3)])
 @pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0"])
 def test_tc_forced_plans(q, fmt, cfg):
     tc_replay(q, fmt, 61, 512, 3, cfg)
 
 
-def test_tc_planner_rejects_long_rows(q):
+def test_tc_long_rows_take_kchunks(q):
+    """Rows longer than 16 slices are dealt into balanced k-chunks of one
+    launch: 14336 weights = 56 slices = 4 chunks of 14, 4352 = 17 slices = 2
+    chunks of 9 (the second one 8); a warps bound forces more chunks."""
+    assert tc_replay(q, "q6k", 4096, 14336, 4)["nchunks"] == 4
+    P = tc_replay(q, "q4k", 64, 4352, 4)
+    assert (P["nchunks"], P["KS"]) == (2, 9)
+    P = tc_replay(q, "q8_0", 13, 1056, 5, dict(warps=2))
+    assert (P["nchunks"], P["KS"]) == (3, 2)
     with pytest.raises(q.QmvError):
-        q.qmm_tc_plan_detail(0, 64, 4352, 4, None, DEVICE)
+        q.qmm_tc_plan_detail(0, 64, 4100, 4, None, DEVICE)   # k not a multiple of 256
 
 
 def _random_cases():
