@@ -162,127 +162,4 @@ struct Q4KB {
     }
 };
 
-// ============================================================== Q6_K batch
-//
-// Unit u covers weights e0 = UW*u .. e0+UW-1 in natural order: half
-// H = e0/128, quarter qd = (e0%128)/32, positions l = e0%32 onwards. Low 4
-// bits: nibble (qd >= 2: high) of ql[64H + 32*(qd%2) + l]; top 2 bits: bits
-// 2qd, 2qd+1 of qh[32H + l]; scale 8H + 2qd + l/16 (two scales for UW = 32).
-// w = (d*scale) * (q - 32), one rounding (d*scale is exact in f32).
-template <int M>
-struct Q6KB {
-    static constexpr int QK = 256;
-    static constexpr int BLOCK_BYTES = 210;
-    static constexpr int UW = BatchUnit<M>::UW;
-    static constexpr int UPB = QK / UW;
-    static constexpr int SLICE_BLOCKS = 32 / UPB;
-    static constexpr int SLACK = 16;
-    static constexpr bool LIMBS = false;
-    static constexpr int DEFAULT_UNROLL = 1;
-    static constexpr int OUTS = M;
-
-    __host__ __device__ static int units(int nb) { return UPB * nb; }
-    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u / UPB) * BLOCK_BYTES; }
-    __device__ __forceinline__ static int unit_elem(int u) { return (u / UPB) * QK + (u % UPB) * UW; }
-
-    struct L {
-        uint32_t ql_off, qh_off;   // byte offsets (multiples of 8) in the block
-        uint32_t sc_word;          // offset of the 4-byte-aligned word holding the first scale
-        uint32_t sel0, sel1;       // sign-extending selectors of the scale byte(s) in 8 bytes from sc_word
-        uint32_t qsh;              // 2*qd
-        bool hinib;                // qd >= 2
-    };
-    __device__ __forceinline__ static L lane_consts(int u, int, int) {
-        const uint32_t e0 = static_cast<uint32_t>((u % UPB) * UW);
-        const uint32_t H = e0 >> 7, qd = (e0 >> 5) & 3u, l0 = e0 & 31u;
-        L l;
-        l.ql_off = 64u * H + 32u * (qd & 1u) + l0;
-        l.qh_off = 128u + 32u * H + l0;
-        const uint32_t sc = 192u + 8u * H + 2u * qd + (l0 >> 4);
-        l.sc_word = sc & ~3u;
-        const uint32_t b0 = sc & 3u, b1 = b0 + 1u;   // byte of the second scale (UW = 32), may be 4
-        l.sel0 = b0 | ((8u | b0) * 0x1110u);
-        l.sel1 = (b1 & 3u) | ((8u | (b1 & 3u)) * 0x1110u);
-        l.qsh = 2u * qd;
-        l.hinib = qd >= 2;
-        return l;
-    }
-
-    // a: shared address of the block (2-byte aligned).
-    __device__ __forceinline__ static void decode(uint32_t a, const L& l, float2 (&w)[UW / 2]) {
-        const uint32_t wa = a & ~3u;
-        const uint32_t sh = (a & 3u) * 8u;   // every field offset used here is a multiple of 4
-        uint32_t ql[UW / 4], qh[UW / 4];
-        lds_words_sh<UW>(wa + l.ql_off, sh, ql);
-        lds_words_sh<UW>(wa + l.qh_off, sh, qh);
-        const uint2 scw = lds8_sh<0>(wa + l.sc_word, sh);
-        const float d = f16_lo(lds32<208>(wa) >> sh);
-        const float nd = -d * THREE22;
-        const uint32_t s0 = prmt(scw.x, 0u, l.sel0);
-        const uint32_t s1 = prmt((l.sel0 & 3u) == 3u ? scw.y : scw.x, 0u, l.sel1);
-        const float ds0 = __fmaf_rn(d, __uint_as_float(s0 + 0x4B400000u), nd);
-        const float ds1 = __fmaf_rn(d, __uint_as_float(s1 + 0x4B400000u), nd);
-        const float2 off = make_float2(-(TWO23 + 32.0f), -(TWO23 + 32.0f));
-#pragma unroll
-        for (int i = 0; i < UW / 4; i++) {
-            const uint32_t lo4 = l.hinib ? ((ql[i] >> 4) & 0x0f0f0f0fu) : (ql[i] & 0x0f0f0f0fu);
-            const uint32_t q6 = lo4 | (((qh[i] >> l.qsh) & 0x03030303u) << 4);
-            const float ds = (UW == 32 && i >= 4) ? ds1 : ds0;
-            const float2 s2 = make_float2(ds, ds);
-            const float2 f01 = add2(make_float2(magic_byte(q6, 0), magic_byte(q6, 1)), off);
-            const float2 f23 = add2(make_float2(magic_byte(q6, 2), magic_byte(q6, 3)), off);
-            w[2 * i] = mul2(s2, f01);
-            w[2 * i + 1] = mul2(s2, f23);
-        }
-    }
-};
-
-// ============================================================== Q8_0 batch
-//
-// Unit u covers weights e0 = UW*(u % UPB) .. of block u / UPB (UPB = 32/UW
-// units per 34-byte block). The int8 codes become floats through their
-// sign-flipped bytes: 2^23 + (q + 128), minus 2^23 + 128, exactly q; w = d*q
-// is exact in f32.
-template <int M>
-struct Q8B {
-    static constexpr int QK = 32;
-    static constexpr int BLOCK_BYTES = 34;
-    static constexpr int UW = BatchUnit<M>::UW;
-    static constexpr int UPB = QK / UW;
-    static constexpr int SLICE_BLOCKS = 32 / UPB;
-    static constexpr int SLACK = 16;
-    static constexpr bool LIMBS = false;
-    static constexpr int DEFAULT_UNROLL = 1;
-    static constexpr int OUTS = M;
-
-    __host__ __device__ static int units(int nb) { return UPB * nb; }
-    __device__ __forceinline__ static uint32_t unit_byte(int u) { return static_cast<uint32_t>(u / UPB) * BLOCK_BYTES; }
-    __device__ __forceinline__ static int unit_elem(int u) { return (u / UPB) * QK + (u % UPB) * UW; }
-
-    struct L {
-        uint32_t qoff;   // 2 + first weight of the unit in the block
-    };
-    __device__ __forceinline__ static L lane_consts(int u, int, int) {
-        return L{2u + static_cast<uint32_t>((u % UPB) * UW)};
-    }
-
-    // a: shared address of the block (2-byte aligned).
-    __device__ __forceinline__ static void decode(uint32_t a, const L& l, float2 (&w)[UW / 2]) {
-        const float d = f16_lo(lds32<0>(a & ~3u) >> ((a & 3u) * 8u));
-        const uint32_t ca = a + l.qoff;
-        uint32_t q[UW / 4];
-        lds_words_sh<UW>(ca & ~3u, (ca & 3u) * 8u, q);
-        const float2 d2 = make_float2(d, d);
-        const float2 off = make_float2(-(TWO23 + 128.0f), -(TWO23 + 128.0f));
-#pragma unroll
-        for (int i = 0; i < UW / 4; i++) {
-            const uint32_t u8 = q[i] ^ 0x80808080u;   // q + 128 as unsigned bytes
-            const float2 f01 = add2(make_float2(magic_byte(u8, 0), magic_byte(u8, 1)), off);
-            const float2 f23 = add2(make_float2(magic_byte(u8, 2), magic_byte(u8, 3)), off);
-            w[2 * i] = mul2(d2, f01);
-            w[2 * i + 1] = mul2(d2, f23);
-        }
-    }
-};
-
 }  // namespace qmv

@@ -372,14 +372,13 @@ int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const q
     if (moe && slots <= 0) return QMV_EINVAL;
     if (fmt == 16) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, 1, cfg, kp, pl);
     if (fmt == 17) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, slots, cfg, kp, pl);
-    if (fmt >= 13) {
-        // batched: `slots` is the tile's row count of x, 2..8
+    if (fmt == 14 || fmt == 15) return QMV_EINVAL;   // Q6_K and Q8_0 batches run on the tensor cores
+    if (fmt == 13) {
+        // batched Q4_K: `slots` is the tile's row count of x, 2..8
         switch (slots) {
-#define QMM_PLAN(MM)                                                                                    \
-    case MM:                                                                                            \
-        return fmt == 13 ? qmv::make_plan_for<qmv::Q4KB<MM>>(di, rows, k, 1, cfg, kp, pl)              \
-             : fmt == 14 ? qmv::make_plan_for<qmv::Q6KB<MM>>(di, rows, k, 1, cfg, kp, pl)              \
-                         : qmv::make_plan_for<qmv::Q8B<MM>>(di, rows, k, 1, cfg, kp, pl);
+#define QMM_PLAN(MM) \
+    case MM:         \
+        return qmv::make_plan_for<qmv::Q4KB<MM>>(di, rows, k, 1, cfg, kp, pl);
             QMM_PLAN(2) QMM_PLAN(3) QMM_PLAN(4) QMM_PLAN(5) QMM_PLAN(6) QMM_PLAN(7) QMM_PLAN(8)
 #undef QMM_PLAN
         default:

@@ -20,7 +20,7 @@ import pytest
 
 DEVICE = (152, 232448, 233472, 1024)
 FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5, "moe6": 6, "moe4d": 7, "q5k": 8,
-          "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12, "qmm4": 13, "qmm6": 14, "qmm8": 15,
+          "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12, "qmm4": 13,
           "q6d": 16, "moe6d": 17}
 
 
@@ -33,17 +33,11 @@ def batch_uw(m):
 # units per row, a unit's block offset in its slice, and the byte range a
 # unit's loads touch relative to its address a (lo may depend on a & 3).
 def fmt_info(fmt, m=1):
-    if fmt in ("qmm4", "qmm6", "qmm8"):
-        qk, bb = (32, 34) if fmt == "qmm8" else (256, 144 if fmt == "qmm4" else 210)
+    if fmt == "qmm4":
+        qk, bb = 256, 144
         uw = batch_uw(m)
         upb = qk // uw
-        if fmt == "qmm4":
-            extent, align = (lambda a: (a, a + 144)), 16
-        elif fmt == "qmm6":
-            # ql / qh funnel loads, the 8 scale bytes and d, from the word below
-            extent, align = (lambda a: (a - (a & 3), a - (a & 3) + 216)), 2
-        else:
-            extent, align = (lambda a: (a - (a & 3), a - (a & 3) + 40)), 2
+        extent, align = (lambda a: (a, a + 144)), 16
         return dict(qk=qk, bb=bb, sb=32 // upb, units=lambda nb: upb * nb, ubyte=lambda u: (u // upb) * bb,
                     extent=extent, align=align, outs=m)
     if fmt in ("q4k", "moe", "q4d", "moe4d"):
@@ -102,7 +96,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
     CL = P["CL"]
     assert CL in (1, 2, 4, 8) and parts % CL == 0 and (k // 16) % (2 * CL) == 0
     assert P["rq"] >= 1
-    if fmt in ("q8d", "q4d", "moe4d", "qmm4", "qmm6", "qmm8", "q6d", "moe6d"):
+    if fmt in ("q8d", "q4d", "moe4d", "qmm4", "q6d", "moe6d"):
         assert CL == 1
     lg = GS.bit_length() - 1
     rpw = 32 >> lg
@@ -112,7 +106,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
 
     # shared-memory layout: disjoint, ordered regions inside the device limit
     regions = []
-    if fmt not in ("q8d", "q4d", "moe4d", "qmm4", "qmm6", "qmm8", "q6d", "moe6d"):
+    if fmt not in ("q8d", "q4d", "moe4d", "qmm4", "q6d", "moe6d"):
         regions += [(P["off_la"], k), (P["off_lb"], k), (P["off_lc"], k), (P["off_xs"], 4 * (k // 32)),
                     (P["off_xsum16"], 4 * (k // 16))]
         for o, _ in regions:
@@ -252,9 +246,7 @@ def test_moe_forced_plan(q):
 
 
 BATCH_SHAPES = [("qmm4", 4096, 4096), ("qmm4", 300, 768), ("qmm4", 1, 256), ("qmm4", 97, 4352),
-                ("qmm4", 20, 16384), ("qmm6", 4096, 4096), ("qmm6", 300, 512), ("qmm6", 41, 14336),
-                ("qmm6", 3, 256), ("qmm8", 4096, 4096), ("qmm8", 300, 96), ("qmm8", 13, 32), ("qmm8", 64, 11008),
-                ("qmm8", 7, 4160)]
+                ("qmm4", 20, 16384)]
 
 
 @pytest.mark.parametrize("m", [2, 3, 4, 5, 8])
@@ -271,9 +263,17 @@ def test_batch_plans(q, shape, m):
 
 
 @pytest.mark.parametrize("cfg", CFGS[:6])
-@pytest.mark.parametrize("fmt,m", [("qmm4", 2), ("qmm4", 8), ("qmm6", 3), ("qmm8", 5)])
+@pytest.mark.parametrize("fmt,m", [("qmm4", 2), ("qmm4", 3), ("qmm4", 8)])
 def test_batch_forced_plans(q, fmt, m, cfg):
     replay(q, fmt, 61, 512, m, cfg)
+
+
+def test_retired_batch_plan_ids(q):
+    """Q6_K and Q8_0 batches run on the tensor cores: plan ids 14 and 15 are
+    refused."""
+    for fid in (14, 15):
+        with pytest.raises(q.QmvError):
+            q.qmv_plan_detail(fid, 64, 512, 2, None, DEVICE)
 
 
 @pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
