@@ -507,7 +507,9 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
             fence_mbar_init();
             *timeout = 0;
         }
-        __syncwarp();
+    }
+    __syncthreads();   // barriers initialized (each warp then starts its tiles as soon as its x is ready)
+    if (ks == 0) {
         const int first = np < p.S ? np : p.S;
         for (int pi = 0; pi < first; pi++) issue(pi, pi);
         if (lane == 0) *issued = first;
@@ -532,7 +534,6 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
         inv1 = __shfl_sync(FULL, inv, 8 * t + 4);
     };
     load_chunk(0);
-    __syncthreads();   // barriers initialized
 
     float* red = reinterpret_cast<float*>(smem + p.off_red);
     const uint32_t wbase32 = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.w));
