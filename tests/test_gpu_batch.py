@@ -168,3 +168,34 @@ def test_full_batch(q, name):
     fmt = c["kind"][4:]
     y = run_qmm(q, fmt, c["w"], c["x"], c["rows"], c["k"], c["m"])
     check_rows(oracle.qmm(fmt, c["w"], c["x"], c["m"], c["rows"], c["k"]), y)
+
+
+@pytest.mark.parametrize("fmt,rows,k", [("q4k", 37, 2048), ("q6k", 29, 2560), ("q8_0", 41, 1312), ("q8_0", 19, 96)])
+@pytest.mark.parametrize("warps", [1, 2, 3])
+@pytest.mark.parametrize("m", [2, 3, 5, 8])
+def test_batch_kchunks(q, fmt, rows, k, warps, m):
+    """Rows dealt into several k-chunks inside one launch (a warps bound of
+    1-3 slices per chunk; Q8_0 1312 = 41 groups: a ragged last slice and a
+    shorter last chunk), packed (m <= 4) and unpacked."""
+    st = synth.Stream(rows * 7 + k + 31 * warps + m)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    # Q4_K with two rows runs the register kernel: no k-chunks to force
+    cfg = None if (fmt == "q4k" and m == 2) else dict(warps=warps, chunks=2)
+    check_rows(oracle.qmm(fmt, w, x, m, rows, k), run_qmm(q, fmt, w, x, rows, k, m, cfg=cfg))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_batch_kchunk_unit_rows_are_exact(q, fmt):
+    """Unit rows of x through a four-chunk plan still give the decoded weight
+    columns bit for bit (the chunks' partial sums are exact zeros elsewhere)."""
+    rows, k, m = 24, 2048, 4
+    w = synth.GEN_ROWS[fmt](synth.Stream(63), rows, k)
+    W = oracle.dequant(fmt, w, rows, k).astype(np.float32)
+    js = [5, 700, 1300, 2047]
+    x = np.zeros((m, k), dtype=np.float32)
+    for i, j in enumerate(js):
+        x[i, j] = 1.0
+    y = run_qmm(q, fmt, w, x, rows, k, m, cfg=dict(warps=2))
+    for i, j in enumerate(js):
+        assert np.array_equal(y[i], W[:, j]), (i, j)
