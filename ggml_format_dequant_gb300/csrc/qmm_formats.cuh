@@ -1,5 +1,7 @@
-// qmm_formats.cuh -- unit decoders of the small-M batched product
-// y[m, rows] = x[m, k] W^T (2 <= m <= 8 activation rows per launch).
+// qmm_formats.cuh -- the unit decoder of the register-activation batched
+// product y[m, rows] = x[m, k] W^T over Q4_K rows (2 <= m <= 8 activation
+// rows per launch; the entry point uses it for two rows, and Q6_K and Q8_0
+// batches run on the tensor cores, qmm_tc.cuh).
 //
 // Each weight is decoded once per launch and used for all M rows of x. A lane
 // owns UW consecutive weights of a row (a "unit": UW = 8 for M >= 5, 16 for
@@ -10,10 +12,10 @@
 // the dequantizers write -- and forms M dot products with packed f32 pair
 // FMAs (fma.rn.f32x2).
 //
-// Byte layouts and decode rules as in qmv_formats.cuh (hanzo-ml
-// src/vulkan_backend.rs: quantize_q4k, quantize_q6k, quantize_q8_blocks; the
-// batched products are the matmul_q4k_gpu / matmul_q6k_gpu / matmul_q8_gpu
-// prefill GEMMs, which decode each weight once for up to eight rows of x).
+// Byte layout and decode rule as in qmv_formats.cuh (hanzo-ml
+// src/vulkan_backend.rs: quantize_q4k; the batched product is the
+// matmul_q4k_gpu prefill GEMM, which decodes each weight once for up to eight
+// rows of x).
 #pragma once
 
 #include "qmv_formats.cuh"

@@ -272,7 +272,7 @@ inline int qmm_max_tile(int k) {
 // A matvec entry of the same format, for tiles of one row.
 using MatvecFn = int (*)(const void*, const float*, float*, int, int, const qmv_cfg*, cudaStream_t);
 
-// y[m, rows] = x[m, k] W^T for format template FB (one of Q4KB, Q6KB, Q8B):
+// y[m, rows] = x[m, k] W^T for format template FB (Q4KB):
 // ceil(m / tile) balanced tiles of rows of x, one launch each (every launch
 // reads W once); tiles of one row go through the matvec. kp carries w, rows,
 // k, nb, rowbytes, matbytes, wbytes.

@@ -1,7 +1,8 @@
 // qmm_q4k.cu -- small-M batched product y[m, rows] = x[m, k] W^T over packed
-// Q4_K rows (m >= 2; tiles of up to 8 rows of x per launch, fewer when k
-// is large; tiles of one row run the matvec). From three rows of x on, the
-// tensor-core kernel of qmm_tc.cuh takes over.
+// Q4_K rows (m >= 2). Two rows of x: the register-activation kernel of
+// qmm_kernel.cuh (one launch, or two of one row each when k is too large for
+// one); from three rows on, the tensor-core kernel of qmm_tc.cuh, one launch
+// per tile of up to 8 rows.
 #include "qmv_internal.h"
 #include "qmm_kernel.cuh"
 #include "qmm_tc.cuh"
