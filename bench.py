@@ -80,7 +80,8 @@ def measured_peak():
 KIND_FMT = {"q4k": "q4k", "q4k_dp4a": "q4k", "q6k": "q6k", "q6k_dp4a": "q6k", "moe_q6k_dp4a": "q6k",
             "q8_0_dp4a": "q8_0", "q5k": "q5k", "q4_0": "q4_0",
             "moe_q4k": "q4k", "moe_q4k_dp4a": "q4k", "moe_q6k": "q6k", "moe_q8_0": "q8_0", "moe_q4_0": "q4_0",
-            "moe_q5k": "q5k", "qmm_q4k": "q4k", "qmm_q6k": "q6k", "qmm_q8_0": "q8_0"}
+            "moe_q5k": "q5k", "qmm_q4k": "q4k", "qmm_q6k": "q6k", "qmm_q8_0": "q8_0",
+            "qmm_q5k": "q5k", "qmm_q4_0": "q4_0"}
 # MoE kinds with an f32 activation (one entry point each, same arguments).
 MOE_F32 = ("moe_q4k", "moe_q6k", "moe_q8_0", "moe_q4_0", "moe_q5k")
 

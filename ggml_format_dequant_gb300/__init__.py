@@ -87,6 +87,10 @@ _SIG = {
     "qmm_q6k_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q8_0": [_P, _P, _P, _I, _I, _I, _P],
     "qmm_q8_0_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q5k": [_P, _P, _P, _I, _I, _I, _P],
+    "qmm_q5k_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q4_0": [_P, _P, _P, _I, _I, _I, _P],
+    "qmm_q4_0_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmv_q5k": [_P, _P, _P, _I, _I, _P],
     "qmv_q5k_cfg": [_P, _P, _P, _I, _I, _P, _P],
     "qmv_q4_0": [_P, _P, _P, _I, _I, _P],
@@ -207,6 +211,14 @@ def qmm_q8_0(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
     return _qmm("qmm_q8_0", w, x, y, rows, k, m, stream, cfg, check)
 
 
+def qmm_q5k(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
+    return _qmm("qmm_q5k", w, x, y, rows, k, m, stream, cfg, check)
+
+
+def qmm_q4_0(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
+    return _qmm("qmm_q4_0", w, x, y, rows, k, m, stream, cfg, check)
+
+
 def qmm_launches(fmt, k, m) -> int:
     """Kernel launches one qmm_<fmt> call makes: the matvec for m = 1; for
     Q4_K and m = 2 the register kernel, ceil(m / tile) launches with the widest
@@ -216,7 +228,7 @@ def qmm_launches(fmt, k, m) -> int:
     if m == 1:
         return 1
     if m >= 3 or fmt != "q4k":
-        return -(-m // 8)
+        return -(-m // 8)   # the tensor-core kernel (Q6_K, Q8_0, Q5_K, Q4_0 from m = 2 on)
     return 1 if (k // 256) * 8 <= 512 else 2
 
 

@@ -249,6 +249,55 @@ __device__ __forceinline__ void tc_load_x(const float* src, bool live, int ng, b
 // shared address of the lane's min-term fragments; y4: the row sums of (g,
 // 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1) in the slice's scaled units.
 
+// Shared by Q4_K and Q5_K, whose 16-byte block headers are alike: d, dmin
+// (f16) and the twelve bytes of six-bit scales and mins.
+struct KHead {
+    uint32_t s_lo, s_hi, m_lo, m_hi;   // sc / m of sub-blocks 0-3 (lo) and 4-7 (hi), one a byte
+    float d, dmin;
+    __device__ __forceinline__ explicit KHead(uint4 h)
+        : s_lo(h.y & 0x3f3f3f3fu),
+          s_hi((h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u)),
+          m_lo(h.z & 0x3f3f3f3fu),
+          m_hi(((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u)),
+          d(f16_lo(h.x)),
+          dmin(f16_hi(h.x)) {}
+    // D * sc_j exactly (sc_j as the float 2^23 + sc_j), D a scaled d.
+    __device__ __forceinline__ float dsc(float D, int j) const {
+        const uint32_t sel = 0x7440u | static_cast<uint32_t>(j & 3);
+        return __fmaf_rn(D, __uint_as_float(prmt(j < 4 ? s_lo : s_hi, 0x4B000000u, sel)), -D * TWO23);
+    }
+};
+
+// The min term, y4 -= dmin * sum_j m_j S_j for rows g and g + 8, as one more
+// product: A' = the m_j as f16 pairs (groups 0,1 | 2,3 | 4,5 | 6,7), B' = the
+// lane's partial group sums (times 1/8; packed in xf.sh, else hi and lo at
+// the shared address sums).
+template <bool P>
+__device__ __forceinline__ void k_min_term(const KHead& a, const KHead& b, const XFrag& xf, uint32_t sums,
+                                           float (&y4)[4]) {
+    const uint32_t one = 0x64006400u;
+    const uint32_t m01a = hsub2(prmt(a.m_lo, 0x64646464u, 0x4140u), one);
+    const uint32_t m23a = hsub2(prmt(a.m_lo, 0x64646464u, 0x4342u), one);
+    const uint32_t m45a = hsub2(prmt(a.m_hi, 0x64646464u, 0x4140u), one);
+    const uint32_t m67a = hsub2(prmt(a.m_hi, 0x64646464u, 0x4342u), one);
+    const uint32_t m01b = hsub2(prmt(b.m_lo, 0x64646464u, 0x4140u), one);
+    const uint32_t m23b = hsub2(prmt(b.m_lo, 0x64646464u, 0x4342u), one);
+    const uint32_t m45b = hsub2(prmt(b.m_hi, 0x64646464u, 0x4140u), one);
+    const uint32_t m67b = hsub2(prmt(b.m_hi, 0x64646464u, 0x4342u), one);
+    float Dm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (P) {
+        mma16816(Dm, m01a, m01b, m23a, m23b, xf.sh[0], xf.sh[1]);
+        mma16816(Dm, m45a, m45b, m67a, m67b, xf.sh[2], xf.sh[3]);
+    } else {
+        const uint4 sh = lds128<0>(sums), sl = lds128<16>(sums);
+        mma16816(Dm, m01a, m01b, m23a, m23b, sh.x, sh.y);
+        mma16816(Dm, m01a, m01b, m23a, m23b, sl.x, sl.y);
+        mma16816(Dm, m45a, m45b, m67a, m67b, sh.z, sh.w);
+        mma16816(Dm, m45a, m45b, m67a, m67b, sl.z, sl.w);
+    }
+    fold(y4, Dm, -8.0f * a.dmin, -8.0f * b.dmin);
+}
+
 // Q4_K: a slice is one 144-byte block; group j = sub-block j. The code bytes
 // of a lane's positions in chunk c (sub-blocks 2c, 2c+1) are qs[32c + 4t ..]
 // and qs[32c + 16 + 4t ..]: low nibbles sub-block 2c, high nibbles 2c + 1.
@@ -263,45 +312,12 @@ struct Q4KT {
                                                  uint32_t sums, float (&y4)[4]) {
         const uint32_t ba = ra + static_cast<uint32_t>(ks) * BLOCK_BYTES;
         const uint32_t bb = rb + static_cast<uint32_t>(ks) * BLOCK_BYTES;
-        const uint4 ha = lds128<0>(ba);
-        const uint4 hb = lds128<0>(bb);
-        // six-bit scales (sc) and mins (m) of sub-blocks 0-3 (lo) and 4-7 (hi)
-        const uint32_t sa_lo = ha.y & 0x3f3f3f3fu, ma_lo = ha.z & 0x3f3f3f3fu;
-        const uint32_t sa_hi = (ha.w & 0x0f0f0f0fu) | ((ha.y >> 2) & 0x30303030u);
-        const uint32_t ma_hi = ((ha.w >> 4) & 0x0f0f0f0fu) | ((ha.z >> 2) & 0x30303030u);
-        const uint32_t sb_lo = hb.y & 0x3f3f3f3fu, mb_lo = hb.z & 0x3f3f3f3fu;
-        const uint32_t sb_hi = (hb.w & 0x0f0f0f0fu) | ((hb.y >> 2) & 0x30303030u);
-        const uint32_t mb_hi = ((hb.w >> 4) & 0x0f0f0f0fu) | ((hb.z >> 2) & 0x30303030u);
-        // The min term first (its operands then die) as one more product, A' =
-        // the m_j as f16 pairs (groups 0,1 | 2,3 | 4,5 | 6,7).
-        {
-            const uint32_t one = 0x64006400u;
-            const uint32_t m01a = hsub2(prmt(ma_lo, 0x64646464u, 0x4140u), one);
-            const uint32_t m23a = hsub2(prmt(ma_lo, 0x64646464u, 0x4342u), one);
-            const uint32_t m45a = hsub2(prmt(ma_hi, 0x64646464u, 0x4140u), one);
-            const uint32_t m67a = hsub2(prmt(ma_hi, 0x64646464u, 0x4342u), one);
-            const uint32_t m01b = hsub2(prmt(mb_lo, 0x64646464u, 0x4140u), one);
-            const uint32_t m23b = hsub2(prmt(mb_lo, 0x64646464u, 0x4342u), one);
-            const uint32_t m45b = hsub2(prmt(mb_hi, 0x64646464u, 0x4140u), one);
-            const uint32_t m67b = hsub2(prmt(mb_hi, 0x64646464u, 0x4342u), one);
-            float Dm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (P) {
-                mma16816(Dm, m01a, m01b, m23a, m23b, xf.sh[0], xf.sh[1]);
-                mma16816(Dm, m45a, m45b, m67a, m67b, xf.sh[2], xf.sh[3]);
-            } else {
-                const uint4 sh = lds128<0>(sums), sl = lds128<16>(sums);
-                mma16816(Dm, m01a, m01b, m23a, m23b, sh.x, sh.y);
-                mma16816(Dm, m01a, m01b, m23a, m23b, sl.x, sl.y);
-                mma16816(Dm, m45a, m45b, m67a, m67b, sh.z, sh.w);
-                mma16816(Dm, m45a, m45b, m67a, m67b, sl.z, sl.w);
-            }
-            // the partial sums carry a factor 1/8
-            fold(y4, Dm, -8.0f * f16_hi(ha.x), -8.0f * f16_hi(hb.x));
-        }
+        const KHead A(lds128<0>(ba)), B(lds128<0>(bb));
+        k_min_term<P>(A, B, xf, sums, y4);   // first: its operands then die
         // d * 2^24 for the low nibbles (q * 2^-24), d * 2^20 for the high ones
         // (16 q * 2^-24), exactly
-        const float da0 = f16_lo(ha.x) * TWO24, da1 = f16_lo(ha.x) * (TWO24 / 16.0f);
-        const float db0 = f16_lo(hb.x) * TWO24, db1 = f16_lo(hb.x) * (TWO24 / 16.0f);
+        const float da0 = A.d * TWO24, da1 = A.d * (TWO24 / 16.0f);
+        const float db0 = B.d * TWO24, db1 = B.d * (TWO24 / 16.0f);
 #pragma unroll
         for (int c = 0; c < 4; c++) {
             const uint32_t off = 16u + 32u * c + 4u * static_cast<uint32_t>(t);
@@ -320,12 +336,61 @@ struct Q4KT {
                               xf.l[j][0], xf.l[j][1]);
                 mma_half_a<P>(D, wa1 & me, wb1 & me, (wa1 >> 8) & me, (wb1 >> 8) & me, xf.h[j][2], xf.h[j][3],
                               xf.l[j][2], xf.l[j][3]);
-                // (d scaled) * sc_j, exactly: sc_j as the float 2^23 + sc_j
-                const float da = h ? da1 : da0, db = h ? db1 : db0;
-                const uint32_t sel = 0x7440u | static_cast<uint32_t>(j & 3);
-                const float dsa = __fmaf_rn(da, __uint_as_float(prmt(j < 4 ? sa_lo : sa_hi, 0x4B000000u, sel)), -da * TWO23);
-                const float dsb = __fmaf_rn(db, __uint_as_float(prmt(j < 4 ? sb_lo : sb_hi, 0x4B000000u, sel)), -db * TWO23);
-                fold(y4, D, dsa, dsb);
+                fold(y4, D, A.dsc(h ? da1 : da0, j), B.dsc(h ? db1 : db0, j));
+            }
+        }
+    }
+};
+
+// Q5_K: a slice is one 176-byte block: the Q4_K header, qh[32] at 16 and
+// qs[128] at 48. Sub-block j's five-bit code at position l is nibble j % 2 of
+// qs[32 (j / 2) + l] plus 16 times bit j of qh[l]; a lane's positions are l =
+// 4t.. and 16 + 4t.. as for Q4_K.
+struct Q5KT {
+    static constexpr int QK = 256;
+    static constexpr int BLOCK_BYTES = 176;
+    static constexpr int SLACK = 0;
+    static constexpr bool SUMS = true;
+
+    // Four code bytes (q <= 31) of sub-block j: nibble j % 2 of w, bit j of
+    // qh moved to bit 4 (j is a constant once the loops are unrolled).
+    __device__ __forceinline__ static uint32_t codes(uint32_t w, uint32_t qh, int j) {
+        const uint32_t nib = (j & 1) ? (w >> 4) & 0x0f0f0f0fu : w & 0x0f0f0f0fu;
+        const uint32_t top = (j <= 4 ? qh << (4 - j) : qh >> (j - 4)) & 0x10101010u;
+        return nib | top;
+    }
+
+    template <bool P>
+    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int, int t, const XFrag& xf,
+                                                 uint32_t sums, float (&y4)[4]) {
+        const uint32_t ba = ra + static_cast<uint32_t>(ks) * BLOCK_BYTES;
+        const uint32_t bb = rb + static_cast<uint32_t>(ks) * BLOCK_BYTES;
+        const KHead A(lds128<0>(ba)), B(lds128<0>(bb));
+        k_min_term<P>(A, B, xf, sums, y4);
+        const uint32_t lt = 4u * static_cast<uint32_t>(t);
+        const uint32_t qha0 = lds32<16>(ba + lt), qha1 = lds32<32>(ba + lt);
+        const uint32_t qhb0 = lds32<16>(bb + lt), qhb1 = lds32<32>(bb + lt);
+        // d * 2^24: the codes enter as the f16 subnormals q * 2^-24
+        const float da = A.d * TWO24, db = B.d * TWO24;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const uint32_t off = 48u + 32u * c + lt;
+            const uint32_t wa0 = lds32<0>(ba + off), wa1 = lds32<16>(ba + off);
+            const uint32_t wb0 = lds32<0>(bb + off), wb1 = lds32<16>(bb + off);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int j = 2 * c + h;
+                const uint32_t ca0 = codes(wa0, qha0, j), ca1 = codes(wa1, qha1, j);
+                const uint32_t cb0 = codes(wb0, qhb0, j), cb1 = codes(wb1, qhb1, j);
+                // bytes 0 and 2 (even columns) by a mask, 1 and 3 by a shift
+                // and a mask: f16 subnormals q * 2^-24
+                const uint32_t me = 0x00ff00ffu;
+                float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                mma_half_a<P>(D, ca0 & me, cb0 & me, (ca0 >> 8) & me, (cb0 >> 8) & me, xf.h[j][0], xf.h[j][1],
+                              xf.l[j][0], xf.l[j][1]);
+                mma_half_a<P>(D, ca1 & me, cb1 & me, (ca1 >> 8) & me, (cb1 >> 8) & me, xf.h[j][2], xf.h[j][3],
+                              xf.l[j][2], xf.l[j][3]);
+                fold(y4, D, A.dsc(da, j), B.dsc(db, j));
             }
         }
     }
@@ -417,6 +482,39 @@ struct Q8T {
                 float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 mma_half<P>(D, ka0, kb0, bias, xf.h[j][0], xf.h[j][1], xf.l[j][0], xf.l[j][1]);
                 mma_half<P>(D, ka1, kb1, bias, xf.h[j][2], xf.h[j][3], xf.l[j][2], xf.l[j][3]);
+                fold(y4, D, da, db);
+            }
+        }
+    }
+};
+
+// Q4_0: a slice is 8 consecutive 18-byte blocks (2-byte aligned), one per
+// group: d, then qs[16] whose byte l carries position l in its low nibble and
+// position 16 + l in its high nibble; a lane's bytes are qs[4t .. 4t + 3]
+// (bias 1024 + 8: the codes become q - 8).
+struct Q40T {
+    static constexpr int QK = 32;
+    static constexpr int BLOCK_BYTES = 18;
+    static constexpr int SLACK = 16;
+    static constexpr bool SUMS = false;
+
+    template <bool P>
+    __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int ng, int t, const XFrag& xf,
+                                                 uint32_t, float (&y4)[4]) {
+        const uint32_t bias = 0x64086408u;
+        const uint32_t lt = 4u * static_cast<uint32_t>(t);
+#pragma unroll
+        for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
+            if (j < ng) {
+                const uint32_t off = static_cast<uint32_t>(ks * TC_GROUPS_PER_SLICE + j) * BLOCK_BYTES;
+                const uint32_t ba = ra + off, bb = rb + off;
+                const float da = f16_lo(lds32_a2(ba)), db = f16_lo(lds32_a2(bb));
+                const uint32_t wa = lds32_a2(ba + 2u + lt), wb = lds32_a2(bb + 2u + lt);
+                float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                mma_half<P>(D, wa & 0x0f0f0f0fu, wb & 0x0f0f0f0fu, bias, xf.h[j][0], xf.h[j][1], xf.l[j][0],
+                            xf.l[j][1]);
+                mma_half<P>(D, (wa >> 4) & 0x0f0f0f0fu, (wb >> 4) & 0x0f0f0f0fu, bias, xf.h[j][2], xf.h[j][3],
+                            xf.l[j][2], xf.l[j][3]);
                 fold(y4, D, da, db);
             }
         }

@@ -130,6 +130,32 @@ int qmm_q8_0(const void* w, const float* x, float* y, int rows, int k, int m, cu
     return qmm_q8_0_cfg(w, x, y, rows, k, m, nullptr, stream);
 }
 
+int qmm_q5k_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+                 cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 176);
+    if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
+        rc = QMV_EINVAL;
+    if (rc) return rc;
+    return m == 1 ? qmvi::q5k(w, x, y, rows, k, cfg, stream) : qmvi::qmm_q5k(w, x, y, rows, k, m, cfg, stream);
+}
+
+int qmm_q5k(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
+    return qmm_q5k_cfg(w, x, y, rows, k, m, nullptr, stream);
+}
+
+int qmm_q4_0_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+                  cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 32, 18);
+    if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
+        rc = QMV_EINVAL;
+    if (rc) return rc;
+    return m == 1 ? qmvi::q4_0(w, x, y, rows, k, cfg, stream) : qmvi::qmm_q4_0(w, x, y, rows, k, m, cfg, stream);
+}
+
+int qmm_q4_0(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
+    return qmm_q4_0_cfg(w, x, y, rows, k, m, nullptr, stream);
+}
+
 int quantize_act_q8(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t stream) {
     if (!x || !xq || !xs) return QMV_EINVAL;
     if (m <= 0 || k <= 0 || k % 32) return QMV_EINVAL;
@@ -460,6 +486,8 @@ int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_cfg* cfg, cons
     case 0: rc = qmv::make_tc_plan_for<qmv::Q4KT>(di, rows, k, m, cfg, &tp, &pl); break;
     case 1: rc = qmv::make_tc_plan_for<qmv::Q6KT>(di, rows, k, m, cfg, &tp, &pl); break;
     case 2: rc = qmv::make_tc_plan_for<qmv::Q8T>(di, rows, k, m, cfg, &tp, &pl); break;
+    case 3: rc = qmv::make_tc_plan_for<qmv::Q5KT>(di, rows, k, m, cfg, &tp, &pl); break;
+    case 4: rc = qmv::make_tc_plan_for<qmv::Q40T>(di, rows, k, m, cfg, &tp, &pl); break;
     default: rc = QMV_EINVAL;
     }
     if (rc) return rc;

@@ -38,6 +38,7 @@ int q5k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
 int moe_q5k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
             int n_experts, const qmv_cfg* cfg, cudaStream_t s);
 int dequant_q5k(const void* w, float* out, int rows, int k, cudaStream_t s);
+int qmm_q5k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s);
 int status_q5k(unsigned int* out, int clear);
 
 // qmv_q4_0.cu
@@ -45,6 +46,7 @@ int q4_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg
 int moe_q4_0(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
              int n_experts, const qmv_cfg* cfg, cudaStream_t s);
 int dequant_q4_0(const void* w, float* out, int rows, int k, cudaStream_t s);
+int qmm_q4_0(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s);
 int status_q4_0(unsigned int* out, int clear);
 
 // qmv_q8.cu

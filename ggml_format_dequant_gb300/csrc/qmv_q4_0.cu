@@ -1,7 +1,8 @@
-// qmv_q4_0.cu -- Q4_0 dense and MoE matvec launches, and the Q4_0 dequantizer
-// used by the tests.
+// qmv_q4_0.cu -- Q4_0 dense and MoE matvec launches, the small-M batched
+// product, and the Q4_0 dequantizer used by the tests.
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
+#include "qmm_tc.cuh"
 
 namespace {
 
@@ -70,6 +71,12 @@ int dequant_q4_0(const void* w, float* out, int rows, int k, cudaStream_t s) {
     const int blocks = static_cast<int>(want < 65536 ? (want > 0 ? want : 1) : 65536);
     dequant_q4_0_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint8_t*>(w), out, nblk);
     return cuda_rc(cudaGetLastError());
+}
+
+// Small-M batched product y[m, rows] = x[m, k] W^T, m >= 2: the
+// tensor-core kernel of qmm_tc.cuh, one launch per tile of up to 8 rows of x.
+int qmm_q4_0(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s) {
+    return qmm_tc_run<Q40T>(w, x, y, rows, k, m, cfg, s);
 }
 
 int status_q4_0(unsigned int* out, int clear) { return status_rw(out, clear); }

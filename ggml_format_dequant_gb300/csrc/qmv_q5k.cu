@@ -1,7 +1,8 @@
-// qmv_q5k.cu -- Q5_K dense and MoE matvec launches, and the Q5_K dequantizer
-// used by the tests.
+// qmv_q5k.cu -- Q5_K dense and MoE matvec launches, the small-M batched
+// product, and the Q5_K dequantizer used by the tests.
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
+#include "qmm_tc.cuh"
 
 namespace {
 
@@ -89,6 +90,12 @@ int dequant_q5k(const void* w, float* out, int rows, int k, cudaStream_t s) {
     const int blocks = static_cast<int>(want < 65536 ? want : 65536);
     dequant_q5k_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint8_t*>(w), out, nsub);
     return cuda_rc(cudaGetLastError());
+}
+
+// Small-M batched product y[m, rows] = x[m, k] W^T, m >= 2: the
+// tensor-core kernel of qmm_tc.cuh, one launch per tile of up to 8 rows of x.
+int qmm_q5k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s) {
+    return qmm_tc_run<Q5KT>(w, x, y, rows, k, m, cfg, s);
 }
 
 int status_q5k(unsigned int* out, int clear) { return status_rw(out, clear); }

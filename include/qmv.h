@@ -100,6 +100,11 @@ int qmv_q4_0(const void *w, const float *x, float *y, int rows, int k, cudaStrea
 int qmm_q4k(const void *w, const float *x, float *y, int rows, int k, int m, cudaStream_t stream);
 int qmm_q6k(const void *w, const float *x, float *y, int rows, int k, int m, cudaStream_t stream);
 int qmm_q8_0(const void *w, const float *x, float *y, int rows, int k, int m, cudaStream_t stream);
+/* The same product over Q5_K and Q4_0 rows (w and k as for qmv_q5k /
+ * qmv_q4_0): m == 1 runs the matvec, m >= 2 the tensor-core kernel.
+ * Cites hanzo-ml src/vulkan_backend.rs, matmul_q5k_gpu / matmul_q4_0_gpu. */
+int qmm_q5k(const void *w, const float *x, float *y, int rows, int k, int m, cudaStream_t stream);
+int qmm_q4_0(const void *w, const float *x, float *y, int rows, int k, int m, cudaStream_t stream);
 
 /* Activation quantization for the dp4a path, per 32-element block of x[m, k]:
  * amax = max|x|; inv = 127/amax and d = amax/127 (IEEE f32 divides);
@@ -289,6 +294,10 @@ int qmm_q6k_cfg(const void *w, const float *x, float *y, int rows, int k, int m,
                 cudaStream_t stream);
 int qmm_q8_0_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
                  cudaStream_t stream);
+int qmm_q5k_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
+                cudaStream_t stream);
+int qmm_q4_0_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
+                 cudaStream_t stream);
 int qmv_q5k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
                 cudaStream_t stream);
 int qmv_q4_0_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
@@ -353,12 +362,12 @@ int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, con
 
 /* The tensor-core plan of the batched product for one tile of m (1..8) rows
  * of x on a described device (as for qmv_plan_detail). fmt: 0 = Q4_K,
- * 1 = Q6_K, 2 = Q8_0. out receives QMM_TC_PLAN_FIELDS ints: threads, ctas,
+ * 1 = Q6_K, 2 = Q8_0, 3 = Q5_K, 4 = Q4_0. out receives QMM_TC_PLAN_FIELDS ints: threads, ctas,
  * dynamic shared bytes, warps (k-slices of 256 weights per k-chunk), rows per
  * ring slot, ring slots, bytes of one row's k-chunk, shared row stride, slot
  * stride, rows per CTA (q, rem), 32-weight groups per row, k-chunks, shared
- * offsets of the parked partials, the min-term fragments (Q4_K, 32 bytes a
- * thread; none for the other formats), the ring, the barriers and the
+ * offsets of the parked partials, the min-term fragments (Q4_K and Q5_K, 32
+ * bytes a thread; none for the other formats), the ring, the barriers and the
  * counters. */
 #define QMM_TC_PLAN_FIELDS 18
 int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_cfg *cfg, const int *device, int *out);

@@ -229,6 +229,8 @@ CONFIGS = {
     "qmm_q4k_4096x4096_m8": dict(kind="qmm_q4k", rows=4096, k=4096, seed=1, m=8),
     "qmm_q6k_4096x14336_m4": dict(kind="qmm_q6k", rows=4096, k=14336, seed=4, m=4),
     "qmm_q8_0_14336x4096_m8": dict(kind="qmm_q8_0", rows=14336, k=4096, seed=2, m=8),
+    "qmm_q5k_4096x4096_m4": dict(kind="qmm_q5k", rows=4096, k=4096, seed=6, m=4),
+    "qmm_q4_0_4096x4096_m4": dict(kind="qmm_q4_0", rows=4096, k=4096, seed=7, m=4),
 }
 
 

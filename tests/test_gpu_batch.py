@@ -1,5 +1,6 @@
 """GPU parity of the small-M batched product y[m, rows] = x[m, k] W^T
-(qmm_q4k, qmm_q6k, qmm_q8_0) against the CPU oracle, through the C ABI.
+(qmm_q4k, qmm_q6k, qmm_q8_0, qmm_q5k, qmm_q4_0) against the CPU oracle,
+through the C ABI.
 
 Bars: x rows that are unit vectors give y rows equal to the decoded weight
 columns bit for bit; otherwise every row of y is within scale-relative error
@@ -17,7 +18,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 SCALE_REL_TOL = 1e-4
-FMTS = ["q4k", "q6k", "q8_0"]
+FMTS = ["q4k", "q6k", "q8_0", "q5k", "q4_0"]
 
 
 @pytest.fixture(scope="module")
@@ -59,7 +60,9 @@ def check_rows(ref, y):
 
 SHAPES = [("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 4352), ("q4k", 64, 4096), ("q4k", 20, 16384),
           ("q6k", 300, 512), ("q6k", 3, 256), ("q6k", 41, 14336), ("q6k", 130, 2816),
-          ("q8_0", 300, 96), ("q8_0", 13, 32), ("q8_0", 7, 4096), ("q8_0", 64, 11008), ("q8_0", 5, 4160)]
+          ("q8_0", 300, 96), ("q8_0", 13, 32), ("q8_0", 7, 4096), ("q8_0", 64, 11008), ("q8_0", 5, 4160),
+          ("q5k", 300, 768), ("q5k", 3, 256), ("q5k", 97, 4352), ("q5k", 20, 16384), ("q4_0", 300, 96),
+          ("q4_0", 13, 32), ("q4_0", 64, 11008), ("q4_0", 5, 4160)]
 
 
 @pytest.mark.parametrize("m", [2, 3, 4, 5, 8])
@@ -105,7 +108,7 @@ def test_batch_unit_rows_are_exact(q, fmt):
 @pytest.mark.parametrize("cfg", [dict(ctas=1, chunk_rows=1, chunks=2), dict(ctas=3, chunk_rows=5, chunks=2),
                                  dict(ctas=2, chunk_rows=3, chunks=1), dict(ctas=7, chunks=3),
                                  dict(ctas=2, chunks=1, warps=4), dict(ctas=1, chunk_rows=7, chunks=2, warps=16)])
-@pytest.mark.parametrize("fmt,m", [("q4k", 2), ("q4k", 8), ("q6k", 3), ("q8_0", 5)])
+@pytest.mark.parametrize("fmt,m", [("q4k", 2), ("q4k", 8), ("q6k", 3), ("q8_0", 5), ("q5k", 4), ("q5k", 8), ("q4_0", 6)])
 def test_batch_forced_pipelines(q, fmt, m, cfg):
     rows, k = 61, 512
     st = synth.Stream(71 + m)
@@ -162,7 +165,7 @@ def test_batch_overlap_modes_give_identical_results(q):
 
 
 @pytest.mark.parametrize("name", ["qmm_q4k_4096x4096_m8", "qmm_q4k_4096x4096_m2", "qmm_q6k_4096x14336_m4",
-                                  "qmm_q8_0_14336x4096_m8"])
+                                  "qmm_q8_0_14336x4096_m8", "qmm_q5k_4096x4096_m4", "qmm_q4_0_4096x4096_m4"])
 def test_full_batch(q, name):
     c = synth.make_config(name)
     fmt = c["kind"][4:]
@@ -170,7 +173,8 @@ def test_full_batch(q, name):
     check_rows(oracle.qmm(fmt, c["w"], c["x"], c["m"], c["rows"], c["k"]), y)
 
 
-@pytest.mark.parametrize("fmt,rows,k", [("q4k", 37, 2048), ("q6k", 29, 2560), ("q8_0", 41, 1312), ("q8_0", 19, 96)])
+@pytest.mark.parametrize("fmt,rows,k", [("q4k", 37, 2048), ("q6k", 29, 2560), ("q8_0", 41, 1312), ("q8_0", 19, 96),
+                                        ("q5k", 23, 2304), ("q4_0", 31, 1568)])
 @pytest.mark.parametrize("warps", [1, 2, 3])
 @pytest.mark.parametrize("m", [2, 3, 5, 8])
 def test_batch_kchunks(q, fmt, rows, k, warps, m):

@@ -306,7 +306,7 @@ def test_planner_rejects(q):
 
 # ------------------------------------------- tensor-core batch plan (qmm_tc)
 
-TC_FMT = {"q4k": (0, 256, 144), "q6k": (1, 256, 210), "q8_0": (2, 32, 34)}
+TC_FMT = {"q4k": (0, 256, 144), "q6k": (1, 256, 210), "q8_0": (2, 32, 34), "q5k": (3, 256, 176), "q4_0": (4, 32, 18)}
 
 
 def tc_max_read(fmt, slices, groups):
@@ -314,8 +314,12 @@ def tc_max_read(fmt, slices, groups):
     row's k-chunk of `slices` slices and `groups` groups."""
     if fmt == "q4k":
         return slices * 144
+    if fmt == "q5k":
+        return slices * 176
     if fmt == "q6k":
         return (slices - 1) * 210 + 216   # funnel loads of d at 208: 8 bytes from the word below
+    if fmt == "q4_0":
+        return (groups - 1) * 18 + 22     # codes at 2 + 4t: 8 bytes from the word below
     return (groups - 1) * 34 + 38          # codes at 18 + 4t: 8 bytes from the word below
 
 
@@ -338,7 +342,7 @@ def tc_replay(q, fmt, rows, k, m, cfg=None):
     assert P["slot_stride"] >= cap * stride and P["slot_stride"] % 128 == 0
     assert P["rq"] * parts + P["rrem"] == rows and P["rq"] >= 1
     rpc = P["rq"] + (1 if P["rrem"] else 0)
-    sums = 32 * 32 * KS if fmt == "q4k" else 0   # 32 bytes a thread (Q4_K min-term fragments)
+    sums = 32 * 32 * KS if fmt in ("q4k", "q5k") else 0   # 32 bytes a thread (min-term fragments)
     regions = [(P["off_red"], 4 * rpc * KS * 8), (P["off_sums"], sums), (P["off_ring"], S * P["slot_stride"]),
                (P["off_bars"], 8 * S), (P["off_cnt"], 4 * (S + 2))]
     regions.sort()
@@ -386,7 +390,9 @@ def tc_replay(q, fmt, rows, k, m, cfg=None):
 TC_SHAPES = [("q4k", 4096, 4096), ("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97, 2304), ("q6k", 4096, 4096),
              ("q6k", 300, 512), ("q6k", 3, 256), ("q6k", 41, 3840), ("q8_0", 14336, 4096), ("q8_0", 300, 96),
              ("q8_0", 13, 32), ("q8_0", 7, 4064), ("q8_0", 64, 1056), ("q4k", 20, 16384), ("q4k", 97, 4352),
-             ("q6k", 4096, 14336), ("q6k", 41, 14336), ("q8_0", 64, 11008), ("q8_0", 5, 4160), ("q8_0", 3, 12320)]
+             ("q6k", 4096, 14336), ("q6k", 41, 14336), ("q8_0", 64, 11008), ("q8_0", 5, 4160), ("q8_0", 3, 12320),
+             ("q5k", 4096, 4096), ("q5k", 37, 512), ("q5k", 3, 4352), ("q5k", 1, 256), ("q4_0", 4096, 4096),
+             ("q4_0", 300, 96), ("q4_0", 13, 32), ("q4_0", 64, 11008), ("q4_0", 7, 4160)]
 
 
 @pytest.mark.parametrize("m", [1, 2, 5, 8])
@@ -400,7 +406,7 @@ def test_tc_plans(q, shape, m):
                                  dict(ctas=2, chunk_rows=20, chunks=1), dict(ctas=7, chunks=3),
                                  dict(ctas=1, chunk_rows=16, chunks=2), dict(ctas=2, chunks=2, warps=1),
                                  dict(ctas=3, chunk_rows=7, chunks=3, warps=3)])
-@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q5k", "q4_0"])
 def test_tc_forced_plans(q, fmt, cfg):
     tc_replay(q, fmt, 61, 512, 3, cfg)
 
