@@ -740,12 +740,14 @@ inline uint32_t tc_row_stride(uint32_t rowbytes, int slack) {
     return s + ((16u + 128u - (s & 127u)) & 127u);
 }
 
-// Launch plan for m (1..8) rows of x on a device described by di. The k-slices
-// of a row (8 groups each) are dealt into the fewest k-chunks of at most
-// MAX_WARPS slices (cfg->warps, when given, lowers that bound), balanced; a
-// chunk's slices are the CTA's warps.
+// Launch plan for m (1..8) rows of x on a device described by di, in at most
+// smem_cap bytes of shared memory a CTA. The k-slices of a row (8 groups
+// each) are dealt into the fewest k-chunks of at most MAX_WARPS slices
+// (cfg->warps, when given, lowers that bound), balanced; a chunk's slices are
+// the CTA's warps.
 template <class F>
-inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv_cfg* cfg, TParams* tp, Plan* pl) {
+inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qmv_cfg* cfg, long long smem_cap,
+                             TParams* tp, Plan* pl) {
     if (m < 1 || m > TC_COLS || rows <= 0 || k <= 0 || k % F::QK) return QMV_EINVAL;
     const int ngroups = k / 32;
     const int NS = (ngroups + TC_GROUPS_PER_SLICE - 1) / TC_GROUPS_PER_SLICE;
@@ -757,7 +759,7 @@ inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv
     if (rowbytes > 0x7fffffffLL) return QMV_ETOOBIG;
     const uint32_t stride = tc_row_stride(static_cast<uint32_t>(std::min(chunk_bytes, rowbytes)), F::SLACK);
     const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
-    const long long full = di.smem_optin;
+    const long long full = std::min<long long>(smem_cap, di.smem_optin);
 
     int parts = (cfg && cfg->ctas > 0) ? cfg->ctas : di.nsm;
     if (!(cfg && cfg->ctas > 0)) {
@@ -814,6 +816,35 @@ inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv
         if (parts >= rows) return QMV_ETOOBIG;
         parts = std::min(rows, parts * 2);   // fewer rows per CTA, smaller tables
     }
+}
+
+// Warps a CTA of independent calls takes at most: 256 threads of 128
+// registers fill half an SM's register file.
+constexpr int TC_WARPS_HALF_SM = 8;
+
+// The plan used. Independent calls (mode 2 of qmv_set_weight_prefetch) take
+// CTAs of at most TC_WARPS_HALF_SM warps in at most half an SM's shared
+// memory, so that two calls' CTAs share an SM, one converting its x while
+// the other runs its tiles (measured on GB300, us a call: Q4_K 4096 x 4096
+// m = 8 6.84 -> 5.97, m = 4 6.47 -> 5.51; Q6_K 4096 x 14336 m = 4 25.1 ->
+// 21.6; Q8_0 14336 x 4096 m = 8 19.1 -> 18.2). Other modes, forced warps, and
+// shapes whose plan does not fit use whole CTAs.
+template <class F>
+inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv_cfg* cfg, TParams* tp, Plan* pl) {
+    const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
+    if (mode == 2 && !(cfg && cfg->warps > 0)) {
+        qmv_cfg c = cfg ? *cfg : qmv_cfg{0, 0, 0, 0, 0, 0};
+        c.warps = TC_WARPS_HALF_SM;
+        const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;
+        TParams t2 = *tp;
+        Plan p2;
+        if (!make_tc_plan_core<F>(di, rows, k, m, &c, half, &t2, &p2)) {
+            *tp = t2;
+            *pl = p2;
+            return QMV_OK;
+        }
+    }
+    return make_tc_plan_core<F>(di, rows, k, m, cfg, di.smem_optin, tp, pl);
 }
 
 template <class F, bool P>

@@ -139,7 +139,36 @@ def test_batch_argument_errors(q):
     assert q.qmm_q8_0(w, x, y, 2, 48, 2, check=False) == q.QMV_EINVAL
 
 
+@pytest.mark.parametrize("fmt,rows,k", [("q4k", 300, 4096), ("q6k", 97, 14336), ("q8_0", 500, 4096),
+                                        ("q5k", 64, 4352), ("q4_0", 77, 4160)])
+@pytest.mark.parametrize("m", [2, 4, 8])
+def test_batch_independent_call_plans(q, fmt, rows, k, m):
+    """Independent calls (mode 2) take half-SM CTAs of at most 8 warps, so rows
+    longer than 2048 weights are cut into more k-chunks than in plain launches:
+    every row of y still matches the oracle, unit rows still give the weight
+    columns bit for bit."""
+    st = synth.Stream(rows + k + 5 * m)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    W = oracle.dequant(fmt, w, rows, k).astype(np.float32)
+    js = [3, 1000, k - 1, 2048, 77, 3000, 5, 4000][:m]
+    xu = np.zeros((m, k), dtype=np.float32)
+    for i, j in enumerate(js):
+        xu[i, j] = 1.0
+    old = q.qmv_set_weight_prefetch(2)
+    try:
+        y = run_qmm(q, fmt, w, x, rows, k, m)
+        yu = run_qmm(q, fmt, w, xu, rows, k, m)
+    finally:
+        q.qmv_set_weight_prefetch(old)
+    check_rows(oracle.qmm(fmt, w, x, m, rows, k), y)
+    for i, j in enumerate(js):
+        assert np.array_equal(yu[i], W[:, j]), (i, j)
+
+
 def test_batch_overlap_modes_give_identical_results(q):
+    """Rows of 2048 weights (8 slices: one k-chunk in every mode) give the same
+    bits in plain, chained and independent calls."""
     st = synth.Stream(91)
     cases = [(fmt, dev(synth.GEN_ROWS[fmt](st, 300, 2048)), dev(synth.gen_normal(st, 5 * 2048)))
              for fmt in FMTS]

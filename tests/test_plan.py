@@ -323,12 +323,23 @@ def tc_max_read(fmt, slices, groups):
     return (groups - 1) * 34 + 38          # codes at 18 + 4t: 8 bytes from the word below
 
 
-def tc_replay(q, fmt, rows, k, m, cfg=None):
+def tc_replay(q, fmt, rows, k, m, cfg=None, mode=0):
+    """Replay the tensor-core plan computed under launch mode `mode` (0:
+    plain, 2: independent calls, where CTAs of at most 8 warps take at most
+    half an SM's shared memory unless that plan does not fit)."""
     fid, qk, bb = TC_FMT[fmt]
-    P = q.qmm_tc_plan_detail(fid, rows, k, m, cfg, DEVICE)
+    old = q.qmv_set_weight_prefetch(mode)
+    try:
+        P = q.qmm_tc_plan_detail(fid, rows, k, m, cfg, DEVICE)
+    finally:
+        q.qmv_set_weight_prefetch(old)
     ng = k // 32
     NS = -(-ng // 8)
     kmax = min(cfg["warps"], 16) if cfg and cfg.get("warps") else 16
+    half = (DEVICE[2] - 2 * DEVICE[3]) // 2
+    if mode == 2 and not (cfg and cfg.get("warps")) and P["threads"] <= 32 * 8:
+        kmax = 8
+        assert P["smem"] <= half
     nch = -(-NS // kmax)
     KS = -(-NS // nch)
     assert P["KS"] == KS and P["nchunks"] == nch and P["threads"] == 32 * KS <= 512 and P["ngroups"] == ng
@@ -409,6 +420,17 @@ def test_tc_plans(q, shape, m):
 @pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q5k", "q4_0"])
 def test_tc_forced_plans(q, fmt, cfg):
     tc_replay(q, fmt, 61, 512, 3, cfg)
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES)
+@pytest.mark.parametrize("m", [2, 4, 8])
+def test_tc_independent_call_plans(q, shape, m):
+    """Independent calls: every index replayed as for the default plans; the
+    suite's large matrices take CTAs of at most 8 warps in half an SM."""
+    fmt, rows, k = shape
+    P = tc_replay(q, fmt, rows, k, m, mode=2)
+    if rows >= 4096 and k >= 4096:
+        assert P["threads"] <= 256 and P["smem"] <= (DEVICE[2] - 2 * DEVICE[3]) // 2
 
 
 def test_tc_long_rows_take_kchunks(q):
