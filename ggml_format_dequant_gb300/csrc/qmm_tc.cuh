@@ -115,6 +115,31 @@ __device__ __forceinline__ uint32_t lds32_a2(uint32_t a) {
     return __funnelshift_r(lds32<0>(wa), lds32<4>(wa), (a & 3u) * 8u);
 }
 
+// 4 bytes at the shared address a whose phase a & 3 is ph: 0 (one load), 2
+// (two loads and a constant shift) or unknown (-1: lds32_a2). ph is a
+// constant once the callers are inlined and their loops unrolled.
+__device__ __forceinline__ uint32_t lds32_ph(uint32_t a, int ph) {
+    if (ph == 0) return lds32<0>(a);
+    if (ph == 2) return __funnelshift_r(lds32<0>(a - 2u), lds32<4>(a - 2u), 16u);
+    return lds32_a2(a);
+}
+
+// The f16 at the 2-byte aligned shared address a (phase ph as above), as f32.
+__device__ __forceinline__ float ldh_ph(uint32_t a, int ph) {
+    if (ph == 0) return f16_lo(lds32<0>(a));
+    if (ph == 2) return f16_hi(lds32<0>(a - 2u));
+    return f16_lo(lds32_a2(a));
+}
+
+// The phase (a & 3) that addresses a and b share in every lane of the warp:
+// 0, 2, or -1 when they differ.
+__device__ __forceinline__ int warp_phase(uint32_t a, uint32_t b) {
+    const uint32_t pa = a & 3u, pb = b & 3u;
+    if (__all_sync(FULL, pa == 0u && pb == 0u)) return 0;
+    if (__all_sync(FULL, pa == 2u && pb == 2u)) return 2;
+    return -1;
+}
+
 // MMA of one 16-column half with A given directly (rows g, g+8; even, odd
 // columns) against hi and lo; packed (P): the lane's one fragment already
 // holds hi (columns 0-3) or lo (columns 4-7), one MMA.
@@ -407,27 +432,39 @@ struct Q6KT {
     static constexpr int SLACK = 16;
     static constexpr bool SUMS = false;
 
+    // Every field read sits a multiple of 4 bytes into the block, so all of a
+    // block's loads share its phase ph (see lds32_ph).
     template <bool P>
     __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int, int t, const XFrag& xf,
                                                  uint32_t, float (&y4)[4]) {
         const uint32_t ba = ra + static_cast<uint32_t>(ks) * BLOCK_BYTES;
         const uint32_t bb = rb + static_cast<uint32_t>(ks) * BLOCK_BYTES;
+        switch (warp_phase(ba, bb)) {
+        case 0: body<P>(ba, bb, t, xf, y4, 0); break;
+        case 2: body<P>(ba, bb, t, xf, y4, 2); break;
+        default: body<P>(ba, bb, t, xf, y4, -1); break;
+        }
+    }
+
+    template <bool P>
+    __device__ __forceinline__ static void body(uint32_t ba, uint32_t bb, int t, const XFrag& xf, float (&y4)[4],
+                                                int ph) {
         const uint32_t bias = 0x64206420u;   // 1024 + 32: the codes become q - 32
-        const float da = f16_lo(lds32_a2(ba + 208u)), db = f16_lo(lds32_a2(bb + 208u));
+        const float da = ldh_ph(ba + 208u, ph), db = ldh_ph(bb + 208u, ph);
         const float nda = -da * THREE22, ndb = -db * THREE22;
         const uint32_t lt = 4u * static_cast<uint32_t>(t);
 #pragma unroll
         for (int H = 0; H < 2; H++) {
-            const uint32_t qha0 = lds32_a2(ba + 128u + 32u * H + lt), qha1 = lds32_a2(ba + 144u + 32u * H + lt);
-            const uint32_t qhb0 = lds32_a2(bb + 128u + 32u * H + lt), qhb1 = lds32_a2(bb + 144u + 32u * H + lt);
+            const uint32_t qha0 = lds32_ph(ba + 128u + 32u * H + lt, ph), qha1 = lds32_ph(ba + 144u + 32u * H + lt, ph);
+            const uint32_t qhb0 = lds32_ph(bb + 128u + 32u * H + lt, ph), qhb1 = lds32_ph(bb + 144u + 32u * H + lt, ph);
             // scales 8H .. 8H + 7 of both rows
-            const uint32_t sca0 = lds32_a2(ba + 192u + 8u * H), sca1 = lds32_a2(ba + 196u + 8u * H);
-            const uint32_t scb0 = lds32_a2(bb + 192u + 8u * H), scb1 = lds32_a2(bb + 196u + 8u * H);
+            const uint32_t sca0 = lds32_ph(ba + 192u + 8u * H, ph), sca1 = lds32_ph(ba + 196u + 8u * H, ph);
+            const uint32_t scb0 = lds32_ph(bb + 192u + 8u * H, ph), scb1 = lds32_ph(bb + 196u + 8u * H, ph);
 #pragma unroll
             for (int p = 0; p < 2; p++) {   // qd % 2
                 const uint32_t o = 64u * H + 32u * p + lt;
-                const uint32_t qla0 = lds32_a2(ba + o), qla1 = lds32_a2(ba + o + 16u);
-                const uint32_t qlb0 = lds32_a2(bb + o), qlb1 = lds32_a2(bb + o + 16u);
+                const uint32_t qla0 = lds32_ph(ba + o, ph), qla1 = lds32_ph(ba + o + 16u, ph);
+                const uint32_t qlb0 = lds32_ph(bb + o, ph), qlb1 = lds32_ph(bb + o + 16u, ph);
 #pragma unroll
                 for (int hi = 0; hi < 2; hi++) {
                     const int qd = 2 * hi + p;
@@ -466,19 +503,33 @@ struct Q8T {
     static constexpr int SLACK = 16;
     static constexpr bool SUMS = false;
 
+    // Block j of the slice starts 34 (8 ks + j) bytes into the row: its phase
+    // is the row's plus 2j (mod 4); d sits at that phase and the codes at the
+    // other one (see lds32_ph).
     template <bool P>
     __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int ng, int t, const XFrag& xf,
                                                  uint32_t, float (&y4)[4]) {
+        switch (warp_phase(ra, rb)) {
+        case 0: body<P>(ra, rb, ks, ng, t, xf, y4, 0); break;
+        case 2: body<P>(ra, rb, ks, ng, t, xf, y4, 2); break;
+        default: body<P>(ra, rb, ks, ng, t, xf, y4, -1); break;
+        }
+    }
+
+    template <bool P>
+    __device__ __forceinline__ static void body(uint32_t ra, uint32_t rb, int ks, int ng, int t, const XFrag& xf,
+                                                float (&y4)[4], int ph0) {
         const uint32_t bias = 0x64806480u;
         const uint32_t lt = 4u * static_cast<uint32_t>(t);
 #pragma unroll
         for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
             if (j < ng) {
+                const int ph = ph0 < 0 ? -1 : ((ph0 + 2 * j) & 3), pc = ph0 < 0 ? -1 : ((ph + 2) & 3);
                 const uint32_t off = static_cast<uint32_t>(ks * TC_GROUPS_PER_SLICE + j) * BLOCK_BYTES;
                 const uint32_t ba = ra + off, bb = rb + off;
-                const float da = f16_lo(lds32_a2(ba)), db = f16_lo(lds32_a2(bb));
-                const uint32_t ka0 = lds32_a2(ba + 2u + lt) ^ 0x80808080u, ka1 = lds32_a2(ba + 18u + lt) ^ 0x80808080u;
-                const uint32_t kb0 = lds32_a2(bb + 2u + lt) ^ 0x80808080u, kb1 = lds32_a2(bb + 18u + lt) ^ 0x80808080u;
+                const float da = ldh_ph(ba, ph), db = ldh_ph(bb, ph);
+                const uint32_t ka0 = lds32_ph(ba + 2u + lt, pc) ^ 0x80808080u, ka1 = lds32_ph(ba + 18u + lt, pc) ^ 0x80808080u;
+                const uint32_t kb0 = lds32_ph(bb + 2u + lt, pc) ^ 0x80808080u, kb1 = lds32_ph(bb + 18u + lt, pc) ^ 0x80808080u;
                 float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 mma_half<P>(D, ka0, kb0, bias, xf.h[j][0], xf.h[j][1], xf.l[j][0], xf.l[j][1]);
                 mma_half<P>(D, ka1, kb1, bias, xf.h[j][2], xf.h[j][3], xf.l[j][2], xf.l[j][3]);
@@ -498,18 +549,30 @@ struct Q40T {
     static constexpr int SLACK = 16;
     static constexpr bool SUMS = false;
 
+    // Phases as for Q8_0: block j starts 18 (8 ks + j) bytes into the row.
     template <bool P>
     __device__ __forceinline__ static void slice(uint32_t ra, uint32_t rb, int ks, int ng, int t, const XFrag& xf,
                                                  uint32_t, float (&y4)[4]) {
+        switch (warp_phase(ra, rb)) {
+        case 0: body<P>(ra, rb, ks, ng, t, xf, y4, 0); break;
+        case 2: body<P>(ra, rb, ks, ng, t, xf, y4, 2); break;
+        default: body<P>(ra, rb, ks, ng, t, xf, y4, -1); break;
+        }
+    }
+
+    template <bool P>
+    __device__ __forceinline__ static void body(uint32_t ra, uint32_t rb, int ks, int ng, int t, const XFrag& xf,
+                                                float (&y4)[4], int ph0) {
         const uint32_t bias = 0x64086408u;
         const uint32_t lt = 4u * static_cast<uint32_t>(t);
 #pragma unroll
         for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
             if (j < ng) {
+                const int ph = ph0 < 0 ? -1 : ((ph0 + 2 * j) & 3), pc = ph0 < 0 ? -1 : ((ph + 2) & 3);
                 const uint32_t off = static_cast<uint32_t>(ks * TC_GROUPS_PER_SLICE + j) * BLOCK_BYTES;
                 const uint32_t ba = ra + off, bb = rb + off;
-                const float da = f16_lo(lds32_a2(ba)), db = f16_lo(lds32_a2(bb));
-                const uint32_t wa = lds32_a2(ba + 2u + lt), wb = lds32_a2(bb + 2u + lt);
+                const float da = ldh_ph(ba, ph), db = ldh_ph(bb, ph);
+                const uint32_t wa = lds32_ph(ba + 2u + lt, pc), wb = lds32_ph(bb + 2u + lt, pc);
                 float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 mma_half<P>(D, wa & 0x0f0f0f0fu, wb & 0x0f0f0f0fu, bias, xf.h[j][0], xf.h[j][1], xf.l[j][0],
                             xf.l[j][1]);
