@@ -75,3 +75,54 @@ def test_random_shape(q, fam, rows, k, cfg):
     got = y.cpu().numpy().astype(np.float64)
     assert not np.any(np.isnan(got))
     assert float(np.max(np.abs(ref - got)) / max(np.max(np.abs(ref)), 1e-30)) <= SCALE_REL_TOL
+
+
+# ------------------------------------------------ small-M batched products
+
+BATCH_FMTS = ["q4k", "q6k", "q8_0", "q5k", "q4_0"]
+
+
+def batch_cases(n=8):
+    """(fmt, rows, k, m, cfg, mode) drawn from a fixed stream: k up to 16384
+    weights (several k-chunks), m = 2..12 (one or two tiles of x rows), a forced
+    plan half of the time, and the plain or independent-call launch mode."""
+    out = []
+    z = synth.Stream(5151).draw(len(BATCH_FMTS) * n * 8).reshape(len(BATCH_FMTS), n, 8)
+    for fi, fmt in enumerate(BATCH_FMTS):
+        qk = QK[fmt]
+        for ci in range(n):
+            d = [int(v >> np.uint64(33)) for v in z[fi, ci]]
+            k = (1 + d[0] % (16384 // qk)) * qk
+            rows = 1 + d[1] % 160
+            m = 2 + d[2] % 11
+            cfg = None
+            if d[3] % 2:
+                cfg = dict(ctas=1 + d[4] % 9, chunk_rows=d[5] % 20, chunks=d[6] % 4, warps=[0, 1, 3, 8][d[7] % 4])
+            mode = 2 if d[7] % 3 == 0 else 0
+            out.append((fmt, rows, k, m, cfg, mode))
+    return out
+
+
+@pytest.mark.parametrize("fmt,rows,k,m,cfg,mode", batch_cases())
+def test_random_batch(q, fmt, rows, k, m, cfg, mode):
+    st = synth.Stream(rows * 17 + k + m)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    old = q.qmv_set_weight_prefetch(mode)
+    try:
+        rc = getattr(q, f"qmm_{fmt}")(torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda(), y, rows, k, m,
+                                      cfg=cfg, check=False)
+        torch.cuda.synchronize()
+    finally:
+        q.qmv_set_weight_prefetch(old)
+    if rc == q.QMV_ETOOBIG:
+        assert cfg is not None   # a forced plan refused on the host, nothing launched
+        return
+    assert rc == q.QMV_OK, q.strerror(rc)
+    ref = oracle.qmm(fmt, w, x, m, rows, k)
+    got = y.cpu().numpy().astype(np.float64)
+    assert not np.any(np.isnan(got))
+    for i in range(m):
+        e = float(np.max(np.abs(ref[i] - got[i])) / max(np.max(np.abs(ref[i])), 1e-30))
+        assert e <= SCALE_REL_TOL, (i, e)

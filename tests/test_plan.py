@@ -459,3 +459,23 @@ def test_random_shape_plans(q, fam, rows, k, cfg):
         replay(q, fam, rows, k, 1, cfg)
     except q.QmvError as e:
         assert cfg is not None and e.code == q.QMV_ETOOBIG
+
+
+def _random_batch_cases():
+    from test_gpu_random_shapes import batch_cases
+    return batch_cases()
+
+
+@pytest.mark.parametrize("fmt,rows,k,m,cfg,mode", _random_batch_cases())
+def test_random_batch_plans(q, fmt, rows, k, m, cfg, mode):
+    """The seeded random batches of the GPU test, every tile's plan replayed on
+    the host before they run (a plan the host refuses is never launched)."""
+    tiles = -(-m // 8)
+    for mt in sorted({m // tiles + (1 if t < m % tiles else 0) for t in range(tiles)}):
+        try:
+            if fmt == "q4k" and mt == 2:
+                replay(q, "qmm4", rows, k, 2, cfg, mode=mode)   # the register kernel
+            else:
+                tc_replay(q, fmt, rows, k, mt, cfg, mode=mode)
+        except q.QmvError as e:
+            assert cfg is not None and e.code == q.QMV_ETOOBIG
