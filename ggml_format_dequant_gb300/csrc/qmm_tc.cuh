@@ -4,13 +4,14 @@
 // launch.
 //
 // The product is a skinny dense contraction (m <= 8 columns), so a warp-level
-// MMA with register accumulators fits it: the weights' per-32 (Q4_K, Q8_0) or
-// per-16 (Q6_K) scales are applied to each group's partial product in
-// registers right after its MMAs, which keeps every operand exact:
+// MMA with register accumulators fits it: the weights' per-32 (Q4_K, Q5_K,
+// Q8_0, Q4_0) or per-16 (Q6_K) scales are applied to each group's partial
+// product in registers right after its MMAs, which keeps every operand exact:
 //  * A (16 weight rows x 16 k): the integer codes, exact in f16: Q4_K's q as
 //    the subnormal q * 2^-24 or 16 q * 2^-24 (one mask, or a shift and a
-//    mask, per pair; the power of two goes into the row scale), Q6_K's q - 32
-//    and Q8_0's q made from the code bytes with one byte permute into the f16
+//    mask, per pair; the power of two goes into the row scale), Q5_K's
+//    five-bit q likewise as q * 2^-24; Q6_K's q - 32, Q8_0's q and Q4_0's
+//    q - 8 made from the code bytes with one byte permute into the f16
 //    pattern of 1024 + v and one f16x2 subtraction.
 //  * B (16 k x 8 rows of x): x in two f16 parts, hi + lo, after a power-of-two
 //    scale per row of x and warp slice (256 weights) that puts the slice's
@@ -18,7 +19,9 @@
 //    pair A*hi + A*lo is the group's integer-code dot at f32 accuracy, and
 //    the scale comes off once per tile when the slice's sums are parked.
 //  * Per group the accumulator D (16 x 8, four values a lane) is folded into
-//    the row sums: y += d*sc * D. Q4_K's min term, dmin * sum_j m_j S_j with
+//    the row sums: y += d*sc * D. Up to 4 rows of x, hi and lo share one MMA
+//    (columns 0-3 hi, 4-7 lo; the final sum adds the halves).
+//  * The min term of Q4_K and Q5_K, dmin * sum_j m_j S_j with
 //    S_j the sum of x over group j, is one more product per tile: A' = the
 //    six-bit m_j of the 16 rows, B' = a lane's partial sums of the groups
 //    (hi + lo), over a k made of (group, lane) pairs, so that no lane needs
@@ -37,7 +40,8 @@
 // and lo, 64 registers) for the chunk's pieces. Rows are processed in tiles of
 // 16; slice partials are parked per (row, slice, column), added over the
 // chunks, and summed in slice order at the end. Waits are bounded as in
-// qmv_kernel.cuh.
+// qmv_kernel.cuh. The planner (make_tc_plan_for) gives independent calls
+// half-SM CTAs of at most 8 warps, so that two calls share an SM.
 #pragma once
 
 #include "qmv_launch.cuh"
