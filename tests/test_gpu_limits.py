@@ -1,6 +1,7 @@
 """The largest row length every matvec entry point takes (sixteen warps of
 k-slices), one row past it (refused on the host with QMV_ETOOBIG, nothing
-launched), and degenerate MoE shapes, through the C ABI against the oracle."""
+launched), degenerate MoE shapes, and batched products over rows of 65536
+weights, through the C ABI against the oracle."""
 
 import numpy as np
 import pytest
@@ -87,3 +88,27 @@ def test_moe_single_expert_bank(q, slots, ids):
     ref = oracle.moe_qmv("q4k", bank, x, np.array(ids, dtype=np.int32), n, k, e)
     for s in range(slots):
         assert scale_rel(ref[s], y[s].cpu().numpy()) <= SCALE_REL_TOL
+
+
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q8_0", "q5k", "q4_0"])
+@pytest.mark.parametrize("m,mode", [(3, 0), (8, 0), (8, 2)])
+def test_batch_long_rows(q, fmt, m, mode):
+    """The batched product has no row-length limit: 65536 weights a row run as
+    16 k-chunks of 16 slices (32 of 8 for independent calls) inside one
+    launch, against the oracle."""
+    rows, k = 40, 65536
+    st = synth.Stream(777 + m)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    old = q.qmv_set_weight_prefetch(mode)
+    try:
+        getattr(q, f"qmm_{fmt}")(dev(w), dev(x), y, rows, k, m)
+        torch.cuda.synchronize()
+    finally:
+        q.qmv_set_weight_prefetch(old)
+    ref = oracle.qmm(fmt, w, x, m, rows, k)
+    got = y.cpu().numpy()
+    assert not np.any(np.isnan(got))
+    for i in range(m):
+        assert scale_rel(ref[i], got[i]) <= SCALE_REL_TOL, i

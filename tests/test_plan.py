@@ -403,7 +403,8 @@ TC_SHAPES = [("q4k", 4096, 4096), ("q4k", 300, 768), ("q4k", 1, 256), ("q4k", 97
              ("q8_0", 13, 32), ("q8_0", 7, 4064), ("q8_0", 64, 1056), ("q4k", 20, 16384), ("q4k", 97, 4352),
              ("q6k", 4096, 14336), ("q6k", 41, 14336), ("q8_0", 64, 11008), ("q8_0", 5, 4160), ("q8_0", 3, 12320),
              ("q5k", 4096, 4096), ("q5k", 37, 512), ("q5k", 3, 4352), ("q5k", 1, 256), ("q4_0", 4096, 4096),
-             ("q4_0", 300, 96), ("q4_0", 13, 32), ("q4_0", 64, 11008), ("q4_0", 7, 4160)]
+             ("q4_0", 300, 96), ("q4_0", 13, 32), ("q4_0", 64, 11008), ("q4_0", 7, 4160), ("q4k", 40, 65536),
+             ("q6k", 40, 65536), ("q8_0", 40, 65536), ("q5k", 40, 65536), ("q4_0", 40, 65536)]
 
 
 @pytest.mark.parametrize("m", [1, 2, 5, 8])
