@@ -26,9 +26,9 @@ QMV_ETOOBIG = -4
 QMV_STATUS_BAD_EXPERT_ID = 1
 QMV_STATUS_WAIT_TIMEOUT = 2
 
-# Plan ids of qmv_plan_info / qmv_plan_detail (14 and 15 are not plans).
+# Plan ids of qmv_plan_info / qmv_plan_detail (13-15 are not plans).
 (FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A,
- FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K, FMT_QMM_Q4K) = range(14)
+ FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K) = range(13)
 FMT_Q6K_DP4A, FMT_MOE_Q6K_DP4A = 16, 17
 
 
@@ -220,16 +220,10 @@ def qmm_q4_0(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
 
 
 def qmm_launches(fmt, k, m) -> int:
-    """Kernel launches one qmm_<fmt> call makes: the matvec for m = 1; for
-    Q4_K and m = 2 the register kernel, ceil(m / tile) launches with the widest
-    tile (2 or 1 rows of x) whose units per row fit a CTA; otherwise the
+    """Kernel launches one qmm_<fmt> call makes: the matvec for m = 1, else the
     tensor-core kernel, one launch per tile of up to 8 rows of x (ceil(m / 8)),
     whatever k."""
-    if m == 1:
-        return 1
-    if m >= 3 or fmt != "q4k":
-        return -(-m // 8)   # the tensor-core kernel (Q6_K, Q8_0, Q5_K, Q4_0 from m = 2 on)
-    return 1 if (k // 256) * 8 <= 512 else 2
+    return 1 if m == 1 else -(-m // 8)
 
 
 def qmv_q5k(w, x, y, rows, k, stream=None, cfg=None, check=True):

@@ -1,7 +1,6 @@
 // qmm_q6k.cu -- small-M batched product y[m, rows] = x[m, k] W^T over packed
 // Q6_K rows (m >= 2): the tensor-core kernel of qmm_tc.cuh, one launch per
-// tile of up to 8 rows of x (for two rows it measured faster than a
-// register-activation kernel on this format).
+// tile of up to 8 rows of x.
 #include "qmv_internal.h"
 #include "qmm_tc.cuh"
 

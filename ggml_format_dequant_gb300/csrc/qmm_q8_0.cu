@@ -1,7 +1,6 @@
 // qmm_q8_0.cu -- small-M batched product y[m, rows] = x[m, k] W^T over packed
 // Q8_0 rows (m >= 2): the tensor-core kernel of qmm_tc.cuh, one launch per
-// tile of up to 8 rows of x (for two rows it measured faster than a
-// register-activation kernel on this format).
+// tile of up to 8 rows of x.
 #include "qmv_internal.h"
 #include "qmm_tc.cuh"
 

@@ -4,7 +4,6 @@
 #include <climits>
 #include <cstdint>
 
-#include "qmm_formats.cuh"
 #include "qmm_tc.cuh"
 #include "qmv_internal.h"
 #include "qmv_launch.cuh"
@@ -398,19 +397,7 @@ int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const q
     if (moe && slots <= 0) return QMV_EINVAL;
     if (fmt == 16) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, 1, cfg, kp, pl);
     if (fmt == 17) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, slots, cfg, kp, pl);
-    if (fmt == 14 || fmt == 15) return QMV_EINVAL;   // Q6_K and Q8_0 batches run on the tensor cores
-    if (fmt == 13) {
-        // batched Q4_K: `slots` is the tile's row count of x, 2..8
-        switch (slots) {
-#define QMM_PLAN(MM) \
-    case MM:         \
-        return qmv::make_plan_for<qmv::Q4KB<MM>>(di, rows, k, 1, cfg, kp, pl);
-            QMM_PLAN(2) QMM_PLAN(3) QMM_PLAN(4) QMM_PLAN(5) QMM_PLAN(6) QMM_PLAN(7) QMM_PLAN(8)
-#undef QMM_PLAN
-        default:
-            return QMV_EINVAL;
-        }
-    }
+    if (fmt >= 13 && fmt <= 15) return QMV_EINVAL;   // batches of two or more rows run on the tensor cores
     if (!moe) slots = 1;
     switch (fmt) {
     case 0: return qmv::make_plan_for<qmv::Q4K>(di, rows, k, 1, cfg, kp, pl);

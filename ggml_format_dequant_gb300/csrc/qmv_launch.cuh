@@ -122,19 +122,6 @@ inline int pow2ceil(int v) {
 
 inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a; }
 
-// Outputs per weight row of format F: F::OUTS where the format declares it
-// (the small-M batch formats), else 1.
-template <class F, class = void>
-struct OutsOf {
-    static constexpr int value = 1;
-};
-template <class F>
-struct OutsOf<F, decltype(void(F::OUTS))> {
-    static constexpr int value = F::OUTS;
-};
-template <class F>
-constexpr int outs_of() { return OutsOf<F>::value; }
-
 // Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense)
 // on a device described by `di`, for a given (or the default) CTA count.
 template <class F>
@@ -160,8 +147,7 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
     // not more than there are rows, and enough that the parked partials fit.
     const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
     const int early = mode >= 2 ? 1 : 0;
-    const int W = KS > 1 ? KS : early;   // parked slice sums per row (per output)
-    const int outs = outs_of<F>();       // outputs per weight row: 1, or the batch width
+    const int W = KS > 1 ? KS : early;   // parked slice sums per row
     if (cfg && cfg->ctas > 0) {
         P.parts = cfg->ctas;
     } else {
@@ -170,7 +156,7 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
         // pays a fixed start-up cost, the activation prep among it)
         const long long by_bytes = std::max<long long>(1, static_cast<long long>(rows) * rowbytes / MIN_CTA_BYTES);
         if (by_bytes < P.parts) P.parts = static_cast<int>(by_bytes);
-        const long long max_rows = std::max<long long>(1, RED_MAX_BYTES / (4LL * std::max(W, 1) * outs));
+        const long long max_rows = std::max<long long>(1, RED_MAX_BYTES / (4LL * std::max(W, 1)));
         const long long need = (rows + max_rows - 1) / max_rows;
         if (need > P.parts) P.parts = static_cast<int>(std::min<long long>(need, 1 << 30));
     }
@@ -223,7 +209,7 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
         kp->lt.xsum16 = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 16), 128);
     }
     kp->off_red = static_cast<uint32_t>(off);
-    off = round_up(off + 4LL * rpc * W * outs, 128);   // W == 0: nothing parked
+    off = round_up(off + 4LL * rpc * W, 128);   // W == 0: nothing parked
     const long long fixed = off;
 
     // Budget: half an SM's shared memory when two CTAs are meant to share it,

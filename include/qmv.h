@@ -339,10 +339,9 @@ int qmv_q6k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int r
  * shared bytes per CTA.
  * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K,
  * 5 = Q4_K dp4a, 6 = MoE Q6_K, 7 = MoE Q4_K dp4a, 8 = Q5_K, 9 = Q4_0,
- * 10 = MoE Q8_0, 11 = MoE Q4_0, 12 = MoE Q5_K, 13 = the batched Q4_K
- * register kernel for one tile of `slots` (2..8) rows of x, 16 = Q6_K dp4a,
- * 17 = MoE Q6_K dp4a. 14 and 15 are not plans (QMV_EINVAL): Q6_K and Q8_0
- * batches of two or more rows run on the tensor cores (qmm_tc_plan_detail). */
+ * 10 = MoE Q8_0, 11 = MoE Q4_0, 12 = MoE Q5_K, 16 = Q6_K dp4a, 17 = MoE Q6_K
+ * dp4a. 13, 14 and 15 are not plans (QMV_EINVAL): batches of two or more rows
+ * of x run on the tensor cores (qmm_tc_plan_detail). */
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
                   int *chunk_rows, int *chunks, int *smem_bytes);
 

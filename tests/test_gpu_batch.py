@@ -213,8 +213,7 @@ def test_batch_kchunks(q, fmt, rows, k, warps, m):
     st = synth.Stream(rows * 7 + k + 31 * warps + m)
     w = synth.GEN_ROWS[fmt](st, rows, k)
     x = synth.gen_normal(st, m * k).reshape(m, k)
-    # Q4_K with two rows runs the register kernel: no k-chunks to force
-    cfg = None if (fmt == "q4k" and m == 2) else dict(warps=warps, chunks=2)
+    cfg = dict(warps=warps, chunks=2)
     check_rows(oracle.qmm(fmt, w, x, m, rows, k), run_qmm(q, fmt, w, x, rows, k, m, cfg=cfg))
 
 

@@ -20,26 +20,14 @@ import pytest
 
 DEVICE = (152, 232448, 233472, 1024)
 FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5, "moe6": 6, "moe4d": 7, "q5k": 8,
-          "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12, "qmm4": 13,
+          "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12,
           "q6d": 16, "moe6d": 17}
-
-
-def batch_uw(m):
-    """Weights per lane unit of the batched product for a tile of m rows."""
-    return 8 if m >= 5 else (16 if m >= 3 else 32)
 
 
 # Per format: weights per block, bytes per block, blocks per warp slice,
 # units per row, a unit's block offset in its slice, and the byte range a
 # unit's loads touch relative to its address a (lo may depend on a & 3).
 def fmt_info(fmt, m=1):
-    if fmt == "qmm4":
-        qk, bb = 256, 144
-        uw = batch_uw(m)
-        upb = qk // uw
-        extent, align = (lambda a: (a, a + 144)), 16
-        return dict(qk=qk, bb=bb, sb=32 // upb, units=lambda nb: upb * nb, ubyte=lambda u: (u // upb) * bb,
-                    extent=extent, align=align, outs=m)
     if fmt in ("q4k", "moe", "q4d", "moe4d"):
         return dict(qk=256, bb=144, sb=8, units=lambda nb: 4 * nb, ubyte=lambda u: (u >> 2) * 144,
                     extent=lambda a: (a, a + 144), align=16)
@@ -80,7 +68,6 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
     finally:
         q.qmv_set_weight_prefetch(old)
     f = fmt_info(fmt, slots)
-    outs = f.get("outs", 1)
     nb = k // f["qk"]
     U = f["units"](nb)
     KS, GS, NG, CR, S, R, W = P["KS"], P["GS"], P["NG"], P["CR"], P["S"], P["unroll"], P["W"]
@@ -96,7 +83,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
     CL = P["CL"]
     assert CL in (1, 2, 4, 8) and parts % CL == 0 and (k // 16) % (2 * CL) == 0
     assert P["rq"] >= 1
-    if fmt in ("q8d", "q4d", "moe4d", "qmm4", "q6d", "moe6d"):
+    if fmt in ("q8d", "q4d", "moe4d", "q6d", "moe6d"):
         assert CL == 1
     lg = GS.bit_length() - 1
     rpw = 32 >> lg
@@ -106,13 +93,13 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
 
     # shared-memory layout: disjoint, ordered regions inside the device limit
     regions = []
-    if fmt not in ("q8d", "q4d", "moe4d", "qmm4", "q6d", "moe6d"):
+    if fmt not in ("q8d", "q4d", "moe4d", "q6d", "moe6d"):
         regions += [(P["off_la"], k), (P["off_lb"], k), (P["off_lc"], k), (P["off_xs"], 4 * (k // 32)),
                     (P["off_xsum16"], 4 * (k // 16))]
         for o, _ in regions:
             assert o % 16 == 0
     rpc = P["rq"] + (1 if P["rrem"] else 0)
-    regions += [(P["off_red"], 4 * rpc * W * outs), (P["off_ring"], NG * S * stride), (P["off_bars"], 8 * NG * S),
+    regions += [(P["off_red"], 4 * rpc * W), (P["off_ring"], NG * S * stride), (P["off_bars"], 8 * NG * S),
                 (P["off_cnt"], 4 * (NG * S + NG + 1))]
     regions.sort()
     for (o1, n1), (o2, _) in zip(regions, regions[1:]):
@@ -245,33 +232,10 @@ def test_moe_forced_plan(q):
         replay(q, fmt, 40, 512, 5, dict(ctas=2, chunk_rows=3, chunks=2))
 
 
-BATCH_SHAPES = [("qmm4", 4096, 4096), ("qmm4", 300, 768), ("qmm4", 1, 256), ("qmm4", 97, 4352),
-                ("qmm4", 20, 16384)]
-
-
-@pytest.mark.parametrize("m", [2, 3, 4, 5, 8])
-@pytest.mark.parametrize("shape", BATCH_SHAPES)
-def test_batch_plans(q, shape, m):
-    fmt, rows, k = shape
-    if k // batch_uw(m) > 512:
-        # more units per row than 16 warps hold: the planner refuses the tile
-        # (the entry point runs such a k in narrower tiles)
-        with pytest.raises(q.QmvError):
-            q.qmv_plan_detail(FMT_ID[fmt], rows, k, m, None, DEVICE)
-        return
-    replay(q, fmt, rows, k, m)
-
-
-@pytest.mark.parametrize("cfg", CFGS[:6])
-@pytest.mark.parametrize("fmt,m", [("qmm4", 2), ("qmm4", 3), ("qmm4", 8)])
-def test_batch_forced_plans(q, fmt, m, cfg):
-    replay(q, fmt, 61, 512, m, cfg)
-
-
 def test_retired_batch_plan_ids(q):
-    """Q6_K and Q8_0 batches run on the tensor cores: plan ids 14 and 15 are
+    """Batches of two or more rows run on the tensor cores: plan ids 13-15 are
     refused."""
-    for fid in (14, 15):
+    for fid in (13, 14, 15):
         with pytest.raises(q.QmvError):
             q.qmv_plan_detail(fid, 64, 512, 2, None, DEVICE)
 
@@ -474,9 +438,6 @@ def test_random_batch_plans(q, fmt, rows, k, m, cfg, mode):
     tiles = -(-m // 8)
     for mt in sorted({m // tiles + (1 if t < m % tiles else 0) for t in range(tiles)}):
         try:
-            if fmt == "q4k" and mt == 2:
-                replay(q, "qmm4", rows, k, 2, cfg, mode=mode)   # the register kernel
-            else:
-                tc_replay(q, fmt, rows, k, mt, cfg, mode=mode)
+            tc_replay(q, fmt, rows, k, mt, cfg, mode=mode)
         except q.QmvError as e:
             assert cfg is not None and e.code == q.QMV_ETOOBIG
