@@ -53,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
 # qmv_q4k launch on the headline workload, valid only for the kernel sources
 # whose hash it is recorded under (profiles/qmv_stream_kernel_full_captures.md).
-NCU_TRAFFIC = {"c2d5b7977e381002": 9488384}
+NCU_TRAFFIC = {"0b170fe643c24bb1": 9488128}
 
 KERNEL_SOURCES = ["qmv_device.cuh", "qmv_formats.cuh", "qmv_kernel.cuh", "qmv_launch.cuh", "qmv_q4k.cu"]
 
