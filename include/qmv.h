@@ -90,11 +90,15 @@ int qmv_q4_0(const void *w, const float *x, float *y, int rows, int k, cudaStrea
  * y[i, r] = sum_j W[r, j] * x[i, j] for the m rows of x.
  * x: f32 [m, k] row-major, 16-byte aligned; y: f32 [m, rows] row-major;
  * w and k as for the matvec of the same format; m >= 1. m == 1 runs the
- * matvec; otherwise each launch handles a tile of 2..8 rows of x (ceil(m/8)
- * balanced tiles, each reading W once), decoding every weight once per tile
- * and accumulating the m dot products in f32. Numerics: each decoded weight
- * is the round-to-nearest f32 of its exact value; results agree with an f64
- * reference to a scale-relative error far below 1e-4 per row of y.
+ * matvec; otherwise the tensor-core kernel, one launch per tile of 2..8 rows
+ * of x (ceil(m/8) balanced tiles, each reading W once; rows of any length, in
+ * k-chunks inside the launch), decoding every weight once per tile and
+ * accumulating the m dot products in f32. Numerics: each decoded weight is
+ * the round-to-nearest f32 of its exact value; results agree with an f64
+ * reference to a scale-relative error far below 1e-4 per row of y. Each plan
+ * is deterministic; independent calls (qmv_set_weight_prefetch mode 2) use
+ * smaller k-chunks, so rows longer than 2048 weights may round differently
+ * there than in plain or chained calls, within the same bound.
  * Cites hanzo-ml src/vulkan_backend.rs, matmul_q4k_gpu / matmul_q6k_gpu /
  * matmul_q8_gpu (decode once, reuse across up to MATMUL_Q_MAX_M = 8 rows). */
 int qmm_q4k(const void *w, const float *x, float *y, int rows, int k, int m, cudaStream_t stream);
