@@ -137,6 +137,11 @@ def test_batch_argument_errors(q):
     assert q.qmm_q4k(w, x, y, 2, 300, 2, check=False) == q.QMV_EINVAL
     assert q.qmm_q4k(w, x.data_ptr() + 4, y, 2, 256, 2, check=False) == q.QMV_EALIGN
     assert q.qmm_q8_0(w, x, y, 2, 48, 2, check=False) == q.QMV_EINVAL
+    assert q.qmm_q5k(w, x, y, 2, 300, 2, check=False) == q.QMV_EINVAL       # k not a multiple of 256
+    assert q.qmm_q5k(w, x, y, 2, 256, 0, check=False) == q.QMV_EINVAL       # m = 0
+    assert q.qmm_q4_0(w, x, y, 2, 48, 2, check=False) == q.QMV_EINVAL       # k not a multiple of 32
+    assert q.qmm_q4_0(w, x.data_ptr() + 4, y, 2, 64, 2, check=False) == q.QMV_EALIGN
+    assert q.qmm_q4_0(w, x, y, -1, 64, 2, check=False) == q.QMV_EINVAL      # rows < 1
 
 
 @pytest.mark.parametrize("fmt,rows,k", [("q4k", 300, 4096), ("q6k", 97, 14336), ("q8_0", 500, 4096),
