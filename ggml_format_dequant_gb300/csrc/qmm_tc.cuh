@@ -186,13 +186,34 @@ struct XFrag {
     uint32_t sh[4];
 };
 
-// The lane's fragments of one slice: its row of x (zeros when !live), groups
-// 0 .. ng - 1 starting at src = &x[row, 32 G + 4t]; inv receives 2^-s, s the
-// power of two that puts the slice's maximum (over the four lanes of the row)
-// in [2^14, 2^15). sums: the lane's 32 bytes of shared memory (Q4_K unpacked).
-template <bool SUMS, bool P>
-__device__ __forceinline__ void tc_load_x(const float* src, bool live, int ng, bool lo_lane, uint32_t sums, XFrag& xf,
-                                          float& inv) {
+// The slice's power-of-two scale from the maximum |x| a lane holds: 2^s puts
+// the maximum over the lanes of the row (xor masks given) in [2^14, 2^15);
+// returns 2^s, inv receives 2^-s.
+__device__ __forceinline__ float tc_scale(float amax, bool partner, float& inv) {
+    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
+    if (partner) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 16));
+    int s = 0;
+    if (amax > 0.0f) {
+        s = 141 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
+        s = s > 126 ? 126 : s;
+    }
+    inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+    return __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
+}
+
+__device__ __forceinline__ float abs_max4(float m, float4 v) {
+    return fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+}
+
+// Unpacked fragments (5..8 rows of x): the lane's row of x is row g (zeros
+// when !live), groups 0 .. ng - 1 from src = &x[g, 32 G + 4t]; the lane makes
+// hi and lo of its 8 values a group. inv receives 2^-s of the slice's scale.
+// Q4_K / Q5_K (SUMS): the lane's partial group sums (times 1/8, hi then lo)
+// go to its 32 bytes of shared memory at sums.
+template <bool SUMS>
+__device__ __forceinline__ void tc_load_x_pair(const float* src, bool live, int ng, uint32_t sums, XFrag& xf,
+                                               float& inv) {
     // all 64 values first (one round of loads), then the slice maximum
     float4 u[2 * TC_GROUPS_PER_SLICE];
 #pragma unroll
@@ -206,44 +227,23 @@ __device__ __forceinline__ void tc_load_x(const float* src, bool live, int ng, b
     }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 2 * TC_GROUPS_PER_SLICE; i++)
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(u[i].x), fabsf(u[i].y)), fmaxf(fabsf(u[i].z), fabsf(u[i].w))));
-    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 2));
-    int s = 0;
-    if (amax > 0.0f) {
-        s = 141 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
-        s = s > 126 ? 126 : s;
-    }
-    const float p2 = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
-    inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-    const float neg = lo_lane ? -1.0f : 0.0f;
+    for (int i = 0; i < 2 * TC_GROUPS_PER_SLICE; i++) amax = abs_max4(amax, u[i]);
+    const float p2 = tc_scale(amax, false, inv);
     if (SUMS) {
         // group sums of the lane's eight values (scaled: the power of two
         // commutes with the rounding), before the conversion frees u
-        float ps[TC_GROUPS_PER_SLICE];
-#pragma unroll
-        for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
-            const float4 a = u[2 * j], b = u[2 * j + 1];
-            ps[j] = (((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w))) * p2;
-        }
-        uint32_t sl[4];
+        uint32_t sh[4], sl[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            const float a = ps[2 * i] * 0.125f, b = ps[2 * i + 1] * 0.125f;
-            const uint32_t hs = pack_h2(a, b);
-            const float2 f = unpack_h2(hs);
-            if (P) {
-                xf.sh[i] = pack_h2(__fmaf_rn(f.x, neg, a), __fmaf_rn(f.y, neg, b));
-            } else {
-                xf.sh[i] = hs;
-                sl[i] = pack_h2(a - f.x, b - f.y);
-            }
+            const float4 a0 = u[4 * i], a1 = u[4 * i + 1], b0 = u[4 * i + 2], b1 = u[4 * i + 3];
+            const float a = ((((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w))) * p2) * 0.125f;
+            const float b = ((((b0.x + b0.y) + (b0.z + b0.w)) + ((b1.x + b1.y) + (b1.z + b1.w))) * p2) * 0.125f;
+            sh[i] = pack_h2(a, b);
+            const float2 f = unpack_h2(sh[i]);
+            sl[i] = pack_h2(a - f.x, b - f.y);
         }
-        if (!P) {
-            sts128(sums, make_uint4(xf.sh[0], xf.sh[1], xf.sh[2], xf.sh[3]));
-            sts128(sums + 16u, make_uint4(sl[0], sl[1], sl[2], sl[3]));
-        }
+        sts128(sums, make_uint4(sh[0], sh[1], sh[2], sh[3]));
+        sts128(sums + 16u, make_uint4(sl[0], sl[1], sl[2], sl[3]));
     }
 #pragma unroll
     for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
@@ -253,19 +253,64 @@ __device__ __forceinline__ void tc_load_x(const float* src, bool live, int ng, b
         const uint32_t h0 = pack_h2(v[0], v[2]), h1 = pack_h2(v[1], v[3]);
         const uint32_t h2 = pack_h2(v[4], v[6]), h3 = pack_h2(v[5], v[7]);
         const float2 f0 = unpack_h2(h0), f1 = unpack_h2(h1), f2 = unpack_h2(h2), f3 = unpack_h2(h3);
-        if (P) {
-            // hi lanes keep v (its pack is hi again), lo lanes v - hi
-            xf.h[j][0] = pack_h2(__fmaf_rn(f0.x, neg, v[0]), __fmaf_rn(f0.y, neg, v[2]));
-            xf.h[j][1] = pack_h2(__fmaf_rn(f1.x, neg, v[1]), __fmaf_rn(f1.y, neg, v[3]));
-            xf.h[j][2] = pack_h2(__fmaf_rn(f2.x, neg, v[4]), __fmaf_rn(f2.y, neg, v[6]));
-            xf.h[j][3] = pack_h2(__fmaf_rn(f3.x, neg, v[5]), __fmaf_rn(f3.y, neg, v[7]));
-        } else {
-            xf.h[j][0] = h0; xf.h[j][1] = h1; xf.h[j][2] = h2; xf.h[j][3] = h3;
-            xf.l[j][0] = pack_h2(v[0] - f0.x, v[2] - f0.y);
-            xf.l[j][1] = pack_h2(v[1] - f1.x, v[3] - f1.y);
-            xf.l[j][2] = pack_h2(v[4] - f2.x, v[6] - f2.y);
-            xf.l[j][3] = pack_h2(v[5] - f3.x, v[7] - f3.y);
+        xf.h[j][0] = h0; xf.h[j][1] = h1; xf.h[j][2] = h2; xf.h[j][3] = h3;
+        xf.l[j][0] = pack_h2(v[0] - f0.x, v[2] - f0.y);
+        xf.l[j][1] = pack_h2(v[1] - f1.x, v[3] - f1.y);
+        xf.l[j][2] = pack_h2(v[4] - f2.x, v[6] - f2.y);
+        xf.l[j][3] = pack_h2(v[5] - f3.x, v[7] - f3.y);
+    }
+}
+
+// Packed fragments (2..4 rows of x): lanes g and g + 4 (lane ^ 16) share row
+// g & 3 of x; lane g holds hi (MMA columns 0-3), its partner lo (4-7). Each
+// of the two converts half of the row's values, the first 16-column half of
+// every group (positions 4t..) in lane g and the second (16 + 4t..) in the
+// partner, and they trade the parts the other needs: lane g sends the lo of
+// its half and receives the hi of the other. inv receives 2^-s; Q4_K / Q5_K
+// (SUMS): xf.sh holds the pair's partial group sums (times 1/8), hi in lane
+// g, lo in the partner.
+template <bool SUMS>
+__device__ __forceinline__ void tc_load_x_split(const float* src, bool live, int ng, bool lo_lane, XFrag& xf,
+                                                float& inv) {
+    const int off = lo_lane ? 16 : 0;
+    float4 u[TC_GROUPS_PER_SLICE];
+#pragma unroll
+    for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
+        u[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (live && j < ng) u[j] = __ldg(reinterpret_cast<const float4*>(src + 32 * j + off));
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) amax = abs_max4(amax, u[j]);
+    const float p2 = tc_scale(amax, true, inv);
+    const float neg = lo_lane ? -1.0f : 0.0f;
+    if (SUMS) {
+        float ps[TC_GROUPS_PER_SLICE];
+#pragma unroll
+        for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
+            ps[j] = ((u[j].x + u[j].y) + (u[j].z + u[j].w)) * p2;
+            ps[j] += __shfl_xor_sync(FULL, ps[j], 16);   // both halves of the lane pair's positions
         }
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float a = ps[2 * i] * 0.125f, b = ps[2 * i + 1] * 0.125f;
+            const float2 f = unpack_h2(pack_h2(a, b));
+            xf.sh[i] = pack_h2(__fmaf_rn(f.x, neg, a), __fmaf_rn(f.y, neg, b));
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < TC_GROUPS_PER_SLICE; j++) {
+        const float4 v = make_float4(u[j].x * p2, u[j].y * p2, u[j].z * p2, u[j].w * p2);
+        // MMA-k order of a half: (4t, 4t+2) then (4t+1, 4t+3)
+        const uint32_t h0 = pack_h2(v.x, v.z), h1 = pack_h2(v.y, v.w);
+        const float2 f0 = unpack_h2(h0), f1 = unpack_h2(h1);
+        const uint32_t l0 = pack_h2(v.x - f0.x, v.z - f0.y), l1 = pack_h2(v.y - f1.x, v.w - f1.y);
+        const uint32_t r0 = __shfl_xor_sync(FULL, lo_lane ? h0 : l0, 16);
+        const uint32_t r1 = __shfl_xor_sync(FULL, lo_lane ? h1 : l1, 16);
+        xf.h[j][0] = lo_lane ? r0 : h0;
+        xf.h[j][1] = lo_lane ? r1 : h1;
+        xf.h[j][2] = lo_lane ? l0 : r0;
+        xf.h[j][3] = lo_lane ? l1 : r1;
     }
 }
 
@@ -693,8 +738,11 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
         ng = max(0, min(TC_GROUPS_PER_SLICE, p.ngroups - G));
         const bool live = xr < p.m && ng > 0;
         float inv;
-        tc_load_x<F::SUMS, P>(p.x + static_cast<long long>(xr) * p.k + 32 * G + 4 * t, live, ng, P && g >= 4, sums_l,
-                              xf, inv);
+        const float* src = p.x + static_cast<long long>(xr) * p.k + 32 * G + 4 * t;
+        if constexpr (P)
+            tc_load_x_split<F::SUMS>(src, live, ng, g >= 4, xf, inv);
+        else
+            tc_load_x_pair<F::SUMS>(src, live, ng, sums_l, xf, inv);
         inv0 = __shfl_sync(FULL, inv, 8 * t);
         inv1 = __shfl_sync(FULL, inv, 8 * t + 4);
     };
