@@ -68,8 +68,31 @@ def test_host_side_validation_without_gpu(lib):
     assert lib.qmv_q8_dp4a_blockdots(A, A + 1, A, 4, 32, stream=S, check=False) == lib.QMV_EALIGN
     assert lib.qmv_selftest_wait_timeout(0, stream=S, check=False) == lib.QMV_EINVAL
     assert lib.qmv_selftest_wait_timeout(200_000_000, stream=S, check=False) == lib.QMV_EINVAL
+    # the batched products: bad k, m, rows, pointers and alignment, for every format
+    for fmt, qk in (("q4k", 256), ("q6k", 256), ("q8_0", 32), ("q5k", 256), ("q4_0", 32)):
+        f = getattr(lib, f"qmm_{fmt}")
+        assert f(A, A, A, 4, qk + 1, 2, stream=S, check=False) == lib.QMV_EINVAL
+        assert f(A, A, A, 4, qk, 0, stream=S, check=False) == lib.QMV_EINVAL
+        assert f(A, A, A, 0, qk, 2, stream=S, check=False) == lib.QMV_EINVAL
+        assert f(None, A, A, 4, qk, 2, stream=S, check=False) == lib.QMV_EINVAL
+        assert f(A, A + 4, A, 4, qk, 2, stream=S, check=False) == lib.QMV_EALIGN
+        assert f(A, A, A + 2, 4, qk, 2, stream=S, check=False) == lib.QMV_EALIGN
     with pytest.raises(lib.QmvError):
         lib.qmv_q4k(A, A, A, 4, 300, stream=S)
+
+
+def test_batch_launch_count():
+    """The kernel launches a batched call makes (bench.py counts them): the
+    matvec for one row of x, else one tensor-core launch per tile of up to 8
+    rows, whatever the format and row length."""
+    import ggml_format_dequant_gb300 as q
+    for fmt in ("q4k", "q6k", "q8_0", "q5k", "q4_0"):
+        for k in (256, 4096, 65536):
+            assert q.qmm_launches(fmt, k, 1) == 1
+            for m in (2, 3, 8):
+                assert q.qmm_launches(fmt, k, m) == 1
+            assert q.qmm_launches(fmt, k, 9) == 2
+            assert q.qmm_launches(fmt, k, 17) == 3
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
