@@ -402,7 +402,10 @@ def run_ours(args):
         names = [n for n in synth.CONFIGS if n == HEADLINE or any(n.startswith(o) for o in args.only.split(","))]
     for name in names:
         w2 = Workload(q, torch, name, l2, device)
-        n = max(64, w2.copies)
+        # graphs of at least 256 calls: a graph boundary serialises calls, so
+        # short graphs under-state independent calls (Q4_K dp4a 4096 x 4096
+        # measured 1.77 / 1.67 / 1.63 us a call in graphs of 64 / 256 / 1000)
+        n = max(256, w2.copies)
         row = None
         for mode in (1, 0, 2):
             q.qmv_set_weight_prefetch(mode)
