@@ -1,7 +1,8 @@
-"""The launch planner without a GPU: for each shape (the five workloads, the
-GPU test shapes and forced configurations) the plan is taken from the library
-for a described GB300 and the kernel's work assignment is replayed here, so
-that every index the kernel forms is checked before it runs:
+"""The launch planners without a GPU: for each shape (the configured
+workloads, the GPU test shapes, forced configurations and the seeded random
+cases) the plan is taken from the library for a described GB300 and the
+kernel's work assignment is replayed here, so that every index the kernel
+forms is checked before it runs. For the matvec kernel:
 
 * every (row, unit) pair of every matrix is decoded exactly once;
 * every shared-memory read of a unit (including the bytes a format's loads
@@ -12,8 +13,14 @@ that every index the kernel forms is checked before it runs:
 * parked partials stay inside the CTA's table, and the shared-memory regions
   are disjoint and fit the device.
 
-The replay restates the kernel's arithmetic (qmv_kernel.cuh) in numpy; it is a
-check of index bounds, not of numerics."""
+For the tensor-core batch kernel (qmm_tc.cuh): the k-chunks tile every row,
+every row's chunk copy fits its slot row, every staged-row read of a tile
+(spare rows included) stays inside its slot, and the shared-memory regions
+are disjoint and fit the device; independent-call plans also fit in half an
+SM.
+
+The replays restate the kernels' arithmetic (qmv_kernel.cuh, qmm_tc.cuh) in
+numpy; they check index bounds, not numerics."""
 
 import numpy as np
 import pytest
