@@ -448,3 +448,35 @@ def test_random_batch_plans(q, fmt, rows, k, m, cfg, mode):
             tc_replay(q, fmt, rows, k, mt, cfg, mode=mode)
         except q.QmvError as e:
             assert cfg is not None and e.code == q.QMV_ETOOBIG
+
+
+def _tc_sweep(n=240):
+    import synth
+    fmts = list(TC_FMT)
+    z = synth.Stream(9090).draw(n * 8).reshape(n, 8)
+    out = []
+    for i in range(n):
+        d = [int(v >> np.uint64(33)) for v in z[i]]
+        fmt = fmts[d[0] % len(fmts)]
+        qk = TC_FMT[fmt][1]
+        k = (1 + d[1] % (20000 // qk)) * qk
+        rows = 1 + d[2] % 3000
+        m = 1 + d[3] % 8
+        cfg = None
+        if d[4] % 3 == 0:
+            cfg = dict(ctas=d[5] % 200, chunk_rows=d[6] % 40, chunks=d[7] % 6, warps=[0, 1, 2, 5, 8, 16][d[4] % 6])
+        mode = 2 if d[6] % 2 else 0
+        out.append((fmt, rows, k, m, cfg, mode))
+    return out
+
+
+@pytest.mark.parametrize("fmt,rows,k,m,cfg,mode", _tc_sweep())
+def test_tc_plan_sweep(q, fmt, rows, k, m, cfg, mode):
+    """A wider seeded sweep of tensor-core plans (rows up to 3000, k up to
+    20000, forced configurations, both launch modes), replayed on the host
+    only: every plan the planner returns keeps its copies and reads in bounds;
+    a forced plan may be refused, never a default one."""
+    try:
+        tc_replay(q, fmt, rows, k, m, cfg, mode=mode)
+    except q.QmvError as e:
+        assert cfg is not None and e.code == q.QMV_ETOOBIG
