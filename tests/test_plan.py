@@ -480,3 +480,40 @@ def test_tc_plan_sweep(q, fmt, rows, k, m, cfg, mode):
         tc_replay(q, fmt, rows, k, m, cfg, mode=mode)
     except q.QmvError as e:
         assert cfg is not None and e.code == q.QMV_ETOOBIG
+
+
+MV_QK = {"q4k": 256, "q6k": 256, "q8_0": 32, "q5k": 256, "q4_0": 32, "q8d": 32, "q4d": 256, "q6d": 256,
+         "moe": 256, "moe6": 256, "moe4d": 256, "moe8": 32, "moe40": 32, "moe5": 256, "moe6d": 256}
+
+
+def _mv_sweep(n=240):
+    import synth
+    fams = list(MV_QK)
+    z = synth.Stream(8080).draw(n * 8).reshape(n, 8)
+    out = []
+    for i in range(n):
+        d = [int(v >> np.uint64(33)) for v in z[i]]
+        fam = fams[d[0] % len(fams)]
+        qk = MV_QK[fam]
+        k = (1 + d[1] % (8192 // qk)) * qk
+        rows = 1 + d[2] % 2500
+        slots = 1 + d[3] % 8 if fam.startswith("moe") else 1
+        cfg = None
+        if d[4] % 3 == 0:
+            cfg = dict(ctas=d[5] % 200, chunk_rows=d[6] % 12, chunks=d[7] % 5, unroll=d[4] % 3,
+                       warps=[0, 2, 4, 8, 16][d[5] % 5])
+        mode = 2 if d[6] % 2 else 0
+        out.append((fam, rows, k, slots, cfg, mode))
+    return out
+
+
+@pytest.mark.parametrize("fam,rows,k,slots,cfg,mode", _mv_sweep())
+def test_matvec_plan_sweep(q, fam, rows, k, slots, cfg, mode):
+    """A wider seeded sweep of matvec and MoE plans (rows up to 2500, k up to
+    8192, 1-8 slots, forced configurations, both launch modes), replayed on the
+    host only: every (row, unit) decoded once, every read inside its slot; a
+    forced plan may be refused, never a default one."""
+    try:
+        replay(q, fam, rows, k, slots, cfg, mode=mode)
+    except q.QmvError as e:
+        assert cfg is not None and e.code == q.QMV_ETOOBIG
