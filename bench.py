@@ -7,18 +7,21 @@ k = 4096, seed 1): qmv_q4k reads the packed weight straight from HBM, decodes
 it in registers and writes y. Consecutive steps cycle through enough distinct
 copies of the weight (more than 3x the L2 size in total) that every call reads
 its weight HBM-cold. The steps are independent (each reads the same x), and
-are launched as such (qmv_set_weight_prefetch mode 2: a call overlaps the
-previous one and waits for it only before writing y); ``--chain`` times a
-dependent decode chain instead (mode 1) and ``--isolated`` plain launches, and
-``per_config`` reports all three for every workload. The K timed steps are one
-CUDA-graph replay bracketed by CUDA events on the launching stream, with a
-barrier and a device synchronize on both sides; the line reports the max over
-ranks.
+are launched as such (QMV_OVERLAP_INDEPENDENT: a call overlaps the previous
+one and waits for it only before writing y); ``--chain`` times a dependent
+decode chain instead (QMV_OVERLAP_CHAIN) and ``--isolated`` plain launches.
+The K timed steps are one CUDA-graph replay bracketed by CUDA events on the
+launching stream, with a barrier and a device synchronize on both sides; the
+line reports the max over ranks.
 
-The printed JSON line also carries the other four workloads of the suite
-(``per_config``), the roofline of the timed kernel against the measured HBM
-copy bandwidth, the end-to-end number through the public API with host
-buffers, the CPU oracle as a baseline and the SM clocks seen while timing.
+Before the headline, one short JSON line per workload of the suite gives its
+us per call and fraction of the measured HBM copy bandwidth in all three
+launch modes (the metric's five workloads last). The headline line, printed
+last, carries the five workloads' figures in ``config.us_per_call``, the
+roofline of the timed kernel against the measured HBM copy bandwidth, the
+end-to-end number through the public API with host buffers, the CPU oracle as
+a baseline (whose output also checks the timed calls' and the end-to-end
+calls' y), and the SM clocks seen while timing.
 
 ``--impl reference`` times the CPU oracle (plain C, f64) on the same workload
 on the host cores: the only other implementation of the method available here
@@ -51,9 +54,9 @@ NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
-# qmv_q4k launch on the headline workload, valid only for the kernel sources
-# whose hash it is recorded under (profiles/qmv_stream_kernel_full_captures.md).
-NCU_TRAFFIC = {"0b170fe643c24bb1": 9488128}
+# qmv_q4k launch on the headline workload, per launch mode, valid only for the
+# kernel sources whose hash it is recorded under.
+NCU_TRAFFIC = {}
 
 KERNEL_SOURCES = ["qmv_device.cuh", "qmv_formats.cuh", "qmv_kernel.cuh", "qmv_launch.cuh", "qmv_q4k.cu"]
 
@@ -217,18 +220,19 @@ class Workload:
             q.quantize_act_q8(self.x, self.xq, self.xs, None, m, self.k)
         self.q = q
         self.cfg = None   # optional forced launch configuration (dict), for tuning sweeps
+        self.overlap = 0  # launch overlap of every call (q.OVERLAP_*)
 
     def call(self, i: int, stream: int, with_quant: bool = False) -> int:
         """Enqueue call i; returns the number of kernels it launched."""
-        q, w, cfg = self.q, self.w[i % self.copies], self.cfg
+        q, w, cfg, ov = self.q, self.w[i % self.copies], self.cfg, self.overlap
         self.y = self.ys[i % self.copies]
         if self.kind == "q4k":
-            q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
+            q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg, overlap=ov)
         elif self.kind in ("q6k", "q5k", "q4_0"):
-            getattr(q, f"qmv_{self.kind}")(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg)
+            getattr(q, f"qmv_{self.kind}")(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg, overlap=ov)
         elif self.kind.startswith("qmm_"):
             m = self.c["m"]
-            getattr(q, self.kind)(w, self.x, self.y, self.rows, self.k, m, stream=stream, cfg=cfg)
+            getattr(q, self.kind)(w, self.x, self.y, self.rows, self.k, m, stream=stream, cfg=cfg, overlap=ov)
             return q.qmm_launches(self.kind[4:], self.k, m)
         elif self.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a"):
             n = 1
@@ -236,13 +240,13 @@ class Workload:
                 q.quantize_act_q8(self.x, self.xq, self.xs, None, 1, self.k, stream=stream)
                 n = 2
             fn = {"q8_0_dp4a": q.qmv_q8_dp4a, "q4k_dp4a": q.qmv_q4k_dp4a, "q6k_dp4a": q.qmv_q6k_dp4a}[self.kind]
-            fn(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg)
+            fn(w, self.xq, self.xs, self.y, self.rows, self.k, stream=stream, cfg=cfg, overlap=ov)
             return n
         elif self.kind in MOE_F32:
             c = self.c
             fn = getattr(q, f"moe_qmv_{self.kind[4:]}")
             fn(w, self.x, self.y, self.rows, self.k, self.ids[i % len(self.ids)], c["slots"],
-               c["n_experts"], stream=stream, cfg=cfg)
+               c["n_experts"], stream=stream, cfg=cfg, overlap=ov)
         elif self.kind in ("moe_q4k_dp4a", "moe_q6k_dp4a"):
             c = self.c
             n = 1
@@ -251,7 +255,7 @@ class Workload:
                 n = 2
             fn = q.moe_qmv_q4k_dp4a if self.kind == "moe_q4k_dp4a" else q.moe_qmv_q6k_dp4a
             fn(w, self.xq, self.xs, self.y, self.rows, self.k, self.ids[i % len(self.ids)],
-               c["slots"], c["n_experts"], stream=stream, cfg=cfg)
+               c["slots"], c["n_experts"], stream=stream, cfg=cfg, overlap=ov)
             return n
         return 1
 
@@ -307,6 +311,25 @@ def time_graph(torch, wl: Workload, n_calls: int, with_quant=False, replays=1, b
     return ms, launches / n_calls, g, s
 
 
+# The five workloads the metric is quoted on, in order (the first is the small
+# case; the second the headline).
+METRIC_CONFIGS = ["q4k_256x1024", "q4k_4096x4096", "q8_0_dp4a_14336x4096", "moe_q4k_e128_n768_k2048_s8",
+                  "q6k_4096x14336"]
+MODE_NAMES = {0: "isolated", 1: "chain", 2: "independent"}
+DP4A_KINDS = ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a", "moe_q4k_dp4a", "moe_q6k_dp4a")
+
+
+def workload_line(name, times, peak):
+    """One short JSON line per workload: us per call and fraction of the
+    measured HBM peak in each launch mode (and with the activation
+    quantization for the dp4a kinds)."""
+    wb = weight_bytes(name)
+    d = {"workload": name, "packed_weight_bytes": wb}
+    for key, ms in times.items():
+        d[key] = {"us": round(ms * 1e3, 3), "frac": round(wb / (ms * 1e-3) / 1e9 / peak, 4)}
+    return d
+
+
 def run_ours(args):
     import torch
 
@@ -338,15 +361,16 @@ def run_ours(args):
 
     # ------------------------------------------------ the headline workload
     # The timed calls are independent of one another (every call reads the
-    # same x, like the Q / K / V projections of one activation), so they run
-    # in mode 2 of qmv_set_weight_prefetch: each call is scheduled while the
-    # previous one runs, streams its weights and decodes at once, and waits for
-    # the previous call only before it writes y. --chain times the
-    # conservative decode chain (mode 1: x is read only after the previous call
-    # is done), --isolated plain launches (mode 0); per_config reports all three.
+    # same x, like the Q / K / V projections of one activation), so they are
+    # launched with QMV_OVERLAP_INDEPENDENT: each call is scheduled while the
+    # previous one runs, streams its weights and decodes at once, and waits
+    # for the previous call only before it writes y. --chain times a
+    # dependent decode chain (QMV_OVERLAP_CHAIN: x is read only after the
+    # previous call is done), --isolated plain launches; the per-workload
+    # lines report all three.
     head_mode = args.headline_mode if args.headline_mode is not None else (0 if args.isolated else (1 if args.chain else 2))
-    q.qmv_set_weight_prefetch(head_mode)
     wl = Workload(q, torch, HEADLINE, l2, device)
+    wl.overlap = head_mode
     K, W = args.steps, args.warmup
     # warm-up steps (untimed)
     _, _, gw, sw = time_graph(torch, wl, max(W, 1))
@@ -362,16 +386,19 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
     with torch.cuda.stream(sk):
+        # a short device-side delay ahead of the start event, so that the
+        # graph launch is queued on the device before the timed region opens
+        # (the region then holds the K steps alone, not the host's launch)
+        torch.cuda._sleep(100000)
         e0.record(sk)
         gk.replay()
         e1.record(sk)
     e1.synchronize()
     torch.cuda.synchronize()
-    t_wall1 = time.time()
     barrier()
     ms_total = e0.elapsed_time(e1)
+    head_y = wl.y.detach().cpu().numpy().copy()   # the last call's output (kept for the parity check)
     post_t0 = time.time()
     while time.time() - post_t0 < 0.5:
         with torch.cuda.stream(sk):
@@ -387,52 +414,60 @@ def run_ours(args):
     achieved = alg / (ms_step * 1e-3) / 1e9
 
     # ------------------------------------------------ end to end (host buffers)
-    e2e = end_to_end(torch, q, wl, device, K)
+    e2e, e2e_y = end_to_end(torch, q, wl, device, K)
 
-    # ------------------------------------------------ the other workloads
-    # every workload: a decode chain (mode 1, the headline's), isolated calls
-    # (mode 0), and a stream of independent calls (mode 2: the calls share no
-    # inputs with the call before, like the Q / K / V projections of one
-    # activation)
-    per_config = {}
+    # ------------------------------------------------ every workload, three modes
+    # A stream of independent calls (they share no inputs with the call
+    # before, like the Q / K / V projections of one activation), a dependent
+    # decode chain, and isolated calls.
+    lines = {}
     del wl, gk, gw
     torch.cuda.empty_cache()
     names = [HEADLINE] if args.headline_only else list(synth.CONFIGS)
     if args.only:
         names = [n for n in synth.CONFIGS if n == HEADLINE or any(n.startswith(o) for o in args.only.split(","))]
+    # the metric's five workloads last, so that they end up next to the headline
+    names = [n for n in names if n not in METRIC_CONFIGS] + [n for n in METRIC_CONFIGS if n in names]
     for name in names:
         w2 = Workload(q, torch, name, l2, device)
         # graphs of at least 256 calls: a graph boundary serialises calls, so
         # short graphs under-state independent calls (Q4_K dp4a 4096 x 4096
         # measured 1.77 / 1.67 / 1.63 us a call in graphs of 64 / 256 / 1000)
         n = max(256, w2.copies)
-        row = None
-        for mode in (1, 0, 2):
-            q.qmv_set_weight_prefetch(mode)
+        times = {}
+        for mode in (2, 1, 0):
+            w2.overlap = mode
             ms, _, g2, _ = time_graph(torch, w2, n, replays=4)
             del g2
-            tag = {1: "", 0: "isolated_", 2: "independent_"}[mode]
-            if mode == 1:
-                row = config_row(name, ms, peak, peak_kind, w2.copies)
-            else:
-                row[tag + "us_per_call"] = round(ms * 1e3, 3)
-                row[tag + "packed_gbs"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9, 1)
-                row[tag + "frac_of_measured_hbm"] = round(weight_bytes(name) / (ms * 1e-3) / 1e9 / peak, 4)
-            if w2.kind in ("q8_0_dp4a", "q4k_dp4a", "q6k_dp4a", "moe_q4k_dp4a", "moe_q6k_dp4a") and mode in (0, 1):
+            times[MODE_NAMES[mode]] = ms
+            if w2.kind in DP4A_KINDS and mode in (1, 0):
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
-                row[tag + "with_quantize_act_q8_us_per_call"] = round(msq * 1e3, 3)
+                times[MODE_NAMES[mode] + "_with_quantize"] = msq
                 del g3
-        per_config[name] = row
+        lines[name] = workload_line(name, times, peak)
+        if rank == 0:
+            print(json.dumps(lines[name]), flush=True)
         del w2
         torch.cuda.empty_cache()
-    q.qmv_set_weight_prefetch(0)
     sampler.stop()
     clocks = sampler.summary(*clock_window)
     clocks["window"] = "nvidia-smi every 50 ms over a 0.5 s pre-roll, the timed region and a 0.5 s post-roll of the same graph"
 
-    traffic = NCU_TRAFFIC.get(kernel_hash())
-    cpu = cpu_baseline(args) if rank == 0 else None
+    traffic = NCU_TRAFFIC.get(kernel_hash(), {}).get(head_mode)
+    cpu, ref_y = cpu_baseline(args) if rank == 0 else (None, None)
     if rank == 0:
+        def srel(a, b):
+            return float(np.max(np.abs(a.astype(np.float64) - b)) / max(float(np.max(np.abs(b))), 1e-30))
+        parity = {"scale_rel_timed_calls": round(srel(head_y, ref_y), 9),
+                  "scale_rel_e2e": round(srel(e2e_y, ref_y), 9), "bound": 1e-4}
+        parity["ok"] = parity["scale_rel_timed_calls"] <= 1e-4 and parity["scale_rel_e2e"] <= 1e-4
+        e2e["matches_oracle"] = parity["scale_rel_e2e"] <= 1e-4
+        summary = {}
+        for nm in METRIC_CONFIGS:
+            if nm in lines:
+                summary[nm] = {m: lines[nm][m]["us"] for m in ("independent", "chain", "isolated") if m in lines[nm]}
+                summary[nm]["independent_frac"] = lines[nm]["independent"]["frac"]
+                summary[nm]["chain_frac"] = lines[nm]["chain"]["frac"]
         line = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -444,22 +479,20 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "i8dp4a+f32",
+            "dtype": "f32 activation as 3 exact int8 limbs, int32 dp4a dots, f32 sums",
             "data": "synthetic (seeded splitmix64 Q4_K blocks and N(0,1) activations; no model weights)",
             "config": {
                 "workload": "q4k_4096x4096: Q4_K matvec rows=4096 k=4096 (attention-projection shape), seed 1",
                 "rows": 4096, "k": 4096, "format": "Q4_K", "packed_weight_bytes": wbytes,
-                "l2": f"inputs larger than L2: {per_config[HEADLINE]['rotation_copies']} rotated weight copies "
-                      f"({per_config[HEADLINE]['rotation_copies'] * wbytes / 2**20:.0f} MiB) vs L2 {l2 / 2**20:.0f} MiB",
+                "l2": f"inputs larger than L2: rotated weight copies ({lines[HEADLINE]['packed_weight_bytes']} B "
+                      f"each, >3x the {l2 / 2**20:.0f} MiB L2 in total)" if HEADLINE in lines else "",
                 "timing": "K calls captured in one CUDA graph, CUDA events on the launching stream",
-                "launch": {0: "isolated calls (qmv_set_weight_prefetch mode 0)",
-                           1: "dependent decode chain (mode 1): programmatic dependent launch, each call streams "
-                              "its weights while the previous call finishes, reads x after it",
-                           2: "independent calls (mode 2): programmatic dependent launch, each call streams its "
-                              "weights and decodes while the previous call finishes, writes y after it"}[head_mode],
-                "dependent_chain_us_per_call": per_config[HEADLINE]["us_per_call"],
-                "isolated_us_per_call": per_config[HEADLINE].get("isolated_us_per_call"),
-                "independent_us_per_call": per_config[HEADLINE].get("independent_us_per_call"),
+                "launch": {0: "isolated calls (plain launches)",
+                           1: "dependent decode chain (QMV_OVERLAP_CHAIN): each call streams its weights while the "
+                              "previous call finishes and reads x after it",
+                           2: "independent calls (QMV_OVERLAP_INDEPENDENT): each call streams its weights and "
+                              "decodes while the previous call finishes and writes y after it"}[head_mode],
+                "us_per_call": summary,
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             },
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -471,27 +504,11 @@ def run_ours(args):
             "gpu_launches": K,
             "clocks": clocks,
             "cpu_baseline": cpu,
-            "per_config": per_config,
+            "parity": parity,
         }
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
-
-
-def config_row(name, ms, peak, peak_kind, copies):
-    wb = weight_bytes(name)
-    gbs = wb / (ms * 1e-3) / 1e9
-    row = {"us_per_call": round(ms * 1e3, 3), "packed_weight_bytes": wb,
-           "packed_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
-           "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
-           "algorithmic_gbs": round(algorithmic_bytes(name) / (ms * 1e-3) / 1e9, 1),
-           "rotation_copies": copies}
-    m = synth.CONFIGS[name].get("m")
-    if m:
-        # a batch of m rows of x: time per row of x, against one matvec each
-        row["m"] = m
-        row["us_per_x_row"] = round(ms * 1e3 / m, 3)
-    return row
 
 
 def end_to_end(torch, q, wl, device, K):
@@ -499,7 +516,10 @@ def end_to_end(torch, q, wl, device, K):
     pinned host memory, run qmv_q4k, copy y back. The steps are enqueued on two
     streams that alternate, each with its own device buffers, so that one
     step's host-to-device copies overlap the previous step's kernel and
-    read-back (every step still moves its own inputs and result)."""
+    read-back (every step still moves its own inputs and result). Plain
+    launches: each call follows host-to-device copies of its own weights and
+    x, which no overlap mode may run ahead of. Returns the record and the last
+    step's output."""
     c = wl.c
     hw = torch.from_numpy(c["w"].reshape(-1)).pin_memory()
     hx = torch.from_numpy(c["x"]).pin_memory()
@@ -510,9 +530,6 @@ def end_to_end(torch, q, wl, device, K):
     streams = [torch.cuda.Stream() for _ in range(2)]
     main = torch.cuda.Stream()
     steps = max(2, min(K, 200))
-    # plain launches: each call follows host-to-device copies of its own
-    # weights and x, which no overlap mode may run ahead of
-    old_mode = q.qmv_set_weight_prefetch(0)
 
     def step(i):
         b = i & 1
@@ -538,13 +555,12 @@ def end_to_end(torch, q, wl, device, K):
     e1.record(main)
     e1.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    q.qmv_set_weight_prefetch(old_mode)
-    ok = all(bool(np.isfinite(h.numpy()).all()) for h in hy)
-    return {"value": round(weight_bytes(HEADLINE) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": hw.numel() + 4 * hx.numel(), "d2h_bytes_per_step": 4 * wl.rows,
-            "ms_per_step": round(ms, 4), "steps": steps, "finite": ok,
-            "pipelining": "two streams alternate steps: a step's host-to-device copies overlap the previous "
-                          "step's kernel and read-back"}
+    last = hy[(steps - 1) & 1].numpy().copy()
+    return ({"value": round(weight_bytes(HEADLINE) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+             "h2d_bytes_per_step": hw.numel() + 4 * hx.numel(), "d2h_bytes_per_step": 4 * wl.rows,
+             "ms_per_step": round(ms, 4), "steps": steps,
+             "pipelining": "two streams alternate steps: a step's host-to-device copies overlap the previous "
+                           "step's kernel and read-back"}, last)
 
 
 # ------------------------------------------------------------- CPU side
@@ -563,7 +579,7 @@ def cpu_baseline(args, seconds: float = 10.0) -> dict:
 
     c = synth.make_config(HEADLINE)
     n = cpu_cores()
-    oracle.qmv_threaded("q4k", c["w"], c["x"], 4096, 4096, n)   # load + warm
+    ref_y = oracle.qmv_threaded("q4k", c["w"], c["x"], 4096, 4096, n)   # load + warm; the expected output
     calls = 0
     t0 = time.perf_counter()
     while True:
@@ -581,12 +597,13 @@ def cpu_baseline(args, seconds: float = 10.0) -> dict:
         if time.perf_counter() - t1 >= seconds / 5:
             break
     dt1 = time.perf_counter() - t1
-    return {"value": round(calls * weight_bytes(HEADLINE) / dt / 1e9, 4), "unit": "GB/s", "cores": n,
-            "kind": "oracle",
-            "sample": f"{calls} full 4096x4096 Q4_K matvecs (f64 dequantize-then-dot), rows split over {n} threads, "
-                      f"{dt:.1f} s",
-            "single_thread": {"value": round(calls1 * weight_bytes(HEADLINE) / dt1 / 1e9, 4), "unit": "GB/s",
-                              "sample": f"{calls1} full matvecs on one thread, {dt1:.1f} s"}}
+    return ({"value": round(calls * weight_bytes(HEADLINE) / dt / 1e9, 4), "unit": "GB/s", "cores": n,
+             "kind": "oracle",
+             "sample": f"{calls} full 4096x4096 Q4_K matvecs (f64 dequantize-then-dot), rows split over {n} threads, "
+                       f"{dt:.1f} s",
+             "single_thread": {"value": round(calls1 * weight_bytes(HEADLINE) / dt1 / 1e9, 4), "unit": "GB/s",
+                               "sample": f"{calls1} full matvecs on one thread, {dt1:.1f} s"}},
+            np.asarray(ref_y, dtype=np.float64))
 
 
 def run_reference(args):
@@ -641,9 +658,9 @@ def run_profile(args):
     __graft_entry__.build()
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    if args.headline_mode is not None:
-        q.qmv_set_weight_prefetch(args.headline_mode)   # the launch mode (and plan) the bench times
     wl = Workload(q, torch, args.profile_workload, 0, device, copies=1)
+    if args.headline_mode is not None:
+        wl.overlap = args.headline_mode   # the launch mode (and plan) the bench times
     s = torch.cuda.current_stream().cuda_stream
     for i in range(args.warmup + args.steps):
         wl.call(i, s, with_quant=True)
@@ -660,7 +677,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="skip the per-config table")
     ap.add_argument("--headline-mode", type=int, choices=[0, 1, 2], default=None,
-                    help="launch mode of the headline calls (qmv_set_weight_prefetch); default 2")
+                    help="launch overlap of the headline calls (0 none, 1 chain, 2 independent); default 2")
     ap.add_argument("--only", default="", help="per-config table for the workloads whose names start with one of "
                                                "these comma-separated prefixes")
     ap.add_argument("--chain", action="store_true",

@@ -45,9 +45,14 @@ class QmvError(RuntimeError):
         super().__init__(msg)
 
 
-class qmv_cfg(ctypes.Structure):
-    _fields_ = [("ctas", ctypes.c_int), ("chunk_rows", ctypes.c_int), ("chunks", ctypes.c_int),
-                ("unroll", ctypes.c_int), ("warps", ctypes.c_int), ("cluster", ctypes.c_int)]
+# Launch overlap of one call (qmv_opts.overlap, see qmv.h).
+OVERLAP_NONE, OVERLAP_CHAIN, OVERLAP_INDEPENDENT = 0, 1, 2
+
+
+class qmv_opts(ctypes.Structure):
+    _fields_ = [("overlap", ctypes.c_int), ("ctas", ctypes.c_int), ("chunk_rows", ctypes.c_int),
+                ("chunks", ctypes.c_int), ("unroll", ctypes.c_int), ("warps", ctypes.c_int),
+                ("cluster", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -61,52 +66,51 @@ _SIG = {
     "moe_qmv_q4k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
     "qmv_q4k_dp4a": [_P, _P, _P, _P, _I, _I, _P],
     "moe_qmv_q6k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
-    "moe_qmv_q6k_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q6k_ex": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "moe_qmv_q4k_dp4a": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P],
-    "moe_qmv_q4k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
-    "qmv_q4k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _P],
+    "moe_qmv_q4k_dp4a_ex": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "qmv_q4k_dp4a_ex": [_P, _P, _P, _P, _I, _I, _P, _P],
     "qmv_q4k_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_q6k_dp4a": [_P, _P, _P, _P, _I, _I, _P],
-    "qmv_q6k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _P],
+    "qmv_q6k_dp4a_ex": [_P, _P, _P, _P, _I, _I, _P, _P],
     "qmv_q6k_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "moe_qmv_q6k_dp4a": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P],
-    "moe_qmv_q6k_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
-    "qmv_q4k_cfg": [_P, _P, _P, _I, _I, _P, _P],
-    "qmv_q6k_cfg": [_P, _P, _P, _I, _I, _P, _P],
-    "qmv_q8_0_cfg": [_P, _P, _P, _I, _I, _P, _P],
-    "qmv_q8_dp4a_cfg": [_P, _P, _P, _P, _I, _I, _P, _P],
-    "moe_qmv_q4k_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q6k_dp4a_ex": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "qmv_q4k_ex": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q6k_ex": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q8_0_ex": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q8_dp4a_ex": [_P, _P, _P, _P, _I, _I, _P, _P],
+    "moe_qmv_q4k_ex": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "qmv_dequant_q4k": [_P, _P, _I, _I, _P],
     "qmv_dequant_q6k": [_P, _P, _I, _I, _P],
     "qmv_dequant_q8_0": [_P, _P, _I, _I, _P],
     "qmv_dequant_q5k": [_P, _P, _I, _I, _P],
     "qmv_dequant_q4_0": [_P, _P, _I, _I, _P],
     "qmm_q4k": [_P, _P, _P, _I, _I, _I, _P],
-    "qmm_q4k_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q4k_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q6k": [_P, _P, _P, _I, _I, _I, _P],
-    "qmm_q6k_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q6k_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q8_0": [_P, _P, _P, _I, _I, _I, _P],
-    "qmm_q8_0_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q8_0_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q5k": [_P, _P, _P, _I, _I, _I, _P],
-    "qmm_q5k_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q5k_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q4_0": [_P, _P, _P, _I, _I, _I, _P],
-    "qmm_q4_0_cfg": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q4_0_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmv_q5k": [_P, _P, _P, _I, _I, _P],
-    "qmv_q5k_cfg": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q5k_ex": [_P, _P, _P, _I, _I, _P, _P],
     "qmv_q4_0": [_P, _P, _P, _I, _I, _P],
-    "qmv_q4_0_cfg": [_P, _P, _P, _I, _I, _P, _P],
+    "qmv_q4_0_ex": [_P, _P, _P, _I, _I, _P, _P],
     "moe_qmv_q8_0": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
-    "moe_qmv_q8_0_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q8_0_ex": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "moe_qmv_q4_0": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
-    "moe_qmv_q4_0_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q4_0_ex": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "moe_qmv_q5k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
-    "moe_qmv_q5k_cfg": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
+    "moe_qmv_q5k_ex": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "qmv_q8_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_device_status": [_P, _I],
     "qmv_selftest_wait_timeout": [ctypes.c_ulonglong, _P],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "qmv_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
-    "qmv_set_weight_prefetch": [_I],
     "qmm_tc_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
 }
 
@@ -158,13 +162,14 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _cfg(cfg):
-    if cfg is None:
+def _opts(cfg, overlap=0):
+    """The qmv_opts of one call: the overlap mode and an optional forced plan
+    (a dict of the other qmv_opts fields); None for a plain call."""
+    if cfg is None and not overlap:
         return None
-    if isinstance(cfg, qmv_cfg):
-        return ctypes.byref(cfg)
-    c = qmv_cfg(int(cfg.get("ctas", 0)), int(cfg.get("chunk_rows", 0)), int(cfg.get("chunks", 0)),
-                int(cfg.get("unroll", 0)), int(cfg.get("warps", 0)), int(cfg.get("cluster", 0)))
+    cfg = cfg or {}
+    c = qmv_opts(int(overlap), int(cfg.get("ctas", 0)), int(cfg.get("chunk_rows", 0)), int(cfg.get("chunks", 0)),
+                 int(cfg.get("unroll", 0)), int(cfg.get("warps", 0)), int(cfg.get("cluster", 0)))
     return ctypes.byref(c)
 
 
@@ -175,48 +180,48 @@ def _call(name, *args, check=True):
     return rc
 
 
-def qmv_q4k(w, x, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q4k(w, x, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q4k", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q4k_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+    return _call("qmv_q4k_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def qmv_q6k(w, x, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q6k(w, x, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q6k", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q6k_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+    return _call("qmv_q6k_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def qmv_q8_0(w, x, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q8_0(w, x, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q8_0", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q8_0_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+    return _call("qmv_q8_0_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def _qmm(name, w, x, y, rows, k, m, stream, cfg, check):
-    if cfg is None:
+def _qmm(name, w, x, y, rows, k, m, stream, cfg, overlap, check):
+    if cfg is None and not overlap:
         return _call(name, _ptr(w), _ptr(x), _ptr(y), rows, k, m, _stream(stream), check=check)
-    return _call(name + "_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _cfg(cfg), _stream(stream), check=check)
+    return _call(name + "_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def qmm_q4k(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
-    return _qmm("qmm_q4k", w, x, y, rows, k, m, stream, cfg, check)
+def qmm_q4k(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):
+    return _qmm("qmm_q4k", w, x, y, rows, k, m, stream, cfg, overlap, check)
 
 
-def qmm_q6k(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
-    return _qmm("qmm_q6k", w, x, y, rows, k, m, stream, cfg, check)
+def qmm_q6k(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):
+    return _qmm("qmm_q6k", w, x, y, rows, k, m, stream, cfg, overlap, check)
 
 
-def qmm_q8_0(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
-    return _qmm("qmm_q8_0", w, x, y, rows, k, m, stream, cfg, check)
+def qmm_q8_0(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):
+    return _qmm("qmm_q8_0", w, x, y, rows, k, m, stream, cfg, overlap, check)
 
 
-def qmm_q5k(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
-    return _qmm("qmm_q5k", w, x, y, rows, k, m, stream, cfg, check)
+def qmm_q5k(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):
+    return _qmm("qmm_q5k", w, x, y, rows, k, m, stream, cfg, overlap, check)
 
 
-def qmm_q4_0(w, x, y, rows, k, m, stream=None, cfg=None, check=True):
-    return _qmm("qmm_q4_0", w, x, y, rows, k, m, stream, cfg, check)
+def qmm_q4_0(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):
+    return _qmm("qmm_q4_0", w, x, y, rows, k, m, stream, cfg, overlap, check)
 
 
 def qmm_launches(fmt, k, m) -> int:
@@ -226,40 +231,40 @@ def qmm_launches(fmt, k, m) -> int:
     return 1 if m == 1 else -(-m // 8)
 
 
-def qmv_q5k(w, x, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q5k(w, x, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q5k", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q5k_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+    return _call("qmv_q5k_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def qmv_q4_0(w, x, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q4_0(w, x, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q4_0", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q4_0_cfg", _ptr(w), _ptr(x), _ptr(y), rows, k, _cfg(cfg), _stream(stream), check=check)
+    return _call("qmv_q4_0_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream), check=check)
 
 
 def quantize_act_q8(x, xq, xs, xsum, m, k, stream=None, check=True):
     return _call("quantize_act_q8", _ptr(x), _ptr(xq), _ptr(xs), _ptr(xsum), m, k, _stream(stream), check=check)
 
 
-def qmv_q8_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q8_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q8_dp4a", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q8_dp4a_cfg", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _cfg(cfg), _stream(stream),
+    return _call("qmv_q8_dp4a_ex", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream),
                  check=check)
 
 
-def qmv_q4k_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q4k_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q4k_dp4a", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q4k_dp4a_cfg", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _cfg(cfg), _stream(stream),
+    return _call("qmv_q4k_dp4a_ex", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream),
                  check=check)
 
 
-def qmv_q6k_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, check=True):
-    if cfg is None:
+def qmv_q6k_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("qmv_q6k_dp4a", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _stream(stream), check=check)
-    return _call("qmv_q6k_dp4a_cfg", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _cfg(cfg), _stream(stream),
+    return _call("qmv_q6k_dp4a_ex", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream),
                  check=check)
 
 
@@ -267,60 +272,60 @@ def qmv_q6k_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):
     return _call("qmv_q6k_dp4a_blockdots", _ptr(w), _ptr(xq), _ptr(dots), rows, k, _stream(stream), check=check)
 
 
-def moe_qmv_q6k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
-    if cfg is None:
+def moe_qmv_q6k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("moe_qmv_q6k_dp4a", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
                      n_experts, _stream(stream), check=check)
-    return _call("moe_qmv_q6k_dp4a_cfg", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
-                 n_experts, _cfg(cfg), _stream(stream), check=check)
+    return _call("moe_qmv_q6k_dp4a_ex", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
+                 n_experts, _opts(cfg, overlap), _stream(stream), check=check)
 
 
 def qmv_q4k_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):
     return _call("qmv_q4k_dp4a_blockdots", _ptr(w), _ptr(xq), _ptr(dots), rows, k, _stream(stream), check=check)
 
 
-def moe_qmv_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
-    if cfg is None:
+def moe_qmv_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("moe_qmv_q4k", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
                      _stream(stream), check=check)
-    return _call("moe_qmv_q4k_cfg", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
-                 _cfg(cfg), _stream(stream), check=check)
+    return _call("moe_qmv_q4k_ex", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                 _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def moe_qmv_q6k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
-    if cfg is None:
+def moe_qmv_q6k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("moe_qmv_q6k", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
                      _stream(stream), check=check)
-    return _call("moe_qmv_q6k_cfg", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
-                 _cfg(cfg), _stream(stream), check=check)
+    return _call("moe_qmv_q6k_ex", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                 _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def _moe_f32(name, w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check):
-    if cfg is None:
+def _moe_f32(name, w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, overlap, check):
+    if cfg is None and not overlap:
         return _call(name, _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
                      _stream(stream), check=check)
-    return _call(name + "_cfg", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
-                 _cfg(cfg), _stream(stream), check=check)
+    return _call(name + "_ex", _ptr(w_bank), _ptr(x), _ptr(y), rows, k, _ptr(ids), slots, n_experts,
+                 _opts(cfg, overlap), _stream(stream), check=check)
 
 
-def moe_qmv_q8_0(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
-    return _moe_f32("moe_qmv_q8_0", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check)
+def moe_qmv_q8_0(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, overlap=0, check=True):
+    return _moe_f32("moe_qmv_q8_0", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, overlap, check)
 
 
-def moe_qmv_q4_0(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
-    return _moe_f32("moe_qmv_q4_0", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check)
+def moe_qmv_q4_0(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, overlap=0, check=True):
+    return _moe_f32("moe_qmv_q4_0", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, overlap, check)
 
 
-def moe_qmv_q5k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
-    return _moe_f32("moe_qmv_q5k", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, check)
+def moe_qmv_q5k(w_bank, x, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, overlap=0, check=True):
+    return _moe_f32("moe_qmv_q5k", w_bank, x, y, rows, k, ids, slots, n_experts, stream, cfg, overlap, check)
 
 
-def moe_qmv_q4k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, check=True):
-    if cfg is None:
+def moe_qmv_q4k_dp4a(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
         return _call("moe_qmv_q4k_dp4a", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
                      n_experts, _stream(stream), check=check)
-    return _call("moe_qmv_q4k_dp4a_cfg", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
-                 n_experts, _cfg(cfg), _stream(stream), check=check)
+    return _call("moe_qmv_q4k_dp4a_ex", _ptr(w_bank), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _ptr(ids), slots,
+                 n_experts, _opts(cfg, overlap), _stream(stream), check=check)
 
 
 def qmv_dequant_q4k(w, out, rows, k, stream=None, check=True):
@@ -357,15 +362,9 @@ def qmv_device_status(clear=True) -> int:
     return v.value
 
 
-def qmv_set_weight_prefetch(mode) -> int:
-    """Decode-chain overlap mode (see qmv.h): 0 off, 1 (or True) weights
-    requested early, 2 inputs read early too. Returns the previous mode."""
-    return int(load().qmv_set_weight_prefetch(int(mode)))
-
-
-def qmv_plan_info(fmt, rows, k, slots=1, cfg=None) -> dict:
+def qmv_plan_info(fmt, rows, k, slots=1, cfg=None, overlap=0) -> dict:
     out = [ctypes.c_int(0) for _ in range(5)]
-    _call("qmv_plan_info", fmt, rows, k, slots, _cfg(cfg), *[ctypes.cast(ctypes.byref(o), ctypes.c_void_p)
+    _call("qmv_plan_info", fmt, rows, k, slots, _opts(cfg, overlap), *[ctypes.cast(ctypes.byref(o), ctypes.c_void_p)
                                                            for o in out])
     return dict(zip(["threads", "ctas", "chunk_rows", "chunks", "smem_bytes"], [o.value for o in out]))
 
@@ -379,12 +378,12 @@ PLAN_DETAIL_FIELDS = ("threads", "ctas", "unroll", "smem", "U", "KS", "GS", "NG"
 GB300_DEVICE = (152, 232448, 233472, 1024)
 
 
-def qmv_plan_detail(fmt, rows, k, slots=1, cfg=None, device=GB300_DEVICE) -> dict:
+def qmv_plan_detail(fmt, rows, k, slots=1, cfg=None, device=GB300_DEVICE, overlap=0) -> dict:
     """The planner's full choice for a described device, computed on the host
     (no GPU needed). Raises QmvError for shapes the planner rejects."""
     dev = (ctypes.c_int * 4)(*device)
     out = (ctypes.c_int * len(PLAN_DETAIL_FIELDS))()
-    _call("qmv_plan_detail", fmt, rows, k, slots, _cfg(cfg), ctypes.cast(dev, ctypes.c_void_p),
+    _call("qmv_plan_detail", fmt, rows, k, slots, _opts(cfg, overlap), ctypes.cast(dev, ctypes.c_void_p),
           ctypes.cast(out, ctypes.c_void_p))
     return dict(zip(PLAN_DETAIL_FIELDS, list(out)))
 
@@ -393,10 +392,10 @@ QMM_TC_PLAN_FIELDS = ("threads", "ctas", "smem", "KS", "CR", "S", "chunk_bytes",
                       "rrem", "ngroups", "nchunks", "off_red", "off_sums", "off_ring", "off_bars", "off_cnt")
 
 
-def qmm_tc_plan_detail(fmt, rows, k, m, cfg=None, device=GB300_DEVICE) -> dict:
+def qmm_tc_plan_detail(fmt, rows, k, m, cfg=None, device=GB300_DEVICE, overlap=0) -> dict:
     """The tensor-core batch planner's choice (fmt 0 = Q4_K, 1 = Q6_K, 2 = Q8_0)
     for a described device, computed on the host without a GPU."""
     out = (ctypes.c_int * len(QMM_TC_PLAN_FIELDS))()
     dev = (ctypes.c_int * 4)(*device)
-    _call("qmm_tc_plan_detail", fmt, rows, k, m, _cfg(cfg), dev, out)
+    _call("qmm_tc_plan_detail", fmt, rows, k, m, _opts(cfg, overlap), dev, out)
     return dict(zip(QMM_TC_PLAN_FIELDS, list(out)))

@@ -8,7 +8,7 @@ namespace qmvi {
 
 using namespace qmv;
 
-int qmm_q6k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s) {
+int qmm_q6k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s) {
     return qmm_tc_run<Q6KT>(w, x, y, rows, k, m, cfg, s);
 }
 

@@ -861,7 +861,7 @@ inline uint32_t tc_row_stride(uint32_t rowbytes, int slack) {
 // (cfg->warps, when given, lowers that bound), balanced; a chunk's slices are
 // the CTA's warps.
 template <class F>
-inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qmv_cfg* cfg, long long smem_cap,
+inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qmv_opts* cfg, long long smem_cap,
                              TParams* tp, Plan* pl) {
     if (m < 1 || m > TC_COLS || rows <= 0 || k <= 0 || k % F::QK) return QMV_EINVAL;
     const int ngroups = k / 32;
@@ -873,7 +873,7 @@ inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qm
     const long long chunk_bytes = static_cast<long long>(KS * TC_GROUPS_PER_SLICE * 32 / F::QK) * F::BLOCK_BYTES;
     if (rowbytes > 0x7fffffffLL) return QMV_ETOOBIG;
     const uint32_t stride = tc_row_stride(static_cast<uint32_t>(std::min(chunk_bytes, rowbytes)), F::SLACK);
-    const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
+    const int mode = overlap_of(cfg);
     const long long full = std::min<long long>(smem_cap, di.smem_optin);
 
     int parts = (cfg && cfg->ctas > 0) ? cfg->ctas : di.nsm;
@@ -923,7 +923,8 @@ inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qm
             tp->S = static_cast<int>(S);
             tp->rq = rows / parts;
             tp->rrem = rows % parts;
-            tp->early_inputs = mode >= 2 ? 1 : 0;
+            tp->early_inputs = mode >= QMV_OVERLAP_INDEPENDENT ? 1 : 0;
+            pl->overlap = mode;
             tp->slot_stride = static_cast<uint32_t>(slot);
             return QMV_OK;
         }
@@ -937,7 +938,7 @@ inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qm
 // registers fill half an SM's register file.
 constexpr int TC_WARPS_HALF_SM = 8;
 
-// The plan used. Independent calls (mode 2 of qmv_set_weight_prefetch) take
+// The plan used. Independent calls (QMV_OVERLAP_INDEPENDENT) take
 // CTAs of at most TC_WARPS_HALF_SM warps in at most half an SM's shared
 // memory, so that two calls' CTAs share an SM, one converting its x while
 // the other runs its tiles (measured on GB300, us a call: Q4_K 4096 x 4096
@@ -945,10 +946,9 @@ constexpr int TC_WARPS_HALF_SM = 8;
 // 21.6; Q8_0 14336 x 4096 m = 8 19.1 -> 18.2). Other modes, forced warps, and
 // shapes whose plan does not fit use whole CTAs.
 template <class F>
-inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv_cfg* cfg, TParams* tp, Plan* pl) {
-    const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
-    if (mode == 2 && !(cfg && cfg->warps > 0)) {
-        qmv_cfg c = cfg ? *cfg : qmv_cfg{0, 0, 0, 0, 0, 0};
+inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv_opts* cfg, TParams* tp, Plan* pl) {
+    if (overlap_of(cfg) == QMV_OVERLAP_INDEPENDENT && cfg->warps <= 0) {
+        qmv_opts c = *cfg;
         c.warps = TC_WARPS_HALF_SM;
         const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;
         TParams t2 = *tp;
@@ -977,7 +977,7 @@ inline int launch_tc_kernel(const TParams& tp, const Plan& pl, cudaStream_t stre
     lc.stream = stream;
     cudaLaunchAttribute at[1];
     int na = 0;
-    if (__atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED)) {
+    if (pl.overlap != QMV_OVERLAP_NONE) {
         at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         at[na].val.programmaticStreamSerializationAllowed = 1;
         na++;
@@ -997,7 +997,7 @@ inline int launch_tc(const TParams& tp, const Plan& pl, cudaStream_t stream) {
 // y[m, rows] = x[m, k] W^T on the tensor cores, m >= 1: ceil(m / 8) balanced
 // tiles of rows of x, one launch each (each launch reads W once).
 template <class F>
-inline int qmm_tc_run(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+inline int qmm_tc_run(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                       cudaStream_t s) {
     const int tiles = (m + TC_COLS - 1) / TC_COLS;
     DevInfo di;

@@ -35,63 +35,75 @@ int check_moe(const int32_t* ids, int slots, int n_experts, int rows, int k, int
     return QMV_OK;
 }
 
+// Launch options: the overlap mode must be one of QMV_OVERLAP_*; the forced
+// plan fields may take any value (<= 0 keeps the automatic choice).
+bool opts_ok(const qmv_opts* o) {
+    return !o || (o->overlap >= QMV_OVERLAP_NONE && o->overlap <= QMV_OVERLAP_INDEPENDENT);
+}
+
 }  // namespace
 
 extern "C" {
 
-int qmv_q4k_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+int qmv_q4k_ex(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg,
                 cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 256, 144);
     return rc ? rc : qmvi::q4k(w, x, y, rows, k, cfg, stream);
 }
 
 int qmv_q4k(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
-    return qmv_q4k_cfg(w, x, y, rows, k, nullptr, stream);
+    return qmv_q4k_ex(w, x, y, rows, k, nullptr, stream);
 }
 
-int qmv_q6k_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+int qmv_q6k_ex(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg,
                 cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 256, 210);
     return rc ? rc : qmvi::q6k(w, x, y, rows, k, cfg, stream);
 }
 
 int qmv_q6k(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
-    return qmv_q6k_cfg(w, x, y, rows, k, nullptr, stream);
+    return qmv_q6k_ex(w, x, y, rows, k, nullptr, stream);
 }
 
-int qmv_q8_0_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+int qmv_q8_0_ex(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg,
                  cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 32, 34);
     return rc ? rc : qmvi::q8_0(w, x, y, rows, k, cfg, stream);
 }
 
 int qmv_q8_0(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
-    return qmv_q8_0_cfg(w, x, y, rows, k, nullptr, stream);
+    return qmv_q8_0_ex(w, x, y, rows, k, nullptr, stream);
 }
 
-int qmv_q5k_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+int qmv_q5k_ex(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg,
                 cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 256, 176);
     return rc ? rc : qmvi::q5k(w, x, y, rows, k, cfg, stream);
 }
 
 int qmv_q5k(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
-    return qmv_q5k_cfg(w, x, y, rows, k, nullptr, stream);
+    return qmv_q5k_ex(w, x, y, rows, k, nullptr, stream);
 }
 
-int qmv_q4_0_cfg(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg,
+int qmv_q4_0_ex(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg,
                  cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 32, 18);
     return rc ? rc : qmvi::q4_0(w, x, y, rows, k, cfg, stream);
 }
 
 int qmv_q4_0(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
-    return qmv_q4_0_cfg(w, x, y, rows, k, nullptr, stream);
+    return qmv_q4_0_ex(w, x, y, rows, k, nullptr, stream);
 }
 
 // Small-M batch: m == 1 is the matvec itself; m >= 2 the batched kernels.
-int qmm_q4k_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+int qmm_q4k_ex(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                 cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 256, 144);
     if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
         rc = QMV_EINVAL;
@@ -100,11 +112,12 @@ int qmm_q4k_cfg(const void* w, const float* x, float* y, int rows, int k, int m,
 }
 
 int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
-    return qmm_q4k_cfg(w, x, y, rows, k, m, nullptr, stream);
+    return qmm_q4k_ex(w, x, y, rows, k, m, nullptr, stream);
 }
 
-int qmm_q6k_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+int qmm_q6k_ex(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                 cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 256, 210);
     if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
         rc = QMV_EINVAL;
@@ -113,11 +126,12 @@ int qmm_q6k_cfg(const void* w, const float* x, float* y, int rows, int k, int m,
 }
 
 int qmm_q6k(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
-    return qmm_q6k_cfg(w, x, y, rows, k, m, nullptr, stream);
+    return qmm_q6k_ex(w, x, y, rows, k, m, nullptr, stream);
 }
 
-int qmm_q8_0_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+int qmm_q8_0_ex(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                  cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 32, 34);
     if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
         rc = QMV_EINVAL;
@@ -126,11 +140,12 @@ int qmm_q8_0_cfg(const void* w, const float* x, float* y, int rows, int k, int m
 }
 
 int qmm_q8_0(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
-    return qmm_q8_0_cfg(w, x, y, rows, k, m, nullptr, stream);
+    return qmm_q8_0_ex(w, x, y, rows, k, m, nullptr, stream);
 }
 
-int qmm_q5k_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+int qmm_q5k_ex(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                  cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 256, 176);
     if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
         rc = QMV_EINVAL;
@@ -139,11 +154,12 @@ int qmm_q5k_cfg(const void* w, const float* x, float* y, int rows, int k, int m,
 }
 
 int qmm_q5k(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
-    return qmm_q5k_cfg(w, x, y, rows, k, m, nullptr, stream);
+    return qmm_q5k_ex(w, x, y, rows, k, m, nullptr, stream);
 }
 
-int qmm_q4_0_cfg(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg,
+int qmm_q4_0_ex(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                   cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w, x, y, rows, k, 32, 18);
     if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
         rc = QMV_EINVAL;
@@ -152,7 +168,7 @@ int qmm_q4_0_cfg(const void* w, const float* x, float* y, int rows, int k, int m
 }
 
 int qmm_q4_0(const void* w, const float* x, float* y, int rows, int k, int m, cudaStream_t stream) {
-    return qmm_q4_0_cfg(w, x, y, rows, k, m, nullptr, stream);
+    return qmm_q4_0_ex(w, x, y, rows, k, m, nullptr, stream);
 }
 
 int quantize_act_q8(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t stream) {
@@ -163,8 +179,9 @@ int quantize_act_q8(const float* x, int8_t* xq, float* xs, float* xsum, int m, i
     return qmvi::quantize_act(x, xq, xs, xsum, m, k, stream);
 }
 
-int qmv_q8_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
-                    const qmv_cfg* cfg, cudaStream_t stream) {
+int qmv_q8_dp4a_ex(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                    const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     if (!xs) return QMV_EINVAL;
     int rc = check_dense(w, xq, y, rows, k, 32, 34);
     if (rc) return rc;
@@ -174,11 +191,12 @@ int qmv_q8_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y, 
 
 int qmv_q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
                 cudaStream_t stream) {
-    return qmv_q8_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
+    return qmv_q8_dp4a_ex(w, xq, xs, y, rows, k, nullptr, stream);
 }
 
-int qmv_q4k_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
-                     const qmv_cfg* cfg, cudaStream_t stream) {
+int qmv_q4k_dp4a_ex(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                     const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     if (!xs) return QMV_EINVAL;
     int rc = check_dense(w, xq, y, rows, k, 256, 144);
     if (rc) return rc;
@@ -188,11 +206,12 @@ int qmv_q4k_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y,
 
 int qmv_q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
                  cudaStream_t stream) {
-    return qmv_q4k_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
+    return qmv_q4k_dp4a_ex(w, xq, xs, y, rows, k, nullptr, stream);
 }
 
-int qmv_q6k_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
-                     const qmv_cfg* cfg, cudaStream_t stream) {
+int qmv_q6k_dp4a_ex(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                     const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     if (!xs) return QMV_EINVAL;
     int rc = check_dense(w, xq, y, rows, k, 256, 210);
     if (rc) return rc;
@@ -202,11 +221,12 @@ int qmv_q6k_dp4a_cfg(const void* w, const int8_t* xq, const float* xs, float* y,
 
 int qmv_q6k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
                  cudaStream_t stream) {
-    return qmv_q6k_dp4a_cfg(w, xq, xs, y, rows, k, nullptr, stream);
+    return qmv_q6k_dp4a_ex(w, xq, xs, y, rows, k, nullptr, stream);
 }
 
-int moe_qmv_q6k_dp4a_cfg(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
-                         const int32_t* ids, int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+int moe_qmv_q6k_dp4a_ex(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                         const int32_t* ids, int slots, int n_experts, const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     if (!xs) return QMV_EINVAL;
     int rc = check_dense(w_bank, xq, y, rows, k, 256, 210);
     if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 210);
@@ -217,7 +237,7 @@ int moe_qmv_q6k_dp4a_cfg(const void* w_bank, const int8_t* xq, const float* xs, 
 
 int moe_qmv_q6k_dp4a(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
                      const int32_t* ids, int slots, int n_experts, cudaStream_t stream) {
-    return moe_qmv_q6k_dp4a_cfg(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, nullptr, stream);
+    return moe_qmv_q6k_dp4a_ex(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
 int qmv_q6k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t stream) {
@@ -227,8 +247,9 @@ int qmv_q6k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int r
     return qmvi::q6k_dp4a_blockdots(w, xq, dots, rows, k, stream);
 }
 
-int moe_qmv_q4k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids,
-                    int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+int moe_qmv_q4k_ex(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids,
+                    int slots, int n_experts, const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w_bank, x, y, rows, k, 256, 144);
     if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 144);
     return rc ? rc : qmvi::moe_q4k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
@@ -236,11 +257,12 @@ int moe_qmv_q4k_cfg(const void* w_bank, const float* x, float* y, int rows, int 
 
 int moe_qmv_q4k(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
                 int n_experts, cudaStream_t stream) {
-    return moe_qmv_q4k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+    return moe_qmv_q4k_ex(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
-int moe_qmv_q6k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-                    int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+int moe_qmv_q6k_ex(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                    int n_experts, const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w_bank, x, y, rows, k, 256, 210);
     if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 210);
     return rc ? rc : qmvi::moe_q6k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
@@ -248,11 +270,12 @@ int moe_qmv_q6k_cfg(const void* w_bank, const float* x, float* y, int rows, int 
 
 int moe_qmv_q6k(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
                 int n_experts, cudaStream_t stream) {
-    return moe_qmv_q6k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+    return moe_qmv_q6k_ex(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
-int moe_qmv_q8_0_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-                     int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+int moe_qmv_q8_0_ex(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                     int n_experts, const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w_bank, x, y, rows, k, 32, 34);
     if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 32, 34);
     return rc ? rc : qmvi::moe_q8_0(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
@@ -260,11 +283,12 @@ int moe_qmv_q8_0_cfg(const void* w_bank, const float* x, float* y, int rows, int
 
 int moe_qmv_q8_0(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
                  int n_experts, cudaStream_t stream) {
-    return moe_qmv_q8_0_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+    return moe_qmv_q8_0_ex(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
-int moe_qmv_q4_0_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-                     int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+int moe_qmv_q4_0_ex(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                     int n_experts, const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w_bank, x, y, rows, k, 32, 18);
     if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 32, 18);
     return rc ? rc : qmvi::moe_q4_0(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
@@ -272,11 +296,12 @@ int moe_qmv_q4_0_cfg(const void* w_bank, const float* x, float* y, int rows, int
 
 int moe_qmv_q4_0(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
                  int n_experts, cudaStream_t stream) {
-    return moe_qmv_q4_0_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+    return moe_qmv_q4_0_ex(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
-int moe_qmv_q5k_cfg(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-                    int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+int moe_qmv_q5k_ex(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
+                    int n_experts, const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     int rc = check_dense(w_bank, x, y, rows, k, 256, 176);
     if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 176);
     return rc ? rc : qmvi::moe_q5k(w_bank, x, y, rows, k, ids, slots, n_experts, cfg, stream);
@@ -284,11 +309,12 @@ int moe_qmv_q5k_cfg(const void* w_bank, const float* x, float* y, int rows, int 
 
 int moe_qmv_q5k(const void* w_bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
                 int n_experts, cudaStream_t stream) {
-    return moe_qmv_q5k_cfg(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
+    return moe_qmv_q5k_ex(w_bank, x, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
-int moe_qmv_q4k_dp4a_cfg(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
-                         const int32_t* ids, int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t stream) {
+int moe_qmv_q4k_dp4a_ex(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
+                         const int32_t* ids, int slots, int n_experts, const qmv_opts* cfg, cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     if (!xs) return QMV_EINVAL;
     int rc = check_dense(w_bank, xq, y, rows, k, 256, 144);
     if (!rc) rc = check_moe(ids, slots, n_experts, rows, k, 256, 144);
@@ -299,7 +325,7 @@ int moe_qmv_q4k_dp4a_cfg(const void* w_bank, const int8_t* xq, const float* xs, 
 
 int moe_qmv_q4k_dp4a(const void* w_bank, const int8_t* xq, const float* xs, float* y, int rows, int k,
                      const int32_t* ids, int slots, int n_experts, cudaStream_t stream) {
-    return moe_qmv_q4k_dp4a_cfg(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, nullptr, stream);
+    return moe_qmv_q4k_dp4a_ex(w_bank, xq, xs, y, rows, k, ids, slots, n_experts, nullptr, stream);
 }
 
 int qmv_dequant_q4k(const void* w, float* out, int rows, int k, cudaStream_t stream) {
@@ -352,12 +378,6 @@ const char* qmv_strerror(int code) {
     }
 }
 
-int qmv_set_weight_prefetch(int mode) {
-    const int old = __atomic_load_n(&qmv::weight_prefetch_flag(), __ATOMIC_RELAXED);
-    __atomic_store_n(&qmv::weight_prefetch_flag(), mode <= 0 ? 0 : (mode >= 2 ? 2 : 1), __ATOMIC_RELAXED);
-    return old;
-}
-
 int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {
     if (limit_ns == 0 || limit_ns > 100000000ull) return QMV_EINVAL;
     return qmvi::selftest_wait_timeout(limit_ns, stream);
@@ -389,7 +409,7 @@ namespace {
 bool plan_is_moe(int fmt) { return fmt == 4 || fmt == 6 || fmt == 7 || (fmt >= 10 && fmt <= 12) || fmt == 17; }
 
 // Plan of format fmt on device `di`.
-int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_cfg* cfg, qmv::KParams* kp,
+int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_opts* cfg, qmv::KParams* kp,
             qmv::Plan* pl) {
     static const int qk[18] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256, 256, 256, 32, 256, 256};
     if (fmt < 0 || fmt > 17 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
@@ -418,8 +438,9 @@ int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const q
 
 }  // namespace
 
-int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* threads, int* ctas,
+int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_opts* cfg, int* threads, int* ctas,
                   int* chunk_rows, int* chunks, int* smem_bytes) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
     qmv::DevInfo di;
     int rc = qmv::dev_info(&di, nullptr);
     if (rc) return rc;
@@ -435,8 +456,8 @@ int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, int* 
     return QMV_OK;
 }
 
-int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, const int* device, int* out) {
-    if (!device || !out) return QMV_EINVAL;
+int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_opts* cfg, const int* device, int* out) {
+    if (!device || !out || !opts_ok(cfg)) return QMV_EINVAL;
     qmv::DevInfo di;
     di.nsm = device[0];
     di.smem_optin = device[1];
@@ -458,8 +479,8 @@ int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg* cfg, con
     return QMV_OK;
 }
 
-int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_cfg* cfg, const int* device, int* out) {
-    if (!device || !out) return QMV_EINVAL;
+int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_opts* cfg, const int* device, int* out) {
+    if (!device || !out || !opts_ok(cfg)) return QMV_EINVAL;
     qmv::DevInfo di;
     di.nsm = device[0];
     di.smem_optin = device[1];

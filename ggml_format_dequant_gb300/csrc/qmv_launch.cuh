@@ -1,6 +1,6 @@
 // qmv_launch.cuh -- host-side launch plan for qmv_stream_kernel: lane groups,
 // row groups, grid size, rows per ring slot, ring depth and the shared-memory
-// layout, chosen per shape (or forced through qmv_cfg for tests and sweeps).
+// layout, chosen per shape (or forced through qmv_opts for tests and sweeps).
 #pragma once
 
 #include <algorithm>
@@ -33,13 +33,16 @@ inline int cuda_rc(cudaError_t e) {
     return QMV_ECUDA;
 }
 
-// Process-wide decode-chain mode (qmv_set_weight_prefetch): 0 plain launches;
+// Launch overlap of one call (qmv_opts.overlap): 0 plain launch;
 // 1 programmatic dependent launch, packed weights requested before waiting for
 // the previous kernel; 2 also x / ids read early (the caller guarantees that
 // the previous kernel writes none of this call's inputs; y still waits).
-inline int& weight_prefetch_flag() {
-    static int f = 0;
-    return f;
+// A call without options is a plain launch.
+inline int overlap_of(const qmv_opts* o) {
+    if (!o) return QMV_OVERLAP_NONE;
+    return o->overlap <= QMV_OVERLAP_NONE ? QMV_OVERLAP_NONE
+                                          : (o->overlap >= QMV_OVERLAP_INDEPENDENT ? QMV_OVERLAP_INDEPENDENT
+                                                                                   : QMV_OVERLAP_CHAIN);
 }
 
 struct DevInfo {
@@ -105,6 +108,7 @@ struct Plan {
     int parts = 1;        // CTAs per matrix (grid.x)
     int R = 1;            // rows per warp step (kernel template parameter)
     int CL = 1;           // cluster size along grid.x
+    int overlap = 0;      // QMV_OVERLAP_* of the call
     size_t smem = 0;
 };
 
@@ -125,7 +129,7 @@ inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a
 // Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense)
 // on a device described by `di`, for a given (or the default) CTA count.
 template <class F>
-inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
+inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const qmv_opts* cfg, KParams* kp, Plan* pl) {
     const int nb = k / F::QK;
     const int U = F::units(nb);
     const int KS = (U + 31) / 32;
@@ -145,8 +149,9 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
     Plan P;
     // CTAs per matrix: one per SM (MoE: the SMs are shared by the slots), but
     // not more than there are rows, and enough that the parked partials fit.
-    const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
-    const int early = mode >= 2 ? 1 : 0;
+    const int mode = overlap_of(cfg);
+    P.overlap = mode;
+    const int early = mode >= QMV_OVERLAP_INDEPENDENT ? 1 : 0;
     const int W = KS > 1 ? KS : early;   // parked slice sums per row
     if (cfg && cfg->ctas > 0) {
         P.parts = cfg->ctas;
@@ -304,25 +309,23 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
     return QMV_OK;
 }
 
-// Launch plan of format F. Independent calls (mode 2 of
-// qmv_set_weight_prefetch) overlap best when one call takes as few CTAs as
+// Launch plan of format F. Independent calls (QMV_OVERLAP_INDEPENDENT) overlap best when one call takes as few CTAs as
 // still hold their whole share in half an SM (but at least half the SMs'
 // worth): more calls are then in flight at once (measured on GB300: MoE Q4_K
 // E128 n768 k2048 with 8 slots 2.32 -> 1.59 us a call, Q4_K 4096 x 4096
 // 2.43 -> 2.18 us, Q4_K dp4a 4096 x 4096 2.25 -> ~1.76 us). Chained and plain
 // calls, and shapes whose share does not fit, use every SM.
 template <class F>
-inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
+inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_opts* cfg, KParams* kp, Plan* pl) {
     const int rc = make_plan_core<F>(di, rows, k, slots, cfg, kp, pl);
-    const int mode = __atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED);
-    if (rc || mode != 2 || (cfg && cfg->ctas > 0)) return rc;
+    if (rc || overlap_of(cfg) != QMV_OVERLAP_INDEPENDENT || cfg->ctas > 0) return rc;
     const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;
     const int per = slots > 1 ? slots : 1;
     // From half the SMs up (with two CTAs an SM, four calls in flight), the
     // fewest CTAs whose whole share fits in half an SM.
     const int start = std::max(1, di.nsm / (2 * per));
     if (start >= pl->parts) return rc;   // small shapes: already fewer CTAs
-    qmv_cfg c = cfg ? *cfg : qmv_cfg{0, 0, 0, 0, 0, 0};
+    qmv_opts c = *cfg;
     for (int parts = start; parts < pl->parts; parts++) {
         c.ctas = parts;
         KParams k2 = *kp;
@@ -341,7 +344,7 @@ inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qm
 
 // The same on the current device.
 template <class F>
-inline int make_plan(int rows, int k, int slots, const qmv_cfg* cfg, KParams* kp, Plan* pl) {
+inline int make_plan(int rows, int k, int slots, const qmv_opts* cfg, KParams* kp, Plan* pl) {
     DevInfo di;
     const int rc = dev_info(&di, nullptr);
     return rc ? rc : make_plan_for<F>(di, rows, k, slots, cfg, kp, pl);
@@ -369,7 +372,7 @@ inline int launch_one(const KParams& kp, const Plan& pl, int slots, cudaStream_t
         at[na].val.clusterDim.z = 1;
         na++;
     }
-    if (__atomic_load_n(&weight_prefetch_flag(), __ATOMIC_RELAXED)) {
+    if (pl.overlap != QMV_OVERLAP_NONE) {
         at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         at[na].val.programmaticStreamSerializationAllowed = 1;
         na++;

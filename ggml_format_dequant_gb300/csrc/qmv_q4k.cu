@@ -46,7 +46,7 @@ namespace qmvi {
 
 using namespace qmv;
 
-int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s) {
+int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(w);
     kp.x = x;
@@ -64,7 +64,7 @@ int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
 }
 
 int moe_q4k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-            int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+            int n_experts, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(bank);
     kp.x = x;
@@ -83,7 +83,7 @@ int moe_q4k(const void* bank, const float* x, float* y, int rows, int k, const i
     return launch<Q4K, true, MODE_MATVEC>(kp, pl, slots, s);
 }
 
-int q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+int q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_opts* cfg,
              cudaStream_t s) {
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(w);
@@ -120,7 +120,7 @@ int q4k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows,
 }
 
 int moe_q4k_dp4a(const void* bank, const int8_t* xq, const float* xs, float* y, int rows, int k, const int32_t* ids,
-                 int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+                 int slots, int n_experts, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(bank);
     kp.xq = xq;

@@ -59,7 +59,7 @@ namespace qmvi {
 
 using namespace qmv;
 
-int q5k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s) {
+int q5k(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp = q5k_params(w, rows, k);
     kp.x = x;
     kp.y = y;
@@ -70,7 +70,7 @@ int q5k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
 }
 
 int moe_q5k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-            int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+            int n_experts, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp = q5k_params(bank, rows, k);
     kp.x = x;
     kp.y = y;
@@ -94,7 +94,7 @@ int dequant_q5k(const void* w, float* out, int rows, int k, cudaStream_t s) {
 
 // Small-M batched product y[m, rows] = x[m, k] W^T, m >= 2: the
 // tensor-core kernel of qmm_tc.cuh, one launch per tile of up to 8 rows of x.
-int qmm_q5k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_cfg* cfg, cudaStream_t s) {
+int qmm_q5k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s) {
     return qmm_tc_run<Q5KT>(w, x, y, rows, k, m, cfg, s);
 }
 

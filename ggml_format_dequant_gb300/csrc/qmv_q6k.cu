@@ -37,7 +37,7 @@ namespace qmvi {
 
 using namespace qmv;
 
-int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s) {
+int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(w);
     kp.x = x;
@@ -55,7 +55,7 @@ int q6k(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg*
 }
 
 int moe_q6k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-            int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+            int n_experts, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp{};
     kp.w = static_cast<const uint8_t*>(bank);
     kp.x = x;
@@ -90,7 +90,7 @@ KParams q6k_params(const void* w, int rows, int k) {
 
 }  // namespace
 
-int q6k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+int q6k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_opts* cfg,
              cudaStream_t s) {
     KParams kp = q6k_params(w, rows, k);
     kp.xq = xq;
@@ -113,7 +113,7 @@ int q6k_dp4a_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows,
 }
 
 int moe_q6k_dp4a(const void* bank, const int8_t* xq, const float* xs, float* y, int rows, int k, const int32_t* ids,
-                 int slots, int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+                 int slots, int n_experts, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp = q6k_params(bank, rows, k);
     kp.xq = xq;
     kp.xqs = xs;

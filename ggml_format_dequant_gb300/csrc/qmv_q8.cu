@@ -80,7 +80,7 @@ namespace qmvi {
 
 using namespace qmv;
 
-int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg* cfg, cudaStream_t s) {
+int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp = q8_params(w, rows, k);
     kp.x = x;
     kp.y = y;
@@ -91,7 +91,7 @@ int q8_0(const void* w, const float* x, float* y, int rows, int k, const qmv_cfg
 }
 
 int moe_q8_0(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
-             int n_experts, const qmv_cfg* cfg, cudaStream_t s) {
+             int n_experts, const qmv_opts* cfg, cudaStream_t s) {
     KParams kp = q8_params(bank, rows, k);
     kp.x = x;
     kp.y = y;
@@ -104,7 +104,7 @@ int moe_q8_0(const void* bank, const float* x, float* y, int rows, int k, const 
     return launch<Q8F, true, MODE_MATVEC>(kp, pl, slots, s);
 }
 
-int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_cfg* cfg,
+int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_opts* cfg,
             cudaStream_t s) {
     KParams kp = q8_params(w, rows, k);
     kp.xq = xq;

@@ -60,6 +60,54 @@ extern "C" {
 #define QMV_ECUDA (-3)   /* a CUDA runtime call or the kernel launch failed */
 #define QMV_ETOOBIG (-4) /* valid shape too large for this build's shared-memory plan */
 
+/* ----------------------------------------------------------------------
+ * Launch options. Every entry point that launches a matvec, an MoE matvec or
+ * a batch has an `_ex` twin with the same arguments plus `const qmv_opts
+ * *opts` (before the stream); opts == NULL, or the entry point without `_ex`,
+ * is a plain launch with the automatic plan. The options belong to the one
+ * call: nothing is remembered between calls, and calls with different options
+ * may run concurrently from any threads.
+ *
+ * overlap (the pages' decode engine records one whole decode step and replays
+ * it, hanzo-ml src/vulkan_backend.rs, VkGraph; on a CUDA stream the same
+ * back-to-back launches overlap through programmatic dependent launch):
+ *   QMV_OVERLAP_NONE: plain launch; the kernel starts after the previous
+ *     work on the stream has finished.
+ *   QMV_OVERLAP_CHAIN: the call may be scheduled while the kernel launched
+ *     just before it on the same stream still runs; it starts streaming its
+ *     packed weights at once and waits for that kernel to finish before it
+ *     reads x (MoE: ids) and before it writes y. Only valid if that kernel
+ *     writes none of this call's packed weights (inference: weights are
+ *     constant). Use it for a dependent decode chain, where each call reads
+ *     the output of the one before.
+ *   QMV_OVERLAP_INDEPENDENT: as CHAIN, and x and ids are read (and the whole
+ *     product computed) before that wait; only the writes of y wait. Only
+ *     valid if the kernel launched just before writes none of this call's
+ *     inputs, e.g. consecutive projections of one activation (Q, K and V;
+ *     gate and up). The plan then takes fewer CTAs so that several calls are
+ *     in flight at once.
+ *   Any other value is QMV_EINVAL.
+ * Forced plan (tests and tuning sweeps; any field <= 0 keeps the automatic
+ * choice): ctas: CTAs per weight matrix (per MoE slot); chunk_rows: rows per
+ * ring slot (one bulk copy); chunks: ring slots per row group; unroll: rows
+ * each warp decodes per step (1 or 2); warps: at most this many warps per CTA
+ * (at least the k-slices of one row); cluster: CTAs (a power of two up to 8)
+ * that share the conversion of the f32 activation (the CTA count is rounded
+ * down to a multiple of it). */
+#define QMV_OVERLAP_NONE 0
+#define QMV_OVERLAP_CHAIN 1
+#define QMV_OVERLAP_INDEPENDENT 2
+
+typedef struct qmv_opts {
+    int overlap;
+    int ctas;
+    int chunk_rows;
+    int chunks;
+    int unroll;
+    int warps;
+    int cluster;
+} qmv_opts;
+
 /* Q4_K matvec: y[r] = sum_j W[r, j] * x[j].
  * w: rows * (k/256) * 144 bytes; x: f32 [k]; y: f32 [rows].
  * k must be a positive multiple of 256, rows > 0.
@@ -96,7 +144,7 @@ int qmv_q4_0(const void *w, const float *x, float *y, int rows, int k, cudaStrea
  * accumulating the m dot products in f32. Numerics: each decoded weight is
  * the round-to-nearest f32 of its exact value; results agree with an f64
  * reference to a scale-relative error far below 1e-4 per row of y. Each plan
- * is deterministic; independent calls (qmv_set_weight_prefetch mode 2) use
+ * is deterministic; independent calls (QMV_OVERLAP_INDEPENDENT) use
  * smaller k-chunks, so rows longer than 2048 weights may round differently
  * there than in plain or chained calls, within the same bound.
  * Cites hanzo-ml src/vulkan_backend.rs, matmul_q4k_gpu / matmul_q6k_gpu /
@@ -205,22 +253,6 @@ int moe_qmv_q4k_dp4a(const void *w_bank, const int8_t *xq, const float *xs, floa
 int moe_qmv_q6k_dp4a(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows, int k,
                      const int32_t *ids, int slots, int n_experts, cudaStream_t stream);
 
-/* Decode-chain overlap (process-wide; 0 by default).
- * mode 1: every matvec launch allows programmatic dependent launch: a call may
- *   be scheduled while the previous kernel on the same stream is still running
- *   and starts streaming its packed weights at once, but it waits for that
- *   kernel to finish before it reads x (or, for MoE, ids) and before it writes
- *   y. Only use it if the packed weights of a call are never written by the
- *   kernel launched just before it on the stream (true for inference, where
- *   weights are constant).
- * mode 2: as mode 1, and x and ids are read (and the whole product computed)
- *   before that wait; only the writes of y wait for the previous kernel. Only
- *   use it when the kernel launched just before writes none of this call's
- *   inputs, e.g. consecutive projections of one activation (Q, K and V; gate
- *   and up).
- * mode 0: plain launches. Returns the previous mode. */
-int qmv_set_weight_prefetch(int mode);
-
 /* Name of a QMV_* return code. Never NULL. */
 const char *qmv_strerror(int code);
 
@@ -248,73 +280,62 @@ int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
 int qmv_device_status(unsigned int *status, int clear);
 
 /* ----------------------------------------------------------------------
+ * The entry points above with launch options (qmv_opts: overlap mode and an
+ * optional forced plan). Arguments, numerics and errors as for the entry
+ * point of the same name without `_ex`; an overlap value outside
+ * QMV_OVERLAP_* is QMV_EINVAL.
+ */
+int qmv_q4k_ex(const void *w, const float *x, float *y, int rows, int k, const qmv_opts *opts,
+                cudaStream_t stream);
+int qmv_q6k_ex(const void *w, const float *x, float *y, int rows, int k, const qmv_opts *opts,
+                cudaStream_t stream);
+int qmv_q8_0_ex(const void *w, const float *x, float *y, int rows, int k, const qmv_opts *opts,
+                 cudaStream_t stream);
+int qmv_q8_dp4a_ex(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                    const qmv_opts *opts, cudaStream_t stream);
+int qmv_q4k_dp4a_ex(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                     const qmv_opts *opts, cudaStream_t stream);
+int moe_qmv_q6k_ex(const void *w_bank, const float *x, float *y, int rows, int k,
+                    const int32_t *ids, int slots, int n_experts, const qmv_opts *opts,
+                    cudaStream_t stream);
+int moe_qmv_q4k_dp4a_ex(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows,
+                         int k, const int32_t *ids, int slots, int n_experts, const qmv_opts *opts,
+                         cudaStream_t stream);
+int moe_qmv_q4k_ex(const void *w_bank, const float *x, float *y, int rows, int k,
+                    const int32_t *ids, int slots, int n_experts, const qmv_opts *opts,
+                    cudaStream_t stream);
+int qmv_q6k_dp4a_ex(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
+                     const qmv_opts *opts, cudaStream_t stream);
+int moe_qmv_q6k_dp4a_ex(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows,
+                         int k, const int32_t *ids, int slots, int n_experts, const qmv_opts *opts,
+                         cudaStream_t stream);
+int qmm_q4k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
+                cudaStream_t stream);
+int qmm_q6k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
+                cudaStream_t stream);
+int qmm_q8_0_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
+                 cudaStream_t stream);
+int qmm_q5k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
+                cudaStream_t stream);
+int qmm_q4_0_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
+                 cudaStream_t stream);
+int qmv_q5k_ex(const void *w, const float *x, float *y, int rows, int k, const qmv_opts *opts,
+                cudaStream_t stream);
+int qmv_q4_0_ex(const void *w, const float *x, float *y, int rows, int k, const qmv_opts *opts,
+                 cudaStream_t stream);
+int moe_qmv_q8_0_ex(const void *w_bank, const float *x, float *y, int rows, int k,
+                     const int32_t *ids, int slots, int n_experts, const qmv_opts *opts,
+                     cudaStream_t stream);
+int moe_qmv_q4_0_ex(const void *w_bank, const float *x, float *y, int rows, int k,
+                     const int32_t *ids, int slots, int n_experts, const qmv_opts *opts,
+                     cudaStream_t stream);
+int moe_qmv_q5k_ex(const void *w_bank, const float *x, float *y, int rows, int k,
+                    const int32_t *ids, int slots, int n_experts, const qmv_opts *opts,
+                    cudaStream_t stream);
+
+/* ----------------------------------------------------------------------
  * Test and benchmark exports (not needed for inference).
  */
-
-/* Forced launch configuration: any field <= 0 keeps the automatic choice.
- * ctas: CTAs per weight matrix (per MoE slot); chunk_rows: rows per ring slot
- * (one bulk copy); chunks: ring slots per row group; unroll: rows each warp
- * decodes per step (1 or 2); warps: at most this many warps per CTA (at least
- * the k-slices of one row); cluster: CTAs (a power of two up to 8) that share
- * the conversion of the f32 activation (the CTA count is rounded down to a
- * multiple of it). Used to exercise ring reuse, ragged pieces and
- * small CTAs on small inputs, and for tuning sweeps. */
-typedef struct qmv_cfg {
-    int ctas;
-    int chunk_rows;
-    int chunks;
-    int unroll;
-    int warps;
-    int cluster;
-} qmv_cfg;
-
-int qmv_q4k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
-                cudaStream_t stream);
-int qmv_q6k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
-                cudaStream_t stream);
-int qmv_q8_0_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
-                 cudaStream_t stream);
-int qmv_q8_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
-                    const qmv_cfg *cfg, cudaStream_t stream);
-int qmv_q4k_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
-                     const qmv_cfg *cfg, cudaStream_t stream);
-int moe_qmv_q6k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
-                    const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
-                    cudaStream_t stream);
-int moe_qmv_q4k_dp4a_cfg(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows,
-                         int k, const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
-                         cudaStream_t stream);
-int moe_qmv_q4k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
-                    const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
-                    cudaStream_t stream);
-int qmv_q6k_dp4a_cfg(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
-                     const qmv_cfg *cfg, cudaStream_t stream);
-int moe_qmv_q6k_dp4a_cfg(const void *w_bank, const int8_t *xq, const float *xs, float *y, int rows,
-                         int k, const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
-                         cudaStream_t stream);
-int qmm_q4k_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
-                cudaStream_t stream);
-int qmm_q6k_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
-                cudaStream_t stream);
-int qmm_q8_0_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
-                 cudaStream_t stream);
-int qmm_q5k_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
-                cudaStream_t stream);
-int qmm_q4_0_cfg(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_cfg *cfg,
-                 cudaStream_t stream);
-int qmv_q5k_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
-                cudaStream_t stream);
-int qmv_q4_0_cfg(const void *w, const float *x, float *y, int rows, int k, const qmv_cfg *cfg,
-                 cudaStream_t stream);
-int moe_qmv_q8_0_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
-                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
-                     cudaStream_t stream);
-int moe_qmv_q4_0_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
-                     const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
-                     cudaStream_t stream);
-int moe_qmv_q5k_cfg(const void *w_bank, const float *x, float *y, int rows, int k,
-                    const int32_t *ids, int slots, int n_experts, const qmv_cfg *cfg,
-                    cudaStream_t stream);
 
 /* Exact decoded weights: out f32 [rows, k] (each the round-to-nearest f32 of
  * the weight's exact value). Same argument rules as the matvecs. */
@@ -346,7 +367,7 @@ int qmv_q6k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int r
  * 10 = MoE Q8_0, 11 = MoE Q4_0, 12 = MoE Q5_K, 16 = Q6_K dp4a, 17 = MoE Q6_K
  * dp4a. 13, 14 and 15 are not plans (QMV_EINVAL): batches of two or more rows
  * of x run on the tensor cores (qmm_tc_plan_detail). */
-int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *threads, int *ctas,
+int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_opts *opts, int *threads, int *ctas,
                   int *chunk_rows, int *chunks, int *smem_bytes);
 
 /* The complete launch plan for a described device, computed on the host
@@ -361,7 +382,7 @@ int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, int *
  * (a, b, c, scales, sums), of the parked partials, the ring, the barriers and
  * the counters, and the cluster size. */
 #define QMV_PLAN_DETAIL_FIELDS 30
-int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, const int *device, int *out);
+int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_opts *opts, const int *device, int *out);
 
 /* The tensor-core plan of the batched product for one tile of m (1..8) rows
  * of x on a described device (as for qmv_plan_detail). fmt: 0 = Q4_K,
@@ -373,7 +394,7 @@ int qmv_plan_detail(int fmt, int rows, int k, int slots, const qmv_cfg *cfg, con
  * bytes a thread; none for the other formats), the ring, the barriers and the
  * counters. */
 #define QMM_TC_PLAN_FIELDS 18
-int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_cfg *cfg, const int *device, int *out);
+int qmm_tc_plan_detail(int fmt, int rows, int k, int m, const qmv_opts *opts, const int *device, int *out);
 
 #ifdef __cplusplus
 }

@@ -104,3 +104,23 @@ def test_binding_fails_loudly_without_library(tmp_path):
             q.load(str(tmp_path / "missing.so"))
     finally:
         q._LIB = saved
+
+
+def test_launch_options_are_validated_per_call(lib):
+    """The overlap mode is an argument of the call (qmv_opts), not process
+    state: an unknown mode is refused on the host, and the planner's choice
+    for one mode does not depend on any earlier call's mode."""
+    A = 0x10000
+    S = 0
+    for bad in (-1, 3, 99):
+        assert lib.qmv_q4k(A, A, A, 4, 256, stream=S, overlap=bad, check=False) == lib.QMV_EINVAL
+        assert lib.qmm_q4k(A, A, A, 4, 256, 2, stream=S, overlap=bad, check=False) == lib.QMV_EINVAL
+        assert lib.moe_qmv_q4k(A, A, A, 4, 256, A, 2, 8, stream=S, overlap=bad, check=False) == lib.QMV_EINVAL
+        with pytest.raises(lib.QmvError):
+            lib.qmv_plan_detail(lib.FMT_Q4K, 4096, 4096, overlap=bad)
+    assert not hasattr(lib.load(), "qmv_set_weight_prefetch")
+    plain = lib.qmv_plan_detail(lib.FMT_Q4K, 4096, 4096)
+    indep = lib.qmv_plan_detail(lib.FMT_Q4K, 4096, 4096, overlap=lib.OVERLAP_INDEPENDENT)
+    assert indep["ctas"] < plain["ctas"]   # independent calls take fewer CTAs so several are in flight
+    assert lib.qmv_plan_detail(lib.FMT_Q4K, 4096, 4096) == plain
+    assert lib.qmv_plan_detail(lib.FMT_Q4K, 4096, 4096, overlap=lib.OVERLAP_CHAIN) == plain

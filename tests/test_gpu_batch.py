@@ -46,9 +46,9 @@ def scale_rel(ref, got):
     return float(np.max(np.abs(ref - got)) / max(float(np.max(np.abs(ref))), 1e-30))
 
 
-def run_qmm(q, fmt, w, x, rows, k, m, cfg=None):
+def run_qmm(q, fmt, w, x, rows, k, m, cfg=None, overlap=0):
     y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    getattr(q, f"qmm_{fmt}")(dev(w), dev(x), y, rows, k, m, cfg=cfg)
+    getattr(q, f"qmm_{fmt}")(dev(w), dev(x), y, rows, k, m, cfg=cfg, overlap=overlap)
     return host(y)
 
 
@@ -148,7 +148,7 @@ def test_batch_argument_errors(q):
                                         ("q5k", 64, 4352), ("q4_0", 77, 4160)])
 @pytest.mark.parametrize("m", [2, 4, 8])
 def test_batch_independent_call_plans(q, fmt, rows, k, m):
-    """Independent calls (mode 2) take half-SM CTAs of at most 8 warps, so rows
+    """Independent calls (QMV_OVERLAP_INDEPENDENT) take half-SM CTAs of at most 8 warps, so rows
     longer than 2048 weights are cut into more k-chunks than in plain launches:
     every row of y still matches the oracle, unit rows still give the weight
     columns bit for bit."""
@@ -160,12 +160,8 @@ def test_batch_independent_call_plans(q, fmt, rows, k, m):
     xu = np.zeros((m, k), dtype=np.float32)
     for i, j in enumerate(js):
         xu[i, j] = 1.0
-    old = q.qmv_set_weight_prefetch(2)
-    try:
-        y = run_qmm(q, fmt, w, x, rows, k, m)
-        yu = run_qmm(q, fmt, w, xu, rows, k, m)
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    y = run_qmm(q, fmt, w, x, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
+    yu = run_qmm(q, fmt, w, xu, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
     check_rows(oracle.qmm(fmt, w, x, m, rows, k), y)
     for i, j in enumerate(js):
         assert np.array_equal(yu[i], W[:, j]), (i, j)
@@ -178,24 +174,19 @@ def test_batch_overlap_modes_give_identical_results(q):
     cases = [(fmt, dev(synth.GEN_ROWS[fmt](st, 300, 2048)), dev(synth.gen_normal(st, 5 * 2048)))
              for fmt in FMTS]
 
-    def chain():
+    def chain(ov):
         outs = []
         for fmt, w, x in cases:
             y = torch.empty(5, 300, dtype=torch.float32, device="cuda")
-            getattr(q, f"qmm_{fmt}")(w, x, y, 300, 2048, 5)
+            getattr(q, f"qmm_{fmt}")(w, x, y, 300, 2048, 5, overlap=ov)
             outs.append(y)
         torch.cuda.synchronize()
         return [o.cpu().numpy() for o in outs]
 
-    old = q.qmv_set_weight_prefetch(0)
-    try:
-        base = chain()
-        for mode in (1, 2):
-            q.qmv_set_weight_prefetch(mode)
-            for a, b in zip(base, chain()):
-                assert np.array_equal(a, b), mode
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    base = chain(q.OVERLAP_NONE)
+    for mode in (q.OVERLAP_CHAIN, q.OVERLAP_INDEPENDENT):
+        for a, b in zip(base, chain(mode)):
+            assert np.array_equal(a, b), mode
 
 
 @pytest.mark.parametrize("name", ["qmm_q4k_4096x4096_m8", "qmm_q4k_4096x4096_m2", "qmm_q6k_4096x14336_m4",

@@ -256,8 +256,9 @@ def test_full_moe(q, fmt):
 # ------------------------------------------------- decode-chain overlap modes
 
 def test_overlap_modes_give_identical_results(q):
-    """Modes 1 and 2 change only when a call waits for the previous kernel:
-    back-to-back calls of every new entry point give the mode-0 results bit
+    """The chain and independent overlaps change only when a call waits for the
+    previous kernel: back-to-back calls of every new entry point give the
+    plain-launch results bit
     for bit (inputs written before the chain, none shared with an output)."""
     st = synth.Stream(71)
     cases = []
@@ -267,25 +268,20 @@ def test_overlap_modes_give_identical_results(q):
     for fmt in MOE_FMT:
         cases.append(("moe", fmt, dev(gen(fmt, st, 6 * 96, 512)), dev(synth.gen_normal(st, 4 * 512)), 96, 512))
 
-    def chain():
+    def chain(ov):
         outs = []
         for kind, fmt, w, x, rows, k in cases:
             if kind == "dense":
                 y = torch.empty(rows, dtype=torch.float32, device="cuda")
-                getattr(q, f"qmv_{fmt}")(w, x, y, rows, k)
+                getattr(q, f"qmv_{fmt}")(w, x, y, rows, k, overlap=ov)
             else:
                 y = torch.empty(4, rows, dtype=torch.float32, device="cuda")
-                getattr(q, f"moe_qmv_{fmt}")(w, x, y, rows, k, ids, 4, 6)
+                getattr(q, f"moe_qmv_{fmt}")(w, x, y, rows, k, ids, 4, 6, overlap=ov)
             outs.append(y)
         torch.cuda.synchronize()
         return [o.cpu().numpy() for o in outs]
 
-    old = q.qmv_set_weight_prefetch(0)
-    try:
-        base = chain()
-        for mode in (1, 2):
-            q.qmv_set_weight_prefetch(mode)
-            for a, b in zip(base, chain()):
-                assert np.array_equal(a, b), mode
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    base = chain(q.OVERLAP_NONE)
+    for mode in (q.OVERLAP_CHAIN, q.OVERLAP_INDEPENDENT):
+        for a, b in zip(base, chain(mode)):
+            assert np.array_equal(a, b), mode

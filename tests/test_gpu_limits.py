@@ -101,12 +101,8 @@ def test_batch_long_rows(q, fmt, m, mode):
     w = synth.GEN_ROWS[fmt](st, rows, k)
     x = synth.gen_normal(st, m * k).reshape(m, k)
     y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    old = q.qmv_set_weight_prefetch(mode)
-    try:
-        getattr(q, f"qmm_{fmt}")(dev(w), dev(x), y, rows, k, m)
-        torch.cuda.synchronize()
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    getattr(q, f"qmm_{fmt}")(dev(w), dev(x), y, rows, k, m, overlap=mode)
+    torch.cuda.synchronize()
     ref = oracle.qmm(fmt, w, x, m, rows, k)
     got = y.cpu().numpy()
     assert not np.any(np.isnan(got))

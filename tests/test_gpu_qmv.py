@@ -516,35 +516,30 @@ def test_weight_prefetch_chain_matches(q):
     bank = dev(synth.gen_q4k_rows(st, 8 * n, n))
     x0 = dev(synth.gen_normal(st, n) / np.float32(16))
 
-    def chain():
+    def chain(ov):
         bufs = [torch.empty(n, device="cuda") for _ in range(8)]
         cur = x0
         for i, w in enumerate(ws):
-            q.qmv_q4k(w, cur, bufs[i], n, n)
+            q.qmv_q4k(w, cur, bufs[i], n, n, overlap=ov)
             cur = bufs[i]
-        q.qmv_q6k(w6, cur, bufs[6], n, n)
+        q.qmv_q6k(w6, cur, bufs[6], n, n, overlap=ov)
         ids = (torch.arange(2, device="cuda", dtype=torch.int32) * 3 + 1)   # written by a torch kernel
         ym = torch.empty(2, n, device="cuda")
         xm = torch.stack([bufs[6], bufs[5]])
-        q.moe_qmv_q4k(bank, xm, ym, n, n, ids, 2, 8)
+        q.moe_qmv_q4k(bank, xm, ym, n, n, ids, 2, 8, overlap=ov)
         torch.cuda.synchronize()
         return [b.clone() for b in bufs[:7]] + [ym.clone()]
 
-    old = q.qmv_set_weight_prefetch(False)
-    try:
-        ref = chain()
-        q.qmv_set_weight_prefetch(True)
-        for _ in range(3):
-            got = chain()
-            for a, b in zip(ref, got):
-                assert torch.equal(a, b)
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    ref = chain(q.OVERLAP_NONE)
+    for _ in range(3):
+        got = chain(q.OVERLAP_CHAIN)
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
     assert torch.isfinite(ref[-1]).all()
 
 
 def test_independent_inputs_mode_matches(q):
-    """Mode 2 (inputs read before the dependency wait): a stream of calls that
+    """QMV_OVERLAP_INDEPENDENT (inputs read before the dependency wait): a stream of calls that
     share one activation (like Q, K, V projections), with every output buffer
     reused by the next-but-one call, must give bitwise the results of plain
     launches; the MoE call reads ids written long before."""
@@ -558,26 +553,21 @@ def test_independent_inputs_mode_matches(q):
     ids = dev(np.array([3, 6], dtype=np.int32))
     torch.cuda.synchronize()
 
-    def stream_of_calls():
+    def stream_of_calls(ov):
         bufs = [torch.full((n,), float("nan"), device="cuda") for _ in range(2)]
         outs = []
         for i, w in enumerate(ws):
-            q.qmv_q4k(w, x, bufs[i % 2], n, n)
+            q.qmv_q4k(w, x, bufs[i % 2], n, n, overlap=ov)
             outs.append(bufs[i % 2].clone())   # a torch kernel between calls
-        q.qmv_q6k(w6, x, bufs[0], n, n)
+        q.qmv_q6k(w6, x, bufs[0], n, n, overlap=ov)
         ym = torch.empty(2, n, device="cuda")
-        q.moe_qmv_q4k(bank, xm, ym, n, n, ids, 2, 8)
+        q.moe_qmv_q4k(bank, xm, ym, n, n, ids, 2, 8, overlap=ov)
         torch.cuda.synchronize()
         return outs + [bufs[0].clone(), ym.clone()]
 
-    old = q.qmv_set_weight_prefetch(0)
-    try:
-        ref = stream_of_calls()
-        for mode in (2, 1, 2):
-            q.qmv_set_weight_prefetch(mode)
-            got = stream_of_calls()
-            for a, b in zip(ref, got):
-                assert torch.equal(a, b)
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    ref = stream_of_calls(q.OVERLAP_NONE)
+    for mode in (2, 1, 2):
+        got = stream_of_calls(mode)
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
     assert all(torch.isfinite(t).all() for t in ref)

@@ -109,13 +109,9 @@ def test_random_batch(q, fmt, rows, k, m, cfg, mode):
     w = synth.GEN_ROWS[fmt](st, rows, k)
     x = synth.gen_normal(st, m * k).reshape(m, k)
     y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    old = q.qmv_set_weight_prefetch(mode)
-    try:
-        rc = getattr(q, f"qmm_{fmt}")(torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda(), y, rows, k, m,
-                                      cfg=cfg, check=False)
-        torch.cuda.synchronize()
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    rc = getattr(q, f"qmm_{fmt}")(torch.from_numpy(w).cuda(), torch.from_numpy(x).cuda(), y, rows, k, m,
+                                  cfg=cfg, overlap=mode, check=False)
+    torch.cuda.synchronize()
     if rc == q.QMV_ETOOBIG:
         assert cfg is not None   # a forced plan refused on the host, nothing launched
         return

@@ -69,11 +69,7 @@ def q():
 def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
     """Replay the plan computed under launch mode `mode` (0: plain, 2:
     independent calls)."""
-    old = q.qmv_set_weight_prefetch(mode)
-    try:
-        P = q.qmv_plan_detail(FMT_ID[fmt], rows, k, slots, cfg, DEVICE)
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    P = q.qmv_plan_detail(FMT_ID[fmt], rows, k, slots, cfg, DEVICE, overlap=mode)
     f = fmt_info(fmt, slots)
     nb = k // f["qk"]
     U = f["units"](nb)
@@ -299,11 +295,7 @@ def tc_replay(q, fmt, rows, k, m, cfg=None, mode=0):
     plain, 2: independent calls, where CTAs of at most 8 warps take at most
     half an SM's shared memory unless that plan does not fit)."""
     fid, qk, bb = TC_FMT[fmt]
-    old = q.qmv_set_weight_prefetch(mode)
-    try:
-        P = q.qmm_tc_plan_detail(fid, rows, k, m, cfg, DEVICE)
-    finally:
-        q.qmv_set_weight_prefetch(old)
+    P = q.qmm_tc_plan_detail(fid, rows, k, m, cfg, DEVICE, overlap=mode)
     ng = k // 32
     NS = -(-ng // 8)
     kmax = min(cfg["warps"], 16) if cfg and cfg.get("warps") else 16
