@@ -282,6 +282,78 @@ __device__ __forceinline__ void limb_words(uint32_t t0, uint32_t t1, uint32_t t2
     aw = (__byte_perm(a01, a23, 0x5410) + 0x60606060u) ^ 0x80808080u;
 }
 
+// Limb words, sum and scale of one 16-element half (elements 16h .. 16h+15)
+// held as four float4 by this thread; its partner lane (lane ^ 1) holds the
+// other half of the 32-element group and calls this at the same time (the
+// group maximum is exchanged with one shuffle, so every lane of the warp must
+// call it). Writes the half's 16-byte chunk of each limb table, its sum, and
+// (even h) the group's scale into the CTA's own tables when `store` is set.
+__device__ __forceinline__ void prep_half(const float4 (&v)[4], uint32_t h, bool store, uint8_t* smem,
+                                          const LimbTables& L) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)), fmaxf(fabsf(v[m].z), fabsf(v[m].w))));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));    // the group's other half
+    const int E = static_cast<int>(__float_as_uint(mx) >> 23);   // biased exponent of the group maximum
+    int s = LIMB_BITS - (E - 126);                               // max < 2^(E-126) for a normal maximum
+    s = s > 126 ? 126 : s;                                       // zero / tiny groups
+    const float p2s = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+    const float p2ms = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+    uint4 A, B, C;
+    uint32_t* Ap = &A.x;
+    uint32_t* Bp = &B.x;
+    uint32_t* Cp = &C.x;
+    uint32_t tsum = 0;
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+        const uint32_t t0 = __float_as_uint(__fmaf_rn(v[m].x, p2s, LIMB_MAGIC));
+        const uint32_t t1 = __float_as_uint(__fmaf_rn(v[m].y, p2s, LIMB_MAGIC));
+        const uint32_t t2 = __float_as_uint(__fmaf_rn(v[m].z, p2s, LIMB_MAGIC));
+        const uint32_t t3 = __float_as_uint(__fmaf_rn(v[m].w, p2s, LIMB_MAGIC));
+        limb_words(t0, t1, t2, t3, Ap[m], Bp[m], Cp[m]);
+        tsum += t0 + t1 + t2 + t3;
+    }
+    // sum of the 16 X: sum of the patterns minus 16 magic patterns (mod 2^32)
+    const int X = static_cast<int>(tsum - 16u * LIMB_MAGIC_BITS);
+    if (store) {
+        const uint32_t o = limb_chunk(h) << 4;
+        *reinterpret_cast<uint4*>(smem + L.la + o) = A;
+        *reinterpret_cast<uint4*>(smem + L.lb + o) = B;
+        *reinterpret_cast<uint4*>(smem + L.lc + o) = C;
+        reinterpret_cast<float*>(smem + L.xsum16)[h] = __int2float_rn(X) * p2ms;
+        if ((h & 1u) == 0) reinterpret_cast<float*>(smem + L.xs)[h >> 1] = p2ms;
+    }
+}
+
+// Fill the CTA's own limb tables for x[0, k) (k a multiple of 32) with all T
+// threads (T even): thread t converts halves t, t + T, t + 2T, ..., BATCH at
+// a time with all of a batch's loads issued before any use. A half and its
+// group partner (h ^ 1) land in neighbouring lanes of one warp because T is
+// even; lanes past the last half join the shuffle with zeros and store
+// nothing. The caller makes the tables visible with a block barrier.
+template <int BATCH>
+__device__ __forceinline__ void prep_limbs_cta(const float* __restrict__ x, int k, uint8_t* smem,
+                                               const LimbTables& L, int tid, int T) {
+    const int nh = k >> 4;
+    const float4* __restrict__ x4 = reinterpret_cast<const float4*>(x);
+    for (int base = 0; base < nh; base += BATCH * T) {
+        float4 v[BATCH][4];
+#pragma unroll
+        for (int b = 0; b < BATCH; b++) {
+            const int h = base + b * T + tid;
+#pragma unroll
+            for (int m = 0; m < 4; m++) v[b][m] = h < nh ? __ldg(x4 + 4 * h + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; b++) {
+            if (base + b * T >= nh) break;   // uniform across the block
+            const int h = base + b * T + tid;
+            prep_half(v[b], static_cast<uint32_t>(h), h < nh, smem, L);
+        }
+    }
+}
+
 // Fill the limb tables for x[0, k) (k a multiple of 32) with all T threads of
 // the block (T even), shared among the CL CTAs of a cluster: CTA `rank`
 // converts halves [rank * nh / CL, (rank + 1) * nh / CL) of the nh = k/16

@@ -58,7 +58,7 @@ struct Q4K {
     struct X {
         uint32_t a[16], b[16], c[16];   // limbs of the chunk's 64 activations
         float xs0, xs1;                 // 2^-s of the two 32-groups
-        float xsum0, xsum1;             // activation sums of the two sub-blocks
+        float nxsum0, nxsum1;           // minus the activation sums of the two sub-blocks
     };
     struct L {
         uint32_t qoff;   // byte offset of the chunk's codes in the block: 16 + 32c
@@ -91,8 +91,8 @@ struct Q4K {
         const float* xsum16 = reinterpret_cast<const float*>(smem + T.xsum16);
         x.xs0 = xs[e0 >> 5];
         x.xs1 = xs[(e0 >> 5) + 1];
-        x.xsum0 = xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1];
-        x.xsum1 = xsum16[(e0 >> 4) + 2] + xsum16[(e0 >> 4) + 3];
+        x.nxsum0 = -(xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1]);
+        x.nxsum1 = -(xsum16[(e0 >> 4) + 2] + xsum16[(e0 >> 4) + 3]);
     }
 
     // a: shared address of the super-block (16-byte aligned).
@@ -126,19 +126,28 @@ struct Q4K {
         const uint32_t m_hi = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
         const uint32_t SC = l.hic ? sc_hi : sc_lo;
         const uint32_t M = l.hic ? m_hi : m_lo;
-        const float d = f16_lo(h.x), dmin = f16_hi(h.x);
-        const float nd = -d * TWO23, ndm = -dmin * TWO23;
-        const float dsc0 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel)), nd);
-        const float dsc1 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel + 1)), nd);
-        const float dm0 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel)), ndm);
-        const float dm1 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel + 1)), ndm);
-        const float t0 = __int2float_rn(s0) * x.xs0;
-        const float t1 = __int2float_rn(s1) * x.xs1;
-        r = __fmaf_rn(dsc0, t0, r);
-        r = __fmaf_rn(-dm0, x.xsum0, r);
-        r = __fmaf_rn(dsc1, t1, r);
-        r = __fmaf_rn(-dm1, x.xsum1, r);
-        return r;
+        return scale_pairs(h.x, SC, M, l.sel, __int2float_rn(s0) * x.xs0, __int2float_rn(s1) * x.xs1, x.nxsum0,
+                           x.nxsum1, r);
+    }
+
+    // r + d*sc_0*t0 - dmin*m_0*S0 + d*sc_1*t1 - dmin*m_1*S1 for the chunk's two
+    // sub-blocks, (d, dmin) the block's f16 pair in dd, the 6-bit scales and
+    // mins as byte lanes of SC and M (byte sel & 3 and the next one), S_j the
+    // activation sums (given negated). The scale and min of a sub-block form
+    // one f32 pair: one packed fma gives (d*sc_j, dmin*m_j) exactly (through
+    // the exponent field, see TWO23), and one more adds d*sc_j*t_j and
+    // -dmin*m_j*S_j into the pair (r, 0).
+    __device__ __forceinline__ static float scale_pairs(uint32_t dd, uint32_t SC, uint32_t M, uint32_t sel, float t0,
+                                                        float t1, float ns0, float ns1, float r) {
+        const float2 d2 = __half22float2(*reinterpret_cast<const __half2*>(&dd));   // (d, dmin)
+        const float2 n2 = __fmul2_rn(d2, make_float2(-TWO23, -TWO23));
+        const float2 g0 = __ffma2_rn(d2, make_float2(__uint_as_float(prmt(SC, 0x4B000000u, sel)),
+                                                     __uint_as_float(prmt(M, 0x4B000000u, sel))), n2);
+        const float2 g1 = __ffma2_rn(d2, make_float2(__uint_as_float(prmt(SC, 0x4B000000u, sel + 1)),
+                                                     __uint_as_float(prmt(M, 0x4B000000u, sel + 1))), n2);
+        float2 acc = __ffma2_rn(g0, make_float2(t0, ns0), make_float2(r, 0.0f));
+        acc = __ffma2_rn(g1, make_float2(t1, ns1), acc);
+        return acc.x + acc.y;
     }
 };
 
@@ -321,17 +330,8 @@ struct Q5K {
         const uint32_t m_hi = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
         const uint32_t SC = l.hic ? sc_hi : sc_lo;
         const uint32_t M = l.hic ? m_hi : m_lo;
-        const float d = f16_lo(h.x), dmin = f16_hi(h.x);
-        const float nd = -d * TWO23, ndm = -dmin * TWO23;
-        const float dsc0 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel)), nd);
-        const float dsc1 = __fmaf_rn(d, __uint_as_float(prmt(SC, 0x4B000000u, l.sel + 1)), nd);
-        const float dm0 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel)), ndm);
-        const float dm1 = __fmaf_rn(dmin, __uint_as_float(prmt(M, 0x4B000000u, l.sel + 1)), ndm);
-        r = __fmaf_rn(dsc0, __int2float_rn(s0) * x.xs0, r);
-        r = __fmaf_rn(-dm0, x.xsum0, r);
-        r = __fmaf_rn(dsc1, __int2float_rn(s1) * x.xs1, r);
-        r = __fmaf_rn(-dm1, x.xsum1, r);
-        return r;
+        return Q4K::scale_pairs(h.x, SC, M, l.sel, __int2float_rn(s0) * x.xs0, __int2float_rn(s1) * x.xs1, x.nxsum0,
+                                x.nxsum1, r);
     }
 };
 
@@ -430,19 +430,28 @@ struct Q6K {
             sb[3] = dp4a_us(w3, x.b[12 + i], sb[3]);
             sc[3] = dp4a_us(w3, x.c[12 + i], sc[3]);
         }
-        const float nd = -d * THREE22;
+        // Quarters (0, 1) and (2, 3) as f32 pairs: scales d*scale (exact,
+        // through the exponent field, see THREE22), the scaled integer sums,
+        // the -32 fold and the accumulation each one packed instruction a pair.
+        const float2 dd = make_float2(d, d);
+        const float2 nd = __fmul2_rn(dd, make_float2(-THREE22, -THREE22));
+        float2 acc = make_float2(r, 0.0f);
 #pragma unroll
-        for (int qd = 0; qd < 4; qd++) {
+        for (int pr = 0; pr < 2; pr++) {
             // |sum q*X| <= 16 * 63 * 2^21 < 2^31 per quarter.
-            const int s = sa[qd] * 65536 + sb[qd] * 256 + sc[qd];
-            const uint32_t sw = (qd < 2) ? scw.x : scw.y;
-            const uint32_t sx = prmt(sw, 0u, (qd & 1) ? l.sel1 : l.sel0);   // the int8 scale, sign-extended
-            const float ds = __fmaf_rn(d, __uint_as_float(sx + 0x4B400000u), nd);
-            const float t = __int2float_rn(s) * x.xs[qd];
-            const float u = __fmaf_rn(-32.0f, x.xsum[qd], t);
-            r = __fmaf_rn(ds, u, r);
+            const int s0 = sa[2 * pr] * 65536 + sb[2 * pr] * 256 + sc[2 * pr];
+            const int s1 = sa[2 * pr + 1] * 65536 + sb[2 * pr + 1] * 256 + sc[2 * pr + 1];
+            const uint32_t sw = pr == 0 ? scw.x : scw.y;
+            const uint32_t sx0 = prmt(sw, 0u, l.sel0);   // the int8 scales, sign-extended
+            const uint32_t sx1 = prmt(sw, 0u, l.sel1);
+            const float2 ds = __ffma2_rn(dd, make_float2(__uint_as_float(sx0 + 0x4B400000u),
+                                                         __uint_as_float(sx1 + 0x4B400000u)), nd);
+            const float2 t = __fmul2_rn(make_float2(__int2float_rn(s0), __int2float_rn(s1)),
+                                        make_float2(x.xs[2 * pr], x.xs[2 * pr + 1]));
+            const float2 u = __ffma2_rn(make_float2(-32.0f, -32.0f), make_float2(x.xsum[2 * pr], x.xsum[2 * pr + 1]), t);
+            acc = __ffma2_rn(ds, u, acc);
         }
-        return r;
+        return acc.x + acc.y;
     }
 };
 

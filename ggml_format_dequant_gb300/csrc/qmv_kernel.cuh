@@ -64,6 +64,8 @@ struct KParams {
     int S;                      // ring slots per row group
     int rq, rrem;               // rows per CTA: rq or rq + 1 (the first rrem CTAs)
     int gq[2], grem[2];         // rows per row group for a CTA of rq ([0]) or rq + 1 ([1]) rows
+    int npc4[4];                // pieces of a row group: [2 * (CTA of rq + 1 rows) + (group of gq + 1 rows)]
+    uint8_t wmap[16];           // warp w works on row group wmap[w] >> 4, k-slice wmap[w] & 15 (0xff: idle)
     int W;                      // parked sums per row: KS, or 1 (early inputs), or 0 (rows written at once)
     int aligned8;               // every unit starts 8-byte aligned in shared memory (Q8_0 dp4a)
     int CL;                     // CTAs per cluster sharing the activation prep (1: no cluster)
@@ -179,15 +181,17 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
     // before the cluster barrier below unless all of its cluster do.)
     if (nrows <= 0) return;
 
-    // ---- this warp: row group rg, k-slice ks
-    const int nwork = p.NG * p.KS;
-    const bool working = warp < nwork;
-    const int rg = warp / p.KS;
-    const int ks = warp - rg * p.KS;
+    // ---- this warp: row group rg, k-slice ks (mapping and piece counts
+    // precomputed on the host)
+    const uint32_t wm = p.wmap[warp];
+    const bool working = wm != 0xffu;
+    const int rg = static_cast<int>(wm >> 4);
+    const int ks = static_cast<int>(wm & 15u);
     const int gq = p.gq[big], grem = p.grem[big];
     const int glo = rg * gq + min(rg, grem);          // first row of the group, CTA-local
-    const int gn = working ? gq + (rg < grem ? 1 : 0) : 0;
-    const int npc = (gn + p.CR - 1) / p.CR;          // pieces of the group
+    const int longer = rg < grem ? 1 : 0;
+    const int gn = working ? gq + longer : 0;
+    const int npc = working ? p.npc4[2 * big + longer] : 0;   // pieces of the group
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t ring = sbase + p.off_ring + static_cast<uint32_t>(rg * p.S) * p.slot_stride;
@@ -228,7 +232,10 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
     if constexpr (F::LIMBS) {
         // The activation limb tables, shared among the CTAs of a cluster (all
         // of them work on the same x: the same matrix, or the same MoE slot).
-        prep_limbs<2>(xrow, p.k, smem, p.lt, tid, static_cast<int>(blockDim.x), p.CL, p.CL > 1 ? cluster_rank() : 0u);
+        if (p.CL > 1)
+            prep_limbs<2>(xrow, p.k, smem, p.lt, tid, static_cast<int>(blockDim.x), p.CL, cluster_rank());
+        else
+            prep_limbs_cta<4>(xrow, p.k, smem, p.lt, tid, static_cast<int>(blockDim.x));
     }
     if (p.CL > 1)
         cluster_sync();   // every CTA's limb tables complete; barriers and counters initialized

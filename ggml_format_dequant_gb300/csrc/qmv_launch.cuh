@@ -129,7 +129,8 @@ inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a
 // Launch plan of format F for `rows` x `k` (slots: MoE slot count, 1 dense)
 // on a device described by `di`, for a given (or the default) CTA count.
 template <class F>
-inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const qmv_opts* cfg, KParams* kp, Plan* pl) {
+inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const qmv_opts* cfg, KParams* kp, Plan* pl,
+                          long long smem_cap = -1) {
     const int nb = k / F::QK;
     const int U = F::units(nb);
     const int KS = (U + 31) / 32;
@@ -221,7 +222,7 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
     // else all a CTA may take.
     const long long per_sm = di.smem_sm - 2LL * di.smem_reserved;
     const long long half = per_sm / 2;
-    const long long full = di.smem_optin;
+    const long long full = smem_cap > 0 ? std::min<long long>(smem_cap, di.smem_optin) : di.smem_optin;
 
     auto slot_stride_of = [&](int cr) { return round_up(static_cast<long long>(cr) * rowbytes + 32 + F::SLACK, 128); };
     auto tail = [&](int s) { return 8LL * NG * s + 4LL * (NG * s + NG + 1); };
@@ -304,7 +305,10 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
         const int n = kp->rq + b;
         kp->gq[b] = n / NG;
         kp->grem[b] = n % NG;
+        for (int l = 0; l < 2; l++) kp->npc4[2 * b + l] = (kp->gq[b] + l + CR - 1) / CR;
     }
+    for (int w = 0; w < MAX_WARPS; w++)
+        kp->wmap[w] = w < NG * KS ? static_cast<uint8_t>(((w / KS) << 4) | (w % KS)) : uint8_t{0xff};
     *pl = P;
     return QMV_OK;
 }
@@ -326,7 +330,8 @@ inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qm
     const int start = std::max(1, di.nsm / (2 * per));
     if (start >= pl->parts) return rc;   // small shapes: already fewer CTAs
     qmv_opts c = *cfg;
-    for (int parts = start; parts < pl->parts; parts++) {
+    // (a share that needs a ring at every-SM CTAs needs one at fewer CTAs too)
+    for (int parts = start; kp->S == 1 && parts < pl->parts; parts++) {
         c.ctas = parts;
         KParams k2 = *kp;
         Plan p2;
@@ -334,6 +339,28 @@ inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qm
         const int rpc = k2.rq + (k2.rrem ? 1 : 0);
         if (k2.S == 1 && k2.CR * k2.NG >= rpc && static_cast<long long>(p2.smem) <= half &&
             p2.T <= 32 * WARPS_TWO_PER_SM) {
+            *kp = k2;
+            *pl = p2;
+            return QMV_OK;
+        }
+    }
+    // A share too large for half an SM: for the f32-activation formats, CTAs
+    // of at most WARPS_TWO_PER_SM warps (one row group) in half an SM's shared
+    // memory, streaming two-row pieces through two ring slots, so that the
+    // next call's CTA runs its start-up (copies, activation prep) beside this
+    // one's decode instead of after it (measured on GB300, Q6_K 4096 x 14336:
+    // 11.76 -> 10.25 us a call; the same plan is slower for chained and plain
+    // calls, where only one of the two CTAs on an SM can decode).
+    if (F::LIMBS && kp->S > 1) {
+        qmv_opts c = *cfg;
+        c.warps = WARPS_TWO_PER_SM;
+        c.ctas = per > 1 ? (di.nsm + per - 1) / per : di.nsm;
+        c.chunk_rows = 2;
+        c.chunks = 2;
+        KParams k2 = *kp;
+        Plan p2;
+        if (!make_plan_core<F>(di, rows, k, slots, &c, &k2, &p2, half) && k2.NG == 1 && k2.S == 2 &&
+            static_cast<long long>(p2.smem) <= half && p2.T <= 32 * WARPS_TWO_PER_SM) {
             *kp = k2;
             *pl = p2;
             return QMV_OK;

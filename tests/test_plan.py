@@ -245,16 +245,21 @@ def test_retired_batch_plan_ids(q):
 
 @pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
 def test_independent_call_plans(q, fmt, rows, k, slots):
-    """Mode 2 (independent calls): the whole-share workloads take about two
-    thirds of the SMs with CTAs that still fit in half an SM; every index is
-    replayed as for the default plans."""
+    """Independent calls: the whole-share workloads take about two thirds of
+    the SMs with CTAs that still fit in half an SM; the f32-activation
+    workloads whose share does not fit take one half-SM CTA an SM, streaming
+    two-row pieces through two ring slots; every index is replayed as for the
+    default plans."""
     P = replay(q, fmt, rows, k, slots, mode=2)
     per = max(slots, 1)
+    half = (DEVICE[2] - 2 * DEVICE[3]) // 2
     if (fmt, rows) in (("q4k", 4096), ("moe", 768), ("q4d", 4096), ("moe4d", 768)):
         assert DEVICE[0] // (2 * per) <= P["ctas"] < -(-DEVICE[0] // per)
-        assert P["S"] == 1 and P["smem"] <= (DEVICE[2] - 2 * DEVICE[3]) // 2 and P["threads"] <= 256
+        assert P["S"] == 1 and P["smem"] <= half and P["threads"] <= 256
     if (fmt, rows) in (("q8d", 14336), ("q6k", 4096)):
         assert P["ctas"] == DEVICE[0]
+    if (fmt, rows) == ("q6k", 4096):
+        assert P["NG"] == 1 and P["S"] == 2 and P["CR"] == 2 and P["smem"] <= half and P["threads"] <= 256
 
 
 def test_chain_shapes(q):
