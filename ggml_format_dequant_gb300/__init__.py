@@ -29,7 +29,7 @@ QMV_STATUS_WAIT_TIMEOUT = 2
 # Plan ids of qmv_plan_info / qmv_plan_detail (13-15 are not plans).
 (FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A,
  FMT_Q5K, FMT_Q4_0, FMT_MOE_Q8_0, FMT_MOE_Q4_0, FMT_MOE_Q5K) = range(13)
-FMT_Q6K_DP4A, FMT_MOE_Q6K_DP4A = 16, 17
+FMT_Q6K_DP4A, FMT_MOE_Q6K_DP4A, FMT_Q8_DP4A_QUANT = 16, 17, 18
 
 
 class QmvLibraryMissing(RuntimeError):
@@ -65,6 +65,8 @@ _SIG = {
     "qmv_q8_dp4a": [_P, _P, _P, _P, _I, _I, _P],
     "moe_qmv_q4k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
     "qmv_q4k_dp4a": [_P, _P, _P, _P, _I, _I, _P],
+    "qmv_q8_dp4a_quant": [_P, _P, _P, _I, _I, _P],
+    "qmv_q8_dp4a_quant_ex": [_P, _P, _P, _I, _I, _P, _P],
     "moe_qmv_q6k": [_P, _P, _P, _I, _I, _P, _I, _I, _P],
     "moe_qmv_q6k_ex": [_P, _P, _P, _I, _I, _P, _I, _I, _P, _P],
     "moe_qmv_q4k_dp4a": [_P, _P, _P, _P, _I, _I, _P, _I, _I, _P],
@@ -109,6 +111,7 @@ _SIG = {
     "qmv_q8_dp4a_blockdots": [_P, _P, _P, _I, _I, _P],
     "qmv_device_status": [_P, _I],
     "qmv_selftest_wait_timeout": [ctypes.c_ulonglong, _P],
+    "qmv_selftest_timeout_path": [_P, _P, _P, _I, _I, _I, _P],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "qmv_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
     "qmm_tc_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
@@ -254,6 +257,13 @@ def qmv_q8_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, overlap=0, check=T
                  check=check)
 
 
+def qmv_q8_dp4a_quant(w, x, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
+    if cfg is None and not overlap:
+        return _call("qmv_q8_dp4a_quant", _ptr(w), _ptr(x), _ptr(y), rows, k, _stream(stream), check=check)
+    return _call("qmv_q8_dp4a_quant_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, _opts(cfg, overlap), _stream(stream),
+                 check=check)
+
+
 def qmv_q4k_dp4a(w, xq, xs, y, rows, k, stream=None, cfg=None, overlap=0, check=True):
     if cfg is None and not overlap:
         return _call("qmv_q4k_dp4a", _ptr(w), _ptr(xq), _ptr(xs), _ptr(y), rows, k, _stream(stream), check=check)
@@ -354,6 +364,10 @@ def qmv_q8_dp4a_blockdots(w, xq, dots, rows, k, stream=None, check=True):
 
 def qmv_selftest_wait_timeout(limit_ns, stream=None, check=True):
     return _call("qmv_selftest_wait_timeout", int(limit_ns), _stream(stream), check=check)
+
+
+def qmv_selftest_timeout_path(w, x, y, rows, k, m=1, stream=None, check=True):
+    return _call("qmv_selftest_timeout_path", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _stream(stream), check=check)
 
 
 def qmv_device_status(clear=True) -> int:

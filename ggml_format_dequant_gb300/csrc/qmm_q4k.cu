@@ -8,8 +8,9 @@ namespace qmvi {
 
 using namespace qmv;
 
-int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s) {
-    return qmm_tc_run<Q4KT>(w, x, y, rows, k, m, cfg, s);
+int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s,
+            int force_timeout) {
+    return qmm_tc_run<Q4KT>(w, x, y, rows, k, m, cfg, s, force_timeout);
 }
 
 int status_qmm_q4k(unsigned int* out, int clear) { return status_rw(out, clear); }

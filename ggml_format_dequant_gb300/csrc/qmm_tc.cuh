@@ -64,6 +64,7 @@ struct TParams {
     int S;                        // ring slots
     int rq, rrem;                 // rows per CTA: rq or rq + 1 (the first rrem CTAs)
     int early_inputs;
+    int force_timeout;            // failure-path test: every first wait reports a copy that did not land
     uint32_t slot_stride;         // bytes per slot (rows rounded up to 16)
     uint32_t off_red, off_sums, off_ring, off_bars, off_cnt;
 };
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
     for (int pi = 0; pi < np; pi++) {
         const int c = pi / npc, pc = pi - (pi / npc) * npc;
         if (pc == 0 && c > 0) load_chunk(c);
-        const bool landed = __all_sync(FULL, mbar_wait_bounded(bars + 8u * s, par));
+        const bool landed = !p.force_timeout && __all_sync(FULL, mbar_wait_bounded(bars + 8u * s, par));
         if (!landed) {
             if (lane == 0) {
                 atomicOr(&g_status, STATUS_WAIT_TIMEOUT);
@@ -827,10 +828,17 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
 
     __syncthreads();
     if (*timeout) {
+        // a copy did not land in time: let the copies in flight land (bounded),
+        // then mark the CTA's outputs NaN so that no stale y reads as a result
         if (tid == 0) {
             const int n = *issued;
             for (int pi = n - p.S > 0 ? n - p.S : 0; pi < n; pi++)
                 if (!mbar_wait_bounded(bars + 8u * (pi % p.S), static_cast<uint32_t>((pi / p.S) & 1))) break;
+        }
+        pdl_dependency_wait();
+        for (int e = tid; e < nrows * p.m; e += blockDim.x) {
+            const int r = e / p.m, i = e - (e / p.m) * p.m;
+            p.y[static_cast<long long>(i) * p.rows + R0 + r] = __int_as_float(0x7fc00000);
         }
         return;
     }
@@ -998,7 +1006,7 @@ inline int launch_tc(const TParams& tp, const Plan& pl, cudaStream_t stream) {
 // tiles of rows of x, one launch each (each launch reads W once).
 template <class F>
 inline int qmm_tc_run(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
-                      cudaStream_t s) {
+                      cudaStream_t s, int force_timeout = 0) {
     const int tiles = (m + TC_COLS - 1) / TC_COLS;
     DevInfo di;
     int rc = dev_info(&di, nullptr);
@@ -1013,6 +1021,7 @@ inline int qmm_tc_run(const void* w, const float* x, float* y, int rows, int k, 
         tp.x = x + static_cast<long long>(m0) * k;
         tp.y = y + static_cast<long long>(m0) * rows;
         tp.wbytes = static_cast<unsigned long long>(rows) * tp.wpitch;
+        tp.force_timeout = force_timeout;
         rc = launch_tc<F>(tp, pl, s);
         if (rc) return rc;
         m0 += mt;

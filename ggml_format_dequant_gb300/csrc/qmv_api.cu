@@ -194,6 +194,17 @@ int qmv_q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int 
     return qmv_q8_dp4a_ex(w, xq, xs, y, rows, k, nullptr, stream);
 }
 
+int qmv_q8_dp4a_quant_ex(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg,
+                         cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
+    int rc = check_dense(w, x, y, rows, k, 32, 34);
+    return rc ? rc : qmvi::q8_dp4a_quant(w, x, y, rows, k, cfg, stream);
+}
+
+int qmv_q8_dp4a_quant(const void* w, const float* x, float* y, int rows, int k, cudaStream_t stream) {
+    return qmv_q8_dp4a_quant_ex(w, x, y, rows, k, nullptr, stream);
+}
+
 int qmv_q4k_dp4a_ex(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k,
                      const qmv_opts* cfg, cudaStream_t stream) {
     if (!opts_ok(cfg)) return QMV_EINVAL;
@@ -378,6 +389,15 @@ const char* qmv_strerror(int code) {
     }
 }
 
+int qmv_selftest_timeout_path(const void* w, const float* x, float* y, int rows, int k, int m,
+                              cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 144);
+    if (!rc && (m <= 0 || m > 8)) rc = QMV_EINVAL;
+    if (rc) return rc;
+    return m == 1 ? qmvi::q4k(w, x, y, rows, k, nullptr, stream, 1)
+                  : qmvi::qmm_q4k(w, x, y, rows, k, m, nullptr, stream, 1);
+}
+
 int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {
     if (limit_ns == 0 || limit_ns > 100000000ull) return QMV_EINVAL;
     return qmvi::selftest_wait_timeout(limit_ns, stream);
@@ -411,12 +431,13 @@ bool plan_is_moe(int fmt) { return fmt == 4 || fmt == 6 || fmt == 7 || (fmt >= 1
 // Plan of format fmt on device `di`.
 int plan_of(const qmv::DevInfo& di, int fmt, int rows, int k, int slots, const qmv_opts* cfg, qmv::KParams* kp,
             qmv::Plan* pl) {
-    static const int qk[18] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256, 256, 256, 32, 256, 256};
-    if (fmt < 0 || fmt > 17 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
+    static const int qk[19] = {256, 256, 32, 32, 256, 256, 256, 256, 256, 32, 32, 32, 256, 256, 256, 32, 256, 256, 32};
+    if (fmt < 0 || fmt > 18 || rows <= 0 || k <= 0 || k % qk[fmt]) return QMV_EINVAL;
     const bool moe = plan_is_moe(fmt);
     if (moe && slots <= 0) return QMV_EINVAL;
     if (fmt == 16) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, 1, cfg, kp, pl);
     if (fmt == 17) return qmv::make_plan_for<qmv::Q6D>(di, rows, k, slots, cfg, kp, pl);
+    if (fmt == 18) return qmv::make_plan_for<qmv::Q8DQ>(di, rows, k, 1, cfg, kp, pl);
     if (fmt >= 13 && fmt <= 15) return QMV_EINVAL;   // batches of two or more rows run on the tensor cores
     if (!moe) slots = 1;
     switch (fmt) {

@@ -354,6 +354,44 @@ __device__ __forceinline__ void prep_limbs_cta(const float* __restrict__ x, int 
     }
 }
 
+// The activation quantization of the dp4a path, done by a CTA into its own
+// shared memory: one warp per 32-element block (four blocks a round, loads
+// first), amax = max|x| (a warp max of the |x| bit patterns, ordered like the
+// magnitudes for finite values), inv = 127/amax and d = amax/127 as IEEE f32
+// divides, q = clamp(round_half_even(x * inv), -127, 127) with one f32
+// multiply; amax == 0 gives d = 0 and q = 0. The same steps as the standalone
+// quantizer, so the codes and scales are the same bit for bit. xq: k bytes,
+// xs: k/32 floats; the caller publishes them with a block barrier.
+__device__ __forceinline__ void quantize_x_cta(const float* __restrict__ x, int k, int8_t* xq, float* xs, int tid,
+                                               int T) {
+    const int lane = tid & 31, warp = tid >> 5, nw = T >> 5;
+    const int nblk = k >> 5;
+    for (int b0 = warp; b0 < nblk; b0 += 4 * nw) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int b = b0 + j * nw;
+            v[j] = b < nblk ? __ldg(x + 32 * b + lane) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int b = b0 + j * nw;
+            if (b >= nblk) break;   // uniform across the warp
+            const float amax = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(v[j]) & 0x7fffffffu));
+            int q = 0;
+            float d = 0.0f;
+            if (amax != 0.0f) {
+                const float inv = __fdiv_rn(127.0f, amax);
+                q = __float2int_rn(__fmul_rn(v[j], inv));
+                q = q > 127 ? 127 : (q < -127 ? -127 : q);
+                d = __fdiv_rn(amax, 127.0f);
+            }
+            xq[32 * b + lane] = static_cast<int8_t>(q);
+            if (lane == 0) xs[b] = d;
+        }
+    }
+}
+
 // Fill the limb tables for x[0, k) (k a multiple of 32) with all T threads of
 // the block (T even), shared among the CL CTAs of a cluster: CTA `rank`
 // converts halves [rank * nh / CL, (rank + 1) * nh / CL) of the nh = k/16

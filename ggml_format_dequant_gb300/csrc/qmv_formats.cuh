@@ -24,6 +24,8 @@
 // units) and SLACK (bytes its loads may read past the end of a row).
 #pragma once
 
+#include <type_traits>
+
 #include "qmv_device.cuh"
 
 namespace qmv {
@@ -822,5 +824,41 @@ struct Q8D {
             if (j < l.nblk) out[j] = block_dot8(q[j], x.q[j]);
     }
 };
+
+// ============================================ Q8_0, f32 x quantized in the kernel
+//
+// The dp4a path of Q8_0 with the activation quantization folded into the
+// launch (hanzo-ml src/vulkan_backend.rs: quantize_act_q8 once per decode step,
+// then the dp4a matvec on its codes): every CTA quantizes the f32 x into its
+// own shared memory exactly as quantize_act_q8 does (same IEEE steps, so the
+// same codes and scales, bit for bit) while its first weight pieces are in
+// flight, and the lanes read their codes from there. Decode as Q8D.
+struct Q8DQ : Q8D {
+    static constexpr bool QPREP = true;
+
+    // Codes and scales from the CTA's shared tables (xq, xs point there).
+    __device__ __forceinline__ static void load_xq(X& x, const L& l, const int8_t* xq, const float* xs, int e0) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (j < l.nblk) {
+                const uint4 a = *reinterpret_cast<const uint4*>(xq + e0 + 32 * j);
+                const uint4 b = *reinterpret_cast<const uint4*>(xq + e0 + 32 * j + 16);
+                x.q[j][0] = a.x; x.q[j][1] = a.y; x.q[j][2] = a.z; x.q[j][3] = a.w;
+                x.q[j][4] = b.x; x.q[j][5] = b.y; x.q[j][6] = b.z; x.q[j][7] = b.w;
+                x.xs[j] = xs[(e0 >> 5) + j];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; i++) x.q[j][i] = 0;
+                x.xs[j] = 0.0f;
+            }
+        }
+    }
+};
+
+// Formats whose kernel quantizes the f32 activation itself (QPREP).
+template <class F, class = void>
+struct quantizes_x : std::false_type {};
+template <class F>
+struct quantizes_x<F, std::void_t<decltype(F::QPREP)>> : std::bool_constant<F::QPREP> {};
 
 }  // namespace qmv

@@ -10,7 +10,10 @@
 namespace qmvi {
 
 // qmv_q4k.cu
-int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s);
+// force_timeout (failure-path tests only): every CTA takes the path of a
+// staged copy that did not land in time.
+int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s,
+        int force_timeout = 0);
 int moe_q4k(const void* bank, const float* x, float* y, int rows, int k, const int32_t* ids, int slots,
             int n_experts, const qmv_opts* cfg, cudaStream_t s);
 int q4k_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_opts* cfg,
@@ -56,13 +59,15 @@ int moe_q8_0(const void* bank, const float* x, float* y, int rows, int k, const 
 int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows, int k, const qmv_opts* cfg,
             cudaStream_t s);
 int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s);
+int q8_dp4a_quant(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s);
 int quantize_act(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t s);
 int dequant_q8_0(const void* w, float* out, int rows, int k, cudaStream_t s);
 int selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t s);
 int status_q8(unsigned int* out, int clear);
 
 // qmm_q4k.cu, qmm_q6k.cu, qmm_q8_0.cu: the small-M batched product (m >= 2)
-int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s);
+int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s,
+            int force_timeout = 0);
 int qmm_q6k(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s);
 int qmm_q8_0(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg, cudaStream_t s);
 int status_qmm_q4k(unsigned int* out, int clear);

@@ -70,6 +70,7 @@ struct KParams {
     int aligned8;               // every unit starts 8-byte aligned in shared memory (Q8_0 dp4a)
     int CL;                     // CTAs per cluster sharing the activation prep (1: no cluster)
     int early_inputs;           // x / ids may be read before waiting for the previous kernel (only y waits)
+    int force_timeout;          // failure-path test: every first wait reports a copy that did not land
     uint32_t slot_stride;
     LimbTables lt;              // activation limb tables (f32-activation formats)
     uint32_t off_red;           // parked slice sums [rows of the CTA][W]
@@ -236,6 +237,13 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
             prep_limbs<2>(xrow, p.k, smem, p.lt, tid, static_cast<int>(blockDim.x), p.CL, cluster_rank());
         else
             prep_limbs_cta<4>(xrow, p.k, smem, p.lt, tid, static_cast<int>(blockDim.x));
+    } else if constexpr (quantizes_x<F>::value) {
+        // the dp4a codes of x, quantized by this CTA into its own tables
+        int8_t* tq = reinterpret_cast<int8_t*>(smem + p.lt.la);
+        float* ts = reinterpret_cast<float*>(smem + p.lt.xs);
+        quantize_x_cta(xrow, p.k, tq, ts, tid, static_cast<int>(blockDim.x));
+        xqrow = tq;
+        xqsrow = ts;
     }
     if (p.CL > 1)
         cluster_sync();   // every CTA's limb tables complete; barriers and counters initialized
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         int s = 0;
         uint32_t par = 0;
         for (int pc = 0; pc < npc; pc++) {
-            const bool landed = __all_sync(FULL, mbar_wait_bounded(bars + 8u * s, par));
+            const bool landed = !p.force_timeout && __all_sync(FULL, mbar_wait_bounded(bars + 8u * s, par));
             if (!landed) {
                 if (lane == 0) {
                     atomicOr(&g_status, STATUS_WAIT_TIMEOUT);
@@ -368,11 +376,17 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
     __syncthreads();
     if (*timeout) {
         // A copy did not land in time: give every copy this group still has in
-        // flight a bounded chance to land before the shared memory is released.
+        // flight a bounded chance to land before the shared memory is released,
+        // and mark every output of the CTA NaN (as an unroutable MoE slot is),
+        // so that no caller reads a stale y as a result.
         if (working && ks == 0 && lane == 0) {
             const int n = *issued;
             for (int pc = n - p.S > 0 ? n - p.S : 0; pc < n; pc++)
                 if (!mbar_wait_bounded(bars + 8u * (pc % p.S), static_cast<uint32_t>((pc / p.S) & 1))) break;
+        }
+        if constexpr (MODE == MODE_MATVEC) {
+            pdl_dependency_wait();
+            for (int r = tid; r < nrows; r += blockDim.x) p.y[yoff + R0 + r] = __int_as_float(0x7fc00000);
         }
         return;
     }

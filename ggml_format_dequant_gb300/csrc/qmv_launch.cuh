@@ -213,6 +213,10 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
         kp->lt.lc = static_cast<uint32_t>(off); off = round_up(off + k, 128);
         kp->lt.xs = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 32), 128);
         kp->lt.xsum16 = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 16), 128);
+    } else if (quantizes_x<F>::value) {
+        // the CTA's own codes (k bytes) and scales (k/32 floats) of x
+        kp->lt.la = static_cast<uint32_t>(off); off = round_up(off + k, 128);
+        kp->lt.xs = static_cast<uint32_t>(off); off = round_up(off + 4LL * (k / 32), 128);
     }
     kp->off_red = static_cast<uint32_t>(off);
     off = round_up(off + 4LL * rpc * W, 128);   // W == 0: nothing parked
@@ -313,54 +317,48 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
     return QMV_OK;
 }
 
-// Launch plan of format F. Independent calls (QMV_OVERLAP_INDEPENDENT) overlap best when one call takes as few CTAs as
-// still hold their whole share in half an SM (but at least half the SMs'
-// worth): more calls are then in flight at once (measured on GB300: MoE Q4_K
-// E128 n768 k2048 with 8 slots 2.32 -> 1.59 us a call, Q4_K 4096 x 4096
-// 2.43 -> 2.18 us, Q4_K dp4a 4096 x 4096 2.25 -> ~1.76 us). Chained and plain
-// calls, and shapes whose share does not fit, use every SM.
+// Independent calls (QMV_OVERLAP_INDEPENDENT): CTAs per call, as a divisor of
+// the SM count (the CTAs of an MoE call are shared by its slots).
+constexpr int INDEP_SM_DIV = 4;
+
+// Launch plan of format F. Independent calls (QMV_OVERLAP_INDEPENDENT) take a
+// few CTAs (about a quarter of the SM count) of at most WARPS_TWO_PER_SM
+// warps in half an SM's shared memory, each streaming a long share of the
+// rows through a two-slot ring of the largest pieces that fit: with two CTAs
+// an SM, many calls are then in flight at once (eight for the Q4_K 4096 x
+// 4096 matvec), and a CTA's fixed costs (start-up, activation prep, the wait
+// before it writes y) are spread over many rows. Measured on GB300, us a call
+// in a stream of 256 independent calls (and of 20): Q4_K 4096 x 4096 with
+// 103 whole-share CTAs 2.12 (2.61), 40 ring CTAs 1.71 (2.37), 16 ring CTAs
+// 1.66 (2.82); Q6_K 4096 x 14336 with 152 CTAs 10.03 (10.7), 38 CTAs 8.65
+// (9.78). Fewer CTAs stream faster in long streams but leave a longer tail in
+// short ones. Chained and plain calls, and forced plans, keep the default
+// plan (every SM).
 template <class F>
 inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_opts* cfg, KParams* kp, Plan* pl) {
     const int rc = make_plan_core<F>(di, rows, k, slots, cfg, kp, pl);
-    if (rc || overlap_of(cfg) != QMV_OVERLAP_INDEPENDENT || cfg->ctas > 0) return rc;
+    if (rc || overlap_of(cfg) != QMV_OVERLAP_INDEPENDENT) return rc;
+    if (cfg->ctas > 0 || cfg->chunk_rows > 0 || cfg->chunks > 0 || cfg->warps > 0 || cfg->unroll > 0 ||
+        cfg->cluster > 0)
+        return rc;   // a forced plan stays as forced
     const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;
     const int per = slots > 1 ? slots : 1;
-    // From half the SMs up (with two CTAs an SM, four calls in flight), the
-    // fewest CTAs whose whole share fits in half an SM.
-    const int start = std::max(1, di.nsm / (2 * per));
-    if (start >= pl->parts) return rc;   // small shapes: already fewer CTAs
+    const int want = std::max(1, (di.nsm / INDEP_SM_DIV + per - 1) / per);
+    if (want >= pl->parts) return rc;   // small shapes: already few CTAs
     qmv_opts c = *cfg;
-    // (a share that needs a ring at every-SM CTAs needs one at fewer CTAs too)
-    for (int parts = start; kp->S == 1 && parts < pl->parts; parts++) {
-        c.ctas = parts;
+    c.ctas = want;
+    c.warps = WARPS_TWO_PER_SM;
+    c.chunks = 2;
+    // the largest pieces (up to 8 rows) whose two-slot rings fit half an SM
+    for (int cr = 8; cr >= 1; cr--) {
+        c.chunk_rows = cr;
         KParams k2 = *kp;
         Plan p2;
-        if (make_plan_core<F>(di, rows, k, slots, &c, &k2, &p2)) continue;
-        const int rpc = k2.rq + (k2.rrem ? 1 : 0);
-        if (k2.S == 1 && k2.CR * k2.NG >= rpc && static_cast<long long>(p2.smem) <= half &&
-            p2.T <= 32 * WARPS_TWO_PER_SM) {
-            *kp = k2;
-            *pl = p2;
-            return QMV_OK;
-        }
-    }
-    // A share too large for half an SM: for the f32-activation formats, CTAs
-    // of at most WARPS_TWO_PER_SM warps (one row group) in half an SM's shared
-    // memory, streaming two-row pieces through two ring slots, so that the
-    // next call's CTA runs its start-up (copies, activation prep) beside this
-    // one's decode instead of after it (measured on GB300, Q6_K 4096 x 14336:
-    // 11.76 -> 10.25 us a call; the same plan is slower for chained and plain
-    // calls, where only one of the two CTAs on an SM can decode).
-    if (F::LIMBS && kp->S > 1) {
-        qmv_opts c = *cfg;
-        c.warps = WARPS_TWO_PER_SM;
-        c.ctas = per > 1 ? (di.nsm + per - 1) / per : di.nsm;
-        c.chunk_rows = 2;
-        c.chunks = 2;
-        KParams k2 = *kp;
-        Plan p2;
-        if (!make_plan_core<F>(di, rows, k, slots, &c, &k2, &p2, half) && k2.NG == 1 && k2.S == 2 &&
-            static_cast<long long>(p2.smem) <= half && p2.T <= 32 * WARPS_TWO_PER_SM) {
+        if (make_plan_core<F>(di, rows, k, slots, &c, &k2, &p2, half)) continue;
+        // two slots (unless a row group has a single piece), so that a
+        // piece is decoded while the next one lands
+        const int most = std::max(k2.npc4[2], k2.npc4[3]);
+        if (static_cast<long long>(p2.smem) <= half && p2.T <= 32 * WARPS_TWO_PER_SM && k2.S >= std::min(2, most)) {
             *kp = k2;
             *pl = p2;
             return QMV_OK;
@@ -419,16 +417,30 @@ inline int launch(const KParams& kp, const Plan& pl, int slots, cudaStream_t str
                      : launch_one<F, 1, MOE, MODE, false>(kp, pl, slots, stream);
 }
 
-// Read (and optionally clear) this translation unit's device status word.
+// Snapshot of this translation unit's status word, taken by status_xchg.
+static __device__ unsigned int g_status_snap;
+
+// One thread: read the status word (and clear it, in the same atomic
+// exchange) into g_status_snap.
+static __global__ void status_xchg(int clear) {
+    g_status_snap = clear ? atomicExch(&g_status, 0u) : atomicOr(&g_status, 0u);
+}
+
+// Read (and optionally clear) this translation unit's device status word:
+// wait for all work on the device, then read and clear it in one atomic
+// exchange, so that no bit raised by a kernel of another host thread is lost
+// between the read and the clear. Calls are serialised by a lock.
 inline int status_rw(unsigned int* out, int clear) {
-    unsigned int v = 0;
-    int rc = cuda_rc(cudaMemcpyFromSymbol(&v, g_status, sizeof(v)));
+    static std::mutex mu;
+    std::lock_guard<std::mutex> g(mu);
+    int rc = cuda_rc(cudaDeviceSynchronize());
     if (rc) return rc;
-    if (clear) {
-        const unsigned int z = 0;
-        rc = cuda_rc(cudaMemcpyToSymbol(g_status, &z, sizeof(z)));
-        if (rc) return rc;
-    }
+    status_xchg<<<1, 1>>>(clear);
+    rc = cuda_rc(cudaGetLastError());
+    if (rc) return rc;
+    unsigned int v = 0;
+    rc = cuda_rc(cudaMemcpyFromSymbol(&v, g_status_snap, sizeof(v)));   // after the kernel (same stream)
+    if (rc) return rc;
     *out = v;
     return QMV_OK;
 }

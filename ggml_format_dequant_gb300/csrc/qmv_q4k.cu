@@ -46,8 +46,10 @@ namespace qmvi {
 
 using namespace qmv;
 
-int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s) {
+int q4k(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s,
+        int force_timeout) {
     KParams kp{};
+    kp.force_timeout = force_timeout;
     kp.w = static_cast<const uint8_t*>(w);
     kp.x = x;
     kp.y = y;

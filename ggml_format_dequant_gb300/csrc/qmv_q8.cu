@@ -116,6 +116,16 @@ int q8_dp4a(const void* w, const int8_t* xq, const float* xs, float* y, int rows
     return launch<Q8D, false, MODE_MATVEC>(kp, pl, 1, s);
 }
 
+int q8_dp4a_quant(const void* w, const float* x, float* y, int rows, int k, const qmv_opts* cfg, cudaStream_t s) {
+    KParams kp = q8_params(w, rows, k);
+    kp.x = x;
+    kp.y = y;
+    Plan pl;
+    int rc = make_plan<Q8DQ>(rows, k, 1, cfg, &kp, &pl);
+    if (rc) return rc;
+    return launch<Q8DQ, false, MODE_MATVEC>(kp, pl, 1, s);
+}
+
 int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k, cudaStream_t s) {
     KParams kp = q8_params(w, rows, k);
     kp.xq = xq;

@@ -176,6 +176,17 @@ int quantize_act_q8(const float *x, int8_t *xq, float *xs, float *xsum, int m, i
 int qmv_q8_dp4a(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
                 cudaStream_t stream);
 
+/* quantize_act_q8 and qmv_q8_dp4a in one launch: y = the Q8_0 dp4a matvec of
+ * x quantized exactly as quantize_act_q8 quantizes it (the same codes and
+ * scales, bit for bit; every CTA quantizes x into its own shared memory while
+ * its first weight pieces are in flight, so the quantization costs no
+ * separate launch and no trip of the codes through global memory). w as for
+ * qmv_q8_0; x: f32 [k], 16-byte aligned; y: f32 [rows]; k % 32 == 0.
+ * Numerics and results as quantize_act_q8 followed by qmv_q8_dp4a.
+ * Cites hanzo-ml src/vulkan_backend.rs, quantize_act_q8 (quantize once per
+ * decode step) and hanzo-kernel src/main.rs, check_dp4a. */
+int qmv_q8_dp4a_quant(const void *w, const float *x, float *y, int rows, int k, cudaStream_t stream);
+
 /* dp4a matvec of Q4_K weights with a quantized activation (the pages' dense
  * dp4a Q4_K decode): y[r] = sum_t xs[t] * (d*sc_t * dot[r, t] - dmin*m_t *
  * sumq[t]) in f32, over the 32-weight sub-blocks t of row r, where dot[r, t]
@@ -265,7 +276,8 @@ const char *qmv_last_cuda_error(void);
  * seen on the host without a synchronization.
  */
 #define QMV_STATUS_BAD_EXPERT_ID 1u /* an MoE id was outside [0, n_experts) */
-#define QMV_STATUS_WAIT_TIMEOUT 2u  /* a staged weight copy did not land in time */
+#define QMV_STATUS_WAIT_TIMEOUT 2u  /* a staged weight copy did not land in time (the
+                                     * CTA's outputs are then NaN) */
 
 /* Failure-path self-test: launches one thread that waits, through the same
  * bounded wait every staged copy goes through, on a barrier nothing arrives
@@ -274,9 +286,20 @@ const char *qmv_last_cuda_error(void);
  * would. Nothing hangs or traps; the context stays usable. */
 int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
 
+/* Failure-path self-test of the product kernels: runs qmv_q4k (m == 1) or
+ * qmm_q4k (m = 2..8) on real Q4_K rows with every CTA taking the path of a
+ * staged weight copy that did not land in time: the CTA raises
+ * QMV_STATUS_WAIT_TIMEOUT, lets the copies it issued land (bounded), writes
+ * NaN to all of its outputs and returns. Arguments as for qmv_q4k / qmm_q4k.
+ * Nothing hangs or traps; the context stays usable. */
+int qmv_selftest_timeout_path(const void *w, const float *x, float *y, int rows, int k, int m,
+                              cudaStream_t stream);
+
 /* OR of the status bits raised on the current device since the last clear;
- * clears them when `clear` is non-zero. Synchronizes with the device (it reads
- * device memory through the legacy stream). */
+ * clears them when `clear` is non-zero. Waits for all work on the current
+ * device (cudaDeviceSynchronize), then reads the word and clears it in one
+ * atomic exchange, so that a bit raised by a kernel launched concurrently
+ * from another host thread is either returned or kept, never lost. */
 int qmv_device_status(unsigned int *status, int clear);
 
 /* ----------------------------------------------------------------------
@@ -293,6 +316,8 @@ int qmv_q8_0_ex(const void *w, const float *x, float *y, int rows, int k, const 
                  cudaStream_t stream);
 int qmv_q8_dp4a_ex(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
                     const qmv_opts *opts, cudaStream_t stream);
+int qmv_q8_dp4a_quant_ex(const void *w, const float *x, float *y, int rows, int k, const qmv_opts *opts,
+                         cudaStream_t stream);
 int qmv_q4k_dp4a_ex(const void *w, const int8_t *xq, const float *xs, float *y, int rows, int k,
                      const qmv_opts *opts, cudaStream_t stream);
 int moe_qmv_q6k_ex(const void *w_bank, const float *x, float *y, int rows, int k,
@@ -365,7 +390,8 @@ int qmv_q6k_dp4a_blockdots(const void *w, const int8_t *xq, int32_t *dots, int r
  * fmt: 0 = Q4_K, 1 = Q6_K, 2 = Q8_0 (f32 x), 3 = Q8_0 dp4a, 4 = MoE Q4_K,
  * 5 = Q4_K dp4a, 6 = MoE Q6_K, 7 = MoE Q4_K dp4a, 8 = Q5_K, 9 = Q4_0,
  * 10 = MoE Q8_0, 11 = MoE Q4_0, 12 = MoE Q5_K, 16 = Q6_K dp4a, 17 = MoE Q6_K
- * dp4a. 13, 14 and 15 are not plans (QMV_EINVAL): batches of two or more rows
+ * dp4a, 18 = Q8_0 dp4a with the quantization in the kernel
+ * (qmv_q8_dp4a_quant). 13, 14 and 15 are not plans (QMV_EINVAL): batches of two or more rows
  * of x run on the tensor cores (qmm_tc_plan_detail). */
 int qmv_plan_info(int fmt, int rows, int k, int slots, const qmv_opts *opts, int *threads, int *ctas,
                   int *chunk_rows, int *chunks, int *smem_bytes);

@@ -28,7 +28,7 @@ import pytest
 DEVICE = (152, 232448, 233472, 1024)
 FMT_ID = {"q4k": 0, "q6k": 1, "q8_0": 2, "q8d": 3, "moe": 4, "q4d": 5, "moe6": 6, "moe4d": 7, "q5k": 8,
           "q4_0": 9, "moe8": 10, "moe40": 11, "moe5": 12,
-          "q6d": 16, "moe6d": 17}
+          "q6d": 16, "moe6d": 17, "q8dq": 18}
 
 
 # Per format: weights per block, bytes per block, blocks per warp slice,
@@ -51,7 +51,7 @@ def fmt_info(fmt, m=1):
     if fmt in ("q8_0", "moe8"):
         return dict(qk=32, bb=34, sb=32, units=lambda nb: nb, ubyte=lambda u: u * 34,
                     extent=lambda a: (a - (a & 3), a - (a & 3) + 40), align=2)
-    if fmt == "q8d":
+    if fmt in ("q8d", "q8dq"):
         # aligned path: [a, a + 136); block-by-block path: up to a + 142
         return dict(qk=32, bb=34, sb=128, units=lambda nb: (nb + 3) // 4, ubyte=lambda u: u * 136,
                     extent=lambda a: (a - (a & 3), a - (a & 3) + 144), align=2)
@@ -86,17 +86,20 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
     CL = P["CL"]
     assert CL in (1, 2, 4, 8) and parts % CL == 0 and (k // 16) % (2 * CL) == 0
     assert P["rq"] >= 1
-    if fmt in ("q8d", "q4d", "moe4d", "q6d", "moe6d"):
+    if fmt in ("q8d", "q4d", "moe4d", "q6d", "moe6d", "q8dq"):
         assert CL == 1
     lg = GS.bit_length() - 1
     rpw = 32 >> lg
     aligned8 = P["aligned8"] == 1
-    if fmt == "q8d":
+    if fmt in ("q8d", "q8dq"):
         assert aligned8 == (rowbytes % 8 == 0)
 
     # shared-memory layout: disjoint, ordered regions inside the device limit
     regions = []
-    if fmt not in ("q8d", "q4d", "moe4d", "q6d", "moe6d"):
+    if fmt == "q8dq":
+        # the CTA's own codes and scales of x
+        regions += [(P["off_la"], k), (P["off_xs"], 4 * (k // 32))]
+    elif fmt not in ("q8d", "q4d", "moe4d", "q6d", "moe6d"):
         regions += [(P["off_la"], k), (P["off_lb"], k), (P["off_lc"], k), (P["off_xs"], 4 * (k // 32)),
                     (P["off_xsum16"], 4 * (k // 16))]
         for o, _ in regions:
@@ -156,7 +159,7 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
                                 lo, hi = f["extent"](int(ai))
                                 assert 0 <= lo and hi <= stride, (ai, lo, hi, stride)
                                 assert ai % f["align"] == 0
-                                if fmt == "q8d" and aligned8:
+                                if fmt in ("q8d", "q8dq") and aligned8:
                                     assert ai % 8 == 0
                             sel = valid & has
                             np.add.at(covered, (R0 + rl0 + j[sel], ug[sel]), 1)
@@ -168,7 +171,8 @@ def replay(q, fmt, rows, k, slots=1, cfg=None, mode=0):
     return P
 
 
-WORKLOADS = [("q4k", 4096, 4096, 1), ("q4k", 256, 1024, 1), ("q8d", 14336, 4096, 1), ("q6k", 4096, 14336, 1),
+WORKLOADS = [("q4k", 4096, 4096, 1), ("q4k", 256, 1024, 1), ("q8d", 14336, 4096, 1), ("q8dq", 14336, 4096, 1),
+             ("q6k", 4096, 14336, 1),
              ("moe", 768, 2048, 8), ("q4d", 4096, 4096, 1), ("moe6", 2048, 768, 8), ("moe4d", 768, 2048, 8),
              ("q5k", 4096, 4096, 1), ("q4_0", 4096, 4096, 1), ("moe8", 768, 2048, 8), ("moe40", 768, 2048, 8),
              ("moe5", 768, 2048, 8), ("q6d", 4096, 14336, 1), ("moe6d", 2048, 768, 8)]
@@ -245,21 +249,24 @@ def test_retired_batch_plan_ids(q):
 
 @pytest.mark.parametrize("fmt,rows,k,slots", WORKLOADS)
 def test_independent_call_plans(q, fmt, rows, k, slots):
-    """Independent calls: the whole-share workloads take about two thirds of
-    the SMs with CTAs that still fit in half an SM; the f32-activation
-    workloads whose share does not fit take one half-SM CTA an SM, streaming
-    two-row pieces through two ring slots; every index is replayed as for the
-    default plans."""
+    """Independent calls: a quarter of the SM count in CTAs (shared by the
+    slots of an MoE call) of at most 8 warps, in half an SM's shared memory,
+    each streaming its share of the rows through two ring slots (one when a
+    row group has a single piece); every index is replayed as for the default
+    plans."""
     P = replay(q, fmt, rows, k, slots, mode=2)
     per = max(slots, 1)
     half = (DEVICE[2] - 2 * DEVICE[3]) // 2
-    if (fmt, rows) in (("q4k", 4096), ("moe", 768), ("q4d", 4096), ("moe4d", 768)):
-        assert DEVICE[0] // (2 * per) <= P["ctas"] < -(-DEVICE[0] // per)
-        assert P["S"] == 1 and P["smem"] <= half and P["threads"] <= 256
-    if (fmt, rows) in (("q8d", 14336), ("q6k", 4096)):
-        assert P["ctas"] == DEVICE[0]
-    if (fmt, rows) == ("q6k", 4096):
-        assert P["NG"] == 1 and P["S"] == 2 and P["CR"] == 2 and P["smem"] <= half and P["threads"] <= 256
+    want = max(1, -(-(DEVICE[0] // 4) // per))
+    default = q.qmv_plan_detail(FMT_ID[fmt], rows, k, slots, None, DEVICE)
+    if want < default["ctas"]:
+        assert P["ctas"] == want
+        assert P["smem"] <= half and P["threads"] <= 256
+        gmax = P["gq1"] + (1 if P["grem1"] else 0)
+        assert P["S"] == min(2, -(-gmax // P["CR"]))
+    else:   # small shapes keep the default CTAs and pieces (y then parked until the wait)
+        assert (P["ctas"], P["CR"], P["S"], P["W"]) == (default["ctas"], default["CR"], default["S"],
+                                                          max(default["W"], 1))
 
 
 def test_chain_shapes(q):
