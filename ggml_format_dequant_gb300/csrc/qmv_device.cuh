@@ -354,41 +354,60 @@ __device__ __forceinline__ void prep_limbs_cta(const float* __restrict__ x, int 
     }
 }
 
-// The activation quantization of the dp4a path, done by a CTA into its own
-// shared memory: one warp per 32-element block (four blocks a round, loads
-// first), amax = max|x| (a warp max of the |x| bit patterns, ordered like the
-// magnitudes for finite values), inv = 127/amax and d = amax/127 as IEEE f32
-// divides, q = clamp(round_half_even(x * inv), -127, 127) with one f32
-// multiply; amax == 0 gives d = 0 and q = 0. The same steps as the standalone
-// quantizer, so the codes and scales are the same bit for bit. xq: k bytes,
-// xs: k/32 floats; the caller publishes them with a block barrier.
+// The activation quantization of the dp4a path for one 32-element block,
+// by one thread: amax = max|x| (exact in any order), inv = 127/amax and
+// d = amax/127 as IEEE f32 divides, q = clamp(round_half_even(x * inv),
+// -127, 127) with one f32 multiply; amax == 0 gives d = 0 and every q = 0.
+// v: the block's 32 values; codes: the 32 int8 codes, four to a word (byte
+// i of word j is code 4j + i). Returns d; sum receives the integer sum of
+// the codes.
+__device__ __forceinline__ float quantize_block_q8(const float4 (&v)[8], uint32_t (&codes)[8], int& sum) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+    float d = 0.0f, inv = 0.0f;
+    if (amax != 0.0f) {
+        inv = __fdiv_rn(127.0f, amax);
+        d = __fdiv_rn(amax, 127.0f);
+    }
+    int s = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        uint32_t w = 0;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            int q = __float2int_rn(__fmul_rn(e[i], inv));
+            q = q > 127 ? 127 : (q < -127 ? -127 : q);
+            s += q;
+            w |= (static_cast<uint32_t>(q) & 0xffu) << (8 * i);
+        }
+        codes[j] = w;
+    }
+    sum = s;
+    return d;
+}
+
+// The activation quantization done by a CTA into its own shared memory: one
+// thread per 32-element block (all of a thread's loads first), the steps of
+// quantize_block_q8, so the codes and scales equal the standalone
+// quantizer's bit for bit. xq: k bytes (16-byte aligned), xs: k/32 floats;
+// the caller publishes them with a block barrier.
 __device__ __forceinline__ void quantize_x_cta(const float* __restrict__ x, int k, int8_t* xq, float* xs, int tid,
                                                int T) {
-    const int lane = tid & 31, warp = tid >> 5, nw = T >> 5;
     const int nblk = k >> 5;
-    for (int b0 = warp; b0 < nblk; b0 += 4 * nw) {
-        float v[4];
+    for (int b = tid; b < nblk; b += T) {
+        const float4* src = reinterpret_cast<const float4*>(x + 32 * b);
+        float4 v[8];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int b = b0 + j * nw;
-            v[j] = b < nblk ? __ldg(x + 32 * b + lane) : 0.0f;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int b = b0 + j * nw;
-            if (b >= nblk) break;   // uniform across the warp
-            const float amax = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(v[j]) & 0x7fffffffu));
-            int q = 0;
-            float d = 0.0f;
-            if (amax != 0.0f) {
-                const float inv = __fdiv_rn(127.0f, amax);
-                q = __float2int_rn(__fmul_rn(v[j], inv));
-                q = q > 127 ? 127 : (q < -127 ? -127 : q);
-                d = __fdiv_rn(amax, 127.0f);
-            }
-            xq[32 * b + lane] = static_cast<int8_t>(q);
-            if (lane == 0) xs[b] = d;
-        }
+        for (int j = 0; j < 8; j++) v[j] = __ldg(src + j);
+        uint32_t codes[8];
+        int sum;
+        xs[b] = quantize_block_q8(v, codes, sum);
+        uint4* dst = reinterpret_cast<uint4*>(xq + 32 * b);
+        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
     }
 }
 

@@ -7,31 +7,44 @@ namespace {
 
 using namespace qmv;
 
-// One warp per 32-element block of x: amax by a warp max over |x| bit
-// patterns (ordered like the magnitudes for finite values), then the IEEE f32
-// divide / multiply / round-half-even steps of the quantizer.
+// One thread per 32-element block of x (quantize_block_q8: the IEEE f32
+// divide / multiply / round-half-even steps of the quantizer). With x and xq
+// 16-byte aligned (VEC) a block's 128 bytes of x are read as eight 16-byte
+// loads and its 32 codes written as two; otherwise element by element. xsum
+// is d times the integer sum of the codes, one f32 multiply. The kernel lets
+// a dependent launch after it start at once (that launch still waits for
+// this kernel before it reads what this one wrote).
+template <bool VEC>
 __global__ void quantize_act_q8_kernel(const float* __restrict__ x, int8_t* __restrict__ xq,
                                        float* __restrict__ xs, float* __restrict__ xsum, long long nblocks) {
-    const int lane = threadIdx.x & 31;
-    const long long wid = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
-    const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    for (long long b = wid; b < nblocks; b += nw) {
-        const float v = x[b * 32 + lane];
-        const float amax = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(v) & 0x7fffffffu));
-        int q = 0;
-        float d = 0.0f;
-        if (amax != 0.0f) {
-            const float inv = __fdiv_rn(127.0f, amax);
-            q = __float2int_rn(__fmul_rn(v, inv));
-            q = q > 127 ? 127 : (q < -127 ? -127 : q);
-            d = __fdiv_rn(amax, 127.0f);
+    pdl_launch_dependents();
+    for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nblocks;
+         b += static_cast<long long>(gridDim.x) * blockDim.x) {
+        float4 v[8];
+        if constexpr (VEC) {
+            const float4* src = reinterpret_cast<const float4*>(x + 32 * b);
+#pragma unroll
+            for (int j = 0; j < 8; j++) v[j] = __ldg(src + j);
+        } else {
+            const float* src = x + 32 * b;
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                v[j] = make_float4(__ldg(src + 4 * j), __ldg(src + 4 * j + 1), __ldg(src + 4 * j + 2),
+                                   __ldg(src + 4 * j + 3));
         }
-        xq[b * 32 + lane] = static_cast<int8_t>(q);
-        const int sum = __reduce_add_sync(FULL, q);
-        if (lane == 0) {
-            xs[b] = d;
-            if (xsum) xsum[b] = __fmul_rn(d, __int2float_rn(sum));
+        uint32_t codes[8];
+        int sum;
+        const float d = quantize_block_q8(v, codes, sum);
+        if constexpr (VEC) {
+            uint4* dst = reinterpret_cast<uint4*>(xq + 32 * b);
+            dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; i++) xq[32 * b + i] = static_cast<int8_t>((codes[i >> 2] >> (8 * (i & 3))) & 0xffu);
         }
+        xs[b] = d;
+        if (xsum) xsum[b] = __fmul_rn(d, __int2float_rn(sum));
     }
 }
 
@@ -138,7 +151,11 @@ int q8_blockdots(const void* w, const int8_t* xq, int32_t* dots, int rows, int k
 
 int quantize_act(const float* x, int8_t* xq, float* xs, float* xsum, int m, int k, cudaStream_t s) {
     const long long nblocks = static_cast<long long>(m) * (k / 32);
-    quantize_act_q8_kernel<<<grid_for(nblocks * 32, 256), 256, 0, s>>>(x, xq, xs, xsum, nblocks);
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xq)) & 15u) == 0;
+    if (vec)
+        quantize_act_q8_kernel<true><<<grid_for(nblocks, 64), 64, 0, s>>>(x, xq, xs, xsum, nblocks);
+    else
+        quantize_act_q8_kernel<false><<<grid_for(nblocks, 64), 64, 0, s>>>(x, xq, xs, xsum, nblocks);
     return cuda_rc(cudaGetLastError());
 }
 

@@ -119,3 +119,24 @@ def test_fused_full_c2(q):
     ref = oracle.qmv_q8_dp4a(c["w"], oq.reshape(-1), os_.reshape(-1), rows, k)
     assert scale_rel(ref, yf.cpu().numpy()) <= SCALE_REL_TOL
     assert q.qmv_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("xoff,qoff", [(0, 0), (1, 0), (0, 3), (3, 5)])
+def test_quantizer_alignments(q, xoff, qoff):
+    """quantize_act_q8 with x and xq at 4-byte / 1-byte offsets from a
+    16-byte boundary (the element-wise path) and aligned (the vector path):
+    codes, scales and sums equal the oracle's bit for bit."""
+    m, k = 3, 1024
+    st = synth.Stream(31 + xoff + 7 * qoff)
+    x = synth.gen_normal(st, m * k).astype(np.float32)
+    xbuf = torch.zeros(m * k + 8, dtype=torch.float32, device="cuda")
+    xbuf[xoff:xoff + m * k] = torch.from_numpy(x).cuda()
+    qbuf = torch.zeros(m * k + 32, dtype=torch.int8, device="cuda")
+    xs = torch.empty(m * k // 32, dtype=torch.float32, device="cuda")
+    xsum = torch.empty(m * k // 32, dtype=torch.float32, device="cuda")
+    q.quantize_act_q8(xbuf.data_ptr() + 4 * xoff, qbuf.data_ptr() + qoff, xs, xsum, m, k)
+    torch.cuda.synchronize()
+    oq, os_, osum = oracle.quantize_act_q8(x, m, k)
+    assert np.array_equal(qbuf.cpu().numpy()[qoff:qoff + m * k], oq.reshape(-1))
+    assert np.array_equal(xs.cpu().numpy(), os_.reshape(-1))
+    assert np.array_equal(xsum.cpu().numpy(), osum.reshape(-1))
