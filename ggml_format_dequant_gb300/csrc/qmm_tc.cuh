@@ -945,6 +945,8 @@ inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qm
 // Warps a CTA of independent calls takes at most: 256 threads of 128
 // registers fill half an SM's register file.
 constexpr int TC_WARPS_HALF_SM = 8;
+// Rows of a ring piece in the streaming plan of independent calls.
+constexpr int TC_RING_ROWS = 32;
 
 // The plan used. Independent calls (QMV_OVERLAP_INDEPENDENT) take
 // CTAs of at most TC_WARPS_HALF_SM warps in at most half an SM's shared
@@ -955,7 +957,32 @@ constexpr int TC_WARPS_HALF_SM = 8;
 // shapes whose plan does not fit use whole CTAs.
 template <class F>
 inline int make_tc_plan_for(const DevInfo& di, int rows, int k, int m, const qmv_opts* cfg, TParams* tp, Plan* pl) {
-    if (overlap_of(cfg) == QMV_OVERLAP_INDEPENDENT && cfg->warps <= 0) {
+    const bool forced = cfg && (cfg->ctas > 0 || cfg->chunk_rows > 0 || cfg->chunks > 0 || cfg->warps > 0);
+    if (overlap_of(cfg) == QMV_OVERLAP_INDEPENDENT && !forced && rows >= 2 * TC_RING_ROWS * (di.nsm / 4)) {
+        // Independent calls of rows that fill a quarter of the SM count with
+        // at least two ring pieces each: that many CTAs of at most
+        // TC_WARPS_HALF_SM warps, streaming 32-row pieces through two ring
+        // slots in half an SM (the matvec's plan for independent calls).
+        // Measured on GB300, Q4_K 4096 x 4096, us a call: m = 2 5.04 -> 3.43,
+        // m = 8 5.89 -> 4.06 (Q6_K 4096 x 14336, m = 4, seven k-chunks of
+        // 8 slices: no gain, so rows of more than two k-chunks keep the plan
+        // below).
+        qmv_opts c = *cfg;
+        c.ctas = di.nsm / 4;
+        c.warps = TC_WARPS_HALF_SM;
+        c.chunk_rows = TC_RING_ROWS;
+        c.chunks = 2;
+        const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;
+        TParams t2 = *tp;
+        Plan p2;
+        if (!make_tc_plan_core<F>(di, rows, k, m, &c, half, &t2, &p2) && t2.nchunks <= 2 && t2.S == 2 &&
+            static_cast<long long>(p2.smem) <= half) {
+            *tp = t2;
+            *pl = p2;
+            return QMV_OK;
+        }
+    }
+    if (overlap_of(cfg) == QMV_OVERLAP_INDEPENDENT && !(cfg && cfg->warps > 0)) {
         qmv_opts c = *cfg;
         c.warps = TC_WARPS_HALF_SM;
         const long long half = (di.smem_sm - 2LL * di.smem_reserved) / 2;

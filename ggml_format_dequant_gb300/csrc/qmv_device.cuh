@@ -282,6 +282,43 @@ __device__ __forceinline__ void limb_words(uint32_t t0, uint32_t t1, uint32_t t2
     aw = (__byte_perm(a01, a23, 0x5410) + 0x60606060u) ^ 0x80808080u;
 }
 
+// Largest magnitude of 16 activations (four float4).
+__device__ __forceinline__ float max_abs16(const float4* v) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)), fmaxf(fabsf(v[m].z), fabsf(v[m].w))));
+    return mx;
+}
+
+// The power-of-two scale of a 32-element group from its largest magnitude
+// mx: p2s = 2^s puts the group maximum just below 2^21, p2ms = 2^-s.
+__device__ __forceinline__ void group_scale(float mx, float& p2s, float& p2ms) {
+    const int E = static_cast<int>(__float_as_uint(mx) >> 23);   // biased exponent of the group maximum
+    int s = LIMB_BITS - (E - 126);                               // max < 2^(E-126) for a normal maximum
+    s = s > 126 ? 126 : s;                                       // zero / tiny groups
+    p2s = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+    p2ms = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+}
+
+// Limb words of 16 consecutive activations (four float4) under the group
+// scale p2s: word m of each limb holds elements 4m .. 4m+3, one signed byte
+// each. Returns the exact integer sum of the 16 X.
+__device__ __forceinline__ int limbs16(const float4* v, float p2s, uint32_t* A, uint32_t* B, uint32_t* C) {
+    uint32_t tsum = 0;
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+        const uint32_t t0 = __float_as_uint(__fmaf_rn(v[m].x, p2s, LIMB_MAGIC));
+        const uint32_t t1 = __float_as_uint(__fmaf_rn(v[m].y, p2s, LIMB_MAGIC));
+        const uint32_t t2 = __float_as_uint(__fmaf_rn(v[m].z, p2s, LIMB_MAGIC));
+        const uint32_t t3 = __float_as_uint(__fmaf_rn(v[m].w, p2s, LIMB_MAGIC));
+        limb_words(t0, t1, t2, t3, A[m], B[m], C[m]);
+        tsum += t0 + t1 + t2 + t3;
+    }
+    // sum of the 16 X: sum of the patterns minus 16 magic patterns (mod 2^32)
+    return static_cast<int>(tsum - 16u * LIMB_MAGIC_BITS);
+}
+
 // Limb words, sum and scale of one 16-element half (elements 16h .. 16h+15)
 // held as four float4 by this thread; its partner lane (lane ^ 1) holds the
 // other half of the 32-element group and calls this at the same time (the
@@ -290,32 +327,12 @@ __device__ __forceinline__ void limb_words(uint32_t t0, uint32_t t1, uint32_t t2
 // (even h) the group's scale into the CTA's own tables when `store` is set.
 __device__ __forceinline__ void prep_half(const float4 (&v)[4], uint32_t h, bool store, uint8_t* smem,
                                           const LimbTables& L) {
-    float mx = 0.0f;
-#pragma unroll
-    for (int m = 0; m < 4; m++)
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)), fmaxf(fabsf(v[m].z), fabsf(v[m].w))));
+    float mx = max_abs16(v);
     mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));    // the group's other half
-    const int E = static_cast<int>(__float_as_uint(mx) >> 23);   // biased exponent of the group maximum
-    int s = LIMB_BITS - (E - 126);                               // max < 2^(E-126) for a normal maximum
-    s = s > 126 ? 126 : s;                                       // zero / tiny groups
-    const float p2s = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
-    const float p2ms = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+    float p2s, p2ms;
+    group_scale(mx, p2s, p2ms);
     uint4 A, B, C;
-    uint32_t* Ap = &A.x;
-    uint32_t* Bp = &B.x;
-    uint32_t* Cp = &C.x;
-    uint32_t tsum = 0;
-#pragma unroll
-    for (int m = 0; m < 4; m++) {
-        const uint32_t t0 = __float_as_uint(__fmaf_rn(v[m].x, p2s, LIMB_MAGIC));
-        const uint32_t t1 = __float_as_uint(__fmaf_rn(v[m].y, p2s, LIMB_MAGIC));
-        const uint32_t t2 = __float_as_uint(__fmaf_rn(v[m].z, p2s, LIMB_MAGIC));
-        const uint32_t t3 = __float_as_uint(__fmaf_rn(v[m].w, p2s, LIMB_MAGIC));
-        limb_words(t0, t1, t2, t3, Ap[m], Bp[m], Cp[m]);
-        tsum += t0 + t1 + t2 + t3;
-    }
-    // sum of the 16 X: sum of the patterns minus 16 magic patterns (mod 2^32)
-    const int X = static_cast<int>(tsum - 16u * LIMB_MAGIC_BITS);
+    const int X = limbs16(v, p2s, &A.x, &B.x, &C.x);
     if (store) {
         const uint32_t o = limb_chunk(h) << 4;
         *reinterpret_cast<uint4*>(smem + L.la + o) = A;
