@@ -97,7 +97,6 @@ struct Q4K {
         x.nxsum1 = -(xsum16[(e0 >> 4) + 2] + xsum16[(e0 >> 4) + 3]);
     }
 
-
     // a: shared address of the super-block (16-byte aligned).
     __device__ __forceinline__ static float dot(uint32_t a, const L& l, const X& x, float r) {
         const uint4 h = lds128<0>(a);
@@ -598,7 +597,6 @@ struct Q8F {
         x.xs = reinterpret_cast<const float*>(smem + T.xs)[e0 >> 5];
     }
 
-
     // a: shared address of the 34-byte block (2-byte aligned).
     __device__ __forceinline__ static float dot(uint32_t a, const L&, const X& x, float r) {
         const uint32_t wa = a & ~3u;
@@ -668,7 +666,6 @@ struct Q40 {
         x.xs = reinterpret_cast<const float*>(smem + T.xs)[e0 >> 5];
         x.xsum = xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1];
     }
-
 
     // a: shared address of the 18-byte block (2-byte aligned).
     __device__ __forceinline__ static float dot(uint32_t a, const L&, const X& x, float r) {
