@@ -371,18 +371,13 @@ __device__ __forceinline__ void prep_limbs_cta(const float* __restrict__ x, int 
     }
 }
 
-// The activation quantization of the dp4a path for one 32-element block,
-// by one thread: amax = max|x| (exact in any order), inv = 127/amax and
-// d = amax/127 as IEEE f32 divides, q = clamp(round_half_even(x * inv),
+// The activation quantization of the dp4a path for 16 values of a 32-element
+// block whose largest magnitude is amax (exact in any order): inv = 127/amax
+// and d = amax/127 as IEEE f32 divides, q = clamp(round_half_even(x * inv),
 // -127, 127) with one f32 multiply; amax == 0 gives d = 0 and every q = 0.
-// v: the block's 32 values; codes: the 32 int8 codes, four to a word (byte
-// i of word j is code 4j + i). Returns d; sum receives the integer sum of
-// the codes.
-__device__ __forceinline__ float quantize_block_q8(const float4 (&v)[8], uint32_t (&codes)[8], int& sum) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; j++)
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+// codes: the 16 int8 codes, four to a word (byte i of word j is code 4j + i).
+// Returns d; sum receives the integer sum of the 16 codes.
+__device__ __forceinline__ float quantize_half_q8(const float4* v, float amax, uint32_t* codes, int& sum) {
     float d = 0.0f, inv = 0.0f;
     if (amax != 0.0f) {
         inv = __fdiv_rn(127.0f, amax);
@@ -390,7 +385,7 @@ __device__ __forceinline__ float quantize_block_q8(const float4 (&v)[8], uint32_
     }
     int s = 0;
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
+    for (int j = 0; j < 4; j++) {
         const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
         uint32_t w = 0;
 #pragma unroll
@@ -406,25 +401,42 @@ __device__ __forceinline__ float quantize_block_q8(const float4 (&v)[8], uint32_
     return d;
 }
 
-// The activation quantization done by a CTA into its own shared memory: one
-// thread per 32-element block (all of a thread's loads first), the steps of
-// quantize_block_q8, so the codes and scales equal the standalone
-// quantizer's bit for bit. xq: k bytes (16-byte aligned), xs: k/32 floats;
-// the caller publishes them with a block barrier.
+// The same for a whole 32-element block held by one thread (v: its 32
+// values; codes: 8 words). Returns d; sum receives the codes' integer sum.
+__device__ __forceinline__ float quantize_block_q8(const float4 (&v)[8], uint32_t (&codes)[8], int& sum) {
+    const float amax = fmaxf(max_abs16(v), max_abs16(v + 4));
+    int s0, s1;
+    const float d = quantize_half_q8(v, amax, codes, s0);
+    quantize_half_q8(v + 4, amax, codes + 4, s1);
+    sum = s0 + s1;
+    return d;
+}
+
+// The activation quantization done by a CTA into its own shared memory: two
+// threads per 32-element block (neighbouring lanes, 16 values each, one
+// shuffle for the block maximum; all lanes of a warp take part), the steps
+// of quantize_half_q8, so the codes and scales equal the standalone
+// quantizer's bit for bit. T even. xq: k bytes (16-byte aligned), xs: k/32
+// floats; the caller publishes them with a block barrier.
 __device__ __forceinline__ void quantize_x_cta(const float* __restrict__ x, int k, int8_t* xq, float* xs, int tid,
                                                int T) {
-    const int nblk = k >> 5;
-    for (int b = tid; b < nblk; b += T) {
-        const float4* src = reinterpret_cast<const float4*>(x + 32 * b);
-        float4 v[8];
+    const int nh = k >> 4;
+    const float4* __restrict__ x4 = reinterpret_cast<const float4*>(x);
+    for (int base = 0; base < nh; base += T) {
+        const int h = base + tid;
+        const bool valid = h < nh;
+        float4 v[4];
 #pragma unroll
-        for (int j = 0; j < 8; j++) v[j] = __ldg(src + j);
-        uint32_t codes[8];
+        for (int m = 0; m < 4; m++) v[m] = valid ? __ldg(x4 + 4 * h + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float amax = max_abs16(v);
+        amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, 1));   // the block's other half
+        uint32_t codes[4];
         int sum;
-        xs[b] = quantize_block_q8(v, codes, sum);
-        uint4* dst = reinterpret_cast<uint4*>(xq + 32 * b);
-        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        const float d = quantize_half_q8(v, amax, codes, sum);
+        if (valid) {
+            *reinterpret_cast<uint4*>(xq + 16 * h) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            if ((h & 1) == 0) xs[h >> 1] = d;
+        }
     }
 }
 

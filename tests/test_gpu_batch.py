@@ -227,3 +227,30 @@ def test_batch_kchunk_unit_rows_are_exact(q, fmt):
     y = run_qmm(q, fmt, w, x, rows, k, m, cfg=dict(warps=2))
     for i, j in enumerate(js):
         assert np.array_equal(y[i], W[:, j]), (i, j)
+
+
+@pytest.mark.parametrize("fmt,rows,k", [("q4k", 4096, 4096), ("q4_0", 2600, 2048), ("q5k", 2500, 4096)])
+@pytest.mark.parametrize("m", [2, 5, 8])
+def test_batch_independent_streaming_plan(q, fmt, rows, k, m):
+    """Independent calls of rows that fill a quarter of the SM count with two
+    32-row pieces each stream their share through two ring slots in a
+    quarter-SM-count of CTAs (Q4_K and Q4_0 here; the Q5_K rows' two slots do
+    not fit half an SM, so they keep the other plan): every row of y matches
+    the oracle and unit rows of x still give the weight columns bit for bit."""
+    P = q.qmm_tc_plan_detail({"q4k": 0, "q5k": 3, "q4_0": 4}[fmt], rows, k, m, overlap=q.OVERLAP_INDEPENDENT,
+                             device=q.GB300_DEVICE)
+    if fmt != "q5k":
+        assert P["ctas"] == q.GB300_DEVICE[0] // 4 and P["CR"] == 32 and P["S"] == 2
+    st = synth.Stream(rows + 3 * k + m)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    y = run_qmm(q, fmt, w, x, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
+    check_rows(oracle.qmm(fmt, w, x, m, rows, k), y)
+    js = [5, k - 1, 1000, 17, k // 2, 333, 64, 2047][:m]
+    xu = np.zeros((m, k), dtype=np.float32)
+    for i, j in enumerate(js):
+        xu[i, j] = 1.0
+    yu = run_qmm(q, fmt, w, xu, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
+    W = oracle.dequant(fmt, w, rows, k).astype(np.float32)
+    for i, j in enumerate(js):
+        assert np.array_equal(yu[i], W[:, j]), (i, j)

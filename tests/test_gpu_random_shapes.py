@@ -122,3 +122,59 @@ def test_random_batch(q, fmt, rows, k, m, cfg, mode):
     for i in range(m):
         e = float(np.max(np.abs(ref[i] - got[i])) / max(np.max(np.abs(ref[i])), 1e-30))
         assert e <= SCALE_REL_TOL, (i, e)
+
+
+def independent_cases(n=3):
+    """(fam, rows, k) drawn from a fixed stream, with rows large enough that
+    independent calls take the streaming plan (a quarter of the SM count in
+    CTAs, each streaming a long share through a two-slot ring)."""
+    fams = ("q4k", "q6k", "q8_0", "q5k", "q4_0", "q8d", "q4d", "q6d")
+    z = synth.Stream(20261203).draw(len(fams) * n * 2).reshape(len(fams), n, 2)
+    out = []
+    for fi, fam in enumerate(fams):
+        for ci in range(n):
+            d = [int(v >> np.uint64(33)) for v in z[fi, ci]]
+            nb = 1 + d[0] % (8 if QK[fam] == 256 else 64)
+            rows = 600 + d[1] % 2400
+            out.append((fam, rows, nb * QK[fam]))
+    return out
+
+
+@pytest.mark.parametrize("fam,rows,k", independent_cases())
+def test_random_shape_independent_calls(q, fam, rows, k):
+    """Independent calls (QMV_OVERLAP_INDEPENDENT, the streaming plan) give the
+    plain launch's bits, back to back with buffers reused, and the oracle's
+    result within the bound."""
+    fmt = FMT.get(fam, fam)
+    st = synth.Stream(rows * 977 + k)
+    w = synth.GEN_ROWS[fmt](st, rows, k)
+    x = synth.gen_normal(st, k)
+    wd = torch.from_numpy(w).cuda()
+    xd = torch.from_numpy(x).cuda()
+    if fam in FMT:
+        xq = torch.empty(k, dtype=torch.int8, device="cuda")
+        xs = torch.empty(k // 32, dtype=torch.float32, device="cuda")
+        q.quantize_act_q8(xd, xq, xs, None, 1, k)
+        entry = {"q8d": q.qmv_q8_dp4a, "q4d": q.qmv_q4k_dp4a, "q6d": q.qmv_q6k_dp4a}[fam]
+
+        def call(y, ov):
+            entry(wd, xq, xs, y, rows, k, overlap=ov)
+        oq, os_, _ = oracle.quantize_act_q8(x, 1, k)
+        ref = {"q8d": oracle.qmv_q8_dp4a, "q4d": oracle.qmv_q4k_dp4a, "q6d": oracle.qmv_q6k_dp4a}[fam](
+            w, oq.reshape(-1), os_.reshape(-1), rows, k)
+    else:
+        def call(y, ov):
+            getattr(q, f"qmv_{fam}")(wd, xd, y, rows, k, overlap=ov)
+        ref = oracle.qmv(fam, w, x, rows, k)
+    plain = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+    call(plain, q.OVERLAP_NONE)
+    bufs = [torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda") for _ in range(2)]
+    outs = []
+    for i in range(4):
+        call(bufs[i % 2], q.OVERLAP_INDEPENDENT)
+        outs.append(bufs[i % 2].clone())
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, plain)
+    got = plain.cpu().numpy().astype(np.float64)
+    assert float(np.max(np.abs(ref - got)) / max(float(np.max(np.abs(ref))), 1e-30)) <= 1e-4
