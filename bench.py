@@ -222,6 +222,7 @@ class Workload:
         self.cfg = None   # optional forced launch configuration (dict), for tuning sweeps
         self.overlap = 0  # launch overlap of every call (q.OVERLAP_*)
         self.fused = False  # q8_0_dp4a: quantize x inside the matvec launch (qmv_q8_dp4a_quant)
+        self.tc5 = False    # qmm_q4k: the fifth-generation tensor-core kernel (qmm_q4k_tc5)
 
     def call(self, i: int, stream: int, with_quant: bool = False) -> int:
         """Enqueue call i; returns the number of kernels it launched."""
@@ -231,6 +232,10 @@ class Workload:
             q.qmv_q4k(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg, overlap=ov)
         elif self.kind in ("q6k", "q5k", "q4_0"):
             getattr(q, f"qmv_{self.kind}")(w, self.x, self.y, self.rows, self.k, stream=stream, cfg=cfg, overlap=ov)
+        elif self.kind == "qmm_q4k" and self.tc5:
+            m = self.c["m"]
+            q.qmm_q4k_tc5(w, self.x, self.y, self.rows, self.k, m, stream=stream, cfg=cfg, overlap=ov)
+            return (m + 7) // 8
         elif self.kind.startswith("qmm_"):
             m = self.c["m"]
             getattr(q, self.kind)(w, self.x, self.y, self.rows, self.k, m, stream=stream, cfg=cfg, overlap=ov)
@@ -448,6 +453,13 @@ def run_ours(args):
                 msq, _, g3, _ = time_graph(torch, w2, n, with_quant=True, replays=4)
                 times[MODE_NAMES[mode] + "_with_quantize"] = msq
                 del g3
+            if w2.kind == "qmm_q4k":
+                # the same product on the fifth-generation tensor cores
+                w2.tc5 = True
+                mst, _, g5, _ = time_graph(torch, w2, n, replays=4)
+                times[MODE_NAMES[mode] + "_tcgen05"] = mst
+                w2.tc5 = False
+                del g5
             if w2.kind == "q8_0_dp4a":
                 # the quantization inside the matvec launch
                 w2.fused = True

@@ -90,6 +90,7 @@ _SIG = {
     "qmv_dequant_q4_0": [_P, _P, _I, _I, _P],
     "qmm_q4k": [_P, _P, _P, _I, _I, _I, _P],
     "qmm_q4k_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q4k_tc5_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q6k": [_P, _P, _P, _I, _I, _I, _P],
     "qmm_q6k_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q8_0": [_P, _P, _P, _I, _I, _I, _P],
@@ -209,6 +210,11 @@ def _qmm(name, w, x, y, rows, k, m, stream, cfg, overlap, check):
 
 def qmm_q4k(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):
     return _qmm("qmm_q4k", w, x, y, rows, k, m, stream, cfg, overlap, check)
+
+
+def qmm_q4k_tc5(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):
+    return _call("qmm_q4k_tc5_ex", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _opts(cfg, overlap), _stream(stream),
+                 check=check)
 
 
 def qmm_q6k(w, x, y, rows, k, m, stream=None, cfg=None, overlap=0, check=True):

@@ -115,6 +115,16 @@ int qmm_q4k(const void* w, const float* x, float* y, int rows, int k, int m, cud
     return qmm_q4k_ex(w, x, y, rows, k, m, nullptr, stream);
 }
 
+int qmm_q4k_tc5_ex(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
+                   cudaStream_t stream) {
+    if (!opts_ok(cfg)) return QMV_EINVAL;
+    int rc = check_dense(w, x, y, rows, k, 256, 144);
+    if (!rc && (m <= 0 || static_cast<long long>(m) * k > INT_MAX || static_cast<long long>(m) * rows > INT_MAX))
+        rc = QMV_EINVAL;
+    if (rc) return rc;
+    return qmvi::qmm_q4k_tc5(w, x, y, rows, k, m, cfg, stream);
+}
+
 int qmm_q6k_ex(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                 cudaStream_t stream) {
     if (!opts_ok(cfg)) return QMV_EINVAL;
@@ -411,7 +421,8 @@ int qmv_device_status(unsigned int* status, int clear) {
     if (!status) return QMV_EINVAL;
     int (*const readers[])(unsigned int*, int) = {qmvi::status_q4k,     qmvi::status_q6k,     qmvi::status_q8,
                                                   qmvi::status_q5k,     qmvi::status_q4_0,    qmvi::status_qmm_q4k,
-                                                  qmvi::status_qmm_q6k, qmvi::status_qmm_q8_0};
+                                                  qmvi::status_qmm_q6k, qmvi::status_qmm_q8_0,
+                                                  qmvi::status_qmm_q4k_tc5};
     unsigned int all = 0;
     for (auto rd : readers) {
         unsigned int v = 0;

@@ -74,4 +74,10 @@ int status_qmm_q4k(unsigned int* out, int clear);
 int status_qmm_q6k(unsigned int* out, int clear);
 int status_qmm_q8_0(unsigned int* out, int clear);
 
+// qmm_q4k_tc5.cu: the small-M batched product on the fifth-generation tensor
+// cores (Q4_K rows)
+int qmm_q4k_tc5(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
+                cudaStream_t s, int force_timeout = 0);
+int status_qmm_q4k_tc5(unsigned int* out, int clear);
+
 }  // namespace qmvi

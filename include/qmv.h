@@ -336,6 +336,24 @@ int moe_qmv_q6k_dp4a_ex(const void *w_bank, const int8_t *xq, const float *xs, f
                          cudaStream_t stream);
 int qmm_q4k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                 cudaStream_t stream);
+
+/* The batched product of qmm_q4k_ex (hanzo-ml src/vulkan_backend.rs,
+ * matmul_q4k_gpu) on the fifth-generation tensor cores: tcgen05.mma with the
+ * decoded weights (sc * q, exact in f16) as the A operand in tensor memory, x
+ * as hi + lo f16 parts in shared memory and f32 accumulators in tensor memory;
+ * each 128-row tile is split along k over the CTAs of one thread-block
+ * cluster, which add their partial sums in rank order. Same result contract as
+ * qmm_q4k_ex (unit rows of x give the weight columns bit for bit; otherwise
+ * within 1e-4 scale-relative of the exact product); arguments, layouts and
+ * errors as there, m >= 1 (tiles of 8 rows of x, one launch each); w and x
+ * must be 16-byte aligned (QMV_EINVAL otherwise). opts->cluster forces the
+ * number of k-chunks of a tile (1..8), opts->chunks the ring depth,
+ * opts->overlap the launch overlap. On a GB300 this path measured slower than
+ * qmm_q4k_ex for m <= 8 on the 4096 x 4096 matrix (each CTA's fixed costs --
+ * tensor-memory allocation, the x conversion, the cluster reduction --
+ * outweigh its few super-blocks of work), so qmm_q4k_ex does not use it. */
+int qmm_q4k_tc5_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
+                   cudaStream_t stream);
 int qmm_q6k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                 cudaStream_t stream);
 int qmm_q8_0_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,

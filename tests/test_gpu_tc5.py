@@ -1,0 +1,140 @@
+"""GPU parity of the batched product on the fifth-generation tensor cores
+(qmm_q4k_tc5: tcgen05.mma with tensor-memory accumulators, 2-D TMA tensor
+copies, k-chunks reduced across a thread-block cluster) against the CPU
+oracle, through the C ABI.
+
+Bars as for the other batch kernels: unit rows of x give the weight columns
+bit for bit; otherwise every row of y is within scale-relative error
+max|a-b|/max|a| <= 1e-4 of the f64 oracle. Shapes cover one and several
+128-row tiles, a ragged last tile, k-chunks of unequal length (k / 256 not a
+multiple of the cluster size), every cluster size, every ring depth, and
+m > 8 (two launches).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+SCALE_REL_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def q():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    import ggml_format_dequant_gb300 as lib
+    lib.qmv_device_status(clear=True)
+    return lib
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def scale_rel(ref, got):
+    ref = np.asarray(ref, dtype=np.float64)
+    got = np.asarray(got, dtype=np.float64)
+    return float(np.max(np.abs(ref - got)) / max(float(np.max(np.abs(ref))), 1e-30))
+
+
+def run(q, w, x, rows, k, m, cfg=None, overlap=0):
+    y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    q.qmm_q4k_tc5(dev(w), dev(x), y, rows, k, m, cfg=cfg, overlap=overlap)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def case(rows, k, m, seed):
+    st = synth.Stream(seed)
+    w = synth.gen_q4k_rows(st, rows, k)
+    x = synth.gen_normal(st, m * k).reshape(m, k)
+    return w, x
+
+
+@pytest.mark.parametrize("rows,k,m", [(128, 256, 1), (300, 1024, 3), (256, 4096, 8), (1000, 14336, 4),
+                                      (4096, 2048, 5), (517, 2560, 9), (4096, 4096, 2)])
+def test_matches_oracle(q, rows, k, m):
+    w, x = case(rows, k, m, rows + 7 * k + m)
+    y = run(q, w, x, rows, k, m)
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    assert not np.any(np.isnan(y))
+    for i in range(m):
+        assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, i
+    assert q.qmv_device_status() == 0
+
+
+@pytest.mark.parametrize("rows,k", [(256, 1024), (4096, 4096), (200, 2560)])
+def test_unit_rows_give_weight_columns(q, rows, k):
+    st = synth.Stream(11 + rows)
+    w = synth.gen_q4k_rows(st, rows, k)
+    js = [5, k - 1, 300, 17, k // 2, 333, 64, 1023]
+    xu = np.zeros((8, k), dtype=np.float32)
+    for i, j in enumerate(js):
+        xu[i, j] = 1.0
+    y = run(q, w, xu, rows, k, 8)
+    W = oracle.dequant("q4k", w, rows, k).astype(np.float32)
+    for i, j in enumerate(js):
+        assert np.array_equal(y[i], W[:, j]), (i, j)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+def test_every_cluster_size_and_ring_depth(q, cluster):
+    """The cluster size sets how k is split (the rounding of the chunk sums
+    changes, so each is checked against the oracle); the ring depth only
+    schedules the same arithmetic, so every depth gives the same bits."""
+    rows, k, m = 384, 3072, 4
+    w, x = case(rows, k, m, 99)
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    ys = [run(q, w, x, rows, k, m, cfg={"cluster": cluster, "chunks": s}) for s in (1, 2, 4)]
+    for y in ys:
+        for i in range(m):
+            assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, (cluster, i)
+    assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
+
+
+def test_launch_overlap_modes_are_bitwise_equal(q):
+    rows, k, m = 4096, 4096, 4
+    w, x = case(rows, k, m, 5)
+    ys = [run(q, w, x, rows, k, m, overlap=o) for o in (q.OVERLAP_NONE, q.OVERLAP_CHAIN, q.OVERLAP_INDEPENDENT)]
+    assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
+
+
+def test_same_as_chained_calls_in_a_stream(q):
+    """Ten calls in a row on one stream, chained (each call's x is the
+    previous call's y, rows == k), all within the tolerance of the oracle fed
+    the inputs each call read."""
+    n, m = 2048, 2
+    st = synth.Stream(77)
+    ws = [synth.gen_q4k_rows(st, n, n) for _ in range(10)]
+    x0 = (synth.gen_normal(st, m * n) / np.float32(16)).astype(np.float32).reshape(m, n)
+    cur = dev(x0)
+    outs = []
+    for w in ws:
+        y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        q.qmm_q4k_tc5(dev(w), cur, y, n, n, m, overlap=q.OVERLAP_CHAIN)
+        outs.append(y)
+        cur = y
+    torch.cuda.synchronize()
+    inputs = [x0] + [o.cpu().numpy() for o in outs[:-1]]
+    for w, xin, o in zip(ws, inputs, outs):
+        ref = oracle.qmm("q4k", w, xin, m, n, n)
+        got = o.cpu().numpy()
+        for i in range(m):
+            assert scale_rel(ref[i], got[i]) <= SCALE_REL_TOL
+
+
+def test_rejects_unaligned_operands(q):
+    rows, k, m = 128, 256, 2
+    w, x = case(rows, k, m, 3)
+    wd = torch.zeros(w.nbytes + 16, dtype=torch.uint8, device="cuda")
+    wd[2:2 + w.nbytes] = dev(w.reshape(-1))
+    y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
+    with pytest.raises(q.QmvError):
+        q.qmm_q4k_tc5(wd[2:], dev(x), y, rows, k, m)
