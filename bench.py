@@ -56,7 +56,7 @@ FALLBACK_HBM_GBS = 6800.0
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one
 # qmv_q4k launch on the headline workload, per launch mode, valid only for the
 # kernel sources whose hash it is recorded under.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"df59e18ef86f0102": {2: 9496064}}
 
 KERNEL_SOURCES = ["qmv_device.cuh", "qmv_formats.cuh", "qmv_kernel.cuh", "qmv_launch.cuh", "qmv_q4k.cu"]
 
@@ -684,6 +684,7 @@ def run_profile(args):
     wl = Workload(q, torch, args.profile_workload, 0, device, copies=1)
     if args.headline_mode is not None:
         wl.overlap = args.headline_mode   # the launch mode (and plan) the bench times
+    wl.tc5 = args.tcgen05
     s = torch.cuda.current_stream().cuda_stream
     for i in range(args.warmup + args.steps):
         wl.call(i, s, with_quant=True)
@@ -709,6 +710,8 @@ def main():
                     help="time the headline without decode-chain overlap (programmatic dependent launch off)")
     ap.add_argument("--profile-workload", choices=list(synth.CONFIGS),
                     help="only run warmup+steps eager calls of this workload (the command ncu captures)")
+    ap.add_argument("--tcgen05", action="store_true",
+                    help="with --profile-workload qmm_q4k_*: run the fifth-generation tensor-core kernel")
     args = ap.parse_args()
     if args.profile_workload:
         run_profile(args)
