@@ -113,6 +113,7 @@ _SIG = {
     "qmv_device_status": [_P, _I],
     "qmv_selftest_wait_timeout": [ctypes.c_ulonglong, _P],
     "qmv_selftest_timeout_path": [_P, _P, _P, _I, _I, _I, _P],
+    "qmm_q4k_tc5_selftest_timeout_path": [_P, _P, _P, _I, _I, _I, _P],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "qmv_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
     "qmm_tc_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
@@ -374,6 +375,11 @@ def qmv_selftest_wait_timeout(limit_ns, stream=None, check=True):
 
 def qmv_selftest_timeout_path(w, x, y, rows, k, m=1, stream=None, check=True):
     return _call("qmv_selftest_timeout_path", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _stream(stream), check=check)
+
+
+def qmm_q4k_tc5_selftest_timeout_path(w, x, y, rows, k, m=2, stream=None, check=True):
+    return _call("qmm_q4k_tc5_selftest_timeout_path", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _stream(stream),
+                 check=check)
 
 
 def qmv_device_status(clear=True) -> int:

@@ -408,6 +408,14 @@ int qmv_selftest_timeout_path(const void* w, const float* x, float* y, int rows,
                   : qmvi::qmm_q4k(w, x, y, rows, k, m, nullptr, stream, 1);
 }
 
+int qmm_q4k_tc5_selftest_timeout_path(const void* w, const float* x, float* y, int rows, int k, int m,
+                                      cudaStream_t stream) {
+    int rc = check_dense(w, x, y, rows, k, 256, 144);
+    if (!rc && (m <= 0 || m > 8)) rc = QMV_EINVAL;
+    if (rc) return rc;
+    return qmvi::qmm_q4k_tc5(w, x, y, rows, k, m, nullptr, stream, 1);
+}
+
 int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {
     if (limit_ns == 0 || limit_ns > 100000000ull) return QMV_EINVAL;
     return qmvi::selftest_wait_timeout(limit_ns, stream);

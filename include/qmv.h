@@ -295,6 +295,15 @@ int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
 int qmv_selftest_timeout_path(const void *w, const float *x, float *y, int rows, int k, int m,
                               cudaStream_t stream);
 
+/* The same failure-path self-test for qmm_q4k_tc5_ex (m = 1..8): every CTA's
+ * decoder warps take the path of a staged copy that did not land; the CTA
+ * lets its copies land (bounded), releases its tensor memory, raises
+ * QMV_STATUS_WAIT_TIMEOUT and its partial sums are NaN, so every output of
+ * the product is NaN. Arguments as for qmm_q4k_tc5_ex. Nothing hangs or
+ * traps; the context stays usable. */
+int qmm_q4k_tc5_selftest_timeout_path(const void *w, const float *x, float *y, int rows, int k, int m,
+                                      cudaStream_t stream);
+
 /* OR of the status bits raised on the current device since the last clear;
  * clears them when `clear` is non-zero. Waits for all work on the current
  * device (cudaDeviceSynchronize), then reads the word and clears it in one

@@ -138,3 +138,22 @@ def test_rejects_unaligned_operands(q):
     y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
     with pytest.raises(q.QmvError):
         q.qmm_q4k_tc5(wd[2:], dev(x), y, rows, k, m)
+
+
+@pytest.mark.parametrize("rows,k,m", [(256, 2048, 2), (300, 1024, 8)])
+def test_timeout_path_marks_outputs_nan(q, rows, k, m):
+    """Every CTA's decoders take the path of a weight copy that did not land:
+    all outputs are NaN, the status word says so, and the next call on the
+    same context is correct again."""
+    w, x = case(rows, k, m, 41 + rows)
+    q.qmv_device_status(clear=True)
+    y = torch.zeros((m, rows), dtype=torch.float32, device="cuda")
+    q.qmm_q4k_tc5_selftest_timeout_path(dev(w), dev(x), y, rows, k, m)
+    torch.cuda.synchronize()
+    assert np.all(np.isnan(y.cpu().numpy()))
+    assert q.qmv_device_status(clear=True) & q.QMV_STATUS_WAIT_TIMEOUT
+    y2 = run(q, w, x, rows, k, m)
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    for i in range(m):
+        assert scale_rel(ref[i], y2[i]) <= SCALE_REL_TOL
+    assert q.qmv_device_status() == 0
