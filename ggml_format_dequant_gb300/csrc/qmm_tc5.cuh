@@ -31,8 +31,11 @@
 //    (tcgen05.mma ... kind::f16, A from tensor memory, B from shared memory)
 //    and commits them to mbarriers. Every wait is bounded; a wait that gives
 //    up marks the CTA's outputs NaN and sets STATUS_WAIT_TIMEOUT.
-//  * Tensor memory is allocated before anything else and released before the
-//    first cluster barrier, so a CTA holding it never waits for another CTA.
+//  * x is staged by bulk copies (after the dependency wait in a chain) and
+//    converted by the decoder warps. Tensor memory is allocated before
+//    anything else and released before the cluster barrier, so a CTA holding
+//    it never waits for another CTA. The partial sums travel by remote stores
+//    into the owning CTA's shared memory before that one barrier.
 #pragma once
 
 #include <cuda.h>   // CUtensorMap (the type only)
