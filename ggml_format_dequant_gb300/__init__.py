@@ -91,6 +91,7 @@ _SIG = {
     "qmm_q4k": [_P, _P, _P, _I, _I, _I, _P],
     "qmm_q4k_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q4k_tc5_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
+    "qmm_q4k_tc5_plan_detail": [_I, _I, _I, _P, _P, _P],
     "qmm_q6k": [_P, _P, _P, _I, _I, _I, _P],
     "qmm_q6k_ex": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmm_q8_0": [_P, _P, _P, _I, _I, _I, _P],
@@ -425,3 +426,16 @@ def qmm_tc_plan_detail(fmt, rows, k, m, cfg=None, device=GB300_DEVICE, overlap=0
     dev = (ctypes.c_int * 4)(*device)
     _call("qmm_tc_plan_detail", fmt, rows, k, m, _opts(cfg, overlap), dev, out)
     return dict(zip(QMM_TC_PLAN_FIELDS, list(out)))
+
+
+TC5_PLAN_FIELDS = ("ctas", "threads", "smem", "CL", "S", "nsb", "off_b", "off_bm", "off_sc", "off_x", "off_in",
+                   "off_bars")
+
+
+def qmm_q4k_tc5_plan_detail(rows, k, m, cfg=None, device=GB300_DEVICE, overlap=0) -> dict:
+    """The plan of qmm_q4k_tc5 for one launch of m <= 8 rows of x on a
+    described device, computed on the host without a GPU."""
+    out = (ctypes.c_int * len(TC5_PLAN_FIELDS))()
+    dev = (ctypes.c_int * 4)(*device)
+    _call("qmm_q4k_tc5_plan_detail", rows, k, m, _opts(cfg, overlap), dev, out)
+    return dict(zip(TC5_PLAN_FIELDS, list(out)))

@@ -20,8 +20,12 @@ constexpr long long T5_STATIC_SMEM = 1024;
 inline int make_t5_plan(const DevInfo& di, int rows, int k, int m, const qmv_opts* cfg, T5Params* tp, Plan* pl) {
     if (rows <= 0 || k <= 0 || k % T5_SB || m < 1 || m > T5_COLS) return QMV_EINVAL;
     const int nsb = k / T5_SB;
-    int CL = (cfg && cfg->cluster > 0) ? std::min(cfg->cluster, CLUSTER_MAX) : std::min(CLUSTER_MAX, nsb);
-    CL = std::max(1, std::min(CL, nsb));
+    // k-chunks: a power of two (so that each of the CL ranks adds up exactly
+    // 128 / CL rows of the tile), at most the cluster limit, the super-blocks
+    // of a row, and the size asked for
+    const int want = std::min((cfg && cfg->cluster > 0) ? std::min(cfg->cluster, CLUSTER_MAX) : CLUSTER_MAX, nsb);
+    int CL = 1;
+    while (2 * CL <= want) CL *= 2;
     const int nq = (nsb + CL - 1) / CL;   // super-blocks of the largest chunk
     int S = (cfg && cfg->chunks > 0) ? cfg->chunks : 4;
     S = std::max(1, std::min(S, nq));
@@ -166,5 +170,23 @@ int qmm_q4k_tc5(const void* w, const float* x, float* y, int rows, int k, int m,
 }
 
 int status_qmm_q4k_tc5(unsigned int* out, int clear) { return status_rw(out, clear); }
+
+int qmm_q4k_tc5_plan(const int* device, int rows, int k, int m, const qmv_opts* cfg, int* out) {
+    DevInfo di;
+    di.nsm = device[0];
+    di.smem_optin = device[1];
+    di.smem_sm = device[2];
+    di.smem_reserved = device[3];
+    if (di.nsm <= 0 || di.smem_optin <= 0 || di.smem_sm <= 0 || di.smem_reserved < 0) return QMV_EINVAL;
+    T5Params tp{};
+    Plan pl;
+    const int rc = make_t5_plan(di, rows, k, m, cfg, &tp, &pl);
+    if (rc) return rc;
+    const int v[12] = {pl.parts, pl.T, static_cast<int>(pl.smem), tp.CL, tp.S, tp.nsb, static_cast<int>(tp.off_b),
+                       static_cast<int>(tp.off_bm), static_cast<int>(tp.off_sc), static_cast<int>(tp.off_x),
+                       static_cast<int>(tp.off_in), static_cast<int>(tp.off_bars)};
+    for (int i = 0; i < 12; i++) out[i] = v[i];
+    return QMV_OK;
+}
 
 }  // namespace qmvi

@@ -408,6 +408,11 @@ int qmv_selftest_timeout_path(const void* w, const float* x, float* y, int rows,
                   : qmvi::qmm_q4k(w, x, y, rows, k, m, nullptr, stream, 1);
 }
 
+int qmm_q4k_tc5_plan_detail(int rows, int k, int m, const qmv_opts* cfg, const int* device, int* out) {
+    if (!device || !out || !opts_ok(cfg) || rows <= 0 || k <= 0 || k % 256 || m <= 0 || m > 8) return QMV_EINVAL;
+    return qmvi::qmm_q4k_tc5_plan(device, rows, k, m, cfg, out);
+}
+
 int qmm_q4k_tc5_selftest_timeout_path(const void* w, const float* x, float* y, int rows, int k, int m,
                                       cudaStream_t stream) {
     int rc = check_dense(w, x, y, rows, k, 256, 144);

@@ -79,5 +79,6 @@ int status_qmm_q8_0(unsigned int* out, int clear);
 int qmm_q4k_tc5(const void* w, const float* x, float* y, int rows, int k, int m, const qmv_opts* cfg,
                 cudaStream_t s, int force_timeout = 0);
 int status_qmm_q4k_tc5(unsigned int* out, int clear);
+int qmm_q4k_tc5_plan(const int* device, int rows, int k, int m, const qmv_opts* cfg, int* out);
 
 }  // namespace qmvi

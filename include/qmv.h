@@ -363,6 +363,15 @@ int qmm_q4k_ex(const void *w, const float *x, float *y, int rows, int k, int m, 
  * outweigh its few super-blocks of work), so qmm_q4k_ex does not use it. */
 int qmm_q4k_tc5_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                    cudaStream_t stream);
+
+/* The plan qmm_q4k_tc5_ex takes for one launch (m = 1..8 rows of x) on a
+ * described device {SM count, opt-in shared memory per CTA, shared memory per
+ * SM, reserved shared memory per CTA}, computed on the host (no GPU needed):
+ * out[12] = {CTAs, threads, dynamic shared memory, cluster size (k-chunks of a
+ * tile), ring slots, super-blocks per row, and the shared-memory offsets of
+ * B, B', the scales, the staged x, the partial-sum inbox and the barriers}.
+ * Returns QMV_ETOOBIG for a shape whose chunk does not fit one CTA. */
+int qmm_q4k_tc5_plan_detail(int rows, int k, int m, const qmv_opts *opts, const int *device, int *out);
 int qmm_q6k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                 cudaStream_t stream);
 int qmm_q8_0_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,

@@ -157,3 +157,35 @@ def test_timeout_path_marks_outputs_nan(q, rows, k, m):
     for i in range(m):
         assert scale_rel(ref[i], y2[i]) <= SCALE_REL_TOL
     assert q.qmv_device_status() == 0
+
+
+def random_cases(n=12):
+    """Seeded random shapes: rows 1..3000 (ragged last tiles), k a multiple of
+    256 up to 16384, m 1..12, a forced cluster size or the default."""
+    z = synth.Stream(20261204).draw(n * 4).reshape(n, 4)
+    out = []
+    for i in range(n):
+        d = [int(v >> np.uint64(33)) for v in z[i]]
+        rows = 1 + d[0] % 3000
+        k = 256 * (1 + d[1] % 64)
+        m = 1 + d[2] % 12
+        cl = [0, 1, 2, 3, 4, 5, 6, 7, 8][d[3] % 9]
+        out.append((rows, k, m, cl))
+    return out
+
+
+@pytest.mark.parametrize("rows,k,m,cluster", random_cases())
+def test_random_shapes(q, rows, k, m, cluster):
+    w, x = case(rows, k, m, rows * 31 + k + m)
+    cfg = {"cluster": cluster} if cluster else None
+    try:
+        y = run(q, w, x, rows, k, m, cfg=cfg)
+    except q.QmvError as e:
+        # a forced cluster size whose chunks do not fit one CTA's shared
+        # memory is refused on the host, never launched
+        assert e.code == q.QMV_ETOOBIG and cluster and k // 256 > cluster
+        return
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    assert not np.any(np.isnan(y))
+    for i in range(m):
+        assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, i
