@@ -319,21 +319,23 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
 
 // Independent calls (QMV_OVERLAP_INDEPENDENT): CTAs per call, as a divisor of
 // the SM count (the CTAs of an MoE call are shared by its slots).
-constexpr int INDEP_SM_DIV = 4;
+constexpr int INDEP_SM_DIV = 5;
 
 // Launch plan of format F. Independent calls (QMV_OVERLAP_INDEPENDENT) take a
-// few CTAs (about a quarter of the SM count) of at most WARPS_TWO_PER_SM
-// warps in half an SM's shared memory, each streaming a long share of the
-// rows through a two-slot ring of the largest pieces that fit: with two CTAs
-// an SM, many calls are then in flight at once (eight for the Q4_K 4096 x
-// 4096 matvec), and a CTA's fixed costs (start-up, activation prep, the wait
-// before it writes y) are spread over many rows. Measured on GB300, us a call
-// in a stream of 256 independent calls (and of 20): Q4_K 4096 x 4096 with
-// 103 whole-share CTAs 2.12 (2.61), 40 ring CTAs 1.71 (2.37), 16 ring CTAs
-// 1.66 (2.82); Q6_K 4096 x 14336 with 152 CTAs 10.03 (10.7), 38 CTAs 8.65
-// (9.78). Fewer CTAs stream faster in long streams but leave a longer tail in
-// short ones. Chained and plain calls, and forced plans, keep the default
-// plan (every SM).
+// few CTAs (about a fifth of the SM count) of at most WARPS_TWO_PER_SM warps
+// in half an SM's shared memory, each streaming a long share of the rows
+// through a two-slot ring of the largest pieces that fit: with two CTAs an SM,
+// many calls are then in flight at once (ten for the Q4_K 4096 x 4096
+// matvec), and a CTA's fixed costs (start-up, activation prep, the wait before
+// it writes y) are spread over many rows. Measured on GB300, us a call in a
+// stream of 256 independent calls (and of 20): Q4_K 4096 x 4096 with 103
+// whole-share CTAs 2.12 (2.61), 38 ring CTAs 1.62 (2.24), 30 ring CTAs 1.56
+// (2.24), 25 ring CTAs 1.56 (2.44), 16 ring CTAs 1.66 (2.82); Q6_K 4096 x
+// 14336 with 152 CTAs 10.03 (10.7), 38 CTAs 8.65 (9.78), 30 CTAs 8.61 (9.68),
+// 25 CTAs 8.61 (11.1); Q8_0 dp4a 14336 x 4096 with 38 CTAs 8.60 (9.7), 30
+// CTAs 8.39 (8.6). Fewer CTAs stream faster in long streams but leave a
+// longer tail in short ones. Chained and plain calls, and forced plans, keep
+// the default plan (every SM).
 template <class F>
 inline int make_plan_for(const DevInfo& di, int rows, int k, int slots, const qmv_opts* cfg, KParams* kp, Plan* pl) {
     const int rc = make_plan_core<F>(di, rows, k, slots, cfg, kp, pl);

@@ -126,7 +126,7 @@ def test_random_batch(q, fmt, rows, k, m, cfg, mode):
 
 def independent_cases(n=3):
     """(fam, rows, k) drawn from a fixed stream, with rows large enough that
-    independent calls take the streaming plan (a quarter of the SM count in
+    independent calls take the streaming plan (a fifth of the SM count in
     CTAs, each streaming a long share through a two-slot ring)."""
     fams = ("q4k", "q6k", "q8_0", "q5k", "q4_0", "q8d", "q4d", "q6d")
     z = synth.Stream(20261203).draw(len(fams) * n * 2).reshape(len(fams), n, 2)
