@@ -114,7 +114,7 @@ _SIG = {
     "qmv_device_status": [_P, _I],
     "qmv_selftest_wait_timeout": [ctypes.c_ulonglong, _P],
     "qmv_selftest_timeout_path": [_P, _P, _P, _I, _I, _I, _P],
-    "qmm_q4k_tc5_selftest_timeout_path": [_P, _P, _P, _I, _I, _I, _P],
+    "qmm_q4k_tc5_selftest_timeout_path": [_P, _P, _P, _I, _I, _I, _P, _P],
     "qmv_plan_info": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
     "qmv_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
     "qmm_tc_plan_detail": [_I, _I, _I, _I, _P, _P, _P],
@@ -378,9 +378,9 @@ def qmv_selftest_timeout_path(w, x, y, rows, k, m=1, stream=None, check=True):
     return _call("qmv_selftest_timeout_path", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _stream(stream), check=check)
 
 
-def qmm_q4k_tc5_selftest_timeout_path(w, x, y, rows, k, m=2, stream=None, check=True):
-    return _call("qmm_q4k_tc5_selftest_timeout_path", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _stream(stream),
-                 check=check)
+def qmm_q4k_tc5_selftest_timeout_path(w, x, y, rows, k, m=2, stream=None, overlap=0, check=True):
+    return _call("qmm_q4k_tc5_selftest_timeout_path", _ptr(w), _ptr(x), _ptr(y), rows, k, m, _opts(None, overlap),
+                 _stream(stream), check=check)
 
 
 def qmv_device_status(clear=True) -> int:
@@ -429,7 +429,7 @@ def qmm_tc_plan_detail(fmt, rows, k, m, cfg=None, device=GB300_DEVICE, overlap=0
 
 
 TC5_PLAN_FIELDS = ("ctas", "threads", "smem", "CL", "S", "nsb", "off_b", "off_bm", "off_sc", "off_x", "off_in",
-                   "off_bars")
+                   "off_bars", "streaming")
 
 
 def qmm_q4k_tc5_plan_detail(rows, k, m, cfg=None, device=GB300_DEVICE, overlap=0) -> dict:

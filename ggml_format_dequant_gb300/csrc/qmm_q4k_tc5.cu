@@ -3,7 +3,7 @@
 #include <mutex>
 
 #include "qmv_internal.h"
-#include "qmm_tc5.cuh"
+#include "qmm_tc5s.cuh"
 
 namespace qmv {
 
@@ -71,6 +71,60 @@ inline int make_t5_plan(const DevInfo& di, int rows, int k, int m, const qmv_opt
     return QMV_OK;
 }
 
+// Shared memory the streaming plan asks for at least: more than half an SM's,
+// so that one CTA holds an SM and its allocation of all 512 tensor-memory
+// columns never waits.
+constexpr long long T5S_MIN_SMEM = 120 * 1024;
+
+// The streaming plan (independent calls): one CTA a 128-row tile for the
+// whole of k; B for the whole of k in shared memory, so rows of up to a few
+// thousand weights (QMV_ETOOBIG beyond).
+inline int make_t5s_plan(const DevInfo& di, int rows, int k, int m, const qmv_opts* cfg, T5SParams* tp, Plan* pl) {
+    if (rows <= 0 || k <= 0 || k % T5_SB || m < 1 || m > T5_COLS) return QMV_EINVAL;
+    const int nsb = k / T5_SB;
+    int S = (cfg && cfg->chunks > 0) ? cfg->chunks : 4;
+    S = std::max(1, std::min(S, nsb));
+    const uint32_t slot = static_cast<uint32_t>(T5_ROWS * T5_SBBYTES);
+    const long long limit = di.smem_optin - T5_STATIC_SMEM;
+    long long smem = 0;
+    for (;; S--) {
+        long long off = static_cast<long long>(S) * slot;
+        tp->off_ring = 0;
+        tp->off_b = static_cast<uint32_t>(round_up(off, 128));
+        off = tp->off_b + static_cast<long long>(nsb) * 32 * 256;
+        tp->off_bm = static_cast<uint32_t>(round_up(off, 128));
+        off = tp->off_bm + static_cast<long long>(nsb) * 512;
+        tp->off_sc = static_cast<uint32_t>(round_up(off, 16));
+        off = tp->off_sc + static_cast<long long>(nsb) * T5_COLS * 2 * 4;
+        tp->off_bars = static_cast<uint32_t>(round_up(off, 8));
+        off = tp->off_bars + 8LL * (2 * S + 13);
+        smem = std::max(round_up(off, 128), T5S_MIN_SMEM);
+        if (smem <= limit) break;
+        if (S == 1) return QMV_ETOOBIG;
+    }
+    tp->rows = rows;
+    tp->k = k;
+    tp->m = m;
+    tp->nsb = nsb;
+    tp->S = S;
+    tp->slot_bytes = slot;
+    const int mode = overlap_of(cfg);
+    tp->early_inputs = mode >= QMV_OVERLAP_INDEPENDENT ? 1 : 0;
+    pl->T = T5S_THREADS;
+    pl->parts = (rows + T5_ROWS - 1) / T5_ROWS;
+    pl->R = 1;
+    pl->CL = 1;
+    pl->overlap = mode;
+    pl->smem = static_cast<size_t>(smem);
+    return QMV_OK;
+}
+
+// Independent calls whose B fits take the streaming plan, unless a cluster
+// size is forced.
+inline bool t5_streams(const qmv_opts* cfg) {
+    return overlap_of(cfg) == QMV_OVERLAP_INDEPENDENT && !(cfg && cfg->cluster > 0);
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -136,6 +190,30 @@ inline int launch_t5(const CUtensorMap& map, const T5Params& tp, const Plan& pl,
     return cuda_rc(cudaLaunchKernelEx(&lc, kern, map, tp));
 }
 
+inline int launch_t5s(const CUtensorMap& map, const T5SParams& tp, const Plan& pl, cudaStream_t stream) {
+    auto kern = qmm_tc5s_q4k_kernel;
+    static SmemOptIn opted;
+    int dev = 0;
+    DevInfo di;
+    if (dev_info(&di, &dev)) return QMV_ECUDA;
+    if (const int rc = ensure_smem(kern, opted, dev, static_cast<int>(pl.smem))) return rc;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(pl.parts, 1, 1);
+    lc.blockDim = dim3(pl.T, 1, 1);
+    lc.dynamicSmemBytes = pl.smem;
+    lc.stream = stream;
+    cudaLaunchAttribute at[1];
+    int na = 0;
+    if (pl.overlap != QMV_OVERLAP_NONE) {
+        at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[na].val.programmaticStreamSerializationAllowed = 1;
+        na++;
+    }
+    lc.attrs = at;
+    lc.numAttrs = na;
+    return cuda_rc(cudaLaunchKernelEx(&lc, kern, map, tp));
+}
+
 }  // namespace qmv
 
 namespace qmvi {
@@ -155,6 +233,19 @@ int qmm_q4k_tc5(const void* w, const float* x, float* y, int rows, int k, int m,
     const int tiles = (m + T5_COLS - 1) / T5_COLS;
     for (int t0 = 0, m0 = 0; t0 < tiles; t0++) {
         const int mt = m / tiles + (t0 < m % tiles ? 1 : 0);
+        if (t5_streams(cfg)) {
+            T5SParams sp{};
+            Plan spl;
+            if (make_t5s_plan(di, rows, k, mt, cfg, &sp, &spl) == QMV_OK) {
+                sp.x = x + static_cast<long long>(m0) * k;
+                sp.y = y + static_cast<long long>(m0) * rows;
+                sp.force_timeout = force_timeout;
+                rc = launch_t5s(map, sp, spl, s);
+                if (rc) return rc;
+                m0 += mt;
+                continue;
+            }
+        }
         T5Params tp{};
         Plan pl;
         rc = make_t5_plan(di, rows, k, mt, cfg, &tp, &pl);
@@ -178,14 +269,25 @@ int qmm_q4k_tc5_plan(const int* device, int rows, int k, int m, const qmv_opts* 
     di.smem_sm = device[2];
     di.smem_reserved = device[3];
     if (di.nsm <= 0 || di.smem_optin <= 0 || di.smem_sm <= 0 || di.smem_reserved < 0) return QMV_EINVAL;
+    if (t5_streams(cfg)) {
+        T5SParams sp{};
+        Plan spl;
+        if (make_t5s_plan(di, rows, k, m, cfg, &sp, &spl) == QMV_OK) {
+            const int v[13] = {spl.parts, spl.T, static_cast<int>(spl.smem), 1, sp.S, sp.nsb,
+                               static_cast<int>(sp.off_b), static_cast<int>(sp.off_bm), static_cast<int>(sp.off_sc), 0,
+                               0, static_cast<int>(sp.off_bars), 1};
+            for (int i = 0; i < 13; i++) out[i] = v[i];
+            return QMV_OK;
+        }
+    }
     T5Params tp{};
     Plan pl;
     const int rc = make_t5_plan(di, rows, k, m, cfg, &tp, &pl);
     if (rc) return rc;
-    const int v[12] = {pl.parts, pl.T, static_cast<int>(pl.smem), tp.CL, tp.S, tp.nsb, static_cast<int>(tp.off_b),
+    const int v[13] = {pl.parts, pl.T, static_cast<int>(pl.smem), tp.CL, tp.S, tp.nsb, static_cast<int>(tp.off_b),
                        static_cast<int>(tp.off_bm), static_cast<int>(tp.off_sc), static_cast<int>(tp.off_x),
-                       static_cast<int>(tp.off_in), static_cast<int>(tp.off_bars)};
-    for (int i = 0; i < 12; i++) out[i] = v[i];
+                       static_cast<int>(tp.off_in), static_cast<int>(tp.off_bars), 0};
+    for (int i = 0; i < 13; i++) out[i] = v[i];
     return QMV_OK;
 }
 

@@ -162,6 +162,97 @@ __device__ __forceinline__ float t5_scale(float mx, float& inv) {
     return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
 }
 
+// B and B' of super-blocks 0 .. nq-1 from x (row j of super-block q at
+// x + j * xstride + 256 q; any readable memory, global or shared), by warps
+// `warp` of `nwarps` that all call it: the (super-block, row of x) pairs are
+// dealt over the warps, four at a time a warp so that their shuffle trees
+// interleave; rows j >= m are zeros. Scales go to scl[(q * 8 + j) * 2 + {0, 1}].
+__device__ __forceinline__ void t5_build_b(const float* x, long long xstride, int nq, int m, int warp, int nwarps,
+                                           int lane, uint8_t* bptr, uint8_t* bmptr, float* scl) {
+    for (int i = warp * 32 + lane; i < nq * 64; i += nwarps * 32)
+        reinterpret_cast<uint32_t*>(bmptr)[(i >> 6) * 128 + 64 + (i & 63)] = 0u;
+    for (int base = warp; base < nq * T5_COLS; base += 4 * nwarps) {
+        float v[4][8], mx[4], part[4];
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            const int pi = base + nwarps * b;
+            const int q = pi / T5_COLS, j = pi % T5_COLS;
+            if (pi < nq * T5_COLS && j < m) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(x + static_cast<long long>(j) * xstride + q * T5_SB + 8 * lane);
+                const float4 a = src[0], c4 = src[1];
+                v[b][0] = a.x; v[b][1] = a.y; v[b][2] = a.z; v[b][3] = a.w;
+                v[b][4] = c4.x; v[b][5] = c4.y; v[b][6] = c4.z; v[b][7] = c4.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; e++) v[b][e] = 0.0f;
+            }
+            mx[b] = 0.0f;
+            part[b] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                mx[b] = fmaxf(mx[b], fabsf(v[b][e]));
+                part[b] += v[b][e];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int b = 0; b < 4; b++) mx[b] = fmaxf(mx[b], __shfl_xor_sync(FULL, mx[b], o));
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            part[b] += __shfl_xor_sync(FULL, part[b], 1);
+        }
+#pragma unroll
+        for (int b = 0; b < 4; b++) part[b] += __shfl_xor_sync(FULL, part[b], 2);
+        float ms[4];
+#pragma unroll
+        for (int b = 0; b < 4; b++) ms[b] = fabsf(part[b]);
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1)
+#pragma unroll
+            for (int b = 0; b < 4; b++) ms[b] = fmaxf(ms[b], __shfl_xor_sync(FULL, ms[b], o2));
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            const int pi = base + nwarps * b;
+            if (pi >= nq * T5_COLS) break;   // uniform across the warp
+            const int q = pi / T5_COLS, j = pi % T5_COLS;
+            float inv;
+            const float p2 = t5_scale(mx[b], inv);
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const float x0 = v[b][2 * e] * p2, x1 = v[b][2 * e + 1] * p2;
+                const __half2 h = __floats2half2_rn(x0, x1);
+                const float2 hf = __half22float2(h);
+                const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+                lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+            }
+            // k = 256q + 8 lane: core matrix (k-block 32q + lane), row j (hi) / 8 + j (lo)
+            const uint32_t o = static_cast<uint32_t>(32 * q + lane) * 256u + 16u * j;
+            *reinterpret_cast<uint4*>(bptr + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(bptr + o + 128u) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            // group sums (lanes 4g .. 4g + 3 hold group g) under their own scale
+            float sinv;
+            const float s2 = t5_scale(ms[b], sinv);
+            const float sp = part[b] * s2;
+            const __half sh = __float2half_rn(sp);
+            const __half sl = __float2half_rn(sp - __half2float(sh));
+            if ((lane & 3) == 0) {
+                const int g = lane >> 2;
+                const uint32_t om = static_cast<uint32_t>(q) * 512u + 16u * j + 2u * g;
+                *reinterpret_cast<__half*>(bmptr + om) = sh;
+                *reinterpret_cast<__half*>(bmptr + om + 128u) = sl;
+            }
+            if (lane == 0) {
+                scl[(q * T5_COLS + j) * 2] = inv;
+                scl[(q * T5_COLS + j) * 2 + 1] = sinv;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------- the kernel
 
 __global__ void __launch_bounds__(T5_THREADS, 1)
@@ -246,89 +337,8 @@ __global__ void __launch_bounds__(T5_THREADS, 1)
     if (warp < 4) {
         const bool xok = __all_sync(FULL, mbar_wait_bounded(xbar, 0u));
         if (!xok && lane == 0) atomicExch(&s_tmo, 1);
-        for (int i = tid; i < nq * 64; i += 128) reinterpret_cast<uint32_t*>(bmptr)[(i >> 6) * 128 + 64 + (i & 63)] = 0u;
-        // (super-block q, row j of x) pairs, four at a time per warp so that
-        // their shuffle trees interleave
-        for (int base = warp; base < nq * T5_COLS; base += 16) {
-            float v[4][8], mx[4], part[4];
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const int pi = base + 4 * b;
-                const int q = pi / T5_COLS, j = pi % T5_COLS;
-                if (pi < nq * T5_COLS && j < p.m) {
-                    const float4* src = reinterpret_cast<const float4*>(smem + p.off_x) +
-                                        (static_cast<long long>(j) * nq * T5_SB + q * T5_SB + 8 * lane) / 4;
-                    const float4 a = src[0], c4 = src[1];
-                    v[b][0] = a.x; v[b][1] = a.y; v[b][2] = a.z; v[b][3] = a.w;
-                    v[b][4] = c4.x; v[b][5] = c4.y; v[b][6] = c4.z; v[b][7] = c4.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; e++) v[b][e] = 0.0f;
-                }
-                mx[b] = 0.0f;
-                part[b] = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    mx[b] = fmaxf(mx[b], fabsf(v[b][e]));
-                    part[b] += v[b][e];
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int b = 0; b < 4; b++) mx[b] = fmaxf(mx[b], __shfl_xor_sync(FULL, mx[b], o));
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                part[b] += __shfl_xor_sync(FULL, part[b], 1);
-            }
-#pragma unroll
-            for (int b = 0; b < 4; b++) part[b] += __shfl_xor_sync(FULL, part[b], 2);
-            float ms[4];
-#pragma unroll
-            for (int b = 0; b < 4; b++) ms[b] = fabsf(part[b]);
-#pragma unroll
-            for (int o2 = 4; o2 < 32; o2 <<= 1)
-#pragma unroll
-                for (int b = 0; b < 4; b++) ms[b] = fmaxf(ms[b], __shfl_xor_sync(FULL, ms[b], o2));
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const int pi = base + 4 * b;
-                if (pi >= nq * T5_COLS) break;   // uniform across the warp
-                const int q = pi / T5_COLS, j = pi % T5_COLS;
-                float inv;
-                const float p2 = t5_scale(mx[b], inv);
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const float x0 = v[b][2 * e] * p2, x1 = v[b][2 * e + 1] * p2;
-                    const __half2 h = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(h);
-                    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-                    hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-                    lo[e] = *reinterpret_cast<const uint32_t*>(&l);
-                }
-                // k = 256q + 8 lane: core matrix (k-block 32q + lane), row j (hi) / 8 + j (lo)
-                const uint32_t o = static_cast<uint32_t>(32 * q + lane) * 256u + 16u * j;
-                *reinterpret_cast<uint4*>(bptr + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(bptr + o + 128u) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                // group sums (lanes 4g .. 4g + 3 hold group g) under their own scale
-                float sinv;
-                const float s2 = t5_scale(ms[b], sinv);
-                const float sp = part[b] * s2;
-                const __half sh = __float2half_rn(sp);
-                const __half sl = __float2half_rn(sp - __half2float(sh));
-                if ((lane & 3) == 0) {
-                    const int g = lane >> 2;
-                    const uint32_t om = static_cast<uint32_t>(q) * 512u + 16u * j + 2u * g;
-                    *reinterpret_cast<__half*>(bmptr + om) = sh;
-                    *reinterpret_cast<__half*>(bmptr + om + 128u) = sl;
-                }
-                if (lane == 0) {
-                    scl[(q * T5_COLS + j) * 2] = inv;
-                    scl[(q * T5_COLS + j) * 2 + 1] = sinv;
-                }
-            }
-        }
+        t5_build_b(reinterpret_cast<const float*>(smem + p.off_x), static_cast<long long>(nq) * T5_SB, nq, p.m, warp, 4,
+                   lane, bptr, bmptr, scl);
         fence_proxy_async();   // B is read by the tensor cores (async proxy)
     }
     tc_fence_before();

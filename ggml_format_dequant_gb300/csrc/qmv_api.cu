@@ -414,11 +414,12 @@ int qmm_q4k_tc5_plan_detail(int rows, int k, int m, const qmv_opts* cfg, const i
 }
 
 int qmm_q4k_tc5_selftest_timeout_path(const void* w, const float* x, float* y, int rows, int k, int m,
-                                      cudaStream_t stream) {
+                                      const qmv_opts* opts, cudaStream_t stream) {
     int rc = check_dense(w, x, y, rows, k, 256, 144);
     if (!rc && (m <= 0 || m > 8)) rc = QMV_EINVAL;
+    if (!rc && !opts_ok(opts)) rc = QMV_EINVAL;
     if (rc) return rc;
-    return qmvi::qmm_q4k_tc5(w, x, y, rows, k, m, nullptr, stream, 1);
+    return qmvi::qmm_q4k_tc5(w, x, y, rows, k, m, opts, stream, 1);
 }
 
 int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream) {

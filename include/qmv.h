@@ -295,14 +295,15 @@ int qmv_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
 int qmv_selftest_timeout_path(const void *w, const float *x, float *y, int rows, int k, int m,
                               cudaStream_t stream);
 
-/* The same failure-path self-test for qmm_q4k_tc5_ex (m = 1..8): every CTA's
- * decoder warps take the path of a staged copy that did not land; the CTA
- * lets its copies land (bounded), releases its tensor memory, raises
- * QMV_STATUS_WAIT_TIMEOUT and its partial sums are NaN, so every output of
- * the product is NaN. Arguments as for qmm_q4k_tc5_ex. Nothing hangs or
- * traps; the context stays usable. */
+/* The same failure-path self-test for qmm_q4k_tc5_ex (m = 1..8), in the plan
+ * `opts` selects (NULL: the cluster plan; QMV_OVERLAP_INDEPENDENT: the
+ * streaming plan where it fits): every CTA's decoder warps take the path of a
+ * staged copy that did not land; the CTA lets its copies land (bounded),
+ * releases its tensor memory, raises QMV_STATUS_WAIT_TIMEOUT and its partial
+ * sums are NaN, so every output of the product is NaN. Other arguments as for
+ * qmm_q4k_tc5_ex. Nothing hangs or traps; the context stays usable. */
 int qmm_q4k_tc5_selftest_timeout_path(const void *w, const float *x, float *y, int rows, int k, int m,
-                                      cudaStream_t stream);
+                                      const qmv_opts *opts, cudaStream_t stream);
 
 /* OR of the status bits raised on the current device since the last clear;
  * clears them when `clear` is non-zero. Waits for all work on the current
@@ -367,10 +368,14 @@ int qmm_q4k_tc5_ex(const void *w, const float *x, float *y, int rows, int k, int
 /* The plan qmm_q4k_tc5_ex takes for one launch (m = 1..8 rows of x) on a
  * described device {SM count, opt-in shared memory per CTA, shared memory per
  * SM, reserved shared memory per CTA}, computed on the host (no GPU needed):
- * out[12] = {CTAs, threads, dynamic shared memory, cluster size (k-chunks of a
+ * out[13] = {CTAs, threads, dynamic shared memory, cluster size (k-chunks of a
  * tile), ring slots, super-blocks per row, and the shared-memory offsets of
- * B, B', the scales, the staged x, the partial-sum inbox and the barriers}.
- * Returns QMV_ETOOBIG for a shape whose chunk does not fit one CTA. */
+ * B, B', the scales, the staged x, the partial-sum inbox and the barriers,
+ * and the plan's kind: 0 the cluster plan, 1 the streaming plan that
+ * independent calls (QMV_OVERLAP_INDEPENDENT, no forced cluster size) take
+ * when B for the whole of k fits one CTA -- one CTA a 128-row tile, no
+ * staged x or inbox (their offsets 0)}. Returns QMV_ETOOBIG for a shape whose
+ * chunk does not fit one CTA. */
 int qmm_q4k_tc5_plan_detail(int rows, int k, int m, const qmv_opts *opts, const int *device, int *out);
 int qmm_q6k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                 cudaStream_t stream);

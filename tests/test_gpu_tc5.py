@@ -100,10 +100,15 @@ def test_every_cluster_size_and_ring_depth(q, cluster):
 
 
 def test_launch_overlap_modes_are_bitwise_equal(q):
+    """The overlap mode only changes when a launch may start: with the plan
+    held (a forced cluster size keeps independent calls on the cluster plan)
+    every mode gives the same bits."""
     rows, k, m = 4096, 4096, 4
     w, x = case(rows, k, m, 5)
-    ys = [run(q, w, x, rows, k, m, overlap=o) for o in (q.OVERLAP_NONE, q.OVERLAP_CHAIN, q.OVERLAP_INDEPENDENT)]
+    ys = [run(q, w, x, rows, k, m, cfg={"cluster": 8}, overlap=o)
+          for o in (q.OVERLAP_NONE, q.OVERLAP_CHAIN, q.OVERLAP_INDEPENDENT)]
     assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
+    assert np.array_equal(ys[0], run(q, w, x, rows, k, m))
 
 
 def test_same_as_chained_calls_in_a_stream(q):
@@ -153,6 +158,89 @@ def test_timeout_path_marks_outputs_nan(q, rows, k, m):
     assert np.all(np.isnan(y.cpu().numpy()))
     assert q.qmv_device_status(clear=True) & q.QMV_STATUS_WAIT_TIMEOUT
     y2 = run(q, w, x, rows, k, m)
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    for i in range(m):
+        assert scale_rel(ref[i], y2[i]) <= SCALE_REL_TOL
+    assert q.qmv_device_status() == 0
+
+
+@pytest.mark.parametrize("rows,k,m", [(128, 256, 1), (300, 1024, 3), (256, 4096, 8), (4096, 4096, 2),
+                                      (4096, 2048, 5), (517, 2560, 9), (1, 512, 8), (4096, 4096, 8)])
+def test_streaming_plan_matches_oracle_and_one_chunk(q, rows, k, m):
+    """Independent calls take the streaming plan (one CTA a 128-row tile over
+    the whole of k). It issues the same MMAs and folds the super-blocks in the
+    same order as the cluster plan with one chunk a tile, so the two agree bit
+    for bit where that plan fits; both are within the tolerance of the
+    oracle."""
+    P = q.qmm_q4k_tc5_plan_detail(rows, k, min(m, 8), overlap=q.OVERLAP_INDEPENDENT)
+    assert P["streaming"] == 1
+    w, x = case(rows, k, m, 3 * rows + k + m)
+    y = run(q, w, x, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    assert not np.any(np.isnan(y))
+    for i in range(m):
+        assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, i
+    try:
+        q.qmm_q4k_tc5_plan_detail(rows, k, min(m, 8), cfg={"cluster": 1})
+        one_chunk_fits = True
+    except q.QmvError as e:
+        # the cluster plan also stages x: one chunk of k = 4096 with 8 rows
+        # of x does not fit one CTA
+        assert e.code == q.QMV_ETOOBIG
+        one_chunk_fits = False
+    if one_chunk_fits:
+        assert np.array_equal(y, run(q, w, x, rows, k, m, cfg={"cluster": 1}))
+    ys = [run(q, w, x, rows, k, m, cfg={"chunks": s}, overlap=q.OVERLAP_INDEPENDENT) for s in (1, 2, 3)]
+    for ysd in ys:
+        assert np.array_equal(ysd, y)
+    assert q.qmv_device_status() == 0
+
+
+def test_streaming_plan_unit_rows_give_weight_columns(q):
+    rows, k = 4096, 4096
+    st = synth.Stream(12)
+    w = synth.gen_q4k_rows(st, rows, k)
+    js = [5, k - 1, 300, 17, k // 2, 333, 64, 1023]
+    xu = np.zeros((8, k), dtype=np.float32)
+    for i, j in enumerate(js):
+        xu[i, j] = 1.0
+    y = run(q, w, xu, rows, k, 8, overlap=q.OVERLAP_INDEPENDENT)
+    W = oracle.dequant("q4k", w, rows, k).astype(np.float32)
+    for i, j in enumerate(js):
+        assert np.array_equal(y[i], W[:, j]), (i, j)
+
+
+def test_streaming_plan_in_a_stream_of_independent_calls(q):
+    """Twenty independent calls on one stream (each may start before the one
+    before it ends), each with its own weights, x and y."""
+    rows, k, m = 2048, 4096, 4
+    st = synth.Stream(313)
+    ws = [synth.gen_q4k_rows(st, rows, k) for _ in range(4)]
+    xs = [synth.gen_normal(st, m * k).reshape(m, k) for _ in range(5)]
+    wd = [dev(w) for w in ws]
+    xd = [dev(x) for x in xs]
+    ys = [torch.empty((m, rows), dtype=torch.float32, device="cuda") for _ in range(20)]
+    for i in range(20):
+        q.qmm_q4k_tc5(wd[i % 4], xd[i % 5], ys[i], rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
+    torch.cuda.synchronize()
+    for i in range(20):
+        ref = oracle.qmm("q4k", ws[i % 4], xs[i % 5], m, rows, k)
+        got = ys[i].cpu().numpy()
+        for j in range(m):
+            assert scale_rel(ref[j], got[j]) <= SCALE_REL_TOL, (i, j)
+    assert q.qmv_device_status() == 0
+
+
+def test_streaming_plan_timeout_path_marks_outputs_nan(q):
+    rows, k, m = 300, 2048, 8
+    w, x = case(rows, k, m, 43)
+    q.qmv_device_status(clear=True)
+    y = torch.zeros((m, rows), dtype=torch.float32, device="cuda")
+    q.qmm_q4k_tc5_selftest_timeout_path(dev(w), dev(x), y, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
+    torch.cuda.synchronize()
+    assert np.all(np.isnan(y.cpu().numpy()))
+    assert q.qmv_device_status(clear=True) & q.QMV_STATUS_WAIT_TIMEOUT
+    y2 = run(q, w, x, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
     ref = oracle.qmm("q4k", w, x, m, rows, k)
     for i in range(m):
         assert scale_rel(ref[i], y2[i]) <= SCALE_REL_TOL

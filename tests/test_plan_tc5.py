@@ -99,3 +99,37 @@ def test_default_cluster_sizes():
     assert q.qmm_q4k_tc5_plan_detail(1578, 5632, 8)["CL"] == 8
     assert q.qmm_q4k_tc5_plan_detail(1578, 5632, 8, cfg={"cluster": 6})["CL"] == 4
     assert q.qmm_q4k_tc5_plan_detail(300, 256, 2)["CL"] == 1
+
+
+def test_streaming_plans_stay_in_bounds():
+    """Independent calls take the streaming plan when B for the whole of k fits
+    one CTA (one CTA a 128-row tile, one CTA an SM); every region the kernel
+    writes fits, in order, and the plan keeps two CTAs off one SM."""
+    seen = set()
+    for k in (256, 512, 1024, 2048, 3072, 4096, 5632, 6144, 7168, 14336):
+        for rows in (1, 128, 300, 4096):
+            for m in (1, 4, 8):
+                for chunks in (0, 1, 2, 4, 8):
+                    cfg = {"chunks": chunks} if chunks else None
+                    P = q.qmm_q4k_tc5_plan_detail(rows, k, m, cfg=cfg, device=DEV, overlap=q.OVERLAP_INDEPENDENT)
+                    seen.add((k, P["streaming"]))
+                    if not P["streaming"]:
+                        continue
+                    nsb, S = k // 256, P["S"]
+                    assert P["CL"] == 1 and P["nsb"] == nsb and 1 <= S <= nsb
+                    assert P["ctas"] == -(-rows // 128) and P["threads"] == 288
+                    assert P["off_b"] >= S * SLOT and P["off_b"] % 128 == 0
+                    assert P["off_bm"] >= P["off_b"] + nsb * 32 * 256 and P["off_bm"] % 16 == 0
+                    assert P["off_sc"] >= P["off_bm"] + nsb * 512
+                    assert P["off_bars"] >= P["off_sc"] + nsb * 8 * 2 * 4 and P["off_bars"] % 8 == 0
+                    assert P["smem"] >= P["off_bars"] + 8 * (2 * S + 13)
+                    assert P["smem"] <= DEV[1] - STATIC_SMEM_MARGIN
+                    # one CTA an SM: two would not fit, so 512 tensor-memory columns are free
+                    assert 2 * (P["smem"] + DEV[3]) > DEV[2]
+                    # B descriptors of the last super-block stay in B
+                    assert (32 * nsb - 1) * 256 + 256 <= nsb * 32 * 256
+    assert (4096, 1) in seen and (14336, 0) in seen
+    # a forced cluster size keeps the cluster plan
+    assert q.qmm_q4k_tc5_plan_detail(4096, 4096, 8, cfg={"cluster": 8}, device=DEV,
+                                     overlap=q.OVERLAP_INDEPENDENT)["streaming"] == 0
+    assert q.qmm_q4k_tc5_plan_detail(4096, 4096, 8, device=DEV)["streaming"] == 0
