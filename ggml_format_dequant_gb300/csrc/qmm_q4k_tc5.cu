@@ -77,12 +77,11 @@ inline int make_t5_plan(const DevInfo& di, int rows, int k, int m, const qmv_opt
 constexpr long long T5S_MIN_SMEM = 120 * 1024;
 
 // The streaming plan (independent calls): one CTA a 128-row tile for the
-// whole of k; B for the whole of k in shared memory, so rows of up to a few
-// thousand weights (QMV_ETOOBIG beyond).
+// whole of k, with rings of weight copies, of B, and of the rows' d / dmin.
 inline int make_t5s_plan(const DevInfo& di, int rows, int k, int m, const qmv_opts* cfg, T5SParams* tp, Plan* pl) {
     if (rows <= 0 || k <= 0 || k % T5_SB || m < 1 || m > T5_COLS) return QMV_EINVAL;
     const int nsb = k / T5_SB;
-    int S = (cfg && cfg->chunks > 0) ? cfg->chunks : 4;
+    int S = (cfg && cfg->chunks > 0) ? cfg->chunks : 6;
     S = std::max(1, std::min(S, nsb));
     const uint32_t slot = static_cast<uint32_t>(T5_ROWS * T5_SBBYTES);
     const long long limit = di.smem_optin - T5_STATIC_SMEM;
@@ -91,13 +90,15 @@ inline int make_t5s_plan(const DevInfo& di, int rows, int k, int m, const qmv_op
         long long off = static_cast<long long>(S) * slot;
         tp->off_ring = 0;
         tp->off_b = static_cast<uint32_t>(round_up(off, 128));
-        off = tp->off_b + static_cast<long long>(nsb) * 32 * 256;
+        off = tp->off_b + static_cast<long long>(T5S_SB) * T5S_BSLOT;
         tp->off_bm = static_cast<uint32_t>(round_up(off, 128));
-        off = tp->off_bm + static_cast<long long>(nsb) * 512;
+        off = tp->off_bm + static_cast<long long>(T5S_SB) * T5S_BMSLOT;
         tp->off_sc = static_cast<uint32_t>(round_up(off, 16));
-        off = tp->off_sc + static_cast<long long>(nsb) * T5_COLS * 2 * 4;
+        off = tp->off_sc + static_cast<long long>(T5S_SB) * T5_COLS * 2 * 4;
+        tp->off_dm = static_cast<uint32_t>(round_up(off, 16));
+        off = tp->off_dm + static_cast<long long>(T5S_SD) * T5_ROWS * 8;
         tp->off_bars = static_cast<uint32_t>(round_up(off, 8));
-        off = tp->off_bars + 8LL * (2 * S + 13);
+        off = tp->off_bars + 8LL * (2 * S + T5S_NBARS_FIXED);
         smem = std::max(round_up(off, 128), T5S_MIN_SMEM);
         if (smem <= limit) break;
         if (S == 1) return QMV_ETOOBIG;
@@ -119,8 +120,7 @@ inline int make_t5s_plan(const DevInfo& di, int rows, int k, int m, const qmv_op
     return QMV_OK;
 }
 
-// Independent calls whose B fits take the streaming plan, unless a cluster
-// size is forced.
+// Independent calls take the streaming plan, unless a cluster size is forced.
 inline bool t5_streams(const qmv_opts* cfg) {
     return overlap_of(cfg) == QMV_OVERLAP_INDEPENDENT && !(cfg && cfg->cluster > 0);
 }
@@ -274,8 +274,8 @@ int qmm_q4k_tc5_plan(const int* device, int rows, int k, int m, const qmv_opts* 
         Plan spl;
         if (make_t5s_plan(di, rows, k, m, cfg, &sp, &spl) == QMV_OK) {
             const int v[13] = {spl.parts, spl.T, static_cast<int>(spl.smem), 1, sp.S, sp.nsb,
-                               static_cast<int>(sp.off_b), static_cast<int>(sp.off_bm), static_cast<int>(sp.off_sc), 0,
-                               0, static_cast<int>(sp.off_bars), 1};
+                               static_cast<int>(sp.off_b), static_cast<int>(sp.off_bm), static_cast<int>(sp.off_sc),
+                               static_cast<int>(sp.off_dm), 0, static_cast<int>(sp.off_bars), 1};
             for (int i = 0; i < 13; i++) out[i] = v[i];
             return QMV_OK;
         }

@@ -1,59 +1,165 @@
 // qmm_tc5s.cuh -- the streaming form of the fifth-generation tensor-core batch
 // kernel (qmm_tc5.cuh), for streams of independent calls: one CTA an SM owns
 // a 128-row tile for the whole of k, so there is no cross-CTA reduction and
-// the CTA's fixed costs (tensor-memory allocation, barrier set-up, building
-// B) are paid once per tile instead of once per k-chunk.
+// the CTA's fixed costs (tensor-memory allocation, barrier set-up) are paid
+// once per tile instead of once per k-chunk.
 //
-//  * B (x as hi / lo f16 parts, and B' the group sums) is built once, for the
-//    whole of k, from x in global memory by the decoder warps, while the
-//    first weight copies land. It takes k x 32 bytes of shared memory, so the
-//    plan is made for rows of up to a few thousand weights (Q4_K 4096).
-//  * Eight decoder warps, two a lane quarter: warp w decodes half hh = w / 4
-//    of every super-block (sub-blocks 4hh .. 4hh+3) for rows 32 (w % 4) .. +31.
-//    Each half's A operand is double-buffered in tensor memory, so a warp
-//    decodes super-block q + 1 while the MMAs of q run.
-//  * One thread of a ninth warp issues the TMA copies and the MMAs, as in
-//    qmm_tc5.cuh. The accumulators alternate between two pairs; decoder warp w
-//    reads back the columns of rows j = 4hh .. 4hh+3 of x and writes them.
-//  * Every wait is bounded; a wait that gives up marks the CTA's outputs NaN
-//    and sets STATUS_WAIT_TIMEOUT. Tensor memory (512 columns) is allocated
-//    and released by the issuing warp; the shared memory the plan asks for
-//    keeps one CTA an SM, so the allocation never waits.
+// The warps have one role each, and each role waits only on the stage that
+// feeds it, so that one super-block's latencies (weight copy, decode, MMA,
+// read-back) overlap the neighbouring super-blocks' instead of adding up:
+//  * warps 0..7 decode: warp w decodes half hh = w / 4 of every super-block
+//    (sub-blocks 4hh .. 4hh+3) of rows 32 (w % 4) .. +31 into the A operand
+//    in tensor memory, double-buffered per half; warps 0..3 also pass each
+//    row's d and dmin to the read-back through a shared-memory ring;
+//  * warp 8 (one thread) issues the MMAs of each super-block into one of ND
+//    accumulator pairs (D, and D' for the min term);
+//  * warps 9..12 read back and fold each super-block's accumulators for
+//    their lane quarter of rows;
+//  * warp 13 (one thread) keeps the ring of S weight copies (2-D TMA) full,
+//    refilling a slot as soon as every decoder has read it;
+//  * warps 14..17 build B and B' (x as hi / lo f16 parts, and the group sums)
+//    into a ring of SB super-blocks, as far ahead as the ring allows, from x
+//    prefetched into registers a super-block earlier.
+// B no longer spans k, so any k fits. Every wait is bounded; a wait that gives
+// up marks the CTA's outputs NaN and sets STATUS_WAIT_TIMEOUT. Tensor memory
+// (512 columns) is allocated and released by warp 8; the shared memory the
+// plan asks for keeps one CTA an SM, so the allocation never waits.
 #pragma once
 
 #include "qmm_tc5.cuh"
 
 namespace qmv {
 
-constexpr int T5S_DECODERS = 8;                        // decoder warps
-constexpr int T5S_THREADS = 32 * (T5S_DECODERS + 1);   // and the issuing warp
+constexpr int T5S_DECODERS = 8;                         // decoder warps 0..7
+constexpr int T5S_ISSUER = 8;                           // MMA-issuing warp
+constexpr int T5S_EPI0 = 9;                             // read-back warps 9..12
+constexpr int T5S_PRODUCER = 13;                        // weight-copy warp
+constexpr int T5S_BUILD0 = 14;                          // B-building warps 14..17
+constexpr int T5S_THREADS = 32 * 18;
 constexpr int T5S_TMEM_COLS = 512;
+constexpr int T5S_SB = 4;   // B ring
+constexpr int T5S_ND = 4;   // accumulator pairs (at least SB: see the builders)
+constexpr int T5S_SD = 8;   // d / dmin ring (at least ND + 2 deep: see the decoders)
+constexpr uint32_t T5S_BSLOT = 32u * 256u;   // one super-block of B: 32 k-blocks x 16 rows x 16 bytes
+constexpr uint32_t T5S_BMSLOT = 512u;        // one super-block of B': two k-blocks, the second zeros
+constexpr int T5S_NBARS_FIXED = 4 + 4 + T5S_SB + T5S_SD + 2 * T5S_ND + 1;
+static_assert(T5S_SB <= T5S_ND, "a builder waits for the accumulators of q - SB to be released");
+
 // Tensor-memory columns: A operand [half][buffer] (64 columns each), the
-// min-term operand [buffer] (8 used of 16), accumulators D and D' [buffer].
+// min-term operand [buffer] (8 used of 16), accumulators D [ND] and D' [ND].
 __host__ __device__ constexpr uint32_t t5s_col_a(int h, int b) {
     return 64u * static_cast<uint32_t>(2 * h + b);
 }
 __host__ __device__ constexpr uint32_t t5s_col_am(int b) { return 256u + 16u * static_cast<uint32_t>(b); }
 __host__ __device__ constexpr uint32_t t5s_col_d(int b) { return 288u + 16u * static_cast<uint32_t>(b); }
-__host__ __device__ constexpr uint32_t t5s_col_dm(int b) { return 320u + 16u * static_cast<uint32_t>(b); }
+__host__ __device__ constexpr uint32_t t5s_col_dm(int b) {
+    return 288u + 16u * static_cast<uint32_t>(T5S_ND + b);
+}
+static_assert(t5s_col_dm(T5S_ND - 1) + 16u <= static_cast<uint32_t>(T5S_TMEM_COLS), "tensor-memory columns");
 
 struct T5SParams {
     const float* x;       // [m, k]
     float* y;             // [m, rows]
     int rows, k, m;
     int nsb;              // super-blocks per row
-    int S;                // ring slots
+    int S;                // weight ring slots
     int early_inputs;     // x read before waiting for the previous kernel (only y waits)
     int force_timeout;    // failure-path test
     uint32_t slot_bytes;  // 128 rows x 144 bytes
-    uint32_t off_ring, off_b, off_bm, off_sc, off_bars;
+    uint32_t off_ring, off_b, off_bm, off_sc, off_dm, off_bars;
 };
 
-__device__ __forceinline__ void tmem_ld4(uint32_t t, uint32_t (&r)[4]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(t)
-                 : "memory");
+// Barriers, in order: full[S], empty[S], afull[4], afree[4], bfull[SB],
+// hfull[SD], dfull[ND], dfree[ND], fin (8 bytes each).
+struct T5SBars {
+    uint32_t full0, empty0, afull0, afree0, bfull0, hfull0, dfull0, dfree0, fin;
+    __device__ __forceinline__ explicit T5SBars(uint32_t bars, int S) {
+        full0 = bars;
+        empty0 = full0 + 8u * S;
+        afull0 = empty0 + 8u * S;
+        afree0 = afull0 + 32u;
+        bfull0 = afree0 + 32u;
+        hfull0 = bfull0 + 8u * T5S_SB;
+        dfull0 = hfull0 + 8u * T5S_SD;
+        dfree0 = dfull0 + 8u * T5S_ND;
+        fin = dfree0 + 8u * T5S_ND;
+    }
+};
+
+// This lane's 8 values of row j of x in super-block q (k = 256 q + 8 lane ..).
+__device__ __forceinline__ void t5s_load_x(const float* x, int k, int q, int j, int lane, float (&v)[8]) {
+    const float4* src = reinterpret_cast<const float4*>(x + static_cast<long long>(j) * k + q * T5_SB + 8 * lane);
+    const float4 a = src[0], c4 = src[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = c4.x; v[5] = c4.y; v[6] = c4.z; v[7] = c4.w;
+}
+
+// B and B' of rows j0 and j1 of x for one super-block (its slot at bptr /
+// bmptr, scales at scl[2 j + {0, 1}]), from the lanes' 8 values each: the
+// arithmetic of t5_build_b, two pairs interleaved; row `j1` < 0 is skipped.
+__device__ __forceinline__ void t5s_convert2(const float (&v)[2][8], int j0, int j1, int lane, uint8_t* bptr,
+                                             uint8_t* bmptr, float* scl) {
+    float mx[2], part[2], ms[2];
+#pragma unroll
+    for (int b = 0; b < 2; b++) {
+        mx[b] = 0.0f;
+        part[b] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            mx[b] = fmaxf(mx[b], fabsf(v[b][e]));
+            part[b] += v[b][e];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int b = 0; b < 2; b++) mx[b] = fmaxf(mx[b], __shfl_xor_sync(FULL, mx[b], o));
+#pragma unroll
+    for (int b = 0; b < 2; b++) part[b] += __shfl_xor_sync(FULL, part[b], 1);
+#pragma unroll
+    for (int b = 0; b < 2; b++) part[b] += __shfl_xor_sync(FULL, part[b], 2);
+#pragma unroll
+    for (int b = 0; b < 2; b++) ms[b] = fabsf(part[b]);
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1)
+#pragma unroll
+        for (int b = 0; b < 2; b++) ms[b] = fmaxf(ms[b], __shfl_xor_sync(FULL, ms[b], o2));
+#pragma unroll
+    for (int b = 0; b < 2; b++) {
+        const int j = b ? j1 : j0;
+        if (j < 0) break;   // uniform across the warp
+        float inv;
+        const float p2 = t5_scale(mx[b], inv);
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float x0 = v[b][2 * e] * p2, x1 = v[b][2 * e + 1] * p2;
+            const __half2 h = __floats2half2_rn(x0, x1);
+            const float2 hf = __half22float2(h);
+            const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+            hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+        // k = 8 lane ..: core matrix (k-block lane), row j (hi) / 8 + j (lo)
+        const uint32_t o = static_cast<uint32_t>(lane) * 256u + 16u * j;
+        *reinterpret_cast<uint4*>(bptr + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(bptr + o + 128u) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        // group sums (lanes 4g .. 4g + 3 hold group g) under their own scale
+        float sinv;
+        const float s2 = t5_scale(ms[b], sinv);
+        const float sp = part[b] * s2;
+        const __half sh = __float2half_rn(sp);
+        const __half sl = __float2half_rn(sp - __half2float(sh));
+        if ((lane & 3) == 0) {
+            const uint32_t om = 16u * j + 2u * static_cast<uint32_t>(lane >> 2);
+            *reinterpret_cast<__half*>(bmptr + om) = sh;
+            *reinterpret_cast<__half*>(bmptr + om + 128u) = sl;
+        }
+        if (lane == 0) {
+            scl[2 * j] = inv;
+            scl[2 * j + 1] = sinv;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(T5S_THREADS, 1)
@@ -68,37 +174,32 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
     const int nq = p.nsb;
     const uint32_t sb = smem_u32(smem);
     const uint32_t ring = sb + p.off_ring;
-    const uint32_t bars = sb + p.off_bars;
-    // barriers: full[S], empty[S], afull[half][buffer], afree[half][buffer], dfull[2], dfree[2], fin
-    const uint32_t full0 = bars, empty0 = bars + 8u * p.S, afull0 = bars + 16u * p.S;
-    const uint32_t afree0 = afull0 + 32u, dfull0 = afull0 + 64u, dfree0 = afull0 + 80u, fin = afull0 + 96u;
+    const T5SBars B(sb + p.off_bars, p.S);
+    float yacc[T5_COLS];   // the read-back warps' row sums
+#pragma unroll
+    for (int j = 0; j < T5_COLS; j++) yacc[j] = 0.0f;
 
     pdl_launch_dependents();
 
-    if (warp == T5S_DECODERS) {
+    if (warp == T5S_ISSUER) {
         if (lane == 0) {
             for (int s = 0; s < p.S; s++) {
-                mbar_init(full0 + 8u * s, 1);
-                mbar_init(empty0 + 8u * s, 32 * T5S_DECODERS);
+                mbar_init(B.full0 + 8u * s, 1);
+                mbar_init(B.empty0 + 8u * s, 32 * T5S_DECODERS);
             }
             for (int i = 0; i < 4; i++) {
-                mbar_init(afull0 + 8u * i, 32 * T5S_DECODERS / 2);
-                mbar_init(afree0 + 8u * i, 1);
+                mbar_init(B.afull0 + 8u * i, 32 * T5S_DECODERS / 2);
+                mbar_init(B.afree0 + 8u * i, 1);
             }
-            for (int b = 0; b < 2; b++) {
-                mbar_init(dfull0 + 8u * b, 1);
-                mbar_init(dfree0 + 8u * b, 32 * T5S_DECODERS);
+            for (int i = 0; i < T5S_SB; i++) mbar_init(B.bfull0 + 8u * i, 128);
+            for (int i = 0; i < T5S_SD; i++) mbar_init(B.hfull0 + 8u * i, 128);
+            for (int i = 0; i < T5S_ND; i++) {
+                mbar_init(B.dfull0 + 8u * i, 1);
+                mbar_init(B.dfree0 + 8u * i, 128);
             }
-            mbar_init(fin, 1);
+            mbar_init(B.fin, 1);
             s_tmo = 0;
             fence_mbar_init();
-            // the weights are constant: the first slots are requested at once
-            const int first = nq < p.S ? nq : p.S;
-            for (int i = 0; i < first; i++) {
-                mbar_arrive_expect_tx(full0 + 8u * i, p.slot_bytes);
-                tma_load_2d(ring + static_cast<uint32_t>(i) * p.slot_bytes, &wmap, i * (T5_SBBYTES / 8), row0,
-                            full0 + 8u * i);
-            }
         }
         __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
@@ -107,110 +208,104 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     // every barrier is initialized (and the tensor-memory address written)
-    // before any thread waits on one
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // x may come from the kernel just before, unless the caller declared it
-    // independent of it
-    if (!p.early_inputs) pdl_dependency_wait();
-
-    // ---- B and B' for the whole of k, by the decoder warps, from x in global
-    // memory (while the first weight copies land)
-    float* scl = reinterpret_cast<float*>(smem + p.off_sc);
-    if (warp < T5S_DECODERS) {
-        t5_build_b(p.x, p.k, nq, p.m, warp, T5S_DECODERS, lane, smem + p.off_b, smem + p.off_bm, scl);
-        fence_proxy_async();   // B is read by the tensor cores (async proxy)
-    }
+    // before any thread uses one
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     volatile int* tmo = &s_tmo;
+    // x may come from the kernel just before, unless the caller declared it
+    // independent of it
+    if (!p.early_inputs) pdl_dependency_wait();
 
-    if (warp == T5S_DECODERS) {
-        // ---- the issuing thread: per super-block, the MMAs of its two halves
-        // (each in the buffer of its parity) and the min term, then the refill
-        // of the ring slot every row has read
-        int next = p.S < nq ? p.S : nq;   // next super-block to request
+    if (warp == T5S_PRODUCER) {
+        // ---- the weight copies: the weights are constant, so the first S
+        // are requested at once; then each slot is refilled as soon as every
+        // decoder has read it
+        if (lane == 0) {
+            const int first = nq < p.S ? nq : p.S;
+            int next = 0;
+            for (; next < first; next++) {
+                mbar_arrive_expect_tx(B.full0 + 8u * next, p.slot_bytes);
+                tma_load_2d(ring + static_cast<uint32_t>(next) * p.slot_bytes, &wmap, next * (T5_SBBYTES / 8), row0,
+                            B.full0 + 8u * next);
+            }
+            if (!p.force_timeout) {
+                for (; next < nq; next++) {
+                    const int q = next - p.S, s = q % p.S;   // the slot super-block q used
+                    if (!mbar_wait_bounded(B.empty0 + 8u * s, static_cast<uint32_t>((q / p.S) & 1))) {
+                        atomicExch(const_cast<int*>(tmo), 1);
+                        break;
+                    }
+                    fence_proxy_async();
+                    mbar_arrive_expect_tx(B.full0 + 8u * s, p.slot_bytes);
+                    tma_load_2d(ring + static_cast<uint32_t>(s) * p.slot_bytes, &wmap, next * (T5_SBBYTES / 8), row0,
+                                B.full0 + 8u * s);
+                }
+            }
+            // every copy requested lands before the CTA ends (a failed run
+            // leaves the last S unread)
+            for (int i = next - p.S > 0 ? next - p.S : 0; i < next; i++)
+                if (!mbar_wait_bounded(B.full0 + 8u * (i % p.S), static_cast<uint32_t>((i / p.S) & 1))) break;
+        }
+        __syncwarp();
+    } else if (warp == T5S_ISSUER) {
+        // ---- the MMAs: per super-block, once its B is built and an
+        // accumulator pair is free, the 8 steps of each half (in the A
+        // buffer of the super-block's parity) and the min term
         if (lane == 0 && !p.force_timeout) {
             const uint32_t bbase = sb + p.off_b, bmbase = sb + p.off_bm;
             bool ok = true;
             for (int q = 0; q < nq && ok; q++) {
-                const int db = q & 1, ab = q & 1;
-                if (q >= 2 && !mbar_wait_bounded(dfree0 + 8u * db, static_cast<uint32_t>(((q - 2) >> 1) & 1))) {
+                const int bs = q % T5S_SB, db = q % T5S_ND, ab = q & 1;
+                if (!mbar_wait_bounded(B.bfull0 + 8u * bs, static_cast<uint32_t>((q / T5S_SB) & 1)) ||
+                    (q >= T5S_ND &&
+                     !mbar_wait_bounded(B.dfree0 + 8u * db, static_cast<uint32_t>(((q - T5S_ND) / T5S_ND) & 1)))) {
                     ok = false;
                     break;
                 }
+                const uint32_t bq = bbase + static_cast<uint32_t>(bs) * T5S_BSLOT;
                 for (int h = 0; h < 2; h++) {
                     const uint32_t ai = static_cast<uint32_t>(2 * h + ab);
-                    if (!mbar_wait_bounded(afull0 + 8u * ai, static_cast<uint32_t>((q >> 1) & 1))) {
+                    if (!mbar_wait_bounded(B.afull0 + 8u * ai, static_cast<uint32_t>((q >> 1) & 1))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int t = 0; t < 8; t++) {
-                        const uint32_t kb = static_cast<uint32_t>(32 * q + 16 * h + 2 * t);   // first k-block of the step
+                        const uint32_t kb = static_cast<uint32_t>(16 * h + 2 * t);   // first k-block of the step
                         mma_f16_ts(tmem + t5s_col_d(db), tmem + t5s_col_a(h, ab) + 8u * t,
-                                   smem_desc(bbase + kb * 256u, 256u, 128u), T5_IDESC, h > 0 || t > 0);
+                                   smem_desc(bq + kb * 256u, 256u, 128u), T5_IDESC, h > 0 || t > 0);
                     }
                     if (h == 1)
                         mma_f16_ts(tmem + t5s_col_dm(db), tmem + t5s_col_am(ab),
-                                   smem_desc(bmbase + static_cast<uint32_t>(q) * 512u, 256u, 128u), T5_IDESC, false);
-                    mma_commit(afree0 + 8u * ai);
+                                   smem_desc(bmbase + static_cast<uint32_t>(bs) * T5S_BMSLOT, 256u, 128u), T5_IDESC,
+                                   false);
+                    mma_commit(B.afree0 + 8u * ai);
                 }
                 if (!ok) break;
-                mma_commit(dfull0 + 8u * db);
-                if (next < nq) {
-                    const int s = q % p.S;
-                    if (!mbar_wait_bounded(empty0 + 8u * s, static_cast<uint32_t>((q / p.S) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async();
-                    mbar_arrive_expect_tx(full0 + 8u * s, p.slot_bytes);
-                    tma_load_2d(ring + static_cast<uint32_t>(s) * p.slot_bytes, &wmap, next * (T5_SBBYTES / 8), row0,
-                                full0 + 8u * s);
-                    next++;
-                }
+                mma_commit(B.dfull0 + 8u * db);
             }
             if (!ok) atomicExch(const_cast<int*>(tmo), 1);
             // every MMA issued is complete before tensor memory is released
-            mma_commit(fin);
-            if (!mbar_wait_bounded(fin, 0u)) atomicExch(const_cast<int*>(tmo), 1);
-            // copies still in flight (a failed run) land before the CTA ends
-            for (int i = next - p.S > 0 ? next - p.S : 0; i < next; i++)
-                if (!mbar_wait_bounded(full0 + 8u * (i % p.S), static_cast<uint32_t>((i / p.S) & 1))) break;
-        } else if (lane == 0) {
-            // failure-path test: no MMA issued; the copies still land
-            for (int i = 0; i < next; i++)
-                if (!mbar_wait_bounded(full0 + 8u * i, 0u)) break;
+            mma_commit(B.fin);
+            if (!mbar_wait_bounded(B.fin, 0u)) atomicExch(const_cast<int*>(tmo), 1);
         }
         __syncwarp();
-        __syncthreads();   // every decoder is done with tensor memory
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T5S_TMEM_COLS)
-                     : "memory");
-        return;
-    }
-
-    // ---- decoder warps: half hh of every super-block of row r of the tile,
-    // and the read-back of rows j = 4hh .. 4hh+3 of x
-    const int lq = warp & 3, hh = warp >> 2;
-    const int r = 32 * lq + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * lq) << 16;
-    float yacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    float dprev = 0.0f, mprev = 0.0f;   // d and dmin of the super-block read back next
-    bool ok = !p.force_timeout;
-    const uint32_t K1024 = 0x64006400u;   // f16x2 (1024, 1024)
-    for (int q = 0; q <= nq && ok; q++) {
-        float dcur = 0.0f, mcur = 0.0f;
-        if (q < nq) {
+    } else if (warp < T5S_DECODERS) {
+        // ---- decoders: half hh of every super-block of row r of the tile
+        const int lq = warp & 3, hh = warp >> 2;
+        const int r = 32 * lq + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * lq) << 16;
+        float2* dmr = reinterpret_cast<float2*>(smem + p.off_dm);
+        bool ok = !p.force_timeout;
+        const uint32_t K1024 = 0x64006400u;   // f16x2 (1024, 1024)
+        for (int q = 0; q < nq && ok; q++) {
             const int s = q % p.S;
             // (every decision a warp takes is a vote: the tensor-memory
             // instructions below are warp-collective)
-            if (!__all_sync(FULL, mbar_wait_bounded(full0 + 8u * s, static_cast<uint32_t>((q / p.S) & 1)) &&
+            if (!__all_sync(FULL, mbar_wait_bounded(B.full0 + 8u * s, static_cast<uint32_t>((q / p.S) & 1)) &&
                                       *tmo == 0)) {
                 ok = false;
                 break;
@@ -223,22 +318,24 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
                 const uint4 v = lds128<0>(a + 16u + 64u * static_cast<uint32_t>(hh) + 16u * i);
                 qs[4 * i] = v.x; qs[4 * i + 1] = v.y; qs[4 * i + 2] = v.z; qs[4 * i + 3] = v.w;
             }
-            mbar_arrive(empty0 + 8u * s);   // this row's half is done with the slot
-            {
-                const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
-                dcur = dd.x;
-                mcur = dd.y;
-            }
-            // the 6-bit scales of sub-blocks 4hh .. 4hh+3, one per byte
-            const uint32_t scw = hh ? ((hd.w & 0x0f0f0f0fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3f3f3f3fu);
+            mbar_arrive(B.empty0 + 8u * s);   // this row's half is done with the slot
             const int ab = q & 1;
             const uint32_t ai = static_cast<uint32_t>(2 * hh + ab);
+            // the A buffer of this parity is free once the MMAs of q - 2 are
+            // done; so are the accumulators of q - 2 - ND and, with them, the
+            // read-back's use of the d / dmin slot written here (SD >= ND + 2)
             if (q >= 2 &&
-                !__all_sync(FULL, mbar_wait_bounded(afree0 + 8u * ai, static_cast<uint32_t>(((q - 2) >> 1) & 1)))) {
+                !__all_sync(FULL, mbar_wait_bounded(B.afree0 + 8u * ai, static_cast<uint32_t>(((q - 2) >> 1) & 1)))) {
                 ok = false;
                 break;
             }
+            if (hh == 0) {
+                dmr[(q % T5S_SD) * T5_ROWS + r] = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
+                mbar_arrive(B.hfull0 + 8u * (q % T5S_SD));
+            }
             tc_fence_after();
+            // the 6-bit scales of sub-blocks 4hh .. 4hh+3, one per byte
+            const uint32_t scw = hh ? ((hd.w & 0x0f0f0f0fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3f3f3f3fu);
             const uint32_t acol = tmem + lane_base + t5s_col_a(hh, ab);
 #pragma unroll
             for (int gg = 0; gg < 4; gg++) {
@@ -270,57 +367,131 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(afull0 + 8u * ai);
+            mbar_arrive(B.afull0 + 8u * ai);
         }
-        if (q >= 1) {
-            // read back super-block q - 1: columns 4hh .. 4hh+3 (hi) and 8 + the
-            // same (lo) of both accumulators
-            const int qb = q - 1, db = qb & 1;
-            if (!__all_sync(FULL, mbar_wait_bounded(dfull0 + 8u * db, static_cast<uint32_t>((qb >> 1) & 1)))) {
+        if (!ok) atomicExch(const_cast<int*>(tmo), 1);
+    } else if (warp >= T5S_BUILD0) {
+        // ---- warps 14..17: B of rows ew and ew + 4 of x, super-block after
+        // super-block. B(qb) takes the slot and the scales of qb - SB: both
+        // are free once the accumulators of qb - SB are released (their MMAs
+        // are done, and the read-back has read the scales).
+        const int ew = warp - T5S_BUILD0;
+        uint8_t* bring = smem + p.off_b;
+        uint8_t* bmring = smem + p.off_bm;
+        float* scr = reinterpret_cast<float*>(smem + p.off_sc);
+        const int j0 = ew < p.m ? ew : -1;
+        const int j1 = ew + 4 < p.m ? ew + 4 : -1;
+        bool ok = !p.force_timeout;
+        // x of the super-block built next and of the one after, in two
+        // register sets used in turn (a copy from one set to the other would
+        // wait for the loads in flight)
+        float xa[2][8] = {}, xb[2][8] = {};
+        auto load = [&](int qq, float(&v)[2][8]) {
+            if (j0 >= 0) t5s_load_x(p.x, p.k, qq, j0, lane, v[0]);
+            if (j1 >= 0) t5s_load_x(p.x, p.k, qq, j1, lane, v[1]);
+        };
+        auto step = [&](int qb, const float(&cur)[2][8], float(&nxt)[2][8]) -> bool {
+            if (qb >= T5S_SB) {
+                // (no phase is skipped: the accumulators of qb - SB + ND
+                // cannot be released before B(qb) exists, and SB <= ND)
+                const int qo = qb - T5S_SB;
+                if (!__all_sync(FULL, mbar_wait_bounded(B.dfree0 + 8u * (qo % T5S_ND),
+                                                        static_cast<uint32_t>((qo / T5S_ND) & 1)) &&
+                                          *tmo == 0))
+                    return false;
+            }
+            if (qb + 1 < nq) load(qb + 1, nxt);
+            const int bs = qb % T5S_SB;
+            if (j0 >= 0)
+                t5s_convert2(cur, j0, j1, lane, bring + bs * T5S_BSLOT, bmring + bs * T5S_BMSLOT,
+                             scr + bs * 2 * T5_COLS);
+            fence_proxy_async();   // B is read by the tensor cores (async proxy)
+            mbar_arrive(B.bfull0 + 8u * bs);
+            return true;
+        };
+        if (ok) {
+            // the second k-block of every B' slot is zeros (the rows of the
+            // first that belong to rows j >= m of x stay unwritten: they reach
+            // only columns of D' that are not read)
+            for (int i = ew * 32 + lane; i < T5S_SB * 64; i += 128)
+                reinterpret_cast<uint32_t*>(bmring)[(i >> 6) * 128 + 64 + (i & 63)] = 0u;
+            load(0, xa);
+        }
+        for (int qb = 0; qb < nq && ok; qb += 2) {
+            ok = step(qb, xa, xb);
+            if (ok && qb + 1 < nq) ok = step(qb + 1, xb, xa);
+        }
+        if (!ok) atomicExch(const_cast<int*>(tmo), 1);
+    } else {
+        // ---- warps 9..12: the read-back and fold of every super-block for
+        // lane quarter warp % 4 of the rows
+        const int lq = warp & 3;
+        const int r = 32 * lq + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * lq) << 16;
+        const float* scr = reinterpret_cast<const float*>(smem + p.off_sc);
+        const float2* dmr = reinterpret_cast<const float2*>(smem + p.off_dm);
+        bool ok = !p.force_timeout;
+        for (int q = 0; q < nq && ok; q++) {
+            const int db = q % T5S_ND, hs = q % T5S_SD, bs = q % T5S_SB;
+            // the accumulators, the rows' d / dmin, and (long done) the
+            // scales of B(q)
+            if (!__all_sync(FULL, mbar_wait_bounded(B.dfull0 + 8u * db, static_cast<uint32_t>((q / T5S_ND) & 1)) &&
+                                      mbar_wait_bounded(B.hfull0 + 8u * hs, static_cast<uint32_t>((q / T5S_SD) & 1)) &&
+                                      mbar_wait_bounded(B.bfull0 + 8u * bs, static_cast<uint32_t>((q / T5S_SB) & 1)) &&
+                                      *tmo == 0)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t dh[4], dl[4], mh[4], ml[4];
-            const uint32_t cj = 4u * static_cast<uint32_t>(hh);
-            tmem_ld4(tmem + lane_base + t5s_col_d(db) + cj, dh);
-            tmem_ld4(tmem + lane_base + t5s_col_d(db) + 8u + cj, dl);
-            tmem_ld4(tmem + lane_base + t5s_col_dm(db) + cj, mh);
-            tmem_ld4(tmem + lane_base + t5s_col_dm(db) + 8u + cj, ml);
+            uint32_t dv[16], mv[16];
+            tmem_ld16(tmem + lane_base + t5s_col_d(db), dv);
+            tmem_ld16(tmem + lane_base + t5s_col_dm(db), mv);
+            const float2 dd = dmr[hs * T5_ROWS + r];
+            float sq[2 * T5_COLS];
+#pragma unroll
+            for (int i = 0; i < T5_COLS / 2; i++) {
+                const float4 v = reinterpret_cast<const float4*>(scr + bs * 2 * T5_COLS)[i];
+                sq[4 * i] = v.x; sq[4 * i + 1] = v.y; sq[4 * i + 2] = v.z; sq[4 * i + 3] = v.w;
+            }
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(dfree0 + 8u * db);
-            const float* sq = scl + qb * T5_COLS * 2;
+            // the accumulators, and with them B(q)'s slot and scales, are free
+            mbar_arrive(B.dfree0 + 8u * db);
 #pragma unroll
-            for (int jj = 0; jj < 4; jj++) {
-                const int j = 4 * hh + jj;
+            for (int j = 0; j < T5_COLS; j++) {
                 if (j < p.m) {
-                    const float t = dprev * (__uint_as_float(dh[jj]) + __uint_as_float(dl[jj]));
-                    const float u = mprev * (__uint_as_float(mh[jj]) + __uint_as_float(ml[jj]));
-                    yacc[jj] = __fmaf_rn(t, sq[2 * j], yacc[jj]);
-                    yacc[jj] = __fmaf_rn(-u, sq[2 * j + 1], yacc[jj]);
+                    const float t = dd.x * (__uint_as_float(dv[j]) + __uint_as_float(dv[8 + j]));
+                    const float u = dd.y * (__uint_as_float(mv[j]) + __uint_as_float(mv[8 + j]));
+                    yacc[j] = __fmaf_rn(t, sq[2 * j], yacc[j]);
+                    yacc[j] = __fmaf_rn(-u, sq[2 * j + 1], yacc[j]);
                 }
             }
         }
-        dprev = dcur;
-        mprev = mcur;
+        if (!ok) atomicExch(const_cast<int*>(tmo), 1);
     }
-    if (!ok) atomicExch(const_cast<int*>(tmo), 1);
+
+    // every role is done: tensor memory is released, and the rows written
     tc_fence_before();
-    __syncthreads();   // with the issuing warp: tensor memory is released after this
+    __syncthreads();
+    if (warp == T5S_ISSUER) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T5S_TMEM_COLS)
+                     : "memory");
+        return;
+    }
+    if (warp < T5S_EPI0 || warp >= T5S_EPI0 + 4) return;
     if (*tmo) {
 #pragma unroll
-        for (int jj = 0; jj < 4; jj++) yacc[jj] = __int_as_float(0x7fc00000);
-        if (tid == 0) atomicOr(&g_status, STATUS_WAIT_TIMEOUT);
+        for (int j = 0; j < T5_COLS; j++) yacc[j] = __int_as_float(0x7fc00000);
+        if (warp == T5S_EPI0 && lane == 0) atomicOr(&g_status, STATUS_WAIT_TIMEOUT);
     }
     // y after the previous kernel is done with it
     if (p.early_inputs) pdl_dependency_wait();
+    const int r = 32 * (warp & 3) + lane;
     if (row0 + r < p.rows) {
 #pragma unroll
-        for (int jj = 0; jj < 4; jj++) {
-            const int j = 4 * hh + jj;
-            if (j < p.m) p.y[static_cast<long long>(j) * p.rows + row0 + r] = yacc[jj];
-        }
+        for (int j = 0; j < T5_COLS; j++)
+            if (j < p.m) p.y[static_cast<long long>(j) * p.rows + row0 + r] = yacc[j];
     }
 }
 

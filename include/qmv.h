@@ -372,10 +372,12 @@ int qmm_q4k_tc5_ex(const void *w, const float *x, float *y, int rows, int k, int
  * tile), ring slots, super-blocks per row, and the shared-memory offsets of
  * B, B', the scales, the staged x, the partial-sum inbox and the barriers,
  * and the plan's kind: 0 the cluster plan, 1 the streaming plan that
- * independent calls (QMV_OVERLAP_INDEPENDENT, no forced cluster size) take
- * when B for the whole of k fits one CTA -- one CTA a 128-row tile, no
- * staged x or inbox (their offsets 0)}. Returns QMV_ETOOBIG for a shape whose
- * chunk does not fit one CTA. */
+ * independent calls (QMV_OVERLAP_INDEPENDENT, no forced cluster size) take --
+ * one CTA a 128-row tile for the whole of k, with rings of B, B' and scales
+ * (4 super-blocks each) in place of B for a whole chunk; its staged-x field
+ * holds the offset of the ring of the rows' d and dmin (8 super-blocks), and
+ * it has no inbox (offset 0)}. Returns QMV_ETOOBIG for a cluster-plan shape
+ * whose chunk does not fit one CTA. */
 int qmm_q4k_tc5_plan_detail(int rows, int k, int m, const qmv_opts *opts, const int *device, int *out);
 int qmm_q6k_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                 cudaStream_t stream);

@@ -102,34 +102,34 @@ def test_default_cluster_sizes():
 
 
 def test_streaming_plans_stay_in_bounds():
-    """Independent calls take the streaming plan when B for the whole of k fits
-    one CTA (one CTA a 128-row tile, one CTA an SM); every region the kernel
+    """Independent calls take the streaming plan for every k (one CTA a
+    128-row tile; rings of weight copies, of B / B' / scales for 4
+    super-blocks, and of the rows' d / dmin for 8); every region the kernel
     writes fits, in order, and the plan keeps two CTAs off one SM."""
-    seen = set()
-    for k in (256, 512, 1024, 2048, 3072, 4096, 5632, 6144, 7168, 14336):
+    SB, SD, NBARS_FIXED = 4, 8, 29
+    for k in (256, 512, 1024, 2048, 3072, 4096, 5632, 6144, 7168, 14336, 65536):
         for rows in (1, 128, 300, 4096):
             for m in (1, 4, 8):
-                for chunks in (0, 1, 2, 4, 8):
+                for chunks in (0, 1, 2, 4, 6, 8, 12):
                     cfg = {"chunks": chunks} if chunks else None
                     P = q.qmm_q4k_tc5_plan_detail(rows, k, m, cfg=cfg, device=DEV, overlap=q.OVERLAP_INDEPENDENT)
-                    seen.add((k, P["streaming"]))
-                    if not P["streaming"]:
-                        continue
+                    assert P["streaming"] == 1
                     nsb, S = k // 256, P["S"]
-                    assert P["CL"] == 1 and P["nsb"] == nsb and 1 <= S <= nsb
-                    assert P["ctas"] == -(-rows // 128) and P["threads"] == 288
+                    assert P["CL"] == 1 and P["nsb"] == nsb and 1 <= S <= min(nsb, chunks or 6)
+                    assert P["ctas"] == -(-rows // 128) and P["threads"] == 18 * 32
                     assert P["off_b"] >= S * SLOT and P["off_b"] % 128 == 0
-                    assert P["off_bm"] >= P["off_b"] + nsb * 32 * 256 and P["off_bm"] % 16 == 0
-                    assert P["off_sc"] >= P["off_bm"] + nsb * 512
-                    assert P["off_bars"] >= P["off_sc"] + nsb * 8 * 2 * 4 and P["off_bars"] % 8 == 0
-                    assert P["smem"] >= P["off_bars"] + 8 * (2 * S + 13)
+                    assert P["off_bm"] >= P["off_b"] + SB * 32 * 256 and P["off_bm"] % 16 == 0
+                    assert P["off_sc"] >= P["off_bm"] + SB * 512 and P["off_sc"] % 16 == 0
+                    off_dm = P["off_x"]
+                    assert off_dm >= P["off_sc"] + SB * 8 * 2 * 4 and off_dm % 8 == 0
+                    assert P["off_in"] == 0
+                    assert P["off_bars"] >= off_dm + SD * 128 * 8 and P["off_bars"] % 8 == 0
+                    assert P["smem"] >= P["off_bars"] + 8 * (2 * S + NBARS_FIXED)
                     assert P["smem"] <= DEV[1] - STATIC_SMEM_MARGIN
                     # one CTA an SM: two would not fit, so 512 tensor-memory columns are free
                     assert 2 * (P["smem"] + DEV[3]) > DEV[2]
-                    # B descriptors of the last super-block stay in B
-                    assert (32 * nsb - 1) * 256 + 256 <= nsb * 32 * 256
-    assert (4096, 1) in seen and (14336, 0) in seen
-    # a forced cluster size keeps the cluster plan
+    # a forced cluster size keeps the cluster plan, and so do the other modes
     assert q.qmm_q4k_tc5_plan_detail(4096, 4096, 8, cfg={"cluster": 8}, device=DEV,
                                      overlap=q.OVERLAP_INDEPENDENT)["streaming"] == 0
     assert q.qmm_q4k_tc5_plan_detail(4096, 4096, 8, device=DEV)["streaming"] == 0
+    assert q.qmm_q4k_tc5_plan_detail(4096, 4096, 8, device=DEV, overlap=q.OVERLAP_CHAIN)["streaming"] == 0
