@@ -9,17 +9,20 @@
 // read-back) overlap the neighbouring super-blocks' instead of adding up:
 //  * warps 0..7 decode: warp w decodes half hh = w / 4 of every super-block
 //    (sub-blocks 4hh .. 4hh+3) of rows 32 (w % 4) .. +31 into the A operand
-//    in tensor memory, double-buffered per half; warps 0..3 also pass each
+//    in tensor memory, three buffers per half; warps 0..3 also pass each
 //    row's d and dmin to the read-back through a shared-memory ring;
-//  * warp 8 (one thread) issues the MMAs of each super-block into one of ND
-//    accumulator pairs (D, and D' for the min term);
+//  * warps 8 and 18 (one thread each) issue the MMAs of each super-block into
+//    one of ND accumulator sets: warp 8 those of the first half into D0,
+//    warp 18 those of the second half into D1 and the min term into D'. (A
+//    thread issues one MMA in about 50 cycles whatever N, so two issuers
+//    double the rate; the read-back adds D0 + D1.)
 //  * warps 9..12 read back and fold each super-block's accumulators for
 //    their lane quarter of rows;
 //  * warp 13 (one thread) keeps the ring of S weight copies (2-D TMA) full,
 //    refilling a slot as soon as every decoder has read it;
 //  * warps 14..17 build B and B' (x as hi / lo f16 parts, and the group sums)
 //    into a ring of SB super-blocks, as far ahead as the ring allows, from x
-//    prefetched into registers a super-block earlier.
+//    prefetched into registers two super-blocks earlier.
 // B no longer spans k, so any k fits. Every wait is bounded; a wait that gives
 // up marks the CTA's outputs NaN and sets STATUS_WAIT_TIMEOUT. Tensor memory
 // (512 columns) is allocated and released by warp 8; the shared memory the
@@ -31,29 +34,36 @@
 namespace qmv {
 
 constexpr int T5S_DECODERS = 8;                         // decoder warps 0..7
-constexpr int T5S_ISSUER = 8;                           // MMA-issuing warp
+constexpr int T5S_ISSUER = 8;                           // MMA-issuing warp of the first halves
 constexpr int T5S_EPI0 = 9;                             // read-back warps 9..12
 constexpr int T5S_PRODUCER = 13;                        // weight-copy warp
 constexpr int T5S_BUILD0 = 14;                          // B-building warps 14..17
-constexpr int T5S_THREADS = 32 * 18;
+constexpr int T5S_ISSUER1 = 18;                         // MMA-issuing warp of the second halves
+constexpr int T5S_THREADS = 32 * 19;
 constexpr int T5S_TMEM_COLS = 512;
+constexpr int T5S_NA = 3;   // A buffers per half
 constexpr int T5S_SB = 4;   // B ring
-constexpr int T5S_ND = 4;   // accumulator pairs (at least SB: see the builders)
-constexpr int T5S_SD = 8;   // d / dmin ring (at least ND + 2 deep: see the decoders)
+constexpr int T5S_ND = 2;   // accumulator sets
+constexpr int T5S_SD = 8;   // d / dmin ring (at least NA + ND deep: see the decoders)
 constexpr uint32_t T5S_BSLOT = 32u * 256u;   // one super-block of B: 32 k-blocks x 16 rows x 16 bytes
 constexpr uint32_t T5S_BMSLOT = 512u;        // one super-block of B': two k-blocks, the second zeros
-constexpr int T5S_NBARS_FIXED = 4 + 4 + T5S_SB + T5S_SD + 2 * T5S_ND + 1;
-static_assert(T5S_SB <= T5S_ND, "a builder waits for the accumulators of q - SB to be released");
+constexpr int T5S_NBARS_FIXED = 4 * T5S_NA + 2 * T5S_SB + T5S_SD + 2 * T5S_ND + 1;
+static_assert(T5S_SD >= T5S_NA + T5S_ND, "the d / dmin ring");
 
 // Tensor-memory columns: A operand [half][buffer] (64 columns each), the
-// min-term operand [buffer] (8 used of 16), accumulators D [ND] and D' [ND].
+// min-term operand [buffer] (8 columns: 16 f16 of k), then on a 16-column
+// boundary the accumulators D0 [ND], D1 [ND] and D' [ND] (16 columns each).
+constexpr uint32_t T5S_COL_AM0 = 128u * T5S_NA;
+constexpr uint32_t T5S_COL_D0 = (T5S_COL_AM0 + 8u * T5S_NA + 15u) & ~15u;
 __host__ __device__ constexpr uint32_t t5s_col_a(int h, int b) {
-    return 64u * static_cast<uint32_t>(2 * h + b);
+    return 64u * static_cast<uint32_t>(T5S_NA * h + b);
 }
-__host__ __device__ constexpr uint32_t t5s_col_am(int b) { return 256u + 16u * static_cast<uint32_t>(b); }
-__host__ __device__ constexpr uint32_t t5s_col_d(int b) { return 288u + 16u * static_cast<uint32_t>(b); }
+__host__ __device__ constexpr uint32_t t5s_col_am(int b) { return T5S_COL_AM0 + 8u * static_cast<uint32_t>(b); }
+__host__ __device__ constexpr uint32_t t5s_col_d(int h, int b) {
+    return T5S_COL_D0 + 16u * static_cast<uint32_t>(h * T5S_ND + b);
+}
 __host__ __device__ constexpr uint32_t t5s_col_dm(int b) {
-    return 288u + 16u * static_cast<uint32_t>(T5S_ND + b);
+    return T5S_COL_D0 + 16u * static_cast<uint32_t>(2 * T5S_ND + b);
 }
 static_assert(t5s_col_dm(T5S_ND - 1) + 16u <= static_cast<uint32_t>(T5S_TMEM_COLS), "tensor-memory columns");
 
@@ -69,17 +79,18 @@ struct T5SParams {
     uint32_t off_ring, off_b, off_bm, off_sc, off_dm, off_bars;
 };
 
-// Barriers, in order: full[S], empty[S], afull[4], afree[4], bfull[SB],
-// hfull[SD], dfull[ND], dfree[ND], fin (8 bytes each).
+// Barriers, in order: full[S], empty[S], afull[2 NA], afree[2 NA], bfull[SB],
+// sfree[SB], hfull[SD], dfull[ND], dfree[ND], fin (8 bytes each).
 struct T5SBars {
-    uint32_t full0, empty0, afull0, afree0, bfull0, hfull0, dfull0, dfree0, fin;
+    uint32_t full0, empty0, afull0, afree0, bfull0, sfree0, hfull0, dfull0, dfree0, fin;
     __device__ __forceinline__ explicit T5SBars(uint32_t bars, int S) {
         full0 = bars;
         empty0 = full0 + 8u * S;
         afull0 = empty0 + 8u * S;
-        afree0 = afull0 + 32u;
-        bfull0 = afree0 + 32u;
-        hfull0 = bfull0 + 8u * T5S_SB;
+        afree0 = afull0 + 16u * T5S_NA;
+        bfull0 = afree0 + 16u * T5S_NA;
+        sfree0 = bfull0 + 8u * T5S_SB;
+        hfull0 = sfree0 + 8u * T5S_SB;
         dfull0 = hfull0 + 8u * T5S_SD;
         dfree0 = dfull0 + 8u * T5S_ND;
         fin = dfree0 + 8u * T5S_ND;
@@ -187,17 +198,20 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
                 mbar_init(B.full0 + 8u * s, 1);
                 mbar_init(B.empty0 + 8u * s, 32 * T5S_DECODERS);
             }
-            for (int i = 0; i < 4; i++) {
+            for (int i = 0; i < 2 * T5S_NA; i++) {
                 mbar_init(B.afull0 + 8u * i, 32 * T5S_DECODERS / 2);
                 mbar_init(B.afree0 + 8u * i, 1);
             }
-            for (int i = 0; i < T5S_SB; i++) mbar_init(B.bfull0 + 8u * i, 128);
+            for (int i = 0; i < T5S_SB; i++) {
+                mbar_init(B.bfull0 + 8u * i, 128);
+                mbar_init(B.sfree0 + 8u * i, 128);
+            }
             for (int i = 0; i < T5S_SD; i++) mbar_init(B.hfull0 + 8u * i, 128);
             for (int i = 0; i < T5S_ND; i++) {
-                mbar_init(B.dfull0 + 8u * i, 1);
+                mbar_init(B.dfull0 + 8u * i, 2);   // one commit from each issuer
                 mbar_init(B.dfree0 + 8u * i, 128);
             }
-            mbar_init(B.fin, 1);
+            mbar_init(B.fin, 2);
             s_tmo = 0;
             fence_mbar_init();
         }
@@ -249,42 +263,36 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
                 if (!mbar_wait_bounded(B.full0 + 8u * (i % p.S), static_cast<uint32_t>((i / p.S) & 1))) break;
         }
         __syncwarp();
-    } else if (warp == T5S_ISSUER) {
-        // ---- the MMAs: per super-block, once its B is built and an
-        // accumulator pair is free, the 8 steps of each half (in the A
-        // buffer of the super-block's parity) and the min term
+    } else if (warp == T5S_ISSUER || warp == T5S_ISSUER1) {
+        // ---- the MMAs of half h of every super-block, once its B is built
+        // and its accumulator set is free: the 8 steps (in A buffer q % NA)
+        // into D_h, and for h = 1 the min term
+        const int h = warp == T5S_ISSUER ? 0 : 1;
         if (lane == 0 && !p.force_timeout) {
             const uint32_t bbase = sb + p.off_b, bmbase = sb + p.off_bm;
             bool ok = true;
-            for (int q = 0; q < nq && ok; q++) {
-                const int bs = q % T5S_SB, db = q % T5S_ND, ab = q & 1;
+            for (int q = 0; q < nq; q++) {
+                const int bs = q % T5S_SB, db = q % T5S_ND, ab = q % T5S_NA;
+                const uint32_t ai = static_cast<uint32_t>(T5S_NA * h + ab);
                 if (!mbar_wait_bounded(B.bfull0 + 8u * bs, static_cast<uint32_t>((q / T5S_SB) & 1)) ||
                     (q >= T5S_ND &&
-                     !mbar_wait_bounded(B.dfree0 + 8u * db, static_cast<uint32_t>(((q - T5S_ND) / T5S_ND) & 1)))) {
+                     !mbar_wait_bounded(B.dfree0 + 8u * db, static_cast<uint32_t>(((q - T5S_ND) / T5S_ND) & 1))) ||
+                    !mbar_wait_bounded(B.afull0 + 8u * ai, static_cast<uint32_t>((q / T5S_NA) & 1))) {
                     ok = false;
                     break;
                 }
+                tc_fence_after();
                 const uint32_t bq = bbase + static_cast<uint32_t>(bs) * T5S_BSLOT;
-                for (int h = 0; h < 2; h++) {
-                    const uint32_t ai = static_cast<uint32_t>(2 * h + ab);
-                    if (!mbar_wait_bounded(B.afull0 + 8u * ai, static_cast<uint32_t>((q >> 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
 #pragma unroll
-                    for (int t = 0; t < 8; t++) {
-                        const uint32_t kb = static_cast<uint32_t>(16 * h + 2 * t);   // first k-block of the step
-                        mma_f16_ts(tmem + t5s_col_d(db), tmem + t5s_col_a(h, ab) + 8u * t,
-                                   smem_desc(bq + kb * 256u, 256u, 128u), T5_IDESC, h > 0 || t > 0);
-                    }
-                    if (h == 1)
-                        mma_f16_ts(tmem + t5s_col_dm(db), tmem + t5s_col_am(ab),
-                                   smem_desc(bmbase + static_cast<uint32_t>(bs) * T5S_BMSLOT, 256u, 128u), T5_IDESC,
-                                   false);
-                    mma_commit(B.afree0 + 8u * ai);
+                for (int t = 0; t < 8; t++) {
+                    const uint32_t kb = static_cast<uint32_t>(16 * h + 2 * t);   // first k-block of the step
+                    mma_f16_ts(tmem + t5s_col_d(h, db), tmem + t5s_col_a(h, ab) + 8u * t,
+                               smem_desc(bq + kb * 256u, 256u, 128u), T5_IDESC, t > 0);
                 }
-                if (!ok) break;
+                if (h == 1)
+                    mma_f16_ts(tmem + t5s_col_dm(db), tmem + t5s_col_am(ab),
+                               smem_desc(bmbase + static_cast<uint32_t>(bs) * T5S_BMSLOT, 256u, 128u), T5_IDESC, false);
+                mma_commit(B.afree0 + 8u * ai);
                 mma_commit(B.dfull0 + 8u * db);
             }
             if (!ok) atomicExch(const_cast<int*>(tmo), 1);
@@ -319,13 +327,15 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
                 qs[4 * i] = v.x; qs[4 * i + 1] = v.y; qs[4 * i + 2] = v.z; qs[4 * i + 3] = v.w;
             }
             mbar_arrive(B.empty0 + 8u * s);   // this row's half is done with the slot
-            const int ab = q & 1;
-            const uint32_t ai = static_cast<uint32_t>(2 * hh + ab);
-            // the A buffer of this parity is free once the MMAs of q - 2 are
-            // done; so are the accumulators of q - 2 - ND and, with them, the
-            // read-back's use of the d / dmin slot written here (SD >= ND + 2)
-            if (q >= 2 &&
-                !__all_sync(FULL, mbar_wait_bounded(B.afree0 + 8u * ai, static_cast<uint32_t>(((q - 2) >> 1) & 1)))) {
+            const int ab = q % T5S_NA;
+            const uint32_t ai = static_cast<uint32_t>(T5S_NA * hh + ab);
+            // A buffer q % NA is free once the MMAs of q - NA are done; those
+            // were issued after the accumulators of q - NA - ND were released,
+            // so the read-back is done with the d / dmin slot written here
+            // (SD >= NA + ND)
+            if (q >= T5S_NA &&
+                !__all_sync(FULL, mbar_wait_bounded(B.afree0 + 8u * ai,
+                                                    static_cast<uint32_t>(((q - T5S_NA) / T5S_NA) & 1)))) {
                 ok = false;
                 break;
             }
@@ -373,8 +383,8 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
     } else if (warp >= T5S_BUILD0) {
         // ---- warps 14..17: B of rows ew and ew + 4 of x, super-block after
         // super-block. B(qb) takes the slot and the scales of qb - SB: both
-        // are free once the accumulators of qb - SB are released (their MMAs
-        // are done, and the read-back has read the scales).
+        // are free once the read-back has read the accumulators (so their
+        // MMAs are done) and the scales of qb - SB.
         const int ew = warp - T5S_BUILD0;
         uint8_t* bring = smem + p.off_b;
         uint8_t* bmring = smem + p.off_bm;
@@ -382,25 +392,24 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
         const int j0 = ew < p.m ? ew : -1;
         const int j1 = ew + 4 < p.m ? ew + 4 : -1;
         bool ok = !p.force_timeout;
-        // x of the super-block built next and of the one after, in two
-        // register sets used in turn (a copy from one set to the other would
-        // wait for the loads in flight)
-        float xa[2][8] = {}, xb[2][8] = {};
+        // x of the next three super-blocks, in three register sets used in
+        // turn (loaded two super-blocks ahead; a copy from one set to another
+        // would wait for the loads in flight)
+        float xa[2][8] = {}, xb[2][8] = {}, xc[2][8] = {};
         auto load = [&](int qq, float(&v)[2][8]) {
             if (j0 >= 0) t5s_load_x(p.x, p.k, qq, j0, lane, v[0]);
             if (j1 >= 0) t5s_load_x(p.x, p.k, qq, j1, lane, v[1]);
         };
         auto step = [&](int qb, const float(&cur)[2][8], float(&nxt)[2][8]) -> bool {
+            // nxt: the set of qb - 1, already built
             if (qb >= T5S_SB) {
-                // (no phase is skipped: the accumulators of qb - SB + ND
-                // cannot be released before B(qb) exists, and SB <= ND)
                 const int qo = qb - T5S_SB;
-                if (!__all_sync(FULL, mbar_wait_bounded(B.dfree0 + 8u * (qo % T5S_ND),
-                                                        static_cast<uint32_t>((qo / T5S_ND) & 1)) &&
+                if (!__all_sync(FULL, mbar_wait_bounded(B.sfree0 + 8u * (qo % T5S_SB),
+                                                        static_cast<uint32_t>((qo / T5S_SB) & 1)) &&
                                           *tmo == 0))
                     return false;
             }
-            if (qb + 1 < nq) load(qb + 1, nxt);
+            if (qb + 2 < nq) load(qb + 2, nxt);
             const int bs = qb % T5S_SB;
             if (j0 >= 0)
                 t5s_convert2(cur, j0, j1, lane, bring + bs * T5S_BSLOT, bmring + bs * T5S_BMSLOT,
@@ -416,10 +425,13 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
             for (int i = ew * 32 + lane; i < T5S_SB * 64; i += 128)
                 reinterpret_cast<uint32_t*>(bmring)[(i >> 6) * 128 + 64 + (i & 63)] = 0u;
             load(0, xa);
+            if (nq > 1) load(1, xb);
         }
-        for (int qb = 0; qb < nq && ok; qb += 2) {
-            ok = step(qb, xa, xb);
+        // B(qb) from the set of qb, x of qb + 2 into the set of qb - 1
+        for (int qb = 0; qb < nq && ok; qb += 3) {
+            ok = step(qb, xa, xc);
             if (ok && qb + 1 < nq) ok = step(qb + 1, xb, xa);
+            if (ok && qb + 2 < nq) ok = step(qb + 2, xc, xb);
         }
         if (!ok) atomicExch(const_cast<int*>(tmo), 1);
     } else {
@@ -443,8 +455,9 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t dv[16], mv[16];
-            tmem_ld16(tmem + lane_base + t5s_col_d(db), dv);
+            uint32_t dv[16], ev[16], mv[16];
+            tmem_ld16(tmem + lane_base + t5s_col_d(0, db), dv);
+            tmem_ld16(tmem + lane_base + t5s_col_d(1, db), ev);
             tmem_ld16(tmem + lane_base + t5s_col_dm(db), mv);
             const float2 dd = dmr[hs * T5_ROWS + r];
             float sq[2 * T5_COLS];
@@ -455,12 +468,15 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
             }
             tmem_wait_ld();
             tc_fence_before();
-            // the accumulators, and with them B(q)'s slot and scales, are free
+            // the accumulators are free, and so are B(q)'s slot and scales
             mbar_arrive(B.dfree0 + 8u * db);
+            mbar_arrive(B.sfree0 + 8u * bs);
 #pragma unroll
             for (int j = 0; j < T5_COLS; j++) {
                 if (j < p.m) {
-                    const float t = dd.x * (__uint_as_float(dv[j]) + __uint_as_float(dv[8 + j]));
+                    const float hi = __uint_as_float(dv[j]) + __uint_as_float(ev[j]);
+                    const float lo = __uint_as_float(dv[8 + j]) + __uint_as_float(ev[8 + j]);
+                    const float t = dd.x * (hi + lo);
                     const float u = dd.y * (__uint_as_float(mv[j]) + __uint_as_float(mv[8 + j]));
                     yacc[j] = __fmaf_rn(t, sq[2 * j], yacc[j]);
                     yacc[j] = __fmaf_rn(-u, sq[2 * j + 1], yacc[j]);

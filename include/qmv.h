@@ -350,18 +350,26 @@ int qmm_q4k_ex(const void *w, const float *x, float *y, int rows, int k, int m, 
 /* The batched product of qmm_q4k_ex (hanzo-ml src/vulkan_backend.rs,
  * matmul_q4k_gpu) on the fifth-generation tensor cores: tcgen05.mma with the
  * decoded weights (sc * q, exact in f16) as the A operand in tensor memory, x
- * as hi + lo f16 parts in shared memory and f32 accumulators in tensor memory;
- * each 128-row tile is split along k over the CTAs of one thread-block
- * cluster, which add their partial sums in rank order. Same result contract as
- * qmm_q4k_ex (unit rows of x give the weight columns bit for bit; otherwise
- * within 1e-4 scale-relative of the exact product); arguments, layouts and
- * errors as there, m >= 1 (tiles of 8 rows of x, one launch each); w and x
- * must be 16-byte aligned (QMV_EINVAL otherwise). opts->cluster forces the
- * number of k-chunks of a tile (1..8), opts->chunks the ring depth,
- * opts->overlap the launch overlap. On a GB300 this path measured slower than
- * qmm_q4k_ex for m <= 8 on the 4096 x 4096 matrix (each CTA's fixed costs --
- * tensor-memory allocation, the x conversion, the cluster reduction --
- * outweigh its few super-blocks of work), so qmm_q4k_ex does not use it. */
+ * as hi + lo f16 parts in shared memory and f32 accumulators in tensor memory.
+ * Two plans:
+ *  - the cluster plan: each 128-row tile is split along k over the CTAs of one
+ *    thread-block cluster, which add their partial sums in rank order;
+ *  - the streaming plan, for independent calls (opts->overlap ==
+ *    QMV_OVERLAP_INDEPENDENT and no forced cluster size): one CTA a tile for
+ *    the whole of k, one role per warp. Its results are bit for bit those of
+ *    the cluster plan with one k-chunk.
+ * Same result contract as qmm_q4k_ex (unit rows of x give the weight columns
+ * bit for bit; otherwise within 1e-4 scale-relative of the exact product);
+ * arguments, layouts and errors as there, m >= 1 (tiles of 8 rows of x, one
+ * launch each); w and x must be 16-byte aligned (QMV_EINVAL otherwise).
+ * opts->cluster forces the number of k-chunks of a tile (1..8) and the
+ * cluster plan; opts->chunks sets the ring depth; opts->overlap the launch
+ * overlap.
+ * On a GB300 this path measured slower than qmm_q4k_ex for m <= 8 on the
+ * 4096 x 4096 matrix, so qmm_q4k_ex does not use it. The bound is the MMA
+ * instruction rate: one tcgen05.mma of M = 128, K = 16 costs about 96 cycles
+ * whatever N up to 128, and with N = 16 (8 rows of x, hi and lo) it covers
+ * only 128 x 16 weights. */
 int qmm_q4k_tc5_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                    cudaStream_t stream);
 
