@@ -366,10 +366,11 @@ int qmm_q4k_ex(const void *w, const float *x, float *y, int rows, int k, int m, 
  * cluster plan; opts->chunks sets the ring depth; opts->overlap the launch
  * overlap.
  * On a GB300 this path measured slower than qmm_q4k_ex for m <= 8 on the
- * 4096 x 4096 matrix, so qmm_q4k_ex does not use it. The bound is the MMA
- * instruction rate: one tcgen05.mma of M = 128, K = 16 costs about 96 cycles
- * whatever N up to 128, and with N = 16 (8 rows of x, hi and lo) it covers
- * only 128 x 16 weights. */
+ * 4096 x 4096 matrix (the streaming plan by 3-11 %), so qmm_q4k_ex does not
+ * use it. A thread issues one tcgen05.mma (M = 128, K = 16) in 50-90 cycles
+ * whatever N, and with N = 16 (8 rows of x, hi and lo) each covers only
+ * 128 x 16 weights; the streaming plan issues from two threads, and is then
+ * bound by the decode's instruction issue. */
 int qmm_q4k_tc5_ex(const void *w, const float *x, float *y, int rows, int k, int m, const qmv_opts *opts,
                    cudaStream_t stream);
 
