@@ -268,3 +268,25 @@ def test_random_shapes(q, rows, k, m, cluster):
     assert not np.any(np.isnan(y))
     for i in range(m):
         assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, i
+
+
+def streaming_cases(n=10):
+    """Seeded random shapes for the streaming plan: rows 1..3000 (ragged last
+    tiles), k a multiple of 256 up to 16384, m 1..16 (two launches past 8)."""
+    z = synth.Stream(20261205).draw(n * 3).reshape(n, 3)
+    out = []
+    for i in range(n):
+        d = [int(v >> np.uint64(33)) for v in z[i]]
+        out.append((1 + d[0] % 3000, 256 * (1 + d[1] % 64), 1 + d[2] % 16))
+    return out
+
+
+@pytest.mark.parametrize("rows,k,m", streaming_cases())
+def test_streaming_plan_random_shapes(q, rows, k, m):
+    w, x = case(rows, k, m, rows * 17 + k + 3 * m)
+    y = run(q, w, x, rows, k, m, overlap=q.OVERLAP_INDEPENDENT)
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    assert not np.any(np.isnan(y))
+    for i in range(m):
+        assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, i
+    assert q.qmv_device_status() == 0
