@@ -14,8 +14,9 @@
 //  * warps 8 and 18 (one thread each) issue the MMAs of each super-block into
 //    one of ND accumulator sets: warp 8 those of the first half into D0,
 //    warp 18 those of the second half into D1 and the min term into D'. (A
-//    thread issues one MMA in about 50 cycles whatever N, so two issuers
-//    double the rate; the read-back adds D0 + D1.)
+//    thread issues one MMA in 50-100 cycles whatever N, while threads of
+//    different warps issue side by side, so two issuers double the rate; the
+//    read-back adds D0 + D1.)
 //  * warps 9..12 read back and fold each super-block's accumulators for
 //    their lane quarter of rows;
 //  * warp 13 (one thread) keeps the ring of S weight copies (2-D TMA) full,
