@@ -71,10 +71,12 @@ inline int make_t5_plan(const DevInfo& di, int rows, int k, int m, const qmv_opt
     return QMV_OK;
 }
 
-// Shared memory the streaming plan asks for at least: more than half an SM's,
-// so that one CTA holds an SM and its allocation of all 512 tensor-memory
-// columns never waits.
-constexpr long long T5S_MIN_SMEM = 120 * 1024;
+// Shared memory the streaming plan asks for at least: enough that no second
+// CTA of this plan (more than half an SM) and no CTA of the cluster plan (at
+// least T5_MIN_SMEM) fits beside it, so its allocation of all 512
+// tensor-memory columns never meets another holder on the SM.
+constexpr long long T5S_MIN_SMEM = 148 * 1024;
+static_assert(T5S_MIN_SMEM + T5_MIN_SMEM + 2 * T5_STATIC_SMEM > 228 * 1024, "cluster-plan CTA beside a streaming one");
 
 // The streaming plan (independent calls): one CTA a 128-row tile for the
 // whole of k, with rings of weight copies, of B, and of the rows' d / dmin.

@@ -26,8 +26,11 @@
 //    prefetched into registers two super-blocks earlier.
 // B no longer spans k, so any k fits. Every wait is bounded; a wait that gives
 // up marks the CTA's outputs NaN and sets STATUS_WAIT_TIMEOUT. Tensor memory
-// (512 columns) is allocated and released by warp 8; the shared memory the
-// plan asks for keeps one CTA an SM, so the allocation never waits.
+// (512 columns) is allocated and released by warp 8. The shared memory the
+// plan asks for keeps any other CTA that uses tensor memory (of this kernel or
+// of the cluster plan) off the SM, and the next kernel is let start only once
+// the columns are held; this kernel waits for the previous one only after
+// releasing them.
 #pragma once
 
 #include "qmm_tc5.cuh"
@@ -191,8 +194,6 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
 #pragma unroll
     for (int j = 0; j < T5_COLS; j++) yacc[j] = 0.0f;
 
-    pdl_launch_dependents();
-
     if (warp == T5S_ISSUER) {
         if (lane == 0) {
             for (int s = 0; s < p.S; s++) {
@@ -229,6 +230,11 @@ __global__ void __launch_bounds__(T5S_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     volatile int* tmo = &s_tmo;
+    // The next kernel may start only now that this CTA holds its tensor
+    // memory: a later kernel's CTA on this SM that took columns first, and
+    // then waited for this kernel while holding them, would leave this CTA's
+    // allocation waiting forever.
+    pdl_launch_dependents();
     // x may come from the kernel just before, unless the caller declared it
     // independent of it
     if (!p.early_inputs) pdl_dependency_wait();

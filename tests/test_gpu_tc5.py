@@ -290,3 +290,27 @@ def test_streaming_plan_random_shapes(q, rows, k, m):
     for i in range(m):
         assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, i
     assert q.qmv_device_status() == 0
+
+
+def test_streaming_and_cluster_plans_interleaved_in_one_stream(q):
+    """Independent calls (streaming plan) alternating with chained calls
+    (cluster plan) in one stream: a CTA of either plan never shares an SM with
+    another tensor-memory CTA that could hold columns it waits for, so the
+    sequence completes, and every call is within the tolerance of the oracle."""
+    rows, k, m = 1024, 2048, 4
+    st = synth.Stream(4242)
+    ws = [synth.gen_q4k_rows(st, rows, k) for _ in range(3)]
+    xs = [synth.gen_normal(st, m * k).reshape(m, k) for _ in range(3)]
+    wd = [dev(w) for w in ws]
+    xd = [dev(x) for x in xs]
+    ys = [torch.empty((m, rows), dtype=torch.float32, device="cuda") for _ in range(12)]
+    for i in range(12):
+        mode = q.OVERLAP_INDEPENDENT if i % 2 == 0 else q.OVERLAP_CHAIN
+        q.qmm_q4k_tc5(wd[i % 3], xd[(i + 1) % 3], ys[i], rows, k, m, overlap=mode)
+    torch.cuda.synchronize()
+    for i in range(12):
+        ref = oracle.qmm("q4k", ws[i % 3], xs[(i + 1) % 3], m, rows, k)
+        got = ys[i].cpu().numpy()
+        for j in range(m):
+            assert scale_rel(ref[j], got[j]) <= SCALE_REL_TOL, (i, j)
+    assert q.qmv_device_status() == 0

@@ -105,7 +105,8 @@ def test_streaming_plans_stay_in_bounds():
     """Independent calls take the streaming plan for every k (one CTA a
     128-row tile; rings of weight copies, of B / B' / scales for 4
     super-blocks, and of the rows' d / dmin for 8); every region the kernel
-    writes fits, in order, and the plan keeps two CTAs off one SM."""
+    writes fits, in order, and the plan keeps every other tensor-memory CTA
+    off its SM."""
     SB, SD, NBARS_FIXED = 4, 8, 33
     for k in (256, 512, 1024, 2048, 3072, 4096, 5632, 6144, 7168, 14336, 65536):
         for rows in (1, 128, 300, 4096):
@@ -126,8 +127,10 @@ def test_streaming_plans_stay_in_bounds():
                     assert P["off_bars"] >= off_dm + SD * 128 * 8 and P["off_bars"] % 8 == 0
                     assert P["smem"] >= P["off_bars"] + 8 * (2 * S + NBARS_FIXED)
                     assert P["smem"] <= DEV[1] - STATIC_SMEM_MARGIN
-                    # one CTA an SM: two would not fit, so 512 tensor-memory columns are free
+                    # one CTA an SM, and no CTA of the cluster plan (at least 80 KB)
+                    # beside it: nothing else on the SM holds tensor memory
                     assert 2 * (P["smem"] + DEV[3]) > DEV[2]
+                    assert P["smem"] + DEV[3] + 80 * 1024 + DEV[3] > DEV[2]
     # a forced cluster size keeps the cluster plan, and so do the other modes
     assert q.qmm_q4k_tc5_plan_detail(4096, 4096, 8, cfg={"cluster": 8}, device=DEV,
                                      overlap=q.OVERLAP_INDEPENDENT)["streaming"] == 0
