@@ -366,7 +366,7 @@ int qmm_q4k_ex(const void *w, const float *x, float *y, int rows, int k, int m, 
  * cluster plan; opts->chunks sets the ring depth; opts->overlap the launch
  * overlap.
  * On a GB300 this path measured slower than qmm_q4k_ex for m <= 8 on the
- * 4096 x 4096 matrix (the streaming plan by 3-11 %), so qmm_q4k_ex does not
+ * 4096 x 4096 matrix (the streaming plan by 5-15 %), so qmm_q4k_ex does not
  * use it. A thread issues one tcgen05.mma (M = 128, K = 16) in 50-100 cycles
  * whatever N, and with N = 16 (8 rows of x, hi and lo) each covers only
  * 128 x 16 weights; the streaming plan issues from two threads, and is then
