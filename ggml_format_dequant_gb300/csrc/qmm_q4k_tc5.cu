@@ -62,6 +62,7 @@ inline int make_t5_plan(const DevInfo& di, int rows, int k, int m, const qmv_opt
     tp->slot_bytes = slot;
     const int mode = overlap_of(cfg);
     tp->early_inputs = mode >= QMV_OVERLAP_INDEPENDENT ? 1 : 0;
+    tp->late_alloc = mode == QMV_OVERLAP_CHAIN ? 1 : 0;
     pl->T = T5_THREADS;
     pl->parts = ((rows + T5_ROWS - 1) / T5_ROWS) * CL;
     pl->R = 1;

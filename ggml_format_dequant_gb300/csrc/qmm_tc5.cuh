@@ -65,6 +65,7 @@ struct T5Params {
     int CL;               // k-chunks of a tile = cluster size
     int S;                // ring slots
     int early_inputs;     // x read before waiting for the previous kernel (only y waits)
+    int late_alloc;       // tensor memory taken after the wait for the previous kernel (chained launches)
     int force_timeout;    // failure-path test
     uint32_t slot_bytes;  // 128 rows x 144 bytes
     uint32_t off_ring, off_b, off_bm, off_sc, off_x, off_in, off_bars;
@@ -313,13 +314,15 @@ __global__ void __launch_bounds__(T5_THREADS, 1)
             }
         }
         __syncwarp();
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "r"(T5_TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (!p.late_alloc) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&s_tmem)),
+                         "r"(T5_TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
-    // every barrier is initialized (and the tensor-memory address written)
-    // before any thread waits on one
+    // every barrier is initialized before any thread waits on one
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -328,6 +331,17 @@ __global__ void __launch_bounds__(T5_THREADS, 1)
     if (!p.early_inputs) {
         pdl_dependency_wait();
         if (tid == 4 * 32) request_x();
+    }
+    // A chained launch takes its tensor memory only now, after its wait for
+    // the previous kernel (while warps 0..3 build B): a CTA never holds
+    // columns while it waits for another kernel that may still need columns
+    // on this SM. (A plain launch starts after the previous kernel has ended;
+    // independent calls release their columns before they wait.)
+    if (p.late_alloc && warp == 4) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(T5_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
     // ---- B: x of the chunk as hi / lo f16 (warps 0..3), zero where j >= m
