@@ -25,6 +25,7 @@ QMV_ECUDA = -3
 QMV_ETOOBIG = -4
 QMV_STATUS_BAD_EXPERT_ID = 1
 QMV_STATUS_WAIT_TIMEOUT = 2
+QMV_STATUS_OUT_OF_BOUNDS = 4   # the checking build only (see _build.FLAVOURS)
 
 # Plan ids of qmv_plan_info / qmv_plan_detail (13-15 are not plans).
 (FMT_Q4K, FMT_Q6K, FMT_Q8_0, FMT_Q8_DP4A, FMT_MOE_Q4K, FMT_Q4K_DP4A, FMT_MOE_Q6K, FMT_MOE_Q4K_DP4A,

@@ -15,6 +15,17 @@ constexpr unsigned FULL = 0xffffffffu;
 // Status bits a kernel may raise in its translation unit's device status word.
 constexpr unsigned STATUS_BAD_EXPERT_ID = 1u;   // an MoE id outside [0, n_experts)
 constexpr unsigned STATUS_WAIT_TIMEOUT = 2u;    // a staged copy did not land in time
+constexpr unsigned STATUS_OUT_OF_BOUNDS = 4u;   // checking build only: an access outside its region
+
+// The checking build (compiled with QMV_BOUNDS_CHECK) tests every shared- and
+// global-memory access of the matvec kernel against the region the plan gives
+// it; an access outside raises STATUS_OUT_OF_BOUNDS and is skipped or moved
+// to the region's start. In the normal build the tests fold away.
+#ifdef QMV_BOUNDS_CHECK
+constexpr bool BOUNDS_CHECK = true;
+#else
+constexpr bool BOUNDS_CHECK = false;
+#endif
 
 // Bound on one wait for a staged copy. A bulk copy of a few tens of KB lands in
 // microseconds; if it has not after this long the kernel records the fact and

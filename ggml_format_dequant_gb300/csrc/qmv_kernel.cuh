@@ -40,6 +40,17 @@ namespace qmv {
 // Device status word of the translation unit that instantiates the kernels.
 static __device__ unsigned int g_status;
 
+// The checking build's test of one access (see BOUNDS_CHECK): whether it may
+// go ahead. Always true in the normal build, where `ok` is never evaluated.
+__device__ __forceinline__ bool in_bounds(bool ok) {
+    if constexpr (BOUNDS_CHECK) {
+        if (!ok) atomicOr(&g_status, STATUS_OUT_OF_BOUNDS);
+        return ok;
+    } else {
+        return true;
+    }
+}
+
 enum Mode : int { MODE_MATVEC = 0, MODE_BLOCKDOTS = 1 };
 
 struct KParams {
@@ -90,6 +101,12 @@ __device__ __forceinline__ void issue_copy(const KParams& p, uint8_t* dst_ptr, u
     const uintptr_t a0 = gs & ~uintptr_t(15);
     uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
     const uintptr_t lim = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(p.wbytes);
+    // (the whole 16-byte cover fits the slot; it reads only the weights)
+    if (!in_bounds(a1 - a0 <= p.slot_stride && a0 >= (reinterpret_cast<uintptr_t>(p.w) & ~uintptr_t(15)) &&
+                   ge <= lim)) {
+        mbar_arrive(bar);   // nothing copied; the waiters go on
+        return;
+    }
     if (a1 > lim) {
         a1 = ge & ~uintptr_t(15);
         for (uintptr_t b = (a1 > a0 ? a1 : a0); b < ge; b++) dst_ptr[b - a0] = *reinterpret_cast<const uint8_t*>(b);
@@ -168,7 +185,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
             // Unroutable slot: NaN marks every output of it, and the status
             // word records the fact. No byte of the bank is touched.
             pdl_dependency_wait();
-            for (int r = R0 + tid; r < R0 + nrows; r += blockDim.x) p.y[yoff + r] = __int_as_float(0x7fc00000);
+            for (int r = R0 + tid; r < R0 + nrows; r += blockDim.x)
+                if (in_bounds(r >= 0 && r < p.rows)) p.y[yoff + r] = __int_as_float(0x7fc00000);
             if (tid == 0) atomicOr(&g_status, STATUS_BAD_EXPERT_ID);
             return;
         }
@@ -207,6 +225,12 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
     auto issue = [&](int pc, int s) {
         const int r0 = R0 + glo + pc * p.CR;
         const int nr = min(p.CR, gn - pc * p.CR);
+        // the piece's rows are the matrix's, its slot lies in the ring
+        if (!in_bounds(rg < p.NG && s < p.S && nr > 0 && r0 >= 0 && r0 + nr <= p.rows &&
+                       static_cast<uint32_t>(rg * p.S + s + 1) * p.slot_stride <= p.off_bars - p.off_ring)) {
+            if (rg < p.NG && s < p.S) mbar_arrive(bars + 8u * s);
+            return;
+        }
         const uintptr_t gs = reinterpret_cast<uintptr_t>(wbase) + static_cast<uintptr_t>(r0) * p.rowbytes;
         issue_copy(p, ring_ptr + static_cast<uint32_t>(s) * p.slot_stride, ring + static_cast<uint32_t>(s) * p.slot_stride,
                    bars + 8u * s, gs, static_cast<uintptr_t>(nr) * p.rowbytes);
@@ -266,8 +290,10 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         const int rpw = 32 >> p.lgGS;               // rows side by side in a warp step
         typename F::X xr;
         const typename F::L lc = F::lane_consts(uc, p.nb, ugc);
+        in_bounds(rg < p.NG);
         {
             const int e0 = ks * F::SLICE_BLOCKS * F::QK + F::unit_elem(uc);
+            in_bounds(e0 >= 0 && e0 < p.k);
             if constexpr (F::LIMBS)
                 F::load_x(xr, smem, p.lt, e0);
             else
@@ -276,6 +302,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         // Byte offset of the lane's unit inside a row, and 16-byte phase of the
         // group's rows in memory (pieces may start off a 16-byte boundary).
         const uint32_t ubyte = static_cast<uint32_t>(ks) * (F::SLICE_BLOCKS * F::BLOCK_BYTES) + F::unit_byte(uc);
+        in_bounds(ubyte < p.rowbytes && ks < p.KS);
         const uint32_t gphase = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(wbase)) +
                                 static_cast<uint32_t>(R0 + glo) * p.rowbytes;
         const uint32_t piece_bytes = static_cast<uint32_t>(p.CR) * p.rowbytes;
@@ -284,10 +311,12 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         // A finished row sum: to y (rows of one slice, no early inputs) or
         // parked by slice until the CTA is done.
         auto store_row = [&](int rl, float v) {
-            if (p.W == 0)
-                p.y[yoff + R0 + rl] = v;
-            else
-                red[rl * p.W + ks] = v;
+            if (p.W == 0) {
+                if (in_bounds(rl >= 0 && R0 + rl < p.rows)) p.y[yoff + R0 + rl] = v;
+            } else {
+                if (in_bounds(rl >= 0 && static_cast<uint32_t>(rl * p.W + ks + 1) * 4u <= p.off_ring - p.off_red))
+                    red[rl * p.W + ks] = v;
+            }
         };
 
         int s = 0;
@@ -306,6 +335,14 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
             const uint32_t d0 = (gphase + static_cast<uint32_t>(pc) * piece_bytes) & 15u;
             const uint32_t prow0 = ring + static_cast<uint32_t>(s) * p.slot_stride + d0 + ubyte;   // unit, row 0
             uint32_t a = prow0 + static_cast<uint32_t>(sub) * p.rowbytes;                     // unit, step 0
+            // The checking build: the piece (from its 16-byte phase on, with
+            // the format's read slack) fits its slot, and every unit a lane
+            // reads starts inside one of the piece's rows.
+            const uint32_t piece_lo = ring + static_cast<uint32_t>(s) * p.slot_stride + d0;
+            in_bounds(d0 + static_cast<uint32_t>(nr) * p.rowbytes + F::SLACK <= p.slot_stride);
+            auto unit_at = [&](uint32_t aa) -> uint32_t {
+                return in_bounds(aa >= piece_lo && aa - piece_lo < static_cast<uint32_t>(nr) * p.rowbytes) ? aa : piece_lo;
+            };
             int jb = 0;
             if constexpr (MODE == MODE_MATVEC) {
                 // Whole steps of R * rpw rows: R independent dots, then the
@@ -314,7 +351,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
                     float acc[R];
 #pragma unroll
                     for (int q = 0; q < R; q++) {
-                        acc[q] = dot_of<F>(a + q * rstep, lc, xr, aligned8);
+                        acc[q] = dot_of<F>(unit_at(a + q * rstep), lc, xr, aligned8);
                         acc[q] = has_unit ? acc[q] : 0.0f;
                     }
                     if constexpr (WIDE && R == 2) {
@@ -332,7 +369,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
                 // row lies past the piece decode row 0 and drop the result.
                 for (; jb < nr; jb += rpw, a += rstep) {
                     const bool valid = jb + sub < nr;
-                    float v = dot_of<F>(valid ? a : prow0, lc, xr, aligned8);
+                    float v = dot_of<F>(unit_at(valid ? a : prow0), lc, xr, aligned8);
                     v = has_unit ? v : 0.0f;
                     v = group_sum<WIDE>(v, p.GS);
                     if (u == 0 && valid) store_row(rl0 + jb + sub, v);
@@ -341,8 +378,9 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
                 // MODE_BLOCKDOTS: the exact int32 dots of every block.
                 if constexpr (!F::LIMBS) {
                     for (; jb < nr; jb += rpw, a += rstep) {
-                        if (has_unit && jb + sub < nr)
-                            F::block_dots(a, lc, xr, aligned8,
+                        if (has_unit && jb + sub < nr &&
+                                in_bounds(R0 + rl0 + jb + sub < p.rows && F::dot_base(ug) < p.k / F::DOT_WEIGHTS))
+                            F::block_dots(unit_at(a), lc, xr, aligned8,
                                           p.dots + static_cast<long long>(R0 + rl0 + jb + sub) * (p.k / F::DOT_WEIGHTS) +
                                               F::dot_base(ug));
                     }
@@ -386,7 +424,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         }
         if constexpr (MODE == MODE_MATVEC) {
             pdl_dependency_wait();
-            for (int r = tid; r < nrows; r += blockDim.x) p.y[yoff + R0 + r] = __int_as_float(0x7fc00000);
+            for (int r = tid; r < nrows; r += blockDim.x)
+                if (in_bounds(R0 + r < p.rows)) p.y[yoff + R0 + r] = __int_as_float(0x7fc00000);
         }
         return;
     }
@@ -396,6 +435,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const KParams p) {
         // in slice order, once the previous kernel is done with y.
         if (p.early_inputs) pdl_dependency_wait();
         for (int r = tid; r < nrows; r += blockDim.x) {
+            if (!in_bounds(R0 + r < p.rows && static_cast<uint32_t>((r + 1) * p.W) * 4u <= p.off_ring - p.off_red))
+                continue;
             float v = 0.0f;
             for (int q = 0; q < p.W; q++) v += red[r * p.W + q];
             p.y[yoff + R0 + r] = v;

@@ -299,6 +299,12 @@ inline int make_plan_core(const DevInfo& di, int rows, int k, int slots, const q
     kp->S = S;
     kp->W = W;
     kp->slot_stride = static_cast<uint32_t>(stride);
+#ifdef QMV_BOUNDS_CHECK_PLANT
+    // A planted fault for the checking build's own test: ring slots half as
+    // long as the plan needs. The checks skip every copy that no longer fits;
+    // all other accesses stay inside the (now shorter) ring.
+    kp->slot_stride = static_cast<uint32_t>(stride / 2) & ~15u;
+#endif
     kp->aligned8 = (rowbytes % 8 == 0) ? 1 : 0;
     kp->CL = P.CL;
     kp->early_inputs = early;

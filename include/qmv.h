@@ -278,6 +278,10 @@ const char *qmv_last_cuda_error(void);
 #define QMV_STATUS_BAD_EXPERT_ID 1u /* an MoE id was outside [0, n_experts) */
 #define QMV_STATUS_WAIT_TIMEOUT 2u  /* a staged weight copy did not land in time (the
                                      * CTA's outputs are then NaN) */
+#define QMV_STATUS_OUT_OF_BOUNDS 4u /* only in the checking build of the library (compiled
+                                     * with QMV_BOUNDS_CHECK, a file of its own): the matvec
+                                     * kernel met an access outside the region its plan
+                                     * gives it, and skipped it (outputs then undefined) */
 
 /* Failure-path self-test: launches one thread that waits, through the same
  * bounded wait every staged copy goes through, on a barrier nothing arrives

@@ -40,6 +40,18 @@ def test_library_exports_every_declared_symbol(lib):
     assert os.path.abspath(lib.library_path()).startswith(ROOT)
 
 
+def test_checking_build_exports_every_declared_symbol(lib):
+    """The bounds-checking flavour is the same boundary: every declared
+    function, in a library file of its own inside the tree."""
+    from ggml_format_dequant_gb300 import _build
+    path = _build.lib_path("check")
+    assert os.path.exists(path) and os.path.abspath(path).startswith(ROOT)
+    assert path != lib.library_path()
+    L = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
 def test_strerror(lib):
     for code in [0, -1, -2, -3, -4, 12345]:
         assert isinstance(lib.strerror(code), str) and lib.strerror(code)
