@@ -644,12 +644,20 @@ struct Q40T {
 __device__ __forceinline__ void tc_issue_warp(const TParams& p, uint8_t* dst_ptr, uint32_t dst, uint32_t bar, int r0,
                                               int nr, uint32_t woff, uint32_t rowbytes, int lane) {
     const uintptr_t lim = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(p.wbytes);
+    // The checking build: row i of the piece is a row of the matrix and of the
+    // slot, its 16-byte cover fits the row stride, and it reads only weights.
+    // (Both passes below take the same rows.)
+    auto row_ok = [&](int i, uintptr_t a0, uintptr_t a1, uintptr_t ge) {
+        return in_bounds(static_cast<uint32_t>(i + 1) * p.stride <= p.slot_stride && r0 + i < p.rows &&
+                         a1 - a0 <= p.stride && a0 >= (reinterpret_cast<uintptr_t>(p.w) & ~uintptr_t(15)) && ge <= lim);
+    };
     uint32_t total = 0;
     for (int i = lane; i < nr; i += 32) {
         const uintptr_t gs = reinterpret_cast<uintptr_t>(p.w) + static_cast<uintptr_t>(r0 + i) * p.wpitch + woff;
         const uintptr_t ge = gs + rowbytes;
         const uintptr_t a0 = gs & ~uintptr_t(15);
         uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
+        if (!row_ok(i, a0, a1, ge)) continue;
         if (a1 > lim) {
             a1 = ge & ~uintptr_t(15);
             uint8_t* row = dst_ptr + static_cast<uint32_t>(i) * p.stride;
@@ -666,6 +674,7 @@ __device__ __forceinline__ void tc_issue_warp(const TParams& p, uint8_t* dst_ptr
         const uintptr_t ge = gs + rowbytes;
         const uintptr_t a0 = gs & ~uintptr_t(15);
         uintptr_t a1 = (ge + 15) & ~uintptr_t(15);
+        if (!row_ok(i, a0, a1, ge)) continue;
         if (a1 > lim) a1 = ge & ~uintptr_t(15);
         if (a1 > a0)
             tma_bulk_g2s(dst + static_cast<uint32_t>(i) * p.stride, reinterpret_cast<const void*>(a0),
@@ -777,8 +786,11 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
                 // rows past the piece read the slot's spare rows (results dropped)
                 const uint32_t pa = (pbase + static_cast<uint32_t>(ia) * p.wpitch) & 15u;
                 const uint32_t pb = (pbase + static_cast<uint32_t>(ib) * p.wpitch) & 15u;
-                const uint32_t ra = slot + static_cast<uint32_t>(ia) * p.stride + pa;
-                const uint32_t rb = slot + static_cast<uint32_t>(ib) * p.stride + pb;
+                uint32_t ra = slot + static_cast<uint32_t>(ia) * p.stride + pa;
+                uint32_t rb = slot + static_cast<uint32_t>(ib) * p.stride + pb;
+                // the checking build: both rows lie in the slot
+                if (!in_bounds(static_cast<uint32_t>(ia + 1) * p.stride <= p.slot_stride)) ra = slot;
+                if (!in_bounds(static_cast<uint32_t>(ib + 1) * p.stride <= p.slot_stride)) rb = slot;
                 float y4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 F::template slice<P>(ra, rb, ks, ng, t, xf, sums_l, y4);
                 // park this slice's sums of columns 2t, 2t + 1, unscaled
@@ -786,7 +798,8 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
                 float2 vb = make_float2(y4[2] * inv0, y4[3] * inv1);
                 float2* qa = reinterpret_cast<float2*>(red + ((rl0 + ia) * p.KS + ks) * TC_COLS + 2 * t);
                 float2* qb = reinterpret_cast<float2*>(red + ((rl0 + ib) * p.KS + ks) * TC_COLS + 2 * t);
-                if (ia < nr) {
+                const uint32_t red_cap = p.off_sums / 4u;   // parked sums: floats before B' sums
+                if (ia < nr && in_bounds(static_cast<uint32_t>(((rl0 + ia) * p.KS + ks) * TC_COLS + 2 * t + 2) <= red_cap)) {
                     if (c > 0) {
                         const float2 o = *qa;
                         va.x += o.x;
@@ -794,7 +807,7 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
                     }
                     *qa = va;
                 }
-                if (ib < nr) {
+                if (ib < nr && in_bounds(static_cast<uint32_t>(((rl0 + ib) * p.KS + ks) * TC_COLS + 2 * t + 2) <= red_cap)) {
                     if (c > 0) {
                         const float2 o = *qb;
                         vb.x += o.x;
@@ -838,13 +851,17 @@ __global__ void __launch_bounds__(512, 1) qmm_tc_kernel(const TParams p) {
         pdl_dependency_wait();
         for (int e = tid; e < nrows * p.m; e += blockDim.x) {
             const int r = e / p.m, i = e - (e / p.m) * p.m;
-            p.y[static_cast<long long>(i) * p.rows + R0 + r] = __int_as_float(0x7fc00000);
+            if (in_bounds(R0 + r < p.rows && i < TC_COLS))
+                p.y[static_cast<long long>(i) * p.rows + R0 + r] = __int_as_float(0x7fc00000);
         }
         return;
     }
     if (p.early_inputs) pdl_dependency_wait();
     for (int e = tid; e < nrows * p.m; e += blockDim.x) {
         const int r = e / p.m, i = e - (e / p.m) * p.m;
+        if (!in_bounds(R0 + r < p.rows && i < TC_COLS &&
+                       static_cast<uint32_t>((r * p.KS + p.KS - 1) * TC_COLS + (P ? i + 4 : i) + 1) <= p.off_sums / 4u))
+            continue;
         float v = 0.0f;
         for (int q = 0; q < p.KS; q++) {
             v += red[(r * p.KS + q) * TC_COLS + i];

@@ -1,9 +1,10 @@
 """Run by tests/test_gpu_bounds_check.py in a process of its own: loads the
 checking build of the library (every shared- and global-memory access of the
-matvec kernel tested against its region, QMV_STATUS_OUT_OF_BOUNDS raised
-instead of an access outside it) and drives it over a seeded sweep of shapes,
-launch modes and forced plans of every matvec family, the dp4a, block-dot and
-fused-quantization entry points, and MoE banks (one bad id among the slots).
+matvec and batch kernels tested against its region, QMV_STATUS_OUT_OF_BOUNDS
+raised instead of an access outside it) and drives it over a seeded sweep of
+shapes, launch modes and forced plans of every matvec family, the dp4a,
+block-dot and fused-quantization entry points, MoE banks (one bad id among the
+slots) and the small-M batched products.
 Every result is checked against the oracle as well. Prints one JSON line:
 calls made, calls refused on the host, the status word, and the failures."""
 
@@ -187,6 +188,29 @@ def main():
                         return f"slot {s}: parity"
                 return None
             record(rc, f"moe {fn.__name__} {rows}x{k} e{ne} s{slots} mode {mode} {cfg}", moe_check)
+
+    # small-M batched products (the tensor-core batch kernel): m = 2..12 rows
+    # of x (one or two launches), forced plans, every launch mode
+    for fi, fmt in enumerate(QK):
+        for d in draws(7400 + fi, 5, 10):
+            qk = QK[fmt]
+            k = qk * (1 + d[0] % (8192 // qk))
+            rows = 1 + d[1] % 600
+            m = 2 + d[2] % 11
+            mode = d[3] % 3
+            cfg = None if d[4] % 2 == 0 else dict(ctas=1 + d[5] % 9, chunk_rows=d[6] % 20, chunks=d[7] % 4,
+                                                   warps=[0, 1, 3, 8][d[8] % 4])
+            st = synth.Stream(rows * 19 + k + m)
+            w = synth.GEN_ROWS[fmt](st, rows, k)
+            x = synth.gen_normal(st, m * k).reshape(m, k)
+            y = torch.full((m, rows), float("nan"), device="cuda")
+            rc = getattr(q, f"qmm_{fmt}")(dev(w), dev(x), y, rows, k, m, cfg=cfg, overlap=mode, check=False)
+
+            def qmm_check():
+                r = oracle.qmm(fmt, w, x, m, rows, k)
+                g = y.cpu().numpy()
+                return None if all(scale_rel(r[i], g[i]) <= TOL for i in range(m)) else "parity"
+            record(rc, f"qmm_{fmt} {rows}x{k} m {m} mode {mode} {cfg}", qmm_check)
 
     # the path of a staged copy that did not land: NaN outputs
     for rows, k in ((300, 2048), (4096, 4096)):

@@ -32,7 +32,7 @@ def test_checking_build_sweep():
     assert r.returncode == 0, r.stderr[-3000:]
     rec = json.loads(r.stdout.strip().splitlines()[-1])
     assert rec["n_failures"] == 0, rec["failures"]
-    assert rec["calls"] >= 110, rec
+    assert rec["calls"] >= 130, rec
     assert not rec["status"] & q.QMV_STATUS_OUT_OF_BOUNDS, rec
 
 
