@@ -951,6 +951,12 @@ inline int make_tc_plan_core(const DevInfo& di, int rows, int k, int m, const qm
             tp->early_inputs = mode >= QMV_OVERLAP_INDEPENDENT ? 1 : 0;
             pl->overlap = mode;
             tp->slot_stride = static_cast<uint32_t>(slot);
+#ifdef QMV_BOUNDS_CHECK_PLANT
+            // A planted fault for the checking build's own test: slots holding
+            // half the rows the plan needs (the checks skip the rows past it
+            // and read the slot's first row in their place).
+            tp->slot_stride = static_cast<uint32_t>(slot / 2) & ~15u;
+#endif
             return QMV_OK;
         }
         if (cfg && cfg->ctas > 0) return QMV_ETOOBIG;

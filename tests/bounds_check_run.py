@@ -53,9 +53,9 @@ def forced(d):
 
 
 def planted():
-    """The build with ring slots half as long as planned: a few Q4_K calls
-    whose pieces hold several rows; the checks must raise the bit (results are
-    undefined, so they are not compared)."""
+    """The build with ring slots half as long as planned: a few Q4_K matvec
+    and batch calls whose pieces hold several rows; the checks of each kernel
+    must raise the bit (results are undefined, so they are not compared)."""
     q.load(_build.lib_path("check_planted"))
     q.qmv_device_status(clear=True)
     calls = 0
@@ -68,7 +68,18 @@ def planted():
             if q.qmv_q4k(dev(w), dev(x), y, rows, k, cfg=cfg, check=False) == q.QMV_OK:
                 calls += 1
     torch.cuda.synchronize()
-    print(json.dumps({"calls": calls, "status": q.qmv_device_status(clear=True)}))
+    matvec_status = q.qmv_device_status(clear=True)
+    # the batch kernel with the same planted fault
+    for rows, k, m in ((300, 2048, 2), (700, 4096, 8)):
+        st = synth.Stream(rows + k + m)
+        w = synth.GEN_ROWS["q4k"](st, rows, k)
+        x = synth.gen_normal(st, m * k).reshape(m, k)
+        y = torch.zeros((m, rows), device="cuda")
+        if q.qmm_q4k(dev(w), dev(x), y, rows, k, m, check=False) == q.QMV_OK:
+            calls += 1
+    torch.cuda.synchronize()
+    batch_status = q.qmv_device_status(clear=True)
+    print(json.dumps({"calls": calls, "status": matvec_status, "batch_status": batch_status}))
 
 
 def main():

@@ -37,9 +37,10 @@ def test_checking_build_sweep():
 
 
 def test_checking_build_catches_a_planted_fault():
-    """The same checks in a build whose planner makes every ring slot half as
+    """The same checks in a build whose planners make every ring slot half as
     long as its pieces need: the copies that would overrun their slot are
-    skipped and QMV_STATUS_OUT_OF_BOUNDS is raised."""
+    skipped and QMV_STATUS_OUT_OF_BOUNDS is raised, by the matvec kernel and
+    by the batch kernel."""
     torch = pytest.importorskip("torch")
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     from ggml_format_dequant_gb300 import _build
@@ -49,5 +50,6 @@ def test_checking_build_catches_a_planted_fault():
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
     rec = json.loads(r.stdout.strip().splitlines()[-1])
-    assert rec["calls"] >= 2, rec
-    assert rec["status"] & q.QMV_STATUS_OUT_OF_BOUNDS, rec
+    assert rec["calls"] >= 4, rec
+    assert rec["status"] & q.QMV_STATUS_OUT_OF_BOUNDS, rec         # the matvec kernel's checks
+    assert rec["batch_status"] & q.QMV_STATUS_OUT_OF_BOUNDS, rec   # the batch kernel's checks
