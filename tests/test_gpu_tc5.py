@@ -314,3 +314,47 @@ def test_streaming_and_cluster_plans_interleaved_in_one_stream(q):
         for j in range(m):
             assert scale_rel(ref[j], got[j]) <= SCALE_REL_TOL, (i, j)
     assert q.qmv_device_status() == 0
+
+
+def test_both_plans_on_two_streams_at_once(q):
+    """Chained cluster-plan calls on one stream and independent streaming-plan
+    calls on another, enqueued alternately so that their CTAs share the GPU:
+    at most two cluster-plan CTAs (256 tensor-memory columns each) fit an SM,
+    and a streaming CTA (512 columns) shares its SM with neither, so no
+    allocation waits on another stream. Every call matches the oracle."""
+    rows, k, m = 2048, 2048, 4
+    st = synth.Stream(5151)
+    ws = [synth.gen_q4k_rows(st, rows, k) for _ in range(2)]
+    x0 = (synth.gen_normal(st, m * k) / np.float32(16)).astype(np.float32).reshape(m, k)
+    xs = synth.gen_normal(st, m * k).reshape(m, k)
+    wd = [dev(w) for w in ws]
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    chain_out, ind_out = [], []
+    cur = dev(x0)
+    xsd = dev(xs)
+    # the inputs were copied on the current stream
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    for i in range(8):
+        with torch.cuda.stream(sa):
+            y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
+            q.qmm_q4k_tc5(wd[0], cur, y, rows, k, m, stream=sa, overlap=q.OVERLAP_CHAIN)
+            chain_out.append(y)
+            cur = y
+        with torch.cuda.stream(sb):
+            y2 = torch.empty((m, rows), dtype=torch.float32, device="cuda")
+            q.qmm_q4k_tc5(wd[1], xsd, y2, rows, k, m, stream=sb, overlap=q.OVERLAP_INDEPENDENT)
+            ind_out.append(y2)
+    torch.cuda.synchronize()
+    inputs = [x0] + [o.cpu().numpy() for o in chain_out[:-1]]
+    for xin, o in zip(inputs, chain_out):
+        ref = oracle.qmm("q4k", ws[0], xin, m, rows, k)
+        got = o.cpu().numpy()
+        for j in range(m):
+            assert scale_rel(ref[j], got[j]) <= SCALE_REL_TOL
+    ref = oracle.qmm("q4k", ws[1], xs, m, rows, k)
+    for o in ind_out:
+        got = o.cpu().numpy()
+        for j in range(m):
+            assert scale_rel(ref[j], got[j]) <= SCALE_REL_TOL
+    assert q.qmv_device_status() == 0
