@@ -358,3 +358,18 @@ def test_both_plans_on_two_streams_at_once(q):
         for j in range(m):
             assert scale_rel(ref[j], got[j]) <= SCALE_REL_TOL
     assert q.qmv_device_status() == 0
+
+
+@pytest.mark.parametrize("overlap", [0, 2])
+def test_many_tiles(q, overlap):
+    """20000 rows: 157 tiles (more CTAs than SMs in either plan, a ragged last
+    tile), k = 4096, m = 8; the cluster plan (plain launch) and the streaming
+    plan (independent call)."""
+    rows, k, m = 20000, 4096, 8
+    w, x = case(rows, k, m, 2026)
+    y = run(q, w, x, rows, k, m, overlap=overlap)
+    ref = oracle.qmm("q4k", w, x, m, rows, k)
+    assert not np.any(np.isnan(y))
+    for i in range(m):
+        assert scale_rel(ref[i], y[i]) <= SCALE_REL_TOL, i
+    assert q.qmv_device_status() == 0
